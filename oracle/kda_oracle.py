@@ -1,0 +1,173 @@
+"""Plain fp64 CPU oracle for the Kimi / Kernel Delta Attention (KDA) forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module: only
+``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may call it.  It shares no code with the CUDA library.
+
+What it computes, and from which passage
+----------------------------------------
+* Recurrence -- ejkernel ``kernel_delta_attention`` module page, "The core recurrence":
+  a per-(batch, head) memory ``h`` of shape ``[dk, dv]``; every token decays it with
+  ``exp(decay_t)``, adds ``k_t (x) (beta_t * (v_t - h @ k_t))`` and emits ``o_t = h_t @ q_t``.
+  ``h @ x`` contracts over the key axis (``h`` is ``[dk, dv]``), so it is ``h^T x`` here.
+* Gate, beta, scale -- NKI "KDA TKG Kernel API Reference", ``kda_tkg`` parameters:
+  the raw per-channel gate ``g`` becomes ``lower_bound * sigmoid(exp(a_log) * (g + dt_bias))``;
+  ``beta`` arrives as logits and goes through a sigmoid; q and k are L2-normalised and
+  ``scale`` is folded into the normalised query.
+* State passthrough -- ``kernel_delta_attention`` page, ``initial_state`` / ``return_state``
+  parameters; ``kda_tkg``'s ``S`` is read and overwritten in place.
+* Varlen packing -- ejkernel ``recurrent`` module page, ``cu_seqlens`` parameter.
+
+Readings where the pages are silent or ambiguous (each is also listed in the design doc)
+-----------------------------------------------------------------------------------
+1. Decay before delta (``order="decay_first"``, the default): the error term is taken
+   against the decayed memory, ``S' = diag(exp(gamma)) S``, ``u = beta (v - S'^T k)``,
+   ``S <- S' + k u^T``.  The recurrence as printed uses the undecayed memory inside the
+   error term; that literal reading is kept as ``order="literal"``.  Both agree when the
+   gate is identically zero.
+2. The output is read after the update (``o_t = h_t @ q_t``).
+3. L2 normalisation is ``x / sqrt(sum(x^2) + 1e-6)`` over the head dimension (epsilon
+   unstated on the pages).
+4. ``scale`` multiplies the normalised query; default ``dk ** -0.5``.
+5. The gate is per channel (``[..., dk]``) and raw, as in ``kda_tkg``; beta is a logit.
+6. Outputs are returned in fp64; dtype handling (bf16 inputs) is the caller's business:
+   callers pass the already-rounded values.
+
+The algorithm is the plain token-by-token scan: no chunking, no blocking and no
+re-association, vectorised only over independent (batch, head) pairs.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+L2_EPS = 1e-6
+
+
+def sigmoid(x):
+    """Logistic function 1 / (1 + exp(-x)) in fp64 (``kda_tkg`` beta and gate)."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-x))
+
+
+def activate_gate(g, a_log, dt_bias, lower_bound):
+    """Per-channel log-decay ``gamma = lower_bound * sigmoid(exp(a_log) * (g + dt_bias))``.
+
+    ``kda_tkg`` parameters g / a_log / dt_bias / lower_bound.  ``g`` has the head axis
+    second-to-last and the channel axis last (``[..., H, dk]``); ``a_log`` is ``[H]``;
+    ``dt_bias`` is ``[dk, H]`` exactly as the page lays it out.  Returns fp64 ``[..., H, dk]``.
+    """
+    g = np.asarray(g, dtype=np.float64)
+    a = np.exp(np.asarray(a_log, dtype=np.float64))[:, None]  # [H, 1]
+    bias = np.asarray(dt_bias, dtype=np.float64).T  # [H, dk]
+    return float(lower_bound) * sigmoid(a * (g + bias))
+
+
+def l2_normalize(x, eps=L2_EPS):
+    """``x / sqrt(sum(x^2) + eps)`` over the last axis (reading 3)."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def kda_token(S, q_hat, k_hat, v, gamma, beta, order="decay_first"):
+    """Advance the memory by one token; returns ``(o, S_new)``.
+
+    Shapes (any leading batch dims ``...``): ``S [..., dk, dv]``, ``q_hat, k_hat, gamma
+    [..., dk]``, ``v [..., dv]``, ``beta [...]``.  ``q_hat`` already carries ``scale``.
+    ``kernel_delta_attention`` page, "The core recurrence" (with reading 1 for the order).
+    """
+    decay = np.exp(gamma)[..., :, None]  # diag(exp(gamma)) acting on the rows of S
+    b = np.asarray(beta)[..., None]
+    if order == "decay_first":
+        S_dec = decay * S
+        pred = np.einsum("...ij,...i->...j", S_dec, k_hat)  # S'^T k
+        u = b * (v - pred)
+        S_new = S_dec + k_hat[..., :, None] * u[..., None, :]
+    elif order == "literal":
+        pred = np.einsum("...ij,...i->...j", S, k_hat)  # h_{t-1} @ k_t, undecayed
+        u = b * (v - pred)
+        S_new = decay * S + k_hat[..., :, None] * u[..., None, :]
+    else:
+        raise ValueError(f"unknown order {order!r}")
+    o = np.einsum("...ij,...i->...j", S_new, q_hat)  # o_t = h_t @ q_t, after the update
+    return o, S_new
+
+
+def kda_forward(q, k, v, g, beta_logits, a_log, dt_bias, scale=None, lower_bound=-5.0,
+                initial_state=None, order="decay_first"):
+    """Whole-sequence KDA forward, the plain token scan.
+
+    Layouts follow ``kernel_delta_attention.run``: ``q, k, g [B, T, H, dk]``,
+    ``v [B, T, H, dv]``, ``beta_logits [B, T, H]``, ``initial_state [B, H, dk, dv]``
+    (``None`` means zeros); gate parameters as in ``kda_tkg`` (``a_log [H]``,
+    ``dt_bias [dk, H]``).  Returns ``(out [B, T, H, dv], final_state [B, H, dk, dv])``
+    in fp64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = dk ** -0.5
+    gamma = activate_gate(g, a_log, dt_bias, lower_bound)  # [B, T, H, dk]
+    beta = sigmoid(beta_logits)  # [B, T, H]
+    q_hat = float(scale) * l2_normalize(q)
+    k_hat = l2_normalize(k)
+    if initial_state is None:
+        S = np.zeros((B, H, dk, dv), dtype=np.float64)
+    else:
+        S = np.array(initial_state, dtype=np.float64, copy=True)
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    for t in range(T):
+        o, S = kda_token(S, q_hat[:, t], k_hat[:, t], v[:, t], gamma[:, t], beta[:, t], order)
+        out[:, t] = o
+    return out, S
+
+
+def kda_forward_varlen(q, k, v, g, beta_logits, a_log, dt_bias, cu_seqlens, scale=None,
+                       lower_bound=-5.0, initial_state=None, order="decay_first"):
+    """Packed variable-length forward (``cu_seqlens`` convention of the ejkernel
+    ``recurrent`` page): sequence ``n`` owns tokens ``cu_seqlens[n]:cu_seqlens[n+1]`` of
+    the packed ``[total_T, H, .]`` tensors and starts from ``initial_state[n]``.
+
+    Returns ``(out [total_T, H, dv], final_state [N, H, dk, dv])``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    total_T, H, dk = q.shape
+    dv = np.shape(v)[-1]
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    N = len(cu) - 1
+    out = np.zeros((total_T, H, dv), dtype=np.float64)
+    final = np.zeros((N, H, dk, dv), dtype=np.float64)
+    for n in range(N):
+        a, b = int(cu[n]), int(cu[n + 1])
+        s0 = None if initial_state is None else np.asarray(initial_state)[n:n + 1]
+        o, s = kda_forward(np.asarray(q)[None, a:b], np.asarray(k)[None, a:b],
+                           np.asarray(v)[None, a:b], np.asarray(g)[None, a:b],
+                           np.asarray(beta_logits)[None, a:b], a_log, dt_bias, scale,
+                           lower_bound, s0, order)
+        out[a:b] = o[0]
+        final[n] = s[0]
+    return out, final
+
+
+def kda_decode_step(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, S,
+                    order="decay_first"):
+    """One token for B requests in the ``kda_tkg`` layouts.
+
+    ``q, k, g [B, dk, H]`` (head innermost), ``v [B, H, dv]``, ``beta_logits [B, 1, H]``,
+    ``a_log [1, H]`` or ``[H]``, ``dt_bias [dk, H]``, ``S [B, H, dk, dv]``.
+    Returns ``(out [B, H, dv], S_new [B, H, dk, dv])``; the input ``S`` is not modified
+    (the kernel's in-place contract is the caller's to emulate).
+    """
+    q = np.swapaxes(np.asarray(q, dtype=np.float64), 1, 2)  # -> [B, H, dk]
+    k = np.swapaxes(np.asarray(k, dtype=np.float64), 1, 2)
+    g = np.swapaxes(np.asarray(g, dtype=np.float64), 1, 2)
+    v = np.asarray(v, dtype=np.float64)
+    gamma = activate_gate(g, np.reshape(a_log, -1), dt_bias, lower_bound)
+    beta = sigmoid(np.asarray(beta_logits, dtype=np.float64)[:, 0, :])  # [B, H]
+    q_hat = float(scale) * l2_normalize(q)
+    k_hat = l2_normalize(k)
+    S = np.asarray(S, dtype=np.float64)
+    return kda_token(S, q_hat, k_hat, v, gamma, beta, order)
