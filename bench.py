@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA forward library on GB300.
+
+One step = one ``kda_chunk_fwd`` over the chunked-prefill workload (B=4, T=4096, H=32,
+dk=dv=128, bf16 q/k/v, fp32 gates/state, chunk 64), inputs resident in HBM (0.82 GB,
+larger than L2, so no flush is needed between steps).  The printed JSON line reports
+tokens/s (B*T per step, whole job over all ranks), the chunk kernel's HBM roofline
+fraction, an end-to-end figure through the same C-ABI call with host buffers, the fp64
+oracle timed on the host as a CPU baseline, SM clocks sampled during the timed region,
+and secondary measurements of the decode step (B=64 and B=512 x 32 tokens) and the packed
+varlen prefill.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the workload
+(independent problems, no collective on the data path: weak scaling); the only
+collectives are the barrier and the max-over-ranks reduction of the timings.
+
+``--impl reference`` times the fp64 CPU oracle instead (rank 0 only), on a bounded sample
+of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA chunked-fwd tokens/s; decode-step HBM GB/s vs peak (1 GB300)"
+L2_BYTES = 126 * 2 ** 20
+CHUNK_KERNEL_SOURCES = ["kda_chunk_simt.cu"]  # sources of the kernel the roofline covers
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the decode / varlen / e2e / cpu-baseline measurements")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def prefill_bytes(B, T, H, dk, dv, in_bytes=2, init_state=False, final_state=True):
+    """Algorithmic HBM bytes of one chunked-forward launch: every input read once, every
+    output written once (per token-head: q, k, v, out in the I/O dtype, g and beta fp32)."""
+    per_tok_head = (2 * dk + dv) * in_bytes + dk * 4 + 4 + dv * in_bytes
+    params = H * 4 + dk * H * 4
+    state = B * H * dk * dv * 4
+    return B * T * H * per_tok_head + params + state * (int(init_state) + int(final_state))
+
+
+def decode_bytes(B, H, dk, dv):
+    """Algorithmic HBM bytes of one decode step: the state read and written once, q/k/g,
+    v/out and beta once, the gate parameters once."""
+    return (2 * B * H * dk * dv * 4 + 3 * B * dk * H * 4 + 2 * B * H * dv * 4 + B * H * 4
+            + H * 4 + dk * H * 4)
+
+
+def source_hash(names):
+    h = hashlib.sha1()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_delta_rule_55_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def traffic_for(kernel_key, names):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the
+    kernel's source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(kernel_key)
+    if not d or d.get("source_sha1") != source_hash(names):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if _torch().cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        torch = _torch()
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+_T = None
+
+
+def _torch():
+    global _T
+    if _T is None:
+        import torch
+        _T = torch
+    return _T
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons around a timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        self.proc = None
+        self.file = None
+        self.t0 = self.t1 = None
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        self.dev = ids[local_rank] if len(ids) > local_rank else str(local_rank)
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.dev, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.4)  # let it start emitting
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if not self.proc:
+            return {"unavailable": "nvidia-smi could not be started"}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.split(", ") for r in f.read().strip().splitlines() if r.count(",") >= 9]
+        os.unlink(self.file.name)
+        samples = []
+        for r in rows:
+            try:
+                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + r[0].split(".")[1]) if "." in r[0] else 0.0
+                samples.append((ts, float(r[2]), float(r[3]), r[5:]))
+            except Exception:
+                continue
+        inside = [s for s in samples if self.t0 - 0.05 <= s[0] <= self.t1 + 0.05]
+        if not inside and samples:
+            after = [s for s in samples if s[0] >= self.t0]
+            inside = after[:1] or samples[-1:]
+        if not inside:
+            return {"unavailable": "no nvidia-smi samples"}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for s in inside:
+            for n, v in zip(names[1:], s[3][1:]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": sorted(reasons),
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------------------- native arm
+
+def device_prefill(w):
+    torch = _torch()
+    from gated_delta_rule_55_gb300 import synth
+    d = synth.workload_inputs(w)
+    io = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dev = {n: torch.from_numpy(d[n]).to("cuda", io) for n in ("q", "k", "v")}
+    for n in ("g", "beta_logits", "a_log", "dt_bias"):
+        dev[n] = torch.from_numpy(d[n]).cuda()
+    dev["initial_state"] = (None if d["initial_state"] is None
+                            else torch.from_numpy(d["initial_state"]).cuda())
+    shape_out = (w.B, w.T, w.H, w.dv) if w.kind == "chunk" else (d["q"].shape[0], w.H, w.dv)
+    dev["out"] = torch.empty(shape_out, device="cuda", dtype=io)
+    nseq = w.B if w.kind == "chunk" else w.n_seqs
+    dev["final_state"] = torch.empty((nseq, w.H, w.dk, w.dv), device="cuda")
+    if w.kind == "varlen":
+        dev["cu_seqlens"] = torch.from_numpy(d["cu_seqlens"]).cuda()
+        dev["total_T"] = int(d["cu_seqlens"][-1])
+    return d, dev
+
+
+def call_chunk(w, x):
+    import gated_delta_rule_55_gb300 as kda
+    if w.kind == "chunk":
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"],
+                          x["dt_bias"], w.q_scale, w.lower_bound, x["initial_state"], x["out"],
+                          x["final_state"], w.B, w.T, w.H, w.dk, w.dv, w.chunk)
+    else:
+        kda.kda_chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"],
+                                 x["dt_bias"], w.q_scale, w.lower_bound, x["cu_seqlens"],
+                                 w.n_seqs, x["total_T"], x["initial_state"], x["out"],
+                                 x["final_state"], w.H, w.dk, w.dv, w.chunk)
+
+
+def timed(fn, K, W, dist=None, clocks=None):
+    """W untimed calls, then exactly K calls bracketed by barrier + synchronize, timed with
+    CUDA events on the current stream; returns the max over ranks in ms."""
+    torch = _torch()
+    for _ in range(W):
+        fn()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.mark("t0")
+    e0.record()
+    for _ in range(K):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("t1")
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    return dist.max(ms) if dist else ms
+
+
+def decode_measure(w, reps, flush_l2):
+    """Median per-step time of kda_decode_step with the L2 flushed before every step."""
+    torch = _torch()
+    import gated_delta_rule_55_gb300 as kda
+    from gated_delta_rule_55_gb300 import synth
+    a_log, dt_bias = (torch.from_numpy(x).cuda() for x in synth.gate_params(w.H, w.dk, w.seed))
+    S = torch.from_numpy(synth.decode_state(w.B, w.H, w.dk, w.dv, w.seed, w.state_std)).cuda()
+    toks = []
+    for step in range(w.steps):
+        t = synth.decode_token_inputs(w.B, w.H, w.dk, w.dv, w.seed, step)
+        toks.append({n: torch.from_numpy(v).cuda() for n, v in t.items()})
+    out = torch.empty((w.B, w.H, w.dv), device="cuda")
+    flush = torch.empty(2 * L2_BYTES // 4, device="cuda") if flush_l2 else None
+
+    def step(t):
+        kda.kda_decode_step(t["q"], t["k"], t["v"], t["g"], t["beta_logits"], a_log, dt_bias,
+                            w.q_scale, w.lower_bound, out, S, w.B, w.H, w.dk, w.dv)
+
+    for i in range(3):
+        step(toks[i % len(toks)])
+    times = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if w.steps == 1:
+        for i in range(reps):
+            if flush is not None:
+                flush.fill_(float(i))
+            e0.record()
+            step(toks[0])
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        total_steps = 1
+    else:  # chained tokens, state passed through, one call per token (autoregressive)
+        for _ in range(max(1, reps // 8)):
+            torch.cuda.synchronize()
+            e0.record()
+            for t in toks:
+                step(t)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times) / w.steps
+        total_steps = w.steps
+    nbytes = decode_bytes(w.B, w.H, w.dk, w.dv)
+    return {"workload": w.name, "ms_per_step": ms, "steps_chained": total_steps,
+            "hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "bytes_per_step": nbytes,
+            "l2": "flushed before every step" if w.steps == 1 else
+                  "state (1.07 GB) larger than L2"}
+
+
+def e2e_measure(w, d, x, K, W):
+    """Same call through the public API with inputs in pinned HOST memory: per step the
+    inputs are copied host->device, the library runs, and out + final state are copied
+    device->host, all inside the timed region."""
+    torch = _torch()
+    io = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {n: torch.from_numpy(d[n]).to(io).pin_memory() for n in ("q", "k", "v")}
+    for n in ("g", "beta_logits", "a_log", "dt_bias"):
+        host[n] = torch.from_numpy(d[n]).pin_memory()
+    h_out = torch.empty(x["out"].shape, dtype=io).pin_memory()
+    h_fs = torch.empty(x["final_state"].shape).pin_memory()
+    dev = dict(x)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_out.numel() * h_out.element_size() + h_fs.numel() * h_fs.element_size()
+
+    def step():
+        for n, t in host.items():
+            dev[n].copy_(t, non_blocking=True)
+        call_chunk(w, dev)
+        h_out.copy_(dev["out"], non_blocking=True)
+        h_fs.copy_(dev["final_state"], non_blocking=True)
+
+    ms = timed(step, K, W)
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w, d, budget_s=12.0):
+    """The fp64 oracle on a bounded sample of the workload: all (b, h) pairs, the first
+    T_s tokens, T_s grown until the run takes a few seconds."""
+    from oracle import kda_forward
+    Ts = 16
+    while True:
+        t0 = time.perf_counter()
+        kda_forward(d["q"][:, :Ts], d["k"][:, :Ts], d["v"][:, :Ts], d["g"][:, :Ts],
+                    d["beta_logits"][:, :Ts], d["a_log"], d["dt_bias"], w.q_scale,
+                    w.lower_bound, d["initial_state"])
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 3 or Ts >= w.T:
+            break
+        Ts = min(w.T, Ts * 2)
+    return {"value": w.B * Ts / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"B={w.B}, all {w.H} heads, first {Ts} of {w.T} tokens "
+                      f"({dt:.1f} s, numpy fp64, single thread; host has {os.cpu_count()} cores)"}
+
+
+def native(args):
+    torch = _torch()
+    dist = Dist()
+    torch.cuda.set_device(dist.local_rank)
+    from gated_delta_rule_55_gb300 import build_lib, synth
+    if dist.local_rank == 0:
+        build_lib.build()
+    dist.barrier()
+    import gated_delta_rule_55_gb300 as kda
+    kda.lib()
+    w = synth.PREFILL_B4
+    d, x = device_prefill(w)
+    K, W = args.steps, max(3, args.warmup)
+    clocks = Clocks(dist.local_rank)
+    clocks.start()
+    ms = timed(lambda: call_chunk(w, x), K, W, dist, clocks)
+    clk = clocks.stop()
+    tokens = w.B * w.T * K * dist.world
+    value = tokens / (ms * 1e-3)
+    pk = peaks()
+    nbytes = prefill_bytes(w.B, w.T, w.H, w.dk, w.dv, 2, False, True)
+    per_launch_s = ms * 1e-3 / K
+    achieved = nbytes / per_launch_s / 1e9
+    flops = w.B * w.T * w.H * (2 * w.chunk * (3 * w.dk + 2 * w.dv) + 6 * w.dk * w.dv
+                               + w.chunk ** 2 / 3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy; q,k,v,g,beta_logits ~ N(0,1), a_log ~ U(-1,1), "
+                "dt_bias ~ N(0,0.1))",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "chunk": w.chunk, "lower_bound": w.lower_bound,
+                   "io": "bf16 q/k/v/out, fp32 g/beta/state",
+                   "l2": f"inputs {nbytes / 1e9:.2f} GB per step, larger than L2; no flush",
+                   "parallelism": f"replica per GPU x{dist.world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": traffic_for("chunk_fwd_prefill_B4", CHUNK_KERNEL_SOURCES),
+                     "kernel": "chunk kernel (one launch per step)",
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "peak_source": f"{pk['source']} (MEASURED_PEAKS hbm_gbs)",
+                     "tensor_frac": flops / per_launch_s / 1e12 / pk["bf16_tflops"],
+                     "algorithmic_flops_per_launch": flops},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    if not args.no_secondary and dist.rank == 0:
+        line["decode"] = [decode_measure(synth.DECODE_B64, 30, True),
+                          decode_measure(synth.DECODE_B512, 32, False)]
+        for dd in line["decode"]:
+            dd["frac_of_hbm_peak"] = dd["hbm_gbs"] / pk["hbm_gbs"]
+        wv = synth.VARLEN_8
+        dv_, xv = device_prefill(wv)
+        msv = timed(lambda: call_chunk(wv, xv), max(3, K // 5), 3)
+        tot = int(dv_["cu_seqlens"][-1])
+        vbytes = (tot * wv.H * ((2 * wv.dk + wv.dv) * 2 + wv.dk * 4 + 4 + wv.dv * 2)
+                  + 2 * wv.n_seqs * wv.H * wv.dk * wv.dv * 4)
+        per = msv * 1e-3 / max(3, K // 5)
+        line["varlen"] = {"workload": wv.name, "total_tokens": tot,
+                          "tokens_per_s": tot / per, "ms_per_call": per * 1e3,
+                          "hbm_gbs": vbytes / per / 1e9,
+                          "frac_of_hbm_peak": vbytes / per / 1e9 / pk["hbm_gbs"],
+                          "longest_seq": int(np.max(np.diff(dv_["cu_seqlens"])))}
+        del xv
+        ems, h2d, d2h = e2e_measure(w, d, x, max(3, K // 5), 3)
+        line["e2e"] = {"value": w.B * w.T * max(3, K // 5) / (ems * 1e-3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        line["cpu_baseline"] = cpu_baseline(w, d)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+# ---------------------------------------------------------------------- reference arm
+
+def reference(args):
+    """The fp64 CPU oracle as the reference arm (rank 0 only; other ranks exit)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from gated_delta_rule_55_gb300 import synth
+    from oracle import kda_forward
+    w = synth.PREFILL_B4
+    d = synth.workload_inputs(w)
+    Ts = 64  # tokens of every (b, h) pair per step: a few seconds of fp64 numpy
+    args_ = (d["a_log"], d["dt_bias"], w.q_scale, w.lower_bound, d["initial_state"])
+
+    def step(i):
+        t0 = (i * Ts) % (w.T - Ts)
+        sl = slice(t0, t0 + Ts)
+        kda_forward(d["q"][:, sl], d["k"][:, sl], d["v"][:, sl], d["g"][:, sl],
+                    d["beta_logits"][:, sl], *args_)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = w.B * Ts * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy)", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk,
+                       "dv": w.dv, "chunk": w.chunk},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: B={w.B}, all {w.H} heads, {Ts} consecutive "
+                                       f"tokens (numpy fp64 token scan, single thread)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse_args()
+    if a.impl == "reference":
+        reference(a)
+    else:
+        native(a)

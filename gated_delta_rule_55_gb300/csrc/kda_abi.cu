@@ -1,0 +1,148 @@
+// The C ABI of libkda (declared in include/kda.h): host-side argument validation,
+// kernel selection and launch on the caller's stream.  Nothing here allocates memory.
+#include <math.h>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+// The library is built for compute capability 10.3 only; check the current device once
+// per device ordinal.
+int check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return KDA_ERR_DEVICE;
+  }
+  static int verdict[64] = {0};  // 0 unknown, 1 ok, -1 bad
+  if (dev < 64 && verdict[dev] != 0) return verdict[dev] > 0 ? KDA_OK : KDA_ERR_DEVICE;
+  int major = 0, minor = 0;
+  const bool ok =
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+      major == 10 && minor == 3;
+  cudaGetLastError();
+  if (dev < 64) verdict[dev] = ok ? 1 : -1;
+  return ok ? KDA_OK : KDA_ERR_DEVICE;
+}
+
+int check_common(float* scale, float lower_bound, int dk, int dv) {
+  if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_HEAD_DIM;
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_LOWER_BOUND;
+  if (!isfinite(*scale)) return KDA_ERR_SCALE;
+  if (*scale <= 0.0f) *scale = 1.0f / sqrtf((float)dk);
+  return KDA_OK;
+}
+
+int chunk_common(const kda::ChunkArgs& a, int dtype, cudaStream_t st) {
+  if (a.chunk != 16 && a.chunk != 64) return KDA_ERR_CHUNK;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  const void* ptrs[] = {a.q, a.k, a.v, a.g, a.beta_logits, a.a_log, a.dt_bias,
+                        a.initial_state, a.out, a.final_state, a.cu_seqlens};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  // Element offsets are 64-bit in the kernels; keep every tensor under 2^40 elements and
+  // the sequence count within one grid dimension.
+  const double elems = (double)a.total_T * a.H * (a.dk > a.dv ? a.dk : a.dv);
+  const double state_elems = (double)a.B * a.H * a.dk * a.dv;
+  if (elems >= 1099511627776.0 || state_elems >= 1099511627776.0 || a.B > 65535 ||
+      a.H > 65535)
+    return KDA_ERR_TOO_LARGE;
+  int s = check_device();
+  if (s != KDA_OK) return s;
+  if (a.B == 0) return KDA_OK;
+  const cudaError_t e = kda::launch_chunk_simt(a, dtype == KDA_BF16, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta_logits, const float* a_log, const float* dt_bias,
+                  float scale, float lower_bound, const float* initial_state, void* out,
+                  float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                  int dtype, kda_stream_t stream) {
+  if (!q || !k || !v || !g || !beta_logits || !a_log || !dt_bias || !out)
+    return KDA_ERR_NULL_POINTER;
+  if (B < 0 || T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
+  int s = check_common(&scale, lower_bound, dk, dv);
+  if (s != KDA_OK) return s;
+  kda::ChunkArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta_logits = beta_logits; a.a_log = a_log;
+  a.dt_bias = dt_bias; a.initial_state = initial_state; a.out = out;
+  a.final_state = final_state; a.cu_seqlens = nullptr; a.scale = scale;
+  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_TOO_LARGE;
+  a.lower_bound = lower_bound; a.B = B; a.T = T; a.total_T = B * T;
+  a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta_logits, const float* a_log, const float* dt_bias,
+                         float scale, float lower_bound, const int32_t* cu_seqlens, int N,
+                         int total_T, const float* initial_state, void* out,
+                         float* final_state, int H, int dk, int dv, int chunk, int dtype,
+                         kda_stream_t stream) {
+  if (!q || !k || !v || !g || !beta_logits || !a_log || !dt_bias || !out || !cu_seqlens)
+    return KDA_ERR_NULL_POINTER;
+  if (N < 0 || total_T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
+  int s = check_common(&scale, lower_bound, dk, dv);
+  if (s != KDA_OK) return s;
+  kda::ChunkArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta_logits = beta_logits; a.a_log = a_log;
+  a.dt_bias = dt_bias; a.initial_state = initial_state; a.out = out;
+  a.final_state = final_state; a.cu_seqlens = cu_seqlens; a.scale = scale;
+  a.lower_bound = lower_bound; a.B = N; a.T = 0; a.total_T = total_T;
+  a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kda_decode_step(const float* q, const float* k, const float* v, const float* g,
+                    const float* beta_logits, const float* a_log, const float* dt_bias,
+                    float scale, float lower_bound, float* out, float* S, int B, int H,
+                    int dk, int dv, kda_stream_t stream) {
+  if (!q || !k || !v || !g || !beta_logits || !a_log || !dt_bias || !out || !S)
+    return KDA_ERR_NULL_POINTER;
+  if (B < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
+  int s = check_common(&scale, lower_bound, dk, dv);
+  if (s != KDA_OK) return s;
+  const void* ptrs[] = {q, k, v, g, beta_logits, a_log, dt_bias, out, S};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return KDA_ERR_MISALIGNED;
+  if ((double)B * H * dk * dv >= 1099511627776.0 || (long long)B * H > 0x7fffffffLL)
+    return KDA_ERR_TOO_LARGE;
+  s = check_device();
+  if (s != KDA_OK) return s;
+  if (B == 0) return KDA_OK;
+  kda::DecodeArgs a{q, k, v, g, beta_logits, a_log, dt_bias, out, S, scale, lower_bound,
+                    B, H, dk, dv};
+  const cudaError_t e = kda::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+const char* kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case KDA_ERR_BAD_SHAPE: return "invalid size (negative, or zero heads)";
+    case KDA_ERR_HEAD_DIM: return "dk and dv must each be 32, 64 or 128";
+    case KDA_ERR_CHUNK: return "chunk must be 16 or 64";
+    case KDA_ERR_LOWER_BOUND: return "lower_bound must be finite and in [-5, 0]";
+    case KDA_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+    case KDA_ERR_DTYPE: return "dtype must be KDA_F32 or KDA_BF16";
+    case KDA_ERR_LAUNCH: return "CUDA launch failed";
+    case KDA_ERR_DEVICE: return "no usable CUDA device of compute capability 10.3";
+    case KDA_ERR_SCALE: return "scale must be finite";
+    case KDA_ERR_TOO_LARGE: return "problem too large for the kernels' index limits";
+    default: return "unknown kda status";
+  }
+}
+
+int kda_version(void) { return 100; }
+
+}  // extern "C"

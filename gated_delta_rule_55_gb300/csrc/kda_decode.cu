@@ -1,0 +1,153 @@
+// Single-token KDA decode step (NKI "KDA TKG Kernel API Reference", kda_tkg): for every
+// (request b, head h) the fp32 memory S[b, h] ([dk, dv]) is streamed from HBM exactly
+// once, decayed, given the delta-rule write and written back in place, while the output
+// o = S_new^T q^ is formed from the same registers.
+//
+// Per (b, h), with S' = diag(exp(gamma)) S:
+//   p_k = S'^T k^,  p_q = S'^T q^            (reductions over the dk rows)
+//   u   = beta (v - p_k)
+//   S   = S' + k^ u^T
+//   o   = S^T q^ = p_q + u (k^ . q^)
+// Every value column is independent (the reductions run over dk only), so one pass
+// over S suffices.  The kernel is bound by HBM: 2 * dk * dv * 4 bytes of state traffic
+// against ~6 flops per state element.
+//
+// Layout of the work: one CTA of 256 threads per (b, h); thread (rg, cg) owns columns
+// 4cg..4cg+3 of the rows rg, rg + NRG, rg + 2 NRG, ... so that a warp reads whole
+// consecutive rows as 16-byte vectors (coalesced, one pass, no shared-memory staging).
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a) {
+  constexpr int NCG = DV / 4;                  // 16-byte column groups per row
+  constexpr int NRG = kDecodeThreads / NCG;    // row groups
+  constexpr int RPT = DK / NRG;                // rows per thread
+  static_assert(DK % NRG == 0 && RPT >= 1, "tile shape");
+
+  __shared__ float s_k[DK], s_q[DK], s_dec[DK];
+  __shared__ float s_v[DV], s_u[DV];
+  __shared__ float s_red_k[NRG][DV + 4];
+  __shared__ float s_red_q[NRG][DV + 4];
+  __shared__ float s_norm[3][4];
+  __shared__ float s_beta;
+
+  const int tid = threadIdx.x;
+  const int cg = tid % NCG;
+  const int rg = tid / NCG;
+  const long long bh = blockIdx.x;
+  const int b = (int)(bh / a.H);
+  const int h = (int)(bh % a.H);
+
+  // 1. Put the whole state tile in flight first (streaming: touched once per step).
+  float4* Sp = reinterpret_cast<float4*>(a.S + bh * (long long)(DK * DV));
+  float4 s[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(Sp + (i * NRG + rg) * NCG + cg);
+
+  // 2. Prologue while the state loads are in flight: gate, norms, beta.
+  float kq = 0.f, kk = 0.f, qq = 0.f;
+  if (tid < DK) {
+    const int c = tid;
+    const long long off = ((long long)b * DK + c) * a.H + h;  // [B, dk, H]
+    const float kc = a.k[off], qc = a.q[off], gc = a.g[off];
+    const float gamma = gate_gamma(gc, a.dt_bias[c * a.H + h], expf(a.a_log[h]),
+                                   a.lower_bound);
+    s_dec[c] = expf(gamma);
+    s_k[c] = kc;
+    s_q[c] = qc;
+    kk = warp_sum(kc * kc);
+    qq = warp_sum(qc * qc);
+    kq = warp_sum(kc * qc);
+    if ((tid & 31) == 0) {
+      s_norm[0][tid >> 5] = kk;
+      s_norm[1][tid >> 5] = qq;
+      s_norm[2][tid >> 5] = kq;
+    }
+  }
+  if (tid < DV) s_v[tid] = a.v[bh * DV + tid];  // [B, H, dv]
+  if (tid == 0) s_beta = sigmoidf_(a.beta_logits[bh]);  // [B, 1, H]
+  __syncthreads();
+  {
+    float k2 = 0.f, q2 = 0.f, kq2 = 0.f;
+#pragma unroll
+    for (int w = 0; w < DK / 32; ++w) {
+      k2 += s_norm[0][w];
+      q2 += s_norm[1][w];
+      kq2 += s_norm[2][w];
+    }
+    const float rk = 1.0f / sqrtf(k2 + kL2Eps);
+    const float rq = a.scale / sqrtf(q2 + kL2Eps);
+    kq = kq2 * rk * rq;  // k^ . q^ (scale included)
+    __syncthreads();     // everyone has read s_norm / raw s_k, s_q
+    if (tid < DK) {
+      s_k[tid] *= rk;
+      s_q[tid] *= rq;
+    }
+  }
+  __syncthreads();
+
+  // 3. Decay and the two partial reductions over this thread's rows.
+  float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int row = i * NRG + rg;
+    const float d = s_dec[row], kr = s_k[row], qr = s_q[row];
+    s[i].x *= d; s[i].y *= d; s[i].z *= d; s[i].w *= d;
+    pk.x += s[i].x * kr; pk.y += s[i].y * kr; pk.z += s[i].z * kr; pk.w += s[i].w * kr;
+    pq.x += s[i].x * qr; pq.y += s[i].y * qr; pq.z += s[i].z * qr; pq.w += s[i].w * qr;
+  }
+  *reinterpret_cast<float4*>(&s_red_k[rg][4 * cg]) = pk;
+  *reinterpret_cast<float4*>(&s_red_q[rg][4 * cg]) = pq;
+  __syncthreads();
+
+  // 4. Column totals, the delta u and the output.
+  if (tid < DV) {
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int r = 0; r < NRG; ++r) {
+      sk += s_red_k[r][tid];
+      sq += s_red_q[r][tid];
+    }
+    const float u = s_beta * (s_v[tid] - sk);
+    s_u[tid] = u;
+    a.out[bh * DV + tid] = sq + u * kq;  // [B, H, dv]
+  }
+  __syncthreads();
+
+  // 5. Rank-1 delta write and the in-place store.
+  const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * cg]);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const float kr = s_k[i * NRG + rg];
+    s[i].x += kr * u4.x; s[i].y += kr * u4.y; s[i].z += kr * u4.z; s[i].w += kr * u4.w;
+    __stcs(Sp + (i * NRG + rg) * NCG + cg, s[i]);
+  }
+}
+
+template <int DK>
+cudaError_t launch_dk(const DecodeArgs& a, cudaStream_t st) {
+  const dim3 grid((unsigned)((long long)a.B * a.H));
+  switch (a.dv) {
+    case 32: decode_kernel<DK, 32><<<grid, kDecodeThreads, 0, st>>>(a); break;
+    case 64: decode_kernel<DK, 64><<<grid, kDecodeThreads, 0, st>>>(a); break;
+    default: decode_kernel<DK, 128><<<grid, kDecodeThreads, 0, st>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+  switch (a.dk) {
+    case 32: return launch_dk<32>(a, st);
+    case 64: return launch_dk<64>(a, st);
+    default: return launch_dk<128>(a, st);
+  }
+}
+
+}  // namespace kda

@@ -1,0 +1,98 @@
+// Internal declarations shared by the translation units of libkda (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr float kL2Eps = 1e-6f;  // L2-norm epsilon: x / sqrt(sum(x^2) + eps)
+
+// Arguments of the chunked forward (fixed-length when cu_seqlens == nullptr).
+struct ChunkArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta_logits;
+  const float* a_log;
+  const float* dt_bias;
+  const float* initial_state;  // nullable
+  void* out;
+  float* final_state;          // nullable
+  const int32_t* cu_seqlens;   // nullable (fixed length)
+  float scale;
+  float lower_bound;
+  int B;        // sequences (B for fixed length, N for varlen)
+  int T;        // tokens per sequence (fixed length) -- unused for varlen
+  int total_T;  // tokens in the packed token axis (varlen); B*T for fixed length
+  int H;
+  int dk;
+  int dv;
+  int chunk;
+};
+
+struct DecodeArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* g;
+  const float* beta_logits;
+  const float* a_log;
+  const float* dt_bias;
+  float* out;
+  float* S;
+  float scale;
+  float lower_bound;
+  int B, H, dk, dv;
+};
+
+// Launchers (return cudaGetLastError() of their launch).
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_simt(const ChunkArgs& a, bool bf16, cudaStream_t stream);
+
+// Device helpers ------------------------------------------------------------------
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// Activated per-channel log-decay: lower_bound * sigmoid(exp(a_log) * (g + dt_bias)),
+// with exp(a_log) passed in pre-computed.
+__device__ __forceinline__ float gate_gamma(float g, float dt_bias, float exp_a_log,
+                                            float lower_bound) {
+  return lower_bound * sigmoidf_(exp_a_log * (g + dt_bias));
+}
+
+__device__ __forceinline__ float load_as_float(const float* p) { return *p; }
+__device__ __forceinline__ float load_as_float(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+__device__ __forceinline__ void store_from_float(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_from_float(__nv_bfloat16* p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Token range of sequence `seq` (clamped into [0, total_T] for packed inputs).
+__device__ __forceinline__ void seq_range(const ChunkArgs& a, int seq, long long& bos,
+                                          int& len) {
+  if (a.cu_seqlens != nullptr) {
+    int lo = a.cu_seqlens[seq], hi = a.cu_seqlens[seq + 1];
+    lo = min(max(lo, 0), a.total_T);
+    hi = min(max(hi, lo), a.total_T);
+    bos = lo;
+    len = hi - lo;
+  } else {
+    bos = (long long)seq * a.T;
+    len = a.T;
+  }
+}
+
+}  // namespace kda

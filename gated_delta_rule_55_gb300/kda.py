@@ -1,0 +1,135 @@
+"""Thin ctypes binding of libkda (include/kda.h): the same entry-point names, argument
+marshalling only.  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback, and every call fails loudly when the library is
+missing or returns an error.
+
+Tensor arguments may be ``torch.Tensor`` (CUDA, contiguous), raw device addresses
+(``int``) or ``None`` for the nullable ones.  ``stream`` defaults to torch's current
+stream on the current device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build_lib import LIB_PATH
+
+KDA_F32 = 0
+KDA_BF16 = 1
+STATUS_NAMES = {
+    0: "KDA_OK", -1: "KDA_ERR_NULL_POINTER", -2: "KDA_ERR_BAD_SHAPE", -3: "KDA_ERR_HEAD_DIM",
+    -4: "KDA_ERR_CHUNK", -5: "KDA_ERR_LOWER_BOUND", -6: "KDA_ERR_MISALIGNED",
+    -7: "KDA_ERR_DTYPE", -8: "KDA_ERR_LAUNCH", -9: "KDA_ERR_DEVICE", -10: "KDA_ERR_SCALE",
+    -11: "KDA_ERR_TOO_LARGE",
+}
+# Exported symbols, in declaration order of include/kda.h.
+EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_decode_step", "kda_status_string",
+           "kda_version")
+
+
+class KDAError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)} "
+                         f"({kda_status_string(status)})")
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """The loaded libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libkda.so is not built ({p}); run "
+                           "`python -m gated_delta_rule_55_gb300.build_lib`")
+    L = ctypes.CDLL(p)
+    L.kda_chunk_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P,
+                                _I, _I, _I, _I, _I, _I, _I, _P]
+    L.kda_chunk_fwd_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _I, _I,
+                                       _P, _P, _P, _I, _I, _I, _I, _I, _P]
+    L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
+                                  _I, _I, _I, _I, _P]
+    for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_decode_step", "kda_version"):
+        getattr(L, f).restype = _I
+    L.kda_status_string.argtypes = [_I]
+    L.kda_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = L
+    return L
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous CUDA tensors")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _dtype_code(x, dtype):
+    if dtype is not None:
+        return dtype
+    import torch
+    if x.dtype == torch.float32:
+        return KDA_F32
+    if x.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise ValueError(f"unsupported q/k/v dtype {x.dtype}")
+
+
+def _check(fn, status):
+    if status != 0:
+        raise KDAError(fn, status)
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def kda_version() -> int:
+    return lib().kda_version()
+
+
+def kda_chunk_fwd(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                  initial_state, out, final_state, B, T, H, dk, dv, chunk=64, dtype=None,
+                  stream=None):
+    """Chunked forward over B equal-length sequences (see include/kda.h)."""
+    _check("kda_chunk_fwd", lib().kda_chunk_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(initial_state), _ptr(out), _ptr(final_state),
+        B, T, H, dk, dv, chunk, _dtype_code(q, dtype), _stream(stream)))
+
+
+def kda_chunk_fwd_varlen(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                         cu_seqlens, N, total_T, initial_state, out, final_state, H, dk, dv,
+                         chunk=64, dtype=None, stream=None):
+    """Chunked forward over N packed sequences (see include/kda.h)."""
+    _check("kda_chunk_fwd_varlen", lib().kda_chunk_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
+        _ptr(out), _ptr(final_state), H, dk, dv, chunk, _dtype_code(q, dtype),
+        _stream(stream)))
+
+
+def kda_decode_step(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, out, S,
+                    B, H, dk, dv, stream=None):
+    """One decode token for B requests, S updated in place (see include/kda.h)."""
+    _check("kda_decode_step", lib().kda_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(out), _ptr(S), B, H, dk, dv, _stream(stream)))

@@ -1,0 +1,143 @@
+/*
+ * kda.h -- C ABI of libkda, the GB300 (sm_103a) Kimi / Kernel Delta Attention forward.
+ *
+ * KDA keeps, per (sequence, head), an fp32 memory S of shape [dk, dv] (rows = key
+ * channels, columns = value channels).  For each token, with
+ *     k^    = k / sqrt(|k|^2 + 1e-6)                  (L2 norm over dk)
+ *     q^    = scale * q / sqrt(|q|^2 + 1e-6)
+ *     gamma = lower_bound * sigmoid(exp(a_log[h]) * (g + dt_bias[:, h]))   (per channel, <= 0)
+ *     beta  = sigmoid(beta_logit)
+ * the memory is first decayed, S' = diag(exp(gamma)) S, then receives the delta-rule
+ * write S = S' + k^ (beta (v - S'^T k^))^T, and the token emits o = S^T q^.
+ *   - recurrence: ejkernel "kernel_delta_attention" module page, "The core recurrence"
+ *     (the error term is taken against the decayed memory: decay first, then write);
+ *   - gate / beta / scale / in-place state: NKI "KDA TKG Kernel API Reference", kda_tkg
+ *     parameters q, k, v, g, beta, a_log, dt_bias, out, S, scale, lower_bound;
+ *   - chunked / state passthrough: kernel_delta_attention page, "Algorithm modes" and the
+ *     chunk_size / initial_state / return_state parameters;
+ *   - packed sequences: ejkernel "recurrent" module page, cu_seqlens parameter.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device, dense (row-major,
+ *     no padding) and 16-byte aligned.  The caller allocates every buffer, outputs
+ *     included; the library allocates nothing and keeps no state between calls.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and
+ *     the call returns without synchronising.  Inputs must stay valid until the stream
+ *     reaches the launch.
+ *   - Head dimensions dk, dv must each be 32, 64 or 128 (kda_tkg: dk <= 128).
+ *   - lower_bound must lie in [-5, 0] (kda_tkg lower_bound): then exp(gamma) is in (0, 1]
+ *     and the kernels' factorised gate exponentials stay inside the fp32 range.
+ *   - scale <= 0 selects the default dk^-0.5 (kernel_delta_attention: softmax_scale None).
+ *   - Return value: KDA_OK (0) or a negative kda_status.  Argument errors are detected on
+ *     the host before anything is enqueued; KDA_ERR_LAUNCH reports cudaGetLastError()
+ *     after the launch.  Errors never abort the process.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (struct CUstream_st*); NULL is the legacy default stream. */
+typedef struct CUstream_st* kda_stream_t;
+
+/* Element type of q, k, v and out in the chunked entry points. */
+enum kda_dtype {
+  KDA_F32 = 0,  /* fp32 q/k/v/out */
+  KDA_BF16 = 1  /* bf16 q/k/v/out (fp32 accumulation, fp32 state) */
+};
+
+enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_NULL_POINTER = -1,    /* a required pointer is NULL */
+  KDA_ERR_BAD_SHAPE = -2,       /* a size is negative / zero where it must be positive */
+  KDA_ERR_HEAD_DIM = -3,        /* dk or dv not in {32, 64, 128} */
+  KDA_ERR_CHUNK = -4,           /* chunk not in {16, 64} */
+  KDA_ERR_LOWER_BOUND = -5,     /* lower_bound outside [-5, 0] or not finite */
+  KDA_ERR_MISALIGNED = -6,      /* a pointer is not 16-byte aligned */
+  KDA_ERR_DTYPE = -7,           /* dtype not a kda_dtype */
+  KDA_ERR_LAUNCH = -8,          /* the CUDA launch failed (cudaGetLastError) */
+  KDA_ERR_DEVICE = -9,          /* no usable device / not a compute capability 10.3 GPU */
+  KDA_ERR_SCALE = -10,          /* scale is NaN or infinite */
+  KDA_ERR_TOO_LARGE = -11       /* an index would overflow the kernels' 64-bit limits */
+};
+
+/*
+ * kda_chunk_fwd -- whole-sequence chunked forward for B equal-length sequences.
+ *   kernel_delta_attention.run / kda_attention (query, key, value, beta, decay,
+ *   initial_state, softmax_scale, chunk_size, return_state), with the per-channel raw gate
+ *   and beta logits of kda_tkg in place of the pre-activated per-head decay and beta.
+ *
+ *   q, k        [B, T, H, dk]   dtype (fp32 or bf16), raw (normalised inside)
+ *   v           [B, T, H, dv]   dtype
+ *   g           [B, T, H, dk]   fp32, raw per-channel gate
+ *   beta_logits [B, T, H]       fp32
+ *   a_log       [H]             fp32 (kda_tkg's [1, H])
+ *   dt_bias     [dk, H]         fp32 (kda_tkg layout)
+ *   initial_state [B, H, dk, dv] fp32, or NULL for zeros
+ *   out         [B, T, H, dv]   dtype, written
+ *   final_state [B, H, dk, dv]  fp32, written; NULL if not wanted.  May alias initial_state
+ *                               (the state is then advanced in place).
+ *   chunk       16 or 64: tokens per chunk of the chunked algorithm ("chunk_size").  The
+ *               result does not depend on it beyond rounding.
+ *   T == 0 is allowed: out is untouched and final_state receives initial_state (or zeros).
+ */
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta_logits, const float* a_log, const float* dt_bias,
+                  float scale, float lower_bound, const float* initial_state, void* out,
+                  float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                  int dtype, kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_varlen -- the same forward over N sequences packed along the token axis
+ *   (recurrent page, cu_seqlens: cumulative sequence lengths, [N + 1]).
+ *
+ *   q, k, g     [total_T, H, dk]; v, out [total_T, H, dv]; beta_logits [total_T, H]
+ *   cu_seqlens  [N + 1] int32 DEVICE array: cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[N] = total_T.  Sequence n owns tokens
+ *               [cu_seqlens[n], cu_seqlens[n + 1]) and starts from initial_state[n].
+ *               The kernels clamp every entry into [0, total_T], so a malformed array
+ *               gives wrong numbers but no out-of-bounds access.
+ *   initial_state, final_state [N, H, dk, dv] fp32 (same NULL / aliasing rules as above).
+ *   Empty sequences are allowed (their final state is their initial state).
+ */
+int kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta_logits, const float* a_log, const float* dt_bias,
+                         float scale, float lower_bound, const int32_t* cu_seqlens, int N,
+                         int total_T, const float* initial_state, void* out,
+                         float* final_state, int H, int dk, int dv, int chunk, int dtype,
+                         kda_stream_t stream);
+
+/*
+ * kda_decode_step -- advance the recurrence by exactly one token for B requests, in the
+ *   kda_tkg layouts (NKI "KDA TKG Kernel API Reference", kda_tkg), all fp32:
+ *
+ *   q, k, g     [B, dk, H]   (head innermost; raw, pre-norm / pre-activation)
+ *   v           [B, H, dv]
+ *   beta_logits [B, 1, H]
+ *   a_log       [H]          (the page's [1, H])
+ *   dt_bias     [dk, H]
+ *   out         [B, H, dv]   written
+ *   S           [B, H, dk, dv] IN/OUT: read, then overwritten with the advanced state.
+ *   scale, lower_bound: host floats (the page passes [1, 1] device tensors; host values
+ *   keep the call free of device reads and capturable in a CUDA graph).
+ */
+int kda_decode_step(const float* q, const float* k, const float* v, const float* g,
+                    const float* beta_logits, const float* a_log, const float* dt_bias,
+                    float scale, float lower_bound, float* out, float* S, int B, int H,
+                    int dk, int dv, kda_stream_t stream);
+
+/* Static, human-readable text for a kda_status value (never NULL). */
+const char* kda_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,121 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol include/kda.h
+declares, and rejects bad arguments on the host with the documented status codes before
+anything touches a device.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_55_gb300 as kda
+from gated_delta_rule_55_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+FAKE = 0x10000  # a 16-byte-aligned non-NULL address; never dereferenced by these tests
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return kda.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"^\s*(?:int|const char\s*\*)\s*(kda_\w+)\s*\(", text, re.M)
+
+
+def test_header_declares_the_boundary():
+    assert set(_declared()) == set(kda.kda.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(L):
+    assert kda.kda_status_string(0) == "ok"
+    for code in range(-11, 0):
+        assert kda.kda_status_string(code) != "unknown kda status"
+    assert kda.kda_status_string(-999) == "unknown kda status"
+    assert kda.kda_version() >= 100
+
+
+def _chunk(L, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, a_log=FAKE, dt_bias=FAKE, scale=0.0,
+             lb=-5.0, s0=None, out=FAKE, s1=None, B=1, T=64, H=2, dk=32, dv=32, chunk=16,
+             dtype=0)
+    a.update(over)
+    return L.kda_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["a_log"],
+                           a["dt_bias"], a["scale"], a["lb"], a["s0"], a["out"], a["s1"],
+                           a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"], a["dtype"],
+                           None)
+
+
+def _decode(L, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, a_log=FAKE, dt_bias=FAKE, scale=0.1,
+             lb=-5.0, out=FAKE, S=FAKE, B=4, H=2, dk=128, dv=128)
+    a.update(over)
+    return L.kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["a_log"],
+                             a["dt_bias"], a["scale"], a["lb"], a["out"], a["S"], a["B"],
+                             a["H"], a["dk"], a["dv"], None)
+
+
+def _varlen(L, **over):
+    a = dict(cu=FAKE, N=2, total=10, H=2, dk=64, dv=64, chunk=64, dtype=1, lb=-1.0)
+    a.update(over)
+    return L.kda_chunk_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, a["lb"],
+                                  a["cu"], a["N"], a["total"], None, FAKE, None, a["H"],
+                                  a["dk"], a["dv"], a["chunk"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), -1), (dict(out=None), -1), (dict(dt_bias=None), -1),
+    (dict(B=-1), -2), (dict(T=-3), -2), (dict(H=0), -2),
+    (dict(dk=48), -3), (dict(dv=256), -3), (dict(dk=16), -3),
+    (dict(chunk=32), -4), (dict(chunk=0), -4),
+    (dict(lb=0.5), -5), (dict(lb=-5.5), -5), (dict(lb=float("nan")), -5),
+    (dict(scale=float("inf")), -10), (dict(scale=float("nan")), -10),
+    (dict(dtype=2), -7), (dict(q=FAKE + 4), -6), (dict(s0=FAKE + 8), -6),
+    (dict(B=70000, T=1), -11),
+])
+def test_chunk_fwd_rejects_bad_arguments(L, over, code):
+    assert _chunk(L, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(S=None), -1), (dict(B=-1), -2), (dict(H=0), -2), (dict(dk=256), -3),
+    (dict(dv=8), -3), (dict(lb=1.0), -5), (dict(scale=float("nan")), -10),
+    (dict(S=FAKE + 4), -6), (dict(q=FAKE + 12), -6),
+])
+def test_decode_rejects_bad_arguments(L, over, code):
+    assert _decode(L, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(cu=None), -1), (dict(N=-1), -2), (dict(total=-1), -2), (dict(dk=100), -3),
+    (dict(chunk=8), -4), (dict(lb=-6.0), -5), (dict(dtype=5), -7), (dict(cu=FAKE + 4), -6),
+])
+def test_varlen_rejects_bad_arguments(L, over, code):
+    assert _varlen(L, **over) == code
+
+
+def test_valid_call_without_a_device_reports_no_device(L):
+    """On a machine without a GPU the first device query fails and the call returns
+    KDA_ERR_DEVICE instead of launching (fake pointers are never touched)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is only meaningful without one")
+    assert _chunk(L) == -9
+    assert _decode(L) == -9
+    assert _varlen(L) == -9
+
+
+def test_binding_raises_on_error_status(L):
+    with pytest.raises(kda.KDAError) as ei:
+        kda.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 3.0, FAKE, FAKE,
+                            1, 1, 128, 128, stream=0)
+    assert ei.value.status == -5
