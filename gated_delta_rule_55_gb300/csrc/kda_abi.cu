@@ -54,7 +54,9 @@ int chunk_common(const kda::ChunkArgs& a, int dtype, cudaStream_t st) {
   int s = check_device();
   if (s != KDA_OK) return s;
   if (a.B == 0) return KDA_OK;
-  const cudaError_t e = kda::launch_chunk_simt(a, dtype == KDA_BF16, st);
+  const bool bf16 = dtype == KDA_BF16;
+  const cudaError_t e = kda::chunk_tc_supported(a, bf16) ? kda::launch_chunk_tc(a, st)
+                                                         : kda::launch_chunk_simt(a, bf16, st);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
@@ -144,5 +146,11 @@ const char* kda_status_string(int status) {
 }
 
 int kda_version(void) { return 100; }
+
+int kda_device_error(int reset) {
+  int s = check_device();
+  if (s != KDA_OK) return s;
+  return (int)kda::chunk_tc_read_error(reset != 0);
+}
 
 }  // extern "C"

@@ -24,7 +24,7 @@ STATUS_NAMES = {
 }
 # Exported symbols, in declaration order of include/kda.h.
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_decode_step", "kda_status_string",
-           "kda_version")
+           "kda_version", "kda_device_error")
 
 
 class KDAError(RuntimeError):
@@ -56,7 +56,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
                                        _P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
                                   _I, _I, _I, _I, _P]
-    for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_decode_step", "kda_version"):
+    L.kda_device_error.argtypes = [_I]
+    for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_decode_step", "kda_version",
+              "kda_device_error"):
         getattr(L, f).restype = _I
     L.kda_status_string.argtypes = [_I]
     L.kda_status_string.restype = ctypes.c_char_p
@@ -104,6 +106,14 @@ def kda_status_string(status: int) -> str:
 
 def kda_version() -> int:
     return lib().kda_version()
+
+
+def kda_device_error(reset: bool = True) -> int:
+    """Bitmask of device-side errors recorded since the last reset (synchronises)."""
+    r = lib().kda_device_error(int(bool(reset)))
+    if r < 0:
+        raise KDAError("kda_device_error", r)
+    return r
 
 
 def kda_chunk_fwd(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,

@@ -136,6 +136,15 @@ const char* kda_status_string(int status);
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 int kda_version(void);
 
+/*
+ * kda_device_error -- bitmask of errors that kernels recorded on the current device since
+ *   the last reset (no paper counterpart: it reports the kernels' own safeguards).
+ *   Bit 0: a bounded wait inside the tensor-core chunk kernel gave up (its outputs for that
+ *   launch are incomplete).  Synchronises the device.  reset != 0 clears the mask.
+ *   Returns the mask (>= 0) or KDA_ERR_DEVICE.
+ */
+int kda_device_error(int reset);
+
 #ifdef __cplusplus
 }
 #endif

@@ -175,8 +175,8 @@ def test_varlen_workload_8seq_sampled():
     picks.append((int(np.argmax(np.diff(cu))), 0))  # the longest sequence
     for n, h in picks:
         a, b = cu[n], cu[n + 1]
-        q, k, v = (oracle_inputs({"x": d[x][None, a:b, h:h + 1]}, True)["x"] for x in ("q", "k", "v"))
-        ro, rs = kda_forward(q, k, v, d["g"][None, a:b, h:h + 1],
+        o = oracle_inputs({x: d[x][None, a:b, h:h + 1] for x in ("q", "k", "v")}, True)
+        ro, rs = kda_forward(o["q"], o["k"], o["v"], d["g"][None, a:b, h:h + 1],
                              d["beta_logits"][None, a:b, h:h + 1], d["a_log"][h:h + 1],
                              d["dt_bias"][:, h:h + 1], w.q_scale, w.lower_bound,
                              d["initial_state"][n:n + 1, h:h + 1])
