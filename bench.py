@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the decode / varlen / e2e / cpu-baseline measurements")
+    p.add_argument("--profile", choices=["chunk", "decode", "varlen"], default=None,
+                   help="run two launches of one kernel on a reduced case (for ncu) and exit")
     return p.parse_args()
 
 
@@ -440,6 +442,28 @@ def native(args):
     dist.close()
 
 
+def profile_case(which):
+    """Two launches of one kernel on a case sized for an ncu capture: inputs larger than
+    L2 but a few hundred MB on the device at most."""
+    torch = _torch()
+    from dataclasses import replace
+    from gated_delta_rule_55_gb300 import build_lib, synth
+    build_lib.build()
+    import gated_delta_rule_55_gb300 as kda
+    kda.lib()
+    if which == "decode":
+        w = synth.DECODE_B64
+        decode_measure(w, 2, False)
+    else:
+        w = replace(synth.PREFILL_B4, H=8) if which == "chunk" else \
+            replace(synth.VARLEN_8, H=4)
+        _, x = device_prefill(w)
+        for _ in range(2):
+            call_chunk(w, x)
+    torch.cuda.synchronize()
+    print(f"profile case {which}: {w.name} done", flush=True)
+
+
 # ---------------------------------------------------------------------- reference arm
 
 def reference(args):
@@ -483,7 +507,9 @@ def reference(args):
 
 if __name__ == "__main__":
     a = parse_args()
-    if a.impl == "reference":
+    if a.profile:
+        profile_case(a.profile)
+    elif a.impl == "reference":
         reference(a)
     else:
         native(a)

@@ -133,6 +133,25 @@ def test_varlen_small_with_empty_and_ragged_sequences(bf16):
     np.testing.assert_array_equal(S[1], d["initial_state"][1])
 
 
+def test_varlen_tensor_core_path_small():
+    """dk = dv = 128, bf16, chunk 64 (the tensor-core kernel) with empty, single-token,
+    exactly-one-chunk and ragged sequences; no bounded wait may have given up."""
+    from gated_delta_rule_55_gb300 import kda_device_error
+    kda_device_error(reset=True)
+    lens = [130, 0, 1, 64, 200, 63]
+    H, dk, dv = 2, 128, 128
+    d = synth.varlen_inputs(lens, H, dk, dv, seed=14, state_std=0.1)
+    for lb in (-5.0, -0.1):
+        out, S = run_varlen(d, H, dk, dv, 0.09, lb, 64, True)
+        o = oracle_inputs(d, True)
+        ref_out, ref_S = kda_forward_varlen(o["q"], o["k"], o["v"], o["g"], o["beta_logits"],
+                                            o["a_log"], o["dt_bias"], d["cu_seqlens"], 0.09,
+                                            lb, o["initial_state"])
+        _check(out, S, ref_out, ref_S, True)
+        np.testing.assert_array_equal(S[1], d["initial_state"][1])
+    assert kda_device_error(reset=True) == 0
+
+
 def _sampled_oracle(d, bs, hs, scale, lb, bf16):
     """Oracle on selected (b, h) pairs of a [B, T, H, .] problem (pairs are independent)."""
     outs, states = [], []
