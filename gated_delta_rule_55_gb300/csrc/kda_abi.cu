@@ -150,7 +150,7 @@ int kda_version(void) { return 100; }
 int kda_device_error(int reset) {
   int s = check_device();
   if (s != KDA_OK) return s;
-  return (int)kda::chunk_tc_read_error(reset != 0);
+  return (int)(kda::chunk_tc_read_error(reset != 0) | kda::decode_read_error(reset != 0));
 }
 
 }  // extern "C"

@@ -52,6 +52,7 @@ struct DecodeArgs {
 
 // Launchers (return cudaGetLastError() of their launch).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+unsigned int decode_read_error(bool reset);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, bool bf16, cudaStream_t stream);
 // Tensor-core chunk kernel: bf16 q/k/v, dk = dv = 128, 64-token chunks.
 bool chunk_tc_supported(const ChunkArgs& a, bool bf16);
