@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float s_gtot[8][kD];
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t s_tmem;
+  __shared__ int s_wait_ok[2];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -222,8 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         : make_float2(0.f, 0.f);
   }
 
+  // One thread polls the barrier; the block learns the outcome through shared memory
+  // (alternating slots: consecutive calls are always separated by this __syncthreads).
+  uint32_t wait_calls = 0;
+  auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const uint32_t slot = wait_calls++ & 1;
+    if (tid == 0) s_wait_ok[slot] = mbar_wait(bar, parity) ? 1 : 0;
+    __syncthreads();
+    return s_wait_ok[slot] != 0;
+  };
   auto mma_wait = [&]() -> bool {
-    const bool w = mbar_wait(&bar_mma, mma_phase & 1);
+    const bool w = block_wait(&bar_mma, mma_phase & 1);
     ++mma_phase;
     return w;
   };
@@ -237,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < kC) {
       s_beta[tid] = tid < n ? sigmoidf_(a.beta_logits[(tok0 + tid) * H + h]) : 0.f;
     }
-    bool w = mbar_wait(&bar_tma, ch & 1);
-    if (!__syncthreads_and(w)) { ok = false; break; }
+    bool w = block_wait(&bar_tma, ch & 1);
+    if (!w) { ok = false; break; }
     tma_pending = false;
 
     // ---- norms (warp w: tokens 4w .. 4w + 3) and the gate prefix (thread: 2 channels)
@@ -401,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar_mma);
     }
     w = mma_wait();
-    if (!__syncthreads_and(w)) { ok = false; break; }
+    if (!w) { ok = false; break; }
     tc_fence_after();
 
     // ---- read A (lanes 0..63) and M (lanes 64..127); warpgroup wg takes columns s of
@@ -482,31 +492,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       // off-diagonal blocks by distance d = i - j: Y = sum_k L_ik X_kj, X_ij = -X_ii Y.
       // Block (i, i - d) is handled by warpgroup (i - d); thread: row a, columns b, b + 1.
-      const int a_ = ln >> 3, b_ = (ln & 7) * 2;
+      const int a_ = ln >> 3, b_ = (ln & 7) * 2, jj = wg;
+#pragma unroll
       for (int d = 1; d < 4; ++d) {
-        const int jj = wg, ii = wg + d;
+        const int ii = jj + d;
         if (ii < 4) {
-          float y0 = 0.f, y1 = 0.f;
-          for (int m = 16 * jj; m < 16 * ii; ++m) {
-            const float l = L[(16 * ii + a_) * LDL + m];
-            const float2 x2 = *reinterpret_cast<const float2*>(X + m * LDL + 16 * jj + b_);
-            y0 += l * x2.x;
-            y1 += l * x2.y;
+          const float* Lr = L + (16 * ii + a_) * LDL + 16 * jj;
+          const float* Xc = X + (16 * jj) * LDL + 16 * jj + b_;
+          float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16 * d; m += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(Lr + m);
+            const float2 x0 = *reinterpret_cast<const float2*>(Xc + (m + 0) * LDL);
+            const float2 x1 = *reinterpret_cast<const float2*>(Xc + (m + 1) * LDL);
+            const float2 x2 = *reinterpret_cast<const float2*>(Xc + (m + 2) * LDL);
+            const float2 x3 = *reinterpret_cast<const float2*>(Xc + (m + 3) * LDL);
+            y0 += l4.x * x0.x + l4.z * x2.x;
+            y1 += l4.x * x0.y + l4.z * x2.y;
+            y2 += l4.y * x1.x + l4.w * x3.x;
+            y3 += l4.y * x1.y + l4.w * x3.y;
           }
-          Y[jj * 272 + a_ * 17 + b_] = y0;
-          Y[jj * 272 + a_ * 17 + b_ + 1] = y1;
+          Y[jj * 272 + a_ * 17 + b_] = y0 + y2;
+          Y[jj * 272 + a_ * 17 + b_ + 1] = y1 + y3;
         }
         __syncthreads();
         if (ii < 4) {
-          float z0 = 0.f, z1 = 0.f;
+          const float* Xr = X + (16 * ii + a_) * LDL + 16 * ii;
+          float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const float xv = X[(16 * ii + a_) * LDL + 16 * ii + m];
-            z0 += xv * Y[jj * 272 + m * 17 + b_];
-            z1 += xv * Y[jj * 272 + m * 17 + b_ + 1];
+          for (int m = 0; m < 16; m += 4) {
+            const float4 x4 = *reinterpret_cast<const float4*>(Xr + m);
+            z0 += x4.x * Y[jj * 272 + (m + 0) * 17 + b_] + x4.z * Y[jj * 272 + (m + 2) * 17 + b_];
+            z1 += x4.x * Y[jj * 272 + (m + 0) * 17 + b_ + 1] + x4.z * Y[jj * 272 + (m + 2) * 17 + b_ + 1];
+            z2 += x4.y * Y[jj * 272 + (m + 1) * 17 + b_] + x4.w * Y[jj * 272 + (m + 3) * 17 + b_];
+            z3 += x4.y * Y[jj * 272 + (m + 1) * 17 + b_ + 1] + x4.w * Y[jj * 272 + (m + 3) * 17 + b_ + 1];
           }
           *reinterpret_cast<float2*>(X + (16 * ii + a_) * LDL + 16 * jj + b_) =
-              make_float2(-z0, -z1);
+              make_float2(-(z0 + z2), -(z1 + z3));
         }
         __syncthreads();
       }
@@ -543,16 +565,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar_mma);
     }
     w = mma_wait();
-    if (!__syncthreads_and(w)) { ok = false; break; }
+    if (!w) { ok = false; break; }
     tc_fence_after();
-    // -W into smem: thread (c = ln, rows 16 wg .. 16 wg + 15)
+    // -W into smem: thread (c = ln, rows 16 wg .. 16 wg + 15); row r has r & 7 == i & 7
     {
       float v16[16];
       tmem_ld16(tl + TM_DW + 16 * wg, v16);
+      const uint32_t wkb = uint32_t(ln >> 6) * 8192u, wch = uint32_t(((ln & 63) * 2) >> 4),
+                     wby = uint32_t(((ln & 63) * 2) & 15);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_W + sw128_offset<2>(64, 16 * wg + i, ln)) =
-            __float2bfloat16_rn(-v16[i]);
+      for (int i = 0; i < 16; ++i) {
+        const int r = 16 * wg + i;
+        const uint32_t off = wkb + uint32_t((r >> 3) * 1024 + (i & 7) * 128) +
+                             (((wch ^ uint32_t(i & 7)) << 4) | wby);
+        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_W + off) = __float2bfloat16_rn(-v16[i]);
+      }
     }
     fence_async_smem();
     tc_fence_before();
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tl + TM_S + 32 * wg, S);
     }
     w = mma_wait();
-    if (!__syncthreads_and(w)) { ok = false; break; }
+    if (!w) { ok = false; break; }
     tc_fence_after();
     // ---- U^T -> bf16 A operand: thread (j = ln, tokens 16 wg .. 16 wg + 15)
     {
@@ -604,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar_mma);
     }
     w = mma_wait();
-    if (!__syncthreads_and(w)) { ok = false; break; }
+    if (!w) { ok = false; break; }
     tc_fence_after();
     // ---- bf16 copy of the new state and the output
     {

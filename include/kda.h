@@ -139,9 +139,8 @@ int kda_version(void);
 /*
  * kda_device_error -- bitmask of errors that kernels recorded on the current device since
  *   the last reset (no paper counterpart: it reports the kernels' own safeguards).
- *   Bit 0: a bounded wait inside the tensor-core chunk kernel gave up; bit 1: one inside the
- *   decode kernel did (the outputs of that launch are incomplete).  Synchronises the
- *   device.  reset != 0 clears the mask.
+ *   Bit 0: a bounded wait inside the tensor-core chunk kernel gave up (the outputs of that
+ *   launch are incomplete).  Synchronises the device.  reset != 0 clears the mask.
  *   Returns the mask (>= 0) or KDA_ERR_DEVICE.
  */
 int kda_device_error(int reset);
