@@ -223,6 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         : make_float2(0.f, 0.f);
   }
 
+  // beta logits of the next chunk, loaded one chunk ahead by threads < 64
+  float blog = (tid < kC && tid < len) ? a.beta_logits[(bos + tid) * H + h] : 0.f;
+
   // One thread polls the barrier; the block learns the outcome through shared memory
   // (alternating slots: consecutive calls are always separated by this __syncthreads).
   uint32_t wait_calls = 0;
@@ -245,7 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- beta, then wait for this chunk's q/k/v tiles
     if (tid < kC) {
-      s_beta[tid] = tid < n ? sigmoidf_(a.beta_logits[(tok0 + tid) * H + h]) : 0.f;
+      s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
+      const int tn = t0 + kC + tid;
+      blog = (tn < len) ? a.beta_logits[(bos + tn) * H + h] : 0.f;
     }
     bool w = block_wait(&bar_tma, ch & 1);
     if (!w) { ok = false; break; }

@@ -12,45 +12,50 @@
 // over S suffices.  The kernel is bound by HBM: 2 * dk * dv * 4 bytes of state traffic
 // against ~6 flops per state element.
 //
-// Layout of the work: one CTA of 256 threads per (b, h); thread (rg, cg) owns columns
-// 4cg..4cg+3 of the rows rg, rg + NRG, rg + 2 NRG, ... so that a warp reads whole
-// consecutive rows as 16-byte vectors (coalesced, one pass, no shared-memory staging).
+// Layout of the work: one CTA of 128 threads per (b, h, 64-column slice); thread
+// (rg, cg) owns columns 4cg..4cg+3 of the rows rg, rg + NRG, ... so that a warp reads
+// 256-byte row segments as 16-byte vectors (coalesced, one pass, no shared-memory
+// staging).  Small CTAs keep several slices in flight per SM.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kDecodeThreads = 256;
-
-template <int DK, int DV>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a) {
-  constexpr int NCG = DV / 4;                  // 16-byte column groups per row
-  constexpr int NRG = kDecodeThreads / NCG;    // row groups
+// Column-slice blocks: every (b, h) state tile is cut into DV / DVB independent slices
+// of DVB value columns (the reductions run over dk only, so slices never interact); the
+// small per-(b, h) prologue is recomputed by each slice.
+template <int DK, int DV, int DVB, int NT>
+__global__ void __launch_bounds__(NT) decode_kernel(DecodeArgs a) {
+  constexpr int NCG = DVB / 4;                 // 16-byte column groups per row slice
+  constexpr int NRG = NT / NCG;                // row groups
   constexpr int RPT = DK / NRG;                // rows per thread
-  static_assert(DK % NRG == 0 && RPT >= 1, "tile shape");
+  constexpr int NSL = DV / DVB;                // slices per (b, h)
+  static_assert(DK % NRG == 0 && RPT >= 1 && NT >= DK && NT >= DVB, "tile shape");
 
   __shared__ float s_k[DK], s_q[DK], s_dec[DK];
-  __shared__ float s_v[DV], s_u[DV];
-  __shared__ float s_red_k[NRG][DV + 4];
-  __shared__ float s_red_q[NRG][DV + 4];
+  __shared__ float s_v[DVB], s_u[DVB];
+  __shared__ __align__(16) float s_red_k[NRG][DVB + 4];
+  __shared__ __align__(16) float s_red_q[NRG][DVB + 4];
   __shared__ float s_norm[3][4];
   __shared__ float s_beta;
 
   const int tid = threadIdx.x;
   const int cg = tid % NCG;
   const int rg = tid / NCG;
-  const long long bh = blockIdx.x;
+  const long long blk = blockIdx.x;
+  const long long bh = blk / NSL;
+  const int j0 = (int)(blk % NSL) * DVB;
   const int b = (int)(bh / a.H);
   const int h = (int)(bh % a.H);
 
-  // 1. Put the whole state tile in flight first (streaming: touched once per step).
-  float4* Sp = reinterpret_cast<float4*>(a.S + bh * (long long)(DK * DV));
+  // 1. Put this slice of the state in flight first (streaming: touched once per step).
+  float4* Sp = reinterpret_cast<float4*>(a.S + bh * (long long)(DK * DV) + j0);
   float4 s[RPT];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(Sp + (i * NRG + rg) * NCG + cg);
+  for (int i = 0; i < RPT; ++i) s[i] = __ldcs(Sp + (i * NRG + rg) * (DV / 4) + cg);
 
   // 2. Prologue while the state loads are in flight: gate, norms, beta.
-  float kq = 0.f, kk = 0.f, qq = 0.f;
+  float kq = 0.f;
   if (tid < DK) {
     const int c = tid;
     const long long off = ((long long)b * DK + c) * a.H + h;  // [B, dk, H]
@@ -60,16 +65,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
     s_dec[c] = expf(gamma);
     s_k[c] = kc;
     s_q[c] = qc;
-    kk = warp_sum(kc * kc);
-    qq = warp_sum(qc * qc);
-    kq = warp_sum(kc * qc);
+    const float kk = warp_sum(kc * kc), qq = warp_sum(qc * qc), kqs = warp_sum(kc * qc);
     if ((tid & 31) == 0) {
       s_norm[0][tid >> 5] = kk;
       s_norm[1][tid >> 5] = qq;
-      s_norm[2][tid >> 5] = kq;
+      s_norm[2][tid >> 5] = kqs;
     }
   }
-  if (tid < DV) s_v[tid] = a.v[bh * DV + tid];  // [B, H, dv]
+  if (tid < DVB) s_v[tid] = a.v[bh * DV + j0 + tid];  // [B, H, dv]
   if (tid == 0) s_beta = sigmoidf_(a.beta_logits[bh]);  // [B, 1, H]
   __syncthreads();
   {
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
   __syncthreads();
 
   // 4. Column totals, the delta u and the output.
-  if (tid < DV) {
+  if (tid < DVB) {
     float sk = 0.f, sq = 0.f;
 #pragma unroll
     for (int r = 0; r < NRG; ++r) {
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
     }
     const float u = s_beta * (s_v[tid] - sk);
     s_u[tid] = u;
-    a.out[bh * DV + tid] = sq + u * kq;  // [B, H, dv]
+    a.out[bh * DV + j0 + tid] = sq + u * kq;  // [B, H, dv]
   }
   __syncthreads();
 
@@ -125,19 +128,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
   for (int i = 0; i < RPT; ++i) {
     const float kr = s_k[i * NRG + rg];
     s[i].x += kr * u4.x; s[i].y += kr * u4.y; s[i].z += kr * u4.z; s[i].w += kr * u4.w;
-    __stcs(Sp + (i * NRG + rg) * NCG + cg, s[i]);
+    __stcs(Sp + (i * NRG + rg) * (DV / 4) + cg, s[i]);
   }
+}
+
+template <int DK, int DV>
+cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
+  // 64-column slices of 128 threads (16 rows x 4 columns per thread) for the wide tiles;
+  // whole tiles for the narrow ones.
+  constexpr int DVB = DV > 64 ? 64 : DV;
+  constexpr int NT = DK > DVB ? DK : DVB;
+  const dim3 grid((unsigned)((long long)a.B * a.H * (DV / DVB)));
+  decode_kernel<DK, DV, DVB, (NT < 128 ? 128 : NT)><<<grid, (NT < 128 ? 128 : NT), 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 template <int DK>
 cudaError_t launch_dk(const DecodeArgs& a, cudaStream_t st) {
-  const dim3 grid((unsigned)((long long)a.B * a.H));
   switch (a.dv) {
-    case 32: decode_kernel<DK, 32><<<grid, kDecodeThreads, 0, st>>>(a); break;
-    case 64: decode_kernel<DK, 64><<<grid, kDecodeThreads, 0, st>>>(a); break;
-    default: decode_kernel<DK, 128><<<grid, kDecodeThreads, 0, st>>>(a); break;
+    case 32: return launch_t<DK, 32>(a, st);
+    case 64: return launch_t<DK, 64>(a, st);
+    default: return launch_t<DK, 128>(a, st);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
