@@ -6,17 +6,21 @@
 // recurrence), with G the in-chunk cumulative log-decay and the chunk cut into four
 // 16-token sub-chunks R whose reference point P_R is G just before the sub-chunk:
 //
-//  prologue (SIMT, fused): L2 norms of q and k, gate activation and its cumulative sum,
-//    beta, and the gate-scaled bf16 operands (K-major, 128-byte swizzle, shared memory)
-//      Xl  = [k^_r e^{G_r - P_R}; q^_r e^{G_r - P_R}]                (128 x dk)
-//      Kb  = [k^_s e^{P_S - G_s} (diagonal sub-chunks);               (160 x dk)
-//             the same times e^{P_R - P_S} for every later sub-chunk R]
-//      Q~  = q^ e^{G},  K^^T = (k^ e^{G_C - G})^T,  K~^T = (k^ e^{G})^T,  V^T
-//  MMA1  [A; M] = Xl Kb^T                              gate-scaled K K^T and Q K^T
+//  prologue (SIMT, fused): gate activation and its cumulative sum, beta, and the
+//    gate-scaled bf16 operands of the RAW q and k (K-major, 128-byte swizzle):
+//      Xl  = [k_r e^{G_r - P_R}; q_r e^{G_r - P_R}]                  (128 x dk)
+//      Kb  = [k_s e^{P_S - G_s} (diagonal sub-chunks);                (224 x dk)
+//             the same times e^{P_R - P_S} for every later sub-chunk R;
+//             q_s e^{P_S - G_s}]
+//      Q~  = q e^{G},  K^^T = (k e^{G_C - G})^T,  K~^T = (k e^{G})^T,  V^T
+//  MMA1  [A; M] = Xl Kb^T: gate-scaled K K^T and Q K^T, and on its diagonal |k_r|^2 and
+//        |q_r|^2, from which the L2 norms rk = 1/|k|, rq = scale/|q| are taken.  The
+//        norms are then applied as row / column factors instead of to every element:
+//        A = diag(rk) A_raw diag(rk), W uses T diag(rk), U' = diag(rk) U, O = diag(rq) O'.
 //  solve T = (I + diag(beta) tril(A, -1))^{-1} diag(beta)     (fp32, blocked by 16)
-//  MMA2  W^T = K~^T T^T,  U~^T = V^T T^T                         (UT / WY transform)
-//  MMA3  U^T = U~^T - S^T W^T,  O^T = S^T Q~^T                   (S^T: bf16 copy in TMEM)
-//  MMA4  O^T += U^T M^T (M = tril(Q K^T part)),  S^T <- S^T diag(e^{G_C}) + U^T K^
+//  MMA2  W^T = K~^T (T diag(rk))^T,  U~^T = V^T T^T              (UT / WY transform)
+//  MMA3  U^T = U~^T - S^T W^T,  O'^T = S^T Q~^T                  (S^T: bf16 copy in TMEM)
+//  MMA4  O'^T += U'^T M_raw^T,  S^T <- S^T diag(e^{G_C}) + U'^T K^
 //        (the fp32 master state lives in Tensor Memory; it is decayed in place before
 //         MMA4 accumulates the chunk's update onto it)
 //
@@ -38,37 +42,42 @@ using namespace tc;
 constexpr int kC = 64;
 constexpr int kD = 128;
 constexpr int kThreads = 512;
-constexpr int kKbRows = 160;  // 64 diagonal + 16 + 32 + 48 off-diagonal key rows
+constexpr int kKbRows = 224;  // 64 diagonal + 16 + 32 + 48 off-diagonal key rows + 64 q rows
 
 // Dynamic shared memory (byte offsets from a 1024-aligned base).
 constexpr int OFF_Q = 0;                    // raw q tile, two SW128 boxes [64 tok x 64 ch]
 constexpr int OFF_K = OFF_Q + 16384;        // raw k tile
 constexpr int OFF_V = OFF_K + 16384;        // raw v tile
 constexpr int OFF_XL = OFF_V + 16384;       // Xl [128 x 128] bf16, K-major SW128
-constexpr int OFF_KB = OFF_XL + 32768;      // Kb [160 x 128]
-constexpr int OFF_QT = OFF_KB + 40960;      // Q~ [64 x 128]
+constexpr int OFF_KB = OFF_XL + 32768;      // Kb [224 x 128]
+constexpr int OFF_QT = OFF_KB + 57344;      // Q~ [64 x 128]
 constexpr int OFF_KHT = OFF_QT + 16384;     // K^^T [128 x 64]
 constexpr int OFF_KTT = OFF_KHT + 16384;    // K~^T [128 x 64]
 constexpr int OFF_VT = OFF_KTT + 16384;     // V^T [128 x 64]
-constexpr int OFF_M = OFF_VT + 16384;       // M [64 x 64]
-constexpr int OFF_W = OFF_M + 8192;         // -W [64 x 128]
-constexpr int OFF_END = OFF_W + 16384;
-// Re-used inside the Xl/Kb region once MMA1 has completed.
+constexpr int OFF_OS = OFF_VT + 16384;      // output staging [64 tok x 128 ch] bf16 SW128
+constexpr int OFF_END = OFF_OS + 16384;
+// Re-used inside the Xl/Kb region once MMA1 has completed (everything below is consumed
+// before the next chunk's prologue rewrites Xl/Kb).
 constexpr int LDL = 68;                     // fp32 row pitch (16-byte aligned rows)
+constexpr int LDY = 24;                     // pitch of the per-warp 16 x 16 scratch
 constexpr int OFF_L = OFF_XL;               // fp32 [64][68] beta-scaled strict lower A
 constexpr int OFF_X = OFF_L + 64 * LDL * 4; // fp32 [64][68] (I + L)^{-1}
-constexpr int OFF_Y = OFF_X + 64 * LDL * 4; // fp32 [3][16][17] solve temporaries
-constexpr int OFF_T = OFF_XL + 40960;       // T [64 x 64] bf16 SW128 (1024-aligned)
-static_assert(OFF_Y + 3 * 16 * 17 * 4 <= OFF_T, "solve scratch overlaps T");
-static_assert(OFF_T + 8192 <= OFF_QT, "T must stay inside the Xl/Kb region");
+constexpr int OFF_Y = OFF_X + 64 * LDL * 4; // fp32 [4][16][24] per-warp solve scratch
+constexpr int OFF_T = OFF_XL + 40960;       // T [64 x 64] bf16 SW128
+constexpr int OFF_TW = OFF_T + 8192;        // T diag(rk) [64 x 64]
+constexpr int OFF_W = OFF_TW + 8192;        // -W [64 x 128]
+constexpr int OFF_M = OFF_W + 16384;        // M_raw [64 x 64]
+static_assert(OFF_Y + 4 * 16 * LDY * 4 <= OFF_T, "solve scratch overlaps T");
+static_assert(OFF_M + 8192 <= OFF_QT, "reused tiles must stay inside the Xl/Kb region");
+static_assert(OFF_T % 1024 == 0 && OFF_W % 1024 == 0 && OFF_M % 1024 == 0, "alignment");
 constexpr size_t kSmemBytes = OFF_END + 1024;
 
 // Tensor Memory columns (512 allocated).
-constexpr uint32_t TM_D1 = 0;     // [A; M] accumulator, 160 columns
+constexpr uint32_t TM_D1 = 0;     // [A; M] accumulator, 224 columns
 constexpr uint32_t TM_DW = 0;     // W^T accumulator (after D1 is consumed), 64
-constexpr uint32_t TM_UA = 128;   // U^T A operand (bf16 pairs), 32
-constexpr uint32_t TM_DU = 160;   // U~^T then U^T accumulator, 64
-constexpr uint32_t TM_DO = 224;   // O^T accumulator, 64
+constexpr uint32_t TM_DU = 64;    // U~^T then U^T accumulator (after D1 is consumed), 64
+constexpr uint32_t TM_UA = 128;   // U'^T A operand (bf16 pairs), 32
+constexpr uint32_t TM_DO = 224;   // O'^T accumulator, 64
 constexpr uint32_t TM_S = 288;    // fp32 master state S^T, 128
 constexpr uint32_t TM_SA = 416;   // bf16 copy of S^T (A operand), 64
 constexpr uint32_t kTmemCols = 512;
@@ -85,8 +94,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ float fast_exp(float x) { return __expf(x); }
-__device__ __forceinline__ float fast_rcp(float x) { return __fdividef(1.0f, x); }
+// e^x as 2^(x log2 e) on the approximate exponential unit, and an approximate reciprocal:
+// single instructions; their relative error (~2^-22) is far below the bf16 rounding of
+// every operand they feed.
+__device__ __forceinline__ float fast_exp(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+  return y;
+}
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Packed bf16 x bf16 -> bf16 products (round to nearest even).
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 
 // tcgen05.st of 8 columns (shape 32x32b, x8), waited for.
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
@@ -97,7 +123,7 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
       : "memory");
 }
 
-// tcgen05.st of 32 columns, waited for.
+// tcgen05.st of 32 fp32 columns, waited for.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   uint32_t r[32];
 #pragma unroll
@@ -114,6 +140,92 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
+// Warp-level tf32 MMA (m16n8k8, fp32 accumulate) for the small 16 x 16 block products of
+// the triangular solve.  Fragment ownership (g = lane / 4, t = lane % 4):
+//   A 16x8: a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
+//   B 8x8:  b0 (t, g), b1 (t + 4, g)
+//   C 16x8: c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t), c3 (g + 8, 2t + 1)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// C[16 x 16] += A[16 x K] B[K x 16] for fp32 matrices in shared memory (row pitches
+// lda, ldb in floats), one warp.  C is two 16 x 8 accumulator tiles.
+template <int K>
+__device__ __forceinline__ void warp_gemm16(const float* A, int lda, const float* B, int ldb,
+                                            float (&c)[2][4], int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    const uint32_t a[4] = {__float_as_uint(A[g * lda + k0 + t]),
+                           __float_as_uint(A[(g + 8) * lda + k0 + t]),
+                           __float_as_uint(A[g * lda + k0 + t + 4]),
+                           __float_as_uint(A[(g + 8) * lda + k0 + t + 4])};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint32_t b[2] = {__float_as_uint(B[(k0 + t) * ldb + 8 * nt + g]),
+                             __float_as_uint(B[(k0 + t + 4) * ldb + 8 * nt + g])};
+      mma_tf32(c[nt], a, b);
+    }
+  }
+}
+
+// Store a 16 x 16 accumulator (times `sign`) to a row-major fp32 matrix (pitch ld).
+__device__ __forceinline__ void warp_store16(float* D, int ld, const float (&c)[2][4],
+                                             float sign, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    *reinterpret_cast<float2*>(D + g * ld + 8 * nt + 2 * t) =
+        make_float2(sign * c[nt][0], sign * c[nt][1]);
+    *reinterpret_cast<float2*>(D + (g + 8) * ld + 8 * nt + 2 * t) =
+        make_float2(sign * c[nt][2], sign * c[nt][3]);
+  }
+}
+
+// One level (block distance D) of the blocked triangular inverse: warp jj computes
+// X_{jj+D, jj} = -X_ii sum_{k=jj}^{jj+D-1} L_{jj+D, k} X_{k, jj} (16 x 16 blocks, fp32
+// storage with pitch LDL, tf32 products), through its own 16 x 16 scratch tile.
+template <int D>
+__device__ __forceinline__ void solve_level(const float* L, float* X, float* Y, int warp,
+                                            int lane) {
+  const int jj = warp, ii = warp + D;
+  if (ii >= 4) return;  // warp-uniform
+  float* Yw = Y + jj * 16 * LDY;
+  float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  warp_gemm16<16 * D>(L + (16 * ii) * LDL + 16 * jj, LDL, X + (16 * jj) * LDL + 16 * jj, LDL,
+                      c, lane);
+  warp_store16(Yw, LDY, c, 1.f, lane);
+  __syncwarp();
+  float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  warp_gemm16<16>(X + (16 * ii) * LDL + 16 * ii, LDL, Yw, LDY, z, lane);
+  warp_store16(X + (16 * ii) * LDL + 16 * jj, LDL, z, -1.f, lane);
+}
+
+// 3-D tiled store of a shared-memory box to global memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Byte offset of the 16-byte chunk holding tokens 8 tg .. 8 tg + 7 of row c of a
 // transposed [128 x 64] tile (rows = channels, tokens contiguous, one 128-byte block).
 __device__ __forceinline__ uint32_t trow_off(int c, int tg) {
@@ -123,7 +235,8 @@ __device__ __forceinline__ uint32_t trow_off(int c, int tg) {
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
-                    const __grid_constant__ CUtensorMap map_v, const ChunkArgs a) {
+                    const __grid_constant__ CUtensorMap map_v,
+                    const __grid_constant__ CUtensorMap map_o, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -141,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int wg = tid >> 7;            // warpgroup
   const int ln = tid & 127;           // TMEM lane of this thread (value index j)
   const int lane_base = 32 * (warp & 3);
-  // prologue mapping: channel pair c0, c0 + 1 and tokens 8 tg .. 8 tg + 7 (quarter R)
+  // prologue mapping: channel pair c0, c0 + 1 and tokens 8 tg .. 8 tg + 7 (quarter Rq)
   const int cp = tid & 63, tg = tid >> 6, Rq = tg >> 1;
   const int c0 = 2 * cp;
   const int h = blockIdx.x, seq = blockIdx.y;
@@ -162,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
     tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -187,17 +301,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float exp_a = __expf(a.a_log[h]);
   const float db0 = a.dt_bias[c0 * H + h], db1 = a.dt_bias[(c0 + 1) * H + h];
   const int nchunks = (len + kC - 1) / kC;
-  const uint32_t idesc_n160 = make_idesc(1, 128, 160);
+  const uint32_t idesc_n224 = make_idesc(1, 128, kKbRows);
   const uint32_t idesc_n64 = make_idesc(1, 128, 64);
   const uint32_t idesc_n128 = make_idesc(1, 128, 128);
-  // swizzle of this thread's channel pair inside a 128-byte row: kb block, chunk, byte
+  // Addressing of this thread's channel pair in the K-major SW128 tiles: element
+  // (8 tg + i + 8 k, c0) of a tile with `rows` rows lies at
+  //   kb * rows * 128 + (tg + k) * 1024 + sw[i],  sw[i] = i * 128 + ((chunk ^ i) << 4 | byte)
   const uint32_t c_kb = uint32_t(c0 >> 6);
   const uint32_t c_chunk = uint32_t(((c0 & 63) * 2) >> 4);
   const uint32_t c_byte = uint32_t(((c0 & 63) * 2) & 15);
-  auto row_off = [&](int rows, int r) -> uint32_t {  // element (r, c0) of a K-major tile
-    return c_kb * uint32_t(rows * 128) + uint32_t((r >> 3) * 1024 + (r & 7) * 128) +
-           (((c_chunk ^ uint32_t(r & 7)) << 4) | c_byte);
-  };
+  uint32_t sw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sw[i] = uint32_t(i * 128) + (((c_chunk ^ uint32_t(i)) << 4) | c_byte);
+  uint8_t* const p64 = sm + c_kb * 8192u + uint32_t(tg) * 1024u;    // 64-row tiles
+  uint8_t* const p128 = sm + OFF_XL + c_kb * 16384u + uint32_t(tg) * 1024u;
+  uint8_t* const p224 = sm + OFF_KB + c_kb * 28672u + uint32_t(tg) * 1024u;
+  // transposed stores: lanes 4..7 of each 8-lane group write row c0 + 1 first, so that
+  // the 8 lanes of one 128-bit wavefront hit 8 different swizzle phases
+  const int tsw = (lane & 4) ? 1 : 0;
 
   uint32_t mma_phase = 0;
   bool ok = true;
@@ -222,7 +343,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     graw[i] = (t < len) ? *reinterpret_cast<const float2*>(a.g + ((bos + t) * H + h) * kD + c0)
                         : make_float2(0.f, 0.f);
   }
-
   // beta logits of the next chunk, loaded one chunk ahead by threads < 64
   float blog = (tid < kC && tid < len) ? a.beta_logits[(bos + tid) * H + h] : 0.f;
 
@@ -246,34 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = min(kC, len - t0);
     const long long tok0 = bos + t0;
 
-    // ---- beta, then wait for this chunk's q/k/v tiles
-    if (tid < kC) {
-      s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
-      const int tn = t0 + kC + tid;
-      blog = (tn < len) ? a.beta_logits[(bos + tn) * H + h] : 0.f;
-    }
-    bool w = block_wait(&bar_tma, ch & 1);
-    if (!w) { ok = false; break; }
-    tma_pending = false;
-
-    // ---- norms (warp w: tokens 4w .. 4w + 3) and the gate prefix (thread: 2 channels)
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int t = 4 * warp + u;
-      const uint32_t off = sw128_offset<2>(64, t, 4 * lane);
-      const uint2 qv = *reinterpret_cast<const uint2*>(sm + OFF_Q + off);
-      const uint2 kv = *reinterpret_cast<const uint2*>(sm + OFF_K + off);
-      float sq = bf16_lo(qv.x) * bf16_lo(qv.x) + bf16_hi(qv.x) * bf16_hi(qv.x) +
-                 bf16_lo(qv.y) * bf16_lo(qv.y) + bf16_hi(qv.y) * bf16_hi(qv.y);
-      float sk = bf16_lo(kv.x) * bf16_lo(kv.x) + bf16_hi(kv.x) * bf16_hi(kv.x) +
-                 bf16_lo(kv.y) * bf16_lo(kv.y) + bf16_hi(kv.y) * bf16_hi(kv.y);
-      sq = warp_sum(sq);
-      sk = warp_sum(sk);
-      if (lane == 0) {
-        s_rq[t] = t < n ? a.scale * rsqrtf(sq + kL2Eps) : 0.f;
-        s_rk[t] = t < n ? rsqrtf(sk + kL2Eps) : 0.f;
-      }
-    }
+    // ---- gate prefix (thread: 2 channels x 8 tokens), beta, wait for q/k/v tiles
     float loc0[8], loc1[8];  // G_t - (G before this 8-token group), channels c0, c0 + 1
     {
       float r0 = 0.f, r1 = 0.f;
@@ -292,7 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       *reinterpret_cast<float2*>(&s_gtot[tg][c0]) = make_float2(r0, r1);
     }
-    __syncthreads();
+    if (tid < kC) {
+      s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
+      const int tn = t0 + kC + tid;
+      blog = (tn < len) ? a.beta_logits[(bos + tn) * H + h] : 0.f;
+    }
+    if (tid == 0) bulk_wait_read_all();  // previous output store done reading its staging
+    bool w = block_wait(&bar_tma, ch & 1);
+    if (!w) { ok = false; break; }
+    tma_pending = false;
     // prefetch the next chunk's raw gates (consumed at the next gate prefix)
     if (ch + 1 < nchunks) {
 #pragma unroll
@@ -323,8 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 1; r < 4; ++r)
         if (Rq == r) { Pm0 = P0[r]; Pm1 = P1[r]; }
       // offset of this group inside its quarter (odd groups follow an even one)
-      const float o0 = (tg & 1) ? tot[tg - 1].x : 0.f, o1 = (tg & 1) ? tot[tg - 1].y : 0.f;
-      const float eP0 = fast_exp(Pm0), eP1 = fast_exp(Pm1);            // e^{P_R}
+      float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+      for (int g = 0; g < 8; g += 2)
+        if (tg == g + 1) { o0 = tot[g].x; o1 = tot[g].y; }
+      const float eP0 = fast_exp(Pm0), eP1 = fast_exp(Pm1);                // e^{P_R}
       const float eCP0 = fast_exp(Gc0 - Pm0), eCP1 = fast_exp(Gc1 - Pm1);  // e^{G_C - P_R}
       float cR0[4], cR1[4];  // e^{P_R' - P_R}, later sub-chunks R'
 #pragma unroll
@@ -334,61 +438,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (tg == 0) *reinterpret_cast<float2*>(&s_dec[c0]) = make_float2(fast_exp(Gc0), fast_exp(Gc1));
 
-      uint32_t kh0[4], kh1[4], kt0[4], kt1[4], vt0[4], vt1[4];  // transposed packs
-      float pkh0 = 0.f, pkh1 = 0.f, pkt0 = 0.f, pkt1 = 0.f, pv0 = 0.f, pv1 = 0.f;
-      const float4 rk4a = *reinterpret_cast<const float4*>(&s_rk[8 * tg]);
-      const float4 rk4b = *reinterpret_cast<const float4*>(&s_rk[8 * tg + 4]);
-      const float4 rq4a = *reinterpret_cast<const float4*>(&s_rq[8 * tg]);
-      const float4 rq4b = *reinterpret_cast<const float4*>(&s_rq[8 * tg + 4]);
-      const float rkv[8] = {rk4a.x, rk4a.y, rk4a.z, rk4a.w, rk4b.x, rk4b.y, rk4b.z, rk4b.w};
-      const float rqv[8] = {rq4a.x, rq4a.y, rq4a.z, rq4a.w, rq4b.x, rq4b.y, rq4b.z, rq4b.w};
+      // Every operand is a product of raw bf16 pairs with per-channel factors, done as
+      // packed bf16x2 multiplies (each operand is rounded to bf16 for the MMA anyway).
+      const uint32_t eP2 = pack_bf16(eP0, eP1), eCP2 = pack_bf16(eCP0, eCP1);
+      const uint32_t c12 = pack_bf16(cR0[1], cR1[1]), c22 = pack_bf16(cR0[2], cR1[2]),
+                     c32 = pack_bf16(cR0[3], cR1[3]);
+      uint32_t khw[8], ktw[8], vvw[8];  // per-token (c0, c0 + 1) words of the transposed tiles
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int t = 8 * tg + i;
-        const uint32_t roff = row_off(64, t);
-        const uint32_t kw = *reinterpret_cast<const uint32_t*>(sm + OFF_K + roff);
-        const uint32_t qw = *reinterpret_cast<const uint32_t*>(sm + OFF_Q + roff);
-        const uint32_t vw = *reinterpret_cast<const uint32_t*>(sm + OFF_V + roff);
-        const float k0 = bf16_lo(kw) * rkv[i], k1 = bf16_hi(kw) * rkv[i];
-        const float q0 = bf16_lo(qw) * rqv[i], q1 = bf16_hi(qw) * rqv[i];
-        const float v0 = (t < n) ? bf16_lo(vw) : 0.f, v1 = (t < n) ? bf16_hi(vw) : 0.f;
+        const bool live = 8 * tg + i < n;
+        uint8_t* const r64 = p64 + sw[i];
+        uint8_t* const r128 = p128 + sw[i];
+        uint8_t* const r224 = p224 + sw[i];
+        const uint32_t kw = live ? *reinterpret_cast<const uint32_t*>(r64 + OFF_K) : 0u;
+        const uint32_t qw = live ? *reinterpret_cast<const uint32_t*>(r64 + OFF_Q) : 0u;
+        vvw[i] = live ? *reinterpret_cast<const uint32_t*>(r64 + OFF_V) : 0u;
         const float e0 = fast_exp(loc0[i] + o0), e1 = fast_exp(loc1[i] + o1);  // e^{G_t - P_R}
-        const float i0 = fast_rcp(e0), i1 = fast_rcp(e1);
-        const float xk0 = k0 * e0, xk1 = k1 * e1, xq0 = q0 * e0, xq1 = q1 * e1;
-        const float kd0 = k0 * i0, kd1 = k1 * i1;  // k^ e^{P_R - G_t}
-        *reinterpret_cast<uint32_t*>(sm + OFF_XL + row_off(128, t)) = pack_bf16(xk0, xk1);
-        *reinterpret_cast<uint32_t*>(sm + OFF_XL + row_off(128, 64 + t)) = pack_bf16(xq0, xq1);
-        *reinterpret_cast<uint32_t*>(sm + OFF_KB + row_off(kKbRows, t)) = pack_bf16(kd0, kd1);
-        if (Rq < 1)
-          *reinterpret_cast<uint32_t*>(sm + OFF_KB + row_off(kKbRows, 64 + t)) =
-              pack_bf16(kd0 * cR0[1], kd1 * cR1[1]);
-        if (Rq < 2)
-          *reinterpret_cast<uint32_t*>(sm + OFF_KB + row_off(kKbRows, 80 + t)) =
-              pack_bf16(kd0 * cR0[2], kd1 * cR1[2]);
-        if (Rq < 3)
-          *reinterpret_cast<uint32_t*>(sm + OFF_KB + row_off(kKbRows, 112 + t)) =
-              pack_bf16(kd0 * cR0[3], kd1 * cR1[3]);
-        *reinterpret_cast<uint32_t*>(sm + OFF_QT + row_off(64, t)) =
-            pack_bf16(xq0 * eP0, xq1 * eP1);  // q^ e^{G_t}
-        const float kh0v = kd0 * eCP0, kh1v = kd1 * eCP1;  // k^ e^{G_C - G_t}
-        const float kt0v = xk0 * eP0, kt1v = xk1 * eP1;    // k^ e^{G_t}
-        if (i & 1) {
-          kh0[i >> 1] = pack_bf16(pkh0, kh0v);
-          kh1[i >> 1] = pack_bf16(pkh1, kh1v);
-          kt0[i >> 1] = pack_bf16(pkt0, kt0v);
-          kt1[i >> 1] = pack_bf16(pkt1, kt1v);
-          vt0[i >> 1] = pack_bf16(pv0, v0);
-          vt1[i >> 1] = pack_bf16(pv1, v1);
-        }
-        pkh0 = kh0v; pkh1 = kh1v; pkt0 = kt0v; pkt1 = kt1v; pv0 = v0; pv1 = v1;
+        const uint32_t e2 = pack_bf16(e0, e1);
+        const uint32_t i2 = pack_bf16(fast_rcp(e0), fast_rcp(e1));  // e^{P_R - G_t}
+        const uint32_t xk = hmul2(kw, e2), xq = hmul2(qw, e2), kd = hmul2(kw, i2);
+        *reinterpret_cast<uint32_t*>(r128) = xk;
+        *reinterpret_cast<uint32_t*>(r128 + 8 * 1024) = xq;  // row 64 + t
+        *reinterpret_cast<uint32_t*>(r224) = kd;
+        if (Rq < 1) *reinterpret_cast<uint32_t*>(r224 + 8 * 1024) = hmul2(kd, c12);
+        if (Rq < 2) *reinterpret_cast<uint32_t*>(r224 + 10 * 1024) = hmul2(kd, c22);
+        if (Rq < 3) *reinterpret_cast<uint32_t*>(r224 + 14 * 1024) = hmul2(kd, c32);
+        // q e^{P_R - G_t}: its product with the q rows of Xl puts |q_t|^2 on a diagonal
+        *reinterpret_cast<uint32_t*>(r224 + 20 * 1024) = hmul2(qw, i2);
+        *reinterpret_cast<uint32_t*>(r64 + OFF_QT) = hmul2(xq, eP2);  // q e^{G_t}
+        khw[i] = hmul2(kd, eCP2);  // k e^{G_C - G_t}
+        ktw[i] = hmul2(xk, eP2);   // k e^{G_t}
       }
-      const uint32_t ta = trow_off(c0, tg), tb = trow_off(c0 + 1, tg);
-      *reinterpret_cast<uint4*>(sm + OFF_KHT + ta) = make_uint4(kh0[0], kh0[1], kh0[2], kh0[3]);
-      *reinterpret_cast<uint4*>(sm + OFF_KHT + tb) = make_uint4(kh1[0], kh1[1], kh1[2], kh1[3]);
-      *reinterpret_cast<uint4*>(sm + OFF_KTT + ta) = make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]);
-      *reinterpret_cast<uint4*>(sm + OFF_KTT + tb) = make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]);
-      *reinterpret_cast<uint4*>(sm + OFF_VT + ta) = make_uint4(vt0[0], vt0[1], vt0[2], vt0[3]);
-      *reinterpret_cast<uint4*>(sm + OFF_VT + tb) = make_uint4(vt1[0], vt1[1], vt1[2], vt1[3]);
+      // transposed tiles: row c0 takes the low halves of tokens 8 tg .. 8 tg + 7, row
+      // c0 + 1 the high halves; lanes 4..7 of each 8-lane group write row c0 + 1 first so
+      // that one 128-bit wavefront covers 8 different swizzle phases
+      uint4 lo[3], hi[3];
+      {
+        const uint32_t* src[3] = {khw, ktw, vvw};
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+          lo[m] = make_uint4(__byte_perm(src[m][0], src[m][1], 0x5410),
+                             __byte_perm(src[m][2], src[m][3], 0x5410),
+                             __byte_perm(src[m][4], src[m][5], 0x5410),
+                             __byte_perm(src[m][6], src[m][7], 0x5410));
+          hi[m] = make_uint4(__byte_perm(src[m][0], src[m][1], 0x7632),
+                             __byte_perm(src[m][2], src[m][3], 0x7632),
+                             __byte_perm(src[m][4], src[m][5], 0x7632),
+                             __byte_perm(src[m][6], src[m][7], 0x7632));
+        }
+      }
+      const uint32_t ta = trow_off(c0 + tsw, tg), tb = trow_off(c0 + 1 - tsw, tg);
+      const int offs[3] = {OFF_KHT, OFF_KTT, OFF_VT};
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        *reinterpret_cast<uint4*>(sm + offs[m] + ta) = tsw ? hi[m] : lo[m];
+        *reinterpret_cast<uint4*>(sm + offs[m] + tb) = tsw ? lo[m] : hi[m];
+      }
     }
     fence_async_smem();
     __syncthreads();
@@ -412,12 +517,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         mma_ss(tm + TM_D1, sw128_kdesc<2>(xa, 128, s), sw128_kdesc<2>(kb, kKbRows, s),
-               idesc_n160, s > 0);
+               idesc_n224, s > 0);
       mma_commit(&bar_mma);
     }
     w = mma_wait();
     if (!w) { ok = false; break; }
     tc_fence_after();
+
+    // ---- norms from the diagonals: |k_r|^2 = A_raw[r][r], |q_r|^2 = D1[64 + r][160 + r]
+    if (wg == 0) {
+      const int w4 = warp & 3, r = 32 * (w4 & 1) + lane;
+      float v32[32];
+      tmem_ld32(tl + TM_D1 + ((w4 < 2) ? 32 * w4 : 160 + 32 * (w4 - 2)), v32);
+      float nn = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) nn = (i == lane) ? v32[i] : nn;
+      if (w4 < 2)
+        s_rk[r] = (r < n) ? rsqrtf(nn + kL2Eps) : 0.f;
+      else
+        s_rq[r] = (r < n) ? a.scale * rsqrtf(nn + kL2Eps) : 0.f;
+    }
+    __syncthreads();
 
     // ---- read A (lanes 0..63) and M (lanes 64..127); warpgroup wg takes columns s of
     //      quarter q = wg.  Every tcgen05.ld address is warp-uniform.
@@ -443,15 +563,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ln < 64) {
-        const float br = s_beta[r];
+        const float sr = s_beta[r] * s_rk[r];
         float* L = reinterpret_cast<float*>(sm + OFF_L) + r * LDL + 16 * q;
 #pragma unroll
         for (int m4 = 0; m4 < 4; ++m4) {
+          const float4 rk4 = *reinterpret_cast<const float4*>(&s_rk[16 * q + 4 * m4]);
           float4 o;
-          o.x = (16 * q + 4 * m4 + 0 < r) ? br * v[4 * m4 + 0] : 0.f;
-          o.y = (16 * q + 4 * m4 + 1 < r) ? br * v[4 * m4 + 1] : 0.f;
-          o.z = (16 * q + 4 * m4 + 2 < r) ? br * v[4 * m4 + 2] : 0.f;
-          o.w = (16 * q + 4 * m4 + 3 < r) ? br * v[4 * m4 + 3] : 0.f;
+          o.x = (16 * q + 4 * m4 + 0 < r) ? sr * rk4.x * v[4 * m4 + 0] : 0.f;
+          o.y = (16 * q + 4 * m4 + 1 < r) ? sr * rk4.y * v[4 * m4 + 1] : 0.f;
+          o.z = (16 * q + 4 * m4 + 2 < r) ? sr * rk4.z * v[4 * m4 + 2] : 0.f;
+          o.w = (16 * q + 4 * m4 + 3 < r) ? sr * rk4.w * v[4 * m4 + 3] : 0.f;
           reinterpret_cast<float4*>(L)[m4] = o;
         }
       } else {
@@ -473,99 +594,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const float* L = reinterpret_cast<const float*>(sm + OFF_L);
       float* X = reinterpret_cast<float*>(sm + OFF_X);
-      float* Y = reinterpret_cast<float*>(sm + OFF_Y);
       // diagonal blocks: warp b inverts block b, lane s < 16 computes column s
       if (warp < 4 && lane < 16) {
         const int b0 = 16 * warp, s = lane;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float acc = 0.f;
+          float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
           for (int m4 = 0; m4 < r; m4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(L + (b0 + r) * LDL + b0 + m4);
-            if (m4 + 0 < r) acc += l4.x * x[m4 + 0];
-            if (m4 + 1 < r) acc += l4.y * x[m4 + 1];
-            if (m4 + 2 < r) acc += l4.z * x[m4 + 2];
-            if (m4 + 3 < r) acc += l4.w * x[m4 + 3];
+            if (m4 + 0 < r) acc0 += l4.x * x[m4 + 0];
+            if (m4 + 1 < r) acc1 += l4.y * x[m4 + 1];
+            if (m4 + 2 < r) acc0 += l4.z * x[m4 + 2];
+            if (m4 + 3 < r) acc1 += l4.w * x[m4 + 3];
           }
-          x[r] = (r == s) ? 1.f : -acc;  // rows above s stay 0: all their terms are 0
+          x[r] = (r == s) ? 1.f : -(acc0 + acc1);  // rows above s stay 0
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) X[(b0 + r) * LDL + b0 + s] = x[r];
       }
       __syncthreads();
-      // off-diagonal blocks by distance d = i - j: Y = sum_k L_ik X_kj, X_ij = -X_ii Y.
-      // Block (i, i - d) is handled by warpgroup (i - d); thread: row a, columns b, b + 1.
-      const int a_ = ln >> 3, b_ = (ln & 7) * 2, jj = wg;
-#pragma unroll
-      for (int d = 1; d < 4; ++d) {
-        const int ii = jj + d;
-        if (ii < 4) {
-          const float* Lr = L + (16 * ii + a_) * LDL + 16 * jj;
-          const float* Xc = X + (16 * jj) * LDL + 16 * jj + b_;
-          float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16 * d; m += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(Lr + m);
-            const float2 x0 = *reinterpret_cast<const float2*>(Xc + (m + 0) * LDL);
-            const float2 x1 = *reinterpret_cast<const float2*>(Xc + (m + 1) * LDL);
-            const float2 x2 = *reinterpret_cast<const float2*>(Xc + (m + 2) * LDL);
-            const float2 x3 = *reinterpret_cast<const float2*>(Xc + (m + 3) * LDL);
-            y0 += l4.x * x0.x + l4.z * x2.x;
-            y1 += l4.x * x0.y + l4.z * x2.y;
-            y2 += l4.y * x1.x + l4.w * x3.x;
-            y3 += l4.y * x1.y + l4.w * x3.y;
-          }
-          Y[jj * 272 + a_ * 17 + b_] = y0 + y2;
-          Y[jj * 272 + a_ * 17 + b_ + 1] = y1 + y3;
-        }
-        __syncthreads();
-        if (ii < 4) {
-          const float* Xr = X + (16 * ii + a_) * LDL + 16 * ii;
-          float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
-#pragma unroll
-          for (int m = 0; m < 16; m += 4) {
-            const float4 x4 = *reinterpret_cast<const float4*>(Xr + m);
-            z0 += x4.x * Y[jj * 272 + (m + 0) * 17 + b_] + x4.z * Y[jj * 272 + (m + 2) * 17 + b_];
-            z1 += x4.x * Y[jj * 272 + (m + 0) * 17 + b_ + 1] + x4.z * Y[jj * 272 + (m + 2) * 17 + b_ + 1];
-            z2 += x4.y * Y[jj * 272 + (m + 1) * 17 + b_] + x4.w * Y[jj * 272 + (m + 3) * 17 + b_];
-            z3 += x4.y * Y[jj * 272 + (m + 1) * 17 + b_ + 1] + x4.w * Y[jj * 272 + (m + 3) * 17 + b_ + 1];
-          }
-          *reinterpret_cast<float2*>(X + (16 * ii + a_) * LDL + 16 * jj + b_) =
-              make_float2(-(z0 + z2), -(z1 + z3));
-        }
-        __syncthreads();
-      }
-      // T[r][s] = X[r][s] beta_s (s <= r): thread row r = tid >> 3, columns 8 (tid & 7) ..
+      // Off-diagonal blocks level by level (distance d = i - j):
+      //   X_ij = -X_ii sum_{k=j}^{i-1} L_ik X_kj,
+      // one warp per block: the sum is one 16 x 16d x 16 product (tf32 warp MMAs), the
+      // result goes through a per-warp scratch tile into a second product with X_ii.
+      // ---- solve level d = 1
+      solve_level<1>(L, X, reinterpret_cast<float*>(sm + OFF_Y), warp, lane);
+      __syncthreads();
+      // ---- solve level d = 2
+      solve_level<2>(L, X, reinterpret_cast<float*>(sm + OFF_Y), warp, lane);
+      __syncthreads();
+      // ---- solve level d = 3
+      solve_level<3>(L, X, reinterpret_cast<float*>(sm + OFF_Y), warp, lane);
+      __syncthreads();
+      // ---- T[r][s] = X[r][s] beta_s and T diag(rk) (s <= r): row r = tid >> 3, 8 columns
       {
         const int r = tid >> 3, s0 = (tid & 7) * 8;
-        uint32_t pk[4];
+        const float4 xa = *reinterpret_cast<const float4*>(X + r * LDL + s0);
+        const float4 xb = *reinterpret_cast<const float4*>(X + r * LDL + s0 + 4);
+        const float4 ba = *reinterpret_cast<const float4*>(&s_beta[s0]);
+        const float4 bb = *reinterpret_cast<const float4*>(&s_beta[s0 + 4]);
+        const float4 ka = *reinterpret_cast<const float4*>(&s_rk[s0]);
+        const float4 kb = *reinterpret_cast<const float4*>(&s_rk[s0 + 4]);
+        const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+        const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+        const float kv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+        uint32_t pt[4], pw[4];
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          const int s = s0 + 2 * p;
-          const float t0v = (s <= r) ? X[r * LDL + s] * s_beta[s] : 0.f;
-          const float t1v = (s + 1 <= r) ? X[r * LDL + s + 1] * s_beta[s + 1] : 0.f;
-          pk[p] = pack_bf16(t0v, t1v);
+          const float t0v = (s0 + 2 * p <= r) ? xv[2 * p] * bv[2 * p] : 0.f;
+          const float t1v = (s0 + 2 * p + 1 <= r) ? xv[2 * p + 1] * bv[2 * p + 1] : 0.f;
+          pt[p] = pack_bf16(t0v, t1v);
+          pw[p] = pack_bf16(t0v * kv[2 * p], t1v * kv[2 * p + 1]);
         }
-        *reinterpret_cast<uint4*>(sm + OFF_T + sw128_offset<2>(64, r, s0)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        const uint32_t off = sw128_offset<2>(64, r, s0);
+        *reinterpret_cast<uint4*>(sm + OFF_T + off) = make_uint4(pt[0], pt[1], pt[2], pt[3]);
+        *reinterpret_cast<uint4*>(sm + OFF_TW + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA2: W^T = K~^T T^T, U~^T = V^T T^T
+    // ---- MMA2: W^T = K~^T (T diag(rk))^T, U~^T = V^T T^T
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t ts = smem_u32(sm + OFF_T), ks = smem_u32(sm + OFF_KTT),
-                     vs = smem_u32(sm + OFF_VT);
+      const uint32_t ts = smem_u32(sm + OFF_T), tw = smem_u32(sm + OFF_TW),
+                     ks = smem_u32(sm + OFF_KTT), vs = smem_u32(sm + OFF_VT);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        const uint64_t bd = sw128_kdesc<2>(ts, 64, s);
-        mma_ss(tm + TM_DW, sw128_kdesc<2>(ks, 128, s), bd, idesc_n64, s > 0);
-        mma_ss(tm + TM_DU, sw128_kdesc<2>(vs, 128, s), bd, idesc_n64, s > 0);
+        mma_ss(tm + TM_DW, sw128_kdesc<2>(ks, 128, s), sw128_kdesc<2>(tw, 64, s), idesc_n64,
+               s > 0);
+        mma_ss(tm + TM_DU, sw128_kdesc<2>(vs, 128, s), sw128_kdesc<2>(ts, 64, s), idesc_n64,
+               s > 0);
       }
       mma_commit(&bar_mma);
     }
@@ -590,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA3: U^T += S^T (-W)^T, O^T = S^T Q~^T
+    // ---- MMA3: U^T += S^T (-W)^T, O'^T = S^T Q~^T
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ws = smem_u32(sm + OFF_W), qs = smem_u32(sm + OFF_QT);
@@ -612,19 +714,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     w = mma_wait();
     if (!w) { ok = false; break; }
     tc_fence_after();
-    // ---- U^T -> bf16 A operand: thread (j = ln, tokens 16 wg .. 16 wg + 15)
+    // ---- U'^T = (diag(rk) U)^T -> bf16 A operand: thread (j = ln, tokens 16 wg .. + 15)
     {
       float v16[16];
       tmem_ld16(tl + TM_DU + 16 * wg, v16);
       uint32_t up[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) up[i] = pack_bf16(v16[2 * i], v16[2 * i + 1]);
+      for (int i = 0; i < 8; ++i)
+        up[i] = pack_bf16(v16[2 * i] * s_rk[16 * wg + 2 * i],
+                          v16[2 * i + 1] * s_rk[16 * wg + 2 * i + 1]);
       tmem_st8(tl + TM_UA + 8 * wg, up);
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA4: O^T += U^T M^T, S^T += U^T K^
+    // ---- MMA4: O'^T += U'^T M_raw^T, S^T += U'^T K^
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ms = smem_u32(sm + OFF_M), ks = smem_u32(sm + OFF_KHT);
@@ -638,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     w = mma_wait();
     if (!w) { ok = false; break; }
     tc_fence_after();
-    // ---- bf16 copy of the new state and the output
+    // ---- bf16 copy of the new state and the output O = diag(rq) O'
     {
       float S[32];
       tmem_ld32(tl + TM_S + 32 * wg, S);
@@ -648,15 +752,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(tl + TM_SA + 16 * wg, sp);
       float o16[16];
       tmem_ld16(tl + TM_DO + 16 * wg, o16);
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+      if (n == kC) {
+        // full chunk: stage the [64 x 128] bf16 tile for one TMA store (row r = 16 wg + i)
+        const uint32_t ob = uint32_t(ln >> 6) * 8192u + uint32_t(wg) * 2048u;
+        const uint32_t och = uint32_t(((ln & 63) * 2) >> 4), oby = uint32_t(((ln & 63) * 2) & 15);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = 16 * wg + i;
-        if (r < n) out[((tok0 + r) * H + h) * kD + ln] = __float2bfloat16_rn(o16[i]);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t off = ob + uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
+                               (((och ^ uint32_t(i & 7)) << 4) | oby);
+          *reinterpret_cast<__nv_bfloat16*>(sm + OFF_OS + off) =
+              __float2bfloat16_rn(o16[i] * s_rq[16 * wg + i]);
+        }
+      } else {
+        // last, partial chunk: plain stores of the live rows only (a full box would spill
+        // into the next sequence)
+        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
+                            ((tok0 + 16 * wg) * H + h) * kD + ln;
+        const long long stride = (long long)H * kD;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (16 * wg + i < n) op[i * stride] = __float2bfloat16_rn(o16[i] * s_rq[16 * wg + i]);
       }
     }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && n == kC) {
+      tma_store_3d(&map_o, sm + OFF_OS, 0, h, (int)tok0);
+      tma_store_3d(&map_o, sm + OFF_OS + 8192, 64, h, (int)tok0);
+      bulk_commit();
+    }
     // ---- end of chunk
   }
 
@@ -676,6 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       a.final_state[state_off + (long long)c * kD + ln] = S[i];
     }
   }
+  if (tid == 0) bulk_wait_all();  // output stores complete before the CTA retires
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -717,17 +843,17 @@ bool chunk_tc_supported(const ChunkArgs& a, bool bf16) {
 
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t st) {
   const long long rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const long long map_rows = rows > 0 ? rows : 1;  // empty inputs: the state still passes
   if (!make_map(&mq, a.q, map_rows, a.H) || !make_map(&mk, a.k, map_rows, a.H) ||
-      !make_map(&mv, a.v, map_rows, a.H))
+      !make_map(&mv, a.v, map_rows, a.H) || !make_map(&mo, a.out, map_rows, a.H))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.H, a.B);
-  chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, a);
+  chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mo, a);
   return cudaGetLastError();
 }
 
