@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "KDA chunked-fwd tokens/s; decode-step HBM GB/s vs peak (1 GB300)"
 L2_BYTES = 126 * 2 ** 20
-CHUNK_KERNEL_SOURCES = ["kda_chunk_simt.cu"]  # sources of the kernel the roofline covers
+CHUNK_KERNEL_SOURCES = ["kda_chunk_tc.cu", "tc_prims.cuh"]  # the kernel the roofline covers
 
 
 # ----------------------------------------------------------------------------- helpers

@@ -390,7 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tn = t0 + kC + tid;
       blog = (tn < len) ? a.beta_logits[(bos + tn) * H + h] : 0.f;
     }
-    if (tid == 0) bulk_wait_read_all();  // previous output store done reading its staging
     bool w = block_wait(&bar_tma, ch & 1);
     if (!w) { ok = false; break; }
     tma_pending = false;
@@ -730,6 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- MMA4: O'^T += U'^T M_raw^T, S^T += U'^T K^
     if (tid == 0) {
+      bulk_wait_read_all();  // the previous chunk's output store has read its staging tile
       tc_fence_after();
       const uint32_t ms = smem_u32(sm + OFF_M), ks = smem_u32(sm + OFF_KHT);
 #pragma unroll
