@@ -37,7 +37,10 @@ int check_common(float* scale, float lower_bound, int dk, int dv) {
   return KDA_OK;
 }
 
-int chunk_common(const kda::ChunkArgs& a, int dtype, cudaStream_t st) {
+// workspace == nullptr: the single-pass kernels; otherwise (a non-zero workspace size was
+// required and checked) the two-launch path.
+int chunk_common(const kda::ChunkArgs& a, int dtype, cudaStream_t st,
+                 void* workspace = nullptr, size_t workspace_bytes = 0, bool use_ws = false) {
   if (a.chunk != 16 && a.chunk != 64) return KDA_ERR_CHUNK;
   if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
   const void* ptrs[] = {a.q, a.k, a.v, a.g, a.beta_logits, a.a_log, a.dt_bias,
@@ -51,13 +54,73 @@ int chunk_common(const kda::ChunkArgs& a, int dtype, cudaStream_t st) {
   if (elems >= 1099511627776.0 || state_elems >= 1099511627776.0 || a.B > 65535 ||
       a.H > 65535)
     return KDA_ERR_TOO_LARGE;
+  const bool bf16 = dtype == KDA_BF16;
+  // (a configuration whose workspace size is 0 -- no tokens -- takes the single pass)
+  const bool split = use_ws && kda::chunk_tc_supported(a, bf16) &&
+                     kda::chunk_split_workspace(a) > 0;
+  if (split) {
+    if (!kda::chunk_split_index_ok(a)) return KDA_ERR_TOO_LARGE;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < kda::chunk_split_workspace(a))
+      return KDA_ERR_WORKSPACE;
+  }
   int s = check_device();
   if (s != KDA_OK) return s;
   if (a.B == 0) return KDA_OK;
-  const bool bf16 = dtype == KDA_BF16;
-  const cudaError_t e = kda::chunk_tc_supported(a, bf16) ? kda::launch_chunk_tc(a, st)
-                                                         : kda::launch_chunk_simt(a, bf16, st);
+  cudaError_t e;
+  if (split)
+    e = kda::launch_chunk_split(a, workspace, st);
+  else
+    e = kda::chunk_tc_supported(a, bf16) ? kda::launch_chunk_tc(a, st)
+                                         : kda::launch_chunk_simt(a, bf16, st);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+// Argument structures of the fixed-length and packed entry points (validated sizes).
+int fill_fixed(kda::ChunkArgs& a, const void* q, const void* k, const void* v, const float* g,
+               const float* beta_logits, const float* a_log, const float* dt_bias, float scale,
+               float lower_bound, const float* initial_state, void* out, float* final_state,
+               int B, int T, int H, int dk, int dv, int chunk) {
+  if (!q || !k || !v || !g || !beta_logits || !a_log || !dt_bias || !out)
+    return KDA_ERR_NULL_POINTER;
+  if (B < 0 || T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
+  int s = check_common(&scale, lower_bound, dk, dv);
+  if (s != KDA_OK) return s;
+  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_TOO_LARGE;
+  a = kda::ChunkArgs{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta_logits = beta_logits; a.a_log = a_log;
+  a.dt_bias = dt_bias; a.initial_state = initial_state; a.out = out;
+  a.final_state = final_state; a.cu_seqlens = nullptr; a.scale = scale;
+  a.lower_bound = lower_bound; a.B = B; a.T = T; a.total_T = B * T;
+  a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  return KDA_OK;
+}
+
+int fill_varlen(kda::ChunkArgs& a, const void* q, const void* k, const void* v,
+                const float* g, const float* beta_logits, const float* a_log,
+                const float* dt_bias, float scale, float lower_bound, const int32_t* cu_seqlens,
+                int N, int total_T, const float* initial_state, void* out, float* final_state,
+                int H, int dk, int dv, int chunk) {
+  if (!q || !k || !v || !g || !beta_logits || !a_log || !dt_bias || !out || !cu_seqlens)
+    return KDA_ERR_NULL_POINTER;
+  if (N < 0 || total_T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
+  int s = check_common(&scale, lower_bound, dk, dv);
+  if (s != KDA_OK) return s;
+  a = kda::ChunkArgs{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta_logits = beta_logits; a.a_log = a_log;
+  a.dt_bias = dt_bias; a.initial_state = initial_state; a.out = out;
+  a.final_state = final_state; a.cu_seqlens = cu_seqlens; a.scale = scale;
+  a.lower_bound = lower_bound; a.B = N; a.T = 0; a.total_T = total_T;
+  a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  return KDA_OK;
+}
+
+// Workspace bytes of the two-launch path (0 when the configuration does not use it or the
+// arguments are invalid).
+size_t ws_size(const kda::ChunkArgs& a, int dtype) {
+  if (a.chunk != 16 && a.chunk != 64) return 0;
+  if (dtype != KDA_BF16 || !kda::chunk_tc_supported(a, true)) return 0;
+  return kda::chunk_split_workspace(a);
 }
 
 }  // namespace
@@ -69,18 +132,10 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
                   float scale, float lower_bound, const float* initial_state, void* out,
                   float* final_state, int B, int T, int H, int dk, int dv, int chunk,
                   int dtype, kda_stream_t stream) {
-  if (!q || !k || !v || !g || !beta_logits || !a_log || !dt_bias || !out)
-    return KDA_ERR_NULL_POINTER;
-  if (B < 0 || T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
-  int s = check_common(&scale, lower_bound, dk, dv);
+  kda::ChunkArgs a;
+  const int s = fill_fixed(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                           initial_state, out, final_state, B, T, H, dk, dv, chunk);
   if (s != KDA_OK) return s;
-  kda::ChunkArgs a{};
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta_logits = beta_logits; a.a_log = a_log;
-  a.dt_bias = dt_bias; a.initial_state = initial_state; a.out = out;
-  a.final_state = final_state; a.cu_seqlens = nullptr; a.scale = scale;
-  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_TOO_LARGE;
-  a.lower_bound = lower_bound; a.B = B; a.T = T; a.total_T = B * T;
-  a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
   return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -90,18 +145,59 @@ int kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const floa
                          int total_T, const float* initial_state, void* out,
                          float* final_state, int H, int dk, int dv, int chunk, int dtype,
                          kda_stream_t stream) {
-  if (!q || !k || !v || !g || !beta_logits || !a_log || !dt_bias || !out || !cu_seqlens)
-    return KDA_ERR_NULL_POINTER;
-  if (N < 0 || total_T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
-  int s = check_common(&scale, lower_bound, dk, dv);
+  kda::ChunkArgs a;
+  const int s = fill_varlen(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                            cu_seqlens, N, total_T, initial_state, out, final_state, H, dk, dv,
+                            chunk);
   if (s != KDA_OK) return s;
-  kda::ChunkArgs a{};
-  a.q = q; a.k = k; a.v = v; a.g = g; a.beta_logits = beta_logits; a.a_log = a_log;
-  a.dt_bias = dt_bias; a.initial_state = initial_state; a.out = out;
-  a.final_state = final_state; a.cu_seqlens = cu_seqlens; a.scale = scale;
-  a.lower_bound = lower_bound; a.B = N; a.T = 0; a.total_T = total_T;
-  a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
   return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
+                                    int dtype) {
+  if (B < 0 || T < 0 || H <= 0 || (long long)B * T > 0x7fffffffLL) return 0;
+  kda::ChunkArgs a{};
+  a.B = B; a.T = T; a.total_T = B * T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  return ws_size(a, dtype);
+}
+
+size_t kda_chunk_fwd_varlen_workspace_size(int N, int total_T, int H, int dk, int dv,
+                                           int chunk, int dtype) {
+  if (N < 0 || total_T < 0 || H <= 0) return 0;
+  static const int32_t marker = 0;  // only the presence of cu_seqlens matters here
+  kda::ChunkArgs a{};
+  a.cu_seqlens = &marker;
+  a.B = N; a.total_T = total_T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  return ws_size(a, dtype);
+}
+
+int kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const float* g,
+                     const float* beta_logits, const float* a_log, const float* dt_bias,
+                     float scale, float lower_bound, const float* initial_state, void* out,
+                     float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                     int dtype, void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+  kda::ChunkArgs a;
+  const int s = fill_fixed(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                           initial_state, out, final_state, B, T, H, dk, dv, chunk);
+  if (s != KDA_OK) return s;
+  return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream), workspace,
+                      workspace_bytes, true);
+}
+
+int kda_chunk_fwd_varlen_ws(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta_logits, const float* a_log,
+                            const float* dt_bias, float scale, float lower_bound,
+                            const int32_t* cu_seqlens, int N, int total_T,
+                            const float* initial_state, void* out, float* final_state, int H,
+                            int dk, int dv, int chunk, int dtype, void* workspace,
+                            size_t workspace_bytes, kda_stream_t stream) {
+  kda::ChunkArgs a;
+  const int s = fill_varlen(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                            cu_seqlens, N, total_T, initial_state, out, final_state, H, dk, dv,
+                            chunk);
+  if (s != KDA_OK) return s;
+  return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream), workspace,
+                      workspace_bytes, true);
 }
 
 int kda_decode_step(const float* q, const float* k, const float* v, const float* g,
@@ -141,6 +237,7 @@ const char* kda_status_string(int status) {
     case KDA_ERR_DEVICE: return "no usable CUDA device of compute capability 10.3";
     case KDA_ERR_SCALE: return "scale must be finite";
     case KDA_ERR_TOO_LARGE: return "problem too large for the kernels' index limits";
+    case KDA_ERR_WORKSPACE: return "workspace NULL, smaller than required or not 256-byte aligned";
     default: return "unknown kda status";
   }
 }
@@ -150,7 +247,8 @@ int kda_version(void) { return 100; }
 int kda_device_error(int reset) {
   int s = check_device();
   if (s != KDA_OK) return s;
-  return (int)(kda::chunk_tc_read_error(reset != 0) | kda::decode_read_error(reset != 0));
+  return (int)(kda::chunk_tc_read_error(reset != 0) | kda::chunk_split_read_error(reset != 0) |
+               kda::decode_read_error(reset != 0));
 }
 
 }  // extern "C"

@@ -1,0 +1,999 @@
+// Chunked KDA forward in two launches, for bf16 q/k/v with dk = dv = 128 and 64-token
+// chunks (kernel_delta_attention page, "Algorithm modes: chunked"; decay-first recurrence).
+//
+// Everything in a chunk except the state is independent of every other chunk.  The work
+// is therefore cut at the state:
+//
+//  chunk_prep_kernel   one CTA per (chunk, head), all chunks of all sequences at once (two
+//                      CTAs per SM).  Gate activation and in-chunk cumulative sum, beta, L2
+//                      norms, the gate-scaled products A and M (tcgen05, 16-token sub-chunk
+//                      reference points), the UT solve T = (I + diag(beta) tril(A,-1))^{-1}
+//                      diag(beta) and the transform W = T diag(rk) K~, U~ = T V (tcgen05).
+//                      It writes one workspace record per (chunk, head):
+//                        Q~   = q e^{G}                     [64 tok][128]  bf16
+//                        -W                                 [64 tok][128]  bf16
+//                        K^^T = (k e^{G_C - G})^T           [128][64 tok]  bf16
+//                        U~^T                               [128][64 tok]  bf16
+//                        M_raw (gate-scaled q k^T, s <= r)  [64][64]       bf16
+//                        e^{G_C} [128], rk [64], rq [64]                    fp32
+//  chunk_scan_kernel   one CTA per (sequence, head) walks its chunks in order, records
+//                      double-buffered through TMA, with only the state-dependent products:
+//                        U^T  = U~^T - S^T W^T,  O'^T = S^T Q~^T
+//                        O'^T += U'^T M_raw^T,   S^T <- S^T diag(e^{G_C}) + U'^T K^
+//                      (U' = diag(rk) U, O = diag(rq) O'; S^T lives in Tensor Memory in fp32,
+//                      with a bf16 copy as the A operand of the next chunk's products).
+//
+// The algebra is that of the single-pass kernel (kda_chunk_tc.cu); here the key side of
+// every chunk runs on all SMs at once instead of inside the per-sequence scan.
+#include <algorithm>
+
+#include "chunk_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+using namespace chunk;
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+
+// ---------------------------------------------------------------- workspace records
+
+constexpr long long kRecTile = 64LL * 128 * 2;  // one [64 x 128] (or [128 x 64]) bf16 tile
+constexpr long long kRecM = 64LL * 64 * 2;
+constexpr long long kRecVec = 256 * 4;          // e^{G_C}[128], rk[64], rq[64]
+
+struct Ws {
+  __nv_bfloat16* qw;   // [2 * recs * 64][128]: Q~ records, then -W records
+  __nv_bfloat16* ku;   // [2 * recs * 128][64]: K^^T records, then U~^T records
+  __nv_bfloat16* m;    // [recs * 64][64]
+  float* vec;          // [recs][256]
+  int32_t* coff;       // [N + 1] first chunk slot of each sequence (packed inputs only)
+  long long recs;      // chunk slots x heads
+  int nck_fixed;       // chunks per sequence (fixed-length inputs)
+};
+
+long long slots_for(const ChunkArgs& a) {
+  if (a.cu_seqlens) return (long long)a.total_T / kC + a.B;
+  return (long long)a.B * ((a.T + kC - 1) / kC);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------- prep kernel
+
+constexpr int kPThreads = 256;
+constexpr int kPKbRows = 160;  // 64 diagonal + 16 + 32 + 48 off-diagonal key rows
+// Dynamic shared memory of the prep kernel (1024-aligned base).
+constexpr int P_XL = 0;                 // Xl [128 x 128] bf16 (k rows, then q rows)
+constexpr int P_KB = P_XL + 32768;      // Kb [160 x 128]
+constexpr int P_KTT = P_KB + 40960;     // K~^T [128 x 64]
+constexpr int P_VT = P_KTT + 16384;     // V^T [128 x 64]
+constexpr int P_END = P_VT + 16384;
+// re-used inside Xl/Kb once MMA1 has completed
+constexpr int P_L = 0;                  // fp32 [64][LDL] beta-scaled strict lower A
+constexpr int P_X = P_L + 64 * LDL * 4; // fp32 [64][LDL] (I + L)^{-1}
+constexpr int P_Y = P_X + 64 * LDL * 4; // fp32 [4][16][LDY] per-warp scratch
+constexpr int P_T = 40960;              // T [64 x 64] bf16 SW128
+constexpr int P_TW = P_T + 8192;        // T diag(rk)
+constexpr int P_W = P_TW + 8192;        // -W [64 x 128] staging for the record store
+static_assert(P_Y + 4 * 16 * LDY * 4 <= P_T, "solve scratch overlaps T");
+static_assert(P_W + 16384 <= P_KTT, "re-used tiles must stay inside Xl/Kb");
+constexpr size_t kPSmem = P_END + 1024;
+
+// Tensor Memory of the prep kernel (256 columns: two CTAs per SM).
+constexpr uint32_t P_TM_D1 = 0;   // [A; M] accumulator, 160 columns
+constexpr uint32_t P_TM_DW = 0;   // W^T (after D1 is consumed), 64
+constexpr uint32_t P_TM_DU = 64;  // U~^T, 64
+constexpr uint32_t kPTmemCols = 256;
+
+__device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split path gave up
+
+__global__ void __launch_bounds__(kPThreads, 2)
+    chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qw, const ChunkArgs a,
+                      const Ws ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  __shared__ __align__(16) float s_rk[kC];
+  __shared__ __align__(16) float s_rq[kC];
+  __shared__ __align__(16) float s_beta[kC];
+  __shared__ __align__(16) float s_dec[kD];
+  __shared__ __align__(16) float s_gtot[4][kD];
+  __shared__ __align__(16) float s_qq[2][kC];
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_wait_ok[2];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int wg = tid >> 7;        // warpgroup (0, 1)
+  const int ln = tid & 127;       // TMEM lane
+  const int lane_base = 32 * (warp & 3);
+  // SIMT mapping: channel pair c0, c0 + 1 and the 16 tokens of sub-chunk R
+  const int cp = tid & 63, R = tid >> 6;
+  const int c0 = 2 * cp;
+  const int H = a.H;
+
+  // record -> (head, chunk slot) -> (sequence, chunk of the sequence); false past the
+  // last chunk of packed inputs (the record count is an upper bound there)
+  auto locate = [&](long long r, int& h_, long long& tok0_, int& n_) -> bool {
+    if (r >= ws.recs) return false;
+    h_ = (int)(r % H);
+    const long long slot = r / H;
+    int seq, jc;
+    if (a.cu_seqlens) {
+      const int N = a.B;
+      if (slot >= ws.coff[N]) return false;
+      int lo = 0, hi = N;  // coff[lo] <= slot < coff[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ws.coff[mid] <= slot) lo = mid; else hi = mid;
+      }
+      seq = lo;
+      jc = (int)(slot - ws.coff[lo]);
+    } else {
+      seq = (int)(slot / ws.nck_fixed);
+      jc = (int)(slot % ws.nck_fixed);
+    }
+    long long bos;
+    int len;
+    seq_range(a, seq, bos, len);
+    n_ = min(kC, len - jc * kC);  // live tokens of this chunk (>= 1)
+    tok0_ = bos + (long long)jc * kC;
+    return true;
+  };
+  // L2 prefetch of a record's q / k / v / g rows (thread t: tensor t / 64, token t % 64)
+  auto prefetch = [&](int h_, long long tok0_, int n_) {
+    const int t = tid & 63, which = tid >> 6;
+    if (t >= n_) return;
+    const long long row = (tok0_ + t) * H + h_;
+    if (which == 3)
+      prefetch_l2(a.g + row * kD, kD * 4);
+    else
+      prefetch_l2(static_cast<const __nv_bfloat16*>(which == 0 ? a.q : which == 1 ? a.k : a.v) +
+                      row * kD, kD * 2);
+  };
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kPTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t tl = tm + (uint32_t(lane_base) << 16);
+  uint32_t mma_phase = 0;
+  uint32_t wait_calls = 0;
+  auto mma_wait = [&]() -> bool {
+    const uint32_t slot_w = wait_calls++ & 1;
+    if (tid == 0) s_wait_ok[slot_w] = mbar_wait(&bar_mma, mma_phase & 1) ? 1 : 0;
+    ++mma_phase;
+    __syncthreads();
+    return s_wait_ok[slot_w] != 0;
+  };
+  bool ok = true;
+
+  int h, n, h_next = 0, n_next = 0;
+  long long tok0, tok0_next = 0;
+  bool have = locate(blockIdx.x, h, tok0, n);
+  for (long long rec = blockIdx.x; have; rec += gridDim.x) {
+    // the next record's rows start moving into L2 while this one is computed
+    const bool have_next = locate(rec + gridDim.x, h_next, tok0_next, n_next);
+    if (have_next) prefetch(h_next, tok0_next, n_next);
+
+    // ---- loads: raw gates, beta logit, v / k / q words of (16 tokens, channels c0, c0 + 1)
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
+    const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v);
+    float2 graw[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * R + i;
+      graw[i] = (t < n) ? *reinterpret_cast<const float2*>(a.g + ((tok0 + t) * H + h) * kD + c0)
+                        : make_float2(0.f, 0.f);
+    }
+    const float blog = (tid < n) ? a.beta_logits[(tok0 + tid) * H + h] : 0.f;  // tid < 64 only
+    uint32_t vw[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * R + i;
+      vw[i] = (t < n) ? *reinterpret_cast<const uint32_t*>(vg + ((tok0 + t) * H + h) * kD + c0)
+                      : 0u;
+    }
+
+    // V^T tile (rows = channels, tokens contiguous): row c0 takes the low halves, row c0 + 1
+    // the high halves; lanes 4..7 of every 8-lane group write row c0 + 1 first so that one
+    // 128-bit wavefront covers 8 swizzle phases.
+    const int tsw = (lane & 4) ? 1 : 0;
+    auto store_t8 = [&](int off, const uint32_t* w8, int g8) {
+      const uint4 lo = make_uint4(__byte_perm(w8[0], w8[1], 0x5410), __byte_perm(w8[2], w8[3], 0x5410),
+                                  __byte_perm(w8[4], w8[5], 0x5410), __byte_perm(w8[6], w8[7], 0x5410));
+      const uint4 hi = make_uint4(__byte_perm(w8[0], w8[1], 0x7632), __byte_perm(w8[2], w8[3], 0x7632),
+                                  __byte_perm(w8[4], w8[5], 0x7632), __byte_perm(w8[6], w8[7], 0x7632));
+      *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + tsw, g8)) = tsw ? hi : lo;
+      *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + 1 - tsw, g8)) = tsw ? lo : hi;
+    };
+    store_t8(P_VT, vw, 2 * R);
+    store_t8(P_VT, vw + 8, 2 * R + 1);
+
+    uint32_t kw[16], qw[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * R + i;
+      const long long off = ((tok0 + t) * H + h) * kD + c0;
+      kw[i] = (t < n) ? *reinterpret_cast<const uint32_t*>(kg + off) : 0u;
+      qw[i] = (t < n) ? *reinterpret_cast<const uint32_t*>(qg + off) : 0u;
+    }
+
+    // ---- gate prefix over this thread's sub-chunk, beta
+    const float exp_a = __expf(a.a_log[h]);
+    const float db0 = a.dt_bias[c0 * H + h], db1 = a.dt_bias[(c0 + 1) * H + h];
+    float loc0[16], loc1[16];  // G_t - P_R for channels c0, c0 + 1
+    {
+      float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float g0 = 0.f, g1 = 0.f;
+        if (16 * R + i < n) {
+          g0 = a.lower_bound * fast_rcp(1.f + fast_exp(-exp_a * (graw[i].x + db0)));
+          g1 = a.lower_bound * fast_rcp(1.f + fast_exp(-exp_a * (graw[i].y + db1)));
+        }
+        r0 += g0;
+        r1 += g1;
+        loc0[i] = r0;
+        loc1[i] = r1;
+      }
+      *reinterpret_cast<float2*>(&s_gtot[R][c0]) = make_float2(r0, r1);
+    }
+    if (tid < kC) s_beta[tid] = (tid < n) ? sigmoidf_(blog) : 0.f;
+
+    // ---- |q_t|^2: this thread's two channels, then a reduce-scatter over the warp's 32
+    //      channel pairs (lanes l and l ^ 1 end with the same token); two warps per token.
+    {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float x = bf16_lo(qw[i]), y = bf16_hi(qw[i]);
+        v[i] = x * x + y * y;
+      }
+#pragma unroll
+      for (int half = 8, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+        const bool up = (lane & bit) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float send = up ? v[i] : v[i + half];
+          const float keep = up ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      const int tq = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 +
+                     ((lane >> 1) & 1);
+      if ((lane & 1) == 0) s_qq[warp & 1][16 * R + tq] = v[0];
+    }
+    // the previous record's -W store has read its staging tile (inside Kb) before Kb is
+    // rewritten below
+    if (tid == 0) bulk_wait_read_all();
+    __syncthreads();
+
+    // ---- gate-scaled operands of (channels c0, c0 + 1) x (tokens 16 R .. 16 R + 15)
+    {
+      float P0[4], P1[4];  // P_R: G just before sub-chunk R
+      P0[0] = 0.f;
+      P1[0] = 0.f;
+#pragma unroll
+      for (int r = 1; r < 4; ++r) {
+        const float2 t2 = *reinterpret_cast<const float2*>(&s_gtot[r - 1][c0]);
+        P0[r] = P0[r - 1] + t2.x;
+        P1[r] = P1[r - 1] + t2.y;
+      }
+      const float2 t3 = *reinterpret_cast<const float2*>(&s_gtot[3][c0]);
+      const float Gc0 = P0[3] + t3.x, Gc1 = P1[3] + t3.y;
+      float Pm0 = P0[0], Pm1 = P1[0];
+#pragma unroll
+      for (int r = 1; r < 4; ++r)
+        if (R == r) { Pm0 = P0[r]; Pm1 = P1[r]; }
+      const float eP0 = fast_exp(Pm0), eP1 = fast_exp(Pm1);                // e^{P_R}
+      const float eCP0 = fast_exp(Gc0 - Pm0), eCP1 = fast_exp(Gc1 - Pm1);  // e^{G_C - P_R}
+      float cR0[4], cR1[4];  // e^{P_R' - P_R} for later sub-chunks R'
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        cR0[r] = (r > R) ? fast_exp(P0[r] - Pm0) : 0.f;
+        cR1[r] = (r > R) ? fast_exp(P1[r] - Pm1) : 0.f;
+      }
+      if (R == 0) *reinterpret_cast<float2*>(&s_dec[c0]) = make_float2(fast_exp(Gc0), fast_exp(Gc1));
+
+      const uint32_t eP2 = pack_bf16(eP0, eP1), eCP2 = pack_bf16(eCP0, eCP1);
+      const uint32_t c12 = pack_bf16(cR0[1], cR1[1]), c22 = pack_bf16(cR0[2], cR1[2]),
+                     c32 = pack_bf16(cR0[3], cR1[3]);
+      // element (row 16 R + i, channel c0) of a K-major SW128 tile with `rows` rows:
+      //   (c0 / 64) * rows * 128 + 2 R * 1024 + sw[i]
+      const uint32_t c_kb = uint32_t(c0 >> 6);
+      const uint32_t c_chunk = uint32_t(((c0 & 63) * 2) >> 4);
+      const uint32_t c_byte = uint32_t(((c0 & 63) * 2) & 15);
+      uint8_t* const p128 = sm + P_XL + c_kb * 16384u + uint32_t(R) * 2048u;
+      uint8_t* const p160 = sm + P_KB + c_kb * 20480u + uint32_t(R) * 2048u;
+      __nv_bfloat16* const qrec = ws.qw + (rec * 64 + 16 * R) * kD + c0;  // Q~ row 16 R
+      __nv_bfloat16* const krec = ws.ku + rec * 128 * 64;                  // K^^T record
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t khw[8], ktw[8];
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+          const int i = 8 * hf + ii;
+          const uint32_t swi = uint32_t(hf * 1024 + ii * 128) +
+                               (((c_chunk ^ uint32_t(ii)) << 4) | c_byte);
+          const float e0 = fast_exp(loc0[i]), e1 = fast_exp(loc1[i]);  // e^{G_t - P_R}
+          const uint32_t e2 = pack_bf16(e0, e1);
+          const uint32_t i2 = pack_bf16(fast_rcp(e0), fast_rcp(e1));  // e^{P_R - G_t}
+          const uint32_t xk = hmul2(kw[i], e2), xq = hmul2(qw[i], e2), kd = hmul2(kw[i], i2);
+          *reinterpret_cast<uint32_t*>(p128 + swi) = xk;             // Xl row t
+          *reinterpret_cast<uint32_t*>(p128 + swi + 8 * 1024) = xq;  // Xl row 64 + t
+          *reinterpret_cast<uint32_t*>(p160 + swi) = kd;             // Kb diagonal row t
+          if (R < 1) *reinterpret_cast<uint32_t*>(p160 + swi + 8 * 1024) = hmul2(kd, c12);
+          if (R < 2) *reinterpret_cast<uint32_t*>(p160 + swi + 10 * 1024) = hmul2(kd, c22);
+          if (R < 3) *reinterpret_cast<uint32_t*>(p160 + swi + 14 * 1024) = hmul2(kd, c32);
+          *reinterpret_cast<uint32_t*>(qrec + i * kD) = hmul2(xq, eP2);  // q e^{G_t}
+          khw[ii] = hmul2(kd, eCP2);  // k e^{G_C - G_t}
+          ktw[ii] = hmul2(xk, eP2);   // k e^{G_t}
+        }
+        store_t8(P_KTT, ktw, 2 * R + hf);
+        // K^^T record rows c0, c0 + 1, tokens 16 R + 8 hf .. + 7
+        const uint4 lo = make_uint4(__byte_perm(khw[0], khw[1], 0x5410), __byte_perm(khw[2], khw[3], 0x5410),
+                                    __byte_perm(khw[4], khw[5], 0x5410), __byte_perm(khw[6], khw[7], 0x5410));
+        const uint4 hi = make_uint4(__byte_perm(khw[0], khw[1], 0x7632), __byte_perm(khw[2], khw[3], 0x7632),
+                                    __byte_perm(khw[4], khw[5], 0x7632), __byte_perm(khw[6], khw[7], 0x7632));
+        *reinterpret_cast<uint4*>(krec + c0 * 64 + 16 * R + 8 * hf) = lo;
+        *reinterpret_cast<uint4*>(krec + (c0 + 1) * 64 + 16 * R + 8 * hf) = hi;
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA1: [A; M] = Xl Kb^T  (M = 128, N = 160, K = 128)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t xa = smem_u32(sm + P_XL), kb = smem_u32(sm + P_KB);
+      const uint32_t idesc = make_idesc(1, 128, kPKbRows);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        mma_ss(tm + P_TM_D1, sw128_kdesc<2>(xa, 128, s), sw128_kdesc<2>(kb, kPKbRows, s), idesc,
+               s > 0);
+      mma_commit(&bar_mma);
+    }
+    if (!(ok = mma_wait())) break;
+    tc_fence_after();
+
+    // ---- norms: |k_r|^2 = A_raw[r][r] (diagonal of D1); |q_r|^2 from the reduction
+    if (warp < 2) {
+      float v32[32];
+      tmem_ld32(tl + P_TM_D1 + 32 * warp, v32);
+      float nn = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) nn = (i == lane) ? v32[i] : nn;
+      const int r = 32 * warp + lane;
+      s_rk[r] = (r < n) ? rsqrtf(nn + kL2Eps) : 0.f;
+    } else if (warp < 4) {
+      const int r = tid - 64;
+      s_rq[r] = (r < n) ? a.scale * rsqrtf(s_qq[0][r] + s_qq[1][r] + kL2Eps) : 0.f;
+    }
+    __syncthreads();
+    // vector record: e^{G_C}, rk, rq
+    ws.vec[rec * 256 + tid] = tid < 128 ? s_dec[tid] : tid < 192 ? s_rk[tid - 128] : s_rq[tid - 192];
+
+    // ---- read A (TMEM lanes 0..63) and M (lanes 64..127); warpgroup wg takes the column
+    //      quarters q = wg, wg + 2.  Every tcgen05.ld address is warp-uniform.
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      const int q = wg + 2 * qq;
+      const int r = ln & 63, Rr = r >> 4;
+      const int Rlo = 2 * ((warp & 3) & 1);  // the two row quarters this warp's lanes span
+      float v[16];
+      {
+        float d16[16];
+        tmem_ld16(tl + P_TM_D1 + 16 * q, d16);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) v[m] = (Rr == q) ? d16[m] : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int Rp = Rlo + e;
+        if (q < Rp) {  // warp-uniform
+          const int offR = (Rp == 1) ? 64 : (Rp == 2) ? 80 : 112;
+          float d16[16];
+          tmem_ld16(tl + P_TM_D1 + offR + 16 * q, d16);
+#pragma unroll
+          for (int m = 0; m < 16; ++m) v[m] = (Rr == Rp) ? d16[m] : v[m];
+        }
+      }
+      if (ln < 64) {
+        const float sr = s_beta[r] * s_rk[r];
+        float* L = reinterpret_cast<float*>(sm + P_L) + r * LDL + 16 * q;
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          const float4 rk4 = *reinterpret_cast<const float4*>(&s_rk[16 * q + 4 * m4]);
+          float4 o;
+          o.x = (16 * q + 4 * m4 + 0 < r) ? sr * rk4.x * v[4 * m4 + 0] : 0.f;
+          o.y = (16 * q + 4 * m4 + 1 < r) ? sr * rk4.y * v[4 * m4 + 1] : 0.f;
+          o.z = (16 * q + 4 * m4 + 2 < r) ? sr * rk4.z * v[4 * m4 + 2] : 0.f;
+          o.w = (16 * q + 4 * m4 + 3 < r) ? sr * rk4.w * v[4 * m4 + 3] : 0.f;
+          reinterpret_cast<float4*>(L)[m4] = o;
+        }
+      } else {
+        uint32_t pk[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int s0 = 16 * q + 2 * p;
+          pk[p] = pack_bf16((s0 <= r) ? v[2 * p] : 0.f, (s0 + 1 <= r) ? v[2 * p + 1] : 0.f);
+        }
+        uint4* mrec = reinterpret_cast<uint4*>(ws.m + (rec * 64 + r) * 64 + 16 * q);
+        mrec[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        mrec[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+    __syncthreads();
+
+    // ---- T = (I + L)^{-1} diag(beta), blocked by 16
+    {
+      const float* L = reinterpret_cast<const float*>(sm + P_L);
+      float* X = reinterpret_cast<float*>(sm + P_X);
+      if (warp < 4 && lane < 16) {
+        const int b0 = 16 * warp, s = lane;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int m4 = 0; m4 < r; m4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(L + (b0 + r) * LDL + b0 + m4);
+            if (m4 + 0 < r) acc0 += l4.x * x[m4 + 0];
+            if (m4 + 1 < r) acc1 += l4.y * x[m4 + 1];
+            if (m4 + 2 < r) acc0 += l4.z * x[m4 + 2];
+            if (m4 + 3 < r) acc1 += l4.w * x[m4 + 3];
+          }
+          x[r] = (r == s) ? 1.f : -(acc0 + acc1);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) X[(b0 + r) * LDL + b0 + s] = x[r];
+      }
+      __syncthreads();
+      solve_level<1>(L, X, reinterpret_cast<float*>(sm + P_Y), warp, lane);
+      __syncthreads();
+      solve_level<2>(L, X, reinterpret_cast<float*>(sm + P_Y), warp, lane);
+      __syncthreads();
+      solve_level<3>(L, X, reinterpret_cast<float*>(sm + P_Y), warp, lane);
+      __syncthreads();
+      // T[r][s] = X[r][s] beta_s and T diag(rk) (s <= r): row r, 8 columns per thread
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int r = (tid >> 3) + 32 * it, s0 = (tid & 7) * 8;
+        const float4 xa = *reinterpret_cast<const float4*>(X + r * LDL + s0);
+        const float4 xb = *reinterpret_cast<const float4*>(X + r * LDL + s0 + 4);
+        const float4 ba = *reinterpret_cast<const float4*>(&s_beta[s0]);
+        const float4 bb = *reinterpret_cast<const float4*>(&s_beta[s0 + 4]);
+        const float4 ka = *reinterpret_cast<const float4*>(&s_rk[s0]);
+        const float4 kb = *reinterpret_cast<const float4*>(&s_rk[s0 + 4]);
+        const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+        const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+        const float kv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+        uint32_t pt[4], pw[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float t0v = (s0 + 2 * p <= r) ? xv[2 * p] * bv[2 * p] : 0.f;
+          const float t1v = (s0 + 2 * p + 1 <= r) ? xv[2 * p + 1] * bv[2 * p + 1] : 0.f;
+          pt[p] = pack_bf16(t0v, t1v);
+          pw[p] = pack_bf16(t0v * kv[2 * p], t1v * kv[2 * p + 1]);
+        }
+        const uint32_t off = sw128_offset<2>(64, r, s0);
+        *reinterpret_cast<uint4*>(sm + P_T + off) = make_uint4(pt[0], pt[1], pt[2], pt[3]);
+        *reinterpret_cast<uint4*>(sm + P_TW + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA2: W^T = K~^T (T diag(rk))^T, U~^T = V^T T^T  (M = 128, N = 64, K = 64)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t ts = smem_u32(sm + P_T), tw = smem_u32(sm + P_TW),
+                     ks = smem_u32(sm + P_KTT), vs = smem_u32(sm + P_VT);
+      const uint32_t idesc = make_idesc(1, 128, 64);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        mma_ss(tm + P_TM_DW, sw128_kdesc<2>(ks, 128, s), sw128_kdesc<2>(tw, 64, s), idesc, s > 0);
+        mma_ss(tm + P_TM_DU, sw128_kdesc<2>(vs, 128, s), sw128_kdesc<2>(ts, 64, s), idesc, s > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    if (!(ok = mma_wait())) break;
+    tc_fence_after();
+
+    // ---- records: -W (through a swizzled staging tile and one bulk-tensor store) and U~^T
+    //      (thread j = ln writes its own row); thread (ln, wg) holds tokens 32 wg .. + 31
+    {
+      float w32[32];
+      tmem_ld32(tl + P_TM_DW + 32 * wg, w32);
+      const uint32_t wkb = uint32_t(ln >> 6) * 8192u, wch = uint32_t(((ln & 63) * 2) >> 4),
+                     wby = uint32_t(((ln & 63) * 2) & 15);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = 32 * wg + i;
+        const uint32_t off = wkb + uint32_t((r >> 3) * 1024 + (i & 7) * 128) +
+                             (((wch ^ uint32_t(i & 7)) << 4) | wby);
+        *reinterpret_cast<__nv_bfloat16*>(sm + P_W + off) = __float2bfloat16_rn(-w32[i]);
+      }
+      float u32[32];
+      tmem_ld32(tl + P_TM_DU + 32 * wg, u32);
+      uint4* urec = reinterpret_cast<uint4*>(ws.ku + ((ws.recs + rec) * 128 + ln) * 64 + 32 * wg);
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        urec[p] = make_uint4(pack_bf16(u32[8 * p + 0], u32[8 * p + 1]),
+                             pack_bf16(u32[8 * p + 2], u32[8 * p + 3]),
+                             pack_bf16(u32[8 * p + 4], u32[8 * p + 5]),
+                             pack_bf16(u32[8 * p + 6], u32[8 * p + 7]));
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      const int row = (int)((ws.recs + rec) * 64);
+      tma_store_2d(&map_qw, sm + P_W, 0, row);
+      tma_store_2d(&map_qw, sm + P_W + 8192, 64, row);
+      bulk_commit();
+    }
+    h = h_next;
+    tok0 = tok0_next;
+    n = n_next;
+    have = have_next;
+  }
+
+  if (!ok) {
+    if (tid == 0) atomicOr(&g_split_error, 2u);
+    mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
+  }
+  if (tid == 0) bulk_wait_read_all();  // the last staging tile is read before exit
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, kPTmemCols);
+}
+
+// ------------------------------------------------------------------- scan kernel
+
+constexpr int kSThreads = 512;
+// one stage = one chunk's record
+constexpr int S_Q = 0;          // Q~ [64 x 128] (two 64-channel boxes)
+constexpr int S_W = 16384;      // -W [64 x 128]
+constexpr int S_KT = 32768;     // K^^T [128 x 64]
+constexpr int S_UT = 49152;     // U~^T [128 x 64]
+constexpr int S_M = 65536;      // M_raw [64 x 64]
+constexpr int S_V = 73728;      // e^{G_C}, rk, rq
+constexpr int kStage = 74752;
+constexpr uint32_t kStageTx = 74752;
+constexpr int S_OS = 2 * kStage;  // output staging [64 tok x 128] bf16 SW128
+constexpr int S_END = S_OS + 16384;
+static_assert(kStage % 1024 == 0 && S_OS % 1024 == 0, "alignment");
+constexpr size_t kSSmem = S_END + 1024;
+
+constexpr uint32_t S_TM_DU = 0;    // S^T (-W)^T, 64
+constexpr uint32_t S_TM_DO = 64;   // O'^T, 64
+constexpr uint32_t S_TM_S = 128;   // fp32 master state S^T, 128
+constexpr uint32_t S_TM_SA = 256;  // bf16 copy of S^T (A operand), 64
+constexpr uint32_t S_TM_UA = 320;  // U'^T A operand (bf16 pairs), 32
+constexpr uint32_t kSTmemCols = 512;
+
+__global__ void __launch_bounds__(kSThreads, 1)
+    chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qw,
+                      const __grid_constant__ CUtensorMap map_ku,
+                      const __grid_constant__ CUtensorMap map_m,
+                      const __grid_constant__ CUtensorMap map_o, const ChunkArgs a,
+                      const Ws ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld[2], bar_mma;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_wait_ok[2];
+  __shared__ __align__(16) float s_vec[256];  // this chunk's e^{G_C}, rk, rq
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int wg = tid >> 7;
+  const int ln = tid & 127;
+  const int lane_base = 32 * (warp & 3);
+  const int h = blockIdx.x, seq = blockIdx.y;
+  const int H = a.H;
+  long long bos;
+  int len;
+  seq_range(a, seq, bos, len);
+  long long slot0;
+  int nck;
+  if (a.cu_seqlens) {
+    slot0 = ws.coff[seq];
+    nck = ws.coff[seq + 1] - ws.coff[seq];
+  } else {
+    slot0 = (long long)seq * ws.nck_fixed;
+    nck = ws.nck_fixed;
+  }
+  const long long state_off = ((long long)seq * H + h) * kD * kD;
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kSTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_ld[0], 1);
+    mbar_init(&bar_ld[1], 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&map_qw);
+    tma_prefetch_desc(&map_ku);
+    tma_prefetch_desc(&map_m);
+    tma_prefetch_desc(&map_o);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t tl = tm + (uint32_t(lane_base) << 16);
+
+  // one chunk record into stage st
+  auto issue_load = [&](int ch, int st) {
+    const long long rec = (slot0 + ch) * H + h;
+    uint8_t* b = sm + st * kStage;
+    uint64_t* bar = &bar_ld[st];
+    mbar_arrive_expect_tx(bar, kStageTx);
+    const int rq = (int)(rec * 64), rw = (int)((ws.recs + rec) * 64);
+    tma_load_2d(b + S_Q, &map_qw, bar, 0, rq);
+    tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, rq);
+    tma_load_2d(b + S_W, &map_qw, bar, 0, rw);
+    tma_load_2d(b + S_W + 8192, &map_qw, bar, 64, rw);
+    tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128));
+    tma_load_2d(b + S_UT, &map_ku, bar, 0, (int)((ws.recs + rec) * 128));
+    tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64));
+    bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar);
+  };
+  // chunk whose record is in flight into each stage (-1: none); same on every thread
+  int inflight[2] = {nck > 0 ? 0 : -1, nck > 1 ? 1 : -1};
+  if (tid == 0) {
+    if (nck > 0) issue_load(0, 0);
+    if (nck > 1) issue_load(1, 1);
+  }
+
+  // Initial state: thread (j = ln, warpgroup wg) owns S^T[j][32 wg .. 32 wg + 31].
+  {
+    float S[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int c = 32 * wg + i;
+      S[i] = a.initial_state ? a.initial_state[state_off + (long long)c * kD + ln] : 0.f;
+    }
+    tmem_st32(tl + S_TM_S + 32 * wg, S);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
+    tmem_st16(tl + S_TM_SA + 16 * wg, w);
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  const uint32_t idesc_n64 = make_idesc(1, 128, 64);
+  const uint32_t idesc_n128 = make_idesc(1, 128, 128);
+  uint32_t mma_phase = 0;
+  uint32_t wait_calls = 0;
+  auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const uint32_t slot_w = wait_calls++ & 1;
+    if (tid == 0) s_wait_ok[slot_w] = mbar_wait(bar, parity) ? 1 : 0;
+    __syncthreads();
+    return s_wait_ok[slot_w] != 0;
+  };
+  auto mma_wait = [&]() -> bool {
+    const bool w = block_wait(&bar_mma, mma_phase & 1);
+    ++mma_phase;
+    return w;
+  };
+  bool ok = true;
+
+  for (int ch = 0; ch < nck; ++ch) {
+    const int st = ch & 1;
+    uint8_t* const b = sm + st * kStage;
+    const float* const vec = s_vec;
+    const int n = min(kC, len - ch * kC);
+    const long long tok0 = bos + (long long)ch * kC;
+
+    if (!(ok = block_wait(&bar_ld[st], (ch >> 1) & 1))) break;
+    inflight[st] = -1;
+    // the stage's vectors move to static shared memory so that the stage can be refilled
+    // as soon as the tensor cores are done with it (the previous chunk's readers of s_vec
+    // are past the barrier inside block_wait)
+    if (tid < 256) s_vec[tid] = reinterpret_cast<const float*>(b + S_V)[tid];
+    __syncthreads();
+
+    // ---- MMA3: D_U = S^T (-W)^T, O'^T = S^T Q~^T  (M = 128, N = 64, K = 128)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t ws_ = smem_u32(b + S_W), qs = smem_u32(b + S_Q);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        mma_ts(tm + S_TM_DU, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(ws_, 64, s), idesc_n64, s > 0);
+        mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
+      }
+      mma_commit(&bar_mma);
+    }
+    // meanwhile: decay the fp32 master state in place (S^T diag(e^{G_C}))
+    {
+      float S[32];
+      tmem_ld32(tl + S_TM_S + 32 * wg, S);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) S[i] *= vec[32 * wg + i];
+      tmem_st32(tl + S_TM_S + 32 * wg, S);
+    }
+    if (!(ok = mma_wait())) break;
+    tc_fence_after();
+    // ---- U'^T = diag(rk) (U~ + D_U) -> bf16 A operand: thread (j = ln, tokens 16 wg .. + 15)
+    {
+      float v16[16];
+      tmem_ld16(tl + S_TM_DU + 16 * wg, v16);
+      const uint8_t* urow = b + S_UT + (ln >> 3) * 1024 + (ln & 7) * 128;
+      const uint4 ua = *reinterpret_cast<const uint4*>(urow + (((2 * wg) ^ (ln & 7)) << 4));
+      const uint4 ub = *reinterpret_cast<const uint4*>(urow + (((2 * wg + 1) ^ (ln & 7)) << 4));
+      const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+      uint32_t up[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        up[i] = pack_bf16((bf16_lo(uw[i]) + v16[2 * i]) * vec[128 + 16 * wg + 2 * i],
+                          (bf16_hi(uw[i]) + v16[2 * i + 1]) * vec[128 + 16 * wg + 2 * i + 1]);
+      tmem_st8(tl + S_TM_UA + 8 * wg, up);
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- MMA4: O'^T += U'^T M_raw^T, S^T += U'^T K^
+    if (tid == 0) {
+      bulk_wait_read_all();  // the previous chunk's output store has read its staging tile
+      tc_fence_after();
+      const uint32_t ms = smem_u32(b + S_M), ks = smem_u32(b + S_KT);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        mma_ts(tm + S_TM_DO, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ms, 64, s), idesc_n64, 1);
+        mma_ts(tm + S_TM_S, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ks, 128, s), idesc_n128, 1);
+      }
+      mma_commit(&bar_mma);
+    }
+    if (!(ok = mma_wait())) break;
+    tc_fence_after();
+    // the stage is consumed (its last readers were MMA4 and the U' pack): refill it
+    if (tid == 0 && ch + 2 < nck) issue_load(ch + 2, st);
+    inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
+    // ---- bf16 copy of the new state and the output O = diag(rq) O'
+    {
+      float S[32];
+      tmem_ld32(tl + S_TM_S + 32 * wg, S);
+      uint32_t sp[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sp[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
+      tmem_st16(tl + S_TM_SA + 16 * wg, sp);
+      float o16[16];
+      tmem_ld16(tl + S_TM_DO + 16 * wg, o16);
+      if (n == kC) {
+        const uint32_t ob = uint32_t(ln >> 6) * 8192u + uint32_t(wg) * 2048u;
+        const uint32_t och = uint32_t(((ln & 63) * 2) >> 4), oby = uint32_t(((ln & 63) * 2) & 15);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t off = ob + uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
+                               (((och ^ uint32_t(i & 7)) << 4) | oby);
+          *reinterpret_cast<__nv_bfloat16*>(sm + S_OS + off) =
+              __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+        }
+      } else {
+        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
+                            ((tok0 + 16 * wg) * H + h) * kD + ln;
+        const long long stride = (long long)H * kD;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (16 * wg + i < n) op[i * stride] = __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      if (n == kC) {
+        tma_store_3d(&map_o, sm + S_OS, 0, h, (int)tok0);
+        tma_store_3d(&map_o, sm + S_OS + 8192, 64, h, (int)tok0);
+        bulk_commit();
+      }
+    }
+    // ---- end of chunk
+  }
+
+  if (!ok) {
+    if (tid == 0) {
+      atomicOr(&g_split_error, 2u);
+      // records still in flight land before the shared memory is released
+      for (int st = 0; st < 2; ++st)
+        if (inflight[st] >= 0) mbar_wait(&bar_ld[st], (inflight[st] >> 1) & 1, 1000000000ull);
+    }
+    mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
+  } else if (a.final_state) {
+    tc_fence_after();
+    float S[32];
+    tmem_ld32(tl + S_TM_S + 32 * wg, S);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int c = 32 * wg + i;
+      a.final_state[state_off + (long long)c * kD + ln] = S[i];
+    }
+  }
+  if (tid == 0) bulk_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, kSTmemCols);
+}
+
+// ------------------------------------------------------------ varlen chunk offsets
+
+// coff[0] = 0, coff[i + 1] = coff[i] + ceil(len_i / 64) (lengths clamped as seq_range does).
+__global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int N,
+                                                             int total_T, int32_t* coff) {
+  __shared__ int s_warp[32];
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_carry = 0;
+    coff[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < N; base += 1024) {
+    const int i = base + tid;
+    int c = 0;
+    if (i < N) {
+      int lo = cu[i], hi = cu[i + 1];
+      lo = min(max(lo, 0), total_T);
+      hi = min(max(hi, lo), total_T);
+      c = (hi - lo + kC - 1) / kC;
+    }
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_warp[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int carry = s_carry;
+    const int incl = x + (warp > 0 ? s_warp[warp - 1] : 0);
+    if (i < N) coff[i + 1] = carry + incl;
+    __syncthreads();
+    if (tid == 1023) s_carry = carry + incl;
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------------- host
+
+bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int inner, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// [rows, H, 128] bf16 output, box {64 ch, 1 head, 64 tokens}, 128-byte swizzle.
+bool make_map_out(CUtensorMap* m, const void* base, long long rows, int H) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+bool carve(const ChunkArgs& a, void* base, Ws& ws) {
+  const long long slots = slots_for(a);
+  const long long recs = slots * a.H;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  ws.recs = recs;
+  ws.nck_fixed = a.cu_seqlens ? 0 : (a.T + kC - 1) / kC;
+  ws.qw = reinterpret_cast<__nv_bfloat16*>(p);
+  p += 2 * recs * kRecTile;
+  ws.ku = reinterpret_cast<__nv_bfloat16*>(p);
+  p += 2 * recs * kRecTile;
+  ws.m = reinterpret_cast<__nv_bfloat16*>(p);
+  p += recs * kRecM;
+  ws.vec = reinterpret_cast<float*>(p);
+  p += recs * kRecVec;
+  ws.coff = reinterpret_cast<int32_t*>(p);
+  return true;
+}
+
+}  // namespace
+
+size_t chunk_split_workspace(const ChunkArgs& a) {
+  const long long recs = slots_for(a) * a.H;
+  const size_t coff = a.cu_seqlens ? align_up(size_t(a.B + 1) * 4, 256) : 0;
+  return size_t(recs) * size_t(4 * kRecTile + kRecM + kRecVec) + coff;
+}
+
+bool chunk_split_index_ok(const ChunkArgs& a) {
+  // TMA row coordinates of the records are 32-bit: 2 * recs * 128 < 2^31
+  return slots_for(a) * a.H * 256 < 0x7fffffffLL;
+}
+
+cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t st) {
+  Ws ws{};
+  carve(a, workspace, ws);
+  const long long rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
+  const long long map_rows = rows > 0 ? rows : 1;
+  const long long rec_rows = ws.recs > 0 ? ws.recs : 1;
+  CUtensorMap mqw, mku, mm, mo;
+  if (!make_map_2d(&mqw, ws.qw, 2 * rec_rows * 64, 128, 64) ||
+      !make_map_2d(&mku, ws.ku, 2 * rec_rows * 128, 64, 128) ||
+      !make_map_2d(&mm, ws.m, rec_rows * 64, 64, 64) ||
+      !make_map_out(&mo, a.out, map_rows, a.H))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSSmem);
+  if (e != cudaSuccess) return e;
+  if (a.cu_seqlens) {
+    chunk_offsets_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.B, a.total_T, ws.coff);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (ws.recs > 0) {
+    // persistent: two CTAs per SM (shared memory and Tensor Memory admit no more)
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    const long long grid = std::min<long long>(ws.recs, 2LL * sms);
+    chunk_prep_kernel<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mqw, a, ws);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  chunk_scan_kernel<<<dim3(a.H, a.B), kSThreads, kSSmem, st>>>(mqw, mku, mm, mo, a, ws);
+  return cudaGetLastError();
+}
+
+unsigned int chunk_split_read_error(bool reset) {
+  unsigned int v = 0;
+  cudaMemcpyFromSymbol(&v, g_split_error, sizeof(v));
+  if (reset) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_split_error, &z, sizeof(z));
+  }
+  return v;
+}
+
+}  // namespace kda

@@ -58,6 +58,12 @@ cudaError_t launch_chunk_simt(const ChunkArgs& a, bool bf16, cudaStream_t stream
 bool chunk_tc_supported(const ChunkArgs& a, bool bf16);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 unsigned int chunk_tc_read_error(bool reset);
+// Two-launch tensor-core path (same configurations as chunk_tc_supported): per-chunk
+// prep over all chunks at once, then the sequential state pass, through a workspace.
+size_t chunk_split_workspace(const ChunkArgs& a);
+bool chunk_split_index_ok(const ChunkArgs& a);
+cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t stream);
+unsigned int chunk_split_read_error(bool reset);
 
 // Device helpers ------------------------------------------------------------------
 

@@ -20,11 +20,12 @@ STATUS_NAMES = {
     0: "KDA_OK", -1: "KDA_ERR_NULL_POINTER", -2: "KDA_ERR_BAD_SHAPE", -3: "KDA_ERR_HEAD_DIM",
     -4: "KDA_ERR_CHUNK", -5: "KDA_ERR_LOWER_BOUND", -6: "KDA_ERR_MISALIGNED",
     -7: "KDA_ERR_DTYPE", -8: "KDA_ERR_LAUNCH", -9: "KDA_ERR_DEVICE", -10: "KDA_ERR_SCALE",
-    -11: "KDA_ERR_TOO_LARGE",
+    -11: "KDA_ERR_TOO_LARGE", -12: "KDA_ERR_WORKSPACE",
 }
 # Exported symbols, in declaration order of include/kda.h.
-EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_decode_step", "kda_status_string",
-           "kda_version", "kda_device_error")
+EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_size",
+           "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
+           "kda_decode_step", "kda_status_string", "kda_version", "kda_device_error")
 
 
 class KDAError(RuntimeError):
@@ -38,6 +39,7 @@ _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
+_Z = ctypes.c_size_t
 
 
 def lib(path: str | None = None) -> ctypes.CDLL:
@@ -54,11 +56,17 @@ def lib(path: str | None = None) -> ctypes.CDLL:
                                 _I, _I, _I, _I, _I, _I, _I, _P]
     L.kda_chunk_fwd_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _I, _I,
                                        _P, _P, _P, _I, _I, _I, _I, _I, _P]
+    L.kda_chunk_fwd_workspace_size.argtypes = [_I] * 7
+    L.kda_chunk_fwd_varlen_workspace_size.argtypes = [_I] * 7
+    L.kda_chunk_fwd_workspace_size.restype = _Z
+    L.kda_chunk_fwd_varlen_workspace_size.restype = _Z
+    L.kda_chunk_fwd_ws.argtypes = L.kda_chunk_fwd.argtypes[:-1] + [_P, _Z, _P]
+    L.kda_chunk_fwd_varlen_ws.argtypes = L.kda_chunk_fwd_varlen.argtypes[:-1] + [_P, _Z, _P]
     L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
                                   _I, _I, _I, _I, _P]
     L.kda_device_error.argtypes = [_I]
-    for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_decode_step", "kda_version",
-              "kda_device_error"):
+    for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
+              "kda_chunk_fwd_varlen_ws", "kda_decode_step", "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
     L.kda_status_string.argtypes = [_I]
     L.kda_status_string.restype = ctypes.c_char_p
@@ -134,6 +142,48 @@ def kda_chunk_fwd_varlen(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_b
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
         float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
         _ptr(out), _ptr(final_state), H, dk, dv, chunk, _dtype_code(q, dtype),
+        _stream(stream)))
+
+
+def kda_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk=64, dtype=KDA_BF16) -> int:
+    """Device workspace bytes kda_chunk_fwd_ws needs (0: none)."""
+    return int(lib().kda_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dtype))
+
+
+def kda_chunk_fwd_varlen_workspace_size(N, total_T, H, dk, dv, chunk=64, dtype=KDA_BF16) -> int:
+    """Device workspace bytes kda_chunk_fwd_varlen_ws needs (0: none)."""
+    return int(lib().kda_chunk_fwd_varlen_workspace_size(N, total_T, H, dk, dv, chunk, dtype))
+
+
+def _ws(workspace):
+    """(pointer, bytes) of a workspace given as a CUDA tensor, (address, bytes) or None."""
+    if workspace is None:
+        return None, 0
+    if isinstance(workspace, tuple):
+        return workspace
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def kda_chunk_fwd_ws(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                     initial_state, out, final_state, B, T, H, dk, dv, chunk=64, dtype=None,
+                     workspace=None, stream=None):
+    """kda_chunk_fwd through a caller workspace (two-launch path; see include/kda.h)."""
+    wp, wb = _ws(workspace)
+    _check("kda_chunk_fwd_ws", lib().kda_chunk_fwd_ws(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(initial_state), _ptr(out), _ptr(final_state),
+        B, T, H, dk, dv, chunk, _dtype_code(q, dtype), wp, wb, _stream(stream)))
+
+
+def kda_chunk_fwd_varlen_ws(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                            cu_seqlens, N, total_T, initial_state, out, final_state, H, dk, dv,
+                            chunk=64, dtype=None, workspace=None, stream=None):
+    """kda_chunk_fwd_varlen through a caller workspace (see include/kda.h)."""
+    wp, wb = _ws(workspace)
+    _check("kda_chunk_fwd_varlen_ws", lib().kda_chunk_fwd_varlen_ws(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
+        _ptr(out), _ptr(final_state), H, dk, dv, chunk, _dtype_code(q, dtype), wp, wb,
         _stream(stream)))
 
 

@@ -35,6 +35,7 @@
 #ifndef KDA_H_
 #define KDA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -62,7 +63,8 @@ enum kda_status {
   KDA_ERR_LAUNCH = -8,          /* the CUDA launch failed (cudaGetLastError) */
   KDA_ERR_DEVICE = -9,          /* no usable device / not a compute capability 10.3 GPU */
   KDA_ERR_SCALE = -10,          /* scale is NaN or infinite */
-  KDA_ERR_TOO_LARGE = -11       /* an index would overflow the kernels' 64-bit limits */
+  KDA_ERR_TOO_LARGE = -11,      /* an index would overflow the kernels' 64-bit limits */
+  KDA_ERR_WORKSPACE = -12       /* workspace NULL, too small or not 256-byte aligned */
 };
 
 /*
@@ -112,6 +114,43 @@ int kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const floa
                          kda_stream_t stream);
 
 /*
+ * Workspace variants of the two chunked entry points.  For bf16 q/k/v with dk = dv = 128
+ * and chunk = 64 they run the forward in two launches: every chunk's state-independent
+ * part (gates, norms, the gate-scaled products, the UT solve and transform; the
+ * kernel_delta_attention page's "parallel within chunks") for all chunks of all sequences
+ * at once, then the sequential pass over the state, which reads one workspace record per
+ * (chunk, head).  The results equal those of kda_chunk_fwd / kda_chunk_fwd_varlen up to
+ * rounding.  For every other configuration the workspace is not used and the call runs the
+ * same kernels as the entry point without it.
+ *
+ *   kda_chunk_fwd_workspace_size / kda_chunk_fwd_varlen_workspace_size
+ *       bytes of device workspace the matching call needs (0: none).  About 74 KB per
+ *       (64-token chunk, head): 612 MB for B = 4, T = 4096, H = 32.  The varlen size is an
+ *       upper bound from total_T and N (every sequence may end in a partial chunk).
+ *   workspace       DEVICE buffer of at least that many bytes, 256-byte aligned, owned by
+ *                   the caller; its contents on entry are irrelevant and on return are
+ *                   unspecified.  It must not be used by anything else until the stream
+ *                   has passed the call.  May be NULL when the size is 0.
+ *   workspace_bytes its size; a smaller or misaligned buffer gives KDA_ERR_WORKSPACE.
+ * All other arguments, layouts and errors are those of kda_chunk_fwd / _varlen.
+ */
+size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int dtype);
+size_t kda_chunk_fwd_varlen_workspace_size(int N, int total_T, int H, int dk, int dv,
+                                           int chunk, int dtype);
+int kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const float* g,
+                     const float* beta_logits, const float* a_log, const float* dt_bias,
+                     float scale, float lower_bound, const float* initial_state, void* out,
+                     float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                     int dtype, void* workspace, size_t workspace_bytes, kda_stream_t stream);
+int kda_chunk_fwd_varlen_ws(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta_logits, const float* a_log,
+                            const float* dt_bias, float scale, float lower_bound,
+                            const int32_t* cu_seqlens, int N, int total_T,
+                            const float* initial_state, void* out, float* final_state, int H,
+                            int dk, int dv, int chunk, int dtype, void* workspace,
+                            size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_decode_step -- advance the recurrence by exactly one token for B requests, in the
  *   kda_tkg layouts (NKI "KDA TKG Kernel API Reference", kda_tkg), all fp32:
  *
@@ -139,8 +178,9 @@ int kda_version(void);
 /*
  * kda_device_error -- bitmask of errors that kernels recorded on the current device since
  *   the last reset (no paper counterpart: it reports the kernels' own safeguards).
- *   Bit 0: a bounded wait inside the tensor-core chunk kernel gave up (the outputs of that
- *   launch are incomplete).  Synchronises the device.  reset != 0 clears the mask.
+ *   Bit 0: a bounded wait inside the single-pass tensor-core chunk kernel gave up; bit 1:
+ *   one inside the two-launch (workspace) chunk kernels did (the outputs of that launch
+ *   are incomplete).  Synchronises the device.  reset != 0 clears the mask.
  *   Returns the mask (>= 0) or KDA_ERR_DEVICE.
  */
 int kda_device_error(int reset);

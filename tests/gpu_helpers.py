@@ -46,8 +46,17 @@ def rel_err(gpu, ref):
     return max_abs(gpu, ref) / max(den, 1e-30)
 
 
-def run_chunk(d, B, T, H, dk, dv, scale, lb, chunk, bf16, want_state=True, alias=False):
-    """Call kda_chunk_fwd on host inputs ``d`` (numpy, [B,T,H,.] layouts)."""
+def workspace(nbytes):
+    """A device workspace of ``nbytes`` (256-byte aligned, as cudaMalloc returns), or None."""
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+
+def run_chunk(d, B, T, H, dk, dv, scale, lb, chunk, bf16, want_state=True, alias=False,
+              ws=False):
+    """Call kda_chunk_fwd (or, with ``ws``, kda_chunk_fwd_ws) on host inputs ``d`` (numpy,
+    [B,T,H,.] layouts)."""
     io = torch.bfloat16 if bf16 else torch.float32
     q, k, v = (to_dev(d[n], io) for n in ("q", "k", "v"))
     g, bl = to_dev(d["g"]), to_dev(d["beta_logits"])
@@ -58,13 +67,19 @@ def run_chunk(d, B, T, H, dk, dv, scale, lb, chunk, bf16, want_state=True, alias
         s1 = s0
     else:
         s1 = torch.full((B, H, dk, dv), float("nan"), device="cuda") if want_state else None
-    kda.kda_chunk_fwd(q, k, v, g, bl, a_log, dt_bias, scale, lb, s0, out, s1, B, T, H, dk,
-                      dv, chunk)
+    if ws:
+        w = workspace(kda.kda_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk,
+                                                       1 if bf16 else 0))
+        kda.kda_chunk_fwd_ws(q, k, v, g, bl, a_log, dt_bias, scale, lb, s0, out, s1, B, T, H,
+                             dk, dv, chunk, workspace=w)
+    else:
+        kda.kda_chunk_fwd(q, k, v, g, bl, a_log, dt_bias, scale, lb, s0, out, s1, B, T, H, dk,
+                          dv, chunk)
     torch.cuda.synchronize()
     return (out.float().cpu().numpy(), None if s1 is None else s1.cpu().numpy())
 
 
-def run_varlen(d, H, dk, dv, scale, lb, chunk, bf16):
+def run_varlen(d, H, dk, dv, scale, lb, chunk, bf16, ws=False):
     io = torch.bfloat16 if bf16 else torch.float32
     total = d["q"].shape[0]
     N = len(d["cu_seqlens"]) - 1
@@ -72,9 +87,15 @@ def run_varlen(d, H, dk, dv, scale, lb, chunk, bf16):
     cu = torch.from_numpy(d["cu_seqlens"].astype(np.int32)).cuda()
     out = torch.full((total, H, dv), float("nan"), device="cuda", dtype=io)
     s1 = torch.full((N, H, dk, dv), float("nan"), device="cuda")
-    kda.kda_chunk_fwd_varlen(q, k, v, to_dev(d["g"]), to_dev(d["beta_logits"]),
-                             to_dev(d["a_log"]), to_dev(d["dt_bias"]), scale, lb, cu, N, total,
-                             to_dev(d.get("initial_state")), out, s1, H, dk, dv, chunk)
+    args = (q, k, v, to_dev(d["g"]), to_dev(d["beta_logits"]), to_dev(d["a_log"]),
+            to_dev(d["dt_bias"]), scale, lb, cu, N, total, to_dev(d.get("initial_state")), out,
+            s1, H, dk, dv, chunk)
+    if ws:
+        w = workspace(kda.kda_chunk_fwd_varlen_workspace_size(N, total, H, dk, dv, chunk,
+                                                              1 if bf16 else 0))
+        kda.kda_chunk_fwd_varlen_ws(*args, workspace=w)
+    else:
+        kda.kda_chunk_fwd_varlen(*args)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), s1.cpu().numpy()
 

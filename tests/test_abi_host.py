@@ -23,7 +23,7 @@ def L():
 
 def _declared():
     text = open(HEADER).read()
-    return re.findall(r"^\s*(?:int|const char\s*\*)\s*(kda_\w+)\s*\(", text, re.M)
+    return re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s*(kda_\w+)\s*\(", text, re.M)
 
 
 def test_header_declares_the_boundary():
@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_status_strings_and_version(L):
     assert kda.kda_status_string(0) == "ok"
-    for code in range(-11, 0):
+    for code in range(-12, 0):
         assert kda.kda_status_string(code) != "unknown kda status"
     assert kda.kda_status_string(-999) == "unknown kda status"
     assert kda.kda_version() >= 100
@@ -119,3 +119,57 @@ def test_binding_raises_on_error_status(L):
         kda.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 3.0, FAKE, FAKE,
                             1, 1, 128, 128, stream=0)
     assert ei.value.status == -5
+
+
+# Workspace record of the two-launch path per (64-token chunk, head): four bf16 [64 x 128]
+# tiles, one bf16 [64 x 64] tile and 256 fp32 values.
+REC = 4 * 64 * 128 * 2 + 64 * 64 * 2 + 256 * 4
+
+
+def test_workspace_size_formula(L):
+    ws = kda.kda_chunk_fwd_workspace_size
+    assert ws(4, 4096, 32, 128, 128, 64, 1) == 4 * 64 * 32 * REC
+    assert ws(2, 65, 3, 128, 128, 64, 1) == 2 * 2 * 3 * REC      # ragged: 2 chunks each
+    assert ws(2, 0, 3, 128, 128, 64, 1) == 0                     # no tokens
+    # configurations that do not use the two-launch path need none
+    assert ws(4, 4096, 32, 128, 128, 64, 0) == 0                 # fp32
+    assert ws(4, 4096, 32, 128, 128, 16, 1) == 0                 # 16-token chunks
+    assert ws(4, 4096, 32, 64, 128, 64, 1) == 0                  # dk = 64
+    assert ws(-1, 4096, 32, 128, 128, 64, 1) == 0                # invalid
+    vs = kda.kda_chunk_fwd_varlen_workspace_size
+    # upper bound: total_T / 64 + N chunks, plus the (N + 1) int32 offsets rounded to 256 B
+    assert vs(8, 1000, 16, 128, 128, 64, 1) == (1000 // 64 + 8) * 16 * REC + 256
+    assert vs(300, 64 * 300, 2, 128, 128, 64, 1) == (300 + 300) * 2 * REC + 1280
+    assert vs(8, 1000, 16, 128, 128, 64, 0) == 0
+
+
+def _chunk_ws(L, ws, nbytes, **over):
+    a = dict(B=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=1)
+    a.update(over)
+    return L.kda_chunk_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, -1.0, None, FAKE,
+                              None, a["B"], a["T"], a["H"], a["dk"], a["dv"], a["chunk"],
+                              a["dtype"], ws, nbytes, None)
+
+
+def test_workspace_entry_rejects_bad_workspace(L):
+    need = kda.kda_chunk_fwd_workspace_size(1, 64, 2, 128, 128, 64, 1)
+    assert need == 2 * REC
+    assert _chunk_ws(L, None, 0) == -12
+    assert _chunk_ws(L, 0x100000, need - 1) == -12          # too small
+    assert _chunk_ws(L, 0x100000 + 16, need) == -12         # not 256-byte aligned
+    assert _chunk_ws(L, 0x100000, need, dk=100) == -3       # argument errors come first
+    v = L.kda_chunk_fwd_varlen_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, -1.0, FAKE, 2,
+                                  100, None, FAKE, None, 2, 128, 128, 64, 1, None, 0, None)
+    assert v == -12
+
+
+def test_workspace_entry_without_device(L):
+    """A valid workspace call (or one whose configuration needs none, with a NULL
+    workspace) reaches the device check and stops there on a machine without a GPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is only meaningful without one")
+    need = kda.kda_chunk_fwd_workspace_size(1, 64, 2, 128, 128, 64, 1)
+    assert _chunk_ws(L, 0x100000, need) == -9
+    assert _chunk_ws(L, None, 0, dtype=0) == -9              # fp32: no workspace used
+    assert _chunk_ws(L, None, 0, chunk=16) == -9

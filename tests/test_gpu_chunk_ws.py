@@ -1,0 +1,173 @@
+"""Parity of the workspace (two-launch) chunked forward -- kda_chunk_fwd_ws and
+kda_chunk_fwd_varlen_ws -- with the fp64 oracle, through the C ABI.
+
+The two-launch path serves bf16 q/k/v with dk = dv = 128 and 64-token chunks; the bar is
+that of the single-pass bf16 path: max |gpu - oracle| / max |oracle| <= 2e-2 per tensor
+(out and final state), the oracle fed the same bf16-rounded q/k/v.  Other configurations
+ignore the workspace and must give the single-pass results exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_55_gb300 as kda
+from gated_delta_rule_55_gb300 import synth
+from gpu_helpers import (BF16_REL, ensure_built, max_abs, oracle_inputs, rel_err, run_chunk,
+                         run_varlen, to_dev, workspace)
+from oracle import kda_forward, kda_forward_varlen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    kda.kda_device_error(reset=True)
+    yield
+    assert kda.kda_device_error(reset=True) == 0, "a bounded wait gave up"
+
+
+def _check(out, S, ref_out, ref_S):
+    assert rel_err(out, ref_out) <= BF16_REL, rel_err(out, ref_out)
+    assert rel_err(S, ref_S) <= BF16_REL, rel_err(S, ref_S)
+
+
+def _case(B, T, H, lb, seed, state_std=0.1, scale=None):
+    d = synth.chunk_inputs(B, T, H, 128, 128, seed, state_std)
+    scale = 128 ** -0.5 if scale is None else scale
+    out, S = run_chunk(d, B, T, H, 128, 128, scale, lb, 64, True, ws=True)
+    o = oracle_inputs(d, True)
+    ref_out, ref_S = kda_forward(o["q"], o["k"], o["v"], o["g"], o["beta_logits"], o["a_log"],
+                                 o["dt_bias"], scale, lb, o["initial_state"])
+    _check(out, S, ref_out, ref_S)
+    return out, S
+
+
+@pytest.mark.parametrize("lb", [-5.0, -0.05])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130, 300])
+def test_bf16_ragged(T, lb):
+    _case(B=2, T=T, H=3, lb=lb, seed=100 + T)
+
+
+def test_zero_initial_state_and_scale():
+    d = synth.chunk_inputs(1, 200, 2, 128, 128, 7, state_std=0.0)
+    d["initial_state"] = None
+    out, S = run_chunk(d, 1, 200, 2, 128, 128, 0.3, -2.0, 64, True, ws=True)
+    o = oracle_inputs(d, True)
+    ref_out, ref_S = kda_forward(o["q"], o["k"], o["v"], o["g"], o["beta_logits"], o["a_log"],
+                                 o["dt_bias"], 0.3, -2.0, None)
+    _check(out, S, ref_out, ref_S)
+
+
+def test_matches_single_pass_path():
+    """Both tensor-core paths compute the same algebra; their difference is rounding."""
+    B, T, H = 2, 257, 4
+    d = synth.chunk_inputs(B, T, H, 128, 128, 9, state_std=0.1)
+    o1, S1 = run_chunk(d, B, T, H, 128, 128, 0.09, -1.0, 64, True, ws=False)
+    o2, S2 = run_chunk(d, B, T, H, 128, 128, 0.09, -1.0, 64, True, ws=True)
+    assert rel_err(o2, o1) <= 1e-2 and rel_err(S2, S1) <= 1e-2
+
+
+def test_state_passthrough_two_calls_equal_one():
+    B, T, H = 2, 200, 2
+    d = synth.chunk_inputs(B, T, H, 128, 128, 11, state_std=0.2)
+    full_o, full_S = run_chunk(d, B, T, H, 128, 128, 0.1, -0.5, 64, True, ws=True)
+    cut = 128  # a chunk boundary: the two halves see the same chunking as one pass
+    d1 = {n: (x[:, :cut] if n in ("q", "k", "v", "g", "beta_logits") else x) for n, x in d.items()}
+    d2 = {n: (x[:, cut:] if n in ("q", "k", "v", "g", "beta_logits") else x) for n, x in d.items()}
+    o1, S1 = run_chunk(d1, B, cut, H, 128, 128, 0.1, -0.5, 64, True, ws=True)
+    d2["initial_state"] = S1
+    o2, S2 = run_chunk(d2, B, T - cut, H, 128, 128, 0.1, -0.5, 64, True, ws=True)
+    assert rel_err(np.concatenate([o1, o2], 1), full_o) <= 1e-2
+    assert rel_err(S2, full_S) <= 1e-2
+
+
+def test_empty_sequence_passes_state_through():
+    d = synth.chunk_inputs(2, 1, 2, 128, 128, 1, state_std=0.3)
+    s0 = to_dev(d["initial_state"])
+    s1 = torch.full_like(s0, float("nan"))
+    dummy = torch.zeros(16, device="cuda", dtype=torch.bfloat16)
+    f = torch.zeros(16, device="cuda")
+    kda.kda_chunk_fwd_ws(dummy, dummy, dummy, f, f, to_dev(d["a_log"]), to_dev(d["dt_bias"]),
+                         0.2, -1.0, s0, dummy, s1, 2, 0, 2, 128, 128, 64, workspace=None)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s0)
+
+
+def test_other_configurations_ignore_the_workspace():
+    """fp32 inputs (the SIMT kernel) through the workspace entry give the plain entry's
+    results bit for bit."""
+    B, T, H = 1, 100, 2
+    d = synth.chunk_inputs(B, T, H, 128, 128, 3, state_std=0.1)
+    o1, S1 = run_chunk(d, B, T, H, 128, 128, 0.1, -1.0, 64, False, ws=False)
+    o2, S2 = run_chunk(d, B, T, H, 128, 128, 0.1, -1.0, 64, False, ws=True)
+    assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
+
+
+def test_varlen_small_with_empty_and_ragged_sequences():
+    lens = [130, 0, 1, 64, 200, 63, 0]
+    H = 2
+    d = synth.varlen_inputs(lens, H, 128, 128, seed=14, state_std=0.1)
+    for lb in (-5.0, -0.1):
+        out, S = run_varlen(d, H, 128, 128, 0.09, lb, 64, True, ws=True)
+        o = oracle_inputs(d, True)
+        ref_out, ref_S = kda_forward_varlen(o["q"], o["k"], o["v"], o["g"], o["beta_logits"],
+                                            o["a_log"], o["dt_bias"], d["cu_seqlens"], 0.09,
+                                            lb, o["initial_state"])
+        _check(out, S, ref_out, ref_S)
+        np.testing.assert_array_equal(S[1], d["initial_state"][1])
+        np.testing.assert_array_equal(S[6], d["initial_state"][6])
+
+
+def test_varlen_many_short_sequences():
+    """More sequences than one pass of the chunk-offset scan (1024), mostly shorter than a
+    chunk, a few spanning several chunks."""
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 6, 1300)
+    lens[[5, 700, 1299]] = [64, 130, 257]
+    H = 1
+    d = synth.varlen_inputs([int(x) for x in lens], H, 128, 128, seed=22, state_std=0.05)
+    out, S = run_varlen(d, H, 128, 128, 0.09, -2.0, 64, True, ws=True)
+    o = oracle_inputs(d, True)
+    ref_out, ref_S = kda_forward_varlen(o["q"], o["k"], o["v"], o["g"], o["beta_logits"],
+                                        o["a_log"], o["dt_bias"], d["cu_seqlens"], 0.09, -2.0,
+                                        o["initial_state"])
+    _check(out, S, ref_out, ref_S)
+
+
+def test_prefill_workload_B4_T4096_sampled():
+    """B=4, T=4096, H=32, bf16, chunk 64, zero initial state, through the workspace: the
+    full launch, checked on sampled (b, h) pairs over the whole sequence."""
+    w = synth.PREFILL_B4
+    d = synth.workload_inputs(w)
+    out, S = run_chunk(d, w.B, w.T, w.H, w.dk, w.dv, w.q_scale, w.lower_bound, w.chunk, True,
+                       ws=True)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(S))
+    rng = np.random.default_rng(3)
+    for b, h in zip(rng.integers(0, w.B, 3), rng.integers(0, w.H, 3)):
+        sub = oracle_inputs({n: np.ascontiguousarray(d[n][b:b + 1, :, h:h + 1])
+                             for n in ("q", "k", "v")}, True)
+        ro, rs = kda_forward(sub["q"], sub["k"], sub["v"], d["g"][b:b + 1, :, h:h + 1],
+                             d["beta_logits"][b:b + 1, :, h:h + 1], d["a_log"][h:h + 1],
+                             d["dt_bias"][:, h:h + 1], w.q_scale, w.lower_bound, None)
+        assert rel_err(out[b, :, h], ro[0, :, 0]) <= BF16_REL
+        assert rel_err(S[b, h], rs[0, 0]) <= BF16_REL
+
+
+def test_varlen_workload_8seq_sampled():
+    w = synth.VARLEN_8
+    d = synth.workload_inputs(w)
+    out, S = run_varlen(d, w.H, w.dk, w.dv, w.q_scale, w.lower_bound, w.chunk, True, ws=True)
+    cu = d["cu_seqlens"]
+    rng = np.random.default_rng(4)
+    picks = [(int(n), int(rng.integers(0, w.H))) for n in rng.choice(w.n_seqs, 2, replace=False)]
+    picks.append((int(np.argmax(np.diff(cu))), 3))
+    for n, h in picks:
+        a, b = cu[n], cu[n + 1]
+        o = oracle_inputs({x: d[x][None, a:b, h:h + 1] for x in ("q", "k", "v")}, True)
+        ro, rs = kda_forward(o["q"], o["k"], o["v"], d["g"][None, a:b, h:h + 1],
+                             d["beta_logits"][None, a:b, h:h + 1], d["a_log"][h:h + 1],
+                             d["dt_bias"][:, h:h + 1], w.q_scale, w.lower_bound,
+                             d["initial_state"][n:n + 1, h:h + 1])
+        assert rel_err(out[a:b, h], ro[0, :, 0]) <= BF16_REL
+        assert rel_err(S[n, h], rs[0, 0]) <= BF16_REL
