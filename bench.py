@@ -1,9 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the KDA forward library on GB300.
 
-One step = one ``kda_chunk_fwd`` over the chunked-prefill workload (B=4, T=4096, H=32,
-dk=dv=128, bf16 q/k/v, fp32 gates/state, chunk 64), inputs resident in HBM (0.82 GB,
-larger than L2, so no flush is needed between steps).  The printed JSON line reports
+One step = one ``kda_chunk_fwd_ws`` over the chunked-prefill workload (B=4, T=4096, H=32,
+dk=dv=128, bf16 q/k/v, fp32 gates/state, chunk 64): the per-chunk prep launch and the
+state-scan launch, inputs resident in HBM (0.82 GB, larger than L2, so no flush is needed
+between steps) and the caller's workspace allocated once outside the timed region.  The printed JSON line reports
 tokens/s (B*T per step, whole job over all ranks), the chunk kernel's HBM roofline
 fraction, an end-to-end figure through the same C-ABI call with host buffers, the fp64
 oracle timed on the host as a CPU baseline, SM clocks sampled during the timed region,
@@ -37,7 +38,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "KDA chunked-fwd tokens/s; decode-step HBM GB/s vs peak (1 GB300)"
 L2_BYTES = 126 * 2 ** 20
-CHUNK_KERNEL_SOURCES = ["kda_chunk_tc.cu", "tc_prims.cuh"]  # the kernel the roofline covers
+# the kernels the roofline covers (the two launches of one kda_chunk_fwd_ws call)
+CHUNK_KERNEL_SOURCES = ["kda_chunk_split.cu", "chunk_common.cuh", "tc_prims.cuh"]
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -50,7 +52,7 @@ def parse_args():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the decode / varlen / e2e / cpu-baseline measurements")
-    p.add_argument("--profile", choices=["chunk", "decode", "varlen"], default=None,
+    p.add_argument("--profile", choices=["chunk", "chunk1", "decode", "varlen"], default=None,
                    help="run two launches of one kernel on a reduced case (for ncu) and exit")
     return p.parse_args()
 
@@ -230,20 +232,36 @@ def device_prefill(w):
     if w.kind == "varlen":
         dev["cu_seqlens"] = torch.from_numpy(d["cu_seqlens"]).cuda()
         dev["total_T"] = int(d["cu_seqlens"][-1])
+    import gated_delta_rule_55_gb300 as kda
+    code = kda.KDA_BF16 if w.dtype == "bf16" else kda.KDA_F32
+    nb = (kda.kda_chunk_fwd_workspace_size(w.B, w.T, w.H, w.dk, w.dv, w.chunk, code)
+          if w.kind == "chunk" else
+          kda.kda_chunk_fwd_varlen_workspace_size(w.n_seqs, dev["total_T"], w.H, w.dk, w.dv,
+                                                  w.chunk, code))
+    dev["workspace"] = torch.empty(nb, dtype=torch.uint8, device="cuda") if nb else None
     return d, dev
 
 
-def call_chunk(w, x):
+def call_chunk(w, x, single_pass=False):
+    """The chunked forward through the workspace entry points (two launches), or with
+    ``single_pass`` through kda_chunk_fwd / _varlen (one launch, no workspace)."""
     import gated_delta_rule_55_gb300 as kda
     if w.kind == "chunk":
-        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"],
-                          x["dt_bias"], w.q_scale, w.lower_bound, x["initial_state"], x["out"],
-                          x["final_state"], w.B, w.T, w.H, w.dk, w.dv, w.chunk)
+        args = (x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"], x["dt_bias"],
+                w.q_scale, w.lower_bound, x["initial_state"], x["out"], x["final_state"], w.B,
+                w.T, w.H, w.dk, w.dv, w.chunk)
+        if single_pass:
+            kda.kda_chunk_fwd(*args)
+        else:
+            kda.kda_chunk_fwd_ws(*args, workspace=x["workspace"])
     else:
-        kda.kda_chunk_fwd_varlen(x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"],
-                                 x["dt_bias"], w.q_scale, w.lower_bound, x["cu_seqlens"],
-                                 w.n_seqs, x["total_T"], x["initial_state"], x["out"],
-                                 x["final_state"], w.H, w.dk, w.dv, w.chunk)
+        args = (x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"], x["dt_bias"],
+                w.q_scale, w.lower_bound, x["cu_seqlens"], w.n_seqs, x["total_T"],
+                x["initial_state"], x["out"], x["final_state"], w.H, w.dk, w.dv, w.chunk)
+        if single_pass:
+            kda.kda_chunk_fwd_varlen(*args)
+        else:
+            kda.kda_chunk_fwd_varlen_ws(*args, workspace=x["workspace"])
 
 
 def timed(fn, K, W, dist=None, clocks=None):
@@ -411,12 +429,13 @@ def native(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                      "traffic": traffic_for("chunk_fwd_prefill_B4", CHUNK_KERNEL_SOURCES),
-                     "kernel": "chunk kernel (one launch per step)",
+                     "kernel": "chunk forward step: prep + scan launches of one "
+                               "kda_chunk_fwd_ws call (both timed together)",
                      "algorithmic_bytes_per_launch": nbytes,
                      "peak_source": f"{pk['source']} (MEASURED_PEAKS hbm_gbs)",
                      "tensor_frac": flops / per_launch_s / 1e12 / pk["bf16_tflops"],
                      "algorithmic_flops_per_launch": flops},
-        "gpu_launches": K,
+        "gpu_launches": 2 * K,
         "clocks": clk,
     }
     if not args.no_secondary and dist.rank == 0:
@@ -436,7 +455,13 @@ def native(args):
                           "hbm_gbs": vbytes / per / 1e9,
                           "frac_of_hbm_peak": vbytes / per / 1e9 / pk["hbm_gbs"],
                           "longest_seq": int(np.max(np.diff(dv_["cu_seqlens"])))}
+        msv1 = timed(lambda: call_chunk(wv, xv, single_pass=True), max(3, K // 5), 3)
+        line["varlen"]["single_pass_ms_per_call"] = msv1 / max(3, K // 5)
         del xv
+        ms1 = timed(lambda: call_chunk(w, x, single_pass=True), max(3, K // 5), 3)
+        line["single_pass"] = {"entry": "kda_chunk_fwd (one launch, no workspace)",
+                               "ms_per_step": ms1 / max(3, K // 5),
+                               "tokens_per_s": w.B * w.T * max(3, K // 5) / (ms1 * 1e-3)}
         ems, h2d, d2h = e2e_measure(w, d, x, max(3, K // 5), 3)
         line["e2e"] = {"value": w.B * w.T * max(3, K // 5) / (ems * 1e-3), "unit": "tokens/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -459,11 +484,11 @@ def profile_case(which):
         w = synth.DECODE_B64
         decode_measure(w, 2, False)
     else:
-        w = replace(synth.PREFILL_B4, H=8) if which == "chunk" else \
+        w = replace(synth.PREFILL_B4, H=8) if which in ("chunk", "chunk1") else \
             replace(synth.VARLEN_8, H=4)
         _, x = device_prefill(w)
         for _ in range(2):
-            call_chunk(w, x)
+            call_chunk(w, x, single_pass=(which == "chunk1"))
     torch.cuda.synchronize()
     print(f"profile case {which}: {w.name} done", flush=True)
 
