@@ -25,7 +25,8 @@ STATUS_NAMES = {
 # Exported symbols, in declaration order of include/kda.h.
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_size",
            "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
-           "kda_decode_step", "kda_status_string", "kda_version", "kda_device_error")
+           "kda_chunk_fwd_noalloc", "kda_decode_step", "kda_status_string", "kda_version",
+           "kda_device_error")
 
 
 class KDAError(RuntimeError):
@@ -62,11 +63,13 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_fwd_varlen_workspace_size.restype = _Z
     L.kda_chunk_fwd_ws.argtypes = L.kda_chunk_fwd.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_varlen_ws.argtypes = L.kda_chunk_fwd_varlen.argtypes[:-1] + [_P, _Z, _P]
+    L.kda_chunk_fwd_noalloc.argtypes = L.kda_chunk_fwd.argtypes
     L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
                                   _I, _I, _I, _I, _P]
     L.kda_device_error.argtypes = [_I]
     for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
-              "kda_chunk_fwd_varlen_ws", "kda_decode_step", "kda_version", "kda_device_error"):
+              "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_decode_step",
+              "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
     L.kda_status_string.argtypes = [_I]
     L.kda_status_string.restype = ctypes.c_char_p
@@ -185,6 +188,20 @@ def kda_chunk_fwd_varlen_ws(q, k, v, g, beta_logits, a_log, dt_bias, scale, lowe
         float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
         _ptr(out), _ptr(final_state), H, dk, dv, chunk, _dtype_code(q, dtype), wp, wb,
         _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 256 << 20  # include/kda.h KDA_NOALLOC_SCRATCH_BYTES
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                          initial_state, out, final_state, B, T, H, dk, dv, chunk=64,
+                          dtype=None, stream=None):
+    """kda_chunk_fwd_ws with the library's own scratch array as the workspace (see
+    include/kda.h)."""
+    _check("kda_chunk_fwd_noalloc", lib().kda_chunk_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(initial_state), _ptr(out), _ptr(final_state),
+        B, T, H, dk, dv, chunk, _dtype_code(q, dtype), _stream(stream)))
 
 
 def kda_decode_step(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, out, S,

@@ -151,6 +151,24 @@ int kda_chunk_fwd_varlen_ws(const void* q, const void* k, const void* v, const f
                             size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd_ws with the workspace taken from a scratch array
+ *   that the library keeps in device memory (KDA_NOALLOC_SCRATCH_BYTES per device), so the
+ *   caller passes none.  It has no counterpart on the source pages: an interface
+ *   convenience over the workspace entry point.
+ *   Arguments, layouts, results and errors are those of kda_chunk_fwd.  A configuration
+ *   whose workspace (kda_chunk_fwd_workspace_size) exceeds the array is rejected with
+ *   KDA_ERR_WORKSPACE before anything is enqueued.  The array is shared by every call on a
+ *   device: calls must not overlap in time (issue them on one stream, or synchronise
+ *   between streams).  Its device memory is taken when the entry point is first used.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)256 << 20)
+int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                          const float* beta_logits, const float* a_log, const float* dt_bias,
+                          float scale, float lower_bound, const float* initial_state, void* out,
+                          float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                          int dtype, kda_stream_t stream);
+
+/*
  * kda_decode_step -- advance the recurrence by exactly one token for B requests, in the
  *   kda_tkg layouts (NKI "KDA TKG Kernel API Reference", kda_tkg), all fp32:
  *
