@@ -6,6 +6,7 @@ legs may import this package.
 from .kda_oracle import (  # noqa: F401
     L2_EPS,
     activate_gate,
+    kda_attention,
     kda_decode_step,
     kda_forward,
     kda_forward_varlen,

@@ -171,3 +171,41 @@ def kda_decode_step(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
     k_hat = l2_normalize(k)
     S = np.asarray(S, dtype=np.float64)
     return kda_token(S, q_hat, k_hat, v, gamma, beta, order)
+
+
+def kda_attention(query, key, value, beta, decay=None, initial_state=None, softmax_scale=None,
+                  use_qk_l2norm=True, order="decay_first"):
+    """The ``kernel_delta_attention`` / ``kda_attention`` call of the ejkernel
+    ``kernel_delta_attention`` page, as the plain token scan.
+
+    Parameters as on that page: ``query, key [B, T, H, dk]``, ``value [B, T, H, dv]``,
+    ``beta [B, T, H]`` -- a per-token learning rate used as given (the page's example
+    passes probabilities through a sigmoid itself) --, ``decay [B, T, H]`` -- a per-head
+    log-decay, the same for every key channel, ``None`` meaning zeros (full retention) --,
+    ``initial_state [B, H, dk, dv]`` (``None`` means zeros), ``softmax_scale`` (default
+    ``dk ** -0.5``, applied to the query), ``use_qk_l2norm`` (normalise q and k over the head
+    dimension before use).  ``use_chunked`` only selects an algorithm for the same result,
+    so it has no counterpart here.  Returns ``(out [B, T, H, dv], final_state)`` in fp64.
+    """
+    q = np.asarray(query, dtype=np.float64)
+    k = np.asarray(key, dtype=np.float64)
+    v = np.asarray(value, dtype=np.float64)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    scale = dk ** -0.5 if softmax_scale is None else float(softmax_scale)
+    if use_qk_l2norm:
+        q = l2_normalize(q)
+        k = l2_normalize(k)
+    q_hat = scale * q
+    d = (np.zeros((B, T, H)) if decay is None else np.asarray(decay, dtype=np.float64))
+    gamma = np.broadcast_to(d[..., None], (B, T, H, dk))  # one log-decay for every channel
+    b = np.asarray(beta, dtype=np.float64)
+    if initial_state is None:
+        S = np.zeros((B, H, dk, dv), dtype=np.float64)
+    else:
+        S = np.array(initial_state, dtype=np.float64, copy=True)
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    for t in range(T):
+        o, S = kda_token(S, q_hat[:, t], k[:, t], v[:, t], gamma[:, t], b[:, t], order)
+        out[:, t] = o
+    return out, S
