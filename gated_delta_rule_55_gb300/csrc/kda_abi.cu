@@ -153,6 +153,44 @@ int kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const floa
   return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kda_attention_fwd(const void* query, const void* key, const void* value, const float* beta,
+                      const float* decay, const float* initial_state, void* out,
+                      float* final_state, float softmax_scale, int B, int T, int H, int dk,
+                      int dv, int chunk, int flags, int dtype, kda_stream_t stream) {
+  if (!query || !key || !value || !beta || !out) return KDA_ERR_NULL_POINTER;
+  if (B < 0 || T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
+  if (flags & ~(KDA_ATTN_NO_QK_L2NORM | KDA_ATTN_RECURRENT | KDA_ATTN_ORDER_LITERAL))
+    return KDA_ERR_FLAGS;
+  int s = check_common(&softmax_scale, -1.0f, dk, dv);
+  if (s != KDA_OK) return s;
+  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_TOO_LARGE;
+  kda::ChunkArgs a{};
+  a.q = query; a.k = key; a.v = value; a.beta_logits = beta; a.decay = decay;
+  a.initial_state = initial_state; a.out = out; a.final_state = final_state;
+  a.scale = softmax_scale; a.lower_bound = 0.f;
+  a.B = B; a.T = T; a.total_T = B * T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  a.gate_head = 1; a.beta_prob = 1;
+  a.no_l2norm = (flags & KDA_ATTN_NO_QK_L2NORM) ? 1 : 0;
+  a.literal = (flags & KDA_ATTN_ORDER_LITERAL) ? 1 : 0;
+  if (a.chunk != 16 && a.chunk != 64) return KDA_ERR_CHUNK;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  const void* ptrs[] = {query, key, value, beta, decay, initial_state, out, final_state};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  const double elems = (double)a.total_T * H * (dk > dv ? dk : dv);
+  if (elems >= 1099511627776.0 || (double)B * H * dk * dv >= 1099511627776.0 || B > 65535 ||
+      H > 65535)
+    return KDA_ERR_TOO_LARGE;
+  s = check_device();
+  if (s != KDA_OK) return s;
+  if (B == 0) return KDA_OK;
+  const bool bf16 = dtype == KDA_BF16;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = (flags & KDA_ATTN_RECURRENT) ? kda::launch_recurrent(a, bf16, st)
+                                                     : kda::launch_chunk_simt(a, bf16, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
                                     int dtype) {
   if (B < 0 || T < 0 || H <= 0 || (long long)B * T > 0x7fffffffLL) return 0;
@@ -238,6 +276,7 @@ const char* kda_status_string(int status) {
     case KDA_ERR_SCALE: return "scale must be finite";
     case KDA_ERR_TOO_LARGE: return "problem too large for the kernels' index limits";
     case KDA_ERR_WORKSPACE: return "workspace NULL, smaller than required or not 256-byte aligned";
+    case KDA_ERR_FLAGS: return "unknown bits in the flags argument";
     default: return "unknown kda status";
   }
 }

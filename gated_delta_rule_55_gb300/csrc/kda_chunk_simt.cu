@@ -6,6 +6,8 @@
 // chunk size beyond rounding).  Per chunk, with G_r the in-chunk cumulative log-decay
 // (kernel_delta_attention page, "Algorithm modes: chunked"; decay-first recurrence):
 //   Xk_r = k^_r e^{G_r}, Xq_r = q^_r e^{G_r}, Kd_s = k^_s e^{-G_s}      (|G| <= 16*5)
+//   (literal order, the error term reading the memory before the token's decay:
+//    Xk_r = k^_r e^{G_{r-1}}; everything else is unchanged)
 //   A_rs = Xk_r . Kd_s (s < r),  M_rs = Xq_r . Kd_s (s <= r)             (gate-scaled K K^T, Q K^T)
 //   T    = (I + diag(beta) A)^{-1} diag(beta)                            (UT / WY transform)
 //   W    = T Xk,  U~ = T V
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(ChunkArgs a) {
   const Tin* v = static_cast<const Tin*>(a.v);
   Tin* out = static_cast<Tin*>(a.out);
   const long long state_off = ((long long)seq * H + h) * DK * DV;
-  const float exp_a = expf(a.a_log[h]);
+  const float exp_a = a.gate_head ? 0.f : expf(a.a_log[h]);
 
   // State slice: initial_state or zeros.
   for (int i = tid; i < DK * kDVS; i += kThreads) {
@@ -75,7 +77,10 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(ChunkArgs a) {
         const long long off = ((bos + t0 + r) * H + h) * DK + c;
         xq = load_as_float(q + off);
         xk = load_as_float(k + off);
-        xg = a.g[off];
+        if (!a.gate_head)
+          xg = a.g[off];
+        else if (a.decay)
+          xg = a.decay[(bos + t0 + r) * H + h];  // one log-decay for every channel
       }
       sQ[r * LD + c] = xq;
       sK[r * LD + c] = xk;
@@ -85,7 +90,14 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(ChunkArgs a) {
       const int r = i / kDVS, j = i % kDVS;
       sV[i] = r < n ? load_as_float(v + ((bos + t0 + r) * H + h) * DV + j0 + j) : 0.f;
     }
-    if (tid < kC) sBeta[tid] = tid < n ? sigmoidf_(a.beta_logits[(bos + t0 + tid) * H + h]) : 0.f;
+    if (tid < kC) {
+      float b = 0.f;
+      if (tid < n) {
+        b = a.beta_logits[(bos + t0 + tid) * H + h];
+        if (!a.beta_prob) b = sigmoidf_(b);
+      }
+      sBeta[tid] = b;
+    }
     __syncthreads();
 
     // -- prologue: L2 norms (warp per row) and the cumulative gate (thread per channel)
@@ -97,17 +109,18 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(ChunkArgs a) {
       }
       sq = warp_sum(sq);
       sk = warp_sum(sk);
-      const float rq = a.scale / sqrtf(sq + kL2Eps), rk = 1.0f / sqrtf(sk + kL2Eps);
+      const float rq = a.no_l2norm ? a.scale : a.scale / sqrtf(sq + kL2Eps);
+      const float rk = a.no_l2norm ? 1.0f : 1.0f / sqrtf(sk + kL2Eps);
       for (int c = lane; c < DK; c += 32) {
         sQ[r * LD + c] *= rq;
         sK[r * LD + c] *= rk;
       }
     }
     for (int c = tid; c < DK; c += kThreads) {
-      const float db = a.dt_bias[c * H + h];
+      const float db = a.gate_head ? 0.f : a.dt_bias[c * H + h];
       float G = 0.f;
       for (int r = 0; r < n; ++r) {
-        G += gate_gamma(sG[r * DK + c], db, exp_a, a.lower_bound);
+        G += a.gate_head ? sG[r * DK + c] : gate_gamma(sG[r * DK + c], db, exp_a, a.lower_bound);
         sG[r * DK + c] = G;
       }
     }
@@ -124,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) chunk_simt_kernel(ChunkArgs a) {
           const float G = sG[r * DK + c];
           const float e = expf(G);
           const float khat = sK[r * LD + c];
-          xk = khat * e;
+          xk = khat * (a.literal ? (r > 0 ? expf(sG[(r - 1) * DK + c]) : 1.f) : e);
           xq = sQ[r * LD + c] * e;
           kd = khat / e;
           kh = khat * expf(Gc - G);

@@ -677,7 +677,8 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, int H) {
 }  // namespace
 
 bool chunk_tc_supported(const ChunkArgs& a, bool bf16) {
-  return bf16 && a.dk == kD && a.dv == kD && a.chunk == 64;
+  return bf16 && a.dk == kD && a.dv == kD && a.chunk == 64 && !a.gate_head && !a.beta_prob &&
+         !a.no_l2norm && !a.literal;
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t st) {

@@ -33,6 +33,13 @@ struct ChunkArgs {
   int dk;
   int dv;
   int chunk;
+  // Variants of the kernel_delta_attention call (all zero: the kda_tkg-style gate and beta,
+  // L2-normalised q / k, decay before the delta write).
+  const float* decay;  // gate_head: per-head log-decay [rows, H], NULL = no decay
+  int gate_head;       // 1: gamma = decay[t, h] on every channel (g, a_log, dt_bias unused)
+  int beta_prob;       // 1: beta_logits hold the rate itself (no sigmoid)
+  int no_l2norm;       // 1: q, k used as given (scale still multiplies q)
+  int literal;         // 1: the error term reads the memory before its decay
 };
 
 struct DecodeArgs {
@@ -54,7 +61,9 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 unsigned int decode_read_error(bool reset);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, bool bf16, cudaStream_t stream);
-// Tensor-core chunk kernel: bf16 q/k/v, dk = dv = 128, 64-token chunks.
+// Sequential (token by token) scan: any supported shape, dtype and variant.
+cudaError_t launch_recurrent(const ChunkArgs& a, bool bf16, cudaStream_t stream);
+// Tensor-core chunk kernel: bf16 q/k/v, dk = dv = 128, 64-token chunks, default variant.
 bool chunk_tc_supported(const ChunkArgs& a, bool bf16);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t stream);
 unsigned int chunk_tc_read_error(bool reset);

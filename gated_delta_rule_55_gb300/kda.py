@@ -20,13 +20,16 @@ STATUS_NAMES = {
     0: "KDA_OK", -1: "KDA_ERR_NULL_POINTER", -2: "KDA_ERR_BAD_SHAPE", -3: "KDA_ERR_HEAD_DIM",
     -4: "KDA_ERR_CHUNK", -5: "KDA_ERR_LOWER_BOUND", -6: "KDA_ERR_MISALIGNED",
     -7: "KDA_ERR_DTYPE", -8: "KDA_ERR_LAUNCH", -9: "KDA_ERR_DEVICE", -10: "KDA_ERR_SCALE",
-    -11: "KDA_ERR_TOO_LARGE", -12: "KDA_ERR_WORKSPACE",
+    -11: "KDA_ERR_TOO_LARGE", -12: "KDA_ERR_WORKSPACE", -13: "KDA_ERR_FLAGS",
 }
 # Exported symbols, in declaration order of include/kda.h.
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_size",
            "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
-           "kda_chunk_fwd_noalloc", "kda_decode_step", "kda_status_string", "kda_version",
-           "kda_device_error")
+           "kda_chunk_fwd_noalloc", "kda_attention_fwd", "kda_decode_step", "kda_status_string",
+           "kda_version", "kda_device_error")
+KDA_ATTN_NO_QK_L2NORM = 1
+KDA_ATTN_RECURRENT = 2
+KDA_ATTN_ORDER_LITERAL = 4
 
 
 class KDAError(RuntimeError):
@@ -64,12 +67,14 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_fwd_ws.argtypes = L.kda_chunk_fwd.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_varlen_ws.argtypes = L.kda_chunk_fwd_varlen.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_noalloc.argtypes = L.kda_chunk_fwd.argtypes
+    L.kda_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
+                                    _I, _I, _P]
     L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
                                   _I, _I, _I, _I, _P]
     L.kda_device_error.argtypes = [_I]
     for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
-              "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_decode_step",
-              "kda_version", "kda_device_error"):
+              "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_attention_fwd",
+              "kda_decode_step", "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
     L.kda_status_string.argtypes = [_I]
     L.kda_status_string.restype = ctypes.c_char_p
@@ -202,6 +207,20 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
         float(scale), float(lower_bound), _ptr(initial_state), _ptr(out), _ptr(final_state),
         B, T, H, dk, dv, chunk, _dtype_code(q, dtype), _stream(stream)))
+
+
+def kda_attention_fwd(query, key, value, beta, decay, initial_state, out, final_state, B, T, H,
+                      dk, dv, softmax_scale=None, chunk=64, use_qk_l2norm=True,
+                      use_chunked=True, order="decay_first", dtype=None, stream=None):
+    """The kernel_delta_attention call: per-head log-decay (None: no decay), beta as given
+    (see include/kda.h)."""
+    flags = ((0 if use_qk_l2norm else KDA_ATTN_NO_QK_L2NORM) |
+             (0 if use_chunked else KDA_ATTN_RECURRENT) |
+             {"decay_first": 0, "literal": KDA_ATTN_ORDER_LITERAL}[order])
+    _check("kda_attention_fwd", lib().kda_attention_fwd(
+        _ptr(query), _ptr(key), _ptr(value), _ptr(beta), _ptr(decay), _ptr(initial_state),
+        _ptr(out), _ptr(final_state), float(softmax_scale or 0.0), B, T, H, dk, dv, chunk,
+        flags, _dtype_code(query, dtype), _stream(stream)))
 
 
 def kda_decode_step(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, out, S,

@@ -64,7 +64,8 @@ enum kda_status {
   KDA_ERR_DEVICE = -9,          /* no usable device / not a compute capability 10.3 GPU */
   KDA_ERR_SCALE = -10,          /* scale is NaN or infinite */
   KDA_ERR_TOO_LARGE = -11,      /* an index would overflow the kernels' 64-bit limits */
-  KDA_ERR_WORKSPACE = -12       /* workspace NULL, too small or not 256-byte aligned */
+  KDA_ERR_WORKSPACE = -12,      /* workspace NULL, too small or not 256-byte aligned */
+  KDA_ERR_FLAGS = -13           /* unknown bits in a flags argument */
 };
 
 /*
@@ -167,6 +168,40 @@ int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
                           float scale, float lower_bound, const float* initial_state, void* out,
                           float* final_state, int B, int T, int H, int dk, int dv, int chunk,
                           int dtype, kda_stream_t stream);
+
+/* Options of kda_attention_fwd (bitwise OR). */
+enum kda_attention_flags {
+  KDA_ATTN_NO_QK_L2NORM = 1,  /* use_qk_l2norm=False: q and k are used as given */
+  KDA_ATTN_RECURRENT = 2,     /* use_chunked=False: the token-by-token scan */
+  KDA_ATTN_ORDER_LITERAL = 4  /* the error term reads the memory before the token's decay,
+                                 as the printed recurrence has it (default: after) */
+};
+
+/*
+ * kda_attention_fwd -- the kernel_delta_attention / kda_attention call of the ejkernel
+ *   kernel_delta_attention page (parameters query, key, value, beta, decay, initial_state,
+ *   softmax_scale, chunk_size, use_qk_l2norm, use_chunked, return_state), for B equal-length
+ *   sequences:
+ *
+ *   query, key  [B, T, H, dk]   dtype (fp32 or bf16)
+ *   value, out  [B, T, H, dv]   dtype
+ *   beta        [B, T, H]       fp32: the per-token rate itself (not a logit)
+ *   decay       [B, T, H]       fp32 per-head log-decay, the same for every key channel
+ *                               (the page asks for values <= 0); NULL = no decay.  Values
+ *                               must lie in [-5, 5] for the chunked algorithm's factorised
+ *                               exponentials to stay in range.
+ *   initial_state / final_state [B, H, dk, dv] fp32, as for kda_chunk_fwd
+ *   softmax_scale  multiplies q (after its L2 norm when that is on); <= 0 selects dk^-0.5
+ *   chunk       16 or 64 (chunked mode; results do not depend on it beyond rounding)
+ *   flags       kda_attention_flags; unknown bits give KDA_ERR_FLAGS
+ *   The recurrence is kda_chunk_fwd's with gamma = decay[t, h] on every channel and beta
+ *   taken as given.  Runs on the fp32 SIMT kernels (chunked, 16-token chunks, or the
+ *   sequential scan).
+ */
+int kda_attention_fwd(const void* query, const void* key, const void* value, const float* beta,
+                      const float* decay, const float* initial_state, void* out,
+                      float* final_state, float softmax_scale, int B, int T, int H, int dk,
+                      int dv, int chunk, int flags, int dtype, kda_stream_t stream);
 
 /*
  * kda_decode_step -- advance the recurrence by exactly one token for B requests, in the

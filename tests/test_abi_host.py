@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_status_strings_and_version(L):
     assert kda.kda_status_string(0) == "ok"
-    for code in range(-12, 0):
+    for code in range(-13, 0):
         assert kda.kda_status_string(code) != "unknown kda status"
     assert kda.kda_status_string(-999) == "unknown kda status"
     assert kda.kda_version() >= 100
@@ -173,3 +173,30 @@ def test_workspace_entry_without_device(L):
     assert _chunk_ws(L, 0x100000, need) == -9
     assert _chunk_ws(L, None, 0, dtype=0) == -9              # fp32: no workspace used
     assert _chunk_ws(L, None, 0, chunk=16) == -9
+
+
+def _attn(L, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, decay=None, s0=None, out=FAKE, s1=None,
+             scale=0.0, B=1, T=64, H=2, dk=64, dv=64, chunk=64, flags=0, dtype=1)
+    a.update(over)
+    return L.kda_attention_fwd(a["q"], a["k"], a["v"], a["beta"], a["decay"], a["s0"], a["out"],
+                               a["s1"], a["scale"], a["B"], a["T"], a["H"], a["dk"], a["dv"],
+                               a["chunk"], a["flags"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), -1), (dict(beta=None), -1), (dict(out=None), -1), (dict(B=-1), -2),
+    (dict(H=0), -2), (dict(dk=48), -3), (dict(dv=16), -3), (dict(chunk=32), -4),
+    (dict(dtype=3), -7), (dict(flags=8), -13), (dict(flags=-1), -13),
+    (dict(decay=FAKE + 4), -6), (dict(scale=float("nan")), -10), (dict(B=70000, T=1), -11),
+])
+def test_attention_rejects_bad_arguments(L, over, code):
+    assert _attn(L, **over) == code
+
+
+def test_attention_without_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is only meaningful without one")
+    for flags in (0, 1, 2, 4, 7):
+        assert _attn(L, flags=flags) == -9
