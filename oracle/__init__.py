@@ -7,6 +7,7 @@ from .kda_oracle import (  # noqa: F401
     L2_EPS,
     activate_gate,
     kda_attention,
+    kda_backward,
     kda_decode_step,
     kda_forward,
     kda_forward_varlen,

@@ -209,3 +209,101 @@ def kda_attention(query, key, value, beta, decay=None, initial_state=None, softm
         o, S = kda_token(S, q_hat[:, t], k[:, t], v[:, t], gamma[:, t], b[:, t], order)
         out[:, t] = o
     return out, S
+
+
+def kda_backward(q, k, v, g, beta_logits, a_log, dt_bias, d_out, d_final_state=None,
+                 scale=None, lower_bound=-5.0, initial_state=None, order="decay_first"):
+    """Gradients of ``L = sum(d_out * out) + sum(d_final_state * final_state)`` for the
+    forward of ``kda_forward`` (same arguments and layouts), by reverse-mode differentiation
+    of the token scan.  The pages give no backward: this is the chain rule applied to each
+    step of the recurrence, in reverse token order.
+
+    Per token (decay first; ``D = diag(exp(gamma))``)::
+
+        S' = D S;  p = S'^T k^;  u = beta (v - p);  S_new = S' + k^ u^T;  o = S_new^T q^
+
+    with the adjoint ``dS`` of ``S_new`` (``d_final_state`` at the end)::
+
+        dS   += q^ do^T;          dq^ = S_new do
+        du    = dS^T k^;          dk^ = dS u
+        dv    = beta du;          dbeta = du . (v - p);   dp = -beta du
+        dS'   = dS + k^ dp^T;     dk^ += S' dp
+        dgamma = exp(gamma) * rowsum(dS' * S);            dS (previous) = D dS'
+
+    (literal order: ``p`` reads ``S``, so ``dk^ += S dp`` and ``dS (previous) = D dS + k^ dp^T``,
+    ``dgamma = exp(gamma) * rowsum(dS * S)``).  Then through the L2 norms, the scale, the
+    beta sigmoid and the gate ``lower_bound * sigmoid(exp(a_log) (g + dt_bias))``.
+
+    Returns a dict: ``dq, dk, dv, dg, dbeta_logits, da_log [H], ddt_bias [dk, H],
+    dinitial_state``, all fp64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = dk ** -0.5
+    a = np.exp(np.asarray(a_log, dtype=np.float64))            # [H]
+    bias = np.asarray(dt_bias, dtype=np.float64).T             # [H, dk]
+    z = a[:, None] * (g + bias)                                # [B, T, H, dk]
+    sz = sigmoid(z)
+    gamma = float(lower_bound) * sz
+    beta = sigmoid(beta_logits)
+    nq = np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + L2_EPS)
+    nk = np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + L2_EPS)
+    q_hat = float(scale) * q / nq
+    k_hat = k / nk
+    S = (np.zeros((B, H, dk, dv)) if initial_state is None
+         else np.array(initial_state, dtype=np.float64, copy=True))
+    states = [S]                                               # state before each token
+    for t in range(T):
+        _, S = kda_token(S, q_hat[:, t], k_hat[:, t], v[:, t], gamma[:, t], beta[:, t], order)
+        states.append(S)
+    d_out = np.asarray(d_out, dtype=np.float64)
+    dS = (np.zeros((B, H, dk, dv)) if d_final_state is None
+          else np.array(d_final_state, dtype=np.float64, copy=True))
+    dq_hat = np.zeros_like(q)
+    dk_hat = np.zeros_like(k)
+    dvv = np.zeros_like(v)
+    dbeta = np.zeros((B, T, H))
+    dgamma = np.zeros_like(g)
+    for t in range(T - 1, -1, -1):
+        S_prev, S_new = states[t], states[t + 1]
+        e = np.exp(gamma[:, t])                                # [B, H, dk]
+        kh, qh, b = k_hat[:, t], q_hat[:, t], beta[:, t]
+        do = d_out[:, t]                                       # [B, H, dv]
+        S_dec = e[..., :, None] * S_prev
+        base = S_dec if order == "decay_first" else S_prev     # what the error term reads
+        p = np.einsum("bhij,bhi->bhj", base, kh)
+        u = b[..., None] * (v[:, t] - p)
+        dS = dS + qh[..., :, None] * do[..., None, :]
+        dq_hat[:, t] = np.einsum("bhij,bhj->bhi", S_new, do)
+        du = np.einsum("bhij,bhi->bhj", dS, kh)
+        dk_t = np.einsum("bhij,bhj->bhi", dS, u)
+        dvv[:, t] = b[..., None] * du
+        dbeta[:, t] = np.sum(du * (v[:, t] - p), axis=-1)
+        dp = -b[..., None] * du
+        dk_t += np.einsum("bhij,bhj->bhi", base, dp)
+        if order == "decay_first":
+            dS_dec = dS + kh[..., :, None] * dp[..., None, :]
+            dgamma[:, t] = e * np.sum(dS_dec * S_prev, axis=-1)
+            dS = e[..., :, None] * dS_dec
+        else:
+            dgamma[:, t] = e * np.sum(dS * S_prev, axis=-1)
+            dS = e[..., :, None] * dS + kh[..., :, None] * dp[..., None, :]
+        dk_hat[:, t] = dk_t
+    # L2 norms (x^ = x / n, n = sqrt(|x|^2 + eps)): dx = dx^ / n - x (x . dx^) / n^3
+    dqn = float(scale) * dq_hat
+    dq = dqn / nq - q * np.sum(q * dqn, axis=-1, keepdims=True) / nq ** 3
+    dk_ = dk_hat / nk - k * np.sum(k * dk_hat, axis=-1, keepdims=True) / nk ** 3
+    dz = dgamma * float(lower_bound) * sz * (1.0 - sz)         # d/dz of lb sigmoid(z)
+    return {
+        "dq": dq, "dk": dk_, "dv": dvv,
+        "dg": dz * a[:, None],
+        "dbeta_logits": dbeta * beta * (1.0 - beta),
+        "da_log": np.sum(dz * z, axis=(0, 1, 3)),
+        "ddt_bias": np.sum(dz * a[:, None], axis=(0, 1)).T,
+        "dinitial_state": dS,
+    }
