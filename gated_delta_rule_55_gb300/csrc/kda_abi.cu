@@ -191,6 +191,54 @@ int kda_attention_fwd(const void* query, const void* key, const void* value, con
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
+size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv) {
+  if (B < 0 || T < 0 || H <= 0 || !head_dim_ok(dk) || !head_dim_ok(dv) ||
+      (long long)B * T > 0x7fffffffLL)
+    return 0;
+  return kda::backward_workspace(B, T, H, dk, dv);
+}
+
+int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta_logits, const float* a_log, const float* dt_bias,
+                  float scale, float lower_bound, const float* initial_state, const void* d_out,
+                  const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                  float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
+                  int B, int T, int H, int dk_, int dv_, int dtype, void* workspace,
+                  size_t workspace_bytes, kda_stream_t stream) {
+  kda::ChunkArgs a;
+  int s = fill_fixed(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                     initial_state, dq, nullptr, B, T, H, dk_, dv_, 64);
+  if (s != KDA_OK) return s;
+  if (!d_out || !dq || !dk || !dv || !dg || !dbeta_logits || !da_log || !ddt_bias)
+    return KDA_ERR_NULL_POINTER;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  const void* ptrs[] = {q, k, v, g, beta_logits, a_log, dt_bias, initial_state, d_out,
+                        d_final_state, dq, dk, dv, dg, dbeta_logits, da_log, ddt_bias,
+                        d_initial_state};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  const double elems = (double)a.total_T * H * (dk_ > dv_ ? dk_ : dv_);
+  if (elems >= 1099511627776.0 || (double)B * H * dk_ * dv_ * ((T + 63) / 64 + 64) >=
+                                      1099511627776.0 || B > 65535 || H > 65535)
+    return KDA_ERR_TOO_LARGE;
+  const size_t need = kda::backward_workspace(B, T, H, dk_, dv_);
+  if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                   workspace_bytes < need))
+    return KDA_ERR_WORKSPACE;
+  s = check_device();
+  if (s != KDA_OK) return s;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (B == 0) {
+    e = cudaMemsetAsync(da_log, 0, sizeof(float) * H, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * dk_ * H, st);
+  } else {
+    e = kda::launch_backward(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
+                             ddt_bias, d_initial_state, workspace, dtype == KDA_BF16, st);
+  }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
                                     int dtype) {
   if (B < 0 || T < 0 || H <= 0 || (long long)B * T > 0x7fffffffLL) return 0;

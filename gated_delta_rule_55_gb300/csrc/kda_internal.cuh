@@ -61,6 +61,13 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 unsigned int decode_read_error(bool reset);
 cudaError_t launch_chunk_simt(const ChunkArgs& a, bool bf16, cudaStream_t stream);
+// Backward of the chunked forward (fixed-length, decay first, kda_tkg gate): checkpointed
+// forward scan, reverse scan, elementwise chain rules.
+size_t backward_workspace(int B, int T, int H, int dk, int dv);
+cudaError_t launch_backward(const ChunkArgs& f, const void* d_out, const float* d_final,
+                            void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
+                            float* da_log, float* ddt_bias, float* d_initial, void* workspace,
+                            bool bf16, cudaStream_t stream);
 // Sequential (token by token) scan: any supported shape, dtype and variant.
 cudaError_t launch_recurrent(const ChunkArgs& a, bool bf16, cudaStream_t stream);
 // Tensor-core chunk kernel: bf16 q/k/v, dk = dv = 128, 64-token chunks, default variant.

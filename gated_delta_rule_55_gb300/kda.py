@@ -25,7 +25,8 @@ STATUS_NAMES = {
 # Exported symbols, in declaration order of include/kda.h.
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_size",
            "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
-           "kda_chunk_fwd_noalloc", "kda_attention_fwd", "kda_decode_step", "kda_status_string",
+           "kda_chunk_fwd_noalloc", "kda_chunk_bwd_workspace_size", "kda_chunk_bwd",
+           "kda_attention_fwd", "kda_decode_step", "kda_status_string",
            "kda_version", "kda_device_error")
 KDA_ATTN_NO_QK_L2NORM = 1
 KDA_ATTN_RECURRENT = 2
@@ -67,13 +68,17 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_fwd_ws.argtypes = L.kda_chunk_fwd.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_varlen_ws.argtypes = L.kda_chunk_fwd_varlen.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_noalloc.argtypes = L.kda_chunk_fwd.argtypes
+    L.kda_chunk_bwd_workspace_size.argtypes = [_I] * 5
+    L.kda_chunk_bwd_workspace_size.restype = _Z
+    L.kda_chunk_bwd.argtypes = ([_P] * 7 + [_F, _F] + [_P] * 11 + [_I] * 6 + [_P, _Z, _P])
     L.kda_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
                                     _I, _I, _P]
     L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
                                   _I, _I, _I, _I, _P]
     L.kda_device_error.argtypes = [_I]
     for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
-              "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_attention_fwd",
+              "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_chunk_bwd",
+              "kda_attention_fwd",
               "kda_decode_step", "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
     L.kda_status_string.argtypes = [_I]
@@ -207,6 +212,25 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
         float(scale), float(lower_bound), _ptr(initial_state), _ptr(out), _ptr(final_state),
         B, T, H, dk, dv, chunk, _dtype_code(q, dtype), _stream(stream)))
+
+
+def kda_chunk_bwd_workspace_size(B, T, H, dk, dv) -> int:
+    """Device workspace bytes kda_chunk_bwd needs."""
+    return int(lib().kda_chunk_bwd_workspace_size(B, T, H, dk, dv))
+
+
+def kda_chunk_bwd(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, initial_state,
+                  d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log, ddt_bias,
+                  d_initial_state, B, T, H, dk_dim, dv_dim, dtype=None, workspace=None,
+                  stream=None):
+    """Gradients of kda_chunk_fwd (see include/kda.h)."""
+    wp, wb = _ws(workspace)
+    _check("kda_chunk_bwd", lib().kda_chunk_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(initial_state), _ptr(d_out), _ptr(d_final_state),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta_logits), _ptr(da_log), _ptr(ddt_bias),
+        _ptr(d_initial_state), B, T, H, dk_dim, dv_dim, _dtype_code(q, dtype), wp, wb,
+        _stream(stream)))
 
 
 def kda_attention_fwd(query, key, value, beta, decay, initial_state, out, final_state, B, T, H,

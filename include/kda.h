@@ -169,6 +169,37 @@ int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
                           float* final_state, int B, int T, int H, int dk, int dv, int chunk,
                           int dtype, kda_stream_t stream);
 
+/*
+ * kda_chunk_bwd -- gradients of the kda_chunk_fwd forward (fixed-length sequences, decay
+ *   first) for L = <d_out, out> + <d_final_state, final_state>.  The pages give no backward
+ *   pass (the kernel_delta_attention page presents the chunked mode as the training path):
+ *   this is reverse-mode differentiation of the token recurrence, computed by a forward
+ *   scan that checkpoints the state every 64 tokens, a reverse scan that recomputes each
+ *   chunk's states from its checkpoint, and an elementwise pass for the norm, sigmoid and
+ *   gate chain rules.
+ *
+ *   Inputs: those of kda_chunk_fwd (q, k, v, g, beta_logits, a_log, dt_bias, scale,
+ *   lower_bound, initial_state; same layouts, dtype for q/k/v) and
+ *     d_out          [B, T, H, dv]   dtype, the output cotangent
+ *     d_final_state  [B, H, dk, dv]  fp32 or NULL (zero)
+ *   Outputs (caller-allocated, fully written):
+ *     dq, dk         [B, T, H, dk]   dtype          dv  [B, T, H, dv] dtype
+ *     dg             [B, T, H, dk]   fp32           dbeta_logits [B, T, H] fp32
+ *     da_log         [H] fp32        ddt_bias       [dk, H] fp32   (sums over B and T)
+ *     d_initial_state [B, H, dk, dv] fp32 or NULL (not wanted)
+ *   workspace / workspace_bytes: device scratch of at least kda_chunk_bwd_workspace_size()
+ *   bytes, 256-byte aligned (checkpoints, one chunk of states per (sequence, head) and
+ *   per-token fp32 intermediates).
+ */
+size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv);
+int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta_logits, const float* a_log, const float* dt_bias,
+                  float scale, float lower_bound, const float* initial_state, const void* d_out,
+                  const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                  float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
+                  int B, int T, int H, int dk_, int dv_, int dtype, void* workspace,
+                  size_t workspace_bytes, kda_stream_t stream);
+
 /* Options of kda_attention_fwd (bitwise OR). */
 enum kda_attention_flags {
   KDA_ATTN_NO_QK_L2NORM = 1,  /* use_qk_l2norm=False: q and k are used as given */

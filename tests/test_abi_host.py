@@ -200,3 +200,41 @@ def test_attention_without_device(L):
         pytest.skip("a GPU is present; this case is only meaningful without one")
     for flags in (0, 1, 2, 4, 7):
         assert _attn(L, flags=flags) == -9
+
+
+def test_backward_workspace_size_formula(L):
+    """Checkpoints every 64 tokens, one chunk of states per (sequence, head), three fp32
+    per-token [dk] intermediates and one fp32 per-token scalar, each 256-byte aligned."""
+    def al(x):
+        return (x + 255) // 256 * 256
+    B, T, H, dk, dv = 2, 150, 3, 128, 64
+    nck = (T + 63) // 64
+    want = (al(B * H * nck * dk * dv * 4) + al(B * H * 64 * dk * dv * 4) +
+            3 * al(B * T * H * dk * 4) + al(B * T * H * 4))
+    assert kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv) == want
+    assert kda.kda_chunk_bwd_workspace_size(B, T, H, 48, dv) == 0
+
+
+def _bwd(L, ws=0x100000, nbytes=1 << 40, **over):
+    a = dict(q=FAKE, dout=FAKE, dq=FAKE, dg=FAKE, B=1, T=64, H=2, dk=64, dv=64, dtype=1)
+    a.update(over)
+    return L.kda_chunk_bwd(a["q"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, -1.0, None,
+                           a["dout"], None, a["dq"], FAKE, FAKE, a["dg"], FAKE, FAKE, FAKE,
+                           None, a["B"], a["T"], a["H"], a["dk"], a["dv"], a["dtype"], ws,
+                           nbytes, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), -1), (dict(dout=None), -1), (dict(dq=None), -1), (dict(dg=None), -1),
+    (dict(B=-1), -2), (dict(dk=48), -3), (dict(dtype=2), -7), (dict(dq=FAKE + 4), -6),
+    (dict(ws=None), -12), (dict(nbytes=16), -12), (dict(ws=0x100000 + 64), -12),
+])
+def test_backward_rejects_bad_arguments(L, over, code):
+    assert _bwd(L, **over) == code
+
+
+def test_backward_without_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is only meaningful without one")
+    assert _bwd(L) == -9
