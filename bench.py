@@ -404,6 +404,50 @@ def e2e_measure(w, d, x, K, W):
     return e0.elapsed_time(e1), h2d, d2h
 
 
+def backward_measure(w, d, x, reps=3):
+    """kda_chunk_bwd on the prefill workload (inputs resident; d_out ~ N(0, 1), no final-state
+    cotangent): median time per call, and its algorithmic bytes (every input, cotangent and
+    gradient moved once) over that time."""
+    torch = _torch()
+    import gated_delta_rule_55_gb300 as kda
+    io = torch.bfloat16
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    r = np.random.default_rng(11)
+    dout = torch.from_numpy(r.standard_normal((B, T, H, dv), dtype=np.float32)).to("cuda", io)
+    g = {"dq": torch.empty(B, T, H, dk, device="cuda", dtype=io),
+         "dk": torch.empty(B, T, H, dk, device="cuda", dtype=io),
+         "dv": torch.empty(B, T, H, dv, device="cuda", dtype=io),
+         "dg": torch.empty(B, T, H, dk, device="cuda"),
+         "db": torch.empty(B, T, H, device="cuda"),
+         "da": torch.empty(H, device="cuda"), "ddt": torch.empty(dk, H, device="cuda")}
+    ws = torch.empty(kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"],
+                          x["dt_bias"], w.q_scale, w.lower_bound, x["initial_state"], dout, None,
+                          g["dq"], g["dk"], g["dv"], g["dg"], g["db"], g["da"], g["ddt"], None,
+                          B, T, H, dk, dv, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    times = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(reps):
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    per = (2 * dk + dv) * 2 + dk * 4 + 4 + dv * 2 + 2 * dk * 2 + dv * 2 + dk * 4 + 4
+    nbytes = B * T * H * per
+    return {"entry": "kda_chunk_bwd", "workload": w.name, "ms_per_call": ms,
+            "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": nbytes,
+            "hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "launches": 3,
+            "workspace_bytes": int(ws.numel())}
+
+
 def cpu_baseline(w, d, budget_s=12.0):
     """The fp64 oracle on a bounded sample of the workload: all (b, h) pairs, the first
     T_s tokens, T_s grown until the run takes a few seconds."""
@@ -502,6 +546,8 @@ def native(args):
                        "ms_per_step": ems / ke, "steps": ke,
                        "how": "pinned host buffers; upload, compute and download of "
                               "consecutive steps overlapped on three streams"}
+        line["backward"] = backward_measure(w, d, x)
+        line["backward"]["frac_of_hbm_peak"] = line["backward"]["hbm_gbs"] / pk["hbm_gbs"]
         line["cpu_baseline"] = cpu_baseline(w, d)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
