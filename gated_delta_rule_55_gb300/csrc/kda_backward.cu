@@ -20,14 +20,19 @@
 //   bwd_post_kernel     elementwise: the L2-norm, sigmoid and gate chain rules, and the
 //                       a_log / dt_bias sums (one atomic add per channel and token block).
 //
-// One CTA of 4 * dv threads per (sequence, head): thread (rg, j) owns column j on rows rg,
-// rg + 4, ...; the state and its adjoint stay in registers.
+// The value columns of the state are independent in the forward, so every scan runs on
+// 32-column slices: one CTA of 128 threads per (sequence, head, slice); thread (rg, j) owns
+// column j of the slice on rows rg, rg + 4, ...; the state and its adjoint stay in
+// registers.  Sums over all value columns (dq^, dk^, dgamma, dbeta) are written per slice
+// and added up by the elementwise pass.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kCK = 64;  // tokens per checkpoint interval
+constexpr int kCK = 64;   // tokens per checkpoint interval
+constexpr int kDVS = 32;  // value columns per CTA
+constexpr int kBT = 4 * kDVS;  // threads per scan CTA
 
 struct BwdArgs {
   ChunkArgs f;              // forward arguments (q, k, v, g, beta_logits, a_log, dt_bias, ...)
@@ -43,46 +48,68 @@ struct BwdArgs {
   float* d_initial;         // [B, H, dk, dv] or NULL
   float* ckpt;              // [B, H, nck, dk, dv]
   float* chunk_states;      // [B, H, kCK, dk, dv]
-  float* dqh;               // [B, T, H, dk] gradient w.r.t. q^ (scale included in q^)
-  float* dkh;               // [B, T, H, dk]
-  float* dgam;              // [B, T, H, dk] gradient w.r.t. gamma
-  float* dbeta;             // [B, T, H] gradient w.r.t. beta
+  float* dqh;               // [ns][B, T, H, dk] per-slice gradient w.r.t. q^ (scale in q^)
+  float* dkh;               // [ns][B, T, H, dk]
+  float* dgam;              // [ns][B, T, H, dk] gradient w.r.t. gamma
+  float* dbeta;             // [ns][B, T, H] gradient w.r.t. beta
+  long long rows;           // B * T * H
   int nck;
+  int ns;                   // value-column slices (dv / 32)
 };
 
 // Per-token quantities shared by the CTA: normalised k and q, decay, v, beta.
-template <int DK, int DV>
+template <int DK>
 struct TokenSmem {
   float k[DK], q[DK], d[DK];
-  float v[DV], dout[DV];
+  float v[kDVS], dout[kDVS];
   float part[3][4];
   float beta;
 };
 
-// Loads token t of (seq, h) into shared memory: k^, q^ (scale folded), e^{gamma}, v,
-// d_out, beta.  Threads tid < DK own channel tid.  Ends with a barrier.
-template <typename Tin, int DK, int DV>
-__device__ void load_token(const BwdArgs& b, long long row, TokenSmem<DK, DV>& s, int tid,
-                           float exp_a, float db, bool want_q) {
+// A token's raw inputs in registers (loaded one step ahead): channel tid of k, q and g
+// (tid < DK), column j0 + tid of v and d_out (tid < 32), the beta logit (thread 0).
+struct TokenRegs {
+  float k, q, g, v, dout, blog;
+};
+
+template <typename Tin, int DK>
+__device__ __forceinline__ TokenRegs fetch_token(const BwdArgs& b, long long row, int tid, int j0,
+                                                 bool want_q) {
   const ChunkArgs& a = b.f;
-  const int lane = tid & 31, w = tid >> 5;
-  float xk = 0.f, xq = 0.f;
+  const int DV = a.dv;
+  TokenRegs r{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (tid < DK) {
-    xk = load_as_float(static_cast<const Tin*>(a.k) + row * DK + tid);
-    if (want_q) xq = load_as_float(static_cast<const Tin*>(a.q) + row * DK + tid);
-    const float gamma = gate_gamma(a.g[row * DK + tid], db, exp_a, a.lower_bound);
-    s.d[tid] = expf(gamma);
-    const float kk = warp_sum(xk * xk), qq = warp_sum(xq * xq);
+    r.k = load_as_float(static_cast<const Tin*>(a.k) + row * DK + tid);
+    if (want_q) r.q = load_as_float(static_cast<const Tin*>(a.q) + row * DK + tid);
+    r.g = a.g[row * DK + tid];
+  }
+  if (tid < kDVS) {
+    r.v = load_as_float(static_cast<const Tin*>(a.v) + row * DV + j0 + tid);
+    if (want_q) r.dout = load_as_float(static_cast<const Tin*>(b.d_out) + row * DV + j0 + tid);
+  }
+  if (tid == 0) r.blog = a.beta_logits[row];
+  return r;
+}
+
+// Stages a fetched token in shared memory: k^, q^ (scale folded), e^{gamma}, this slice's
+// v and d_out, beta.  Threads tid < DK own channel tid.  Ends with a barrier.
+template <int DK>
+__device__ void stage_token(const ChunkArgs& a, const TokenRegs& r, TokenSmem<DK>& s, int tid,
+                            float exp_a, float db) {
+  const int lane = tid & 31, w = tid >> 5;
+  if (tid < DK) {
+    s.d[tid] = expf(gate_gamma(r.g, db, exp_a, a.lower_bound));
+    const float kk = warp_sum(r.k * r.k), qq = warp_sum(r.q * r.q);
     if (lane == 0) {
       s.part[0][w] = kk;
       s.part[1][w] = qq;
     }
   }
-  if (tid < DV) {
-    s.v[tid] = load_as_float(static_cast<const Tin*>(a.v) + row * DV + tid);
-    if (want_q) s.dout[tid] = load_as_float(static_cast<const Tin*>(b.d_out) + row * DV + tid);
+  if (tid < kDVS) {
+    s.v[tid] = r.v;
+    s.dout[tid] = r.dout;
   }
-  if (tid == 0) s.beta = sigmoidf_(a.beta_logits[row]);
+  if (tid == 0) s.beta = sigmoidf_(r.blog);
   __syncthreads();
   if (tid < DK) {
     float kk = 0.f, qq = 0.f;
@@ -91,16 +118,16 @@ __device__ void load_token(const BwdArgs& b, long long row, TokenSmem<DK, DV>& s
       kk += s.part[0][i];
       qq += s.part[1][i];
     }
-    s.k[tid] = xk * rsqrtf(kk + kL2Eps);
-    s.q[tid] = xq * a.scale * rsqrtf(qq + kL2Eps);
+    s.k[tid] = r.k * rsqrtf(kk + kL2Eps);
+    s.q[tid] = r.q * a.scale * rsqrtf(qq + kL2Eps);
   }
   __syncthreads();
 }
 
-// One forward token step on the register state S (rows rg + 4 i of column j):
-// S <- D S + k^ u^T with u = beta (v - (D S)^T k^).  Uses red[4][DV].
-template <int DK, int DV>
-__device__ void forward_step(float (&S)[DK / 4], const TokenSmem<DK, DV>& s, float (*red)[DV],
+// One forward token step on the register state S (rows rg + 4 i of slice column j):
+// S <- D S + k^ u^T with u = beta (v - (D S)^T k^).  Uses red[4][kDVS].
+template <int DK>
+__device__ void forward_step(float (&S)[DK / 4], const TokenSmem<DK>& s, float (*red)[kDVS],
                              int rg, int j) {
   constexpr int RPT = DK / 4;
   float p = 0.f;
@@ -118,14 +145,14 @@ __device__ void forward_step(float (&S)[DK / 4], const TokenSmem<DK, DV>& s, flo
   __syncthreads();  // red[] is rewritten by the next step
 }
 
-template <typename Tin, int DK, int DV>
-__global__ void __launch_bounds__(4 * DV) bwd_forward_kernel(BwdArgs b) {
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(kBT) bwd_forward_kernel(BwdArgs b) {
   constexpr int RPT = DK / 4;
-  __shared__ TokenSmem<DK, DV> s;
-  __shared__ float red[4][DV];
+  __shared__ TokenSmem<DK> s;
+  __shared__ float red[4][kDVS];
   const ChunkArgs& a = b.f;
-  const int tid = threadIdx.x, rg = tid / DV, j = tid % DV;
-  const int h = blockIdx.x, seq = blockIdx.y, H = a.H;
+  const int tid = threadIdx.x, rg = tid / kDVS, j = tid % kDVS;
+  const int j0 = blockIdx.x * kDVS, h = blockIdx.y, seq = blockIdx.z, H = a.H, DV = a.dv;
   long long bos;
   int len;
   seq_range(a, seq, bos, len);
@@ -135,15 +162,18 @@ __global__ void __launch_bounds__(4 * DV) bwd_forward_kernel(BwdArgs b) {
   float S[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
-    S[i] = a.initial_state ? a.initial_state[sh * DK * DV + (rg + 4 * i) * DV + j] : 0.f;
+    S[i] = a.initial_state ? a.initial_state[sh * DK * DV + (rg + 4 * i) * DV + j0 + j] : 0.f;
+  TokenRegs nx = len > 0 ? fetch_token<Tin, DK>(b, bos * H + h, tid, j0, false) : TokenRegs{};
   for (int t = 0; t < len; ++t) {
     if (t % kCK == 0) {
-      float* cp = b.ckpt + (sh * b.nck + t / kCK) * DK * DV;
+      float* cp = b.ckpt + (sh * b.nck + t / kCK) * DK * DV + j0 + j;
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) cp[(rg + 4 * i) * DV + j] = S[i];
+      for (int i = 0; i < RPT; ++i) cp[(rg + 4 * i) * DV] = S[i];
     }
-    load_token<Tin, DK, DV>(b, (bos + t) * H + h, s, tid, exp_a, db, false);
-    forward_step<DK, DV>(S, s, red, rg, j);
+    const TokenRegs cur = nx;
+    if (t + 1 < len) nx = fetch_token<Tin, DK>(b, (bos + t + 1) * H + h, tid, j0, false);
+    stage_token<DK>(a, cur, s, tid, exp_a, db);
+    forward_step<DK>(S, s, red, rg, j);
   }
 }
 
@@ -178,30 +208,30 @@ __device__ __forceinline__ bool row_writer(int lane) {
   return (lane & (32 / RPT - 1)) == 0;
 }
 
-template <typename Tin, int DK, int DV>
-__global__ void __launch_bounds__(4 * DV) bwd_scan_kernel(BwdArgs b) {
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(kBT) bwd_scan_kernel(BwdArgs b) {
   constexpr int RPT = DK / 4;
-  constexpr int WPG = DV / 32;  // warps per row group
-  __shared__ TokenSmem<DK, DV> s;
-  __shared__ float red[4][DV];
-  __shared__ float jred[3][WPG][DK];
-  __shared__ float bred[4 * DV / 32];
+  __shared__ TokenSmem<DK> s;
+  __shared__ float red[4][kDVS];
+  __shared__ float bred[4];
   const ChunkArgs& a = b.f;
-  const int tid = threadIdx.x, lane = tid & 31, rg = tid / DV, j = tid % DV;
-  const int wig = j >> 5;  // warp index inside the row group
-  const int h = blockIdx.x, seq = blockIdx.y, H = a.H;
+  const int tid = threadIdx.x, lane = tid & 31, rg = tid / kDVS, j = tid % kDVS;
+  const int slice = blockIdx.x, j0 = slice * kDVS, h = blockIdx.y, seq = blockIdx.z;
+  const int H = a.H, DV = a.dv;
   long long bos;
   int len;
   seq_range(a, seq, bos, len);
   const long long sh = (long long)seq * H + h;
   const float exp_a = tid < DK ? expf(a.a_log[h]) : 0.f;
   const float db = tid < DK ? a.dt_bias[tid * H + h] : 0.f;
-  float* const cs = b.chunk_states + sh * kCK * DK * DV;
+  // this CTA's chunk scratch: [kCK][DK][kDVS]
+  float* const cs = b.chunk_states + (sh * b.ns + slice) * kCK * DK * kDVS;
+  const long long pofs = (long long)slice * b.rows;  // offset of this slice's partials
 
   float dS[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
-    dS[i] = b.d_final ? b.d_final[sh * DK * DV + (rg + 4 * i) * DV + j] : 0.f;
+    dS[i] = b.d_final ? b.d_final[sh * DK * DV + (rg + 4 * i) * DV + j0 + j] : 0.f;
 
   const int nck = (len + kCK - 1) / kCK;
   for (int ck = nck - 1; ck >= 0; --ck) {
@@ -209,32 +239,50 @@ __global__ void __launch_bounds__(4 * DV) bwd_scan_kernel(BwdArgs b) {
     // recompute the chunk's pre-token states from its checkpoint
     {
       float S[RPT];
-      const float* cp = b.ckpt + (sh * b.nck + ck) * DK * DV;
+      const float* cp = b.ckpt + (sh * b.nck + ck) * DK * DV + j0 + j;
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) S[i] = cp[(rg + 4 * i) * DV + j];
+      for (int i = 0; i < RPT; ++i) S[i] = cp[(rg + 4 * i) * DV];
+      TokenRegs nx = fetch_token<Tin, DK>(b, (bos + t0) * H + h, tid, j0, false);
       for (int t = t0; t < t1; ++t) {
-        float* dst = cs + (t - t0) * DK * DV;
+        float* dst = cs + (t - t0) * DK * kDVS + j;
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) dst[(rg + 4 * i) * DV + j] = S[i];
+        for (int i = 0; i < RPT; ++i) dst[(rg + 4 * i) * kDVS] = S[i];
         if (t + 1 < t1) {  // the last token's own update is not needed
-          load_token<Tin, DK, DV>(b, (bos + t) * H + h, s, tid, exp_a, db, false);
-          forward_step<DK, DV>(S, s, red, rg, j);
+          const TokenRegs cur = nx;
+          if (t + 2 < t1) nx = fetch_token<Tin, DK>(b, (bos + t + 1) * H + h, tid, j0, false);
+          stage_token<DK>(a, cur, s, tid, exp_a, db);
+          forward_step<DK>(S, s, red, rg, j);
         }
       }
     }
     __syncthreads();
-    // walk the chunk backwards
+    // walk the chunk backwards; the next (earlier) token's inputs and pre-token state are
+    // loaded into registers while the current one is processed
+    TokenRegs nx = fetch_token<Tin, DK>(b, (bos + t1 - 1) * H + h, tid, j0, true);
+    float Sn[RPT];
+    {
+      const float* src = cs + (t1 - 1 - t0) * DK * kDVS + j;
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) Sn[i] = src[(rg + 4 * i) * kDVS];
+    }
     for (int t = t1 - 1; t >= t0; --t) {
       const long long row = (bos + t) * H + h;
-      load_token<Tin, DK, DV>(b, row, s, tid, exp_a, db, true);
-      // the pre-token state S is re-read from the chunk scratch (L1-resident: each thread
-      // reads back what it wrote) instead of being held in registers
-      const float* src = cs + (t - t0) * DK * DV + j;
+      const TokenRegs cur = nx;
+      float Sp[RPT];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) Sp[i] = Sn[i];
+      if (t > t0) {
+        nx = fetch_token<Tin, DK>(b, row - H, tid, j0, true);
+        const float* src = cs + (t - 1 - t0) * DK * kDVS + j;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) Sn[i] = src[(rg + 4 * i) * kDVS];
+      }
+      stage_token<DK>(a, cur, s, tid, exp_a, db);
       float p = 0.f;
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int c = rg + 4 * i;
-        p += s.d[c] * src[c * DV] * s.k[c];
+        p += s.d[c] * Sp[i] * s.k[c];
       }
       red[rg][j] = p;
       __syncthreads();
@@ -255,66 +303,52 @@ __global__ void __launch_bounds__(4 * DV) bwd_scan_kernel(BwdArgs b) {
       __syncthreads();
       const float du = red[0][j] + red[1][j] + red[2][j] + red[3][j];
       const float dp = -s.beta * du;
-      // per-row partial products of this column, reduced over the columns one at a time:
+      // per-row partial products over this slice's columns, reduced across the warp's 32
+      // lanes (= the slice's columns):
       //   dq^_c = sum_j S_new[c][j] do_j,  dk^_c = sum_j (dS u + S' dp),
       //   dgamma_c / d_c = sum_j dS'[c][j] S[c][j]   (then dS <- D dS')
       float x[RPT];
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int c = rg + 4 * i;
-        x[i] = (s.d[c] * src[c * DV] + s.k[c] * u) * doj;
+        x[i] = (s.d[c] * Sp[i] + s.k[c] * u) * doj;
       }
       warp_reduce_scatter<RPT>(x, lane);
-      if (row_writer<RPT>(lane)) jred[0][wig][rg + 4 * row_of_lane<RPT>(lane)] = x[0];
+      if (row_writer<RPT>(lane))
+        b.dqh[(pofs + row) * DK + rg + 4 * row_of_lane<RPT>(lane)] = x[0];
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int c = rg + 4 * i;
-        x[i] = dS[i] * u + s.d[c] * src[c * DV] * dp;
+        x[i] = dS[i] * u + s.d[c] * Sp[i] * dp;
       }
       warp_reduce_scatter<RPT>(x, lane);
-      if (row_writer<RPT>(lane)) jred[1][wig][rg + 4 * row_of_lane<RPT>(lane)] = x[0];
+      if (row_writer<RPT>(lane))
+        b.dkh[(pofs + row) * DK + rg + 4 * row_of_lane<RPT>(lane)] = x[0];
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int c = rg + 4 * i;
         const float dSd = dS[i] + s.k[c] * dp;  // dS'
-        x[i] = dSd * src[c * DV];
+        x[i] = dSd * Sp[i];
         dS[i] = s.d[c] * dSd;                   // adjoint of the previous state
       }
       warp_reduce_scatter<RPT>(x, lane);
-      if (row_writer<RPT>(lane)) jred[2][wig][rg + 4 * row_of_lane<RPT>(lane)] = x[0];
-      // dv and the dbeta partials (row group 0 holds one copy of every column)
-      float dbp = 0.f;
+      if (row_writer<RPT>(lane)) {
+        const int c = rg + 4 * row_of_lane<RPT>(lane);
+        b.dgam[(pofs + row) * DK + c] = x[0] * s.d[c];
+      }
+      // dv and the dbeta partial (row group 0 holds one copy of every slice column)
       if (rg == 0) {
-        store_from_float(static_cast<Tin*>(b.dv) + row * DV + j, s.beta * du);
-        dbp = du * vmp;
+        store_from_float(static_cast<Tin*>(b.dv) + row * DV + j0 + j, s.beta * du);
+        const float dbp = warp_sum(du * vmp);
+        if (lane == 0) b.dbeta[pofs + row] = dbp;
       }
-      dbp = warp_sum(dbp);
-      if (lane == 0) bred[tid >> 5] = dbp;
-      __syncthreads();
-      if (tid < DK) {
-        float q_ = 0.f, k_ = 0.f, g_ = 0.f;
-#pragma unroll
-        for (int w = 0; w < WPG; ++w) {
-          q_ += jred[0][w][tid];
-          k_ += jred[1][w][tid];
-          g_ += jred[2][w][tid];
-        }
-        b.dqh[row * DK + tid] = q_;
-        b.dkh[row * DK + tid] = k_;
-        b.dgam[row * DK + tid] = g_ * s.d[tid];
-      }
-      if (tid == 0) {
-        float t_ = 0.f;
-#pragma unroll
-        for (int w = 0; w < WPG; ++w) t_ += bred[w];
-        b.dbeta[row] = t_;
-      }
-      __syncthreads();  // shared token data, red[] and jred[] are rewritten next token
+      __syncthreads();  // shared token data and red[] are rewritten by the next token
     }
   }
   if (b.d_initial) {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) b.d_initial[sh * DK * DV + (rg + 4 * i) * DV + j] = dS[i];
+    for (int i = 0; i < RPT; ++i)
+      b.d_initial[sh * DK * DV + (rg + 4 * i) * DV + j0 + j] = dS[i];
   }
 }
 
@@ -351,8 +385,13 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(BwdArgs b) {
       const int c = lane + 32 * m;
       qv[m] = load_as_float(static_cast<const Tin*>(a.q) + row * DK + c);
       kv[m] = load_as_float(static_cast<const Tin*>(a.k) + row * DK + c);
-      dq[m] = a.scale * b.dqh[row * DK + c];
-      dk[m] = b.dkh[row * DK + c];
+      float sq = 0.f, sk = 0.f;
+      for (int sl = 0; sl < b.ns; ++sl) {
+        sq += b.dqh[(sl * b.rows + row) * DK + c];
+        sk += b.dkh[(sl * b.rows + row) * DK + c];
+      }
+      dq[m] = a.scale * sq;
+      dk[m] = sk;
       qq += qv[m] * qv[m];
       kk += kv[m] * kv[m];
       qd += qv[m] * dq[m];
@@ -370,14 +409,18 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(BwdArgs b) {
       // gamma = lb sigmoid(z), z = e^{a_log} (g + dt_bias)
       const float z = ea * (a.g[row * DK + c] + db[m]);
       const float sz = sigmoidf_(z);
-      const float dz = b.dgam[row * DK + c] * a.lower_bound * sz * (1.f - sz);
+      float dgm = 0.f;
+      for (int sl = 0; sl < b.ns; ++sl) dgm += b.dgam[(sl * b.rows + row) * DK + c];
+      const float dz = dgm * a.lower_bound * sz * (1.f - sz);
       b.dg[row * DK + c] = dz * ea;
       acc_b[m] += dz * ea;
       acc_a += dz * z;
     }
     if (lane == 0) {
       const float beta = sigmoidf_(a.beta_logits[row]);
-      b.dbeta_logits[row] = b.dbeta[row] * beta * (1.f - beta);
+      float dbt = 0.f;
+      for (int sl = 0; sl < b.ns; ++sl) dbt += b.dbeta[sl * b.rows + row];
+      b.dbeta_logits[row] = dbt * beta * (1.f - beta);
     }
   }
 #pragma unroll
@@ -386,35 +429,26 @@ __global__ void __launch_bounds__(128) bwd_post_kernel(BwdArgs b) {
   if (lane == 0) atomicAdd(&b.da_log[h], acc_a);
 }
 
-template <typename Tin, int DK, int DV>
+template <typename Tin, int DK>
 cudaError_t launch_t(const BwdArgs& b, cudaStream_t st) {
   const ChunkArgs& a = b.f;
-  const dim3 grid(a.H, a.B);
-  bwd_forward_kernel<Tin, DK, DV><<<grid, 4 * DV, 0, st>>>(b);
+  const dim3 grid(b.ns, a.H, a.B);
+  bwd_forward_kernel<Tin, DK><<<grid, kBT, 0, st>>>(b);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_scan_kernel<Tin, DK, DV><<<grid, 4 * DV, 0, st>>>(b);
+  bwd_scan_kernel<Tin, DK><<<grid, kBT, 0, st>>>(b);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const dim3 pgrid(a.H, (a.T + kPostTok - 1) / kPostTok, a.B);
   if (a.T > 0) bwd_post_kernel<Tin, DK><<<pgrid, 128, 0, st>>>(b);
   return cudaGetLastError();
 }
 
-template <typename Tin, int DK>
-cudaError_t launch_dk(const BwdArgs& b, cudaStream_t st) {
-  switch (b.f.dv) {
-    case 32: return launch_t<Tin, DK, 32>(b, st);
-    case 64: return launch_t<Tin, DK, 64>(b, st);
-    default: return launch_t<Tin, DK, 128>(b, st);
-  }
-}
-
 template <typename Tin>
 cudaError_t launch_dtype(const BwdArgs& b, cudaStream_t st) {
   switch (b.f.dk) {
-    case 32: return launch_dk<Tin, 32>(b, st);
-    case 64: return launch_dk<Tin, 64>(b, st);
-    default: return launch_dk<Tin, 128>(b, st);
+    case 32: return launch_t<Tin, 32>(b, st);
+    case 64: return launch_t<Tin, 64>(b, st);
+    default: return launch_t<Tin, 128>(b, st);
   }
 }
 
@@ -425,9 +459,9 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 size_t backward_workspace(int B, int T, int H, int dk, int dv) {
   const size_t nck = (size_t)(T + kCK - 1) / kCK;
   const size_t st = (size_t)dk * dv * 4;
-  const size_t rows = (size_t)B * T * H;
+  const size_t rows = (size_t)B * T * H, ns = (size_t)dv / kDVS;
   return align256((size_t)B * H * nck * st) + align256((size_t)B * H * kCK * st) +
-         3 * align256(rows * dk * 4) + align256(rows * 4);
+         3 * align256(ns * rows * dk * 4) + align256(ns * rows * 4);
 }
 
 cudaError_t launch_backward(const ChunkArgs& f, const void* d_out, const float* d_final,
@@ -440,19 +474,21 @@ cudaError_t launch_backward(const ChunkArgs& f, const void* d_out, const float* 
   b.dq = dq; b.dk = dk; b.dv = dv; b.dg = dg; b.dbeta_logits = dbeta_logits;
   b.da_log = da_log; b.ddt_bias = ddt_bias; b.d_initial = d_initial;
   b.nck = (f.T + kCK - 1) / kCK;
+  b.ns = f.dv / kDVS;
   const size_t st_bytes = (size_t)f.dk * f.dv * 4;
   const size_t rows = (size_t)f.B * f.T * f.H;
+  b.rows = (long long)rows;
   uint8_t* p = static_cast<uint8_t*>(workspace);
   b.ckpt = reinterpret_cast<float*>(p);
   p += align256((size_t)f.B * f.H * b.nck * st_bytes);
   b.chunk_states = reinterpret_cast<float*>(p);
   p += align256((size_t)f.B * f.H * kCK * st_bytes);
   b.dqh = reinterpret_cast<float*>(p);
-  p += align256(rows * f.dk * 4);
+  p += align256(b.ns * rows * f.dk * 4);
   b.dkh = reinterpret_cast<float*>(p);
-  p += align256(rows * f.dk * 4);
+  p += align256(b.ns * rows * f.dk * 4);
   b.dgam = reinterpret_cast<float*>(p);
-  p += align256(rows * f.dk * 4);
+  p += align256(b.ns * rows * f.dk * 4);
   b.dbeta = reinterpret_cast<float*>(p);
   cudaError_t e = cudaMemsetAsync(da_log, 0, sizeof(float) * f.H, st);
   if (e != cudaSuccess) return e;

@@ -203,14 +203,15 @@ def test_attention_without_device(L):
 
 
 def test_backward_workspace_size_formula(L):
-    """Checkpoints every 64 tokens, one chunk of states per (sequence, head), three fp32
-    per-token [dk] intermediates and one fp32 per-token scalar, each 256-byte aligned."""
+    """Checkpoints every 64 tokens, one chunk of states per (sequence, head), and per
+    32-column value slice three fp32 per-token [dk] partial sums and one fp32 per-token
+    scalar, each region 256-byte aligned."""
     def al(x):
         return (x + 255) // 256 * 256
     B, T, H, dk, dv = 2, 150, 3, 128, 64
-    nck = (T + 63) // 64
+    nck, ns = (T + 63) // 64, dv // 32
     want = (al(B * H * nck * dk * dv * 4) + al(B * H * 64 * dk * dv * 4) +
-            3 * al(B * T * H * dk * 4) + al(B * T * H * 4))
+            3 * al(ns * B * T * H * dk * 4) + al(ns * B * T * H * 4))
     assert kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv) == want
     assert kda.kda_chunk_bwd_workspace_size(B, T, H, 48, dv) == 0
 
