@@ -80,6 +80,15 @@ constexpr int P_TW = P_T + 8192;        // T diag(rk)
 constexpr int P_W = P_TW + 8192;        // -W [64 x 128] staging for the record store
 static_assert(P_Y + 4 * 16 * LDY * 4 <= P_T, "solve scratch overlaps T");
 static_assert(P_W + 16384 <= P_KTT, "re-used tiles must stay inside Xl/Kb");
+// Staging of the NEXT record's raw inputs (TMA), in tiles that are free from the end of
+// MMA2 until the next record's operand build: v and g inside the solve area, q and k in
+// the K~^T / V^T tiles.  None overlaps the -W staging tile of the record phase.
+constexpr int ST_V = 0;                 // v [64 tok x 128] bf16, two SW128 boxes
+constexpr int ST_G = 16384;             // g [4 quarters][64 tok][32] fp32, no swizzle
+constexpr int ST_Q = P_KTT;             // q, two SW128 boxes
+constexpr int ST_K = P_VT;              // k
+constexpr uint32_t kStageBytes = 3 * 16384 + 32768;
+static_assert(ST_G + 32768 <= P_W, "staging overlaps the -W tile");
 constexpr size_t kPSmem = P_END + 1024;
 
 // Tensor Memory of the prep kernel (256 columns: two CTAs per SM).
@@ -91,7 +100,11 @@ constexpr uint32_t kPTmemCols = 256;
 __device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split path gave up
 
 __global__ void __launch_bounds__(kPThreads, 2)
-    chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qw, const ChunkArgs a,
+    chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qw,
+                      const __grid_constant__ CUtensorMap map_q,
+                      const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v,
+                      const __grid_constant__ CUtensorMap map_g, const ChunkArgs a,
                       const Ws ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -102,7 +115,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
   __shared__ __align__(16) float s_dec[kD];
   __shared__ __align__(16) float s_gtot[4][kD];
   __shared__ __align__(16) float s_qq[2][kC];
-  __shared__ uint64_t bar_mma;
+  __shared__ uint64_t bar_mma, bar_ld;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
 
@@ -144,16 +157,17 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tok0_ = bos + (long long)jc * kC;
     return true;
   };
-  // L2 prefetch of a record's q / k / v / g rows (thread t: tensor t / 64, token t % 64)
-  auto prefetch = [&](int h_, long long tok0_, int n_) {
-    const int t = tid & 63, which = tid >> 6;
-    if (t >= n_) return;
-    const long long row = (tok0_ + t) * H + h_;
-    if (which == 3)
-      prefetch_l2(a.g + row * kD, kD * 4);
-    else
-      prefetch_l2(static_cast<const __nv_bfloat16*>(which == 0 ? a.q : which == 1 ? a.k : a.v) +
-                      row * kD, kD * 2);
+  // a record's raw q / k / v / g tiles into the staging area (one thread)
+  auto stage = [&](int h_, long long tok0_) {
+    mbar_arrive_expect_tx(&bar_ld, kStageBytes);
+    const int r0 = (int)tok0_;
+    for (int half = 0; half < 2; ++half) {
+      tma_load_3d(sm + ST_Q + half * 8192, &map_q, &bar_ld, 64 * half, h_, r0);
+      tma_load_3d(sm + ST_K + half * 8192, &map_k, &bar_ld, 64 * half, h_, r0);
+      tma_load_3d(sm + ST_V + half * 8192, &map_v, &bar_ld, 64 * half, h_, r0);
+    }
+    for (int qtr = 0; qtr < 4; ++qtr)
+      tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, r0);
   };
 
   if (warp == 0) {
@@ -162,7 +176,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
   }
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_ld, 1);
     fence_mbar_init();
+    tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_g);
   }
   tc_fence_before();
   __syncthreads();
@@ -183,30 +202,57 @@ __global__ void __launch_bounds__(kPThreads, 2)
   int h, n, h_next = 0, n_next = 0;
   long long tok0, tok0_next = 0;
   bool have = locate(blockIdx.x, h, tok0, n);
+  if (have && tid == 0) stage(h, tok0);
+  uint32_t ld_parity = 0;
+  bool ld_pending = have;  // a staging batch was issued and not yet waited for
+  // element (row 16 R + i, channel c0) of a [64 x 128] bf16 tile of two SW128 boxes:
+  //   (c0 / 64) * 8192 + 2 R * 1024 + swz(i)
+  const uint32_t c_kb = uint32_t(c0 >> 6);
+  const uint32_t c_chunk = uint32_t(((c0 & 63) * 2) >> 4);
+  const uint32_t c_byte = uint32_t(((c0 & 63) * 2) & 15);
+  auto swz = [&](int i) -> uint32_t {
+    return uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
+           (((c_chunk ^ uint32_t(i & 7)) << 4) | c_byte);
+  };
+  const uint32_t tile_base = c_kb * 8192u + uint32_t(R) * 2048u;
+  float blog = (have && tid < n) ? a.beta_logits[(tok0 + tid) * H + h] : 0.f;  // tid < 64
   for (long long rec = blockIdx.x; have; rec += gridDim.x) {
-    // the next record's rows start moving into L2 while this one is computed
     const bool have_next = locate(rec + gridDim.x, h_next, tok0_next, n_next);
-    if (have_next) prefetch(h_next, tok0_next, n_next);
 
-    // ---- loads: raw gates, beta logit, v / k / q words of (16 tokens, channels c0, c0 + 1)
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v);
+    // ---- loads: this record's staged tiles; raw gates, v / k / q words of (16 tokens,
+    //      channels c0, c0 + 1)
+    {
+      const uint32_t slot_w = wait_calls++ & 1;
+      if (tid == 0) s_wait_ok[slot_w] = mbar_wait(&bar_ld, ld_parity) ? 1 : 0;
+      __syncthreads();
+      if (!s_wait_ok[slot_w]) { ok = false; break; }
+      ld_pending = false;
+      ld_parity ^= 1u;
+    }
     float2 graw[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int t = 16 * R + i;
-      graw[i] = (t < n) ? *reinterpret_cast<const float2*>(a.g + ((tok0 + t) * H + h) * kD + c0)
+      graw[i] = (t < n) ? *reinterpret_cast<const float2*>(sm + ST_G + (c0 >> 5) * 8192 +
+                                                             t * 128 + (c0 & 31) * 4)
                         : make_float2(0.f, 0.f);
     }
-    const float blog = (tid < n) ? a.beta_logits[(tok0 + tid) * H + h] : 0.f;  // tid < 64 only
     uint32_t vw[16];
 #pragma unroll
+    for (int i = 0; i < 16; ++i)
+      vw[i] = (16 * R + i < n)
+                  ? *reinterpret_cast<const uint32_t*>(sm + ST_V + tile_base + swz(i))
+                  : 0u;
+    uint32_t kw[16], qw[16];
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int t = 16 * R + i;
-      vw[i] = (t < n) ? *reinterpret_cast<const uint32_t*>(vg + ((tok0 + t) * H + h) * kD + c0)
-                      : 0u;
+      const bool live = 16 * R + i < n;
+      kw[i] = live ? *reinterpret_cast<const uint32_t*>(sm + ST_K + tile_base + swz(i)) : 0u;
+      qw[i] = live ? *reinterpret_cast<const uint32_t*>(sm + ST_Q + tile_base + swz(i)) : 0u;
     }
+    // every staged word is in registers before the V^T tile (which shares space with the
+    // staged k) is written
+    __syncthreads();
 
     // V^T tile (rows = channels, tokens contiguous): row c0 takes the low halves, row c0 + 1
     // the high halves; lanes 4..7 of every 8-lane group write row c0 + 1 first so that one
@@ -223,14 +269,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
     store_t8(P_VT, vw, 2 * R);
     store_t8(P_VT, vw + 8, 2 * R + 1);
 
-    uint32_t kw[16], qw[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = 16 * R + i;
-      const long long off = ((tok0 + t) * H + h) * kD + c0;
-      kw[i] = (t < n) ? *reinterpret_cast<const uint32_t*>(kg + off) : 0u;
-      qw[i] = (t < n) ? *reinterpret_cast<const uint32_t*>(qg + off) : 0u;
-    }
 
     // ---- gate prefix over this thread's sub-chunk, beta
     const float exp_a = __expf(a.a_log[h]);
@@ -315,9 +353,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
                      c32 = pack_bf16(cR0[3], cR1[3]);
       // element (row 16 R + i, channel c0) of a K-major SW128 tile with `rows` rows:
       //   (c0 / 64) * rows * 128 + 2 R * 1024 + sw[i]
-      const uint32_t c_kb = uint32_t(c0 >> 6);
-      const uint32_t c_chunk = uint32_t(((c0 & 63) * 2) >> 4);
-      const uint32_t c_byte = uint32_t(((c0 & 63) * 2) & 15);
       uint8_t* const p128 = sm + P_XL + c_kb * 16384u + uint32_t(R) * 2048u;
       uint8_t* const p160 = sm + P_KB + c_kb * 20480u + uint32_t(R) * 2048u;
       __nv_bfloat16* const qrec = ws.qw + (rec * 64 + 16 * R) * kD + c0;  // Q~ row 16 R
@@ -516,6 +551,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
+    // every tile the staging area reuses is free now (MMA2 was their last reader)
+    if (have_next) {
+      if (tid == 0) stage(h_next, tok0_next);
+      ld_pending = true;
+    }
 
     // ---- records: -W (through a swizzled staging tile and one bulk-tensor store) and U~^T
     //      (thread j = ln writes its own row); thread (ln, wg) holds tokens 32 wg .. + 31
@@ -554,10 +594,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tok0 = tok0_next;
     n = n_next;
     have = have_next;
+    blog = (have && tid < n) ? a.beta_logits[(tok0 + tid) * H + h] : 0.f;
   }
 
   if (!ok) {
-    if (tid == 0) atomicOr(&g_split_error, 2u);
+    if (tid == 0) {
+      atomicOr(&g_split_error, 2u);
+      if (ld_pending) mbar_wait(&bar_ld, ld_parity, 1000000000ull);  // staging in flight
+    }
     mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
   }
   if (tid == 0) bulk_wait_read_all();  // the last staging tile is read before exit
@@ -919,6 +963,23 @@ bool make_map_out(CUtensorMap* m, const void* base, long long rows, int H) {
          CUDA_SUCCESS;
 }
 
+// [rows, H, 128] inputs, box {64 ch, 1 head, 64 tokens} bf16 with 128-byte swizzle, or
+// {32 ch, 1, 64} fp32 without swizzle; rows past the end read as zeros.
+bool make_map_in(CUtensorMap* m, const void* base, long long rows, int H, bool fp32) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const int es = fp32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * es, (cuuint64_t)H * kD * es};
+  cuuint32_t box[3] = {fp32 ? 32u : 64u, 1, 64};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             fp32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 bool carve(const ChunkArgs& a, void* base, Ws& ws) {
   const long long slots = slots_for(a);
   const long long recs = slots * a.H;
@@ -956,11 +1017,14 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t
   const long long rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
   const long long map_rows = rows > 0 ? rows : 1;
   const long long rec_rows = ws.recs > 0 ? ws.recs : 1;
-  CUtensorMap mqw, mku, mm, mo;
+  CUtensorMap mqw, mku, mm, mo, mq, mk, mv, mg;
   if (!make_map_2d(&mqw, ws.qw, 2 * rec_rows * 64, 128, 64) ||
       !make_map_2d(&mku, ws.ku, 2 * rec_rows * 128, 64, 128) ||
       !make_map_2d(&mm, ws.m, rec_rows * 64, 64, 64) ||
-      !make_map_out(&mo, a.out, map_rows, a.H))
+      !make_map_out(&mo, a.out, map_rows, a.H) ||
+      !make_map_in(&mq, a.q, map_rows, a.H, false) ||
+      !make_map_in(&mk, a.k, map_rows, a.H, false) ||
+      !make_map_in(&mv, a.v, map_rows, a.H, false) || !make_map_in(&mg, a.g, map_rows, a.H, true))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
@@ -979,7 +1043,7 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
     const long long grid = std::min<long long>(ws.recs, 2LL * sms);
-    chunk_prep_kernel<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mqw, a, ws);
+    chunk_prep_kernel<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mqw, mq, mk, mv, mg, a, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   chunk_scan_kernel<<<dim3(a.H, a.B), kSThreads, kSSmem, st>>>(mqw, mku, mm, mo, a, ws);
