@@ -158,16 +158,24 @@ __global__ void __launch_bounds__(kPThreads, 2)
     return true;
   };
   // a record's raw q / k / v / g tiles into the staging area (one thread)
-  auto stage = [&](int h_, long long tok0_) {
-    mbar_arrive_expect_tx(&bar_ld, kStageBytes);
+  // The ten box loads of a record are issued by lane 0 of the eight warps (loads w and
+  // w + 8), so that no single thread spends the issue time; the barrier's expected bytes are
+  // registered beforehand by thread 0 (stage_expect), with a block barrier in between.
+  auto stage_expect = [&]() { mbar_arrive_expect_tx(&bar_ld, kStageBytes); };
+  auto stage_issue = [&](int h_, long long tok0_) {
+    if (lane != 0) return;
     const int r0 = (int)tok0_;
-    for (int half = 0; half < 2; ++half) {
-      tma_load_3d(sm + ST_Q + half * 8192, &map_q, &bar_ld, 64 * half, h_, r0);
-      tma_load_3d(sm + ST_K + half * 8192, &map_k, &bar_ld, 64 * half, h_, r0);
-      tma_load_3d(sm + ST_V + half * 8192, &map_v, &bar_ld, 64 * half, h_, r0);
+    for (int box = warp; box < 10; box += 8) {
+      if (box < 6) {
+        const int half = box & 1, which = box >> 1;  // q, k, v halves
+        const CUtensorMap* m = which == 0 ? &map_q : which == 1 ? &map_k : &map_v;
+        const int dst = (which == 0 ? ST_Q : which == 1 ? ST_K : ST_V) + half * 8192;
+        tma_load_3d(sm + dst, m, &bar_ld, 64 * half, h_, r0);
+      } else {
+        const int qtr = box - 6;  // g quarters
+        tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, r0);
+      }
     }
-    for (int qtr = 0; qtr < 4; ++qtr)
-      tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, r0);
   };
 
   if (warp == 0) {
@@ -202,7 +210,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
   int h, n, h_next = 0, n_next = 0;
   long long tok0, tok0_next = 0;
   bool have = locate(blockIdx.x, h, tok0, n);
-  if (have && tid == 0) stage(h, tok0);
+  if (have && tid == 0) stage_expect();
+  __syncthreads();
+  if (have) stage_issue(h, tok0);
   uint32_t ld_parity = 0;
   bool ld_pending = have;  // a staging batch was issued and not yet waited for
   // element (row 16 R + i, channel c0) of a [64 x 128] bf16 tile of two SW128 boxes:
@@ -230,25 +240,22 @@ __global__ void __launch_bounds__(kPThreads, 2)
       ld_parity ^= 1u;
     }
     float2 graw[16];
+    uint32_t vw[16], kw[16], qw[16];
+    const uint8_t* gsrc = sm + ST_G + (c0 >> 5) * 8192 + (16 * R) * 128 + (c0 & 31) * 4;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int t = 16 * R + i;
-      graw[i] = (t < n) ? *reinterpret_cast<const float2*>(sm + ST_G + (c0 >> 5) * 8192 +
-                                                             t * 128 + (c0 & 31) * 4)
-                        : make_float2(0.f, 0.f);
+      graw[i] = *reinterpret_cast<const float2*>(gsrc + i * 128);
+      vw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_V + tile_base + swz(i));
+      kw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_K + tile_base + swz(i));
+      qw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_Q + tile_base + swz(i));
     }
-    uint32_t vw[16];
+    if (n < kC) {  // partial chunk (uniform): rows past n belong to the next sequence
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      vw[i] = (16 * R + i < n)
-                  ? *reinterpret_cast<const uint32_t*>(sm + ST_V + tile_base + swz(i))
-                  : 0u;
-    uint32_t kw[16], qw[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const bool live = 16 * R + i < n;
-      kw[i] = live ? *reinterpret_cast<const uint32_t*>(sm + ST_K + tile_base + swz(i)) : 0u;
-      qw[i] = live ? *reinterpret_cast<const uint32_t*>(sm + ST_Q + tile_base + swz(i)) : 0u;
+      for (int i = 0; i < 16; ++i)
+        if (16 * R + i >= n) {
+          graw[i] = make_float2(0.f, 0.f);
+          vw[i] = kw[i] = qw[i] = 0u;
+        }
     }
     // every staged word is in registers before the V^T tile (which shares space with the
     // staged k) is written
@@ -548,12 +555,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
         mma_ss(tm + P_TM_DU, sw128_kdesc<2>(vs, 128, s), sw128_kdesc<2>(ts, 64, s), idesc, s > 0);
       }
       mma_commit(&bar_mma);
+      if (have_next) stage_expect();  // the next record's staging completes on bar_ld
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
-    // every tile the staging area reuses is free now (MMA2 was their last reader)
+    // every tile the staging area reuses is free now (MMA2 was their last reader); the
+    // expected bytes were registered when MMA2 was issued
     if (have_next) {
-      if (tid == 0) stage(h_next, tok0_next);
+      stage_issue(h_next, tok0_next);
       ld_pending = true;
     }
 
