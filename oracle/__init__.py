@@ -13,5 +13,6 @@ from .kda_oracle import (  # noqa: F401
     kda_forward_varlen,
     kda_token,
     l2_normalize,
+    recurrent_attention,
     sigmoid,
 )

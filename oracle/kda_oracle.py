@@ -307,3 +307,58 @@ def kda_backward(q, k, v, g, beta_logits, a_log, dt_bias, d_out, d_final_state=N
         "ddt_bias": np.sum(dz * a[:, None], axis=(0, 1)).T,
         "dinitial_state": dS,
     }
+
+
+def recurrent_attention(query, key, value, g=None, g_gamma=None, gk=None, gv=None,
+                        softmax_scale=None, initial_state=None, reverse=False, cu_seqlens=None):
+    """The ``recurrent_attention`` call of the ejkernel ``recurrent`` page, as a plain token
+    loop.  The page lists the parameters but prints no recurrence; the reading used here is
+    the gated linear recurrence its gate names describe (all gates are log-space decays):
+
+        a_t = g_t + gk_t + g_gamma    (key axis; each term only when given)
+        h_t = diag(exp(a_t)) h_{t-1} diag(exp(gv_t)) + k_t v_t^T,    o_t = h_t^T (scale q_t)
+
+    Layouts as on the page: ``query [B, T, Hq, D]``, ``key, value [B, T, Hkv, D]`` (query head
+    ``h`` reads key/value head ``h // (Hq / Hkv)``), ``g, gk, gv [B, T, Hq, D]``,
+    ``g_gamma [B, Hq]``, ``initial_state [B, Hq, D, D]`` (``None``: zeros).  ``reverse`` runs
+    each sequence from its last token to its first.  With ``cu_seqlens`` the tensors are
+    packed (``B = 1``) and sequence ``n`` owns tokens ``cu_seqlens[n]:cu_seqlens[n + 1]``,
+    with ``initial_state [N, Hq, D, D]``.  Returns ``(out [B, T, Hq, D], final_state)``,
+    fp64.
+    """
+    q = np.asarray(query, dtype=np.float64)
+    k = np.asarray(key, dtype=np.float64)
+    v = np.asarray(value, dtype=np.float64)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    grp = Hq // Hkv
+    scale = D ** -0.5 if softmax_scale is None else float(softmax_scale)
+    a = np.zeros((B, T, Hq, D))
+    if g is not None:
+        a = a + np.asarray(g, dtype=np.float64)
+    if gk is not None:
+        a = a + np.asarray(gk, dtype=np.float64)
+    if g_gamma is not None:
+        a = a + np.asarray(g_gamma, dtype=np.float64)[:, None, :, None]
+    bv = np.zeros((B, T, Hq, D)) if gv is None else np.asarray(gv, dtype=np.float64)
+    kk = np.repeat(k, grp, axis=2)  # key / value head of every query head
+    vv = np.repeat(v, grp, axis=2)
+    if cu_seqlens is None:
+        spans = [(b, 0, T) for b in range(B)]
+        nstate = B
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        spans = [(0, int(cu[n]), int(cu[n + 1])) for n in range(len(cu) - 1)]
+        nstate = len(cu) - 1
+    out = np.zeros((B, T, Hq, D))
+    final = np.zeros((nstate, Hq, D, D))
+    for n, (b, lo, hi) in enumerate(spans):
+        h = (np.zeros((Hq, D, D)) if initial_state is None
+             else np.array(initial_state[n], dtype=np.float64, copy=True))
+        order = range(hi - 1, lo - 1, -1) if reverse else range(lo, hi)
+        for t in order:
+            h = np.exp(a[b, t])[:, :, None] * h * np.exp(bv[b, t])[:, None, :]
+            h = h + kk[b, t][:, :, None] * vv[b, t][:, None, :]
+            out[b, t] = np.einsum("hij,hi->hj", h, scale * q[b, t])
+        final[n] = h
+    return out, final
