@@ -448,6 +448,44 @@ def backward_measure(w, d, x, reps=3):
             "workspace_bytes": int(ws.numel())}
 
 
+def recurrent_attention_measure(reps=3):
+    """kda_recurrent_attention_fwd on B=4, T=4096, Hq=32, Hkv=8, D=128, bf16 q/k/v with
+    per-channel key and value gates (gk, gv fp32): median time per call and its algorithmic
+    bytes (q, k, v, gk, gv, out and the final state, each once)."""
+    torch = _torch()
+    import gated_delta_rule_55_gb300 as kda
+    B, T, Hq, Hkv, D = 4, 4096, 32, 8, 128
+    g = torch.Generator(device="cuda").manual_seed(7)
+    q = torch.randn(B, T, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
+    k = (torch.randn(B, T, Hkv, D, device="cuda", generator=g) * D ** -0.5).to(torch.bfloat16)
+    v = torch.randn(B, T, Hkv, D, device="cuda", generator=g).to(torch.bfloat16)
+    gk = -0.05 * torch.rand(B, T, Hq, D, device="cuda", generator=g)
+    gv = -0.05 * torch.rand(B, T, Hq, D, device="cuda", generator=g)
+    out = torch.empty(B, T, Hq, D, device="cuda", dtype=torch.bfloat16)
+    fs = torch.empty(B, Hq, D, D, device="cuda")
+
+    def call():
+        kda.kda_recurrent_attention_fwd(q, k, v, out, B, T, Hq, Hkv, D, gk=gk, gv=gv,
+                                        final_state=fs)
+
+    call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(reps):
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    nbytes = B * T * (Hq * D * 2 + 2 * Hkv * D * 2 + 2 * Hq * D * 4 + Hq * D * 2) + B * Hq * D * D * 4
+    return {"entry": "kda_recurrent_attention_fwd",
+            "workload": "B4 T4096 Hq32 Hkv8 D128 bf16, gk + gv gates", "ms_per_call": ms,
+            "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": nbytes,
+            "hbm_gbs": nbytes / (ms * 1e-3) / 1e9}
+
+
 def cpu_baseline(w, d, budget_s=12.0):
     """The fp64 oracle on a bounded sample of the workload: all (b, h) pairs, the first
     T_s tokens, T_s grown until the run takes a few seconds."""
@@ -546,6 +584,9 @@ def native(args):
                        "ms_per_step": ems / ke, "steps": ke,
                        "how": "pinned host buffers; upload, compute and download of "
                               "consecutive steps overlapped on three streams"}
+        line["recurrent_attention"] = recurrent_attention_measure()
+        line["recurrent_attention"]["frac_of_hbm_peak"] = (
+            line["recurrent_attention"]["hbm_gbs"] / pk["hbm_gbs"])
         line["backward"] = backward_measure(w, d, x)
         line["backward"]["frac_of_hbm_peak"] = line["backward"]["hbm_gbs"] / pk["hbm_gbs"]
         line["cpu_baseline"] = cpu_baseline(w, d)

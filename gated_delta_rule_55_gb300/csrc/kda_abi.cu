@@ -153,6 +153,40 @@ int kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const floa
   return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kda_recurrent_attention_fwd(const void* query, const void* key, const void* value,
+                                const float* g, const float* g_gamma, const float* gk,
+                                const float* gv, float softmax_scale, const float* initial_state,
+                                void* out, float* final_state, const int32_t* cu_seqlens, int N,
+                                int B, int T, int Hq, int Hkv, int D, int reverse, int dtype,
+                                kda_stream_t stream) {
+  if (!query || !key || !value || !out) return KDA_ERR_NULL_POINTER;
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return KDA_ERR_BAD_SHAPE;
+  if (cu_seqlens && (B != 1 || N < 0)) return KDA_ERR_BAD_SHAPE;
+  if (!head_dim_ok(D)) return KDA_ERR_HEAD_DIM;
+  if (!isfinite(softmax_scale)) return KDA_ERR_SCALE;
+  if (softmax_scale <= 0.f) softmax_scale = 1.0f / sqrtf((float)D);
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  const void* ptrs[] = {query, key, value, g, g_gamma, gk, gv, initial_state, out,
+                        final_state, cu_seqlens};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  const long long nseq = cu_seqlens ? N : B;
+  if ((double)B * T * Hq * D >= 1099511627776.0 || (double)nseq * Hq * D * D >= 1099511627776.0 ||
+      (long long)B * T > 0x7fffffffLL || nseq > 65535 || Hq > 65535)
+    return KDA_ERR_TOO_LARGE;
+  int s = check_device();
+  if (s != KDA_OK) return s;
+  if (nseq == 0) return KDA_OK;
+  kda::GlaArgs a{};
+  a.q = query; a.k = key; a.v = value; a.g = g; a.g_gamma = g_gamma; a.gk = gk; a.gv = gv;
+  a.initial_state = initial_state; a.out = out; a.final_state = final_state;
+  a.cu_seqlens = cu_seqlens; a.scale = softmax_scale; a.T = T; a.nseq = (int)nseq;
+  a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.reverse = reverse ? 1 : 0;
+  const cudaError_t e = kda::launch_gla(a, dtype == KDA_BF16,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 int kda_attention_fwd(const void* query, const void* key, const void* value, const float* beta,
                       const float* decay, const float* initial_state, void* out,
                       float* final_state, float softmax_scale, int B, int T, int H, int dk,

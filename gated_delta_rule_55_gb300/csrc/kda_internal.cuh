@@ -42,6 +42,25 @@ struct ChunkArgs {
   int literal;         // 1: the error term reads the memory before its decay
 };
 
+// Gated linear recurrent attention (kda_recurrent_attention_fwd).
+struct GlaArgs {
+  const void* q;               // [B, T, Hq, D]
+  const void* k;               // [B, T, Hkv, D]
+  const void* v;               // [B, T, Hkv, D]
+  const float* g;              // [B, T, Hq, D] or NULL
+  const float* g_gamma;        // [B, Hq] or NULL
+  const float* gk;             // [B, T, Hq, D] or NULL
+  const float* gv;             // [B, T, Hq, D] or NULL
+  const float* initial_state;  // [nseq, Hq, D, D] or NULL
+  void* out;                   // [B, T, Hq, D]
+  float* final_state;          // [nseq, Hq, D, D] or NULL
+  const int32_t* cu_seqlens;   // [nseq + 1] or NULL (then nseq = B)
+  float scale;
+  int T;                       // tokens per sequence, or the packed token count
+  int nseq, Hq, Hkv, D;
+  int reverse;
+};
+
 struct DecodeArgs {
   const float* q;
   const float* k;
@@ -68,6 +87,7 @@ cudaError_t launch_backward(const ChunkArgs& f, const void* d_out, const float* 
                             void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
                             float* da_log, float* ddt_bias, float* d_initial, void* workspace,
                             bool bf16, cudaStream_t stream);
+cudaError_t launch_gla(const GlaArgs& a, bool bf16, cudaStream_t stream);
 // Sequential (token by token) scan: any supported shape, dtype and variant.
 cudaError_t launch_recurrent(const ChunkArgs& a, bool bf16, cudaStream_t stream);
 // Tensor-core chunk kernel: bf16 q/k/v, dk = dv = 128, 64-token chunks, default variant.

@@ -26,7 +26,8 @@ STATUS_NAMES = {
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_size",
            "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
            "kda_chunk_fwd_noalloc", "kda_chunk_bwd_workspace_size", "kda_chunk_bwd",
-           "kda_attention_fwd", "kda_decode_step", "kda_status_string",
+           "kda_recurrent_attention_fwd", "kda_attention_fwd", "kda_decode_step",
+           "kda_status_string",
            "kda_version", "kda_device_error")
 KDA_ATTN_NO_QK_L2NORM = 1
 KDA_ATTN_RECURRENT = 2
@@ -68,6 +69,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_fwd_ws.argtypes = L.kda_chunk_fwd.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_varlen_ws.argtypes = L.kda_chunk_fwd_varlen.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_noalloc.argtypes = L.kda_chunk_fwd.argtypes
+    L.kda_recurrent_attention_fwd.argtypes = ([_P] * 7 + [_F] + [_P] * 4 + [_I] * 8 + [_P])
     L.kda_chunk_bwd_workspace_size.argtypes = [_I] * 5
     L.kda_chunk_bwd_workspace_size.restype = _Z
     L.kda_chunk_bwd.argtypes = ([_P] * 7 + [_F, _F] + [_P] * 11 + [_I] * 6 + [_P, _Z, _P])
@@ -78,7 +80,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_device_error.argtypes = [_I]
     for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
               "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_chunk_bwd",
-              "kda_attention_fwd",
+              "kda_attention_fwd", "kda_recurrent_attention_fwd",
               "kda_decode_step", "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
     L.kda_status_string.argtypes = [_I]
@@ -230,6 +232,18 @@ def kda_chunk_bwd(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, i
         float(scale), float(lower_bound), _ptr(initial_state), _ptr(d_out), _ptr(d_final_state),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta_logits), _ptr(da_log), _ptr(ddt_bias),
         _ptr(d_initial_state), B, T, H, dk_dim, dv_dim, _dtype_code(q, dtype), wp, wb,
+        _stream(stream)))
+
+
+def kda_recurrent_attention_fwd(query, key, value, out, B, T, Hq, Hkv, D, g=None, g_gamma=None,
+                                gk=None, gv=None, softmax_scale=None, initial_state=None,
+                                final_state=None, cu_seqlens=None, N=0, reverse=False,
+                                dtype=None, stream=None):
+    """The recurrent page's gated linear recurrence (see include/kda.h)."""
+    _check("kda_recurrent_attention_fwd", lib().kda_recurrent_attention_fwd(
+        _ptr(query), _ptr(key), _ptr(value), _ptr(g), _ptr(g_gamma), _ptr(gk), _ptr(gv),
+        float(softmax_scale or 0.0), _ptr(initial_state), _ptr(out), _ptr(final_state),
+        _ptr(cu_seqlens), N, B, T, Hq, Hkv, D, int(bool(reverse)), _dtype_code(query, dtype),
         _stream(stream)))
 
 

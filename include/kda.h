@@ -235,6 +235,33 @@ int kda_attention_fwd(const void* query, const void* key, const void* value, con
                       int dv, int chunk, int flags, int dtype, kda_stream_t stream);
 
 /*
+ * kda_recurrent_attention_fwd -- the recurrent_attention call of the ejkernel "recurrent"
+ *   page: a gated linear recurrence per (sequence, query head), token by token.  The page
+ *   names the gates but prints no formula; the reading implemented is (all gates are
+ *   log-space decays, each term only when its pointer is non-NULL)
+ *       a_t = g_t + gk_t + g_gamma           (per key channel)
+ *       h_t = diag(exp(a_t)) h_{t-1} diag(exp(gv_t)) + k_t v_t^T,   o_t = h_t^T (scale q_t)
+ *
+ *   query, out   [B, T, Hq, D]    dtype (fp32 or bf16)
+ *   key, value   [B, T, Hkv, D]   dtype; query head h reads kv head h / (Hq / Hkv)
+ *   g, gk, gv    [B, T, Hq, D]    fp32 or NULL
+ *   g_gamma      [B, Hq]          fp32 or NULL
+ *   initial_state / final_state [nseq, Hq, D, D] fp32 (NULL: zeros / not wanted)
+ *   softmax_scale  multiplies q; <= 0 selects D^-0.5
+ *   cu_seqlens   NULL for B sequences of T tokens (nseq = B); otherwise [N + 1] int32
+ *                DEVICE offsets of N packed sequences, B must be 1 and T is the packed
+ *                token count (nseq = N); entries are clamped into [0, T]
+ *   reverse      non-zero: each sequence is processed from its last token to its first
+ *   D in {32, 64, 128}; Hq a multiple of Hkv.
+ */
+int kda_recurrent_attention_fwd(const void* query, const void* key, const void* value,
+                                const float* g, const float* g_gamma, const float* gk,
+                                const float* gv, float softmax_scale, const float* initial_state,
+                                void* out, float* final_state, const int32_t* cu_seqlens, int N,
+                                int B, int T, int Hq, int Hkv, int D, int reverse, int dtype,
+                                kda_stream_t stream);
+
+/*
  * kda_decode_step -- advance the recurrence by exactly one token for B requests, in the
  *   kda_tkg layouts (NKI "KDA TKG Kernel API Reference", kda_tkg), all fp32:
  *

@@ -239,3 +239,31 @@ def test_backward_without_device(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; this case is only meaningful without one")
     assert _bwd(L) == -9
+
+
+def _gla(L, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=None, gg=None, gk=None, gv=None, scale=0.0, s0=None,
+             out=FAKE, s1=None, cu=None, N=0, B=2, T=16, Hq=4, Hkv=2, D=64, rev=0, dtype=1)
+    a.update(over)
+    return L.kda_recurrent_attention_fwd(a["q"], a["k"], a["v"], a["g"], a["gg"], a["gk"],
+                                         a["gv"], a["scale"], a["s0"], a["out"], a["s1"],
+                                         a["cu"], a["N"], a["B"], a["T"], a["Hq"], a["Hkv"],
+                                         a["D"], a["rev"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), -1), (dict(v=None), -1), (dict(out=None), -1), (dict(B=-1), -2),
+    (dict(Hq=3), -2), (dict(Hkv=0), -2), (dict(cu=FAKE, B=2), -2), (dict(cu=FAKE, B=1, N=-1), -2),
+    (dict(D=48), -3), (dict(scale=float("inf")), -10), (dict(dtype=4), -7),
+    (dict(gk=FAKE + 8), -6),
+])
+def test_recurrent_attention_rejects_bad_arguments(L, over, code):
+    assert _gla(L, **over) == code
+
+
+def test_recurrent_attention_without_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is only meaningful without one")
+    assert _gla(L) == -9
+    assert _gla(L, cu=FAKE, B=1, N=3, rev=1) == -9
