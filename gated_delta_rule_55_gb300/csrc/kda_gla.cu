@@ -15,6 +15,8 @@
 // so tokens go in blocks of kTB: the block's inputs are staged in shared memory (gate
 // exponentials applied), every thread advances its state through the whole block keeping one
 // partial output per token, and the outputs are reduced over the key axis once per block.
+// The raw inputs of the next block are copied global -> shared with cp.async (no registers)
+// while the current block is computed.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -22,11 +24,37 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kDVS = 32;
-constexpr int kTB = 16;  // tokens per staged block
+constexpr int kTB = 8;  // tokens per staged block (4 CTAs per SM fit with the double buffer)
+
+// 16-byte asynchronous global -> shared copy (cp.async, cache-global), and its group fences.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_one() {  // all but the newest group landed
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// Raw inputs of one block of tokens as they sit in memory.
+template <typename Tin, int D>
+struct RawBlock {
+  Tin q[kTB][D], k[kTB][D];
+  float a[kTB][D];            // g + gk (g_gamma is added on conversion)
+  float gk2[kTB][D];          // the second key gate when both g and gk are given
+  Tin v[kTB][kDVS];
+  float gv[kTB][kDVS];
+};
 
 template <typename Tin, int D>
 __global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
   constexpr int RPT = D / 16;          // rows per thread
+  extern __shared__ __align__(16) uint8_t dyn[];
+  RawBlock<Tin, D>* raw = reinterpret_cast<RawBlock<Tin, D>*>(dyn);  // [2], double-buffered
   __shared__ float4 s_kaq[kTB][D];     // (k, e^{a}, scale q, -) per token and key channel
   __shared__ __align__(16) float2 s_vb[kTB][kDVS];   // (v, e^{gv}) per token and column
   __shared__ __align__(16) float s_o[kTB][4][kDVS];  // per-warp partial outputs
@@ -67,25 +95,72 @@ __global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
   // token slot u of a block starting at position p0 is position p0 + u (forward) or
   // p0 - u (reverse)
   const int dir = a.reverse ? -1 : 1;
-  for (int b0 = 0; b0 < len; b0 += kTB) {
-    const int nb = min(kTB, len - b0);
+  const int nblocks = (len + kTB - 1) / kTB;
+  // copies block bi's raw rows into raw[bi & 1] (16-byte pieces; one commit group)
+  auto fetch = [&](int bi) {
+    if (bi < nblocks) {
+      RawBlock<Tin, D>& r = raw[bi & 1];
+      const int b0 = bi * kTB, nb = min(kTB, len - b0);
+      const int p0 = a.reverse ? len - 1 - b0 : b0;
+      constexpr int QP = D * sizeof(Tin) / 16;    // 16-byte pieces per q / k row
+      constexpr int FP = D * 4 / 16;              // per fp32 gate row
+      constexpr int VP = kDVS * sizeof(Tin) / 16; // per v slice row
+      constexpr int GP = kDVS * 4 / 16;           // per gv slice row
+      for (int e = tid; e < nb * QP; e += kThreads) {
+        const int u = e / QP, pc = e % QP;
+        const long long tok = bos + p0 + dir * u;
+        cp_async16(reinterpret_cast<uint8_t*>(r.q[u]) + 16 * pc,
+                   reinterpret_cast<const uint8_t*>(q + (tok * Hq + h) * D) + 16 * pc);
+        cp_async16(reinterpret_cast<uint8_t*>(r.k[u]) + 16 * pc,
+                   reinterpret_cast<const uint8_t*>(k + (tok * Hkv + hk) * D) + 16 * pc);
+      }
+      const float* ga = a.g ? a.g : a.gk;          // first key gate, if any
+      const float* gb = (a.g && a.gk) ? a.gk : nullptr;
+      for (int e = tid; e < nb * FP; e += kThreads) {
+        const int u = e / FP, pc = e % FP;
+        const long long rq = (bos + p0 + dir * u) * Hq + h;
+        if (ga) cp_async16(reinterpret_cast<uint8_t*>(r.a[u]) + 16 * pc,
+                           reinterpret_cast<const uint8_t*>(ga + rq * D) + 16 * pc);
+        if (gb) cp_async16(reinterpret_cast<uint8_t*>(r.gk2[u]) + 16 * pc,
+                           reinterpret_cast<const uint8_t*>(gb + rq * D) + 16 * pc);
+      }
+      for (int e = tid; e < nb * VP; e += kThreads) {
+        const int u = e / VP, pc = e % VP;
+        const long long tok = bos + p0 + dir * u;
+        cp_async16(reinterpret_cast<uint8_t*>(r.v[u]) + 16 * pc,
+                   reinterpret_cast<const uint8_t*>(v + (tok * Hkv + hk) * D + j0) + 16 * pc);
+      }
+      if (a.gv) {
+        for (int e = tid; e < nb * GP; e += kThreads) {
+          const int u = e / GP, pc = e % GP;
+          const long long rq = (bos + p0 + dir * u) * Hq + h;
+          cp_async16(reinterpret_cast<uint8_t*>(r.gv[u]) + 16 * pc,
+                     reinterpret_cast<const uint8_t*>(a.gv + rq * D + j0) + 16 * pc);
+        }
+      }
+    }
+    cp_async_commit();  // (an empty group past the last block keeps the counting uniform)
+  };
+  fetch(0);
+  for (int bi = 0; bi < nblocks; ++bi) {
+    const int b0 = bi * kTB, nb = min(kTB, len - b0);
     const int p0 = a.reverse ? len - 1 - b0 : b0;
-    // stage the block (rows past nb are never read)
+    fetch(bi + 1);      // in flight while this block is converted and computed
+    cp_async_wait_one();  // this block's copies have landed (for this thread)
+    __syncthreads();      // ... and for every thread
+    const RawBlock<Tin, D>& r = raw[bi & 1];
+    const bool has_a = a.g || a.gk, has_b = a.g && a.gk;
     for (int e = tid; e < nb * D; e += kThreads) {
       const int u = e / D, c = e % D;
-      const long long tok = bos + p0 + dir * u;
-      const long long rq = tok * Hq + h;
       float x = gamma;
-      if (a.g) x += a.g[rq * D + c];
-      if (a.gk) x += a.gk[rq * D + c];
-      s_kaq[u][c] = make_float4(load_as_float(k + (tok * Hkv + hk) * D + c), expf(x),
-                                a.scale * load_as_float(q + rq * D + c), 0.f);
+      if (has_a) x += r.a[u][c];
+      if (has_b) x += r.gk2[u][c];
+      s_kaq[u][c] = make_float4(load_as_float(&r.k[u][c]), expf(x),
+                                a.scale * load_as_float(&r.q[u][c]), 0.f);
     }
     for (int e = tid; e < nb * kDVS; e += kThreads) {
       const int u = e / kDVS, jj = e % kDVS;
-      const long long tok = bos + p0 + dir * u;
-      s_vb[u][jj] = make_float2(load_as_float(v + (tok * Hkv + hk) * D + j0 + jj),
-                                a.gv ? expf(a.gv[(tok * Hq + h) * D + j0 + jj]) : 1.f);
+      s_vb[u][jj] = make_float2(load_as_float(&r.v[u][jj]), a.gv ? expf(r.gv[u][jj]) : 1.f);
     }
     __syncthreads();
     for (int u = 0; u < nb; ++u) {
@@ -118,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
       const float tot = s_o[u][0][jj] + s_o[u][1][jj] + s_o[u][2][jj] + s_o[u][3][jj];
       store_from_float(out + ((bos + p0 + dir * u) * Hq + h) * D + j0 + jj, tot);
     }
-    __syncthreads();  // the staged block and the partials are rewritten next
+    __syncthreads();  // the staged block, the partials and raw[bi & 1] are rewritten next
   }
   if (a.final_state) {
 #pragma unroll
@@ -132,7 +207,11 @@ __global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
 template <typename Tin, int D>
 cudaError_t launch_t(const GlaArgs& a, cudaStream_t st) {
   const dim3 grid(D / kDVS, a.Hq, a.nseq);
-  gla_kernel<Tin, D><<<grid, kThreads, 0, st>>>(a);
+  const int dyn = 2 * (int)sizeof(RawBlock<Tin, D>);
+  cudaError_t e = cudaFuncSetAttribute(gla_kernel<Tin, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  if (e != cudaSuccess) return e;
+  gla_kernel<Tin, D><<<grid, kThreads, dyn, st>>>(a);
   return cudaGetLastError();
 }
 
