@@ -29,12 +29,18 @@ int check_device() {
   return ok ? KDA_OK : KDA_ERR_DEVICE;
 }
 
-int check_common(float* scale, float lower_bound, int dk, int dv) {
+// Head dimensions and the query scale (scale <= 0 selects dk^-0.5).
+int check_dims_scale(float* scale, int dk, int dv) {
   if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_HEAD_DIM;
-  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_LOWER_BOUND;
   if (!isfinite(*scale)) return KDA_ERR_SCALE;
   if (*scale <= 0.0f) *scale = 1.0f / sqrtf((float)dk);
   return KDA_OK;
+}
+
+int check_common(float* scale, float lower_bound, int dk, int dv) {
+  if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_HEAD_DIM;
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_LOWER_BOUND;
+  return check_dims_scale(scale, dk, dv);
 }
 
 // workspace == nullptr: the single-pass kernels; otherwise (a non-zero workspace size was
@@ -195,7 +201,7 @@ int kda_attention_fwd(const void* query, const void* key, const void* value, con
   if (B < 0 || T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
   if (flags & ~(KDA_ATTN_NO_QK_L2NORM | KDA_ATTN_RECURRENT | KDA_ATTN_ORDER_LITERAL))
     return KDA_ERR_FLAGS;
-  int s = check_common(&softmax_scale, -1.0f, dk, dv);
+  int s = check_dims_scale(&softmax_scale, dk, dv);
   if (s != KDA_OK) return s;
   if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_TOO_LARGE;
   kda::ChunkArgs a{};
@@ -237,11 +243,11 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   float scale, float lower_bound, const float* initial_state, const void* d_out,
                   const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
                   float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
-                  int B, int T, int H, int dk_, int dv_, int dtype, void* workspace,
+                  int B, int T, int H, int dim_k, int dim_v, int dtype, void* workspace,
                   size_t workspace_bytes, kda_stream_t stream) {
   kda::ChunkArgs a;
   int s = fill_fixed(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
-                     initial_state, dq, nullptr, B, T, H, dk_, dv_, 64);
+                     initial_state, dq, nullptr, B, T, H, dim_k, dim_v, 64);
   if (s != KDA_OK) return s;
   if (!d_out || !dq || !dk || !dv || !dg || !dbeta_logits || !da_log || !ddt_bias)
     return KDA_ERR_NULL_POINTER;
@@ -251,11 +257,12 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                         d_initial_state};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
-  const double elems = (double)a.total_T * H * (dk_ > dv_ ? dk_ : dv_);
-  if (elems >= 1099511627776.0 || (double)B * H * dk_ * dv_ * ((T + 63) / 64 + 64) >=
-                                      1099511627776.0 || B > 65535 || H > 65535)
+  const double elems = (double)a.total_T * H * (dim_k > dim_v ? dim_k : dim_v);
+  if (elems >= 1099511627776.0 ||
+      (double)B * H * dim_k * dim_v * ((T + 63) / 64 + 64) >= 1099511627776.0 || B > 65535 ||
+      H > 65535)
     return KDA_ERR_TOO_LARGE;
-  const size_t need = kda::backward_workspace(B, T, H, dk_, dv_);
+  const size_t need = kda::backward_workspace(B, T, H, dim_k, dim_v);
   if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                    workspace_bytes < need))
     return KDA_ERR_WORKSPACE;
@@ -265,7 +272,7 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
   cudaError_t e;
   if (B == 0) {
     e = cudaMemsetAsync(da_log, 0, sizeof(float) * H, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * dk_ * H, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * dim_k * H, st);
   } else {
     e = kda::launch_backward(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
                              ddt_bias, d_initial_state, workspace, dtype == KDA_BF16, st);

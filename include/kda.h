@@ -187,6 +187,7 @@ int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
  *     dg             [B, T, H, dk]   fp32           dbeta_logits [B, T, H] fp32
  *     da_log         [H] fp32        ddt_bias       [dk, H] fp32   (sums over B and T)
  *     d_initial_state [B, H, dk, dv] fp32 or NULL (not wanted)
+ *   dim_k, dim_v   the head dimensions dk, dv (named apart from the dk / dv gradients)
  *   workspace / workspace_bytes: device scratch of at least kda_chunk_bwd_workspace_size()
  *   bytes, 256-byte aligned (checkpoints, one chunk of states per (sequence, head) and
  *   per-token fp32 intermediates).
@@ -197,7 +198,7 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   float scale, float lower_bound, const float* initial_state, const void* d_out,
                   const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
                   float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
-                  int B, int T, int H, int dk_, int dv_, int dtype, void* workspace,
+                  int B, int T, int H, int dim_k, int dim_v, int dtype, void* workspace,
                   size_t workspace_bytes, kda_stream_t stream);
 
 /* Options of kda_attention_fwd (bitwise OR). */
