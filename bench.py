@@ -420,7 +420,8 @@ def backward_measure(w, d, x, reps=3):
          "dg": torch.empty(B, T, H, dk, device="cuda"),
          "db": torch.empty(B, T, H, device="cuda"),
          "da": torch.empty(H, device="cuda"), "ddt": torch.empty(dk, H, device="cuda")}
-    ws = torch.empty(kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv), dtype=torch.uint8,
+    ws = torch.empty(kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv, kda.KDA_BF16),
+                     dtype=torch.uint8,
                      device="cuda")
 
     def call():
@@ -444,7 +445,7 @@ def backward_measure(w, d, x, reps=3):
     nbytes = B * T * H * per
     return {"entry": "kda_chunk_bwd", "workload": w.name, "ms_per_call": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": nbytes,
-            "hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "launches": 3,
+            "hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "launches": 4,
             "workspace_bytes": int(ws.numel())}
 
 

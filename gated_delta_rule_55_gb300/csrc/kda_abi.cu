@@ -231,10 +231,19 @@ int kda_attention_fwd(const void* query, const void* key, const void* value, con
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
-size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv) {
+// Backward arguments for sizing only (no pointers are read).
+kda::ChunkArgs bwd_shape(int B, int T, int H, int dk, int dv) {
+  kda::ChunkArgs a{};
+  a.B = B; a.T = T; a.total_T = B * T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = 64;
+  return a;
+}
+
+size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int dtype) {
   if (B < 0 || T < 0 || H <= 0 || !head_dim_ok(dk) || !head_dim_ok(dv) ||
-      (long long)B * T > 0x7fffffffLL)
+      (long long)B * T > 0x7fffffffLL || (dtype != KDA_F32 && dtype != KDA_BF16))
     return 0;
+  const kda::ChunkArgs a = bwd_shape(B, T, H, dk, dv);
+  if (B > 0 && kda::chunk_bwd_supported(a, dtype == KDA_BF16)) return kda::chunk_bwd_workspace(a);
   return kda::backward_workspace(B, T, H, dk, dv);
 }
 
@@ -262,7 +271,9 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
       (double)B * H * dim_k * dim_v * ((T + 63) / 64 + 64) >= 1099511627776.0 || B > 65535 ||
       H > 65535)
     return KDA_ERR_TOO_LARGE;
-  const size_t need = kda::backward_workspace(B, T, H, dim_k, dim_v);
+  const bool chunked = B > 0 && kda::chunk_bwd_supported(a, dtype == KDA_BF16);
+  const size_t need =
+      chunked ? kda::chunk_bwd_workspace(a) : kda::backward_workspace(B, T, H, dim_k, dim_v);
   if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                    workspace_bytes < need))
     return KDA_ERR_WORKSPACE;
@@ -273,6 +284,9 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
   if (B == 0) {
     e = cudaMemsetAsync(da_log, 0, sizeof(float) * H, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * dim_k * H, st);
+  } else if (chunked) {
+    e = kda::launch_chunk_bwd(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
+                              ddt_bias, d_initial_state, workspace, st);
   } else {
     e = kda::launch_backward(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
                              ddt_bias, d_initial_state, workspace, dtype == KDA_BF16, st);
@@ -376,7 +390,7 @@ int kda_device_error(int reset) {
   int s = check_device();
   if (s != KDA_OK) return s;
   return (int)(kda::chunk_tc_read_error(reset != 0) | kda::chunk_split_read_error(reset != 0) |
-               kda::decode_read_error(reset != 0));
+               kda::chunk_bwd_read_error(reset != 0) | kda::decode_read_error(reset != 0));
 }
 
 }  // extern "C"

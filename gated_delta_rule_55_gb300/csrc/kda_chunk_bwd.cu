@@ -1,0 +1,943 @@
+// Chunked backward of the KDA forward on the tensor cores (bf16 q/k/v/d_out, dk = dv = 128,
+// 64-token chunks, fixed-length sequences, decay-first recurrence with the kda_tkg gate and
+// beta logits).  The pages give no backward ("Algorithm modes: chunked" is named as the
+// training path); this is reverse-mode differentiation of the chunk form of the forward,
+//
+//   U = T (V - K~ S),   O = Q~ S + M U,   S' = diag(e^{G_C}) S + Kd^T U,
+//   T = N diag(beta),   N = (I + diag(beta) tril(A, -1))^{-1},
+//
+// with K~ = k^ e^{G}, Q~ = q^ e^{G}, Kd = k^ e^{G_C - G}, A / M the gate-scaled k^ k^T and
+// q^ k^T of the chunk.  Given the adjoint dS' of the state leaving a chunk and d_out:
+//
+//   dU  = Kd dS' + M^T dO                            (sequential over chunks, reversed)
+//   dS  = diag(e^{G_C}) dS' + Q~^T dO - W^T dU
+//   lam = N^T dU,  dV = diag(beta) lam,  dK~ = -dV S^T,  dQ~ = dO S^T,  dKd = U dS'^T
+//   dA  = -dV U^T (s < r),  dM = dO U^T (s <= r),  dbeta_logit_r = (1 - beta_r) lam_r . u_r
+//
+// and the gate-scaled products A, M are differentiated through the same 16-token sub-chunk
+// operand tiles (Xl, Kb) that form them in the forward.  Launches:
+//
+//   chunk_prep_kernel / chunk_scan_kernel (kda_chunk_split.cu, backward mode): the forward
+//       records with rq folded into Q~ and M, N, and per chunk the entering state S and U;
+//   bwd_scan_kernel: one CTA per (sequence, head) walks the chunks in reverse with dS' in
+//       Tensor Memory, writing per chunk dS' and dU (bf16) and finally d_initial_state;
+//   bwd_chunk_kernel: one CTA per (chunk, head), all at once: every other product above,
+//       then the gate, L2-norm and sigmoid chain rules, writing dq, dk, dv, dg, dbeta_logits
+//       and adding into da_log and ddt_bias.
+//
+// Operands are the row-major 128-byte-swizzled tiles that TMA moves; a tile [lines][64] is
+// read K-major when the contraction runs along its rows' elements and MN-major when it runs
+// across its lines, so no operand is transposed in memory.
+#include "chunk_records.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+using namespace chunk;
+using namespace split;
+
+__device__ unsigned int g_bwd_error;  // bit 2: a bounded wait of the chunked backward gave up
+
+struct BwdWs {
+  Ws f;                // forward records (backward mode) and the forward scan's S, U
+  __nv_bfloat16* ds;   // [recs * 128][128]: dS'^T of each chunk (row = value column j)
+  __nv_bfloat16* dut;  // [recs * 128][64]: dU^T of each chunk
+};
+
+struct BwdOut {
+  const float* d_final;  // [B, H, 128, 128] or NULL
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dg;
+  float* dbeta_logits;
+  float* da_log;
+  float* ddt_bias;
+  float* d_initial;      // [B, H, 128, 128] or NULL
+};
+
+// Byte offset of element e (bf16) of line `line` of a tile cut into 64-element boxes
+// ([lines][64] each, `bs` bytes apart), 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw_off(int line, int e, uint32_t bs) {
+  const uint32_t byte = uint32_t(e & 63) * 2u;
+  return uint32_t(e >> 6) * bs + uint32_t(line >> 3) * 1024u + uint32_t(line & 7) * 128u +
+         ((((byte >> 4) ^ uint32_t(line & 7)) << 4) | (byte & 15u));
+}
+
+// MN-major operand descriptor of K-step s (16 lines) of such a tile: 64-element blocks of
+// the M / N extent `bs` bytes apart, 8-line groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t mn_desc(uint32_t tile, uint32_t bs, int s) {
+  return make_sdesc(tile + uint32_t(s) * 2048u, bs, 1024u, kSwizzle128);
+}
+
+// Zeroes rows n .. 63 of a [64 x 128] bf16 tile of two boxes 8192 bytes apart (rows that
+// belong to the next sequence or lie past the tensor); 8 threads per row.
+__device__ __forceinline__ void zero_rows(uint8_t* tile, int n, int tid) {
+  const int row = tid >> 3, piece = tid & 7;
+  if (row < 64 && row >= n) {
+    const uint32_t base = uint32_t(piece >> 2) * 8192u + uint32_t(row >> 3) * 1024u +
+                          uint32_t(row & 7) * 128u;
+    const uint32_t c0 = uint32_t(piece & 3) * 2u;
+    *reinterpret_cast<uint4*>(tile + base + ((c0 ^ uint32_t(row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(tile + base + (((c0 + 1) ^ uint32_t(row & 7)) << 4)) =
+        make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Sum over the 32 lanes of eight per-lane values v[0..7]; the sum for index
+// tq = 4 b4 + 2 b3 + b2 (bits of the lane) ends in v[0] of lanes with (lane & 3) == 0.
+__device__ __forceinline__ float reduce_scatter8(float (&v)[8], int lane, int& tq) {
+#pragma unroll
+  for (int half = 4, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  tq = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+  return v[0];
+}
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------ reverse chunk scan
+
+constexpr int kBSThreads = 512;
+// one stage = one chunk: the forward records it needs and the chunk's d_out tile
+constexpr int B_Q = 0;          // Q~ = q^ e^{G} [64 tok][128] (two boxes)
+constexpr int B_W = 16384;      // -W [64 tok][128]
+constexpr int B_KT = 32768;     // K^^T = (k e^{G_C - G})^T [128][64 tok]
+constexpr int B_M = 49152;      // rq_r M_raw[r][s] [64][64]
+constexpr int B_DO = 57344;     // d_out [64 tok][128] (two boxes)
+constexpr int B_V = 73728;      // e^{G_C}, rk, rq
+constexpr int kBStage = 74752;
+constexpr uint32_t kBStageTx = 74752;
+static_assert(kBStage % 1024 == 0, "alignment");
+constexpr size_t kBSSmem = 2 * kBStage + 1024;
+
+constexpr uint32_t BT_DU = 0;    // dU^T accumulator, 64 columns
+constexpr uint32_t BT_S = 128;   // fp32 dS^T, 128
+constexpr uint32_t BT_SA = 256;  // bf16 copy of dS^T (A operand), 64
+constexpr uint32_t BT_UA = 320;  // bf16 dU^T (A operand), 32
+constexpr uint32_t kBTmemCols = 512;
+
+__global__ void __launch_bounds__(kBSThreads, 1)
+    bwd_scan_kernel(const __grid_constant__ CUtensorMap map_qw,
+                    const __grid_constant__ CUtensorMap map_ku,
+                    const __grid_constant__ CUtensorMap map_m,
+                    const __grid_constant__ CUtensorMap map_do, const ChunkArgs a,
+                    const BwdWs bw, const BwdOut o) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld[2], bar_mma;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_wait_ok[2];
+  __shared__ __align__(16) float s_vec[256];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int wg = tid >> 7;
+  const int ln = tid & 127;
+  const int lane_base = 32 * (warp & 3);
+  const int h = blockIdx.x, seq = blockIdx.y;
+  const int H = a.H;
+  const long long bos = (long long)seq * a.T;
+  const int len = a.T;
+  const int nck = bw.f.nck_fixed;
+  const long long slot0 = (long long)seq * nck;
+  const long long state_off = ((long long)seq * H + h) * kD * kD;
+  auto rec_of = [&](int ch) -> long long { return (slot0 + ch) * H + h; };
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kBTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_ld[0], 1);
+    mbar_init(&bar_ld[1], 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&map_qw);
+    tma_prefetch_desc(&map_ku);
+    tma_prefetch_desc(&map_m);
+    tma_prefetch_desc(&map_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t tl = tm + (uint32_t(lane_base) << 16);
+
+  // step `it` handles chunk nck - 1 - it
+  auto issue_load = [&](int it, int st) {
+    const int ch = nck - 1 - it;
+    const long long rec = rec_of(ch);
+    uint8_t* b = sm + st * kBStage;
+    uint64_t* bar = &bar_ld[st];
+    mbar_arrive_expect_tx(bar, kBStageTx);
+    const int rq = (int)(rec * 64), rw = (int)((bw.f.recs + rec) * 64);
+    const int tok0 = (int)(bos + (long long)ch * kC);
+    tma_load_2d(b + B_Q, &map_qw, bar, 0, rq);
+    tma_load_2d(b + B_Q + 8192, &map_qw, bar, 64, rq);
+    tma_load_2d(b + B_W, &map_qw, bar, 0, rw);
+    tma_load_2d(b + B_W + 8192, &map_qw, bar, 64, rw);
+    tma_load_2d(b + B_KT, &map_ku, bar, 0, (int)(rec * 128));
+    tma_load_2d(b + B_M, &map_m, bar, 0, (int)(rec * 64));
+    tma_load_3d(b + B_DO, &map_do, bar, 0, h, tok0);
+    tma_load_3d(b + B_DO + 8192, &map_do, bar, 64, h, tok0);
+    bulk_load(b + B_V, bw.f.vec + rec * 256, 1024, bar);
+  };
+  int inflight[2] = {nck > 0 ? 0 : -1, nck > 1 ? 1 : -1};
+  if (tid == 0) {
+    if (nck > 0) issue_load(0, 0);
+    if (nck > 1) issue_load(1, 1);
+  }
+
+  // dS' of the last chunk = d_final_state: thread (j = ln, wg) owns dS^T[j][32 wg .. + 31]
+  {
+    float S[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int c = 32 * wg + i;
+      S[i] = o.d_final ? o.d_final[state_off + (long long)c * kD + ln] : 0.f;
+    }
+    tmem_st32(tl + BT_S + 32 * wg, S);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
+    tmem_st16(tl + BT_SA + 16 * wg, w);
+    if (nck > 0) {
+      uint4* d = reinterpret_cast<uint4*>(bw.ds + (rec_of(nck - 1) * 128 + ln) * 128 + 32 * wg);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) d[p] = make_uint4(w[4 * p], w[4 * p + 1], w[4 * p + 2], w[4 * p + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  const uint32_t idesc_du_ts = make_idesc(1, 128, 64, false, true);
+  const uint32_t idesc_du_ss = make_idesc(1, 128, 64, true, true);
+  const uint32_t idesc_s_ss = make_idesc(1, 128, 128, true, true);
+  const uint32_t idesc_s_ts = make_idesc(1, 128, 128, false, true);
+  uint32_t mma_phase = 0;
+  uint32_t wait_calls = 0;
+  auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const uint32_t slot_w = wait_calls++ & 1;
+    if (tid == 0) s_wait_ok[slot_w] = mbar_wait(bar, parity) ? 1 : 0;
+    __syncthreads();
+    return s_wait_ok[slot_w] != 0;
+  };
+  auto mma_wait = [&]() -> bool {
+    const bool w = block_wait(&bar_mma, mma_phase & 1);
+    ++mma_phase;
+    return w;
+  };
+  bool ok = true;
+
+  for (int it = 0; it < nck; ++it) {
+    const int ch = nck - 1 - it;
+    const int st = it & 1;
+    uint8_t* const b = sm + st * kBStage;
+    const int n = min(kC, len - ch * kC);
+    const long long rec = rec_of(ch);
+
+    if (!(ok = block_wait(&bar_ld[st], (it >> 1) & 1))) break;
+    inflight[st] = -1;
+    if (tid < 256) s_vec[tid] = reinterpret_cast<const float*>(b + B_V)[tid];
+    if (n < kC) {
+      zero_rows(b + B_DO, n, tid);
+      fence_async_smem();
+    }
+    __syncthreads();
+
+    // ---- dU^T = dS'^T K^ + dO^T (rq M_raw)  (the rk column factor is applied below)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t kt = smem_u32(b + B_KT), ms = smem_u32(b + B_M), dos = smem_u32(b + B_DO);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        mma_ts(tm + BT_DU, tm + BT_SA + 8 * s, mn_desc(kt, 8192, s), idesc_du_ts, s > 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_ss(tm + BT_DU, mn_desc(dos, 8192, s), mn_desc(ms, 8192, s), idesc_du_ss, 1);
+      mma_commit(&bar_mma);
+    }
+    // meanwhile: dS'^T diag(e^{G_C}) in place
+    {
+      float S[32];
+      tmem_ld32(tl + BT_S + 32 * wg, S);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) S[i] *= s_vec[32 * wg + i];
+      tmem_st32(tl + BT_S + 32 * wg, S);
+    }
+    if (!(ok = mma_wait())) break;
+    tc_fence_after();
+    // ---- dU^T (rk column factor) -> bf16 A operand and the dU^T record: thread
+    //      (j = ln, tokens 16 wg .. + 15)
+    {
+      float v16[16];
+      tmem_ld16(tl + BT_DU + 16 * wg, v16);
+      uint32_t up[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        up[i] = pack_bf16(v16[2 * i] * s_vec[128 + 16 * wg + 2 * i],
+                          v16[2 * i + 1] * s_vec[128 + 16 * wg + 2 * i + 1]);
+      tmem_st8(tl + BT_UA + 8 * wg, up);
+      uint4* d = reinterpret_cast<uint4*>(bw.dut + (rec * 128 + ln) * 64 + 16 * wg);
+      d[0] = make_uint4(up[0], up[1], up[2], up[3]);
+      d[1] = make_uint4(up[4], up[5], up[6], up[7]);
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- dS^T += dO^T Q~ + dU^T (-W)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t qs = smem_u32(b + B_Q), wsm = smem_u32(b + B_W), dos = smem_u32(b + B_DO);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_ss(tm + BT_S, mn_desc(dos, 8192, s), mn_desc(qs, 8192, s), idesc_s_ss, 1);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_ts(tm + BT_S, tm + BT_UA + 8 * s, mn_desc(wsm, 8192, s), idesc_s_ts, 1);
+      mma_commit(&bar_mma);
+    }
+    if (!(ok = mma_wait())) break;
+    tc_fence_after();
+    if (tid == 0 && it + 2 < nck) issue_load(it + 2, st);
+    inflight[st] = (it + 2 < nck) ? it + 2 : -1;
+    // ---- bf16 copy of dS (= dS' of the previous chunk) and its record
+    {
+      float S[32];
+      tmem_ld32(tl + BT_S + 32 * wg, S);
+      uint32_t sp[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sp[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
+      tmem_st16(tl + BT_SA + 16 * wg, sp);
+      if (ch > 0) {
+        uint4* d = reinterpret_cast<uint4*>(bw.ds + (rec_of(ch - 1) * 128 + ln) * 128 + 32 * wg);
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          d[p] = make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+
+  if (!ok) {
+    if (tid == 0) {
+      atomicOr(&g_bwd_error, 4u);
+      for (int st = 0; st < 2; ++st)
+        if (inflight[st] >= 0) mbar_wait(&bar_ld[st], (inflight[st] >> 1) & 1, 1000000000ull);
+    }
+    mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
+  } else if (o.d_initial) {
+    tc_fence_after();
+    float S[32];
+    tmem_ld32(tl + BT_S + 32 * wg, S);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int c = 32 * wg + i;
+      o.d_initial[state_off + (long long)c * kD + ln] = S[i];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, kBTmemCols);
+}
+
+// ------------------------------------------------------------ per-chunk products
+
+constexpr int kKThreads = 512;
+// Dynamic shared memory (1024-aligned offsets).
+constexpr int K_DUT = 0;        // dU^T [128 j][64 r]; dV^T once lam is read
+constexpr int K_NN = 16384;     // N [64][64]
+constexpr int K_UT = 24576;     // U^T [128 j][64 s]
+constexpr int K_DO = 40960;     // d_out [64 r][128 j] (two boxes, 8192 apart)
+constexpr int K_S0 = 57344;     // S^T [128 j][128 c] (two boxes, 16384 apart)
+constexpr int K_DS = 90112;     // dS'^T [128 j][128 c]
+constexpr int K_D1 = K_S0;      // dD1 [128 rows][192] (three boxes, 16384 apart), after S / dS'
+constexpr int K_XL = 122880;    // Xl [128 rows][128 c] (two boxes, 16384 apart)
+constexpr int K_KB = 155648;    // Kb [160 rows][128 c] (two boxes, 20480 apart)
+constexpr int K_END = 196608;
+constexpr int K_AQ = K_XL;      // fp32 [64 tok][128 c] dq^ (epilogue, after the last MMA)
+constexpr int K_DKH = K_KB;     // fp32 [64 tok][128 c] dk^
+static_assert(K_D1 + 3 * 16384 <= K_XL, "dD1 overlaps Xl");
+static_assert(K_DO + 3 * 8192 <= K_END, "rows 64..127 of the d_out A operand read in bounds");
+static_assert(K_DUT + 2 * 16384 <= K_DO, "second M block of the dV^T A operand in bounds");
+static_assert(K_AQ + 32768 <= K_KB && K_DKH + 32768 <= K_END, "epilogue scratch");
+constexpr uint32_t kKLoadTx = 16384 + 8192 + 16384 + 16384 + 32768 + 32768;
+constexpr size_t kKSmem = K_END + 1024;
+
+// Tensor Memory (512 columns, one CTA per SM).
+constexpr uint32_t KT_P1 = 0;    // dQ~^T [c][r]
+constexpr uint32_t KT_P3 = 64;   // dKd^T [c][s]
+constexpr uint32_t KT_P2 = 128;  // (dV S^T)^T [c][r] = -dK~^T
+constexpr uint32_t KT_L = 192;   // lam^T [j][r]
+constexpr uint32_t KT_DA = 256;  // dV U^T [r][s] (lanes 0..63)
+constexpr uint32_t KT_DM = 320;  // dO U^T [r][s] (lanes 0..63)
+constexpr uint32_t KT_P6 = 192;  // dXl^T [c][row], 128 (after lam, dA, dM are read)
+constexpr uint32_t KT_P7 = 320;  // dKb^T [c][col], 160
+constexpr uint32_t kKTmemCols = 512;
+
+// first Kb row (and dD1 column) of the block that refers the earlier tokens to P_g
+__device__ __forceinline__ int kb_base(int g) { return g == 1 ? 64 : g == 2 ? 80 : 112; }
+
+__global__ void __launch_bounds__(kKThreads, 1)
+    bwd_chunk_kernel(const __grid_constant__ CUtensorMap map_dut,
+                     const __grid_constant__ CUtensorMap map_n,
+                     const __grid_constant__ CUtensorMap map_ut,
+                     const __grid_constant__ CUtensorMap map_do,
+                     const __grid_constant__ CUtensorMap map_s0,
+                     const __grid_constant__ CUtensorMap map_ds, const ChunkArgs a,
+                     const BwdWs bw, const BwdOut o) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_wait_ok[4];
+  __shared__ __align__(16) float s_gtot[4][kD];
+  __shared__ __align__(16) float s_beta[kC], s_rk[kC], s_rq[kC];
+  __shared__ __align__(16) float s_lu[4][kC];
+  __shared__ __align__(16) float s_sdot[4][kD];
+  __shared__ __align__(16) float s_dgs[4][kD];
+  __shared__ __align__(16) float s_dgc[4][kD];
+  __shared__ __align__(16) float s_qd[4][kC], s_kd[4][kC];
+  __shared__ __align__(16) float s_ddb[4][kD];
+  __shared__ float s_dal[16];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int R = tid >> 7;      // sub-chunk (tokens 16 R .. 16 R + 15)
+  const int c = tid & 127;     // channel (Tensor Memory lane)
+  const int sp = warp & 3;     // Tensor Memory sub-partition
+  const int H = a.H;
+  const long long rec = blockIdx.x;
+  const int h = (int)(rec % H);
+  const long long slot = rec / H;
+  const int nck = bw.f.nck_fixed;
+  const int seq = (int)(slot / nck), jc = (int)(slot % nck);
+  const long long tok0 = (long long)seq * a.T + (long long)jc * kC;
+  const int n = min(kC, a.T - jc * kC);
+
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kKTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar_ld, kKLoadTx);
+    tma_load_2d(sm + K_DUT, &map_dut, &bar_ld, 0, (int)(rec * 128));
+    tma_load_2d(sm + K_NN, &map_n, &bar_ld, 0, (int)(rec * 64));
+    tma_load_2d(sm + K_UT, &map_ut, &bar_ld, 0, (int)(rec * 128));
+    tma_load_3d(sm + K_DO, &map_do, &bar_ld, 0, h, (int)tok0);
+    tma_load_3d(sm + K_DO + 8192, &map_do, &bar_ld, 64, h, (int)tok0);
+    tma_load_2d(sm + K_S0, &map_s0, &bar_ld, 0, (int)(rec * 128));
+    tma_load_2d(sm + K_S0 + 16384, &map_s0, &bar_ld, 64, (int)(rec * 128));
+    tma_load_2d(sm + K_DS, &map_ds, &bar_ld, 0, (int)(rec * 128));
+    tma_load_2d(sm + K_DS + 16384, &map_ds, &bar_ld, 64, (int)(rec * 128));
+  }
+  if (tid < kC) {
+    s_beta[tid] = (tid < n) ? sigmoidf_(a.beta_logits[(tok0 + tid) * H + h]) : 0.f;
+    s_rk[tid] = bw.f.vec[rec * 256 + 128 + tid];
+    s_rq[tid] = bw.f.vec[rec * 256 + 192 + tid];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t tl = tm + (uint32_t(32 * sp) << 16);
+  uint32_t mma_phase = 0;
+  uint32_t wait_calls = 0;
+  auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const uint32_t slot_w = wait_calls++ & 3;
+    if (tid == 0) s_wait_ok[slot_w] = mbar_wait(bar, parity) ? 1 : 0;
+    __syncthreads();
+    return s_wait_ok[slot_w] != 0;
+  };
+  bool ld_done = false;
+
+  const __nv_bfloat16* qin = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(a.k);
+  auto row_of = [&](int t) -> long long { return (tok0 + t) * H + h; };
+
+  // ---- gates: G_t - P_R for this thread's channel and sub-chunk
+  const float ea = __expf(a.a_log[h]);
+  const float db = a.dt_bias[c * H + h];
+  float loc[16];
+  {
+    float run = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * R + i;
+      float gm = 0.f;
+      if (t < n) gm = a.lower_bound * fast_rcp(1.f + fast_exp(-ea * (a.g[row_of(t) * kD + c] + db)));
+      run += gm;
+      loc[i] = run;
+    }
+    s_gtot[R][c] = run;
+  }
+  __syncthreads();
+  float P[4];
+  P[0] = 0.f;
+#pragma unroll
+  for (int r = 1; r < 4; ++r) P[r] = P[r - 1] + s_gtot[r - 1][c];
+  const float GC = P[3] + s_gtot[3][c];
+  float PR = P[0];
+#pragma unroll
+  for (int r = 1; r < 4; ++r) PR = (R == r) ? P[r] : PR;
+
+  // ---- operand tiles: Xl rows t (k^ e^{G_t - P_R}) and 64 + t (q^ e^{G_t - P_R}); Kb rows
+  //      t (k^ e^{P_R - G_t}) and base_g + t (k^ e^{P_g - G_t}) for the later sub-chunks g
+  {
+    float fg[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) fg[g] = (g > R) ? fast_exp(P[g] - PR) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * R + i;
+      float kh = 0.f, qh = 0.f;
+      if (t < n) {
+        kh = __bfloat162float(kin[row_of(t) * kD + c]) * s_rk[t];
+        qh = __bfloat162float(qin[row_of(t) * kD + c]) * s_rq[t];
+      }
+      const float e = fast_exp(loc[i]), ei = fast_exp(-loc[i]);
+      *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(t, c, 16384)) = __float2bfloat16_rn(kh * e);
+      *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(64 + t, c, 16384)) =
+          __float2bfloat16_rn(qh * e);
+      const float kd = kh * ei;
+      *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(t, c, 20480)) = __float2bfloat16_rn(kd);
+#pragma unroll
+      for (int g = 1; g < 4; ++g)
+        if (g > R)
+          *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(kb_base(g) + t, c, 20480)) =
+              __float2bfloat16_rn(kd * fg[g]);
+    }
+  }
+
+  // ---- loaded tiles: clear d_out rows past the chunk, S . dS' per channel (quarter of j)
+  if (!block_wait(&bar_ld, 0)) goto fail;
+  ld_done = true;
+  if (n < kC) zero_rows(sm + K_DO, n, tid);
+  {
+    float acc = 0.f;
+#pragma unroll 8
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = 32 * R + jj;
+      const uint32_t off = sw_off(j, c, 16384);
+      acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + K_S0 + off)) *
+             __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + K_DS + off));
+    }
+    s_sdot[R][c] = acc;
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- lam^T = dU^T N;  dQ~^T = S^T-as-MN x d_out;  dKd^T = dS'^T-as-MN x U^T-as-MN
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t dut = smem_u32(sm + K_DUT), nn = smem_u32(sm + K_NN), ut = smem_u32(sm + K_UT),
+                   dos = smem_u32(sm + K_DO), s0 = smem_u32(sm + K_S0), ds = smem_u32(sm + K_DS);
+    const uint32_t id_l = make_idesc(1, 128, 64, false, true);
+    const uint32_t id_p1 = make_idesc(1, 128, 64, true, false);
+    const uint32_t id_p3 = make_idesc(1, 128, 64, true, true);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      mma_ss(tm + KT_L, sw128_kdesc<2>(dut, 128, s), mn_desc(nn, 8192, s), id_l, s > 0);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      mma_ss(tm + KT_P1, mn_desc(s0, 16384, s), sw128_kdesc<2>(dos, 64, s), id_p1, s > 0);
+      mma_ss(tm + KT_P3, mn_desc(ds, 16384, s), mn_desc(ut, 8192, s), id_p3, s > 0);
+    }
+    mma_commit(&bar_mma);
+  }
+  if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
+  tc_fence_after();
+
+  // ---- lam -> dV (output and dV^T operand), lam . u per token
+  {
+    const int j = c;
+    float lam[16];
+    tmem_ld16(tl + KT_L + 16 * R, lam);
+    const uint32_t rowb = uint32_t(j >> 3) * 1024u + uint32_t(j & 7) * 128u;
+    const uint32_t ca = uint32_t(2 * R) ^ uint32_t(j & 7), cb = uint32_t(2 * R + 1) ^ uint32_t(j & 7);
+    const uint4 ua = *reinterpret_cast<const uint4*>(sm + K_UT + rowb + (ca << 4));
+    const uint4 ub = *reinterpret_cast<const uint4*>(sm + K_UT + rowb + (cb << 4));
+    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+    uint32_t dw[8];
+    float lu0[8], lu1[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int t0 = 16 * R + 2 * p;
+      const float v0 = s_beta[t0] * lam[2 * p], v1 = s_beta[t0 + 1] * lam[2 * p + 1];
+      dw[p] = pack_bf16(v0, v1);
+      if (t0 < n) o.dv[row_of(t0) * kD + j] = __float2bfloat16_rn(v0);
+      if (t0 + 1 < n) o.dv[row_of(t0 + 1) * kD + j] = __float2bfloat16_rn(v1);
+      const float l0 = lam[2 * p] * bf16_lo(uw[p]), l1 = lam[2 * p + 1] * bf16_hi(uw[p]);
+      if (p < 4) { lu0[2 * p] = l0; lu0[2 * p + 1] = l1; }
+      else { lu1[2 * (p - 4)] = l0; lu1[2 * (p - 4) + 1] = l1; }
+    }
+    *reinterpret_cast<uint4*>(sm + K_DUT + rowb + (ca << 4)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+    *reinterpret_cast<uint4*>(sm + K_DUT + rowb + (cb << 4)) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+    int tq;
+    const float s0v = reduce_scatter8(lu0, lane, tq);
+    const float s1v = reduce_scatter8(lu1, lane, tq);
+    if ((lane & 3) == 0) {
+      s_lu[sp][16 * R + tq] = s0v;
+      s_lu[sp][16 * R + 8 + tq] = s1v;
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- -dK~^T (as dV S^T), dV U^T and dO U^T (rows 64..127 of the last two A operands
+  //      are unused)
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t dvt = smem_u32(sm + K_DUT), ut = smem_u32(sm + K_UT),
+                   dos = smem_u32(sm + K_DO), s0 = smem_u32(sm + K_S0);
+    const uint32_t id_p2 = make_idesc(1, 128, 64, true, true);
+    const uint32_t id_dm = make_idesc(1, 128, 64, false, true);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      mma_ss(tm + KT_P2, mn_desc(s0, 16384, s), mn_desc(dvt, 8192, s), id_p2, s > 0);
+      mma_ss(tm + KT_DA, mn_desc(dvt, 16384, s), mn_desc(ut, 8192, s), id_p2, s > 0);
+      mma_ss(tm + KT_DM, sw128_kdesc<2>(dos, 64, s), mn_desc(ut, 8192, s), id_dm, s > 0);
+    }
+    mma_commit(&bar_mma);
+  }
+  if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
+  tc_fence_after();
+
+  // ---- dD1 = [dA; dM] in the column layout of the forward's Kb rows; dbeta_logits
+  if (sp < 2) {
+    float da[16], dm[16];
+    tmem_ld16(tl + KT_DA + 16 * R, da);
+    tmem_ld16(tl + KT_DM + 16 * R, dm);
+    const int r = 32 * sp + lane, Rr = r >> 4;
+    const bool live = r < n;
+    uint32_t wa[8], wm[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int s0 = 16 * R + 2 * p;
+      wa[p] = pack_bf16((live && s0 < r) ? -da[2 * p] : 0.f, (live && s0 + 1 < r) ? -da[2 * p + 1] : 0.f);
+      wm[p] = pack_bf16((live && s0 <= r) ? dm[2 * p] : 0.f, (live && s0 + 1 <= r) ? dm[2 * p + 1] : 0.f);
+    }
+    auto put = [&](int row, int col0, bool on, const uint32_t (&w)[8]) {
+      uint8_t* t = sm + K_D1;
+      const uint4 lo = on ? make_uint4(w[0], w[1], w[2], w[3]) : make_uint4(0, 0, 0, 0);
+      const uint4 hi = on ? make_uint4(w[4], w[5], w[6], w[7]) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(t + sw_off(row, col0, 16384)) = lo;
+      *reinterpret_cast<uint4*>(t + sw_off(row, col0 + 8, 16384)) = hi;
+    };
+    put(r, 16 * R, R == Rr, wa);
+    put(64 + r, 16 * R, R == Rr, wm);
+#pragma unroll
+    for (int g = 1; g < 4; ++g)
+      if (g > R) {
+        put(r, kb_base(g) + 16 * R, Rr == g, wa);
+        put(64 + r, kb_base(g) + 16 * R, Rr == g, wm);
+      }
+  } else if (tid >= 64 && tid < 64 + kC) {  // warps 2 and 3 (sub-partitions 2, 3)
+    const int t = tid - 64;
+    if (t < n)
+      o.dbeta_logits[row_of(t)] =
+          (1.f - s_beta[t]) * (s_lu[0][t] + s_lu[1][t] + s_lu[2][t] + s_lu[3][t]);
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- dXl^T = Kb-as-MN x dD1 (K = 160 Kb rows), dKb^T = Xl-as-MN x dD1-as-MN
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t kb = smem_u32(sm + K_KB), xl = smem_u32(sm + K_XL), d1 = smem_u32(sm + K_D1);
+    const uint32_t id_p6 = make_idesc(1, 128, 128, true, false);
+    const uint32_t id_p7 = make_idesc(1, 128, 160, true, true);
+#pragma unroll
+    for (int s = 0; s < 10; ++s)
+      mma_ss(tm + KT_P6, mn_desc(kb, 20480, s), sw128_kdesc<2>(d1, 128, s), id_p6, s > 0);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      mma_ss(tm + KT_P7, mn_desc(xl, 16384, s), mn_desc(d1, 16384, s), id_p7, s > 0);
+    mma_commit(&bar_mma);
+  }
+  if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
+  tc_fence_after();
+
+  // ---- epilogue: per (channel c, token t of sub-chunk R)
+  {
+    float* AQ = reinterpret_cast<float*>(sm + K_AQ);
+    float* DKH = reinterpret_cast<float*>(sm + K_DKH);
+    const float eP = fast_exp(PR), eCP = fast_exp(GC - PR);
+    float fg[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) fg[g] = (g > R) ? fast_exp(P[g] - PR) : 0.f;
+    float dG[16];
+    float dgc = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int cb = 16 * R + 8 * hh;  // first token of this half
+      float e[8], ei[8], kh[8], qh[8], aq[8], pos[8], neg[8], t8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int t = cb + i;
+        e[i] = fast_exp(loc[8 * hh + i]);
+        ei[i] = fast_exp(-loc[8 * hh + i]);
+        kh[i] = (t < n) ? __bfloat162float(kin[row_of(t) * kD + c]) * s_rk[t] : 0.f;
+        qh[i] = (t < n) ? __bfloat162float(qin[row_of(t) * kD + c]) * s_rq[t] : 0.f;
+      }
+      // dq^, dk^ (exact gate factors) and dG; each Xl / Kb term of dG is weighted by the bf16
+      // operand value the product used, so that the +G and -G terms of a pair (r, s) of the
+      // gate-scaled products cancel as they do in exact arithmetic
+      float dG8[8];
+      tmem_ld8(tl + KT_P1 + cb, t8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        aq[i] = eP * e[i] * t8[i];
+        dG8[i] = qh[i] * aq[i];
+      }
+      tmem_ld8(tl + KT_P6 + 64 + cb, t8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        aq[i] += e[i] * t8[i];
+        dG8[i] += bf16_round(qh[i] * e[i]) * t8[i];
+      }
+      tmem_ld8(tl + KT_P2 + cb, t8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        pos[i] = -eP * e[i] * t8[i];
+        dG8[i] += kh[i] * pos[i];
+      }
+      tmem_ld8(tl + KT_P6 + cb, t8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        pos[i] += e[i] * t8[i];
+        dG8[i] += bf16_round(kh[i] * e[i]) * t8[i];
+      }
+      tmem_ld8(tl + KT_P3 + cb, t8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        neg[i] = eCP * ei[i] * t8[i];
+        dgc += kh[i] * neg[i];
+        dG8[i] -= kh[i] * neg[i];
+      }
+      tmem_ld8(tl + KT_P7 + cb, t8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float kd = kh[i] * ei[i];
+        neg[i] += ei[i] * t8[i];
+        dG8[i] -= bf16_round(kd) * t8[i];
+      }
+#pragma unroll
+      for (int g = 1; g < 4; ++g)
+        if (g > R) {
+          tmem_ld8(tl + KT_P7 + kb_base(g) + cb, t8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float kd = kh[i] * ei[i];
+            neg[i] += ei[i] * fg[g] * t8[i];
+            dG8[i] -= bf16_round(kd * fg[g]) * t8[i];
+          }
+        }
+      float qd[8], kd[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float dkh = pos[i] + neg[i];
+        dG[8 * hh + i] = dG8[i];
+        AQ[(cb + i) * kD + c] = aq[i];
+        DKH[(cb + i) * kD + c] = dkh;
+        qd[i] = qh[i] * aq[i];
+        kd[i] = kh[i] * dkh;
+      }
+      int tq;
+      const float qs = reduce_scatter8(qd, lane, tq);
+      const float ks = reduce_scatter8(kd, lane, tq);
+      if ((lane & 3) == 0) {
+        s_qd[sp][cb + tq] = qs;
+        s_kd[sp][cb + tq] = ks;
+      }
+    }
+    {
+      float sg = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sg += dG[i];
+      s_dgs[R][c] = sg;
+      s_dgc[R][c] = dgc;
+    }
+    __syncthreads();
+    // dgamma_t = sum_{r >= t} dG_r + dG_C
+    const float dGC = s_dgc[0][c] + s_dgc[1][c] + s_dgc[2][c] + s_dgc[3][c] +
+                      fast_exp(GC) * (s_sdot[0][c] + s_sdot[1][c] + s_sdot[2][c] + s_sdot[3][c]);
+    float carry = dGC;
+#pragma unroll
+    for (int r = 1; r < 4; ++r)
+      if (r > R) carry += s_dgs[r][c];
+    float ddb = 0.f, dal = 0.f;
+    const float inv_s2 = 1.f / (a.scale * a.scale);
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {
+      carry += dG[i];
+      const int t = 16 * R + i;
+      if (t < n) {
+        const long long row = row_of(t);
+        // gate: gamma = lb sigmoid(x), x = e^{a_log} (g + dt_bias)
+        const float x = ea * (a.g[row * kD + c] + db);
+        const float sg = sigmoidf_(x);
+        const float dx = carry * a.lower_bound * sg * (1.f - sg);
+        o.dg[row * kD + c] = dx * ea;
+        ddb += dx * ea;
+        dal += dx * x;
+        // L2 norms: q^ = rq q with rq = scale / |q|, k^ = rk k
+        const float qdt = s_qd[0][t] + s_qd[1][t] + s_qd[2][t] + s_qd[3][t];
+        const float kdt = s_kd[0][t] + s_kd[1][t] + s_kd[2][t] + s_kd[3][t];
+        const float rq = s_rq[t], rk = s_rk[t];
+        const float qh = __bfloat162float(qin[row * kD + c]) * rq;
+        const float kh = __bfloat162float(kin[row * kD + c]) * rk;
+        o.dq[row * kD + c] = __float2bfloat16_rn(rq * AQ[t * kD + c] - qh * qdt * rq * inv_s2);
+        o.dk[row * kD + c] = __float2bfloat16_rn(rk * DKH[t * kD + c] - kh * kdt * rk);
+      }
+    }
+    s_ddb[R][c] = ddb;
+    dal = warp_sum(dal);
+    if (lane == 0) s_dal[warp] = dal;
+    __syncthreads();
+    if (R == 0) atomicAdd(&o.ddt_bias[c * H + h], s_ddb[0][c] + s_ddb[1][c] + s_ddb[2][c] + s_ddb[3][c]);
+    if (tid == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < 16; ++w) t += s_dal[w];
+      atomicAdd(&o.da_log[h], t);
+    }
+  }
+  goto done;
+
+fail:
+  if (tid == 0) {
+    atomicOr(&g_bwd_error, 4u);
+    if (!ld_done) mbar_wait(&bar_ld, 0, 1000000000ull);
+    if (mma_phase > 0) mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, kKTmemCols);
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace(const ChunkArgs& a) {
+  const long long recs = slots_for(a) * a.H;
+  return align_up(record_bytes(recs), 256) +
+         size_t(recs) * size_t(kRecM + kRecState + kRecTile + kRecState + kRecTile);
+}
+
+bool chunk_bwd_supported(const ChunkArgs& a, bool bf16) {
+  return bf16 && a.dk == 128 && a.dv == 128 && a.chunk == 64 && !a.cu_seqlens && !a.gate_head &&
+         !a.beta_prob && !a.no_l2norm && !a.literal && a.T > 0 &&
+         slots_for(a) * a.H * 256 < 0x7fffffffLL;
+}
+
+cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float* d_final,
+                             void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
+                             float* da_log, float* ddt_bias, float* d_initial, void* workspace,
+                             cudaStream_t st) {
+  BwdWs bw{};
+  uint8_t* p = static_cast<uint8_t*>(workspace);
+  carve_records(a, p, bw.f);
+  const long long recs = bw.f.recs;
+  p += align_up(record_bytes(recs), 256);
+  bw.f.nrec = reinterpret_cast<__nv_bfloat16*>(p);
+  p += recs * kRecM;
+  bw.f.s0 = reinterpret_cast<__nv_bfloat16*>(p);
+  p += recs * kRecState;
+  bw.f.ut = reinterpret_cast<__nv_bfloat16*>(p);
+  p += recs * kRecTile;
+  bw.ds = reinterpret_cast<__nv_bfloat16*>(p);
+  p += recs * kRecState;
+  bw.dut = reinterpret_cast<__nv_bfloat16*>(p);
+  bw.f.bwd = 1;
+  BwdOut o{};
+  o.d_final = d_final;
+  o.dq = static_cast<__nv_bfloat16*>(dq);
+  o.dk = static_cast<__nv_bfloat16*>(dk);
+  o.dv = static_cast<__nv_bfloat16*>(dv);
+  o.dg = dg;
+  o.dbeta_logits = dbeta_logits;
+  o.da_log = da_log;
+  o.ddt_bias = ddt_bias;
+  o.d_initial = d_initial;
+
+  cudaError_t e = cudaMemsetAsync(da_log, 0, sizeof(float) * a.H, st);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * kD * a.H, st)) != cudaSuccess) return e;
+  ChunkArgs f = a;
+  f.out = nullptr;
+  f.final_state = nullptr;
+  if ((e = split::launch_prep_scan(f, bw.f, st)) != cudaSuccess) return e;
+
+  const long long rows = (long long)a.B * a.T;
+  CUtensorMap mqw, mku, mm, mdo, mdut, mn, mut, ms0, mds;
+  if (!make_map_2d(&mqw, bw.f.qw, 2 * recs * 64, 128, 64) ||
+      !make_map_2d(&mku, bw.f.ku, 2 * recs * 128, 64, 128) ||
+      !make_map_2d(&mm, bw.f.m, recs * 64, 64, 64) || !make_map_in(&mdo, d_out, rows, a.H, false) ||
+      !make_map_2d(&mdut, bw.dut, recs * 128, 64, 128) ||
+      !make_map_2d(&mn, bw.f.nrec, recs * 64, 64, 64) ||
+      !make_map_2d(&mut, bw.f.ut, recs * 128, 64, 128) ||
+      !make_map_2d(&ms0, bw.f.s0, recs * 128, 128, 128) ||
+      !make_map_2d(&mds, bw.ds, recs * 128, 128, 128))
+    return cudaErrorInvalidValue;
+  if ((e = cudaFuncSetAttribute(bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kBSSmem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kKSmem)) != cudaSuccess)
+    return e;
+  bwd_scan_kernel<<<dim3(a.H, a.B), kBSThreads, kBSSmem, st>>>(mqw, mku, mm, mdo, a, bw, o);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_chunk_kernel<<<(unsigned)recs, kKThreads, kKSmem, st>>>(mdut, mn, mut, mdo, ms0, mds, a, bw,
+                                                               o);
+  return cudaGetLastError();
+}
+
+unsigned int chunk_bwd_read_error(bool reset) {
+  unsigned int v = 0;
+  cudaMemcpyFromSymbol(&v, g_bwd_error, sizeof(v));
+  if (reset) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_bwd_error, &z, sizeof(z));
+  }
+  return v;
+}
+
+}  // namespace kda

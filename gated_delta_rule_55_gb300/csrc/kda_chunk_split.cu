@@ -25,41 +25,14 @@
 //
 // The algebra is that of the single-pass kernel (kda_chunk_tc.cu); here the key side of
 // every chunk runs on all SMs at once instead of inside the per-sequence scan.
-#include <algorithm>
-
-#include "chunk_common.cuh"
+#include "chunk_records.cuh"
 
 namespace kda {
 namespace {
 
 using namespace tc;
 using namespace chunk;
-
-constexpr int kC = 64;
-constexpr int kD = 128;
-
-// ---------------------------------------------------------------- workspace records
-
-constexpr long long kRecTile = 64LL * 128 * 2;  // one [64 x 128] (or [128 x 64]) bf16 tile
-constexpr long long kRecM = 64LL * 64 * 2;
-constexpr long long kRecVec = 256 * 4;          // e^{G_C}[128], rk[64], rq[64]
-
-struct Ws {
-  __nv_bfloat16* qw;   // [2 * recs * 64][128]: Q~ records, then -W records
-  __nv_bfloat16* ku;   // [2 * recs * 128][64]: K^^T records, then U~^T records
-  __nv_bfloat16* m;    // [recs * 64][64]
-  float* vec;          // [recs][256]
-  int32_t* coff;       // [N + 1] first chunk slot of each sequence (packed inputs only)
-  long long recs;      // chunk slots x heads
-  int nck_fixed;       // chunks per sequence (fixed-length inputs)
-};
-
-long long slots_for(const ChunkArgs& a) {
-  if (a.cu_seqlens) return (long long)a.total_T / kC + a.B;
-  return (long long)a.B * ((a.T + kC - 1) / kC);
-}
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+using namespace split;
 
 // ------------------------------------------------------------------- prep kernel
 
@@ -382,7 +355,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
           if (R < 1) *reinterpret_cast<uint32_t*>(p160 + swi + 8 * 1024) = hmul2(kd, c12);
           if (R < 2) *reinterpret_cast<uint32_t*>(p160 + swi + 10 * 1024) = hmul2(kd, c22);
           if (R < 3) *reinterpret_cast<uint32_t*>(p160 + swi + 14 * 1024) = hmul2(kd, c32);
-          *reinterpret_cast<uint32_t*>(qrec + i * kD) = hmul2(xq, eP2);  // q e^{G_t}
+          if (ws.bwd) {  // q^ e^{G_t} = rq q e^{G_t}
+            const int t = 16 * R + i;
+            const float rqt =
+                (t < n) ? a.scale * rsqrtf(s_qq[0][t] + s_qq[1][t] + kL2Eps) : 0.f;
+            *reinterpret_cast<uint32_t*>(qrec + i * kD) =
+                pack_bf16(bf16_lo(qw[i]) * e0 * eP0 * rqt, bf16_hi(qw[i]) * e1 * eP1 * rqt);
+          } else {
+            *reinterpret_cast<uint32_t*>(qrec + i * kD) = hmul2(xq, eP2);  // q e^{G_t}
+          }
           khw[ii] = hmul2(kd, eCP2);  // k e^{G_C - G_t}
           ktw[ii] = hmul2(xk, eP2);   // k e^{G_t}
         }
@@ -471,10 +452,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
         }
       } else {
         uint32_t pk[8];
+        const float mf = ws.bwd ? s_rq[r] : 1.f;  // backward records: rows of rq_r M_raw
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           const int s0 = 16 * q + 2 * p;
-          pk[p] = pack_bf16((s0 <= r) ? v[2 * p] : 0.f, (s0 + 1 <= r) ? v[2 * p + 1] : 0.f);
+          pk[p] = pack_bf16((s0 <= r) ? mf * v[2 * p] : 0.f,
+                            (s0 + 1 <= r) ? mf * v[2 * p + 1] : 0.f);
         }
         uint4* mrec = reinterpret_cast<uint4*>(ws.m + (rec * 64 + r) * 64 + 16 * q);
         mrec[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -535,6 +518,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
           pw[p] = pack_bf16(t0v * kv[2 * p], t1v * kv[2 * p + 1]);
         }
         const uint32_t off = sw128_offset<2>(64, r, s0);
+        if (ws.bwd) {  // N = (I + L)^{-1}, lower triangle, row r, columns s0 .. s0 + 7
+          uint32_t pn[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            pn[p] = pack_bf16((s0 + 2 * p <= r) ? xv[2 * p] : 0.f,
+                              (s0 + 2 * p + 1 <= r) ? xv[2 * p + 1] : 0.f);
+          *reinterpret_cast<uint4*>(ws.nrec + (rec * 64 + r) * 64 + s0) =
+              make_uint4(pn[0], pn[1], pn[2], pn[3]);
+        }
         *reinterpret_cast<uint4*>(sm + P_T + off) = make_uint4(pt[0], pt[1], pt[2], pt[3]);
         *reinterpret_cast<uint4*>(sm + P_TW + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       }
@@ -632,6 +624,7 @@ constexpr int S_M = 65536;      // M_raw [64 x 64]
 constexpr int S_V = 73728;      // e^{G_C}, rk, rq
 constexpr int kStage = 74752;
 constexpr uint32_t kStageTx = 74752;
+constexpr uint32_t kStageTxBwd = kStageTx - 2 * 8192 - 8192;  // no Q~, no M
 constexpr int S_OS = 2 * kStage;  // output staging [64 tok x 128] bf16 SW128
 constexpr int S_END = S_OS + 16384;
 static_assert(kStage % 1024 == 0 && S_OS % 1024 == 0, "alignment");
@@ -704,15 +697,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const long long rec = (slot0 + ch) * H + h;
     uint8_t* b = sm + st * kStage;
     uint64_t* bar = &bar_ld[st];
-    mbar_arrive_expect_tx(bar, kStageTx);
+    mbar_arrive_expect_tx(bar, ws.bwd ? kStageTxBwd : kStageTx);
     const int rq = (int)(rec * 64), rw = (int)((ws.recs + rec) * 64);
-    tma_load_2d(b + S_Q, &map_qw, bar, 0, rq);
-    tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, rq);
+    if (!ws.bwd) {  // the backward's forward pass computes no output
+      tma_load_2d(b + S_Q, &map_qw, bar, 0, rq);
+      tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, rq);
+      tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64));
+    }
     tma_load_2d(b + S_W, &map_qw, bar, 0, rw);
     tma_load_2d(b + S_W + 8192, &map_qw, bar, 64, rw);
     tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128));
     tma_load_2d(b + S_UT, &map_ku, bar, 0, (int)((ws.recs + rec) * 128));
-    tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64));
     bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar);
   };
   // chunk whose record is in flight into each stage (-1: none); same on every thread
@@ -735,6 +730,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
     tmem_st16(tl + S_TM_SA + 16 * wg, w);
+    if (ws.bwd && nck > 0) {  // the state entering chunk 0
+      uint4* d = reinterpret_cast<uint4*>(ws.s0 + ((slot0 * H + h) * 128 + ln) * 128 + 32 * wg);
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        d[p] = make_uint4(w[4 * p], w[4 * p + 1], w[4 * p + 2], w[4 * p + 3]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -778,7 +779,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         mma_ts(tm + S_TM_DU, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(ws_, 64, s), idesc_n64, s > 0);
-        mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
+        if (!ws.bwd)
+          mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
       }
       mma_commit(&bar_mma);
     }
@@ -806,6 +808,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
         up[i] = pack_bf16((bf16_lo(uw[i]) + v16[2 * i]) * vec[128 + 16 * wg + 2 * i],
                           (bf16_hi(uw[i]) + v16[2 * i + 1]) * vec[128 + 16 * wg + 2 * i + 1]);
       tmem_st8(tl + S_TM_UA + 8 * wg, up);
+      if (ws.bwd) {  // U^T of this chunk (before the rk row factor)
+        uint32_t u8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          u8[i] = pack_bf16(bf16_lo(uw[i]) + v16[2 * i], bf16_hi(uw[i]) + v16[2 * i + 1]);
+        uint4* d = reinterpret_cast<uint4*>(ws.ut + (((slot0 + ch) * H + h) * 128 + ln) * 64 +
+                                            16 * wg);
+        d[0] = make_uint4(u8[0], u8[1], u8[2], u8[3]);
+        d[1] = make_uint4(u8[4], u8[5], u8[6], u8[7]);
+      }
     }
     tc_fence_before();
     __syncthreads();
@@ -817,7 +829,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const uint32_t ms = smem_u32(b + S_M), ks = smem_u32(b + S_KT);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        mma_ts(tm + S_TM_DO, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ms, 64, s), idesc_n64, 1);
+        if (!ws.bwd)
+          mma_ts(tm + S_TM_DO, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ms, 64, s), idesc_n64, 1);
         mma_ts(tm + S_TM_S, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ks, 128, s), idesc_n128, 1);
       }
       mma_commit(&bar_mma);
@@ -835,31 +848,41 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) sp[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
       tmem_st16(tl + S_TM_SA + 16 * wg, sp);
-      float o16[16];
-      tmem_ld16(tl + S_TM_DO + 16 * wg, o16);
-      if (n == kC) {
-        const uint32_t ob = uint32_t(ln >> 6) * 8192u + uint32_t(wg) * 2048u;
-        const uint32_t och = uint32_t(((ln & 63) * 2) >> 4), oby = uint32_t(((ln & 63) * 2) & 15);
+      if (ws.bwd) {
+        if (ch + 1 < nck) {  // the state entering the next chunk
+          uint4* d = reinterpret_cast<uint4*>(
+              ws.s0 + (((slot0 + ch + 1) * H + h) * 128 + ln) * 128 + 32 * wg);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t off = ob + uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
-                               (((och ^ uint32_t(i & 7)) << 4) | oby);
-          *reinterpret_cast<__nv_bfloat16*>(sm + S_OS + off) =
-              __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+          for (int p = 0; p < 4; ++p)
+            d[p] = make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
         }
       } else {
-        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
-                            ((tok0 + 16 * wg) * H + h) * kD + ln;
-        const long long stride = (long long)H * kD;
+        float o16[16];
+        tmem_ld16(tl + S_TM_DO + 16 * wg, o16);
+        if (n == kC) {
+          const uint32_t ob = uint32_t(ln >> 6) * 8192u + uint32_t(wg) * 2048u;
+          const uint32_t och = uint32_t(((ln & 63) * 2) >> 4), oby = uint32_t(((ln & 63) * 2) & 15);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (16 * wg + i < n) op[i * stride] = __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t off = ob + uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
+                                 (((och ^ uint32_t(i & 7)) << 4) | oby);
+            *reinterpret_cast<__nv_bfloat16*>(sm + S_OS + off) =
+                __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+          }
+        } else {
+          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
+                              ((tok0 + 16 * wg) * H + h) * kD + ln;
+          const long long stride = (long long)H * kD;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (16 * wg + i < n) op[i * stride] = __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+        }
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0 && !ws.bwd) {
       if (n == kC) {
         tma_store_3d(&map_o, sm + S_OS, 0, h, (int)tok0);
         tma_store_3d(&map_o, sm + S_OS + 8192, 64, h, (int)tok0);
@@ -945,74 +968,12 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
 
 // ------------------------------------------------------------------------- host
 
-bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int inner, int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
-// [rows, H, 128] bf16 output, box {64 ch, 1 head, 64 tokens}, 128-byte swizzle.
-bool make_map_out(CUtensorMap* m, const void* base, long long rows, int H) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-  cuuint32_t box[3] = {64, 1, 64};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
-// [rows, H, 128] inputs, box {64 ch, 1 head, 64 tokens} bf16 with 128-byte swizzle, or
-// {32 ch, 1, 64} fp32 without swizzle; rows past the end read as zeros.
-bool make_map_in(CUtensorMap* m, const void* base, long long rows, int H, bool fp32) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  const int es = fp32 ? 4 : 2;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)kD * es, (cuuint64_t)H * kD * es};
-  cuuint32_t box[3] = {fp32 ? 32u : 64u, 1, 64};
-  cuuint32_t elem[3] = {1, 1, 1};
-  return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-             const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             fp32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
-bool carve(const ChunkArgs& a, void* base, Ws& ws) {
-  const long long slots = slots_for(a);
-  const long long recs = slots * a.H;
-  uint8_t* p = static_cast<uint8_t*>(base);
-  ws.recs = recs;
-  ws.nck_fixed = a.cu_seqlens ? 0 : (a.T + kC - 1) / kC;
-  ws.qw = reinterpret_cast<__nv_bfloat16*>(p);
-  p += 2 * recs * kRecTile;
-  ws.ku = reinterpret_cast<__nv_bfloat16*>(p);
-  p += 2 * recs * kRecTile;
-  ws.m = reinterpret_cast<__nv_bfloat16*>(p);
-  p += recs * kRecM;
-  ws.vec = reinterpret_cast<float*>(p);
-  p += recs * kRecVec;
-  ws.coff = reinterpret_cast<int32_t*>(p);
-  return true;
-}
-
 }  // namespace
 
 size_t chunk_split_workspace(const ChunkArgs& a) {
   const long long recs = slots_for(a) * a.H;
   const size_t coff = a.cu_seqlens ? align_up(size_t(a.B + 1) * 4, 256) : 0;
-  return size_t(recs) * size_t(4 * kRecTile + kRecM + kRecVec) + coff;
+  return record_bytes(recs) + coff;
 }
 
 bool chunk_split_index_ok(const ChunkArgs& a) {
@@ -1020,17 +981,16 @@ bool chunk_split_index_ok(const ChunkArgs& a) {
   return slots_for(a) * a.H * 256 < 0x7fffffffLL;
 }
 
-cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t st) {
-  Ws ws{};
-  carve(a, workspace, ws);
+cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream_t st) {
   const long long rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
   const long long map_rows = rows > 0 ? rows : 1;
   const long long rec_rows = ws.recs > 0 ? ws.recs : 1;
   CUtensorMap mqw, mku, mm, mo, mq, mk, mv, mg;
+  // the backward's scan writes no output: its (unused) output map is laid over q
   if (!make_map_2d(&mqw, ws.qw, 2 * rec_rows * 64, 128, 64) ||
       !make_map_2d(&mku, ws.ku, 2 * rec_rows * 128, 64, 128) ||
       !make_map_2d(&mm, ws.m, rec_rows * 64, 64, 64) ||
-      !make_map_out(&mo, a.out, map_rows, a.H) ||
+      !make_map_out(&mo, ws.bwd ? a.q : a.out, map_rows, a.H) ||
       !make_map_in(&mq, a.q, map_rows, a.H, false) ||
       !make_map_in(&mk, a.k, map_rows, a.H, false) ||
       !make_map_in(&mv, a.v, map_rows, a.H, false) || !make_map_in(&mg, a.g, map_rows, a.H, true))
@@ -1041,10 +1001,6 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t
   e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSSmem);
   if (e != cudaSuccess) return e;
-  if (a.cu_seqlens) {
-    chunk_offsets_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.B, a.total_T, ws.coff);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
   if (ws.recs > 0) {
     // persistent: two CTAs per SM (shared memory and Tensor Memory admit no more)
     int dev = 0, sms = 0;
@@ -1057,6 +1013,17 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t
   }
   chunk_scan_kernel<<<dim3(a.H, a.B), kSThreads, kSSmem, st>>>(mqw, mku, mm, mo, a, ws);
   return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t st) {
+  Ws ws{};
+  carve_records(a, workspace, ws);
+  if (a.cu_seqlens) {
+    chunk_offsets_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.B, a.total_T, ws.coff);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return split::launch_prep_scan(a, ws, st);
 }
 
 unsigned int chunk_split_read_error(bool reset) {

@@ -87,6 +87,15 @@ cudaError_t launch_backward(const ChunkArgs& f, const void* d_out, const float* 
                             void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
                             float* da_log, float* ddt_bias, float* d_initial, void* workspace,
                             bool bf16, cudaStream_t stream);
+// Chunked tensor-core backward (bf16, dk = dv = 128, 64-token chunks, fixed length, default
+// variant): forward records and states, reverse chunk scan, per-chunk products.
+bool chunk_bwd_supported(const ChunkArgs& a, bool bf16);
+size_t chunk_bwd_workspace(const ChunkArgs& a);
+cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float* d_final,
+                             void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
+                             float* da_log, float* ddt_bias, float* d_initial, void* workspace,
+                             cudaStream_t stream);
+unsigned int chunk_bwd_read_error(bool reset);
 cudaError_t launch_gla(const GlaArgs& a, bool bf16, cudaStream_t stream);
 // Sequential (token by token) scan: any supported shape, dtype and variant.
 cudaError_t launch_recurrent(const ChunkArgs& a, bool bf16, cudaStream_t stream);

@@ -70,7 +70,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_fwd_varlen_ws.argtypes = L.kda_chunk_fwd_varlen.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_noalloc.argtypes = L.kda_chunk_fwd.argtypes
     L.kda_recurrent_attention_fwd.argtypes = ([_P] * 7 + [_F] + [_P] * 4 + [_I] * 8 + [_P])
-    L.kda_chunk_bwd_workspace_size.argtypes = [_I] * 5
+    L.kda_chunk_bwd_workspace_size.argtypes = [_I] * 6
     L.kda_chunk_bwd_workspace_size.restype = _Z
     L.kda_chunk_bwd.argtypes = ([_P] * 7 + [_F, _F] + [_P] * 11 + [_I] * 6 + [_P, _Z, _P])
     L.kda_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
@@ -216,9 +216,9 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_
         B, T, H, dk, dv, chunk, _dtype_code(q, dtype), _stream(stream)))
 
 
-def kda_chunk_bwd_workspace_size(B, T, H, dk, dv) -> int:
-    """Device workspace bytes kda_chunk_bwd needs."""
-    return int(lib().kda_chunk_bwd_workspace_size(B, T, H, dk, dv))
+def kda_chunk_bwd_workspace_size(B, T, H, dk, dv, dtype=KDA_BF16) -> int:
+    """Device workspace bytes kda_chunk_bwd needs for q/k/v of `dtype` (0: unsupported)."""
+    return int(lib().kda_chunk_bwd_workspace_size(B, T, H, dk, dv, dtype))
 
 
 def kda_chunk_bwd(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, initial_state,

@@ -173,10 +173,13 @@ int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
  * kda_chunk_bwd -- gradients of the kda_chunk_fwd forward (fixed-length sequences, decay
  *   first) for L = <d_out, out> + <d_final_state, final_state>.  The pages give no backward
  *   pass (the kernel_delta_attention page presents the chunked mode as the training path):
- *   this is reverse-mode differentiation of the token recurrence, computed by a forward
- *   scan that checkpoints the state every 64 tokens, a reverse scan that recomputes each
- *   chunk's states from its checkpoint, and an elementwise pass for the norm, sigmoid and
- *   gate chain rules.
+ *   this is reverse-mode differentiation of the recurrence.  For bf16 with dk = dv = 128 it
+ *   runs on the chunk form (64-token chunks, tensor cores): the forward's chunk records
+ *   and per-chunk states, a reverse scan over chunks carrying the state's adjoint, and one
+ *   pass over all (chunk, head) pairs for the remaining products and the norm, sigmoid and
+ *   gate chain rules.  Other shapes and fp32 differentiate token by token: a forward scan
+ *   that checkpoints the state every 64 tokens, a reverse scan that recomputes each
+ *   chunk's states from its checkpoint, and an elementwise pass for the chain rules.
  *
  *   Inputs: those of kda_chunk_fwd (q, k, v, g, beta_logits, a_log, dt_bias, scale,
  *   lower_bound, initial_state; same layouts, dtype for q/k/v) and
@@ -188,11 +191,13 @@ int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
  *     da_log         [H] fp32        ddt_bias       [dk, H] fp32   (sums over B and T)
  *     d_initial_state [B, H, dk, dv] fp32 or NULL (not wanted)
  *   dim_k, dim_v   the head dimensions dk, dv (named apart from the dk / dv gradients)
- *   workspace / workspace_bytes: device scratch of at least kda_chunk_bwd_workspace_size()
- *   bytes, 256-byte aligned (checkpoints, one chunk of states per (sequence, head) and
- *   per-token fp32 intermediates).
+ *   workspace / workspace_bytes: device scratch of at least
+ *   kda_chunk_bwd_workspace_size(B, T, H, dk, dv, dtype) bytes, 256-byte aligned (chunk
+ *   records and bf16 states and adjoints per (chunk, head) on the tensor-core path;
+ *   checkpoints, one chunk of states per (sequence, head) and per-token fp32 intermediates
+ *   otherwise).  0 is returned for unsupported arguments.
  */
-size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv);
+size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int dtype);
 int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   const float* beta_logits, const float* a_log, const float* dt_bias,
                   float scale, float lower_bound, const float* initial_state, const void* d_out,
@@ -291,8 +296,8 @@ int kda_version(void);
  * kda_device_error -- bitmask of errors that kernels recorded on the current device since
  *   the last reset (no paper counterpart: it reports the kernels' own safeguards).
  *   Bit 0: a bounded wait inside the single-pass tensor-core chunk kernel gave up; bit 1:
- *   one inside the two-launch (workspace) chunk kernels did (the outputs of that launch
- *   are incomplete).  Synchronises the device.  reset != 0 clears the mask.
+ *   one inside the two-launch (workspace) chunk kernels did; bit 2: one inside the
+ *   chunked backward's kernels did (the outputs of that launch are incomplete).  Synchronises the device.  reset != 0 clears the mask.
  *   Returns the mask (>= 0) or KDA_ERR_DEVICE.
  */
 int kda_device_error(int reset);

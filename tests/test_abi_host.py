@@ -202,18 +202,38 @@ def test_attention_without_device(L):
         assert _attn(L, flags=flags) == -9
 
 
-def test_backward_workspace_size_formula(L):
-    """Checkpoints every 64 tokens, one chunk of states per (sequence, head), and per
-    32-column value slice three fp32 per-token [dk] partial sums and one fp32 per-token
-    scalar, each region 256-byte aligned."""
-    def al(x):
-        return (x + 255) // 256 * 256
-    B, T, H, dk, dv = 2, 150, 3, 128, 64
+def _al(x):
+    return (x + 255) // 256 * 256
+
+
+def _token_bwd_ws(B, T, H, dk, dv):
     nck, ns = (T + 63) // 64, dv // 32
-    want = (al(B * H * nck * dk * dv * 4) + al(B * H * 64 * dk * dv * 4) +
-            3 * al(ns * B * T * H * dk * 4) + al(ns * B * T * H * 4))
-    assert kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv) == want
+    return (_al(B * H * nck * dk * dv * 4) + _al(B * H * 64 * dk * dv * 4) +
+            3 * _al(ns * B * T * H * dk * 4) + _al(ns * B * T * H * 4))
+
+
+def test_backward_workspace_size_formula(L):
+    """Token-level path (fp32, or head dims other than 128): checkpoints every 64 tokens, one
+    chunk of states per (sequence, head), and per 32-column value slice three fp32 per-token
+    [dk] partial sums and one fp32 per-token scalar, each region 256-byte aligned."""
+    B, T, H, dk, dv = 2, 150, 3, 128, 64
+    for dt in (kda.KDA_F32, kda.KDA_BF16):
+        assert kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv, dt) == _token_bwd_ws(B, T, H, dk, dv)
+    assert kda.kda_chunk_bwd_workspace_size(B, T, H, 128, 128, kda.KDA_F32) == \
+        _token_bwd_ws(B, T, H, 128, 128)
     assert kda.kda_chunk_bwd_workspace_size(B, T, H, 48, dv) == 0
+    assert kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv, 2) == 0
+
+
+def test_chunked_backward_workspace_size_formula(L):
+    """Tensor-core path (bf16, dk = dv = 128): per (64-token chunk slot, head) the forward
+    records (four 16 KB tiles, an 8 KB M tile, 1 KB of vectors; the region 256-byte aligned),
+    then N (8 KB), the entering state and the state adjoint (32 KB each, bf16) and U^T and
+    dU^T (16 KB each)."""
+    B, T, H = 2, 150, 3
+    recs = B * ((T + 63) // 64) * H
+    want = _al(recs * (4 * 16384 + 8192 + 1024)) + recs * (8192 + 32768 + 16384 + 32768 + 16384)
+    assert kda.kda_chunk_bwd_workspace_size(B, T, H, 128, 128, kda.KDA_BF16) == want
 
 
 def _bwd(L, ws=0x100000, nbytes=1 << 40, **over):

@@ -37,7 +37,8 @@ def _run(d, cot, B, T, H, dk, dv, scale, lb, bf16, want_state=True):
            "da_log": torch.full((H,), float("nan"), device="cuda"),
            "ddt_bias": torch.full((dk, H), float("nan"), device="cuda"),
            "dinitial_state": torch.full((B, H, dk, dv), float("nan"), device="cuda")}
-    w = workspace(kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv))
+    w = workspace(kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv,
+                                                   kda.KDA_BF16 if bf16 else kda.KDA_F32))
     kda.kda_chunk_bwd(q, k, v, g, bl, al, db, scale, lb, to_dev(d.get("initial_state")), dout,
                       dfin, out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta_logits"],
                       out["da_log"], out["ddt_bias"],
@@ -99,3 +100,53 @@ def test_strong_decay_and_no_final_cotangent():
     d, cot = _case(B, T, H, dk, dv, 7, state=True, final=False)
     gpu = _run(d, cot, B, T, H, dk, dv, 0.09, -5.0, False)
     _check(gpu, _oracle(d, cot, 0.09, -5.0, False), False)
+
+
+# ---- tensor-core chunk path (bf16, dk = dv = 128): chunk-boundary, decay and state cases
+
+
+@pytest.mark.parametrize("B,T,H,lb,state,final", [
+    (1, 64, 1, -2.0, True, True),     # one full chunk
+    (2, 300, 2, -2.0, True, True),    # five chunks, ragged tail of 44 tokens
+    (1, 200, 3, -5.0, False, False),  # strongest decay the ABI admits, no states
+    (2, 129, 2, 0.0, True, True),     # no decay (lower_bound 0), one-token tail
+    (1, 1, 2, -1.0, True, True),      # a single token
+    (1, 1024, 1, -1.0, True, True),   # sixteen chunks: the state adjoint over many steps
+])
+def test_chunked_bf16_gradients(B, T, H, lb, state, final):
+    d, cot = _case(B, T, H, 128, 128, 40 + T + H, state=state, final=final)
+    gpu = _run(d, cot, B, T, H, 128, 128, 128 ** -0.5, lb, True)
+    _check(gpu, _oracle(d, cot, 128 ** -0.5, lb, True), True)
+    assert kda.kda_device_error(1) == 0
+
+
+def test_chunked_bf16_gradients_without_initial_state_output():
+    B, T, H = 2, 100, 2
+    d, cot = _case(B, T, H, 128, 128, 77)
+    gpu = _run(d, cot, B, T, H, 128, 128, 0.1, -2.0, True, want_state=False)
+    _check(gpu, _oracle(d, cot, 0.1, -2.0, True), True, names=GRADS[:-1])
+
+
+def test_chunked_bf16_prefill_workload_sampled_head():
+    """The prefill workload's full size (B 4, T 4096, H 32) through the chunked backward,
+    every per-token gradient of one sampled (sequence, head) compared with the oracle run on
+    that slice alone (sequences and heads are independent; da_log and ddt_bias sum over all
+    of them and are checked at the smaller sizes above)."""
+    w = synth.PREFILL_B4
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    d = synth.workload_inputs(w)
+    r = np.random.default_rng(11)
+    cot = {"d_out": r.standard_normal((B, T, H, dv), dtype=np.float32)}
+    gpu = _run(d, cot, B, T, H, dk, dv, w.q_scale, w.lower_bound, True, want_state=True)
+    b, h = 2, 19
+    sl = {n: d[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v", "g", "beta_logits")}
+    sl["a_log"] = d["a_log"][h:h + 1]
+    sl["dt_bias"] = d["dt_bias"][:, h:h + 1]
+    sl["initial_state"] = None
+    csl = {"d_out": cot["d_out"][b:b + 1, :, h:h + 1]}
+    ref = _oracle(sl, csl, w.q_scale, w.lower_bound, True)
+    for n in ("dq", "dk", "dv", "dg", "dbeta_logits"):
+        got = gpu[n][b:b + 1, :, h:h + 1]
+        assert rel_err(got, ref[n]) <= BF16_REL, (n, rel_err(got, ref[n]))
+    got = gpu["dinitial_state"][b:b + 1, h:h + 1]
+    assert rel_err(got, ref["dinitial_state"]) <= BF16_REL
