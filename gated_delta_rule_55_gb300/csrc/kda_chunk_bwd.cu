@@ -373,24 +373,29 @@ __global__ void __launch_bounds__(kBSThreads, 1)
 // ------------------------------------------------------------ per-chunk products
 
 constexpr int kKThreads = 512;
-// Dynamic shared memory (1024-aligned offsets).
+// Dynamic shared memory (1024-aligned offsets).  Loaded at the start:
 constexpr int K_DUT = 0;        // dU^T [128 j][64 r]; dV^T once lam is read
 constexpr int K_NN = 16384;     // N [64][64]
 constexpr int K_UT = 24576;     // U^T [128 j][64 s]
 constexpr int K_DO = 40960;     // d_out [64 r][128 j] (two boxes, 8192 apart)
 constexpr int K_S0 = 57344;     // S^T [128 j][128 c] (two boxes, 16384 apart)
 constexpr int K_DS = 90112;     // dS'^T [128 j][128 c]
-constexpr int K_D1 = K_S0;      // dD1 [128 rows][192] (three boxes, 16384 apart), after S / dS'
-constexpr int K_XL = 122880;    // Xl [128 rows][128 c] (two boxes, 16384 apart)
-constexpr int K_KB = 155648;    // Kb [160 rows][128 c] (two boxes, 20480 apart)
-constexpr int K_END = 196608;
-constexpr int K_AQ = K_XL;      // fp32 [64 tok][128 c] dq^ (epilogue, after the last MMA)
-constexpr int K_DKH = K_KB;     // fp32 [64 tok][128 c] dk^
-static_assert(K_D1 + 3 * 16384 <= K_XL, "dD1 overlaps Xl");
+constexpr int K_RQ = 122880;    // raw q [64 tok][128] bf16 (two boxes, 8192 apart)
+constexpr int K_RK = 139264;    // raw k
+constexpr int K_RG = 155648;    // raw g fp32 [4 quarters][64 tok][32] (8192 apart)
+constexpr int K_END = 188416;
+// Built later, in tiles whose readers are done:
+constexpr int K_XL = K_DS;      // Xl [128 rows][128 c] (two boxes, 16384 apart): after dKd^T
+constexpr int K_KB = 0;         // Kb [160 rows][128 c] (two boxes, 20480 apart): after dA, dM
+constexpr int K_D1 = K_DO;      // dD1 [128 rows][192] (three boxes, 16384 apart): after dA, dM
+constexpr int K_AQ = 0;         // fp32 [64 tok][128 c] dq^ (epilogue)
+constexpr int K_DKH = 32768;    // fp32 [64 tok][128 c] dk^
+static_assert(K_KB + 2 * 20480 <= K_D1 && K_D1 + 3 * 16384 <= K_XL, "late tiles overlap");
+static_assert(K_XL + 32768 <= K_RQ && K_DKH + 32768 <= K_RQ, "late tiles overlap the raw tiles");
 static_assert(K_DO + 3 * 8192 <= K_END, "rows 64..127 of the d_out A operand read in bounds");
 static_assert(K_DUT + 2 * 16384 <= K_DO, "second M block of the dV^T A operand in bounds");
-static_assert(K_AQ + 32768 <= K_KB && K_DKH + 32768 <= K_END, "epilogue scratch");
 constexpr uint32_t kKLoadTx = 16384 + 8192 + 16384 + 16384 + 32768 + 32768;
+constexpr uint32_t kKRawTx = 16384 + 16384 + 32768;
 constexpr size_t kKSmem = K_END + 1024;
 
 // Tensor Memory (512 columns, one CTA per SM).
@@ -413,12 +418,15 @@ __global__ void __launch_bounds__(kKThreads, 1)
                      const __grid_constant__ CUtensorMap map_ut,
                      const __grid_constant__ CUtensorMap map_do,
                      const __grid_constant__ CUtensorMap map_s0,
-                     const __grid_constant__ CUtensorMap map_ds, const ChunkArgs a,
+                     const __grid_constant__ CUtensorMap map_ds,
+                     const __grid_constant__ CUtensorMap map_q,
+                     const __grid_constant__ CUtensorMap map_k,
+                     const __grid_constant__ CUtensorMap map_g, const ChunkArgs a,
                      const BwdWs bw, const BwdOut o) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint64_t bar_ld, bar_raw, bar_mma;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[4];
   __shared__ __align__(16) float s_gtot[4][kD];
@@ -451,8 +459,18 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
+    mbar_init(&bar_raw, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
+    // this chunk's raw q, k, g first (the gates need them), then the records and states
+    mbar_arrive_expect_tx(&bar_raw, kKRawTx);
+    tma_load_3d(sm + K_RQ, &map_q, &bar_raw, 0, h, (int)tok0);
+    tma_load_3d(sm + K_RQ + 8192, &map_q, &bar_raw, 64, h, (int)tok0);
+    tma_load_3d(sm + K_RK, &map_k, &bar_raw, 0, h, (int)tok0);
+    tma_load_3d(sm + K_RK + 8192, &map_k, &bar_raw, 64, h, (int)tok0);
+#pragma unroll
+    for (int qt = 0; qt < 4; ++qt)
+      tma_load_3d(sm + K_RG + qt * 8192, &map_g, &bar_raw, 32 * qt, h, (int)tok0);
     mbar_arrive_expect_tx(&bar_ld, kKLoadTx);
     tma_load_2d(sm + K_DUT, &map_dut, &bar_ld, 0, (int)(rec * 128));
     tma_load_2d(sm + K_NN, &map_n, &bar_ld, 0, (int)(rec * 64));
@@ -469,6 +487,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
     s_rk[tid] = bw.f.vec[rec * 256 + 128 + tid];
     s_rq[tid] = bw.f.vec[rec * 256 + 192 + tid];
   }
+  const float ea = __expf(a.a_log[h]);
+  const float db = a.dt_bias[c * H + h];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -482,64 +502,35 @@ __global__ void __launch_bounds__(kKThreads, 1)
     __syncthreads();
     return s_wait_ok[slot_w] != 0;
   };
-  bool ld_done = false;
+  bool raw_done = false, ld_done = false;
+  float loc[16], P[4], fg[4], GC, PR;
 
-  const __nv_bfloat16* qin = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(a.k);
+  // element (t, c) of the staged tiles
+  const uint8_t* const rq_t = sm + K_RQ;
+  const uint8_t* const rk_t = sm + K_RK;
+  const float* const rg_t = reinterpret_cast<const float*>(sm + K_RG) + (c >> 5) * 2048 + (c & 31);
+  auto raw_q = [&](int t) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rq_t + sw_off(t, c, 8192)));
+  };
+  auto raw_k = [&](int t) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rk_t + sw_off(t, c, 8192)));
+  };
   auto row_of = [&](int t) -> long long { return (tok0 + t) * H + h; };
 
   // ---- gates: G_t - P_R for this thread's channel and sub-chunk
-  const float ea = __expf(a.a_log[h]);
-  const float db = a.dt_bias[c * H + h];
-  float loc[16];
+  if (!block_wait(&bar_raw, 0)) goto fail;
+  raw_done = true;
   {
     float run = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int t = 16 * R + i;
       float gm = 0.f;
-      if (t < n) gm = a.lower_bound * fast_rcp(1.f + fast_exp(-ea * (a.g[row_of(t) * kD + c] + db)));
+      if (t < n) gm = a.lower_bound * fast_rcp(1.f + fast_exp(-ea * (rg_t[t * 32] + db)));
       run += gm;
       loc[i] = run;
     }
     s_gtot[R][c] = run;
-  }
-  __syncthreads();
-  float P[4];
-  P[0] = 0.f;
-#pragma unroll
-  for (int r = 1; r < 4; ++r) P[r] = P[r - 1] + s_gtot[r - 1][c];
-  const float GC = P[3] + s_gtot[3][c];
-  float PR = P[0];
-#pragma unroll
-  for (int r = 1; r < 4; ++r) PR = (R == r) ? P[r] : PR;
-
-  // ---- operand tiles: Xl rows t (k^ e^{G_t - P_R}) and 64 + t (q^ e^{G_t - P_R}); Kb rows
-  //      t (k^ e^{P_R - G_t}) and base_g + t (k^ e^{P_g - G_t}) for the later sub-chunks g
-  {
-    float fg[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) fg[g] = (g > R) ? fast_exp(P[g] - PR) : 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = 16 * R + i;
-      float kh = 0.f, qh = 0.f;
-      if (t < n) {
-        kh = __bfloat162float(kin[row_of(t) * kD + c]) * s_rk[t];
-        qh = __bfloat162float(qin[row_of(t) * kD + c]) * s_rq[t];
-      }
-      const float e = fast_exp(loc[i]), ei = fast_exp(-loc[i]);
-      *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(t, c, 16384)) = __float2bfloat16_rn(kh * e);
-      *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(64 + t, c, 16384)) =
-          __float2bfloat16_rn(qh * e);
-      const float kd = kh * ei;
-      *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(t, c, 20480)) = __float2bfloat16_rn(kd);
-#pragma unroll
-      for (int g = 1; g < 4; ++g)
-        if (g > R)
-          *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(kb_base(g) + t, c, 20480)) =
-              __float2bfloat16_rn(kd * fg[g]);
-    }
   }
 
   // ---- loaded tiles: clear d_out rows past the chunk, S . dS' per channel (quarter of j)
@@ -579,6 +570,16 @@ __global__ void __launch_bounds__(kKThreads, 1)
     }
     mma_commit(&bar_mma);
   }
+  // meanwhile: the sub-chunk reference points
+  P[0] = 0.f;
+#pragma unroll
+  for (int r = 1; r < 4; ++r) P[r] = P[r - 1] + s_gtot[r - 1][c];
+  GC = P[3] + s_gtot[3][c];
+  PR = P[0];
+#pragma unroll
+  for (int r = 1; r < 4; ++r) PR = (R == r) ? P[r] : PR;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) fg[g] = (g > R) ? fast_exp(P[g] - PR) : 0.f;
   if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
   tc_fence_after();
 
@@ -635,10 +636,25 @@ __global__ void __launch_bounds__(kKThreads, 1)
     }
     mma_commit(&bar_mma);
   }
+  // meanwhile: Xl rows t (k^ e^{G_t - P_R}) and 64 + t (q^ e^{G_t - P_R}) into the dS' tile,
+  // whose readers (dKd^T and the S . dS' sums) are done
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int t = 16 * R + i;
+    const bool live = t < n;
+    const float kh = live ? raw_k(t) * s_rk[t] : 0.f;
+    const float qh = live ? raw_q(t) * s_rq[t] : 0.f;
+    const float e = fast_exp(loc[i]);
+    *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(t, c, 16384)) = __float2bfloat16_rn(kh * e);
+    *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(64 + t, c, 16384)) =
+        __float2bfloat16_rn(qh * e);
+  }
   if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
   tc_fence_after();
 
-  // ---- dD1 = [dA; dM] in the column layout of the forward's Kb rows; dbeta_logits
+  // ---- dD1 = [dA; dM] in the column layout of the Kb rows (over d_out and S); Kb rows t
+  //      (k^ e^{P_R - G_t}) and base_g + t (k^ e^{P_g - G_t}) over dU^T, N and U^T;
+  //      dbeta_logits
   if (sp < 2) {
     float da[16], dm[16];
     tmem_ld16(tl + KT_DA + 16 * R, da);
@@ -673,6 +689,17 @@ __global__ void __launch_bounds__(kKThreads, 1)
       o.dbeta_logits[row_of(t)] =
           (1.f - s_beta[t]) * (s_lu[0][t] + s_lu[1][t] + s_lu[2][t] + s_lu[3][t]);
   }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int t = 16 * R + i;
+    const float kd = (t < n) ? raw_k(t) * s_rk[t] * fast_exp(-loc[i]) : 0.f;
+    *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(t, c, 20480)) = __float2bfloat16_rn(kd);
+#pragma unroll
+    for (int g = 1; g < 4; ++g)
+      if (g > R)
+        *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(kb_base(g) + t, c, 20480)) =
+            __float2bfloat16_rn(kd * fg[g]);
+  }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -699,9 +726,6 @@ __global__ void __launch_bounds__(kKThreads, 1)
     float* AQ = reinterpret_cast<float*>(sm + K_AQ);
     float* DKH = reinterpret_cast<float*>(sm + K_DKH);
     const float eP = fast_exp(PR), eCP = fast_exp(GC - PR);
-    float fg[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) fg[g] = (g > R) ? fast_exp(P[g] - PR) : 0.f;
     float dG[16];
     float dgc = 0.f;
 #pragma unroll
@@ -713,8 +737,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
         const int t = cb + i;
         e[i] = fast_exp(loc[8 * hh + i]);
         ei[i] = fast_exp(-loc[8 * hh + i]);
-        kh[i] = (t < n) ? __bfloat162float(kin[row_of(t) * kD + c]) * s_rk[t] : 0.f;
-        qh[i] = (t < n) ? __bfloat162float(qin[row_of(t) * kD + c]) * s_rq[t] : 0.f;
+        kh[i] = (t < n) ? raw_k(t) * s_rk[t] : 0.f;
+        qh[i] = (t < n) ? raw_q(t) * s_rq[t] : 0.f;
       }
       // dq^, dk^ (exact gate factors) and dG; each Xl / Kb term of dG is weighted by the bf16
       // operand value the product used, so that the +G and -G terms of a pair (r, s) of the
@@ -802,6 +826,14 @@ __global__ void __launch_bounds__(kKThreads, 1)
 #pragma unroll
     for (int r = 1; r < 4; ++r)
       if (r > R) carry += s_dgs[r][c];
+    // per-token sums of q^ . dq^ and k^ . dk^ over the four warps of each sub-chunk
+    if (tid < kC) {
+      s_qd[0][tid] += s_qd[1][tid] + s_qd[2][tid] + s_qd[3][tid];
+    } else if (tid < 2 * kC) {
+      const int t = tid - kC;
+      s_kd[0][t] += s_kd[1][t] + s_kd[2][t] + s_kd[3][t];
+    }
+    __syncthreads();
     float ddb = 0.f, dal = 0.f;
     const float inv_s2 = 1.f / (a.scale * a.scale);
 #pragma unroll
@@ -811,18 +843,17 @@ __global__ void __launch_bounds__(kKThreads, 1)
       if (t < n) {
         const long long row = row_of(t);
         // gate: gamma = lb sigmoid(x), x = e^{a_log} (g + dt_bias)
-        const float x = ea * (a.g[row * kD + c] + db);
-        const float sg = sigmoidf_(x);
+        const float x = ea * (rg_t[t * 32] + db);
+        const float sg = fast_rcp(1.f + fast_exp(-x));
         const float dx = carry * a.lower_bound * sg * (1.f - sg);
         o.dg[row * kD + c] = dx * ea;
         ddb += dx * ea;
         dal += dx * x;
         // L2 norms: q^ = rq q with rq = scale / |q|, k^ = rk k
-        const float qdt = s_qd[0][t] + s_qd[1][t] + s_qd[2][t] + s_qd[3][t];
-        const float kdt = s_kd[0][t] + s_kd[1][t] + s_kd[2][t] + s_kd[3][t];
+        const float qdt = s_qd[0][t], kdt = s_kd[0][t];
         const float rq = s_rq[t], rk = s_rk[t];
-        const float qh = __bfloat162float(qin[row * kD + c]) * rq;
-        const float kh = __bfloat162float(kin[row * kD + c]) * rk;
+        const float qh = raw_q(t) * rq;
+        const float kh = raw_k(t) * rk;
         o.dq[row * kD + c] = __float2bfloat16_rn(rq * AQ[t * kD + c] - qh * qdt * rq * inv_s2);
         o.dk[row * kD + c] = __float2bfloat16_rn(rk * DKH[t * kD + c] - kh * kdt * rk);
       }
@@ -844,6 +875,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
 fail:
   if (tid == 0) {
     atomicOr(&g_bwd_error, 4u);
+    if (!raw_done) mbar_wait(&bar_raw, 0, 1000000000ull);
     if (!ld_done) mbar_wait(&bar_ld, 0, 1000000000ull);
     if (mma_phase > 0) mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
   }
@@ -907,7 +939,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
   if ((e = split::launch_prep_scan(f, bw.f, st)) != cudaSuccess) return e;
 
   const long long rows = (long long)a.B * a.T;
-  CUtensorMap mqw, mku, mm, mdo, mdut, mn, mut, ms0, mds;
+  CUtensorMap mqw, mku, mm, mdo, mdut, mn, mut, ms0, mds, mq, mk, mg;
   if (!make_map_2d(&mqw, bw.f.qw, 2 * recs * 64, 128, 64) ||
       !make_map_2d(&mku, bw.f.ku, 2 * recs * 128, 64, 128) ||
       !make_map_2d(&mm, bw.f.m, recs * 64, 64, 64) || !make_map_in(&mdo, d_out, rows, a.H, false) ||
@@ -915,7 +947,9 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
       !make_map_2d(&mn, bw.f.nrec, recs * 64, 64, 64) ||
       !make_map_2d(&mut, bw.f.ut, recs * 128, 64, 128) ||
       !make_map_2d(&ms0, bw.f.s0, recs * 128, 128, 128) ||
-      !make_map_2d(&mds, bw.ds, recs * 128, 128, 128))
+      !make_map_2d(&mds, bw.ds, recs * 128, 128, 128) ||
+      !make_map_in(&mq, a.q, rows, a.H, false) || !make_map_in(&mk, a.k, rows, a.H, false) ||
+      !make_map_in(&mg, a.g, rows, a.H, true))
     return cudaErrorInvalidValue;
   if ((e = cudaFuncSetAttribute(bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kBSSmem)) != cudaSuccess)
@@ -925,8 +959,8 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
     return e;
   bwd_scan_kernel<<<dim3(a.H, a.B), kBSThreads, kBSSmem, st>>>(mqw, mku, mm, mdo, a, bw, o);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_chunk_kernel<<<(unsigned)recs, kKThreads, kKSmem, st>>>(mdut, mn, mut, mdo, ms0, mds, a, bw,
-                                                               o);
+  bwd_chunk_kernel<<<(unsigned)recs, kKThreads, kKSmem, st>>>(mdut, mn, mut, mdo, ms0, mds, mq,
+                                                               mk, mg, a, bw, o);
   return cudaGetLastError();
 }
 
