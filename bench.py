@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA chunked-fwd tokens/s; decode-step HBM GB/s vs peak (1 GB300)"
 L2_BYTES = 126 * 2 ** 20
 # the kernels the roofline covers (the two launches of one kda_chunk_fwd_ws call)
-CHUNK_KERNEL_SOURCES = ["kda_chunk_split.cu", "chunk_common.cuh", "tc_prims.cuh"]
+CHUNK_KERNEL_SOURCES = ["kda_chunk_split.cu", "chunk_records.cuh", "chunk_common.cuh", "tc_prims.cuh"]
 
 
 # ----------------------------------------------------------------------------- helpers
