@@ -408,7 +408,9 @@ def e2e_measure(w, d, x, K, W):
 def backward_measure(w, d, x, reps=3):
     """kda_chunk_bwd on the prefill workload (inputs resident; d_out ~ N(0, 1), no final-state
     cotangent): median time per call, and its algorithmic bytes (every input, cotangent and
-    gradient moved once) over that time."""
+    gradient moved once) over that time.  Also the training pair: kda_chunk_fwd_train (the
+    forward keeping the backward's records) and kda_chunk_bwd_saved (the backward reading
+    them), each timed alone."""
     torch = _torch()
     import gated_delta_rule_55_gb300 as kda
     io = torch.bfloat16
@@ -422,33 +424,51 @@ def backward_measure(w, d, x, reps=3):
          "db": torch.empty(B, T, H, device="cuda"),
          "da": torch.empty(H, device="cuda"), "ddt": torch.empty(dk, H, device="cuda")}
     ws = torch.empty(kda.kda_chunk_bwd_workspace_size(B, T, H, dk, dv, kda.KDA_BF16),
-                     dtype=torch.uint8,
-                     device="cuda")
+                     dtype=torch.uint8, device="cuda")
+    grads = (g["dq"], g["dk"], g["dv"], g["dg"], g["db"], g["da"], g["ddt"], None)
+    ins = (x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"], x["dt_bias"],
+           w.q_scale, w.lower_bound, x["initial_state"])
 
     def call():
-        kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta_logits"], x["a_log"],
-                          x["dt_bias"], w.q_scale, w.lower_bound, x["initial_state"], dout, None,
-                          g["dq"], g["dk"], g["dv"], g["dg"], g["db"], g["da"], g["ddt"], None,
-                          B, T, H, dk, dv, workspace=ws)
+        kda.kda_chunk_bwd(*ins, dout, None, *grads, B, T, H, dk, dv, workspace=ws)
 
-    call()
-    torch.cuda.synchronize()
-    times = []
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(reps):
-        e0.record()
-        call()
-        e1.record()
+    def fwd_train():
+        kda.kda_chunk_fwd_train(*ins, x["out"], x["final_state"], B, T, H, dk, dv,
+                                workspace=ws)
+
+    def bwd_saved():
+        kda.kda_chunk_bwd_saved(*ins, dout, None, *grads, B, T, H, dk, dv, workspace=ws)
+
+    def timed(fn, pre=None):
+        if pre:
+            pre()
+        fn()
         torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times)
+        times = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(reps):
+            if pre:
+                pre()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    ms = timed(call)
+    ms_train_fwd = timed(fwd_train)
+    ms_saved = timed(bwd_saved, pre=fwd_train)
     per = (2 * dk + dv) * 2 + dk * 4 + 4 + dv * 2 + 2 * dk * 2 + dv * 2 + dk * 4 + 4
     nbytes = B * T * H * per
     return {"entry": "kda_chunk_bwd", "workload": w.name, "ms_per_call": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": nbytes,
             "hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "launches": 4,
-            "workspace_bytes": int(ws.numel())}
-
+            "workspace_bytes": int(ws.numel()),
+            "training_pair": {"kda_chunk_fwd_train_ms": ms_train_fwd,
+                              "kda_chunk_bwd_saved_ms": ms_saved,
+                              "step_ms": ms_train_fwd + ms_saved,
+                              "tokens_per_s": B * T / ((ms_train_fwd + ms_saved) * 1e-3)}}
 
 def recurrent_attention_measure(reps=3):
     """kda_recurrent_attention_fwd on B=4, T=4096, Hq=32, Hkv=8, D=128, bf16 q/k/v with

@@ -28,8 +28,9 @@ struct Ws {
   long long recs;      // chunk slots x heads
   int nck_fixed;       // chunks per sequence (fixed-length inputs)
   // Records kept for the backward (bwd != 0).  The prep then folds rq into Q~ and into the
-  // rows of M (Q~ = q^ e^{G}, M[r][s] = rq_r M_raw[r][s]) and writes N; the scan computes
-  // no output and writes, per chunk, the state entering it and the chunk's U.
+  // rows of M (Q~ = q^ e^{G}, M[r][s] = rq_r M_raw[r][s]) and writes N; the scan writes,
+  // per chunk, the state entering it and the chunk's U, and computes the output only in
+  // the training forward (bwd == 2), not in the backward's own forward pass (bwd == 1).
   __nv_bfloat16* nrec;  // [recs * 64][64]: N = (I + diag(beta) tril(A, -1))^{-1}, s <= r
   __nv_bfloat16* s0;    // [recs * 128][128]: S^T entering the chunk (row = value column j)
   __nv_bfloat16* ut;    // [recs * 128][64]: U^T of the chunk (row j, column = token)

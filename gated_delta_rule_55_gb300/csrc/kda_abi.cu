@@ -231,6 +231,11 @@ int kda_attention_fwd(const void* query, const void* key, const void* value, con
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
+
+}  // extern "C"
+
+namespace {
+
 // Backward arguments for sizing only (no pointers are read).
 kda::ChunkArgs bwd_shape(int B, int T, int H, int dk, int dv) {
   kda::ChunkArgs a{};
@@ -238,22 +243,13 @@ kda::ChunkArgs bwd_shape(int B, int T, int H, int dk, int dv) {
   return a;
 }
 
-size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int dtype) {
-  if (B < 0 || T < 0 || H <= 0 || !head_dim_ok(dk) || !head_dim_ok(dv) ||
-      (long long)B * T > 0x7fffffffLL || (dtype != KDA_F32 && dtype != KDA_BF16))
-    return 0;
-  const kda::ChunkArgs a = bwd_shape(B, T, H, dk, dv);
-  if (B > 0 && kda::chunk_bwd_supported(a, dtype == KDA_BF16)) return kda::chunk_bwd_workspace(a);
-  return kda::backward_workspace(B, T, H, dk, dv);
-}
-
-int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
-                  const float* beta_logits, const float* a_log, const float* dt_bias,
-                  float scale, float lower_bound, const float* initial_state, const void* d_out,
-                  const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
-                  float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
-                  int B, int T, int H, int dim_k, int dim_v, int dtype, void* workspace,
-                  size_t workspace_bytes, kda_stream_t stream) {
+int bwd_common(const void* q, const void* k, const void* v, const float* g,
+               const float* beta_logits, const float* a_log, const float* dt_bias, float scale,
+               float lower_bound, const float* initial_state, const void* d_out,
+               const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+               float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
+               int B, int T, int H, int dim_k, int dim_v, int dtype, void* workspace,
+               size_t workspace_bytes, kda_stream_t stream, bool saved) {
   kda::ChunkArgs a;
   int s = fill_fixed(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
                      initial_state, dq, nullptr, B, T, H, dim_k, dim_v, 64);
@@ -272,6 +268,10 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
       H > 65535)
     return KDA_ERR_TOO_LARGE;
   const bool chunked = B > 0 && kda::chunk_bwd_supported(a, dtype == KDA_BF16);
+  // the saved-records entry serves exactly the tensor-core configurations (no tokens: the
+  // plain path, which has nothing to read back)
+  if (saved && !chunked && (long long)B * T > 0)
+    return dtype != KDA_BF16 ? KDA_ERR_DTYPE : KDA_ERR_HEAD_DIM;
   const size_t need =
       chunked ? kda::chunk_bwd_workspace(a) : kda::backward_workspace(B, T, H, dim_k, dim_v);
   if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
@@ -286,11 +286,83 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
     if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * dim_k * H, st);
   } else if (chunked) {
     e = kda::launch_chunk_bwd(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
-                              ddt_bias, d_initial_state, workspace, st);
+                              ddt_bias, d_initial_state, workspace, saved, st);
   } else {
     e = kda::launch_backward(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
                              ddt_bias, d_initial_state, workspace, dtype == KDA_BF16, st);
   }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int dtype) {
+  if (B < 0 || T < 0 || H <= 0 || !head_dim_ok(dk) || !head_dim_ok(dv) ||
+      (long long)B * T > 0x7fffffffLL || (dtype != KDA_F32 && dtype != KDA_BF16))
+    return 0;
+  const kda::ChunkArgs a = bwd_shape(B, T, H, dk, dv);
+  if (B > 0 && kda::chunk_bwd_supported(a, dtype == KDA_BF16)) return kda::chunk_bwd_workspace(a);
+  return kda::backward_workspace(B, T, H, dk, dv);
+}
+
+int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta_logits, const float* a_log, const float* dt_bias,
+                  float scale, float lower_bound, const float* initial_state, const void* d_out,
+                  const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                  float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
+                  int B, int T, int H, int dim_k, int dim_v, int dtype, void* workspace,
+                  size_t workspace_bytes, kda_stream_t stream) {
+  return bwd_common(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, initial_state,
+                    d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log, ddt_bias,
+                    d_initial_state, B, T, H, dim_k, dim_v, dtype, workspace, workspace_bytes,
+                    stream, false);
+}
+
+int kda_chunk_bwd_saved(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta_logits, const float* a_log, const float* dt_bias,
+                        float scale, float lower_bound, const float* initial_state,
+                        const void* d_out, const float* d_final_state, void* dq, void* dk,
+                        void* dv, float* dg, float* dbeta_logits, float* da_log, float* ddt_bias,
+                        float* d_initial_state, int B, int T, int H, int dim_k, int dim_v,
+                        int dtype, void* workspace, size_t workspace_bytes,
+                        kda_stream_t stream) {
+  return bwd_common(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, initial_state,
+                    d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log, ddt_bias,
+                    d_initial_state, B, T, H, dim_k, dim_v, dtype, workspace, workspace_bytes,
+                    stream, true);
+}
+
+int kda_chunk_fwd_train(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta_logits, const float* a_log, const float* dt_bias,
+                        float scale, float lower_bound, const float* initial_state, void* out,
+                        float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                        int dtype, void* workspace, size_t workspace_bytes,
+                        kda_stream_t stream) {
+  kda::ChunkArgs a;
+  const int s = fill_fixed(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                           initial_state, out, final_state, B, T, H, dk, dv, chunk);
+  if (s != KDA_OK) return s;
+  if ((long long)B * T == 0)  // no tokens: the plain forward (state copy), nothing to keep
+    return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+  if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_DTYPE;
+  if (chunk != 16 && chunk != 64) return KDA_ERR_CHUNK;
+  if (!kda::chunk_bwd_supported(a, dtype == KDA_BF16))
+    return dtype != KDA_BF16 ? KDA_ERR_DTYPE : chunk != 64 ? KDA_ERR_CHUNK : KDA_ERR_HEAD_DIM;
+  const void* ptrs[] = {q, k, v, g, beta_logits, a_log, dt_bias, initial_state, out,
+                        final_state};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  if ((double)a.total_T * H * 128 >= 1099511627776.0 || B > 65535 || H > 65535)
+    return KDA_ERR_TOO_LARGE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < kda::chunk_bwd_workspace(a))
+    return KDA_ERR_WORKSPACE;
+  const int d = check_device();
+  if (d != KDA_OK) return d;
+  const cudaError_t e =
+      kda::launch_chunk_fwd_train(a, workspace, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 

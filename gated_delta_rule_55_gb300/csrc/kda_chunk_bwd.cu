@@ -900,11 +900,11 @@ bool chunk_bwd_supported(const ChunkArgs& a, bool bf16) {
          slots_for(a) * a.H * 256 < 0x7fffffffLL;
 }
 
-cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float* d_final,
-                             void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
-                             float* da_log, float* ddt_bias, float* d_initial, void* workspace,
-                             cudaStream_t st) {
-  BwdWs bw{};
+namespace {
+
+// The backward workspace: the forward records, N, the per-chunk entering state and U, then
+// the reverse scan's dS' and dU per chunk.
+void carve_bwd(const ChunkArgs& a, void* workspace, BwdWs& bw) {
   uint8_t* p = static_cast<uint8_t*>(workspace);
   carve_records(a, p, bw.f);
   const long long recs = bw.f.recs;
@@ -918,7 +918,24 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
   bw.ds = reinterpret_cast<__nv_bfloat16*>(p);
   p += recs * kRecState;
   bw.dut = reinterpret_cast<__nv_bfloat16*>(p);
-  bw.f.bwd = 1;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_fwd_train(const ChunkArgs& a, void* workspace, cudaStream_t st) {
+  BwdWs bw{};
+  carve_bwd(a, workspace, bw);
+  bw.f.bwd = 2;
+  return split::launch_prep_scan(a, bw.f, st);
+}
+
+cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float* d_final,
+                             void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
+                             float* da_log, float* ddt_bias, float* d_initial, void* workspace,
+                             bool saved, cudaStream_t st) {
+  BwdWs bw{};
+  carve_bwd(a, workspace, bw);
+  const long long recs = bw.f.recs;
   BwdOut o{};
   o.d_final = d_final;
   o.dq = static_cast<__nv_bfloat16*>(dq);
@@ -933,10 +950,13 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
   cudaError_t e = cudaMemsetAsync(da_log, 0, sizeof(float) * a.H, st);
   if (e != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * kD * a.H, st)) != cudaSuccess) return e;
-  ChunkArgs f = a;
-  f.out = nullptr;
-  f.final_state = nullptr;
-  if ((e = split::launch_prep_scan(f, bw.f, st)) != cudaSuccess) return e;
+  if (!saved) {  // the forward's records and states, without its output
+    ChunkArgs f = a;
+    f.out = nullptr;
+    f.final_state = nullptr;
+    bw.f.bwd = 1;
+    if ((e = split::launch_prep_scan(f, bw.f, st)) != cudaSuccess) return e;
+  }
 
   const long long rows = (long long)a.B * a.T;
   CUtensorMap mqw, mku, mm, mdo, mdut, mn, mut, ms0, mds, mq, mk, mg;

@@ -650,6 +650,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
   __shared__ __align__(16) float s_vec[256];  // this chunk's e^{G_C}, rk, rq
+  __shared__ __align__(16) float s_one[64];   // unit output scale (rq folded into the records)
+  const bool want_out = ws.bwd != 1;
+  if (threadIdx.x < 64) s_one[threadIdx.x] = 1.f;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -697,9 +700,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const long long rec = (slot0 + ch) * H + h;
     uint8_t* b = sm + st * kStage;
     uint64_t* bar = &bar_ld[st];
-    mbar_arrive_expect_tx(bar, ws.bwd ? kStageTxBwd : kStageTx);
+    mbar_arrive_expect_tx(bar, want_out ? kStageTx : kStageTxBwd);
     const int rq = (int)(rec * 64), rw = (int)((ws.recs + rec) * 64);
-    if (!ws.bwd) {  // the backward's forward pass computes no output
+    if (want_out) {  // the backward's own forward pass computes no output
       tma_load_2d(b + S_Q, &map_qw, bar, 0, rq);
       tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, rq);
       tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64));
@@ -779,7 +782,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         mma_ts(tm + S_TM_DU, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(ws_, 64, s), idesc_n64, s > 0);
-        if (!ws.bwd)
+        if (want_out)
           mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
       }
       mma_commit(&bar_mma);
@@ -829,7 +832,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const uint32_t ms = smem_u32(b + S_M), ks = smem_u32(b + S_KT);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        if (!ws.bwd)
+        if (want_out)
           mma_ts(tm + S_TM_DO, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ms, 64, s), idesc_n64, 1);
         mma_ts(tm + S_TM_S, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ks, 128, s), idesc_n128, 1);
       }
@@ -840,7 +843,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // the stage is consumed (its last readers were MMA4 and the U' pack): refill it
     if (tid == 0 && ch + 2 < nck) issue_load(ch + 2, st);
     inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
-    // ---- bf16 copy of the new state and the output O = diag(rq) O'
+    // ---- bf16 copy of the new state and the output O = diag(rq) O' (O' itself when the
+    //      records carry rq)
     {
       float S[32];
       tmem_ld32(tl + S_TM_S + 32 * wg, S);
@@ -848,15 +852,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) sp[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
       tmem_st16(tl + S_TM_SA + 16 * wg, sp);
-      if (ws.bwd) {
-        if (ch + 1 < nck) {  // the state entering the next chunk
-          uint4* d = reinterpret_cast<uint4*>(
-              ws.s0 + (((slot0 + ch + 1) * H + h) * 128 + ln) * 128 + 32 * wg);
+      if (ws.bwd && ch + 1 < nck) {  // the state entering the next chunk
+        uint4* d = reinterpret_cast<uint4*>(
+            ws.s0 + (((slot0 + ch + 1) * H + h) * 128 + ln) * 128 + 32 * wg);
 #pragma unroll
-          for (int p = 0; p < 4; ++p)
-            d[p] = make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
-        }
-      } else {
+        for (int p = 0; p < 4; ++p)
+          d[p] = make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
+      }
+      if (want_out) {
+        // backward records carry rq inside Q~ and M: O' is the output itself
+        const float* const rqv = ws.bwd ? s_one : vec + 192;
         float o16[16];
         tmem_ld16(tl + S_TM_DO + 16 * wg, o16);
         if (n == kC) {
@@ -867,7 +872,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             const uint32_t off = ob + uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
                                  (((och ^ uint32_t(i & 7)) << 4) | oby);
             *reinterpret_cast<__nv_bfloat16*>(sm + S_OS + off) =
-                __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+                __float2bfloat16_rn(o16[i] * rqv[16 * wg + i]);
           }
         } else {
           __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
@@ -875,14 +880,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
           const long long stride = (long long)H * kD;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            if (16 * wg + i < n) op[i * stride] = __float2bfloat16_rn(o16[i] * vec[192 + 16 * wg + i]);
+            if (16 * wg + i < n) op[i * stride] = __float2bfloat16_rn(o16[i] * rqv[16 * wg + i]);
         }
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && !ws.bwd) {
+    if (tid == 0 && want_out) {
       if (n == kC) {
         tma_store_3d(&map_o, sm + S_OS, 0, h, (int)tok0);
         tma_store_3d(&map_o, sm + S_OS + 8192, 64, h, (int)tok0);
@@ -990,7 +995,7 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
   if (!make_map_2d(&mqw, ws.qw, 2 * rec_rows * 64, 128, 64) ||
       !make_map_2d(&mku, ws.ku, 2 * rec_rows * 128, 64, 128) ||
       !make_map_2d(&mm, ws.m, rec_rows * 64, 64, 64) ||
-      !make_map_out(&mo, ws.bwd ? a.q : a.out, map_rows, a.H) ||
+      !make_map_out(&mo, ws.bwd == 1 ? a.q : a.out, map_rows, a.H) ||
       !make_map_in(&mq, a.q, map_rows, a.H, false) ||
       !make_map_in(&mk, a.k, map_rows, a.H, false) ||
       !make_map_in(&mv, a.v, map_rows, a.H, false) || !make_map_in(&mg, a.g, map_rows, a.H, true))

@@ -91,10 +91,14 @@ cudaError_t launch_backward(const ChunkArgs& f, const void* d_out, const float* 
 // variant): forward records and states, reverse chunk scan, per-chunk products.
 bool chunk_bwd_supported(const ChunkArgs& a, bool bf16);
 size_t chunk_bwd_workspace(const ChunkArgs& a);
+// The training forward: the output and final state, plus the records and per-chunk states
+// the backward reads, left in its workspace (same configurations and size).
+cudaError_t launch_chunk_fwd_train(const ChunkArgs& a, void* workspace, cudaStream_t stream);
+// saved: the workspace already holds what launch_chunk_fwd_train left for these inputs.
 cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float* d_final,
                              void* dq, void* dk, void* dv, float* dg, float* dbeta_logits,
                              float* da_log, float* ddt_bias, float* d_initial, void* workspace,
-                             cudaStream_t stream);
+                             bool saved, cudaStream_t stream);
 unsigned int chunk_bwd_read_error(bool reset);
 cudaError_t launch_gla(const GlaArgs& a, bool bf16, cudaStream_t stream);
 // Sequential (token by token) scan: any supported shape, dtype and variant.

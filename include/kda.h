@@ -206,6 +206,42 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   int B, int T, int H, int dim_k, int dim_v, int dtype, void* workspace,
                   size_t workspace_bytes, kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_train -- the forward of kda_chunk_fwd_ws (same inputs, outputs, layouts and
+ *   error codes) for training: besides out and final_state it leaves in `workspace` the
+ *   chunk records and per-chunk states that kda_chunk_bwd_saved reads, so that the backward
+ *   does not recompute them.  No paper counterpart: the pages present the chunked mode as
+ *   the training path and give no backward.  Serves bf16 q/k/v with dk = dv = 128 and
+ *   chunk = 64 (fixed-length sequences); other dtypes, head dims or chunk sizes give
+ *   KDA_ERR_DTYPE / KDA_ERR_HEAD_DIM / KDA_ERR_CHUNK (no tokens at all: the plain forward).
+ *   workspace / workspace_bytes: at least kda_chunk_bwd_workspace_size(B, T, H, 128, 128,
+ *   KDA_BF16) bytes, 256-byte aligned, caller-owned; what it holds stays valid for
+ *   kda_chunk_bwd_saved until the caller reuses the buffer.  The output can differ from
+ *   kda_chunk_fwd_ws's in the last bf16 bit (the query scale rides in the operands instead
+ *   of the output).
+ */
+int kda_chunk_fwd_train(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta_logits, const float* a_log, const float* dt_bias,
+                        float scale, float lower_bound, const float* initial_state, void* out,
+                        float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                        int dtype, void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_chunk_bwd_saved -- kda_chunk_bwd (same arguments, outputs and error codes) that reads
+ *   the records and per-chunk states kda_chunk_fwd_train left in `workspace` for the same
+ *   inputs instead of recomputing them (the workspace is also its scratch).  Only the
+ *   configurations of kda_chunk_fwd_train (others give KDA_ERR_DTYPE / KDA_ERR_HEAD_DIM).
+ *   On a workspace that kda_chunk_fwd_train did not fill for these inputs the gradients are
+ *   wrong, though every access stays inside the workspace.
+ */
+int kda_chunk_bwd_saved(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta_logits, const float* a_log, const float* dt_bias,
+                        float scale, float lower_bound, const float* initial_state,
+                        const void* d_out, const float* d_final_state, void* dq, void* dk,
+                        void* dv, float* dg, float* dbeta_logits, float* da_log, float* ddt_bias,
+                        float* d_initial_state, int B, int T, int H, int dim_k, int dim_v,
+                        int dtype, void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
 /* Options of kda_attention_fwd (bitwise OR). */
 enum kda_attention_flags {
   KDA_ATTN_NO_QK_L2NORM = 1,  /* use_qk_l2norm=False: q and k are used as given */

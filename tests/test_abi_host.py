@@ -287,3 +287,49 @@ def test_recurrent_attention_without_device(L):
         pytest.skip("a GPU is present; this case is only meaningful without one")
     assert _gla(L) == -9
     assert _gla(L, cu=FAKE, B=1, N=3, rev=1) == -9
+
+
+def _train(L, ws=0x100000, nbytes=1 << 40, **over):
+    a = dict(B=1, T=64, H=2, dk=128, dv=128, chunk=64, dtype=1, out=FAKE)
+    a.update(over)
+    return L.kda_chunk_fwd_train(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, -1.0, None,
+                                 a["out"], None, a["B"], a["T"], a["H"], a["dk"], a["dv"],
+                                 a["chunk"], a["dtype"], ws, nbytes, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(out=None), -1), (dict(H=0), -2), (dict(dk=100), -3), (dict(dtype=0), -7),
+    (dict(dtype=3), -7), (dict(dk=64), -3), (dict(dv=64), -3), (dict(chunk=16), -4),
+    (dict(chunk=32), -4), (dict(ws=None), -12), (dict(nbytes=16), -12),
+    (dict(ws=0x100000 + 64), -12),
+])
+def test_train_forward_rejects_bad_arguments(L, over, code):
+    """The training forward serves the tensor-core configuration only; argument errors come
+    before the device check."""
+    assert _train(L, **over) == code
+
+
+def test_train_forward_workspace_is_the_backward_workspace(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is only meaningful without one")
+    need = kda.kda_chunk_bwd_workspace_size(1, 64, 2, 128, 128, kda.KDA_BF16)
+    assert _train(L, nbytes=need - 1) == -12
+    assert _train(L, nbytes=need) == -9                      # reaches the device check
+
+
+def _bwd_saved(L, **over):
+    a = dict(B=1, T=64, H=2, dk=128, dv=128, dtype=1)
+    a.update(over)
+    return L.kda_chunk_bwd_saved(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, -1.0, None,
+                                 FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                 a["B"], a["T"], a["H"], a["dk"], a["dv"], a["dtype"], 0x100000,
+                                 1 << 40, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dtype=0), -7), (dict(dk=64), -3), (dict(dv=32), -3), (dict(dk=48), -3),
+    (dict(B=-1), -2),
+])
+def test_saved_backward_rejects_other_configurations(L, over, code):
+    assert _bwd_saved(L, **over) == code
