@@ -134,7 +134,9 @@ constexpr int B_V = 73728;      // e^{G_C}, rk, rq
 constexpr int kBStage = 74752;
 constexpr uint32_t kBStageTx = 74752;
 static_assert(kBStage % 1024 == 0, "alignment");
-constexpr size_t kBSSmem = 2 * kBStage + 1024;
+constexpr int B_SDS = 2 * kBStage;   // staged dS'^T image [128 x 128] (two boxes)
+constexpr int B_SDU = B_SDS + 32768;  // staged dU^T image [128 x 64]
+constexpr size_t kBSSmem = B_SDU + 16384 + 1024;
 
 constexpr uint32_t BT_DU = 0;    // dU^T accumulator, 64 columns
 constexpr uint32_t BT_S = 128;   // fp32 dS^T, 128
@@ -146,7 +148,9 @@ __global__ void __launch_bounds__(kBSThreads, 1)
     bwd_scan_kernel(const __grid_constant__ CUtensorMap map_qw,
                     const __grid_constant__ CUtensorMap map_ku,
                     const __grid_constant__ CUtensorMap map_m,
-                    const __grid_constant__ CUtensorMap map_do, const ChunkArgs a,
+                    const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ CUtensorMap map_ds,
+                    const __grid_constant__ CUtensorMap map_dut, const ChunkArgs a,
                     const BwdWs bw, const BwdOut o) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -263,6 +267,8 @@ __global__ void __launch_bounds__(kBSThreads, 1)
     const int n = min(kC, len - ch * kC);
     const long long rec = rec_of(ch);
 
+    // the previous step's image stores have read their staging tiles before they are rewritten
+    if (tid == 0) bulk_wait_read_all();
     if (!(ok = block_wait(&bar_ld[st], (it >> 1) & 1))) break;
     inflight[st] = -1;
     if (tid < 256) s_vec[tid] = reinterpret_cast<const float*>(b + B_V)[tid];
@@ -305,15 +311,20 @@ __global__ void __launch_bounds__(kBSThreads, 1)
         up[i] = pack_bf16(v16[2 * i] * s_vec[128 + 16 * wg + 2 * i],
                           v16[2 * i + 1] * s_vec[128 + 16 * wg + 2 * i + 1]);
       tmem_st8(tl + BT_UA + 8 * wg, up);
-      uint4* d = reinterpret_cast<uint4*>(bw.dut + (rec * 128 + ln) * 64 + 16 * wg);
-      d[0] = make_uint4(up[0], up[1], up[2], up[3]);
-      d[1] = make_uint4(up[4], up[5], up[6], up[7]);
+      uint8_t* row = sm + B_SDU + (ln >> 3) * 1024 + (ln & 7) * 128;
+      *reinterpret_cast<uint4*>(row + (((2 * wg) ^ (ln & 7)) << 4)) =
+          make_uint4(up[0], up[1], up[2], up[3]);
+      *reinterpret_cast<uint4*>(row + (((2 * wg + 1) ^ (ln & 7)) << 4)) =
+          make_uint4(up[4], up[5], up[6], up[7]);
+      fence_async_smem();
     }
     tc_fence_before();
     __syncthreads();
 
     // ---- dS^T += dO^T Q~ + dU^T (-W)
     if (tid == 0) {
+      tma_store_2d(&map_dut, sm + B_SDU, 0, (int)(rec * 128));
+      bulk_commit();
       tc_fence_after();
       const uint32_t qs = smem_u32(b + B_Q), wsm = smem_u32(b + B_W), dos = smem_u32(b + B_DO);
 #pragma unroll
@@ -336,15 +347,23 @@ __global__ void __launch_bounds__(kBSThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) sp[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
       tmem_st16(tl + BT_SA + 16 * wg, sp);
-      if (ch > 0) {
-        uint4* d = reinterpret_cast<uint4*>(bw.ds + (rec_of(ch - 1) * 128 + ln) * 128 + 32 * wg);
+      if (ch > 0) {  // staged for a TMA store
+        uint8_t* row = sm + B_SDS + (wg >> 1) * 16384 + (ln >> 3) * 1024 + (ln & 7) * 128;
 #pragma unroll
         for (int p = 0; p < 4; ++p)
-          d[p] = make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
+          *reinterpret_cast<uint4*>(row + (((4 * (wg & 1) + p) ^ (ln & 7)) << 4)) =
+              make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
+        fence_async_smem();
       }
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ch > 0) {
+      const int row = (int)(rec_of(ch - 1) * 128);
+      tma_store_2d(&map_ds, sm + B_SDS, 0, row);
+      tma_store_2d(&map_ds, sm + B_SDS + 16384, 64, row);
+      bulk_commit();
+    }
   }
 
   if (!ok) {
@@ -364,6 +383,7 @@ __global__ void __launch_bounds__(kBSThreads, 1)
       o.d_initial[state_off + (long long)c * kD + ln] = S[i];
     }
   }
+  if (tid == 0) bulk_wait_all();  // the image stores are done before the CTA leaves
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -977,7 +997,8 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
   if ((e = cudaFuncSetAttribute(bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kKSmem)) != cudaSuccess)
     return e;
-  bwd_scan_kernel<<<dim3(a.H, a.B), kBSThreads, kBSSmem, st>>>(mqw, mku, mm, mdo, a, bw, o);
+  bwd_scan_kernel<<<dim3(a.H, a.B), kBSThreads, kBSSmem, st>>>(mqw, mku, mm, mdo, mds, mdut, a,
+                                                                 bw, o);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bwd_chunk_kernel<<<(unsigned)recs, kKThreads, kKSmem, st>>>(mdut, mn, mut, mdo, ms0, mds, mq,
                                                                mk, mg, a, bw, o);

@@ -72,6 +72,8 @@ constexpr uint32_t kPTmemCols = 256;
 
 __device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split path gave up
 
+// kBwd: also the backward's records (rq folded into Q~ and M, and N)
+template <bool kBwd>
 __global__ void __launch_bounds__(kPThreads, 2)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qw,
                       const __grid_constant__ CUtensorMap map_q,
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
           if (R < 1) *reinterpret_cast<uint32_t*>(p160 + swi + 8 * 1024) = hmul2(kd, c12);
           if (R < 2) *reinterpret_cast<uint32_t*>(p160 + swi + 10 * 1024) = hmul2(kd, c22);
           if (R < 3) *reinterpret_cast<uint32_t*>(p160 + swi + 14 * 1024) = hmul2(kd, c32);
-          if (ws.bwd) {  // q^ e^{G_t} = rq q e^{G_t}
+          if constexpr (kBwd) {  // q^ e^{G_t} = rq q e^{G_t}
             const int t = 16 * R + i;
             const float rqt =
                 (t < n) ? a.scale * rsqrtf(s_qq[0][t] + s_qq[1][t] + kL2Eps) : 0.f;
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
         }
       } else {
         uint32_t pk[8];
-        const float mf = ws.bwd ? s_rq[r] : 1.f;  // backward records: rows of rq_r M_raw
+        const float mf = kBwd ? s_rq[r] : 1.f;  // backward records: rows of rq_r M_raw
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           const int s0 = 16 * q + 2 * p;
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
           pw[p] = pack_bf16(t0v * kv[2 * p], t1v * kv[2 * p + 1]);
         }
         const uint32_t off = sw128_offset<2>(64, r, s0);
-        if (ws.bwd) {  // N = (I + L)^{-1}, lower triangle, row r, columns s0 .. s0 + 7
+        if constexpr (kBwd) {  // N = (I + L)^{-1}, lower triangle, row r, columns s0 .. s0 + 7
           uint32_t pn[4];
 #pragma unroll
           for (int p = 0; p < 4; ++p)
@@ -627,8 +629,13 @@ constexpr uint32_t kStageTx = 74752;
 constexpr uint32_t kStageTxBwd = kStageTx - 2 * 8192 - 8192;  // no Q~, no M
 constexpr int S_OS = 2 * kStage;  // output staging [64 tok x 128] bf16 SW128
 constexpr int S_END = S_OS + 16384;
-static_assert(kStage % 1024 == 0 && S_OS % 1024 == 0, "alignment");
+// backward records only (the launch asks for this shared memory only then):
+constexpr int S_SD = S_END;         // staged S^T image [128 x 128] (two boxes)
+constexpr int S_UD = S_SD + 32768;  // staged U^T image [128 x 64]
+constexpr int S_END_BWD = S_UD + 16384;
+static_assert(kStage % 1024 == 0 && S_OS % 1024 == 0 && S_SD % 1024 == 0, "alignment");
 constexpr size_t kSSmem = S_END + 1024;
+constexpr size_t kSSmemBwd = S_END_BWD + 1024;
 
 constexpr uint32_t S_TM_DU = 0;    // S^T (-W)^T, 64
 constexpr uint32_t S_TM_DO = 64;   // O'^T, 64
@@ -637,11 +644,16 @@ constexpr uint32_t S_TM_SA = 256;  // bf16 copy of S^T (A operand), 64
 constexpr uint32_t S_TM_UA = 320;  // U'^T A operand (bf16 pairs), 32
 constexpr uint32_t kSTmemCols = 512;
 
+// kMode 0: the forward; 1: the backward's own forward pass (per-chunk images, no output);
+// 2: the training forward (output and per-chunk images)
+template <int kMode>
 __global__ void __launch_bounds__(kSThreads, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qw,
                       const __grid_constant__ CUtensorMap map_ku,
                       const __grid_constant__ CUtensorMap map_m,
-                      const __grid_constant__ CUtensorMap map_o, const ChunkArgs a,
+                      const __grid_constant__ CUtensorMap map_o,
+                      const __grid_constant__ CUtensorMap map_s0,
+                      const __grid_constant__ CUtensorMap map_ut, const ChunkArgs a,
                       const Ws ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -651,7 +663,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __shared__ int s_wait_ok[2];
   __shared__ __align__(16) float s_vec[256];  // this chunk's e^{G_C}, rk, rq
   __shared__ __align__(16) float s_one[64];   // unit output scale (rq folded into the records)
-  const bool want_out = ws.bwd != 1;
+  constexpr bool bwd = kMode != 0;
+  constexpr bool want_out = kMode != 1;
   if (threadIdx.x < 64) s_one[threadIdx.x] = 1.f;
 
   const int tid = threadIdx.x;
@@ -733,7 +746,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
     tmem_st16(tl + S_TM_SA + 16 * wg, w);
-    if (ws.bwd && nck > 0) {  // the state entering chunk 0
+    if (bwd && nck > 0) {  // the state entering chunk 0
       uint4* d = reinterpret_cast<uint4*>(ws.s0 + ((slot0 * H + h) * 128 + ln) * 128 + 32 * wg);
 #pragma unroll
       for (int p = 0; p < 4; ++p)
@@ -767,6 +780,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int n = min(kC, len - ch * kC);
     const long long tok0 = bos + (long long)ch * kC;
 
+    // the previous step's image stores have read their staging tiles before they are rewritten
+    if (tid == 0 && bwd) bulk_wait_read_all();
     if (!(ok = block_wait(&bar_ld[st], (ch >> 1) & 1))) break;
     inflight[st] = -1;
     // the stage's vectors move to static shared memory so that the stage can be refilled
@@ -811,15 +826,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
         up[i] = pack_bf16((bf16_lo(uw[i]) + v16[2 * i]) * vec[128 + 16 * wg + 2 * i],
                           (bf16_hi(uw[i]) + v16[2 * i + 1]) * vec[128 + 16 * wg + 2 * i + 1]);
       tmem_st8(tl + S_TM_UA + 8 * wg, up);
-      if (ws.bwd) {  // U^T of this chunk (before the rk row factor)
+      if (bwd) {  // U^T of this chunk (before the rk row factor), staged for a TMA store
         uint32_t u8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           u8[i] = pack_bf16(bf16_lo(uw[i]) + v16[2 * i], bf16_hi(uw[i]) + v16[2 * i + 1]);
-        uint4* d = reinterpret_cast<uint4*>(ws.ut + (((slot0 + ch) * H + h) * 128 + ln) * 64 +
-                                            16 * wg);
-        d[0] = make_uint4(u8[0], u8[1], u8[2], u8[3]);
-        d[1] = make_uint4(u8[4], u8[5], u8[6], u8[7]);
+        uint8_t* row = sm + S_UD + (ln >> 3) * 1024 + (ln & 7) * 128;
+        *reinterpret_cast<uint4*>(row + (((2 * wg) ^ (ln & 7)) << 4)) =
+            make_uint4(u8[0], u8[1], u8[2], u8[3]);
+        *reinterpret_cast<uint4*>(row + (((2 * wg + 1) ^ (ln & 7)) << 4)) =
+            make_uint4(u8[4], u8[5], u8[6], u8[7]);
+        fence_async_smem();
       }
     }
     tc_fence_before();
@@ -828,6 +845,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // ---- MMA4: O'^T += U'^T M_raw^T, S^T += U'^T K^
     if (tid == 0) {
       bulk_wait_read_all();  // the previous chunk's output store has read its staging tile
+      if (bwd) {
+        tma_store_2d(&map_ut, sm + S_UD, 0, (int)(((slot0 + ch) * H + h) * 128));
+        bulk_commit();
+      }
       tc_fence_after();
       const uint32_t ms = smem_u32(b + S_M), ks = smem_u32(b + S_KT);
 #pragma unroll
@@ -852,16 +873,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) sp[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
       tmem_st16(tl + S_TM_SA + 16 * wg, sp);
-      if (ws.bwd && ch + 1 < nck) {  // the state entering the next chunk
-        uint4* d = reinterpret_cast<uint4*>(
-            ws.s0 + (((slot0 + ch + 1) * H + h) * 128 + ln) * 128 + 32 * wg);
+      if (bwd && ch + 1 < nck) {  // the state entering the next chunk, staged
+        uint8_t* row = sm + S_SD + (wg >> 1) * 16384 + (ln >> 3) * 1024 + (ln & 7) * 128;
 #pragma unroll
         for (int p = 0; p < 4; ++p)
-          d[p] = make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
+          *reinterpret_cast<uint4*>(row + (((4 * (wg & 1) + p) ^ (ln & 7)) << 4)) =
+              make_uint4(sp[4 * p], sp[4 * p + 1], sp[4 * p + 2], sp[4 * p + 3]);
       }
       if (want_out) {
         // backward records carry rq inside Q~ and M: O' is the output itself
-        const float* const rqv = ws.bwd ? s_one : vec + 192;
+        const float* const rqv = bwd ? s_one : vec + 192;
         float o16[16];
         tmem_ld16(tl + S_TM_DO + 16 * wg, o16);
         if (n == kC) {
@@ -893,6 +914,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tma_store_3d(&map_o, sm + S_OS + 8192, 64, h, (int)tok0);
         bulk_commit();
       }
+    }
+    if (tid == 0 && bwd && ch + 1 < nck) {
+      const int row = (int)(((slot0 + ch + 1) * H + h) * 128);
+      tma_store_2d(&map_s0, sm + S_SD, 0, row);
+      tma_store_2d(&map_s0, sm + S_SD + 16384, 64, row);
+      bulk_commit();
     }
     // ---- end of chunk
   }
@@ -990,7 +1017,7 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
   const long long rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
   const long long map_rows = rows > 0 ? rows : 1;
   const long long rec_rows = ws.recs > 0 ? ws.recs : 1;
-  CUtensorMap mqw, mku, mm, mo, mq, mk, mv, mg;
+  CUtensorMap mqw, mku, mm, mo, mq, mk, mv, mg, ms0, mut;
   // the backward's scan writes no output: its (unused) output map is laid over q
   if (!make_map_2d(&mqw, ws.qw, 2 * rec_rows * 64, 128, 64) ||
       !make_map_2d(&mku, ws.ku, 2 * rec_rows * 128, 64, 128) ||
@@ -1000,11 +1027,19 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
       !make_map_in(&mk, a.k, map_rows, a.H, false) ||
       !make_map_in(&mv, a.v, map_rows, a.H, false) || !make_map_in(&mg, a.g, map_rows, a.H, true))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
+  // the per-chunk images of the backward records (laid over q when there are none)
+  if (!make_map_2d(&ms0, ws.bwd ? (const void*)ws.s0 : a.q, ws.bwd ? rec_rows * 128 : 1, 128,
+                   128) ||
+      !make_map_2d(&mut, ws.bwd ? (const void*)ws.ut : a.q, ws.bwd ? rec_rows * 128 : 1, 64, 128))
+    return cudaErrorInvalidValue;
+  auto prep = ws.bwd ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+  auto scan = ws.bwd == 0 ? chunk_scan_kernel<0> : ws.bwd == 1 ? chunk_scan_kernel<1>
+                                                                : chunk_scan_kernel<2>;
+  const size_t scan_smem = ws.bwd ? kSSmemBwd : kSSmem;
+  cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kPSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSSmem);
+  e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem);
   if (e != cudaSuccess) return e;
   if (ws.recs > 0) {
     // persistent: two CTAs per SM (shared memory and Tensor Memory admit no more)
@@ -1013,10 +1048,10 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
     const long long grid = std::min<long long>(ws.recs, 2LL * sms);
-    chunk_prep_kernel<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mqw, mq, mk, mv, mg, a, ws);
+    prep<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mqw, mq, mk, mv, mg, a, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  chunk_scan_kernel<<<dim3(a.H, a.B), kSThreads, kSSmem, st>>>(mqw, mku, mm, mo, a, ws);
+  scan<<<dim3(a.H, a.B), kSThreads, scan_smem, st>>>(mqw, mku, mm, mo, ms0, mut, a, ws);
   return cudaGetLastError();
 }
 
