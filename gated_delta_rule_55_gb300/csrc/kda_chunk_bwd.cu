@@ -615,13 +615,15 @@ __global__ void __launch_bounds__(kKThreads, 1)
     const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
     uint32_t dw[8];
     float lu0[8], lu1[8];
+    __nv_bfloat16* const dv_p = o.dv + row_of(16 * R) * kD + j;  // token 16 R; H * 128 apart
+    const long long tstride = (long long)H * kD;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       const int t0 = 16 * R + 2 * p;
       const float v0 = s_beta[t0] * lam[2 * p], v1 = s_beta[t0 + 1] * lam[2 * p + 1];
       dw[p] = pack_bf16(v0, v1);
-      if (t0 < n) o.dv[row_of(t0) * kD + j] = __float2bfloat16_rn(v0);
-      if (t0 + 1 < n) o.dv[row_of(t0 + 1) * kD + j] = __float2bfloat16_rn(v1);
+      if (t0 < n) dv_p[(2 * p) * tstride] = __float2bfloat16_rn(v0);
+      if (t0 + 1 < n) dv_p[(2 * p + 1) * tstride] = __float2bfloat16_rn(v1);
       const float l0 = lam[2 * p] * bf16_lo(uw[p]), l1 = lam[2 * p + 1] * bf16_hi(uw[p]);
       if (p < 4) { lu0[2 * p] = l0; lu0[2 * p + 1] = l1; }
       else { lu1[2 * (p - 4)] = l0; lu1[2 * (p - 4) + 1] = l1; }
@@ -856,17 +858,22 @@ __global__ void __launch_bounds__(kKThreads, 1)
     __syncthreads();
     float ddb = 0.f, dal = 0.f;
     const float inv_s2 = 1.f / (a.scale * a.scale);
+    const float lb = a.lower_bound;
+    // this thread's element of token 16 R in each [B, T, H, 128] output; tokens H * 128 apart
+    const long long base = row_of(16 * R) * kD + c, tstride = (long long)H * kD;
+    float* const dg_p = o.dg + base;
+    __nv_bfloat16* const dq_p = o.dq + base;
+    __nv_bfloat16* const dk_p = o.dk + base;
 #pragma unroll
     for (int i = 15; i >= 0; --i) {
       carry += dG[i];
       const int t = 16 * R + i;
       if (t < n) {
-        const long long row = row_of(t);
         // gate: gamma = lb sigmoid(x), x = e^{a_log} (g + dt_bias)
         const float x = ea * (rg_t[t * 32] + db);
         const float sg = fast_rcp(1.f + fast_exp(-x));
-        const float dx = carry * a.lower_bound * sg * (1.f - sg);
-        o.dg[row * kD + c] = dx * ea;
+        const float dx = carry * lb * sg * (1.f - sg);
+        dg_p[i * tstride] = dx * ea;
         ddb += dx * ea;
         dal += dx * x;
         // L2 norms: q^ = rq q with rq = scale / |q|, k^ = rk k
@@ -874,8 +881,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
         const float rq = s_rq[t], rk = s_rk[t];
         const float qh = raw_q(t) * rq;
         const float kh = raw_k(t) * rk;
-        o.dq[row * kD + c] = __float2bfloat16_rn(rq * AQ[t * kD + c] - qh * qdt * rq * inv_s2);
-        o.dk[row * kD + c] = __float2bfloat16_rn(rk * DKH[t * kD + c] - kh * kdt * rk);
+        dq_p[i * tstride] = __float2bfloat16_rn(rq * AQ[t * kD + c] - qh * qdt * rq * inv_s2);
+        dk_p[i * tstride] = __float2bfloat16_rn(rk * DKH[t * kD + c] - kh * kdt * rk);
       }
     }
     s_ddb[R][c] = ddb;
