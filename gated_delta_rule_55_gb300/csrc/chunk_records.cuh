@@ -117,6 +117,8 @@ inline bool make_map_in(CUtensorMap* m, const void* base, long long rows, int H,
 // must already be in ws.coff).  With ws.bwd set they keep the backward's records instead
 // of producing the output.
 cudaError_t launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream_t st);
+// The first chunk slot of every packed sequence into ws.coff (one CTA).
+cudaError_t launch_chunk_offsets(const ChunkArgs& a, const Ws& ws, cudaStream_t st);
 
 }  // namespace split
 }  // namespace kda

@@ -334,6 +334,61 @@ int kda_chunk_bwd_saved(const void* q, const void* k, const void* v, const float
                     stream, true);
 }
 
+size_t kda_chunk_bwd_varlen_workspace_size(int N, int total_T, int H, int dk, int dv,
+                                          int dtype) {
+  if (N < 0 || total_T < 0 || H <= 0 || !head_dim_ok(dk) || !head_dim_ok(dv)) return 0;
+  static const int32_t marker = 0;  // only the presence of cu_seqlens matters here
+  kda::ChunkArgs a = bwd_shape(N, 0, H, dk, dv);
+  a.cu_seqlens = &marker;
+  a.total_T = total_T;
+  if (!kda::chunk_bwd_supported(a, dtype == KDA_BF16)) return 0;
+  return kda::chunk_bwd_workspace(a);
+}
+
+int kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta_logits, const float* a_log, const float* dt_bias,
+                         float scale, float lower_bound, const int32_t* cu_seqlens, int N,
+                         int total_T, const float* initial_state, const void* d_out,
+                         const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                         float* dbeta_logits, float* da_log, float* ddt_bias,
+                         float* d_initial_state, int H, int dim_k, int dim_v, int dtype,
+                         void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+  kda::ChunkArgs a;
+  int s = fill_varlen(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                      cu_seqlens, N, total_T, initial_state, dq, nullptr, H, dim_k, dim_v, 64);
+  if (s != KDA_OK) return s;
+  if (!d_out || !dq || !dk || !dv || !dg || !dbeta_logits || !da_log || !ddt_bias)
+    return KDA_ERR_NULL_POINTER;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  // packed sequences are served on the tensor-core path only
+  if (!kda::chunk_bwd_supported(a, dtype == KDA_BF16))
+    return dtype != KDA_BF16 ? KDA_ERR_DTYPE
+                             : (dim_k != 128 || dim_v != 128) ? KDA_ERR_HEAD_DIM
+                                                              : KDA_ERR_TOO_LARGE;
+  const void* ptrs[] = {q, k, v, g, beta_logits, a_log, dt_bias, cu_seqlens, initial_state,
+                        d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log, ddt_bias,
+                        d_initial_state};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  if ((double)total_T * H * 128 >= 1099511627776.0 || N > 65535 || H > 65535)
+    return KDA_ERR_TOO_LARGE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < kda::chunk_bwd_workspace(a))
+    return KDA_ERR_WORKSPACE;
+  s = check_device();
+  if (s != KDA_OK) return s;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (N == 0) {
+    e = cudaMemsetAsync(da_log, 0, sizeof(float) * H, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * dim_k * H, st);
+  } else {
+    e = kda::launch_chunk_bwd(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
+                              ddt_bias, d_initial_state, workspace, false, st);
+  }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 int kda_chunk_fwd_train(const void* q, const void* k, const void* v, const float* g,
                         const float* beta_logits, const float* a_log, const float* dt_bias,
                         float scale, float lower_bound, const float* initial_state, void* out,

@@ -167,10 +167,18 @@ __global__ void __launch_bounds__(kBSThreads, 1)
   const int lane_base = 32 * (warp & 3);
   const int h = blockIdx.x, seq = blockIdx.y;
   const int H = a.H;
-  const long long bos = (long long)seq * a.T;
-  const int len = a.T;
-  const int nck = bw.f.nck_fixed;
-  const long long slot0 = (long long)seq * nck;
+  long long bos;
+  int len;
+  seq_range(a, seq, bos, len);
+  long long slot0;
+  int nck;
+  if (a.cu_seqlens) {
+    slot0 = bw.f.coff[seq];
+    nck = bw.f.coff[seq + 1] - bw.f.coff[seq];
+  } else {
+    slot0 = (long long)seq * bw.f.nck_fixed;
+    nck = bw.f.nck_fixed;
+  }
   const long long state_off = ((long long)seq * H + h) * kD * kD;
   auto rec_of = [&](int ch) -> long long { return (slot0 + ch) * H + h; };
 
@@ -468,10 +476,28 @@ __global__ void __launch_bounds__(kKThreads, 1)
   const long long rec = blockIdx.x;
   const int h = (int)(rec % H);
   const long long slot = rec / H;
-  const int nck = bw.f.nck_fixed;
-  const int seq = (int)(slot / nck), jc = (int)(slot % nck);
-  const long long tok0 = (long long)seq * a.T + (long long)jc * kC;
-  const int n = min(kC, a.T - jc * kC);
+  int seq, jc;
+  if (a.cu_seqlens) {
+    // record -> sequence; records past the last chunk exist because their count is an
+    // upper bound for packed sequences (uniform over the CTA, before any setup)
+    const int N = a.B;
+    if (slot >= bw.f.coff[N]) return;
+    int lo = 0, hi = N;  // coff[lo] <= slot < coff[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (bw.f.coff[mid] <= slot) lo = mid; else hi = mid;
+    }
+    seq = lo;
+    jc = (int)(slot - bw.f.coff[lo]);
+  } else {
+    seq = (int)(slot / bw.f.nck_fixed);
+    jc = (int)(slot % bw.f.nck_fixed);
+  }
+  long long bos;
+  int len;
+  seq_range(a, seq, bos, len);
+  const long long tok0 = bos + (long long)jc * kC;
+  const int n = min(kC, len - jc * kC);
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, kKTmemCols);
@@ -915,15 +941,21 @@ done:
 
 }  // namespace
 
+// Bytes of the forward records and, for packed sequences, the chunk offsets after them.
+size_t head_bytes(const ChunkArgs& a, long long recs) {
+  const size_t coff = a.cu_seqlens ? size_t(a.B + 1) * 4 : 0;
+  return align_up(record_bytes(recs) + coff, 256);
+}
+
 size_t chunk_bwd_workspace(const ChunkArgs& a) {
   const long long recs = slots_for(a) * a.H;
-  return align_up(record_bytes(recs), 256) +
+  return head_bytes(a, recs) +
          size_t(recs) * size_t(kRecM + kRecState + kRecTile + kRecState + kRecTile);
 }
 
 bool chunk_bwd_supported(const ChunkArgs& a, bool bf16) {
-  return bf16 && a.dk == 128 && a.dv == 128 && a.chunk == 64 && !a.cu_seqlens && !a.gate_head &&
-         !a.beta_prob && !a.no_l2norm && !a.literal && a.T > 0 &&
+  return bf16 && a.dk == 128 && a.dv == 128 && a.chunk == 64 && !a.gate_head && !a.beta_prob &&
+         !a.no_l2norm && !a.literal && (a.cu_seqlens || a.T > 0) &&
          slots_for(a) * a.H * 256 < 0x7fffffffLL;
 }
 
@@ -935,7 +967,7 @@ void carve_bwd(const ChunkArgs& a, void* workspace, BwdWs& bw) {
   uint8_t* p = static_cast<uint8_t*>(workspace);
   carve_records(a, p, bw.f);
   const long long recs = bw.f.recs;
-  p += align_up(record_bytes(recs), 256);
+  p += head_bytes(a, recs);
   bw.f.nrec = reinterpret_cast<__nv_bfloat16*>(p);
   p += recs * kRecM;
   bw.f.s0 = reinterpret_cast<__nv_bfloat16*>(p);
@@ -953,6 +985,10 @@ cudaError_t launch_chunk_fwd_train(const ChunkArgs& a, void* workspace, cudaStre
   BwdWs bw{};
   carve_bwd(a, workspace, bw);
   bw.f.bwd = 2;
+  if (a.cu_seqlens) {
+    const cudaError_t e = split::launch_chunk_offsets(a, bw.f, st);
+    if (e != cudaSuccess) return e;
+  }
   return split::launch_prep_scan(a, bw.f, st);
 }
 
@@ -982,10 +1018,12 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
     f.out = nullptr;
     f.final_state = nullptr;
     bw.f.bwd = 1;
+    if (a.cu_seqlens && (e = split::launch_chunk_offsets(a, bw.f, st)) != cudaSuccess) return e;
     if ((e = split::launch_prep_scan(f, bw.f, st)) != cudaSuccess) return e;
   }
 
-  const long long rows = (long long)a.B * a.T;
+  const long long tok_rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
+  const long long rows = tok_rows > 0 ? tok_rows : 1;
   CUtensorMap mqw, mku, mm, mdo, mdut, mn, mut, ms0, mds, mq, mk, mg;
   if (!make_map_2d(&mqw, bw.f.qw, 2 * recs * 64, 128, 64) ||
       !make_map_2d(&mku, bw.f.ku, 2 * recs * 128, 64, 128) ||

@@ -1055,12 +1055,16 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
   return cudaGetLastError();
 }
 
+cudaError_t split::launch_chunk_offsets(const ChunkArgs& a, const Ws& ws, cudaStream_t st) {
+  chunk_offsets_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.B, a.total_T, ws.coff);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t st) {
   Ws ws{};
   carve_records(a, workspace, ws);
   if (a.cu_seqlens) {
-    chunk_offsets_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.B, a.total_T, ws.coff);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = split::launch_chunk_offsets(a, ws, st);
     if (e != cudaSuccess) return e;
   }
   return split::launch_prep_scan(a, ws, st);

@@ -26,6 +26,7 @@ STATUS_NAMES = {
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_size",
            "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
            "kda_chunk_fwd_noalloc", "kda_chunk_bwd_workspace_size", "kda_chunk_bwd",
+           "kda_chunk_bwd_varlen_workspace_size", "kda_chunk_bwd_varlen",
            "kda_chunk_fwd_train", "kda_chunk_bwd_saved", "kda_recurrent_attention_fwd", "kda_attention_fwd", "kda_decode_step",
            "kda_status_string",
            "kda_version", "kda_device_error")
@@ -74,6 +75,10 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_bwd_workspace_size.restype = _Z
     L.kda_chunk_bwd.argtypes = ([_P] * 7 + [_F, _F] + [_P] * 11 + [_I] * 6 + [_P, _Z, _P])
     L.kda_chunk_bwd_saved.argtypes = L.kda_chunk_bwd.argtypes
+    L.kda_chunk_bwd_varlen_workspace_size.argtypes = [_I] * 6
+    L.kda_chunk_bwd_varlen_workspace_size.restype = _Z
+    L.kda_chunk_bwd_varlen.argtypes = ([_P] * 7 + [_F, _F, _P, _I, _I] + [_P] * 11 + [_I] * 4 +
+                                       [_P, _Z, _P])
     L.kda_chunk_fwd_train.argtypes = L.kda_chunk_fwd_ws.argtypes
     L.kda_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
                                     _I, _I, _P]
@@ -82,7 +87,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_device_error.argtypes = [_I]
     for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
               "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_chunk_bwd",
-              "kda_chunk_bwd_saved", "kda_chunk_fwd_train",
+              "kda_chunk_bwd_saved", "kda_chunk_fwd_train", "kda_chunk_bwd_varlen",
               "kda_attention_fwd", "kda_recurrent_attention_fwd",
               "kda_decode_step", "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
@@ -236,6 +241,25 @@ def kda_chunk_bwd(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, i
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta_logits), _ptr(da_log), _ptr(ddt_bias),
         _ptr(d_initial_state), B, T, H, dk_dim, dv_dim, _dtype_code(q, dtype), wp, wb,
         _stream(stream)))
+
+
+def kda_chunk_bwd_varlen_workspace_size(N, total_T, H, dk, dv, dtype=KDA_BF16) -> int:
+    """Device workspace bytes kda_chunk_bwd_varlen needs (0: unsupported)."""
+    return int(lib().kda_chunk_bwd_varlen_workspace_size(N, total_T, H, dk, dv, dtype))
+
+
+def kda_chunk_bwd_varlen(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                         cu_seqlens, N, total_T, initial_state, d_out, d_final_state, dq, dk,
+                         dv, dg, dbeta_logits, da_log, ddt_bias, d_initial_state, H, dk_dim,
+                         dv_dim, dtype=None, workspace=None, stream=None):
+    """Gradients of kda_chunk_fwd_varlen (packed sequences; see include/kda.h)."""
+    wp, wb = _ws(workspace)
+    _check("kda_chunk_bwd_varlen", lib().kda_chunk_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
+        _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+        _ptr(dbeta_logits), _ptr(da_log), _ptr(ddt_bias), _ptr(d_initial_state), H, dk_dim,
+        dv_dim, _dtype_code(q, dtype), wp, wb, _stream(stream)))
 
 
 def kda_chunk_fwd_train(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,

@@ -207,6 +207,28 @@ int kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_bwd_varlen -- kda_chunk_bwd for packed sequences (the cu_seqlens convention of
+ *   kda_chunk_fwd_varlen): q, k, g, d_out, dq, dk, dg [total_T, H, dk], v, dv [total_T, H, dv],
+ *   beta_logits, dbeta_logits [total_T, H]; initial_state, d_final_state, d_initial_state
+ *   [N, H, dk, dv] (each nullable as in kda_chunk_bwd); da_log [H] and ddt_bias [dk, H] sum
+ *   over every sequence.  Each sequence is differentiated on its own (its own initial state
+ *   and final-state cotangent).  Served on the tensor-core path only: bf16 q/k/v/d_out with
+ *   dk = dv = 128 (others give KDA_ERR_DTYPE / KDA_ERR_HEAD_DIM).  workspace: at least
+ *   kda_chunk_bwd_varlen_workspace_size(N, total_T, H, dk, dv, dtype) bytes (0 for an
+ *   unsupported configuration), 256-byte aligned.
+ */
+size_t kda_chunk_bwd_varlen_workspace_size(int N, int total_T, int H, int dk, int dv,
+                                          int dtype);
+int kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta_logits, const float* a_log, const float* dt_bias,
+                         float scale, float lower_bound, const int32_t* cu_seqlens, int N,
+                         int total_T, const float* initial_state, const void* d_out,
+                         const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                         float* dbeta_logits, float* da_log, float* ddt_bias,
+                         float* d_initial_state, int H, int dim_k, int dim_v, int dtype,
+                         void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_train -- the forward of kda_chunk_fwd_ws (same inputs, outputs, layouts and
  *   error codes) for training: besides out and final_state it leaves in `workspace` the
  *   chunk records and per-chunk states that kda_chunk_bwd_saved reads, so that the backward

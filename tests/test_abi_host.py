@@ -333,3 +333,32 @@ def _bwd_saved(L, **over):
 ])
 def test_saved_backward_rejects_other_configurations(L, over, code):
     assert _bwd_saved(L, **over) == code
+
+
+def test_varlen_backward_workspace_size_formula(L):
+    """Packed sequences: the fixed-length chunked layout over total_T / 64 + N chunk slots,
+    with the (N + 1) int32 chunk offsets after the forward records."""
+    N, total, H = 3, 1000, 2
+    recs = (total // 64 + N) * H
+    head = _al(recs * (4 * 16384 + 8192 + 1024) + (N + 1) * 4)
+    want = head + recs * (8192 + 32768 + 16384 + 32768 + 16384)
+    assert kda.kda_chunk_bwd_varlen_workspace_size(N, total, H, 128, 128, kda.KDA_BF16) == want
+    assert kda.kda_chunk_bwd_varlen_workspace_size(N, total, H, 128, 128, kda.KDA_F32) == 0
+    assert kda.kda_chunk_bwd_varlen_workspace_size(N, total, H, 64, 128, kda.KDA_BF16) == 0
+
+
+def _bwd_varlen(L, **over):
+    a = dict(cu=FAKE, N=2, total=100, H=2, dk=128, dv=128, dtype=1, ws=0x100000, nbytes=1 << 40)
+    a.update(over)
+    return L.kda_chunk_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, -1.0, a["cu"],
+                                  a["N"], a["total"], None, FAKE, None, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, FAKE, FAKE, None, a["H"], a["dk"], a["dv"], a["dtype"],
+                                  a["ws"], a["nbytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(cu=None), -1), (dict(N=-1), -2), (dict(dtype=0), -7), (dict(dk=64), -3),
+    (dict(dv=32), -3), (dict(ws=None), -12), (dict(nbytes=16), -12),
+])
+def test_varlen_backward_rejects_bad_arguments(L, over, code):
+    assert _bwd_varlen(L, **over) == code

@@ -1,0 +1,123 @@
+"""kda_chunk_bwd_varlen (packed sequences) against the oracle backward run on each sequence
+alone (its own initial state and final-state cotangent; da_log and ddt_bias summed over the
+sequences), and against kda_chunk_bwd when every sequence has the same length.  bf16:
+max-norm relative error <= 2e-2 per gradient tensor, the oracle fed the same bf16-rounded
+q, k, v and d_out."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_55_gb300 as kda
+from gated_delta_rule_55_gb300 import synth
+from gpu_helpers import BF16_REL, bf16_round, ensure_built, rel_err, to_dev, workspace
+from oracle import kda_backward
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _packed(lengths, H, seed):
+    d = synth.varlen_inputs(lengths, H, 128, 128, seed)
+    total = int(d["cu_seqlens"][-1])
+    r = np.random.default_rng(700 + seed)
+    d["d_out"] = r.normal(size=(total, H, 128))
+    d["d_final_state"] = r.normal(size=(len(lengths), H, 128, 128))
+    return d, total
+
+
+def _run(d, total, N, H, scale, lb):
+    io = torch.bfloat16
+    q, k, v = (to_dev(d[n], io) for n in ("q", "k", "v"))
+    g, bl, al, db = (to_dev(d[n]) for n in ("g", "beta_logits", "a_log", "dt_bias"))
+    cu = torch.from_numpy(d["cu_seqlens"].astype(np.int32)).cuda()
+    dout = to_dev(d["d_out"], io)
+    out = {"dq": torch.full((total, H, 128), float("nan"), device="cuda", dtype=io),
+           "dk": torch.full((total, H, 128), float("nan"), device="cuda", dtype=io),
+           "dv": torch.full((total, H, 128), float("nan"), device="cuda", dtype=io),
+           "dg": torch.full((total, H, 128), float("nan"), device="cuda"),
+           "dbeta_logits": torch.full((total, H), float("nan"), device="cuda"),
+           "da_log": torch.full((H,), float("nan"), device="cuda"),
+           "ddt_bias": torch.full((128, H), float("nan"), device="cuda"),
+           "dinitial_state": torch.full((N, H, 128, 128), float("nan"), device="cuda")}
+    w = workspace(kda.kda_chunk_bwd_varlen_workspace_size(N, total, H, 128, 128))
+    kda.kda_chunk_bwd_varlen(q, k, v, g, bl, al, db, scale, lb, cu, N, total,
+                             to_dev(d["initial_state"]), dout, to_dev(d["d_final_state"]),
+                             out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta_logits"],
+                             out["da_log"], out["ddt_bias"], out["dinitial_state"], H, 128, 128,
+                             workspace=w)
+    torch.cuda.synchronize()
+    return {n: t.float().cpu().numpy() for n, t in out.items()}
+
+
+def _oracle(d, lengths, H, scale, lb):
+    cu = d["cu_seqlens"]
+    per = {"dq": [], "dk": [], "dv": [], "dg": [], "dbeta_logits": [], "dinitial_state": []}
+    da = np.zeros(H)
+    ddt = np.zeros((128, H))
+    for i, L in enumerate(lengths):
+        a, b = int(cu[i]), int(cu[i + 1])
+        sl = lambda x: x[a:b][None]  # noqa: E731
+        r = kda_backward(bf16_round(sl(d["q"])), bf16_round(sl(d["k"])), bf16_round(sl(d["v"])),
+                         sl(d["g"]), sl(d["beta_logits"]), d["a_log"], d["dt_bias"],
+                         bf16_round(sl(d["d_out"])), d["d_final_state"][i:i + 1], scale, lb,
+                         d["initial_state"][i:i + 1])
+        for n in ("dq", "dk", "dv", "dg", "dbeta_logits"):
+            per[n].append(r[n][0])
+        per["dinitial_state"].append(r["dinitial_state"][0])
+        da += r["da_log"]
+        ddt += r["ddt_bias"]
+    ref = {n: np.concatenate(v, axis=0) for n, v in per.items() if n != "dinitial_state"}
+    ref["dinitial_state"] = np.stack(per["dinitial_state"])
+    ref["da_log"], ref["ddt_bias"] = da, ddt
+    return ref
+
+
+@pytest.mark.parametrize("lengths,lb", [
+    ([70, 0, 129, 64, 1], -2.0),   # ragged tails, an empty sequence, a one-token sequence
+    ([300, 45], -5.0),
+])
+def test_varlen_backward_matches_per_sequence_oracle(lengths, lb):
+    H, scale = 2, 128 ** -0.5
+    d, total = _packed(lengths, H, len(lengths))
+    gpu = _run(d, total, len(lengths), H, scale, lb)
+    ref = _oracle(d, lengths, H, scale, lb)
+    for n in ref:
+        assert rel_err(gpu[n], ref[n]) <= BF16_REL, (n, rel_err(gpu[n], ref[n]))
+    assert kda.kda_device_error(1) == 0
+
+
+def test_varlen_backward_equals_fixed_length_backward():
+    """Equal lengths: the packed layout is the fixed-length layout, so the gradients agree
+    with kda_chunk_bwd exactly (da_log and ddt_bias up to the order of their atomic sums)."""
+    N, T, H, scale, lb = 2, 150, 2, 128 ** -0.5, -2.0
+    d, total = _packed([T] * N, H, 9)
+    gpu = _run(d, total, N, H, scale, lb)
+    io = torch.bfloat16
+    q, k, v = (to_dev(d[n].reshape(N, T, H, 128), io) for n in ("q", "k", "v"))
+    g = to_dev(d["g"].reshape(N, T, H, 128))
+    bl = to_dev(d["beta_logits"].reshape(N, T, H))
+    al, db = to_dev(d["a_log"]), to_dev(d["dt_bias"])
+    dout = to_dev(d["d_out"].reshape(N, T, H, 128), io)
+    f = {"dq": torch.empty(N, T, H, 128, device="cuda", dtype=io),
+         "dk": torch.empty(N, T, H, 128, device="cuda", dtype=io),
+         "dv": torch.empty(N, T, H, 128, device="cuda", dtype=io),
+         "dg": torch.empty(N, T, H, 128, device="cuda"),
+         "dbeta_logits": torch.empty(N, T, H, device="cuda"),
+         "da_log": torch.empty(H, device="cuda"), "ddt_bias": torch.empty(128, H, device="cuda"),
+         "dinitial_state": torch.empty(N, H, 128, 128, device="cuda")}
+    w = workspace(kda.kda_chunk_bwd_workspace_size(N, T, H, 128, 128))
+    kda.kda_chunk_bwd(q, k, v, g, bl, al, db, scale, lb, to_dev(d["initial_state"]), dout,
+                      to_dev(d["d_final_state"]), f["dq"], f["dk"], f["dv"], f["dg"],
+                      f["dbeta_logits"], f["da_log"], f["ddt_bias"], f["dinitial_state"], N, T, H,
+                      128, 128, workspace=w)
+    torch.cuda.synchronize()
+    for n, t in f.items():
+        fixed = t.float().cpu().numpy()
+        if n in ("da_log", "ddt_bias"):
+            assert rel_err(gpu[n], fixed) <= 1e-5, n
+        else:
+            assert np.array_equal(gpu[n].reshape(fixed.shape), fixed), n
