@@ -345,14 +345,18 @@ size_t kda_chunk_bwd_varlen_workspace_size(int N, int total_T, int H, int dk, in
   return kda::chunk_bwd_workspace(a);
 }
 
-int kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const float* g,
-                         const float* beta_logits, const float* a_log, const float* dt_bias,
-                         float scale, float lower_bound, const int32_t* cu_seqlens, int N,
-                         int total_T, const float* initial_state, const void* d_out,
-                         const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
-                         float* dbeta_logits, float* da_log, float* ddt_bias,
-                         float* d_initial_state, int H, int dim_k, int dim_v, int dtype,
-                         void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int bwd_varlen_common(const void* q, const void* k, const void* v, const float* g,
+                      const float* beta_logits, const float* a_log, const float* dt_bias,
+                      float scale, float lower_bound, const int32_t* cu_seqlens, int N,
+                      int total_T, const float* initial_state, const void* d_out,
+                      const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                      float* dbeta_logits, float* da_log, float* ddt_bias, float* d_initial_state,
+                      int H, int dim_k, int dim_v, int dtype, void* workspace,
+                      size_t workspace_bytes, kda_stream_t stream, bool saved) {
   kda::ChunkArgs a;
   int s = fill_varlen(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
                       cu_seqlens, N, total_T, initial_state, dq, nullptr, H, dim_k, dim_v, 64);
@@ -384,8 +388,77 @@ int kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const floa
     if (e == cudaSuccess) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * dim_k * H, st);
   } else {
     e = kda::launch_chunk_bwd(a, d_out, d_final_state, dq, dk, dv, dg, dbeta_logits, da_log,
-                              ddt_bias, d_initial_state, workspace, false, st);
+                              ddt_bias, d_initial_state, workspace, saved, st);
   }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta_logits, const float* a_log, const float* dt_bias,
+                         float scale, float lower_bound, const int32_t* cu_seqlens, int N,
+                         int total_T, const float* initial_state, const void* d_out,
+                         const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                         float* dbeta_logits, float* da_log, float* ddt_bias,
+                         float* d_initial_state, int H, int dim_k, int dim_v, int dtype,
+                         void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+  return bwd_varlen_common(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                           cu_seqlens, N, total_T, initial_state, d_out, d_final_state, dq, dk,
+                           dv, dg, dbeta_logits, da_log, ddt_bias, d_initial_state, H, dim_k,
+                           dim_v, dtype, workspace, workspace_bytes, stream, false);
+}
+
+int kda_chunk_bwd_saved_varlen(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta_logits, const float* a_log,
+                               const float* dt_bias, float scale, float lower_bound,
+                               const int32_t* cu_seqlens, int N, int total_T,
+                               const float* initial_state, const void* d_out,
+                               const float* d_final_state, void* dq, void* dk, void* dv,
+                               float* dg, float* dbeta_logits, float* da_log, float* ddt_bias,
+                               float* d_initial_state, int H, int dim_k, int dim_v, int dtype,
+                               void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+  return bwd_varlen_common(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                           cu_seqlens, N, total_T, initial_state, d_out, d_final_state, dq, dk,
+                           dv, dg, dbeta_logits, da_log, ddt_bias, d_initial_state, H, dim_k,
+                           dim_v, dtype, workspace, workspace_bytes, stream, true);
+}
+
+int kda_chunk_fwd_train_varlen(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta_logits, const float* a_log,
+                               const float* dt_bias, float scale, float lower_bound,
+                               const int32_t* cu_seqlens, int N, int total_T,
+                               const float* initial_state, void* out, float* final_state, int H,
+                               int dk, int dv, int chunk, int dtype, void* workspace,
+                               size_t workspace_bytes, kda_stream_t stream) {
+  kda::ChunkArgs a;
+  const int s = fill_varlen(a, q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                            cu_seqlens, N, total_T, initial_state, out, final_state, H, dk, dv,
+                            chunk);
+  if (s != KDA_OK) return s;
+  if (N == 0 || total_T == 0)  // no tokens: the plain forward (state copy), nothing to keep
+    return chunk_common(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+  if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_DTYPE;
+  if (chunk != 16 && chunk != 64) return KDA_ERR_CHUNK;
+  if (!kda::chunk_bwd_supported(a, dtype == KDA_BF16))
+    return dtype != KDA_BF16 ? KDA_ERR_DTYPE
+           : chunk != 64     ? KDA_ERR_CHUNK
+           : (dk != 128 || dv != 128) ? KDA_ERR_HEAD_DIM : KDA_ERR_TOO_LARGE;
+  const void* ptrs[] = {q, k, v, g, beta_logits, a_log, dt_bias, cu_seqlens, initial_state,
+                        out, final_state};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  if ((double)total_T * H * 128 >= 1099511627776.0 || N > 65535 || H > 65535)
+    return KDA_ERR_TOO_LARGE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < kda::chunk_bwd_workspace(a))
+    return KDA_ERR_WORKSPACE;
+  const int d = check_device();
+  if (d != KDA_OK) return d;
+  const cudaError_t e =
+      kda::launch_chunk_fwd_train(a, workspace, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 

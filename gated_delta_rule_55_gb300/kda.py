@@ -27,6 +27,7 @@ EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_siz
            "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
            "kda_chunk_fwd_noalloc", "kda_chunk_bwd_workspace_size", "kda_chunk_bwd",
            "kda_chunk_bwd_varlen_workspace_size", "kda_chunk_bwd_varlen",
+           "kda_chunk_fwd_train_varlen", "kda_chunk_bwd_saved_varlen",
            "kda_chunk_fwd_train", "kda_chunk_bwd_saved", "kda_recurrent_attention_fwd", "kda_attention_fwd", "kda_decode_step",
            "kda_status_string",
            "kda_version", "kda_device_error")
@@ -79,6 +80,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_bwd_varlen_workspace_size.restype = _Z
     L.kda_chunk_bwd_varlen.argtypes = ([_P] * 7 + [_F, _F, _P, _I, _I] + [_P] * 11 + [_I] * 4 +
                                        [_P, _Z, _P])
+    L.kda_chunk_bwd_saved_varlen.argtypes = L.kda_chunk_bwd_varlen.argtypes
+    L.kda_chunk_fwd_train_varlen.argtypes = L.kda_chunk_fwd_varlen_ws.argtypes
     L.kda_chunk_fwd_train.argtypes = L.kda_chunk_fwd_ws.argtypes
     L.kda_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
                                     _I, _I, _P]
@@ -88,6 +91,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
               "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_chunk_bwd",
               "kda_chunk_bwd_saved", "kda_chunk_fwd_train", "kda_chunk_bwd_varlen",
+              "kda_chunk_fwd_train_varlen", "kda_chunk_bwd_saved_varlen",
               "kda_attention_fwd", "kda_recurrent_attention_fwd",
               "kda_decode_step", "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
@@ -255,6 +259,32 @@ def kda_chunk_bwd_varlen(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_b
     """Gradients of kda_chunk_fwd_varlen (packed sequences; see include/kda.h)."""
     wp, wb = _ws(workspace)
     _check("kda_chunk_bwd_varlen", lib().kda_chunk_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
+        _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+        _ptr(dbeta_logits), _ptr(da_log), _ptr(ddt_bias), _ptr(d_initial_state), H, dk_dim,
+        dv_dim, _dtype_code(q, dtype), wp, wb, _stream(stream)))
+
+
+def kda_chunk_fwd_train_varlen(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                               cu_seqlens, N, total_T, initial_state, out, final_state, H, dk,
+                               dv, chunk=64, dtype=None, workspace=None, stream=None):
+    """The packed-sequence training forward (see include/kda.h)."""
+    wp, wb = _ws(workspace)
+    _check("kda_chunk_fwd_train_varlen", lib().kda_chunk_fwd_train_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
+        float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
+        _ptr(out), _ptr(final_state), H, dk, dv, chunk, _dtype_code(q, dtype), wp, wb,
+        _stream(stream)))
+
+
+def kda_chunk_bwd_saved_varlen(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,
+                               cu_seqlens, N, total_T, initial_state, d_out, d_final_state, dq,
+                               dk, dv, dg, dbeta_logits, da_log, ddt_bias, d_initial_state, H,
+                               dk_dim, dv_dim, dtype=None, workspace=None, stream=None):
+    """kda_chunk_bwd_varlen reading what kda_chunk_fwd_train_varlen kept in ``workspace``."""
+    wp, wb = _ws(workspace)
+    _check("kda_chunk_bwd_saved_varlen", lib().kda_chunk_bwd_saved_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta_logits), _ptr(a_log), _ptr(dt_bias),
         float(scale), float(lower_bound), _ptr(cu_seqlens), N, total_T, _ptr(initial_state),
         _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),

@@ -229,6 +229,29 @@ int kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const floa
                          void* workspace, size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_train_varlen / kda_chunk_bwd_saved_varlen -- the training pair below
+ *   (kda_chunk_fwd_train, kda_chunk_bwd_saved) for packed sequences: the arguments of
+ *   kda_chunk_fwd_varlen_ws and of kda_chunk_bwd_varlen, the workspace of
+ *   kda_chunk_bwd_varlen_workspace_size(N, total_T, H, 128, 128, KDA_BF16).
+ */
+int kda_chunk_fwd_train_varlen(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta_logits, const float* a_log,
+                               const float* dt_bias, float scale, float lower_bound,
+                               const int32_t* cu_seqlens, int N, int total_T,
+                               const float* initial_state, void* out, float* final_state, int H,
+                               int dk, int dv, int chunk, int dtype, void* workspace,
+                               size_t workspace_bytes, kda_stream_t stream);
+int kda_chunk_bwd_saved_varlen(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta_logits, const float* a_log,
+                               const float* dt_bias, float scale, float lower_bound,
+                               const int32_t* cu_seqlens, int N, int total_T,
+                               const float* initial_state, const void* d_out,
+                               const float* d_final_state, void* dq, void* dk, void* dv,
+                               float* dg, float* dbeta_logits, float* da_log, float* ddt_bias,
+                               float* d_initial_state, int H, int dim_k, int dim_v, int dtype,
+                               void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_train -- the forward of kda_chunk_fwd_ws (same inputs, outputs, layouts and
  *   error codes) for training: besides out and final_state it leaves in `workspace` the
  *   chunk records and per-chunk states that kda_chunk_bwd_saved reads, so that the backward

@@ -362,3 +362,17 @@ def _bwd_varlen(L, **over):
 ])
 def test_varlen_backward_rejects_bad_arguments(L, over, code):
     assert _bwd_varlen(L, **over) == code
+
+
+def test_varlen_training_forward_rejects_other_configurations(L):
+    def call(**over):
+        a = dict(dtype=1, dk=128, chunk=64, ws=0x100000, nbytes=1 << 40)
+        a.update(over)
+        return L.kda_chunk_fwd_train_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, -1.0,
+                                            FAKE, 2, 100, None, FAKE, None, 2, a["dk"], 128,
+                                            a["chunk"], a["dtype"], a["ws"], a["nbytes"], None)
+    assert call(dtype=0) == -7
+    assert call(dk=64) == -3
+    assert call(chunk=16) == -4
+    assert call(ws=None) == -12
+    assert call(nbytes=64) == -12

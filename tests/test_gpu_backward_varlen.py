@@ -121,3 +121,57 @@ def test_varlen_backward_equals_fixed_length_backward():
             assert rel_err(gpu[n], fixed) <= 1e-5, n
         else:
             assert np.array_equal(gpu[n].reshape(fixed.shape), fixed), n
+
+
+def test_varlen_training_pair():
+    """kda_chunk_fwd_train_varlen matches kda_chunk_fwd_varlen_ws (last-bit bf16 differences:
+    the query scale rides in the operands) and leaves records from which
+    kda_chunk_bwd_saved_varlen reproduces kda_chunk_bwd_varlen exactly."""
+    lengths, H, scale, lb = [200, 64, 3, 0, 77], 2, 128 ** -0.5, -3.0
+    N = len(lengths)
+    d, total = _packed(lengths, H, 21)
+    io = torch.bfloat16
+    q, k, v = (to_dev(d[n], io) for n in ("q", "k", "v"))
+    g, bl, al, db = (to_dev(d[n]) for n in ("g", "beta_logits", "a_log", "dt_bias"))
+    cu = torch.from_numpy(d["cu_seqlens"].astype(np.int32)).cuda()
+    s0 = to_dev(d["initial_state"])
+    out = torch.full((total, H, 128), float("nan"), device="cuda", dtype=io)
+    s1 = torch.full((N, H, 128, 128), float("nan"), device="cuda")
+    w = workspace(kda.kda_chunk_bwd_varlen_workspace_size(N, total, H, 128, 128))
+    kda.kda_chunk_fwd_train_varlen(q, k, v, g, bl, al, db, scale, lb, cu, N, total, s0, out, s1,
+                                   H, 128, 128, workspace=w)
+    ref_out = torch.full_like(out, float("nan"))
+    ref_s1 = torch.full_like(s1, float("nan"))
+    w0 = workspace(kda.kda_chunk_fwd_varlen_workspace_size(N, total, H, 128, 128))
+    kda.kda_chunk_fwd_varlen_ws(q, k, v, g, bl, al, db, scale, lb, cu, N, total, s0, ref_out,
+                                ref_s1, H, 128, 128, workspace=w0)
+    torch.cuda.synchronize()
+    assert rel_err(out.float().cpu().numpy(), ref_out.float().cpu().numpy()) <= 1e-2
+    assert rel_err(s1.cpu().numpy(), ref_s1.cpu().numpy()) <= 1e-5
+
+    dout = to_dev(d["d_out"], io)
+    dfin = to_dev(d["d_final_state"])
+
+    def grads():
+        return [torch.full((total, H, 128), float("nan"), device="cuda", dtype=io),
+                torch.full((total, H, 128), float("nan"), device="cuda", dtype=io),
+                torch.full((total, H, 128), float("nan"), device="cuda", dtype=io),
+                torch.full((total, H, 128), float("nan"), device="cuda"),
+                torch.full((total, H), float("nan"), device="cuda"),
+                torch.full((H,), float("nan"), device="cuda"),
+                torch.full((128, H), float("nan"), device="cuda"),
+                torch.full((N, H, 128, 128), float("nan"), device="cuda")]
+    saved, fresh = grads(), grads()
+    kda.kda_chunk_bwd_saved_varlen(q, k, v, g, bl, al, db, scale, lb, cu, N, total, s0, dout,
+                                   dfin, *saved, H, 128, 128, workspace=w)
+    w2 = workspace(kda.kda_chunk_bwd_varlen_workspace_size(N, total, H, 128, 128))
+    kda.kda_chunk_bwd_varlen(q, k, v, g, bl, al, db, scale, lb, cu, N, total, s0, dout, dfin,
+                             *fresh, H, 128, 128, workspace=w2)
+    torch.cuda.synchronize()
+    for i, (a_, b_) in enumerate(zip(saved, fresh)):
+        x, y = a_.float().cpu().numpy(), b_.float().cpu().numpy()
+        if i in (5, 6):  # da_log, ddt_bias: atomic sums
+            assert rel_err(x, y) <= 1e-5, i
+        else:
+            assert np.array_equal(x, y), i
+    assert kda.kda_device_error(1) == 0
