@@ -52,7 +52,8 @@ def parse_args():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the decode / varlen / e2e / cpu-baseline measurements")
-    p.add_argument("--profile", choices=["chunk", "chunk1", "decode", "varlen", "bwd", "bwd_full"],
+    p.add_argument("--profile", choices=["chunk", "chunk1", "decode", "varlen", "bwd", "bwd_full",
+                                         "gla"],
                    default=None,
                    help="run two launches of one kernel on a reduced case (for ncu) and exit")
     return p.parse_args()
@@ -629,6 +630,10 @@ def profile_case(which):
     if which == "decode":
         w = synth.DECODE_B64
         decode_measure(w, 2, False)
+    elif which == "gla":
+        # two kda_recurrent_attention_fwd calls on the benchmark's recurrent workload
+        w = synth.PREFILL_B4
+        recurrent_attention_measure(reps=1)
     elif which in ("bwd", "bwd_full"):
         # two kda_chunk_bwd calls: a quarter of the prefill workload's heads, or all of them
         w = replace(synth.PREFILL_B4, H=8) if which == "bwd" else synth.PREFILL_B4

@@ -8,9 +8,12 @@
 // oracle).  Query head h reads key / value head h / (Hq / Hkv); `reverse` walks each
 // sequence from its last token to its first.
 //
-// One CTA of 128 threads per (sequence, query head, 32-wide slice of the value axis): thread
-// (r, c) = (tid / 8, tid % 8) owns columns 4 c .. 4 c + 3 on rows r, r + 16, ...; the state
-// slice stays in registers, and every staged key-channel vector feeds four columns.  The
+// One CTA per (sequence, query head, 32-wide slice of the value axis): thread (r, c) =
+// (tid / 8, tid % 8) owns columns 4 c .. 4 c + 3 on the row pairs (2 p, 2 p + 1),
+// p = r, r + G, ... (G = threads / 8 row groups); the state slice stays in registers as pairs of adjacent key channels,
+// so that every update is a packed two-lane fp32 multiply or fma (Blackwell's f32x2) whose
+// key-channel operands (k, e^{a}, scale q) load as pairs and whose value-column operands
+// (v, e^{gv}) are broadcast once per token.  The
 // state update needs no other thread's data, and no token needs an earlier token's output,
 // so tokens go in blocks of kTB: the block's inputs are staged in shared memory (gate
 // exponentials applied), every thread advances its state through the whole block keeping one
@@ -22,8 +25,11 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 128;
 constexpr int kDVS = 32;
+// Threads per CTA: 8 column groups x 16 row groups (256 threads measured slower: the
+// per-block staging and output reduction grow while the work per thread halves).
+template <int D>
+__host__ __device__ constexpr int gla_threads() { return 128; }
 constexpr int kTB = 8;  // tokens per staged block (4 CTAs per SM fit with the double buffer)
 
 // 16-byte asynchronous global -> shared copy (cp.async, cache-global), and its group fences.
@@ -50,17 +56,41 @@ struct RawBlock {
   float gv[kTB][kDVS];
 };
 
+// Packed two-lane fp32 arithmetic (sm_100 family): a 64-bit register holds (lo, hi).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
-  constexpr int RPT = D / 16;          // rows per thread
+__global__ void __launch_bounds__(gla_threads<D>()) gla_kernel(GlaArgs a) {
+  constexpr int kThreads = gla_threads<D>();
+  constexpr int NRG = kThreads / 8;    // row groups
+  constexpr int NW = kThreads / 32;    // warps
+  constexpr int PPT = D / (2 * NRG);   // row pairs per thread
   extern __shared__ __align__(16) uint8_t dyn[];
   RawBlock<Tin, D>* raw = reinterpret_cast<RawBlock<Tin, D>*>(dyn);  // [2], double-buffered
-  __shared__ float4 s_kaq[kTB][D];     // (k, e^{a}, scale q, -) per token and key channel
+  // per token and key channel: k, e^{a}, scale q
+  __shared__ __align__(16) float s_k[kTB][D], s_ea[kTB][D], s_q[kTB][D];
   __shared__ __align__(16) float2 s_vb[kTB][kDVS];   // (v, e^{gv}) per token and column
-  __shared__ __align__(16) float s_o[kTB][4][kDVS];  // per-warp partial outputs
+  __shared__ __align__(16) float s_o[kTB][NW][kDVS];  // per-warp partial outputs
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int r16 = tid >> 3, c4 = tid & 7;
+  const int rg = tid >> 3, c4 = tid & 7;
   const int j0 = blockIdx.x * kDVS, h = blockIdx.y, seq = blockIdx.z;
   const int Hq = a.Hq, Hkv = a.Hkv, hk = h / (Hq / Hkv);
   long long bos;
@@ -83,14 +113,16 @@ __global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
   const long long st_off = ((long long)seq * Hq + h) * D * D;
   const float gamma = a.g_gamma ? a.g_gamma[bidx * Hq + h] : 0.f;
 
-  float S[RPT][4];
+  // S2[i][jj] = (S[2 p][j], S[2 p + 1][j]) with p = rg + NRG i, j = j0 + 4 c4 + jj
+  uint64_t S2[PPT][4];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i)
+  for (int i = 0; i < PPT; ++i)
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-      S[i][jj] = a.initial_state
-                     ? a.initial_state[st_off + (r16 + 16 * i) * D + j0 + 4 * c4 + jj]
-                     : 0.f;
+    for (int jj = 0; jj < 4; ++jj) {
+      const long long e0 = st_off + (long long)(2 * (rg + NRG * i)) * D + j0 + 4 * c4 + jj;
+      S2[i][jj] = a.initial_state ? f2pack(a.initial_state[e0], a.initial_state[e0 + D])
+                                  : f2pack(0.f, 0.f);
+    }
 
   // token slot u of a block starting at position p0 is position p0 + u (forward) or
   // p0 - u (reverse)
@@ -155,28 +187,42 @@ __global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
       float x = gamma;
       if (has_a) x += r.a[u][c];
       if (has_b) x += r.gk2[u][c];
-      s_kaq[u][c] = make_float4(load_as_float(&r.k[u][c]), expf(x),
-                                a.scale * load_as_float(&r.q[u][c]), 0.f);
+      s_k[u][c] = load_as_float(&r.k[u][c]);
+      s_ea[u][c] = __expf(x);
+      s_q[u][c] = a.scale * load_as_float(&r.q[u][c]);
     }
     for (int e = tid; e < nb * kDVS; e += kThreads) {
       const int u = e / kDVS, jj = e % kDVS;
-      s_vb[u][jj] = make_float2(load_as_float(&r.v[u][jj]), a.gv ? expf(r.gv[u][jj]) : 1.f);
+      s_vb[u][jj] = make_float2(load_as_float(&r.v[u][jj]), a.gv ? __expf(r.gv[u][jj]) : 1.f);
     }
     __syncthreads();
     for (int u = 0; u < nb; ++u) {
       const float4 vb01 = *reinterpret_cast<const float4*>(&s_vb[u][4 * c4]);
       const float4 vb23 = *reinterpret_cast<const float4*>(&s_vb[u][4 * c4 + 2]);
-      const float vv[4] = {vb01.x, vb01.z, vb23.x, vb23.z};
-      const float bb[4] = {vb01.y, vb01.w, vb23.y, vb23.w};
-      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t vv2[4] = {f2pack(vb01.x, vb01.x), f2pack(vb01.z, vb01.z),
+                               f2pack(vb23.x, vb23.x), f2pack(vb23.z, vb23.z)};
+      const uint64_t bb2[4] = {f2pack(vb01.y, vb01.y), f2pack(vb01.w, vb01.w),
+                               f2pack(vb23.y, vb23.y), f2pack(vb23.w, vb23.w)};
+      uint64_t o2[4] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        const float4 kaq = s_kaq[u][r16 + 16 * i];
+      for (int i = 0; i < PPT; ++i) {
+        const int c = 2 * (rg + NRG * i);
+        const uint64_t k2 = *reinterpret_cast<const uint64_t*>(&s_k[u][c]);
+        const uint64_t ea2 = *reinterpret_cast<const uint64_t*>(&s_ea[u][c]);
+        const uint64_t q2 = *reinterpret_cast<const uint64_t*>(&s_q[u][c]);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          S[i][jj] = kaq.y * bb[jj] * S[i][jj] + kaq.x * vv[jj];
-          o[jj] += S[i][jj] * kaq.z;
+          // S = (e^{a} e^{gv}) S + k v, then the output partial q . S over the two rows
+          S2[i][jj] = f2fma(f2mul(ea2, bb2[jj]), S2[i][jj], f2mul(k2, vv2[jj]));
+          o2[jj] = f2fma(S2[i][jj], q2, o2[jj]);
         }
+      }
+      float o[4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        float lo, hi;
+        f2unpack(o2[jj], lo, hi);
+        o[jj] = lo + hi;
       }
       // the warp's four row groups (lanes c4, c4 + 8, c4 + 16, c4 + 24) share columns
 #pragma unroll
@@ -190,17 +236,24 @@ __global__ void __launch_bounds__(kThreads) gla_kernel(GlaArgs a) {
     __syncthreads();
     for (int e = tid; e < nb * kDVS; e += kThreads) {
       const int u = e / kDVS, jj = e % kDVS;
-      const float tot = s_o[u][0][jj] + s_o[u][1][jj] + s_o[u][2][jj] + s_o[u][3][jj];
+      float tot = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < NW; ++ww) tot += s_o[u][ww][jj];
       store_from_float(out + ((bos + p0 + dir * u) * Hq + h) * D + j0 + jj, tot);
     }
     __syncthreads();  // the staged block, the partials and raw[bi & 1] are rewritten next
   }
   if (a.final_state) {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
+    for (int i = 0; i < PPT; ++i)
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-        a.final_state[st_off + (r16 + 16 * i) * D + j0 + 4 * c4 + jj] = S[i][jj];
+      for (int jj = 0; jj < 4; ++jj) {
+        const long long e0 = st_off + (long long)(2 * (rg + NRG * i)) * D + j0 + 4 * c4 + jj;
+        float lo, hi;
+        f2unpack(S2[i][jj], lo, hi);
+        a.final_state[e0] = lo;
+        a.final_state[e0 + D] = hi;
+      }
   }
 }
 
@@ -211,7 +264,7 @@ cudaError_t launch_t(const GlaArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(gla_kernel<Tin, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
-  gla_kernel<Tin, D><<<grid, kThreads, dyn, st>>>(a);
+  gla_kernel<Tin, D><<<grid, gla_threads<D>(), dyn, st>>>(a);
   return cudaGetLastError();
 }
 
