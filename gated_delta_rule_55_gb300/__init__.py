@@ -7,7 +7,8 @@ from .kda import (KDA_BF16, KDA_F32, KDAError, kda_attention_fwd, kda_chunk_bwd,
                   kda_chunk_fwd_varlen,
                   kda_chunk_fwd_varlen_workspace_size, kda_chunk_fwd_varlen_ws,
                   kda_chunk_fwd_workspace_size, kda_chunk_fwd_ws, kda_decode_step,
-                  kda_device_error, kda_recurrent_attention_fwd, kda_status_string,
+                  kda_device_error, kda_recurrent_attention_fwd, kda_selftest_bounded_wait,
+                  kda_status_string,
                   kda_version, lib)
 
 __all__ = ["KDA_BF16", "KDA_F32", "KDAError", "kda_attention_fwd", "kda_chunk_bwd",
@@ -18,5 +19,5 @@ __all__ = ["KDA_BF16", "KDA_F32", "KDAError", "kda_attention_fwd", "kda_chunk_bw
            "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_size",
            "kda_chunk_fwd_varlen_workspace_size", "kda_chunk_fwd_ws", "kda_chunk_fwd_varlen_ws",
            "kda_chunk_fwd_noalloc", "kda_recurrent_attention_fwd", "kda_decode_step",
-           "kda_device_error", "kda_status_string",
+           "kda_device_error", "kda_selftest_bounded_wait", "kda_status_string",
            "kda_version", "lib"]

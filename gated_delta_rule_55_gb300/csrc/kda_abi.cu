@@ -590,7 +590,18 @@ int kda_device_error(int reset) {
   int s = check_device();
   if (s != KDA_OK) return s;
   return (int)(kda::chunk_tc_read_error(reset != 0) | kda::chunk_split_read_error(reset != 0) |
-               kda::chunk_bwd_read_error(reset != 0) | kda::decode_read_error(reset != 0));
+               kda::chunk_bwd_read_error(reset != 0) | kda::decode_read_error(reset != 0) |
+               kda::selftest_read_error(reset != 0));
+}
+
+int kda_selftest_bounded_wait(unsigned long long limit_ns, kda_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return KDA_ERR_BAD_SHAPE;
+  const int s = check_device();
+  if (s != KDA_OK) return s;
+  return kda::launch_wait_selftest(limit_ns, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_LAUNCH;
 }
 
 }  // extern "C"

@@ -101,6 +101,9 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
                              bool saved, cudaStream_t stream);
 unsigned int chunk_bwd_read_error(bool reset);
 cudaError_t launch_gla(const GlaArgs& a, bool bf16, cudaStream_t stream);
+// One bounded wait on a barrier nothing arrives on (the give-up path of every kernel wait).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
+unsigned int selftest_read_error(bool reset);
 // Sequential (token by token) scan: any supported shape, dtype and variant.
 cudaError_t launch_recurrent(const ChunkArgs& a, bool bf16, cudaStream_t stream);
 // Tensor-core chunk kernel: bf16 q/k/v, dk = dv = 128, 64-token chunks, default variant.

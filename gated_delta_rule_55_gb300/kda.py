@@ -30,7 +30,7 @@ EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_siz
            "kda_chunk_fwd_train_varlen", "kda_chunk_bwd_saved_varlen",
            "kda_chunk_fwd_train", "kda_chunk_bwd_saved", "kda_recurrent_attention_fwd", "kda_attention_fwd", "kda_decode_step",
            "kda_status_string",
-           "kda_version", "kda_device_error")
+           "kda_version", "kda_device_error", "kda_selftest_bounded_wait")
 KDA_ATTN_NO_QK_L2NORM = 1
 KDA_ATTN_RECURRENT = 2
 KDA_ATTN_ORDER_LITERAL = 4
@@ -88,6 +88,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
                                   _I, _I, _I, _I, _P]
     L.kda_device_error.argtypes = [_I]
+    L.kda_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, _P]
+    L.kda_selftest_bounded_wait.restype = _I
     for f in ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_ws",
               "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_chunk_bwd",
               "kda_chunk_bwd_saved", "kda_chunk_fwd_train", "kda_chunk_bwd_varlen",
@@ -149,6 +151,12 @@ def kda_device_error(reset: bool = True) -> int:
     if r < 0:
         raise KDAError("kda_device_error", r)
     return r
+
+
+def kda_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launch one bounded wait that runs out (sets bit 3 of kda_device_error)."""
+    _check("kda_selftest_bounded_wait", lib().kda_selftest_bounded_wait(int(limit_ns),
+                                                                         _stream(stream)))
 
 
 def kda_chunk_fwd(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound,

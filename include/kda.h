@@ -378,10 +378,20 @@ int kda_version(void);
  *   the last reset (no paper counterpart: it reports the kernels' own safeguards).
  *   Bit 0: a bounded wait inside the single-pass tensor-core chunk kernel gave up; bit 1:
  *   one inside the two-launch (workspace) chunk kernels did; bit 2: one inside the
- *   chunked backward's kernels did (the outputs of that launch are incomplete).  Synchronises the device.  reset != 0 clears the mask.
+ *   chunked backward's kernels did (the outputs of that launch are incomplete); bit 3: the
+ *   wait of kda_selftest_bounded_wait gave up (which is what it is for).  Synchronises the device.  reset != 0 clears the mask.
  *   Returns the mask (>= 0) or KDA_ERR_DEVICE.
  */
 int kda_device_error(int reset);
+
+/*
+ * kda_selftest_bounded_wait -- launches one kernel whose single wait, on an mbarrier that
+ *   nothing arrives on, runs out after limit_ns nanoseconds (1 .. 1e9) and records bit 3 of
+ *   kda_device_error: the give-up path every tensor-core kernel takes instead of hanging
+ *   the device.  No paper counterpart.  Returns KDA_OK once enqueued; limit_ns outside
+ *   (0, 1e9] gives KDA_ERR_BAD_SHAPE.
+ */
+int kda_selftest_bounded_wait(unsigned long long limit_ns, kda_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -376,3 +376,9 @@ def test_varlen_training_forward_rejects_other_configurations(L):
     assert call(chunk=16) == -4
     assert call(ws=None) == -12
     assert call(nbytes=64) == -12
+
+
+@pytest.mark.parametrize("limit", [0, 1_000_000_001, 2**63])
+def test_selftest_rejects_unbounded_limits(L, limit):
+    """The self-test's wait limit must lie in (0, 1 s]: no argument can make it wait longer."""
+    assert L.kda_selftest_bounded_wait(limit, None) == -2
