@@ -1,6 +1,6 @@
 // Chunked backward of the KDA forward on the tensor cores (bf16 q/k/v/d_out, dk = dv = 128,
-// 64-token chunks, fixed-length sequences, decay-first recurrence with the kda_tkg gate and
-// beta logits).  The pages give no backward ("Algorithm modes: chunked" is named as the
+// 64-token chunks, fixed-length or packed sequences, decay-first recurrence with the kda_tkg
+// gate and beta logits).  The pages give no backward ("Algorithm modes: chunked" is named as the
 // training path); this is reverse-mode differentiation of the chunk form of the forward,
 //
 //   U = T (V - K~ S),   O = Q~ S + M U,   S' = diag(e^{G_C}) S + Kd^T U,
@@ -24,6 +24,9 @@
 //   bwd_chunk_kernel: one CTA per (chunk, head), all at once: every other product above,
 //       then the gate, L2-norm and sigmoid chain rules, writing dq, dk, dv, dg, dbeta_logits
 //       and adding into da_log and ddt_bias.
+//
+// The training forward (launch_chunk_fwd_train) runs the first two launches with the output
+// written as well; a backward on its workspace then starts at bwd_scan_kernel.
 //
 // Operands are the row-major 128-byte-swizzled tiles that TMA moves; a tile [lines][64] is
 // read K-major when the contraction runs along its rows' elements and MN-major when it runs

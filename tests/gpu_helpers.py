@@ -46,6 +46,34 @@ def rel_err(gpu, ref):
     return max_abs(gpu, ref) / max(den, 1e-30)
 
 
+def param_grad_scales(dg_ref, g, dt_bias):
+    """Summed magnitudes of the terms of the two parameter gradients (from the oracle's dg):
+    da_log[h] = sum over tokens and channels of dg * (g + dt_bias), ddt_bias[c, h] = sum over
+    tokens of dg.  Both are sums with heavy cancellation, so their error is judged against
+    these magnitudes (the standard bound for a sum of terms with a relative error each)."""
+    dg_ref = np.asarray(dg_ref, np.float64)
+    H = dg_ref.shape[-2]
+    x = np.asarray(g, np.float64) + np.asarray(dt_bias, np.float64).T.reshape(
+        (1,) * (dg_ref.ndim - 2) + (H, -1))
+    lead = tuple(range(dg_ref.ndim - 2))
+    da = np.abs(dg_ref * x).sum(axis=lead + (dg_ref.ndim - 1,))       # [H]
+    ddt = np.abs(dg_ref).sum(axis=lead).T                              # [dk, H]
+    return {"da_log": da, "ddt_bias": ddt}
+
+
+def sum_err(gpu, ref, scale):
+    """max |gpu - ref| / max(scale): the error of a sum against its terms' magnitudes."""
+    return max_abs(gpu, ref) / max(float(np.max(np.abs(scale))), 1e-30)
+
+
+def bwd_err(name, gpu, ref, scales):
+    """The bf16 error measure of one backward output: max-norm relative, except for the two
+    parameter gradients (sum_err against param_grad_scales)."""
+    if name in scales:
+        return sum_err(gpu, ref, scales[name])
+    return rel_err(gpu, ref)
+
+
 def workspace(nbytes):
     """A device workspace of ``nbytes`` (256-byte aligned, as cudaMalloc returns), or None."""
     if nbytes == 0:

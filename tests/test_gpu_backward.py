@@ -10,7 +10,8 @@ import torch
 
 import gated_delta_rule_55_gb300 as kda
 from gated_delta_rule_55_gb300 import synth
-from gpu_helpers import BF16_REL, bf16_round, ensure_built, max_abs, rel_err, to_dev, workspace
+from gpu_helpers import (BF16_REL, bf16_round, bwd_err, ensure_built, max_abs, param_grad_scales,
+                         rel_err, to_dev, workspace)
 from oracle import kda_backward
 
 pytestmark = pytest.mark.gpu
@@ -60,10 +61,12 @@ def _oracle(d, cot, scale, lb, bf16):
                         o.get("initial_state"))
 
 
-def _check(gpu, ref, bf16, names=GRADS):
+def _check(gpu, ref, bf16, names=GRADS, d=None):
+    scales = param_grad_scales(ref["dg"], d["g"], d["dt_bias"]) if bf16 else {}
     for n in names:
         if bf16:
-            assert rel_err(gpu[n], ref[n]) <= BF16_REL, (n, rel_err(gpu[n], ref[n]))
+            e = bwd_err(n, gpu[n], ref[n], scales)
+            assert e <= BF16_REL, (n, e)
         else:
             tol = 1e-4 * max(1.0, float(np.max(np.abs(ref[n]))))
             assert max_abs(gpu[n], ref[n]) <= tol, (n, max_abs(gpu[n], ref[n]), tol)
@@ -84,7 +87,7 @@ def test_gradients_dk128(T, bf16):
     B, H, dk, dv = 2, 2, 128, 128
     d, cot = _case(B, T, H, dk, dv, T)
     gpu = _run(d, cot, B, T, H, dk, dv, 0.1, -2.0, bf16)
-    _check(gpu, _oracle(d, cot, 0.1, -2.0, bf16), bf16)
+    _check(gpu, _oracle(d, cot, 0.1, -2.0, bf16), bf16, d=d)
 
 
 @pytest.mark.parametrize("dk,dv", [(64, 32), (32, 64), (128, 32)])
@@ -116,7 +119,7 @@ def test_strong_decay_and_no_final_cotangent():
 def test_chunked_bf16_gradients(B, T, H, lb, state, final):
     d, cot = _case(B, T, H, 128, 128, 40 + T + H, state=state, final=final)
     gpu = _run(d, cot, B, T, H, 128, 128, 128 ** -0.5, lb, True)
-    _check(gpu, _oracle(d, cot, 128 ** -0.5, lb, True), True)
+    _check(gpu, _oracle(d, cot, 128 ** -0.5, lb, True), True, d=d)
     assert kda.kda_device_error(1) == 0
 
 
@@ -124,7 +127,7 @@ def test_chunked_bf16_gradients_without_initial_state_output():
     B, T, H = 2, 100, 2
     d, cot = _case(B, T, H, 128, 128, 77)
     gpu = _run(d, cot, B, T, H, 128, 128, 0.1, -2.0, True, want_state=False)
-    _check(gpu, _oracle(d, cot, 0.1, -2.0, True), True, names=GRADS[:-1])
+    _check(gpu, _oracle(d, cot, 0.1, -2.0, True), True, names=GRADS[:-1], d=d)
 
 
 def test_chunked_bf16_prefill_workload_sampled_head():
