@@ -178,3 +178,56 @@ def test_varlen_training_pair():
         else:
             assert np.array_equal(x, y), i
     assert kda.kda_device_error(1) == 0
+
+
+def test_varlen_backward_many_sequences():
+    """Forty packed sequences of random lengths 0..150: the per-chunk kernel's binary search
+    over the chunk offsets and the reverse scan's per-sequence chunk ranges."""
+    H, scale, lb = 2, 128 ** -0.5, -2.0
+    lengths = list(np.random.default_rng(41).integers(0, 150, size=40))
+    d, total = _packed(lengths, H, 41)
+    gpu = _run(d, total, len(lengths), H, scale, lb)
+    ref = _oracle(d, lengths, H, scale, lb)
+    scales = param_grad_scales(ref["dg"], d["g"], d["dt_bias"])
+    for n in ref:
+        e = bwd_err(n, gpu[n], ref[n], scales)
+        assert e <= BF16_REL, (n, e)
+    assert kda.kda_device_error(1) == 0
+
+
+def test_varlen_backward_all_sequences_empty():
+    """No tokens at all: the state cotangent passes straight through (d_initial_state =
+    d_final_state) and the parameter gradients are zero.  The per-token tensors are empty,
+    so small placeholder buffers stand in for their (never read) pointers."""
+    N, H = 3, 2
+    r = np.random.default_rng(5)
+    s0 = to_dev(r.normal(size=(N, H, 128, 128)) * 0.02)
+    dfin_h = r.normal(size=(N, H, 128, 128)).astype(np.float32)
+    dfin = to_dev(dfin_h)
+    cu = torch.zeros(N + 1, dtype=torch.int32, device="cuda")
+    xb = torch.zeros(H * 128, device="cuda", dtype=torch.bfloat16)
+    xf = torch.zeros(H * 128, device="cuda")
+    al, db = to_dev(r.uniform(-1, 1, H)), to_dev(r.normal(size=(128, H)) * 0.1)
+    da = torch.full((H,), float("nan"), device="cuda")
+    ddt = torch.full((128, H), float("nan"), device="cuda")
+    dinit = torch.full((N, H, 128, 128), float("nan"), device="cuda")
+    w = workspace(kda.kda_chunk_bwd_varlen_workspace_size(N, 0, H, 128, 128))
+    kda.kda_chunk_bwd_varlen(xb, xb, xb, xf, xf, al, db, 128 ** -0.5, -2.0, cu, N, 0, s0, xb,
+                             dfin, xb, xb, xb, xf, xf, da, ddt, dinit, H, 128, 128, workspace=w)
+    torch.cuda.synchronize()
+    assert np.array_equal(dinit.cpu().numpy(), dfin_h)
+    assert not torch.any(da).item() and not torch.any(ddt).item()
+    assert kda.kda_device_error(1) == 0
+
+
+def test_backward_without_sequences():
+    """B = 0: nothing to differentiate; the parameter gradients are zeroed."""
+    H = 2
+    da = torch.full((H,), float("nan"), device="cuda")
+    ddt = torch.full((128, H), float("nan"), device="cuda")
+    x = torch.empty(16, device="cuda", dtype=torch.bfloat16)
+    f = torch.empty(16, device="cuda")
+    kda.kda_chunk_bwd(x, x, x, f, f, f, f, 0.1, -1.0, None, x, None, x, x, x, f, f, da, ddt, None,
+                      0, 64, H, 128, 128, dtype=kda.KDA_BF16, workspace=None)
+    torch.cuda.synchronize()
+    assert not torch.any(da).item() and not torch.any(ddt).item()
