@@ -646,7 +646,7 @@ def profile_case(which):
         for _ in range(2):
             call_chunk(w, x, single_pass=(which == "chunk1"))
     torch.cuda.synchronize()
-    print(f"profile case {which}: {w.name} done", flush=True)
+    print(f"profile case {which}: {w.name} (B={w.B}, H={w.H}) done", flush=True)
 
 
 # ---------------------------------------------------------------------- reference arm

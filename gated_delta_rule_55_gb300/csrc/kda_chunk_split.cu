@@ -104,12 +104,43 @@ __global__ void __launch_bounds__(kPThreads, 2)
   const int c0 = 2 * cp;
   const int H = a.H;
 
-  // record -> (head, chunk slot) -> (sequence, chunk of the sequence); false past the
-  // last chunk of packed inputs (the record count is an upper bound there)
-  auto locate = [&](long long r, int& h_, long long& tok0_, int& n_) -> bool {
-    if (r >= ws.recs) return false;
-    h_ = (int)(r % H);
-    const long long slot = r / H;
+  // The CTA walks the records r = blockIdx.x, blockIdx.x + gridDim.x, ... with
+  // r = slot * H + h.  Its (slot, h) pair, and for fixed-length inputs the (sequence, chunk)
+  // pair of the slot, is stepped from record to record rather than divided out each time.
+  const int step_h = (int)(gridDim.x % (unsigned)H);
+  const long long step_slot = gridDim.x / (unsigned)H;
+  long long cur_rec = blockIdx.x, cur_slot = blockIdx.x / (unsigned)H;
+  int cur_h = (int)(blockIdx.x % (unsigned)H);
+  int cur_seq = 0, cur_jc = 0;
+  if (!a.cu_seqlens) {
+    cur_seq = (int)(cur_slot / ws.nck_fixed);
+    cur_jc = (int)(cur_slot % ws.nck_fixed);
+  }
+  auto advance = [&]() {
+    cur_rec += gridDim.x;
+    cur_h += step_h;
+    long long carry = step_slot;
+    if (cur_h >= H) {
+      cur_h -= H;
+      ++carry;
+    }
+    cur_slot += carry;
+    if (!a.cu_seqlens) {
+      long long jc = cur_jc + carry;
+      while (jc >= ws.nck_fixed) {
+        jc -= ws.nck_fixed;
+        ++cur_seq;
+      }
+      cur_jc = (int)jc;
+    }
+  };
+  // the current record -> (head, chunk slot) -> (sequence, chunk of the sequence); false
+  // past the last record, and past the last chunk of packed inputs (the record count is an
+  // upper bound there)
+  auto locate = [&](int& h_, long long& tok0_, int& n_) -> bool {
+    if (cur_rec >= ws.recs) return false;
+    h_ = cur_h;
+    const long long slot = cur_slot;
     int seq, jc;
     if (a.cu_seqlens) {
       const int N = a.B;
@@ -122,8 +153,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
       seq = lo;
       jc = (int)(slot - ws.coff[lo]);
     } else {
-      seq = (int)(slot / ws.nck_fixed);
-      jc = (int)(slot % ws.nck_fixed);
+      seq = cur_seq;
+      jc = cur_jc;
     }
     long long bos;
     int len;
@@ -184,7 +215,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
 
   int h, n, h_next = 0, n_next = 0;
   long long tok0, tok0_next = 0;
-  bool have = locate(blockIdx.x, h, tok0, n);
+  bool have = locate(h, tok0, n);
   if (have && tid == 0) stage_expect();
   __syncthreads();
   if (have) stage_issue(h, tok0);
@@ -202,7 +233,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
   const uint32_t tile_base = c_kb * 8192u + uint32_t(R) * 2048u;
   float blog = (have && tid < n) ? a.beta_logits[(tok0 + tid) * H + h] : 0.f;  // tid < 64
   for (long long rec = blockIdx.x; have; rec += gridDim.x) {
-    const bool have_next = locate(rec + gridDim.x, h_next, tok0_next, n_next);
+    advance();
+    const bool have_next = locate(h_next, tok0_next, n_next);
 
     // ---- loads: this record's staged tiles; raw gates, v / k / q words of (16 tokens,
     //      channels c0, c0 + 1)
@@ -253,17 +285,19 @@ __global__ void __launch_bounds__(kPThreads, 2)
 
 
     // ---- gate prefix over this thread's sub-chunk, beta
-    const float exp_a = __expf(a.a_log[h]);
-    const float db0 = a.dt_bias[c0 * H + h], db1 = a.dt_bias[(c0 + 1) * H + h];
-    float loc0[16], loc1[16];  // G_t - P_R for channels c0, c0 + 1
+    // the gate in log2 units: gamma log2 e = lb2 / (1 + 2^(na2 (g + dt_bias)))
+    const float na2 = -__expf(a.a_log[h]) * kLog2E;
+    const float cb0 = na2 * a.dt_bias[c0 * H + h], cb1 = na2 * a.dt_bias[(c0 + 1) * H + h];
+    const float lb2 = a.lower_bound * kLog2E;
+    float loc0[16], loc1[16];  // (G_t - P_R) log2 e for channels c0, c0 + 1
     {
       float r0 = 0.f, r1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         float g0 = 0.f, g1 = 0.f;
         if (16 * R + i < n) {
-          g0 = a.lower_bound * fast_rcp(1.f + fast_exp(-exp_a * (graw[i].x + db0)));
-          g1 = a.lower_bound * fast_rcp(1.f + fast_exp(-exp_a * (graw[i].y + db1)));
+          g0 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(na2, graw[i].x, cb0)));
+          g1 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(na2, graw[i].y, cb1)));
         }
         r0 += g0;
         r1 += g1;
@@ -320,15 +354,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
 #pragma unroll
       for (int r = 1; r < 4; ++r)
         if (R == r) { Pm0 = P0[r]; Pm1 = P1[r]; }
-      const float eP0 = fast_exp(Pm0), eP1 = fast_exp(Pm1);                // e^{P_R}
-      const float eCP0 = fast_exp(Gc0 - Pm0), eCP1 = fast_exp(Gc1 - Pm1);  // e^{G_C - P_R}
+      const float eP0 = fast_exp2(Pm0), eP1 = fast_exp2(Pm1);                // e^{P_R}
+      const float eCP0 = fast_exp2(Gc0 - Pm0), eCP1 = fast_exp2(Gc1 - Pm1);  // e^{G_C - P_R}
       float cR0[4], cR1[4];  // e^{P_R' - P_R} for later sub-chunks R'
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        cR0[r] = (r > R) ? fast_exp(P0[r] - Pm0) : 0.f;
-        cR1[r] = (r > R) ? fast_exp(P1[r] - Pm1) : 0.f;
+        cR0[r] = (r > R) ? fast_exp2(P0[r] - Pm0) : 0.f;
+        cR1[r] = (r > R) ? fast_exp2(P1[r] - Pm1) : 0.f;
       }
-      if (R == 0) *reinterpret_cast<float2*>(&s_dec[c0]) = make_float2(fast_exp(Gc0), fast_exp(Gc1));
+      if (R == 0) *reinterpret_cast<float2*>(&s_dec[c0]) = make_float2(fast_exp2(Gc0), fast_exp2(Gc1));
 
       const uint32_t eP2 = pack_bf16(eP0, eP1), eCP2 = pack_bf16(eCP0, eCP1);
       const uint32_t c12 = pack_bf16(cR0[1], cR1[1]), c22 = pack_bf16(cR0[2], cR1[2]),
@@ -347,7 +381,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
           const int i = 8 * hf + ii;
           const uint32_t swi = uint32_t(hf * 1024 + ii * 128) +
                                (((c_chunk ^ uint32_t(ii)) << 4) | c_byte);
-          const float e0 = fast_exp(loc0[i]), e1 = fast_exp(loc1[i]);  // e^{G_t - P_R}
+          const float e0 = fast_exp2(loc0[i]), e1 = fast_exp2(loc1[i]);  // e^{G_t - P_R}
           const uint32_t e2 = pack_bf16(e0, e1);
           const uint32_t i2 = pack_bf16(fast_rcp(e0), fast_rcp(e1));  // e^{P_R - G_t}
           const uint32_t xk = hmul2(kw[i], e2), xq = hmul2(qw[i], e2), kd = hmul2(kw[i], i2);
