@@ -20,8 +20,10 @@ constexpr long long kRecVec = 256 * 4;          // e^{G_C}[128], rk[64], rq[64]
 constexpr long long kRecState = 128LL * 128 * 2;  // a bf16 [128 x 128] state image
 
 struct Ws {
-  __nv_bfloat16* qw;   // [2 * recs * 64][128]: Q~ records, then -W records
-  __nv_bfloat16* ku;   // [2 * recs * 128][64]: K^^T records, then U~^T records
+  __nv_bfloat16* qw;   // [recs * 64][128]: Q~ records
+  // [3 * recs * 128][64]: K^^T records ([128][64] each), then U~^T records (16-byte pieces
+  // stored piece-major, [8][128][8]), then -W^T records ([128][64])
+  __nv_bfloat16* ku;
   __nv_bfloat16* m;    // [recs * 64][64]
   float* vec;          // [recs][256]
   int32_t* coff;       // [N + 1] first chunk slot of each sequence (packed inputs only)
@@ -56,9 +58,9 @@ inline uint8_t* carve_records(const ChunkArgs& a, void* base, Ws& ws) {
   ws.recs = recs;
   ws.nck_fixed = a.cu_seqlens ? 0 : (a.T + kC - 1) / kC;
   ws.qw = reinterpret_cast<__nv_bfloat16*>(p);
-  p += 2 * recs * kRecTile;
+  p += recs * kRecTile;
   ws.ku = reinterpret_cast<__nv_bfloat16*>(p);
-  p += 2 * recs * kRecTile;
+  p += 3 * recs * kRecTile;
   ws.m = reinterpret_cast<__nv_bfloat16*>(p);
   p += recs * kRecM;
   ws.vec = reinterpret_cast<float*>(p);

@@ -129,7 +129,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 constexpr int kBSThreads = 512;
 // one stage = one chunk: the forward records it needs and the chunk's d_out tile
 constexpr int B_Q = 0;          // Q~ = q^ e^{G} [64 tok][128] (two boxes)
-constexpr int B_W = 16384;      // -W [64 tok][128]
+constexpr int B_W = 16384;      // -W^T [128][64 tok]
 constexpr int B_KT = 32768;     // K^^T = (k e^{G_C - G})^T [128][64 tok]
 constexpr int B_M = 49152;      // rq_r M_raw[r][s] [64][64]
 constexpr int B_DO = 57344;     // d_out [64 tok][128] (two boxes)
@@ -212,12 +212,11 @@ __global__ void __launch_bounds__(kBSThreads, 1)
     uint8_t* b = sm + st * kBStage;
     uint64_t* bar = &bar_ld[st];
     mbar_arrive_expect_tx(bar, kBStageTx);
-    const int rq = (int)(rec * 64), rw = (int)((bw.f.recs + rec) * 64);
+    const int rq = (int)(rec * 64), rw = (int)((2 * bw.f.recs + rec) * 128);
     const int tok0 = (int)(bos + (long long)ch * kC);
     tma_load_2d(b + B_Q, &map_qw, bar, 0, rq);
     tma_load_2d(b + B_Q + 8192, &map_qw, bar, 64, rq);
-    tma_load_2d(b + B_W, &map_qw, bar, 0, rw);
-    tma_load_2d(b + B_W + 8192, &map_qw, bar, 64, rw);
+    tma_load_2d(b + B_W, &map_ku, bar, 0, rw);
     tma_load_2d(b + B_KT, &map_ku, bar, 0, (int)(rec * 128));
     tma_load_2d(b + B_M, &map_m, bar, 0, (int)(rec * 64));
     tma_load_3d(b + B_DO, &map_do, bar, 0, h, tok0);
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(kBSThreads, 1)
   const uint32_t idesc_du_ts = make_idesc(1, 128, 64, false, true);
   const uint32_t idesc_du_ss = make_idesc(1, 128, 64, true, true);
   const uint32_t idesc_s_ss = make_idesc(1, 128, 128, true, true);
-  const uint32_t idesc_s_ts = make_idesc(1, 128, 128, false, true);
+  const uint32_t idesc_s_ts = make_idesc(1, 128, 128, false, false);
   uint32_t mma_phase = 0;
   uint32_t wait_calls = 0;
   auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -343,7 +342,7 @@ __global__ void __launch_bounds__(kBSThreads, 1)
         mma_ss(tm + BT_S, mn_desc(dos, 8192, s), mn_desc(qs, 8192, s), idesc_s_ss, 1);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma_ts(tm + BT_S, tm + BT_UA + 8 * s, mn_desc(wsm, 8192, s), idesc_s_ts, 1);
+        mma_ts(tm + BT_S, tm + BT_UA + 8 * s, sw128_kdesc<2>(wsm, 128, s), idesc_s_ts, 1);
       mma_commit(&bar_mma);
     }
     if (!(ok = mma_wait())) break;
@@ -959,7 +958,7 @@ size_t chunk_bwd_workspace(const ChunkArgs& a) {
 bool chunk_bwd_supported(const ChunkArgs& a, bool bf16) {
   return bf16 && a.dk == 128 && a.dv == 128 && a.chunk == 64 && !a.gate_head && !a.beta_prob &&
          !a.no_l2norm && !a.literal && (a.cu_seqlens || a.T > 0) &&
-         slots_for(a) * a.H * 256 < 0x7fffffffLL;
+         slots_for(a) * a.H * 384 < 0x7fffffffLL;
 }
 
 namespace {
@@ -1028,8 +1027,8 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
   const long long tok_rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
   const long long rows = tok_rows > 0 ? tok_rows : 1;
   CUtensorMap mqw, mku, mm, mdo, mdut, mn, mut, ms0, mds, mq, mk, mg;
-  if (!make_map_2d(&mqw, bw.f.qw, 2 * recs * 64, 128, 64) ||
-      !make_map_2d(&mku, bw.f.ku, 2 * recs * 128, 64, 128) ||
+  if (!make_map_2d(&mqw, bw.f.qw, recs * 64, 128, 64) ||
+      !make_map_2d(&mku, bw.f.ku, 3 * recs * 128, 64, 128) ||
       !make_map_2d(&mm, bw.f.m, recs * 64, 64, 64) || !make_map_in(&mdo, d_out, rows, a.H, false) ||
       !make_map_2d(&mdut, bw.dut, recs * 128, 64, 128) ||
       !make_map_2d(&mn, bw.f.nrec, recs * 64, 64, 64) ||

@@ -11,9 +11,9 @@
 //                      diag(beta) and the transform W = T diag(rk) K~, U~ = T V (tcgen05).
 //                      It writes one workspace record per (chunk, head):
 //                        Q~   = q e^{G}                     [64 tok][128]  bf16
-//                        -W                                 [64 tok][128]  bf16
 //                        K^^T = (k e^{G_C - G})^T           [128][64 tok]  bf16
-//                        U~^T                               [128][64 tok]  bf16
+//                        U~^T  16-byte pieces, piece-major  [8][128][8 tok] bf16
+//                        -W^T                               [128][64 tok]  bf16
 //                        M_raw (gate-scaled q k^T, s <= r)  [64][64]       bf16
 //                        e^{G_C} [128], rk [64], rq [64]                    fp32
 //  chunk_scan_kernel   one CTA per (sequence, head) walks its chunks in order, records
@@ -42,26 +42,26 @@ constexpr int kPKbRows = 160;  // 64 diagonal + 16 + 32 + 48 off-diagonal key ro
 constexpr int P_XL = 0;                 // Xl [128 x 128] bf16 (k rows, then q rows)
 constexpr int P_KB = P_XL + 32768;      // Kb [160 x 128]
 constexpr int P_KTT = P_KB + 40960;     // K~^T [128 x 64]
-constexpr int P_VT = P_KTT + 16384;     // V^T [128 x 64]
-constexpr int P_END = P_VT + 16384;
+constexpr int P_V = P_KTT + 16384;      // v [64 tok x 128] as staged (MMA2's MN-major A)
+constexpr int P_END = P_V + 16384;
 // re-used inside Xl/Kb once MMA1 has completed
 constexpr int P_L = 0;                  // fp32 [64][LDL] beta-scaled strict lower A
 constexpr int P_X = P_L + 64 * LDL * 4; // fp32 [64][LDL] (I + L)^{-1}
 constexpr int P_Y = P_X + 64 * LDL * 4; // fp32 [4][16][LDY] per-warp scratch
 constexpr int P_T = 40960;              // T [64 x 64] bf16 SW128
 constexpr int P_TW = P_T + 8192;        // T diag(rk)
-constexpr int P_W = P_TW + 8192;        // -W [64 x 128] staging for the record store
+constexpr int P_W = P_TW + 8192;        // -W^T [128 x 64] staging for the record store
+constexpr int P_MS = P_T;               // M record [64 x 64] staging (readback to T write)
 static_assert(P_Y + 4 * 16 * LDY * 4 <= P_T, "solve scratch overlaps T");
 static_assert(P_W + 16384 <= P_KTT, "re-used tiles must stay inside Xl/Kb");
 // Staging of the NEXT record's raw inputs (TMA), in tiles that are free from the end of
-// MMA2 until the next record's operand build: v and g inside the solve area, q and k in
-// the K~^T / V^T tiles.  None overlaps the -W staging tile of the record phase.
-constexpr int ST_V = 0;                 // v [64 tok x 128] bf16, two SW128 boxes
+// MMA2 until the next record's operand build: k and g inside the solve area, q in the K~^T
+// tile, v in its own tile, where MMA2 reads it as staged.
+constexpr int ST_K = 0;                 // k [64 tok x 128] bf16, two SW128 boxes
 constexpr int ST_G = 16384;             // g [4 quarters][64 tok][32] fp32, no swizzle
 constexpr int ST_Q = P_KTT;             // q, two SW128 boxes
-constexpr int ST_K = P_VT;              // k
+constexpr int ST_V = P_V;               // v
 constexpr uint32_t kStageBytes = 3 * 16384 + 32768;
-static_assert(ST_G + 32768 <= P_W, "staging overlaps the -W tile");
 constexpr size_t kPSmem = P_END + 1024;
 
 // Tensor Memory of the prep kernel (256 columns: two CTAs per SM).
@@ -75,7 +75,8 @@ __device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split pa
 // kBwd: also the backward's records (rq folded into Q~ and M, and N)
 template <bool kBwd>
 __global__ void __launch_bounds__(kPThreads, 2)
-    chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qw,
+    chunk_prep_kernel(const __grid_constant__ CUtensorMap map_ku,
+                      const __grid_constant__ CUtensorMap map_m,
                       const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v,
@@ -247,12 +248,11 @@ __global__ void __launch_bounds__(kPThreads, 2)
       ld_parity ^= 1u;
     }
     float2 graw[16];
-    uint32_t vw[16], kw[16], qw[16];
+    uint32_t kw[16], qw[16];
     const uint8_t* gsrc = sm + ST_G + (c0 >> 5) * 8192 + (16 * R) * 128 + (c0 & 31) * 4;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       graw[i] = *reinterpret_cast<const float2*>(gsrc + i * 128);
-      vw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_V + tile_base + swz(i));
       kw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_K + tile_base + swz(i));
       qw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_Q + tile_base + swz(i));
     }
@@ -261,16 +261,21 @@ __global__ void __launch_bounds__(kPThreads, 2)
       for (int i = 0; i < 16; ++i)
         if (16 * R + i >= n) {
           graw[i] = make_float2(0.f, 0.f);
-          vw[i] = kw[i] = qw[i] = 0u;
+          kw[i] = qw[i] = 0u;
         }
+      // the v tile's rows past n are zeroed where MMA2 reads them (whole 128-byte rows, so
+      // the swizzle does not matter)
+      for (int u = tid; u < 1024; u += kPThreads) {
+        const int row = (u >> 3) & 63;
+        if (row >= n)
+          *reinterpret_cast<uint4*>(sm + ST_V + (u >> 9) * 8192 + row * 128 + (u & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
     }
-    // every staged word is in registers before the V^T tile (which shares space with the
-    // staged k) is written
-    __syncthreads();
 
-    // V^T tile (rows = channels, tokens contiguous): row c0 takes the low halves, row c0 + 1
-    // the high halves; lanes 4..7 of every 8-lane group write row c0 + 1 first so that one
-    // 128-bit wavefront covers 8 swizzle phases.
+    // transposed [128 x 64] tile rows c0, c0 + 1 (tokens contiguous): row c0 takes the low
+    // halves, row c0 + 1 the high halves; lanes 4..7 of every 8-lane group write row c0 + 1
+    // first so that one 128-bit wavefront covers 8 swizzle phases.
     const int tsw = (lane & 4) ? 1 : 0;
     auto store_t8 = [&](int off, const uint32_t* w8, int g8) {
       const uint4 lo = make_uint4(__byte_perm(w8[0], w8[1], 0x5410), __byte_perm(w8[2], w8[3], 0x5410),
@@ -280,8 +285,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
       *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + tsw, g8)) = tsw ? hi : lo;
       *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + 1 - tsw, g8)) = tsw ? lo : hi;
     };
-    store_t8(P_VT, vw, 2 * R);
-    store_t8(P_VT, vw + 8, 2 * R + 1);
 
 
     // ---- gate prefix over this thread's sub-chunk, beta
@@ -332,12 +335,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
                      ((lane >> 1) & 1);
       if ((lane & 1) == 0) s_qq[warp & 1][16 * R + tq] = v[0];
     }
-    // the previous record's -W store has read its staging tile (inside Kb) before Kb is
+    // the previous record's -W^T store has read its staging tile (inside Kb) before Kb is
     // rewritten below
     if (tid == 0) bulk_wait_read_all();
     __syncthreads();
 
     // ---- gate-scaled operands of (channels c0, c0 + 1) x (tokens 16 R .. 16 R + 15)
+    // K^^T words (rows c0, c0 + 1, tokens 16 R + 8 hf .. + 7): staged once MMA1 is done
+    uint4 khv[4];
     {
       float P0[4], P1[4];  // P_R: G just before sub-chunk R
       P0[0] = 0.f;
@@ -372,7 +377,6 @@ __global__ void __launch_bounds__(kPThreads, 2)
       uint8_t* const p128 = sm + P_XL + c_kb * 16384u + uint32_t(R) * 2048u;
       uint8_t* const p160 = sm + P_KB + c_kb * 20480u + uint32_t(R) * 2048u;
       __nv_bfloat16* const qrec = ws.qw + (rec * 64 + 16 * R) * kD + c0;  // Q~ row 16 R
-      __nv_bfloat16* const krec = ws.ku + rec * 128 * 64;                  // K^^T record
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t khw[8], ktw[8];
@@ -409,8 +413,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
                                     __byte_perm(khw[4], khw[5], 0x5410), __byte_perm(khw[6], khw[7], 0x5410));
         const uint4 hi = make_uint4(__byte_perm(khw[0], khw[1], 0x7632), __byte_perm(khw[2], khw[3], 0x7632),
                                     __byte_perm(khw[4], khw[5], 0x7632), __byte_perm(khw[6], khw[7], 0x7632));
-        *reinterpret_cast<uint4*>(krec + c0 * 64 + 16 * R + 8 * hf) = lo;
-        *reinterpret_cast<uint4*>(krec + (c0 + 1) * 64 + 16 * R + 8 * hf) = hi;
+        khv[2 * hf] = lo;
+        khv[2 * hf + 1] = hi;
       }
     }
     fence_async_smem();
@@ -430,6 +434,23 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
+    // K^^T record into the swizzled [128 x 64] staging tile (inside Kb, free once MMA1 is
+    // done); stored by TMA after the next block barrier
+    // (lanes 4..7 of every 8-lane group take row c0 + 1 first: one wavefront covers all
+    // eight swizzle phases)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint32_t piece = uint32_t(2 * R + hf);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int e = k ^ ((lane >> 2) & 1);
+        const int c = c0 + e;
+        *reinterpret_cast<uint4*>(sm + P_W + (c >> 3) * 1024 + (c & 7) * 128 +
+                                  ((piece ^ uint32_t(c & 7)) << 4)) =
+            e ? khv[2 * hf + 1] : khv[2 * hf];
+      }
+    }
+    fence_async_smem();
 
     // ---- norms: |k_r|^2 = A_raw[r][r] (diagonal of D1); |q_r|^2 from the reduction
     if (warp < 2) {
@@ -445,6 +466,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
       s_rq[r] = (r < n) ? a.scale * rsqrtf(s_qq[0][r] + s_qq[1][r] + kL2Eps) : 0.f;
     }
     __syncthreads();
+    if (tid == 0) {
+      tma_store_2d(&map_ku, sm + P_W, 0, (int)(rec * 128));
+      bulk_commit();
+    }
     // vector record: e^{G_C}, rk, rq
     ws.vec[rec * 256 + tid] = tid < 128 ? s_dec[tid] : tid < 192 ? s_rk[tid - 128] : s_rq[tid - 192];
 
@@ -495,12 +520,21 @@ __global__ void __launch_bounds__(kPThreads, 2)
           pk[p] = pack_bf16((s0 <= r) ? mf * v[2 * p] : 0.f,
                             (s0 + 1 <= r) ? mf * v[2 * p + 1] : 0.f);
         }
-        uint4* mrec = reinterpret_cast<uint4*>(ws.m + (rec * 64 + r) * 64 + 16 * q);
-        mrec[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        mrec[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        // row r, 16-byte chunks 2 q and 2 q + 1 of the swizzled [64 x 64] staging tile
+        uint8_t* const mrow = sm + P_MS + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t sw = uint32_t(r & 7);
+        *reinterpret_cast<uint4*>(mrow + ((uint32_t(2 * q) ^ sw) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(mrow + ((uint32_t(2 * q + 1) ^ sw) << 4)) =
+            make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
     }
+    fence_async_smem();
     __syncthreads();
+    if (tid == 0) {
+      tma_store_2d(&map_m, sm + P_MS, 0, (int)(rec * 64));
+      bulk_commit();
+    }
 
     // ---- T = (I + L)^{-1} diag(beta), blocked by 16
     {
@@ -531,6 +565,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       solve_level<2>(L, X, reinterpret_cast<float*>(sm + P_Y), warp, lane);
       __syncthreads();
       solve_level<3>(L, X, reinterpret_cast<float*>(sm + P_Y), warp, lane);
+      if (tid == 0) bulk_wait_read_all();  // the M store has read its staging tile (T's)
       __syncthreads();
       // T[r][s] = X[r][s] beta_s and T diag(rk) (s <= r): row r, 8 columns per thread
 #pragma unroll
@@ -575,15 +610,20 @@ __global__ void __launch_bounds__(kPThreads, 2)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ts = smem_u32(sm + P_T), tw = smem_u32(sm + P_TW),
-                     ks = smem_u32(sm + P_KTT), vs = smem_u32(sm + P_VT);
+                     ks = smem_u32(sm + P_KTT), vs = smem_u32(sm + P_V);
       const uint32_t idesc = make_idesc(1, 128, 64);
+      // V^T as the A operand is v as staged ([64 tok][128] in two 64-channel boxes), read
+      // MN-major: 16 tokens (2 KB) per K step, the channel boxes 8 KB apart
+      const uint32_t idesc_amn = make_idesc(1, 128, 64, true, false);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         mma_ss(tm + P_TM_DW, sw128_kdesc<2>(ks, 128, s), sw128_kdesc<2>(tw, 64, s), idesc, s > 0);
-        mma_ss(tm + P_TM_DU, sw128_kdesc<2>(vs, 128, s), sw128_kdesc<2>(ts, 64, s), idesc, s > 0);
+        mma_ss(tm + P_TM_DU, make_sdesc(vs + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
+               sw128_kdesc<2>(ts, 64, s), idesc_amn, s > 0);
       }
       mma_commit(&bar_mma);
       if (have_next) stage_expect();  // the next record's staging completes on bar_ld
+      bulk_wait_read_all();  // the K^^T store has read the staging tile the -W^T rows reuse
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
@@ -594,26 +634,29 @@ __global__ void __launch_bounds__(kPThreads, 2)
       ld_pending = true;
     }
 
-    // ---- records: -W (through a swizzled staging tile and one bulk-tensor store) and U~^T
-    //      (thread j = ln writes its own row); thread (ln, wg) holds tokens 32 wg .. + 31
+    // ---- records: thread (j = ln, wg) holds row j of W^T and U~^T for tokens 32 wg .. + 31.
+    //      -W^T goes through a swizzled staging tile and one bulk-tensor store; U~^T (read
+    //      only by the scan's threads) is stored piece-major, coalesced as it stands.
     {
       float w32[32];
       tmem_ld32(tl + P_TM_DW + 32 * wg, w32);
-      const uint32_t wkb = uint32_t(ln >> 6) * 8192u, wch = uint32_t(((ln & 63) * 2) >> 4),
-                     wby = uint32_t(((ln & 63) * 2) & 15);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = 32 * wg + i;
-        const uint32_t off = wkb + uint32_t((r >> 3) * 1024 + (i & 7) * 128) +
-                             (((wch ^ uint32_t(i & 7)) << 4) | wby);
-        *reinterpret_cast<__nv_bfloat16*>(sm + P_W + off) = __float2bfloat16_rn(-w32[i]);
-      }
-      float u32[32];
-      tmem_ld32(tl + P_TM_DU + 32 * wg, u32);
-      uint4* urec = reinterpret_cast<uint4*>(ws.ku + ((ws.recs + rec) * 128 + ln) * 64 + 32 * wg);
+      // row ln of the swizzled [128 x 64] staging tile: 16-byte pieces 4 wg .. 4 wg + 3
+      uint8_t* const wrow = sm + P_W + (ln >> 3) * 1024 + (ln & 7) * 128;
 #pragma unroll
       for (int p = 0; p < 4; ++p)
-        urec[p] = make_uint4(pack_bf16(u32[8 * p + 0], u32[8 * p + 1]),
+        *reinterpret_cast<uint4*>(wrow + (((4 * wg + p) ^ (ln & 7)) << 4)) =
+            make_uint4(pack_bf16(-w32[8 * p + 0], -w32[8 * p + 1]),
+                       pack_bf16(-w32[8 * p + 2], -w32[8 * p + 3]),
+                       pack_bf16(-w32[8 * p + 4], -w32[8 * p + 5]),
+                       pack_bf16(-w32[8 * p + 6], -w32[8 * p + 7]));
+      float u32[32];
+      tmem_ld32(tl + P_TM_DU + 32 * wg, u32);
+      // piece P = 4 wg + p of row ln (tokens 8 P .. 8 P + 7) at piece-major position
+      // P * 128 + ln: a warp's store covers 512 contiguous bytes
+      uint4* urec = reinterpret_cast<uint4*>(ws.ku + (ws.recs + rec) * 8192);
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        urec[(4 * wg + p) * 128 + ln] = make_uint4(pack_bf16(u32[8 * p + 0], u32[8 * p + 1]),
                              pack_bf16(u32[8 * p + 2], u32[8 * p + 3]),
                              pack_bf16(u32[8 * p + 4], u32[8 * p + 5]),
                              pack_bf16(u32[8 * p + 6], u32[8 * p + 7]));
@@ -622,9 +665,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-      const int row = (int)((ws.recs + rec) * 64);
-      tma_store_2d(&map_qw, sm + P_W, 0, row);
-      tma_store_2d(&map_qw, sm + P_W + 8192, 64, row);
+      tma_store_2d(&map_ku, sm + P_W, 0, (int)((2 * ws.recs + rec) * 128));
       bulk_commit();
     }
     h = h_next;
@@ -653,9 +694,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
 constexpr int kSThreads = 512;
 // one stage = one chunk's record
 constexpr int S_Q = 0;          // Q~ [64 x 128] (two 64-channel boxes)
-constexpr int S_W = 16384;      // -W [64 x 128]
+constexpr int S_W = 16384;      // -W^T [128 x 64]
 constexpr int S_KT = 32768;     // K^^T [128 x 64]
-constexpr int S_UT = 49152;     // U~^T [128 x 64]
+constexpr int S_UT = 49152;     // U~^T, piece-major [8][128][8 tok]
 constexpr int S_M = 65536;      // M_raw [64 x 64]
 constexpr int S_V = 73728;      // e^{G_C}, rk, rq
 constexpr int kStage = 74752;
@@ -748,16 +789,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
     uint8_t* b = sm + st * kStage;
     uint64_t* bar = &bar_ld[st];
     mbar_arrive_expect_tx(bar, want_out ? kStageTx : kStageTxBwd);
-    const int rq = (int)(rec * 64), rw = (int)((ws.recs + rec) * 64);
+    const int rq = (int)(rec * 64), rw = (int)((2 * ws.recs + rec) * 128);
     if (want_out) {  // the backward's own forward pass computes no output
       tma_load_2d(b + S_Q, &map_qw, bar, 0, rq);
       tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, rq);
       tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64));
     }
-    tma_load_2d(b + S_W, &map_qw, bar, 0, rw);
-    tma_load_2d(b + S_W + 8192, &map_qw, bar, 64, rw);
+    tma_load_2d(b + S_W, &map_ku, bar, 0, rw);
     tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128));
-    tma_load_2d(b + S_UT, &map_ku, bar, 0, (int)((ws.recs + rec) * 128));
+    bulk_load(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar);
     bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar);
   };
   // chunk whose record is in flight into each stage (-1: none); same on every thread
@@ -791,6 +831,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __syncthreads();
 
   const uint32_t idesc_n64 = make_idesc(1, 128, 64);
+  const uint32_t idesc_n64_bmn = make_idesc(1, 128, 64, false, true);
   const uint32_t idesc_n128 = make_idesc(1, 128, 128);
   uint32_t mma_phase = 0;
   uint32_t wait_calls = 0;
@@ -824,13 +865,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (tid < 256) s_vec[tid] = reinterpret_cast<const float*>(b + S_V)[tid];
     __syncthreads();
 
-    // ---- MMA3: D_U = S^T (-W)^T, O'^T = S^T Q~^T  (M = 128, N = 64, K = 128)
+    // ---- MMA3: D_U = S^T (-W)^T, O'^T = S^T Q~^T  (M = 128, N = 64, K = 128; the -W^T
+    //      record is the B operand read MN-major, 16 channel rows per K step)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ws_ = smem_u32(b + S_W), qs = smem_u32(b + S_Q);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        mma_ts(tm + S_TM_DU, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(ws_, 64, s), idesc_n64, s > 0);
+        mma_ts(tm + S_TM_DU, tm + S_TM_SA + 8 * s,
+               make_sdesc(ws_ + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128), idesc_n64_bmn,
+               s > 0);
         if (want_out)
           mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
       }
@@ -850,9 +894,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     {
       float v16[16];
       tmem_ld16(tl + S_TM_DU + 16 * wg, v16);
-      const uint8_t* urow = b + S_UT + (ln >> 3) * 1024 + (ln & 7) * 128;
-      const uint4 ua = *reinterpret_cast<const uint4*>(urow + (((2 * wg) ^ (ln & 7)) << 4));
-      const uint4 ub = *reinterpret_cast<const uint4*>(urow + (((2 * wg + 1) ^ (ln & 7)) << 4));
+      const uint4 ua = *reinterpret_cast<const uint4*>(b + S_UT + ((2 * wg) * 128 + ln) * 16);
+      const uint4 ub = *reinterpret_cast<const uint4*>(b + S_UT + ((2 * wg + 1) * 128 + ln) * 16);
       const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
       uint32_t up[8];
 #pragma unroll
@@ -1043,8 +1086,8 @@ size_t chunk_split_workspace(const ChunkArgs& a) {
 }
 
 bool chunk_split_index_ok(const ChunkArgs& a) {
-  // TMA row coordinates of the records are 32-bit: 2 * recs * 128 < 2^31
-  return slots_for(a) * a.H * 256 < 0x7fffffffLL;
+  // TMA row coordinates of the records are 32-bit: 3 * recs * 128 < 2^31
+  return slots_for(a) * a.H * 384 < 0x7fffffffLL;
 }
 
 cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream_t st) {
@@ -1053,8 +1096,8 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
   const long long rec_rows = ws.recs > 0 ? ws.recs : 1;
   CUtensorMap mqw, mku, mm, mo, mq, mk, mv, mg, ms0, mut;
   // the backward's scan writes no output: its (unused) output map is laid over q
-  if (!make_map_2d(&mqw, ws.qw, 2 * rec_rows * 64, 128, 64) ||
-      !make_map_2d(&mku, ws.ku, 2 * rec_rows * 128, 64, 128) ||
+  if (!make_map_2d(&mqw, ws.qw, rec_rows * 64, 128, 64) ||
+      !make_map_2d(&mku, ws.ku, 3 * rec_rows * 128, 64, 128) ||
       !make_map_2d(&mm, ws.m, rec_rows * 64, 64, 64) ||
       !make_map_out(&mo, ws.bwd == 1 ? a.q : a.out, map_rows, a.H) ||
       !make_map_in(&mq, a.q, map_rows, a.H, false) ||
@@ -1082,7 +1125,7 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
     const long long grid = std::min<long long>(ws.recs, 2LL * sms);
-    prep<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mqw, mq, mk, mv, mg, a, ws);
+    prep<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mku, mm, mq, mk, mv, mg, a, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   scan<<<dim3(a.H, a.B), kSThreads, scan_smem, st>>>(mqw, mku, mm, mo, ms0, mut, a, ws);
