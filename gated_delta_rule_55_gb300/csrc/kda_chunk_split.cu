@@ -50,17 +50,20 @@ constexpr int P_X = P_L + 64 * LDL * 4; // fp32 [64][LDL] (I + L)^{-1}
 constexpr int P_Y = P_X + 64 * LDL * 4; // fp32 [4][16][LDY] per-warp scratch
 constexpr int P_T = 40960;              // T [64 x 64] bf16 SW128
 constexpr int P_TW = P_T + 8192;        // T diag(rk)
-constexpr int P_W = P_TW + 8192;        // -W^T [128 x 64] staging for the record store
+constexpr int P_KS = P_TW + 8192;       // K^^T [128 x 64] staging (after MMA1)
 constexpr int P_MS = P_T;               // M record [64 x 64] staging (readback to T write)
+constexpr int P_W = P_T;                // -W^T [128 x 64] staging (T and T diag(rk), after MMA2)
 static_assert(P_Y + 4 * 16 * LDY * 4 <= P_T, "solve scratch overlaps T");
-static_assert(P_W + 16384 <= P_KTT, "re-used tiles must stay inside Xl/Kb");
-// Staging of the NEXT record's raw inputs (TMA), in tiles that are free from the end of
-// MMA2 until the next record's operand build: k and g inside the solve area, q in the K~^T
-// tile, v in its own tile, where MMA2 reads it as staged.
-constexpr int ST_K = 0;                 // k [64 tok x 128] bf16, two SW128 boxes
-constexpr int ST_G = 16384;             // g [4 quarters][64 tok][32] fp32, no swizzle
+static_assert(P_KS + 16384 <= P_KTT, "re-used tiles must stay inside Xl/Kb");
+// Staging of the NEXT record's raw inputs (TMA), each tile issued as soon as its space is
+// free: k into the K^^T staging tile once the K^^T store has read it (after the A/M
+// readback), g into L and X once the T tiles are written, q into K~^T and v into its own
+// tile (where MMA2 reads it as staged) once MMA2 is done.  All land on one barrier phase.
+constexpr int ST_K = P_KS;              // k [64 tok x 128] bf16, two SW128 boxes
+constexpr int ST_G = 0;                 // g [4 quarters][64 tok][32] fp32, no swizzle
 constexpr int ST_Q = P_KTT;             // q, two SW128 boxes
 constexpr int ST_V = P_V;               // v
+static_assert(ST_G + 32768 <= P_T, "g staging must stay inside the solve area");
 constexpr uint32_t kStageBytes = 3 * 16384 + 32768;
 constexpr size_t kPSmem = P_END + 1024;
 
@@ -169,6 +172,28 @@ __global__ void __launch_bounds__(kPThreads, 2)
   // w + 8), so that no single thread spends the issue time; the barrier's expected bytes are
   // registered beforehand by thread 0 (stage_expect), with a block barrier in between.
   auto stage_expect = [&]() { mbar_arrive_expect_tx(&bar_ld, kStageBytes); };
+  // the next record's k (thread 0; its bytes join the barrier phase without arriving)
+  auto stage_k = [&](int h_, long long tok0_) {
+    mbar_expect_tx(&bar_ld, 16384);
+    tma_load_3d(sm + ST_K, &map_k, &bar_ld, 0, h_, (int)tok0_);
+    tma_load_3d(sm + ST_K + 8192, &map_k, &bar_ld, 64, h_, (int)tok0_);
+  };
+  // the next record's g (thread 0, also without arriving)
+  auto stage_g = [&](int h_, long long tok0_) {
+    mbar_expect_tx(&bar_ld, 32768);
+    for (int qtr = 0; qtr < 4; ++qtr)
+      tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, (int)tok0_);
+  };
+  // the next record's q and v halves (lane 0 of warps 0..3), after thread 0's arrival
+  // registered their bytes
+  auto stage_qv = [&](int h_, long long tok0_) {
+    if (lane != 0 || warp >= 4) return;
+    const int half = warp & 1;
+    if (warp < 2)
+      tma_load_3d(sm + ST_Q + half * 8192, &map_q, &bar_ld, 64 * half, h_, (int)tok0_);
+    else
+      tma_load_3d(sm + ST_V + half * 8192, &map_v, &bar_ld, 64 * half, h_, (int)tok0_);
+  };
   auto stage_issue = [&](int h_, long long tok0_) {
     if (lane != 0) return;
     const int r0 = (int)tok0_;
@@ -445,7 +470,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       for (int k = 0; k < 2; ++k) {
         const int e = k ^ ((lane >> 2) & 1);
         const int c = c0 + e;
-        *reinterpret_cast<uint4*>(sm + P_W + (c >> 3) * 1024 + (c & 7) * 128 +
+        *reinterpret_cast<uint4*>(sm + P_KS + (c >> 3) * 1024 + (c & 7) * 128 +
                                   ((piece ^ uint32_t(c & 7)) << 4)) =
             e ? khv[2 * hf + 1] : khv[2 * hf];
       }
@@ -467,7 +492,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     __syncthreads();
     if (tid == 0) {
-      tma_store_2d(&map_ku, sm + P_W, 0, (int)(rec * 128));
+      tma_store_2d(&map_ku, sm + P_KS, 0, (int)(rec * 128));
       bulk_commit();
     }
     // vector record: e^{G_C}, rk, rq
@@ -532,9 +557,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
+      if (have_next) {
+        bulk_wait_read_all();  // the K^^T store has read its staging tile: k goes there
+        stage_k(h_next, tok0_next);
+      }
       tma_store_2d(&map_m, sm + P_MS, 0, (int)(rec * 64));
       bulk_commit();
     }
+    if (have_next) ld_pending = true;
 
     // ---- T = (I + L)^{-1} diag(beta), blocked by 16
     {
@@ -622,17 +652,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
                sw128_kdesc<2>(ts, 64, s), idesc_amn, s > 0);
       }
       mma_commit(&bar_mma);
-      if (have_next) stage_expect();  // the next record's staging completes on bar_ld
-      bulk_wait_read_all();  // the K^^T store has read the staging tile the -W^T rows reuse
+      if (have_next) {
+        stage_g(h_next, tok0_next);                // L and X are free (T tiles written)
+        mbar_arrive_expect_tx(&bar_ld, 2 * 16384);  // q and v, issued once MMA2 is done
+      }
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
-    // every tile the staging area reuses is free now (MMA2 was their last reader); the
-    // expected bytes were registered when MMA2 was issued
-    if (have_next) {
-      stage_issue(h_next, tok0_next);
-      ld_pending = true;
-    }
+    // K~^T and the v tile are free now (MMA2 was their last reader)
+    if (have_next) stage_qv(h_next, tok0_next);
 
     // ---- records: thread (j = ln, wg) holds row j of W^T and U~^T for tokens 32 wg .. + 31.
     //      -W^T goes through a swizzled staging tile and one bulk-tensor store; U~^T (read
