@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
   __shared__ __align__(16) float s_dec[kD];
   __shared__ __align__(16) float s_gtot[4][kD];
   __shared__ __align__(16) float s_qq[2][kC];
-  __shared__ uint64_t bar_mma, bar_ld;
+  __shared__ uint64_t bar_mma, bar_ld, bar_qv;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
 
@@ -171,16 +171,20 @@ __global__ void __launch_bounds__(kPThreads, 2)
   // The ten box loads of a record are issued by lane 0 of the eight warps (loads w and
   // w + 8), so that no single thread spends the issue time; the barrier's expected bytes are
   // registered beforehand by thread 0 (stage_expect), with a block barrier in between.
-  auto stage_expect = [&]() { mbar_arrive_expect_tx(&bar_ld, kStageBytes); };
+  // the first record: k and g on bar_ld, q and v on bar_qv
+  auto stage_expect = [&]() {
+    mbar_arrive_expect_tx(&bar_ld, 16384 + 32768);
+    mbar_arrive_expect_tx(&bar_qv, 2 * 16384);
+  };
   // the next record's k (thread 0; its bytes join the barrier phase without arriving)
   auto stage_k = [&](int h_, long long tok0_) {
     mbar_expect_tx(&bar_ld, 16384);
     tma_load_3d(sm + ST_K, &map_k, &bar_ld, 0, h_, (int)tok0_);
     tma_load_3d(sm + ST_K + 8192, &map_k, &bar_ld, 64, h_, (int)tok0_);
   };
-  // the next record's g (thread 0, also without arriving)
+  // the next record's g (thread 0), with the arrival that closes bar_ld's batch
   auto stage_g = [&](int h_, long long tok0_) {
-    mbar_expect_tx(&bar_ld, 32768);
+    mbar_arrive_expect_tx(&bar_ld, 32768);
     for (int qtr = 0; qtr < 4; ++qtr)
       tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, (int)tok0_);
   };
@@ -190,9 +194,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
     if (lane != 0 || warp >= 4) return;
     const int half = warp & 1;
     if (warp < 2)
-      tma_load_3d(sm + ST_Q + half * 8192, &map_q, &bar_ld, 64 * half, h_, (int)tok0_);
+      tma_load_3d(sm + ST_Q + half * 8192, &map_q, &bar_qv, 64 * half, h_, (int)tok0_);
     else
-      tma_load_3d(sm + ST_V + half * 8192, &map_v, &bar_ld, 64 * half, h_, (int)tok0_);
+      tma_load_3d(sm + ST_V + half * 8192, &map_v, &bar_qv, 64 * half, h_, (int)tok0_);
   };
   auto stage_issue = [&](int h_, long long tok0_) {
     if (lane != 0) return;
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
         const int half = box & 1, which = box >> 1;  // q, k, v halves
         const CUtensorMap* m = which == 0 ? &map_q : which == 1 ? &map_k : &map_v;
         const int dst = (which == 0 ? ST_Q : which == 1 ? ST_K : ST_V) + half * 8192;
-        tma_load_3d(sm + dst, m, &bar_ld, 64 * half, h_, r0);
+        tma_load_3d(sm + dst, m, which == 1 ? &bar_ld : &bar_qv, 64 * half, h_, r0);
       } else {
         const int qtr = box - 6;  // g quarters
         tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, r0);
@@ -217,6 +221,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_ld, 1);
+    mbar_init(&bar_qv, 1);
     fence_mbar_init();
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_k);
@@ -246,7 +251,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
   __syncthreads();
   if (have) stage_issue(h, tok0);
   uint32_t ld_parity = 0;
-  bool ld_pending = have;  // a staging batch was issued and not yet waited for
+  bool ld_pending = have;  // a staging batch was issued and not yet waited for (k, g)
+  bool qv_pending = have;  // (q, v)
   // element (row 16 R + i, channel c0) of a [64 x 128] bf16 tile of two SW128 boxes:
   //   (c0 / 64) * 8192 + 2 R * 1024 + swz(i)
   const uint32_t c_kb = uint32_t(c0 >> 6);
@@ -262,15 +268,14 @@ __global__ void __launch_bounds__(kPThreads, 2)
     advance();
     const bool have_next = locate(h_next, tok0_next, n_next);
 
-    // ---- loads: this record's staged tiles; raw gates, v / k / q words of (16 tokens,
-    //      channels c0, c0 + 1)
+    // ---- loads: this record's staged k and g tiles; raw gates and k words of (16 tokens,
+    //      channels c0, c0 + 1).  q and v may still be in flight.
     {
       const uint32_t slot_w = wait_calls++ & 1;
       if (tid == 0) s_wait_ok[slot_w] = mbar_wait(&bar_ld, ld_parity) ? 1 : 0;
       __syncthreads();
       if (!s_wait_ok[slot_w]) { ok = false; break; }
       ld_pending = false;
-      ld_parity ^= 1u;
     }
     float2 graw[16];
     uint32_t kw[16], qw[16];
@@ -279,38 +284,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
     for (int i = 0; i < 16; ++i) {
       graw[i] = *reinterpret_cast<const float2*>(gsrc + i * 128);
       kw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_K + tile_base + swz(i));
-      qw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_Q + tile_base + swz(i));
     }
     if (n < kC) {  // partial chunk (uniform): rows past n belong to the next sequence
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (16 * R + i >= n) {
           graw[i] = make_float2(0.f, 0.f);
-          kw[i] = qw[i] = 0u;
+          kw[i] = 0u;
         }
-      // the v tile's rows past n are zeroed where MMA2 reads them (whole 128-byte rows, so
-      // the swizzle does not matter)
-      for (int u = tid; u < 1024; u += kPThreads) {
-        const int row = (u >> 3) & 63;
-        if (row >= n)
-          *reinterpret_cast<uint4*>(sm + ST_V + (u >> 9) * 8192 + row * 128 + (u & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-      }
     }
-
-    // transposed [128 x 64] tile rows c0, c0 + 1 (tokens contiguous): row c0 takes the low
-    // halves, row c0 + 1 the high halves; lanes 4..7 of every 8-lane group write row c0 + 1
-    // first so that one 128-bit wavefront covers 8 swizzle phases.
-    const int tsw = (lane & 4) ? 1 : 0;
-    auto store_t8 = [&](int off, const uint32_t* w8, int g8) {
-      const uint4 lo = make_uint4(__byte_perm(w8[0], w8[1], 0x5410), __byte_perm(w8[2], w8[3], 0x5410),
-                                  __byte_perm(w8[4], w8[5], 0x5410), __byte_perm(w8[6], w8[7], 0x5410));
-      const uint4 hi = make_uint4(__byte_perm(w8[0], w8[1], 0x7632), __byte_perm(w8[2], w8[3], 0x7632),
-                                  __byte_perm(w8[4], w8[5], 0x7632), __byte_perm(w8[6], w8[7], 0x7632));
-      *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + tsw, g8)) = tsw ? hi : lo;
-      *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + 1 - tsw, g8)) = tsw ? lo : hi;
-    };
-
 
     // ---- gate prefix over this thread's sub-chunk, beta
     // the gate in log2 units: gamma log2 e = lb2 / (1 + 2^(na2 (g + dt_bias)))
@@ -335,6 +317,45 @@ __global__ void __launch_bounds__(kPThreads, 2)
       *reinterpret_cast<float2*>(&s_gtot[R][c0]) = make_float2(r0, r1);
     }
     if (tid < kC) s_beta[tid] = (tid < n) ? sigmoidf_(blog) : 0.f;
+
+    // transposed [128 x 64] tile rows c0, c0 + 1 (tokens contiguous): row c0 takes the low
+    // halves, row c0 + 1 the high halves; lanes 4..7 of every 8-lane group write row c0 + 1
+    // first so that one 128-bit wavefront covers 8 swizzle phases.
+    const int tsw = (lane & 4) ? 1 : 0;
+    auto store_t8 = [&](int off, const uint32_t* w8, int g8) {
+      const uint4 lo = make_uint4(__byte_perm(w8[0], w8[1], 0x5410), __byte_perm(w8[2], w8[3], 0x5410),
+                                  __byte_perm(w8[4], w8[5], 0x5410), __byte_perm(w8[6], w8[7], 0x5410));
+      const uint4 hi = make_uint4(__byte_perm(w8[0], w8[1], 0x7632), __byte_perm(w8[2], w8[3], 0x7632),
+                                  __byte_perm(w8[4], w8[5], 0x7632), __byte_perm(w8[6], w8[7], 0x7632));
+      *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + tsw, g8)) = tsw ? hi : lo;
+      *reinterpret_cast<uint4*>(sm + off + trow_off(c0 + 1 - tsw, g8)) = tsw ? lo : hi;
+    };
+
+    // ---- the staged q and v tiles; q words
+    {
+      const uint32_t slot_w = wait_calls++ & 1;
+      if (tid == 0) s_wait_ok[slot_w] = mbar_wait(&bar_qv, ld_parity) ? 1 : 0;
+      __syncthreads();
+      if (!s_wait_ok[slot_w]) { ok = false; break; }
+      qv_pending = false;
+      ld_parity ^= 1u;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      qw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_Q + tile_base + swz(i));
+    if (n < kC) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (16 * R + i >= n) qw[i] = 0u;
+      // the v tile's rows past n are zeroed where MMA2 reads them (whole 128-byte rows, so
+      // the swizzle does not matter)
+      for (int u = tid; u < 1024; u += kPThreads) {
+        const int row = (u >> 3) & 63;
+        if (row >= n)
+          *reinterpret_cast<uint4*>(sm + ST_V + (u >> 9) * 8192 + row * 128 + (u & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
 
     // ---- |q_t|^2: this thread's two channels, then a reduce-scatter over the warp's 32
     //      channel pairs (lanes l and l ^ 1 end with the same token); two warps per token.
@@ -654,13 +675,16 @@ __global__ void __launch_bounds__(kPThreads, 2)
       mma_commit(&bar_mma);
       if (have_next) {
         stage_g(h_next, tok0_next);                // L and X are free (T tiles written)
-        mbar_arrive_expect_tx(&bar_ld, 2 * 16384);  // q and v, issued once MMA2 is done
+        mbar_arrive_expect_tx(&bar_qv, 2 * 16384);  // q and v, issued once MMA2 is done
       }
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
     // K~^T and the v tile are free now (MMA2 was their last reader)
-    if (have_next) stage_qv(h_next, tok0_next);
+    if (have_next) {
+      stage_qv(h_next, tok0_next);
+      qv_pending = true;
+    }
 
     // ---- records: thread (j = ln, wg) holds row j of W^T and U~^T for tokens 32 wg .. + 31.
     //      -W^T goes through a swizzled staging tile and one bulk-tensor store; U~^T (read
@@ -707,6 +731,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     if (tid == 0) {
       atomicOr(&g_split_error, 2u);
       if (ld_pending) mbar_wait(&bar_ld, ld_parity, 1000000000ull);  // staging in flight
+      if (qv_pending) mbar_wait(&bar_qv, ld_parity, 1000000000ull);
     }
     mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
   }
