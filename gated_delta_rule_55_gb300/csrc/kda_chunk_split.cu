@@ -107,6 +107,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
   const int cp = tid & 63, R = tid >> 6;
   const int c0 = 2 * cp;
   const int H = a.H;
+  // lane 0 of the last warp issues the bulk stores of the records (and waits for their
+  // reads) and the early staging of the next record: that warp is idle during the solve,
+  // which warp 0 leads
+  const bool tma_thread = tid == kPThreads - 32;
 
   // The CTA walks the records r = blockIdx.x, blockIdx.x + gridDim.x, ... with
   // r = slot * H + h.  Its (slot, h) pair, and for fixed-length inputs the (sequence, chunk)
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     // the previous record's -W^T store has read its staging tile (inside Kb) before Kb is
     // rewritten below
-    if (tid == 0) bulk_wait_read_all();
+    if (tma_thread) bulk_wait_read_all();
     __syncthreads();
 
     // ---- gate-scaled operands of (channels c0, c0 + 1) x (tokens 16 R .. 16 R + 15)
@@ -512,7 +516,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       s_rq[r] = (r < n) ? a.scale * rsqrtf(s_qq[0][r] + s_qq[1][r] + kL2Eps) : 0.f;
     }
     __syncthreads();
-    if (tid == 0) {
+    if (tma_thread) {
       tma_store_2d(&map_ku, sm + P_KS, 0, (int)(rec * 128));
       bulk_commit();
     }
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     fence_async_smem();
     __syncthreads();
-    if (tid == 0) {
+    if (tma_thread) {
       if (have_next) {
         bulk_wait_read_all();  // the K^^T store has read its staging tile: k goes there
         stage_k(h_next, tok0_next);
@@ -616,7 +620,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
       solve_level<2>(L, X, reinterpret_cast<float*>(sm + P_Y), warp, lane);
       __syncthreads();
       solve_level<3>(L, X, reinterpret_cast<float*>(sm + P_Y), warp, lane);
-      if (tid == 0) bulk_wait_read_all();  // the M store has read its staging tile (T's)
+      if (tma_thread) bulk_wait_read_all();  // the M store has read its staging tile (T's)
       __syncthreads();
       // T[r][s] = X[r][s] beta_s and T diag(rk) (s <= r): row r, 8 columns per thread
 #pragma unroll
@@ -673,10 +677,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
                sw128_kdesc<2>(ts, 64, s), idesc_amn, s > 0);
       }
       mma_commit(&bar_mma);
-      if (have_next) {
-        stage_g(h_next, tok0_next);                // L and X are free (T tiles written)
-        mbar_arrive_expect_tx(&bar_qv, 2 * 16384);  // q and v, issued once MMA2 is done
-      }
+    }
+    if (tma_thread && have_next) {
+      stage_g(h_next, tok0_next);                // L and X are free (T tiles written)
+      mbar_arrive_expect_tx(&bar_qv, 2 * 16384);  // q and v, issued once MMA2 is done
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
@@ -716,7 +720,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tma_thread) {
       tma_store_2d(&map_ku, sm + P_W, 0, (int)((2 * ws.recs + rec) * 128));
       bulk_commit();
     }
@@ -735,7 +739,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
     mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
   }
-  if (tid == 0) bulk_wait_read_all();  // the last staging tile is read before exit
+  if (tma_thread) bulk_wait_read_all();  // the last staging tile is read before exit
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
