@@ -205,6 +205,26 @@ __global__ void __launch_bounds__(kBSThreads, 1)
   const uint32_t tm = s_tmem;
   const uint32_t tl = tm + (uint32_t(lane_base) << 16);
 
+  // the refill of stage st for step it, its boxes spread over lane 0 of warps 1..8 (the
+  // expected bytes were registered by thread 0 with the MMAs that last read the stage)
+  auto issue_load_spread = [&](int it, int st) {
+    if ((tid & 31) != 0 || warp == 0 || warp > 8) return;
+    const int ch = nck - 1 - it;
+    const long long rec = rec_of(ch);
+    uint8_t* b = sm + st * kBStage;
+    uint64_t* bar = &bar_ld[st];
+    const int tok0 = (int)(bos + (long long)ch * kC);
+    switch (warp) {
+      case 1: tma_load_2d(b + B_Q, &map_qw, bar, 0, (int)(rec * 64)); break;
+      case 2: tma_load_2d(b + B_Q + 8192, &map_qw, bar, 64, (int)(rec * 64)); break;
+      case 3: tma_load_2d(b + B_W, &map_ku, bar, 0, (int)((2 * bw.f.recs + rec) * 128)); break;
+      case 4: tma_load_2d(b + B_KT, &map_ku, bar, 0, (int)(rec * 128)); break;
+      case 5: tma_load_2d(b + B_M, &map_m, bar, 0, (int)(rec * 64)); break;
+      case 6: tma_load_3d(b + B_DO, &map_do, bar, 0, h, tok0); break;
+      case 7: tma_load_3d(b + B_DO + 8192, &map_do, bar, 64, h, tok0); break;
+      default: bulk_load(b + B_V, bw.f.vec + rec * 256, 1024, bar); break;
+    }
+  };
   // step `it` handles chunk nck - 1 - it
   auto issue_load = [&](int it, int st) {
     const int ch = nck - 1 - it;
@@ -344,10 +364,13 @@ __global__ void __launch_bounds__(kBSThreads, 1)
       for (int s = 0; s < 4; ++s)
         mma_ts(tm + BT_S, tm + BT_UA + 8 * s, sw128_kdesc<2>(wsm, 128, s), idesc_s_ts, 1);
       mma_commit(&bar_mma);
+      // the refill's bytes land on the stage's next phase (its current phase completed at
+      // the top of this step)
+      if (it + 2 < nck) mbar_arrive_expect_tx(&bar_ld[st], kBStageTx);
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
-    if (tid == 0 && it + 2 < nck) issue_load(it + 2, st);
+    if (it + 2 < nck) issue_load_spread(it + 2, st);
     inflight[st] = (it + 2 < nck) ? it + 2 : -1;
     // ---- bf16 copy of dS (= dS' of the previous chunk) and its record
     {

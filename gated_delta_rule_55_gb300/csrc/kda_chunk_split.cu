@@ -64,7 +64,8 @@ constexpr int ST_G = 0;                 // g [4 quarters][64 tok][32] fp32, no s
 constexpr int ST_Q = P_KTT;             // q, two SW128 boxes
 constexpr int ST_V = P_V;               // v
 static_assert(ST_G + 32768 <= P_T, "g staging must stay inside the solve area");
-constexpr uint32_t kStageBytes = 3 * 16384 + 32768;
+constexpr uint32_t kStageBytes = 3 * 16384 + 32768;  // one record's staged tiles
+static_assert(kStageBytes == (16384 + 32768) + 2 * 16384, "k + g batch and q + v batch");
 constexpr size_t kPSmem = P_END + 1024;
 
 // Tensor Memory of the prep kernel (256 columns: two CTAs per SM).
@@ -840,6 +841,23 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t tm = s_tmem;
   const uint32_t tl = tm + (uint32_t(lane_base) << 16);
 
+  // the refill of stage st with chunk ch, its boxes spread over lane 0 of warps 1..7 (the
+  // expected bytes were registered by thread 0 with the MMAs that last read the stage)
+  auto issue_load_spread = [&](int ch, int st) {
+    if ((tid & 31) != 0 || warp == 0 || warp > 7) return;
+    const long long rec = (slot0 + ch) * H + h;
+    uint8_t* b = sm + st * kStage;
+    uint64_t* bar = &bar_ld[st];
+    switch (warp) {
+      case 1: tma_load_2d(b + S_W, &map_ku, bar, 0, (int)((2 * ws.recs + rec) * 128)); break;
+      case 2: tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128)); break;
+      case 3: bulk_load(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar); break;
+      case 4: bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar); break;
+      case 5: if (want_out) tma_load_2d(b + S_Q, &map_qw, bar, 0, (int)(rec * 64)); break;
+      case 6: if (want_out) tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, (int)(rec * 64)); break;
+      default: if (want_out) tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64)); break;
+    }
+  };
   // one chunk record into stage st
   auto issue_load = [&](int ch, int st) {
     const long long rec = (slot0 + ch) * H + h;
@@ -992,11 +1010,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
         mma_ts(tm + S_TM_S, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ks, 128, s), idesc_n128, 1);
       }
       mma_commit(&bar_mma);
+      // the refill's bytes land on the stage's next phase (its current phase completed at
+      // the top of this chunk)
+      if (ch + 2 < nck) mbar_arrive_expect_tx(&bar_ld[st], want_out ? kStageTx : kStageTxBwd);
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
     // the stage is consumed (its last readers were MMA4 and the U' pack): refill it
-    if (tid == 0 && ch + 2 < nck) issue_load(ch + 2, st);
+    if (ch + 2 < nck) issue_load_spread(ch + 2, st);
     inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
     // ---- bf16 copy of the new state and the output O = diag(rq) O' (O' itself when the
     //      records carry rq)
