@@ -58,7 +58,8 @@ static_assert(P_KS + 16384 <= P_KTT, "re-used tiles must stay inside Xl/Kb");
 // Staging of the NEXT record's raw inputs (TMA), each tile issued as soon as its space is
 // free: k into the K^^T staging tile once the K^^T store has read it (after the A/M
 // readback), g into L and X once the T tiles are written, q into K~^T and v into its own
-// tile (where MMA2 reads it as staged) once MMA2 is done.  All land on one barrier phase.
+// tile (where MMA2 reads it as staged) once MMA2 is done.  k and g land on one barrier, q
+// and v on a second, so that the next record's gate prefix can start before q and v arrive.
 constexpr int ST_K = P_KS;              // k [64 tok x 128] bf16, two SW128 boxes
 constexpr int ST_G = 0;                 // g [4 quarters][64 tok][32] fp32, no swizzle
 constexpr int ST_Q = P_KTT;             // q, two SW128 boxes
