@@ -130,6 +130,31 @@ def test_chunked_bf16_gradients_without_initial_state_output():
     _check(gpu, _oracle(d, cot, 0.1, -2.0, True), True, names=GRADS[:-1], d=d)
 
 
+def test_chunked_bf16_multi_record_ctas_odd_head_count():
+    """More (chunk, head) records (16 x 23 = 368) than the prep's persistent CTAs, an odd head
+    count (the record walk's head carry) and a partial last chunk, with an initial state and
+    a final-state cotangent; three heads compared with the oracle run on each alone (heads
+    are independent, the parameter gradients of a head included)."""
+    B, T, H = 1, 1000, 23
+    d, cot = _case(B, T, H, 128, 128, 61, state=True, final=True)
+    lb, scale = -3.0, 128 ** -0.5
+    gpu = _run(d, cot, B, T, H, 128, 128, scale, lb, True)
+    for h in (0, 11, 22):
+        sl = {n: d[n][:, :, h:h + 1] for n in ("q", "k", "v", "g", "beta_logits")}
+        sl["a_log"] = d["a_log"][h:h + 1]
+        sl["dt_bias"] = d["dt_bias"][:, h:h + 1]
+        sl["initial_state"] = d["initial_state"][:, h:h + 1]
+        csl = {"d_out": cot["d_out"][:, :, h:h + 1],
+               "d_final_state": cot["d_final_state"][:, h:h + 1]}
+        ref = _oracle(sl, csl, scale, lb, True)
+        got = {n: gpu[n][:, :, h:h + 1] for n in ("dq", "dk", "dv", "dg", "dbeta_logits")}
+        got["dinitial_state"] = gpu["dinitial_state"][:, h:h + 1]
+        got["da_log"] = gpu["da_log"][h:h + 1]
+        got["ddt_bias"] = gpu["ddt_bias"][:, h:h + 1]
+        _check(got, ref, True, d=sl)
+    assert kda.kda_device_error(1) == 0
+
+
 def test_chunked_bf16_prefill_workload_sampled_head():
     """The prefill workload's full size (B 4, T 4096, H 32) through the chunked backward,
     every per-token gradient of one sampled (sequence, head) compared with the oracle run on

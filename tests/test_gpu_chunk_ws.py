@@ -135,6 +135,29 @@ def test_varlen_many_short_sequences():
     _check(out, S, ref_out, ref_S)
 
 
+def test_multi_record_ctas_odd_head_count():
+    """More (chunk, head) records (16 x 23 = 368) than the prep's persistent CTAs (two per
+    SM), so CTAs walk several records (head and chunk indices stepped by the grid size, with
+    a carry: the grid size is not a multiple of 23) and stage the next record's tiles while
+    they finish the current one; the last chunk is partial (1000 = 15 x 64 + 40)."""
+    _case(B=1, T=1000, H=23, lb=-3.0, seed=31)
+
+
+def test_varlen_multi_record_ctas_odd_head_count():
+    """Packed sequences with more records than persistent CTAs (an odd head count, empty,
+    single-chunk and partial sequences among them), every output compared."""
+    lens = [1000, 37, 0, 513, 64, 700]
+    H = 11
+    d = synth.varlen_inputs(lens, H, 128, 128, seed=32, state_std=0.1)
+    out, S = run_varlen(d, H, 128, 128, 0.09, -1.5, 64, True, ws=True)
+    o = oracle_inputs(d, True)
+    ref_out, ref_S = kda_forward_varlen(o["q"], o["k"], o["v"], o["g"], o["beta_logits"],
+                                        o["a_log"], o["dt_bias"], d["cu_seqlens"], 0.09, -1.5,
+                                        o["initial_state"])
+    _check(out, S, ref_out, ref_S)
+    np.testing.assert_array_equal(S[2], d["initial_state"][2])
+
+
 def test_prefill_workload_B4_T4096_sampled():
     """B=4, T=4096, H=32, bf16, chunk 64, zero initial state, through the workspace: the
     full launch, checked on sampled (b, h) pairs over the whole sequence."""
