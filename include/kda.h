@@ -20,7 +20,8 @@
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers of the current CUDA device, dense (row-major,
  *     no padding) and 16-byte aligned.  The caller allocates every buffer, outputs
- *     included; the library allocates nothing and keeps no state between calls.
+ *     included; the library allocates nothing and keeps no state between calls (the one
+ *     exception is the fixed scratch array behind kda_chunk_fwd_noalloc).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and
  *     the call returns without synchronising.  Inputs must stay valid until the stream
  *     reaches the launch.
@@ -154,13 +155,22 @@ int kda_chunk_fwd_varlen_ws(const void* q, const void* k, const void* v, const f
 /*
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd_ws with the workspace taken from a scratch array
  *   that the library keeps in device memory (KDA_NOALLOC_SCRATCH_BYTES per device), so the
- *   caller passes none.  It has no counterpart on the source pages: an interface
- *   convenience over the workspace entry point.
- *   Arguments, layouts, results and errors are those of kda_chunk_fwd.  A configuration
- *   whose workspace (kda_chunk_fwd_workspace_size) exceeds the array is rejected with
- *   KDA_ERR_WORKSPACE before anything is enqueued.  The array is shared by every call on a
- *   device: calls must not overlap in time (issue them on one stream, or synchronise
- *   between streams).  Its device memory is taken when the entry point is first used.
+ *   caller passes none.  It is meant for callers that cannot call cudaMalloc themselves
+ *   (an allocator that owns all device memory, code running inside a captured or
+ *   pre-planned execution that forbids allocation).  It has no counterpart on the source
+ *   pages: an interface convenience over the workspace entry point.
+ *   Arguments, layouts and results are those of kda_chunk_fwd.  Errors are those of
+ *   kda_chunk_fwd, checked in the same order; a configuration whose arguments are valid but
+ *   whose workspace (kda_chunk_fwd_workspace_size) exceeds the array is then rejected with
+ *   KDA_ERR_WORKSPACE, before anything is enqueued.  The array is shared by every call on
+ *   a device and keeps the last call's contents: calls must not overlap in time (issue them
+ *   on one stream, or synchronise between streams); overlapping calls race.
+ *   Set-up: the array's device address is looked up once per CUDA context, by the first
+ *   call made with that context current (a context that replaces one destroyed by
+ *   cudaDeviceReset gets its own lookup); make that first call before any stream capture.
+ *   Under lazy module loading (the CUDA default) the array's device memory is reserved by
+ *   that first call; with CUDA_MODULE_LOADING=EAGER every context that loads the library
+ *   reserves it at start-up.  Either way it is held until the process exits.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)256 << 20)
 int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,

@@ -18,8 +18,8 @@ What it computes, and from which passage
   parameters; ``kda_tkg``'s ``S`` is read and overwritten in place.
 * Varlen packing -- ejkernel ``recurrent`` module page, ``cu_seqlens`` parameter.
 
-Readings where the pages are silent or ambiguous (each is also listed in the design doc)
------------------------------------------------------------------------------------
+Readings where the pages are silent or ambiguous
+------------------------------------------------
 1. Decay before delta (``order="decay_first"``, the default): the error term is taken
    against the decayed memory, ``S' = diag(exp(gamma)) S``, ``u = beta (v - S'^T k)``,
    ``S <- S' + k u^T``.  The recurrence as printed uses the undecayed memory inside the

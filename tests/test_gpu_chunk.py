@@ -2,16 +2,17 @@
 
 fp32 q/k/v: max |gpu - oracle| <= 1e-4.  bf16 q/k/v: max |gpu - oracle| / max |oracle|
 <= 2e-2 per tensor (out and final state), the oracle fed the same bf16-rounded values.
-Sizes span several chunks and a ragged last chunk; full-size workloads are checked on
-sampled (sequence, head) pairs, which are independent of each other.
+Sizes span several chunks and a ragged last chunk; the full-size workloads are compared
+element by element over every (sequence, head) pair, the oracle running over the pairs in a
+pool of host processes.
 """
 import numpy as np
 import pytest
 import torch
 
 from gated_delta_rule_55_gb300 import kda_chunk_fwd, synth
-from gpu_helpers import (BF16_REL, F32_ATOL, ensure_built, max_abs, oracle_inputs, rel_err,
-                         run_chunk, run_varlen, to_dev)
+from gpu_helpers import (BF16_REL, F32_ATOL, check_full, check_rel, ensure_built, max_abs, oracle_inputs,
+                         rel_err, run_chunk, run_varlen, to_dev, workload_reference)
 from oracle import kda_forward, kda_forward_varlen
 
 pytestmark = pytest.mark.gpu
@@ -24,9 +25,9 @@ def _built():
 
 def _check(gpu_out, gpu_state, ref_out, ref_state, bf16):
     if bf16:
-        assert rel_err(gpu_out, ref_out) <= BF16_REL, rel_err(gpu_out, ref_out)
+        check_rel(None, "out", gpu_out, ref_out)
         if gpu_state is not None:
-            assert rel_err(gpu_state, ref_state) <= BF16_REL, rel_err(gpu_state, ref_state)
+            check_rel(None, "final_state", gpu_state, ref_state)
     else:
         assert max_abs(gpu_out, ref_out) <= F32_ATOL, max_abs(gpu_out, ref_out)
         if gpu_state is not None:
@@ -152,52 +153,19 @@ def test_varlen_tensor_core_path_small():
     assert kda_device_error(reset=True) == 0
 
 
-def _sampled_oracle(d, bs, hs, scale, lb, bf16):
-    """Oracle on selected (b, h) pairs of a [B, T, H, .] problem (pairs are independent)."""
-    outs, states = [], []
-    for b, h in zip(bs, hs):
-        sub = {n: np.ascontiguousarray(d[n][b:b + 1, :, h:h + 1])
-               for n in ("q", "k", "v", "g", "beta_logits")}
-        sub = oracle_inputs(sub, bf16)
-        s0 = None if d.get("initial_state") is None else d["initial_state"][b:b + 1, h:h + 1]
-        ro, rs = kda_forward(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta_logits"],
-                             d["a_log"][h:h + 1], d["dt_bias"][:, h:h + 1], scale, lb, s0)
-        outs.append(ro[0, :, 0])
-        states.append(rs[0, 0])
-    return outs, states
-
-
-def test_prefill_workload_B4_T4096_sampled():
-    """B=4, T=4096, H=32, dk=dv=128, bf16 q/k/v, chunk 64, zero initial state: the full
-    launch, checked on sampled (b, h) pairs over the whole sequence."""
-    w = synth.PREFILL_B4
-    d = synth.workload_inputs(w)
+def test_prefill_workload_B4_T4096_full():
+    """B=4, T=4096, H=32, dk=dv=128, bf16 q/k/v, chunk 64, zero initial state, through the
+    single-pass kernel: every element of all 128 (b, h) pairs against the oracle."""
+    w, d, (ref_out, ref_S) = workload_reference(synth.PREFILL_B4.name)
     out, S = run_chunk(d, w.B, w.T, w.H, w.dk, w.dv, w.q_scale, w.lower_bound, w.chunk, True)
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(S))
-    rng = np.random.default_rng(1)
-    bs, hs = rng.integers(0, w.B, 4), rng.integers(0, w.H, 4)
-    ro, rs = _sampled_oracle(d, bs, hs, w.q_scale, w.lower_bound, True)
-    for i, (b, h) in enumerate(zip(bs, hs)):
-        assert rel_err(out[b, :, h], ro[i]) <= BF16_REL
-        assert rel_err(S[b, h], rs[i]) <= BF16_REL
+    check_full("prefill B4 T4096 H32, kda_chunk_fwd", out, ref_out, S, ref_S)
 
 
-def test_varlen_workload_8seq_sampled():
+def test_varlen_workload_8seq_full():
     """8 packed sequences of 512..8192 tokens (seeded), H=16, bf16, chunk 64, seeded
-    N(0, 0.02) initial states: sampled (sequence, head) pairs over whole sequences."""
-    w = synth.VARLEN_8
-    d = synth.workload_inputs(w)
+    N(0, 0.02) initial states, single pass: every (sequence, head) pair, every element."""
+    w, d, (ref_out, ref_S) = workload_reference(synth.VARLEN_8.name)
     out, S = run_varlen(d, w.H, w.dk, w.dv, w.q_scale, w.lower_bound, w.chunk, True)
-    cu = d["cu_seqlens"]
-    rng = np.random.default_rng(2)
-    picks = [(int(n), int(rng.integers(0, w.H))) for n in rng.choice(w.n_seqs, 3, replace=False)]
-    picks.append((int(np.argmax(np.diff(cu))), 0))  # the longest sequence
-    for n, h in picks:
-        a, b = cu[n], cu[n + 1]
-        o = oracle_inputs({x: d[x][None, a:b, h:h + 1] for x in ("q", "k", "v")}, True)
-        ro, rs = kda_forward(o["q"], o["k"], o["v"], d["g"][None, a:b, h:h + 1],
-                             d["beta_logits"][None, a:b, h:h + 1], d["a_log"][h:h + 1],
-                             d["dt_bias"][:, h:h + 1], w.q_scale, w.lower_bound,
-                             d["initial_state"][n:n + 1, h:h + 1])
-        assert rel_err(out[a:b, h], ro[0, :, 0]) <= BF16_REL
-        assert rel_err(S[n, h], rs[0, 0]) <= BF16_REL
+    check_full("varlen 8 seq H16, kda_chunk_fwd_varlen", out, ref_out, S, ref_S,
+               d["cu_seqlens"])

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from gated_delta_rule_55_gb300 import kda_decode_step, synth
-from gpu_helpers import F32_ATOL, ensure_built, max_abs, to_dev
+from gpu_helpers import F32_ATOL, ensure_built, max_abs, oracle_pool, to_dev
 from oracle import kda_decode_step as oracle_decode
 
 pytestmark = pytest.mark.gpu
@@ -72,33 +72,30 @@ def test_decode_workload_B64_full_compare():
     assert max_abs(Sd.cpu().numpy(), S_ref) <= F32_ATOL
 
 
-def test_decode_workload_B512_32_chained_steps_sampled():
-    """B=512, H=32, 128x128 state (1.07 GB) advanced by 32 consecutive calls with the
-    state passed through in place; sampled (b, h) pairs against 32 oracle steps."""
+def test_decode_workload_B512_32_chained_steps_full():
+    """B=512, H=32, 128x128 state (1.07 GB) advanced by 32 consecutive calls with the state
+    passed through in place: every output of every step and every final-state entry of all
+    16,384 (b, h) pairs against 32 chained oracle steps (run over head ranges in a pool of
+    host processes)."""
+    from oracle import pool
     w = synth.DECODE_B512
     B, H, dk, dv = w.B, w.H, w.dk, w.dv
     a_log, dt_bias = synth.gate_params(H, dk, w.seed)
     S0 = synth.decode_state(B, H, dk, dv, w.seed, w.state_std)
+    toks = [synth.decode_token_inputs(B, H, dk, dv, w.seed, step) for step in range(w.steps)]
+    oracle_pool()  # start the workers before the device work
     Sd = to_dev(S0)
-    rng = np.random.default_rng(0)
-    bs = rng.choice(B, 6, replace=False)
-    hs = rng.choice(H, 6)
-    S_ref = [S0[b, h][None, None].astype(np.float64) for b, h in zip(bs, hs)]
-    worst_o = 0.0
-    for step in range(w.steps):
-        tok = synth.decode_token_inputs(B, H, dk, dv, w.seed, step)
+    outs = []
+    for tok in toks:
         out, Sd = _run(tok, a_log, dt_bias, Sd, w.q_scale, w.lower_bound)
-        for i, (b, h) in enumerate(zip(bs, hs)):
-            one = {"q": tok["q"][b:b + 1, :, h:h + 1], "k": tok["k"][b:b + 1, :, h:h + 1],
-                   "g": tok["g"][b:b + 1, :, h:h + 1], "v": tok["v"][b:b + 1, h:h + 1],
-                   "beta_logits": tok["beta_logits"][b:b + 1, :, h:h + 1]}
-            o, S_ref[i] = oracle_decode(**one, a_log=a_log[h:h + 1], dt_bias=dt_bias[:, h:h + 1],
-                                        scale=w.q_scale, lower_bound=w.lower_bound, S=S_ref[i])
-            worst_o = max(worst_o, max_abs(out[b, h], o[0, 0]))
-    assert worst_o <= F32_ATOL
-    Sg = Sd.cpu().numpy()
-    for i, (b, h) in enumerate(zip(bs, hs)):
-        assert max_abs(Sg[b, h], S_ref[i][0, 0]) <= F32_ATOL
+        outs.append(out)
+    S_gpu = Sd.cpu().numpy()
+    del Sd
+    o_ref, S_ref = pool.decode_chain(oracle_pool(), toks, a_log, dt_bias, w.q_scale,
+                                     w.lower_bound, S0)
+    worst_o = max(max_abs(o, r) for o, r in zip(outs, o_ref))
+    assert worst_o <= F32_ATOL, worst_o
+    assert max_abs(S_gpu, S_ref) <= F32_ATOL
 
 
 def test_decode_batch_zero_is_a_no_op():
