@@ -472,9 +472,11 @@ def backward_measure(w, d, x, reps=3):
                               "tokens_per_s": B * T / ((ms_train_fwd + ms_saved) * 1e-3)}}
 
 def recurrent_attention_measure(reps=3):
-    """kda_recurrent_attention_fwd on B=4, T=4096, Hq=32, Hkv=8, D=128, bf16 q/k/v with
-    per-channel key and value gates (gk, gv fp32): median time per call and its algorithmic
-    bytes (q, k, v, gk, gv, out and the final state, each once)."""
+    """kda_recurrent_attention_fwd on B=4, T=4096, Hq=32, Hkv=8, D=128, bf16 q/k/v: with
+    per-channel key and value gates (gk, gv fp32; the token-serial kernel), and with the key
+    gate only through kda_recurrent_attention_fwd_ws (the chunked tensor-core path).  Median
+    time per call and its algorithmic bytes (q, k, v, the gates, out and the final state,
+    each once)."""
     torch = _torch()
     import gated_delta_rule_55_gb300 as kda
     B, T, Hq, Hkv, D = 4, 4096, 32, 8, 128
@@ -486,12 +488,68 @@ def recurrent_attention_measure(reps=3):
     gv = -0.05 * torch.rand(B, T, Hq, D, device="cuda", generator=g)
     out = torch.empty(B, T, Hq, D, device="cuda", dtype=torch.bfloat16)
     fs = torch.empty(B, Hq, D, D, device="cuda")
+    ws = torch.empty(kda.kda_recurrent_attention_fwd_workspace_size(B, T, Hq, Hkv, D),
+                     dtype=torch.uint8, device="cuda")
 
-    def call():
+    def both():
         kda.kda_recurrent_attention_fwd(q, k, v, out, B, T, Hq, Hkv, D, gk=gk, gv=gv,
                                         final_state=fs)
 
-    call()
+    def key_only():
+        kda.kda_recurrent_attention_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, gk=gk,
+                                           final_state=fs, workspace=ws)
+
+    def median_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(reps):
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    io = B * T * (Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * 2) + B * Hq * D * D * 4
+    gate = B * T * Hq * D * 4
+    ms = median_ms(both)
+    ms_k = median_ms(key_only)
+    return {"entry": "kda_recurrent_attention_fwd",
+            "workload": "B4 T4096 Hq32 Hkv8 D128 bf16, gk + gv gates", "ms_per_call": ms,
+            "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": io + 2 * gate,
+            "hbm_gbs": (io + 2 * gate) / (ms * 1e-3) / 1e9,
+            "key_gate_only": {"entry": "kda_recurrent_attention_fwd_ws (chunked, tensor cores)",
+                              "workload": "B4 T4096 Hq32 Hkv8 D128 bf16, gk gate",
+                              "ms_per_call": ms_k, "tokens_per_s": B * T / (ms_k * 1e-3),
+                              "algorithmic_bytes": io + gate,
+                              "hbm_gbs": (io + gate) / (ms_k * 1e-3) / 1e9,
+                              "workspace_bytes": int(ws.numel())}}
+
+
+def attention_measure(w, x, reps=5):
+    """kda_attention_fwd_ws (the kernel_delta_attention call on the tensor-core path) on the
+    prefill workload's q, k, v (B=4, T=4096, H=32, bf16): beta = sigmoid(N(0, 1)) and the
+    page example's per-head decay N(0, 1) * -0.01, L2-normalised q / k, decay first.  Median
+    time per call and its algorithmic bytes (q, k, v, out bf16; beta, decay fp32; the final
+    state), each once."""
+    torch = _torch()
+    import gated_delta_rule_55_gb300 as kda
+    B, T, H, dk, dv = w.B, w.T, w.H, w.dk, w.dv
+    g = torch.Generator(device="cuda").manual_seed(12)
+    beta = torch.sigmoid(torch.randn(B, T, H, device="cuda", generator=g))
+    decay = torch.randn(B, T, H, device="cuda", generator=g) * -0.01
+    ws = torch.empty(kda.kda_attention_fwd_workspace_size(B, T, H, dk, dv, 64),
+                     dtype=torch.uint8, device="cuda")
+
+    def call():
+        kda.kda_attention_fwd_ws(x["q"], x["k"], x["v"], beta, decay, None, x["out"],
+                                 x["final_state"], B, T, H, dk, dv, softmax_scale=w.q_scale,
+                                 workspace=ws)
+
+    for _ in range(3):
+        call()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times = []
@@ -502,10 +560,9 @@ def recurrent_attention_measure(reps=3):
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
     ms = statistics.median(times)
-    nbytes = B * T * (Hq * D * 2 + 2 * Hkv * D * 2 + 2 * Hq * D * 4 + Hq * D * 2) + B * Hq * D * D * 4
-    return {"entry": "kda_recurrent_attention_fwd",
-            "workload": "B4 T4096 Hq32 Hkv8 D128 bf16, gk + gv gates", "ms_per_call": ms,
-            "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": nbytes,
+    nbytes = B * T * H * ((2 * dk + dv) * 2 + 4 + 4 + dv * 2) + B * H * dk * dv * 4
+    return {"entry": "kda_attention_fwd_ws", "workload": w.name + " (beta given, page decay)",
+            "ms_per_call": ms, "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": nbytes,
             "hbm_gbs": nbytes / (ms * 1e-3) / 1e9}
 
 
@@ -617,6 +674,11 @@ def native(args):
         line["recurrent_attention"] = recurrent_attention_measure()
         line["recurrent_attention"]["frac_of_hbm_peak"] = (
             line["recurrent_attention"]["hbm_gbs"] / pk["hbm_gbs"])
+        line["recurrent_attention"]["key_gate_only"]["frac_of_hbm_peak"] = (
+            line["recurrent_attention"]["key_gate_only"]["hbm_gbs"] / pk["hbm_gbs"])
+        line["attention"] = attention_measure(w, x)
+        line["attention"]["frac_of_hbm_peak"] = line["attention"]["hbm_gbs"] / pk["hbm_gbs"]
+        line["attention"]["vs_chunk_fwd_ws_step"] = line["attention"]["ms_per_call"] / (ms / K)
         line["backward"] = backward_measure(w, d, x)
         line["backward"]["frac_of_hbm_peak"] = line["backward"]["hbm_gbs"] / pk["hbm_gbs"]
         line["cpu_baseline"] = cpu_baseline(w, d)

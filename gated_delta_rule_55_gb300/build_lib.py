@@ -16,7 +16,7 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libkda.so")
 SOURCES = ["kda_abi.cu", "kda_decode.cu", "kda_chunk_simt.cu", "kda_chunk_tc.cu",
            "kda_chunk_split.cu", "kda_noalloc.cu", "kda_recurrent.cu", "kda_backward.cu",
-           "kda_gla.cu", "kda_chunk_bwd.cu", "kda_selftest.cu"]
+           "kda_gla.cu", "kda_gla_chunk.cu", "kda_chunk_bwd.cu", "kda_selftest.cu"]
 HEADERS = ["kda_internal.cuh", "tc_prims.cuh", "chunk_common.cuh", "chunk_records.cuh"]
 
 NVCC_FLAGS = [

@@ -43,6 +43,113 @@ int check_common(float* scale, float lower_bound, int dk, int dv) {
   return check_dims_scale(scale, dk, dv);
 }
 
+// The kernel_delta_attention call takes the two-launch tensor-core path for bf16 q/k/v with
+// dk = dv = 128 in the chunked mode with 64-token chunks.
+bool attn_split(int dk, int dv, int chunk, int flags, int dtype) {
+  return dtype == KDA_BF16 && dk == 128 && dv == 128 && chunk == 64 &&
+         !(flags & KDA_ATTN_RECURRENT);
+}
+
+// kda_attention_fwd (use_ws false) and kda_attention_fwd_ws (true).
+int attention_common(const void* query, const void* key, const void* value, const float* beta,
+                     const float* decay, const float* initial_state, void* out,
+                     float* final_state, float softmax_scale, int B, int T, int H, int dk, int dv,
+                     int chunk, int flags, int dtype, void* workspace, size_t workspace_bytes,
+                     bool use_ws, kda_stream_t stream) {
+  if (!query || !key || !value || !beta || !out) return KDA_ERR_NULL_POINTER;
+  if (B < 0 || T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
+  if (flags & ~(KDA_ATTN_NO_QK_L2NORM | KDA_ATTN_RECURRENT | KDA_ATTN_ORDER_LITERAL))
+    return KDA_ERR_FLAGS;
+  int s = check_dims_scale(&softmax_scale, dk, dv);
+  if (s != KDA_OK) return s;
+  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_TOO_LARGE;
+  kda::ChunkArgs a{};
+  a.q = query; a.k = key; a.v = value; a.beta_logits = beta; a.decay = decay;
+  a.initial_state = initial_state; a.out = out; a.final_state = final_state;
+  a.scale = softmax_scale; a.lower_bound = 0.f;
+  a.B = B; a.T = T; a.total_T = B * T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
+  a.gate_head = 1; a.beta_prob = 1;
+  a.no_l2norm = (flags & KDA_ATTN_NO_QK_L2NORM) ? 1 : 0;
+  a.literal = (flags & KDA_ATTN_ORDER_LITERAL) ? 1 : 0;
+  if (a.chunk != 16 && a.chunk != 64) return KDA_ERR_CHUNK;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  const void* ptrs[] = {query, key, value, beta, decay, initial_state, out, final_state};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  const double elems = (double)a.total_T * H * (dk > dv ? dk : dv);
+  if (elems >= 1099511627776.0 || (double)B * H * dk * dv >= 1099511627776.0 || B > 65535 ||
+      H > 65535)
+    return KDA_ERR_TOO_LARGE;
+  // the workspace entry takes the two-launch tensor-core path where it applies (a
+  // configuration with no tokens needs no workspace: the SIMT path passes the state through)
+  const bool split = use_ws && attn_split(dk, dv, chunk, flags, dtype) &&
+                     kda::chunk_split_workspace(a) > 0;
+  if (split) {
+    if (!kda::chunk_split_index_ok(a)) return KDA_ERR_TOO_LARGE;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < kda::chunk_split_workspace(a))
+      return KDA_ERR_WORKSPACE;
+  }
+  s = check_device();
+  if (s != KDA_OK) return s;
+  if (B == 0) return KDA_OK;
+  const bool bf16 = dtype == KDA_BF16;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (split)
+    e = kda::launch_chunk_split(a, workspace, st);
+  else
+    e = (flags & KDA_ATTN_RECURRENT) ? kda::launch_recurrent(a, bf16, st)
+                                     : kda::launch_chunk_simt(a, bf16, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+// kda_recurrent_attention_fwd (use_ws false) and its workspace variant (true).
+int recurrent_common(const void* query, const void* key, const void* value, const float* g,
+                     const float* g_gamma, const float* gk, const float* gv,
+                     float softmax_scale, const float* initial_state, void* out,
+                     float* final_state, const int32_t* cu_seqlens, int N, int B, int T, int Hq,
+                     int Hkv, int D, int reverse, int dtype, void* workspace,
+                     size_t workspace_bytes, bool use_ws, kda_stream_t stream) {
+  if (!query || !key || !value || !out) return KDA_ERR_NULL_POINTER;
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return KDA_ERR_BAD_SHAPE;
+  if (cu_seqlens && (B != 1 || N < 0)) return KDA_ERR_BAD_SHAPE;
+  if (!head_dim_ok(D)) return KDA_ERR_HEAD_DIM;
+  if (!isfinite(softmax_scale)) return KDA_ERR_SCALE;
+  if (softmax_scale <= 0.f) softmax_scale = 1.0f / sqrtf((float)D);
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  const void* ptrs[] = {query, key, value, g, g_gamma, gk, gv, initial_state, out,
+                        final_state, cu_seqlens};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  const long long nseq = cu_seqlens ? N : B;
+  if ((double)B * T * Hq * D >= 1099511627776.0 || (double)nseq * Hq * D * D >= 1099511627776.0 ||
+      (long long)B * T > 0x7fffffffLL || nseq > 65535 || Hq > 65535)
+    return KDA_ERR_TOO_LARGE;
+  kda::GlaArgs a{};
+  a.q = query; a.k = key; a.v = value; a.g = g; a.g_gamma = g_gamma; a.gk = gk; a.gv = gv;
+  a.initial_state = initial_state; a.out = out; a.final_state = final_state;
+  a.cu_seqlens = cu_seqlens; a.scale = softmax_scale; a.T = T; a.nseq = (int)nseq;
+  a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.reverse = reverse ? 1 : 0;
+  // the workspace entry takes the chunked tensor-core path where it applies (no tokens:
+  // none needed, the token-serial kernel passes the state through)
+  const bool chunked = use_ws && kda::gla_chunk_supported(a, dtype == KDA_BF16) &&
+                       nseq > 0 && T > 0;
+  if (chunked) {
+    if (!kda::gla_chunk_index_ok(a)) return KDA_ERR_TOO_LARGE;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < kda::gla_chunk_workspace(a))
+      return KDA_ERR_WORKSPACE;
+  }
+  int s = check_device();
+  if (s != KDA_OK) return s;
+  if (nseq == 0) return KDA_OK;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = chunked ? kda::launch_gla_chunk(a, workspace, st)
+                                : kda::launch_gla(a, dtype == KDA_BF16, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
 // workspace == nullptr: the single-pass kernels; otherwise (a non-zero workspace size was
 // required and checked) the two-launch path.
 int chunk_common(const kda::ChunkArgs& a, int dtype, cudaStream_t st,
@@ -165,70 +272,66 @@ int kda_recurrent_attention_fwd(const void* query, const void* key, const void* 
                                 void* out, float* final_state, const int32_t* cu_seqlens, int N,
                                 int B, int T, int Hq, int Hkv, int D, int reverse, int dtype,
                                 kda_stream_t stream) {
-  if (!query || !key || !value || !out) return KDA_ERR_NULL_POINTER;
-  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return KDA_ERR_BAD_SHAPE;
-  if (cu_seqlens && (B != 1 || N < 0)) return KDA_ERR_BAD_SHAPE;
-  if (!head_dim_ok(D)) return KDA_ERR_HEAD_DIM;
-  if (!isfinite(softmax_scale)) return KDA_ERR_SCALE;
-  if (softmax_scale <= 0.f) softmax_scale = 1.0f / sqrtf((float)D);
-  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
-  const void* ptrs[] = {query, key, value, g, g_gamma, gk, gv, initial_state, out,
-                        final_state, cu_seqlens};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
-  const long long nseq = cu_seqlens ? N : B;
-  if ((double)B * T * Hq * D >= 1099511627776.0 || (double)nseq * Hq * D * D >= 1099511627776.0 ||
-      (long long)B * T > 0x7fffffffLL || nseq > 65535 || Hq > 65535)
-    return KDA_ERR_TOO_LARGE;
-  int s = check_device();
-  if (s != KDA_OK) return s;
-  if (nseq == 0) return KDA_OK;
+  return recurrent_common(query, key, value, g, g_gamma, gk, gv, softmax_scale, initial_state,
+                          out, final_state, cu_seqlens, N, B, T, Hq, Hkv, D, reverse, dtype,
+                          nullptr, 0, false, stream);
+}
+
+size_t kda_recurrent_attention_fwd_workspace_size(int N, int B, int T, int Hq, int Hkv, int D,
+                                                  int flags, int dtype) {
+  if (flags & ~(KDA_REC_PACKED | KDA_REC_VALUE_GATE | KDA_REC_REVERSE)) return 0;
+  if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || N < 0) return 0;
+  if ((long long)B * T > 0x7fffffffLL) return 0;
+  static const int32_t marker = 0;  // only the presence of cu_seqlens matters here
   kda::GlaArgs a{};
-  a.q = query; a.k = key; a.v = value; a.g = g; a.g_gamma = g_gamma; a.gk = gk; a.gv = gv;
-  a.initial_state = initial_state; a.out = out; a.final_state = final_state;
-  a.cu_seqlens = cu_seqlens; a.scale = softmax_scale; a.T = T; a.nseq = (int)nseq;
-  a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.reverse = reverse ? 1 : 0;
-  const cudaError_t e = kda::launch_gla(a, dtype == KDA_BF16,
-                                        reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  a.cu_seqlens = (flags & KDA_REC_PACKED) ? &marker : nullptr;
+  a.gv = (flags & KDA_REC_VALUE_GATE) ? reinterpret_cast<const float*>(&marker) : nullptr;
+  a.reverse = (flags & KDA_REC_REVERSE) ? 1 : 0;
+  a.T = T;  // tokens per sequence, or the packed token count
+  a.nseq = (flags & KDA_REC_PACKED) ? N : B;
+  a.Hq = Hq; a.Hkv = Hkv; a.D = D;
+  if (!kda::gla_chunk_supported(a, dtype == KDA_BF16) || a.nseq == 0 || T == 0) return 0;
+  return kda::gla_chunk_workspace(a);
+}
+
+int kda_recurrent_attention_fwd_ws(const void* query, const void* key, const void* value,
+                                   const float* g, const float* g_gamma, const float* gk,
+                                   const float* gv, float softmax_scale,
+                                   const float* initial_state, void* out, float* final_state,
+                                   const int32_t* cu_seqlens, int N, int B, int T, int Hq,
+                                   int Hkv, int D, int reverse, int dtype, void* workspace,
+                                   size_t workspace_bytes, kda_stream_t stream) {
+  return recurrent_common(query, key, value, g, g_gamma, gk, gv, softmax_scale, initial_state,
+                          out, final_state, cu_seqlens, N, B, T, Hq, Hkv, D, reverse, dtype,
+                          workspace, workspace_bytes, true, stream);
 }
 
 int kda_attention_fwd(const void* query, const void* key, const void* value, const float* beta,
                       const float* decay, const float* initial_state, void* out,
                       float* final_state, float softmax_scale, int B, int T, int H, int dk,
                       int dv, int chunk, int flags, int dtype, kda_stream_t stream) {
-  if (!query || !key || !value || !beta || !out) return KDA_ERR_NULL_POINTER;
-  if (B < 0 || T < 0 || H <= 0) return KDA_ERR_BAD_SHAPE;
-  if (flags & ~(KDA_ATTN_NO_QK_L2NORM | KDA_ATTN_RECURRENT | KDA_ATTN_ORDER_LITERAL))
-    return KDA_ERR_FLAGS;
-  int s = check_dims_scale(&softmax_scale, dk, dv);
-  if (s != KDA_OK) return s;
-  if ((long long)B * T > 0x7fffffffLL) return KDA_ERR_TOO_LARGE;
+  return attention_common(query, key, value, beta, decay, initial_state, out, final_state,
+                          softmax_scale, B, T, H, dk, dv, chunk, flags, dtype, nullptr, 0, false,
+                          stream);
+}
+
+size_t kda_attention_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
+                                        int flags, int dtype) {
+  if (B < 0 || T < 0 || H <= 0 || (long long)B * T > 0x7fffffffLL) return 0;
+  if (!attn_split(dk, dv, chunk, flags, dtype)) return 0;
   kda::ChunkArgs a{};
-  a.q = query; a.k = key; a.v = value; a.beta_logits = beta; a.decay = decay;
-  a.initial_state = initial_state; a.out = out; a.final_state = final_state;
-  a.scale = softmax_scale; a.lower_bound = 0.f;
   a.B = B; a.T = T; a.total_T = B * T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk;
-  a.gate_head = 1; a.beta_prob = 1;
-  a.no_l2norm = (flags & KDA_ATTN_NO_QK_L2NORM) ? 1 : 0;
-  a.literal = (flags & KDA_ATTN_ORDER_LITERAL) ? 1 : 0;
-  if (a.chunk != 16 && a.chunk != 64) return KDA_ERR_CHUNK;
-  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
-  const void* ptrs[] = {query, key, value, beta, decay, initial_state, out, final_state};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
-  const double elems = (double)a.total_T * H * (dk > dv ? dk : dv);
-  if (elems >= 1099511627776.0 || (double)B * H * dk * dv >= 1099511627776.0 || B > 65535 ||
-      H > 65535)
-    return KDA_ERR_TOO_LARGE;
-  s = check_device();
-  if (s != KDA_OK) return s;
-  if (B == 0) return KDA_OK;
-  const bool bf16 = dtype == KDA_BF16;
-  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = (flags & KDA_ATTN_RECURRENT) ? kda::launch_recurrent(a, bf16, st)
-                                                     : kda::launch_chunk_simt(a, bf16, st);
-  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  return kda::chunk_split_workspace(a);
+}
+
+int kda_attention_fwd_ws(const void* query, const void* key, const void* value,
+                         const float* beta, const float* decay, const float* initial_state,
+                         void* out, float* final_state, float softmax_scale, int B, int T, int H,
+                         int dk, int dv, int chunk, int flags, int dtype, void* workspace,
+                         size_t workspace_bytes, kda_stream_t stream) {
+  return attention_common(query, key, value, beta, decay, initial_state, out, final_state,
+                          softmax_scale, B, T, H, dk, dv, chunk, flags, dtype, workspace,
+                          workspace_bytes, true, stream);
 }
 
 
@@ -591,7 +694,7 @@ int kda_device_error(int reset) {
   if (s != KDA_OK) return s;
   return (int)(kda::chunk_tc_read_error(reset != 0) | kda::chunk_split_read_error(reset != 0) |
                kda::chunk_bwd_read_error(reset != 0) | kda::decode_read_error(reset != 0) |
-               kda::selftest_read_error(reset != 0));
+               kda::selftest_read_error(reset != 0) | kda::gla_chunk_read_error(reset != 0));
 }
 
 int kda_selftest_bounded_wait(unsigned long long limit_ns, kda_stream_t stream) {

@@ -49,7 +49,7 @@ constexpr int P_L = 0;                  // fp32 [64][LDL] beta-scaled strict low
 constexpr int P_X = P_L + 64 * LDL * 4; // fp32 [64][LDL] (I + L)^{-1}
 constexpr int P_Y = P_X + 64 * LDL * 4; // fp32 [4][16][LDY] per-warp scratch
 constexpr int P_T = 40960;              // T [64 x 64] bf16 SW128
-constexpr int P_TW = P_T + 8192;        // T diag(rk)
+constexpr int P_TW = P_T + 8192;        // -T diag(rk)
 constexpr int P_KS = P_TW + 8192;       // K^^T [128 x 64] staging (after MMA1)
 constexpr int P_MS = P_T;               // M record [64 x 64] staging (readback to T write)
 constexpr int P_W = P_T;                // -W^T [128 x 64] staging (T and T diag(rk), after MMA2)
@@ -71,14 +71,19 @@ constexpr size_t kPSmem = P_END + 1024;
 
 // Tensor Memory of the prep kernel (256 columns: two CTAs per SM).
 constexpr uint32_t P_TM_D1 = 0;   // [A; M] accumulator, 160 columns
-constexpr uint32_t P_TM_DW = 0;   // W^T (after D1 is consumed), 64
+constexpr uint32_t P_TM_DW = 0;   // -W^T (after D1 is consumed), 64
 constexpr uint32_t P_TM_DU = 64;  // U~^T, 64
 constexpr uint32_t kPTmemCols = 256;
 
 __device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split path gave up
 
-// kBwd: also the backward's records (rq folded into Q~ and M, and N)
-template <bool kBwd>
+// kBwd: also the backward's records (rq folded into Q~ and M, and N).
+// kAttn: the kernel_delta_attention call's own variants (ChunkArgs gate_head): a per-head
+// log-decay decay[t, h] on every channel instead of the raw per-channel gate (no g tiles are
+// staged), beta used as given, and the runtime choices no_l2norm (q and k as given, scale
+// still on q) and literal (the key side of A and K~ takes the decay up to the token before:
+// e^{G_{t-1}} instead of e^{G_t}; with one decay per token |k|^2 = A_tt e^{gamma_t}).
+template <bool kBwd, bool kAttn>
 __global__ void __launch_bounds__(kPThreads, 2)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_ku,
                       const __grid_constant__ CUtensorMap map_m,
@@ -96,6 +101,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
   __shared__ __align__(16) float s_dec[kD];
   __shared__ __align__(16) float s_gtot[4][kD];
   __shared__ __align__(16) float s_qq[2][kC];
+  __shared__ __align__(16) float s_gam[kC];  // kAttn: this record's per-token log2-decay
   __shared__ uint64_t bar_mma, bar_ld, bar_qv;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
@@ -114,57 +120,41 @@ __global__ void __launch_bounds__(kPThreads, 2)
   // which warp 0 leads
   const bool tma_thread = tid == kPThreads - 32;
 
-  // The CTA walks the records r = blockIdx.x, blockIdx.x + gridDim.x, ... with
-  // r = slot * H + h.  Its (slot, h) pair, and for fixed-length inputs the (sequence, chunk)
-  // pair of the slot, is stepped from record to record rather than divided out each time.
-  const int step_h = (int)(gridDim.x % (unsigned)H);
-  const long long step_slot = gridDim.x / (unsigned)H;
-  long long cur_rec = blockIdx.x, cur_slot = blockIdx.x / (unsigned)H;
-  int cur_h = (int)(blockIdx.x % (unsigned)H);
-  int cur_seq = 0, cur_jc = 0;
-  if (!a.cu_seqlens) {
-    cur_seq = (int)(cur_slot / ws.nck_fixed);
-    cur_jc = (int)(cur_slot % ws.nck_fixed);
-  }
-  auto advance = [&]() {
-    cur_rec += gridDim.x;
-    cur_h += step_h;
-    long long carry = step_slot;
-    if (cur_h >= H) {
-      cur_h -= H;
-      ++carry;
-    }
-    cur_slot += carry;
-    if (!a.cu_seqlens) {
-      long long jc = cur_jc + carry;
-      while (jc >= ws.nck_fixed) {
-        jc -= ws.nck_fixed;
-        ++cur_seq;
-      }
-      cur_jc = (int)jc;
-    }
-  };
-  // the current record -> (head, chunk slot) -> (sequence, chunk of the sequence); false
-  // past the last record, and past the last chunk of packed inputs (the record count is an
-  // upper bound there)
-  auto locate = [&](int& h_, long long& tok0_, int& n_) -> bool {
-    if (cur_rec >= ws.recs) return false;
-    h_ = cur_h;
-    const long long slot = cur_slot;
+  // The CTA walks processing indices p = blockIdx.x, blockIdx.x + gridDim.x, ...  For
+  // fixed-length inputs p runs over (chunk, sequence, head), head fastest, with the chunk
+  // index DESCENDING: the records the scan reads first (every sequence's first chunks) are
+  // the last ones written, so they are still in L2 when the scan starts.  For packed inputs
+  // p is the record index itself (record r = slot * H + h).
+  const unsigned BH = (unsigned)a.B * (unsigned)H;  // fixed-length: records per chunk index
+  long long cur_p = blockIdx.x;
+  auto advance = [&]() { cur_p += gridDim.x; };
+  // the current processing index -> (record, head, first token, live tokens); false past
+  // the last record, and past the last chunk of packed inputs (the record count is an upper
+  // bound there).  Record counts stay below 2^31 (the records' TMA row coordinates are
+  // 32-bit), so the index arithmetic is 32-bit.
+  auto locate = [&](long long& rec_, int& h_, long long& tok0_, int& n_) -> bool {
+    if (cur_p >= ws.recs) return false;
+    const unsigned p32 = (unsigned)cur_p;
     int seq, jc;
     if (a.cu_seqlens) {
+      const unsigned slot = p32 / (unsigned)H;
+      h_ = (int)(p32 - slot * (unsigned)H);
+      rec_ = cur_p;
       const int N = a.B;
-      if (slot >= ws.coff[N]) return false;
+      if ((long long)slot >= ws.coff[N]) return false;
       int lo = 0, hi = N;  // coff[lo] <= slot < coff[hi]
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (ws.coff[mid] <= slot) lo = mid; else hi = mid;
+        if ((unsigned)ws.coff[mid] <= slot) lo = mid; else hi = mid;
       }
       seq = lo;
-      jc = (int)(slot - ws.coff[lo]);
+      jc = (int)(slot - (unsigned)ws.coff[lo]);
     } else {
-      seq = cur_seq;
-      jc = cur_jc;
+      const unsigned jr = p32 / BH, rem = p32 - jr * BH;
+      seq = (int)(rem / (unsigned)H);
+      h_ = (int)(rem - (unsigned)seq * (unsigned)H);
+      jc = ws.nck_fixed - 1 - (int)jr;
+      rec_ = ((long long)seq * ws.nck_fixed + jc) * H + h_;
     }
     long long bos;
     int len;
@@ -179,20 +169,28 @@ __global__ void __launch_bounds__(kPThreads, 2)
   // registered beforehand by thread 0 (stage_expect), with a block barrier in between.
   // the first record: k and g on bar_ld, q and v on bar_qv
   auto stage_expect = [&]() {
-    mbar_arrive_expect_tx(&bar_ld, 16384 + 32768);
+    mbar_arrive_expect_tx(&bar_ld, kAttn ? 16384 : 16384 + 32768);
     mbar_arrive_expect_tx(&bar_qv, 2 * 16384);
   };
   // the next record's k (thread 0; its bytes join the barrier phase without arriving)
+  // (the inputs are read once: they are loaded with an evict-first L2 policy, so that the
+  // L2 keeps the records instead)
+  const uint64_t pol_in = policy_evict_first();
   auto stage_k = [&](int h_, long long tok0_) {
     mbar_expect_tx(&bar_ld, 16384);
-    tma_load_3d(sm + ST_K, &map_k, &bar_ld, 0, h_, (int)tok0_);
-    tma_load_3d(sm + ST_K + 8192, &map_k, &bar_ld, 64, h_, (int)tok0_);
+    tma_load_3d_hint(sm + ST_K, &map_k, &bar_ld, 0, h_, (int)tok0_, pol_in);
+    tma_load_3d_hint(sm + ST_K + 8192, &map_k, &bar_ld, 64, h_, (int)tok0_, pol_in);
   };
   // the next record's g (thread 0), with the arrival that closes bar_ld's batch
   auto stage_g = [&](int h_, long long tok0_) {
+    if constexpr (kAttn) {  // no gate tiles: the arrival alone closes the batch
+      mbar_arrive(&bar_ld);
+      return;
+    }
     mbar_arrive_expect_tx(&bar_ld, 32768);
     for (int qtr = 0; qtr < 4; ++qtr)
-      tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, (int)tok0_);
+      tma_load_3d_hint(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, (int)tok0_,
+                       pol_in);
   };
   // the next record's q and v halves (lane 0 of warps 0..3), after thread 0's arrival
   // registered their bytes
@@ -200,22 +198,25 @@ __global__ void __launch_bounds__(kPThreads, 2)
     if (lane != 0 || warp >= 4) return;
     const int half = warp & 1;
     if (warp < 2)
-      tma_load_3d(sm + ST_Q + half * 8192, &map_q, &bar_qv, 64 * half, h_, (int)tok0_);
+      tma_load_3d_hint(sm + ST_Q + half * 8192, &map_q, &bar_qv, 64 * half, h_, (int)tok0_,
+                       pol_in);
     else
-      tma_load_3d(sm + ST_V + half * 8192, &map_v, &bar_qv, 64 * half, h_, (int)tok0_);
+      tma_load_3d_hint(sm + ST_V + half * 8192, &map_v, &bar_qv, 64 * half, h_, (int)tok0_,
+                       pol_in);
   };
   auto stage_issue = [&](int h_, long long tok0_) {
     if (lane != 0) return;
     const int r0 = (int)tok0_;
-    for (int box = warp; box < 10; box += 8) {
+    for (int box = warp; box < (kAttn ? 6 : 10); box += 8) {
       if (box < 6) {
         const int half = box & 1, which = box >> 1;  // q, k, v halves
         const CUtensorMap* m = which == 0 ? &map_q : which == 1 ? &map_k : &map_v;
         const int dst = (which == 0 ? ST_Q : which == 1 ? ST_K : ST_V) + half * 8192;
-        tma_load_3d(sm + dst, m, which == 1 ? &bar_ld : &bar_qv, 64 * half, h_, r0);
+        tma_load_3d_hint(sm + dst, m, which == 1 ? &bar_ld : &bar_qv, 64 * half, h_, r0,
+                         pol_in);
       } else {
         const int qtr = box - 6;  // g quarters
-        tma_load_3d(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, r0);
+        tma_load_3d_hint(sm + ST_G + qtr * 8192, &map_g, &bar_ld, 32 * qtr, h_, r0, pol_in);
       }
     }
   };
@@ -251,8 +252,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
   bool ok = true;
 
   int h, n, h_next = 0, n_next = 0;
-  long long tok0, tok0_next = 0;
-  bool have = locate(h, tok0, n);
+  long long tok0, tok0_next = 0, rec = 0, rec_next = 0;
+  bool have = locate(rec, h, tok0, n);
   if (have && tid == 0) stage_expect();
   __syncthreads();
   if (have) stage_issue(h, tok0);
@@ -270,9 +271,16 @@ __global__ void __launch_bounds__(kPThreads, 2)
   };
   const uint32_t tile_base = c_kb * 8192u + uint32_t(R) * 2048u;
   float blog = (have && tid < n) ? a.beta_logits[(tok0 + tid) * H + h] : 0.f;  // tid < 64
-  for (long long rec = blockIdx.x; have; rec += gridDim.x) {
+  // kAttn: the per-token decay in log2 units (0 past the chunk's end), read by every thread
+  // after the next block barrier (the staged-tile wait)
+  if constexpr (kAttn)
+    if (tid < kC)
+      s_gam[tid] = (have && tid < n && a.decay) ? a.decay[(tok0 + tid) * H + h] * kLog2E : 0.f;
+  const bool lit = kAttn && a.literal != 0;
+  const bool norm = !kAttn || a.no_l2norm == 0;
+  while (have) {
     advance();
-    const bool have_next = locate(h_next, tok0_next, n_next);
+    const bool have_next = locate(rec_next, h_next, tok0_next, n_next);
 
     // ---- loads: this record's staged k and g tiles; raw gates and k words of (16 tokens,
     //      channels c0, c0 + 1).  q and v may still be in flight.
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     const uint8_t* gsrc = sm + ST_G + (c0 >> 5) * 8192 + (16 * R) * 128 + (c0 & 31) * 4;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      graw[i] = *reinterpret_cast<const float2*>(gsrc + i * 128);
+      if constexpr (!kAttn) graw[i] = *reinterpret_cast<const float2*>(gsrc + i * 128);
       kw[i] = *reinterpret_cast<const uint32_t*>(sm + ST_K + tile_base + swz(i));
     }
     if (n < kC) {  // partial chunk (uniform): rows past n belong to the next sequence
@@ -301,28 +309,44 @@ __global__ void __launch_bounds__(kPThreads, 2)
     }
 
     // ---- gate prefix over this thread's sub-chunk, beta
-    // the gate in log2 units: gamma log2 e = lb2 / (1 + 2^(na2 (g + dt_bias)))
-    const float na2 = -__expf(a.a_log[h]) * kLog2E;
-    const float cb0 = na2 * a.dt_bias[c0 * H + h], cb1 = na2 * a.dt_bias[(c0 + 1) * H + h];
-    const float lb2 = a.lower_bound * kLog2E;
-    float loc0[16], loc1[16];  // (G_t - P_R) log2 e for channels c0, c0 + 1
-    {
-      float r0 = 0.f, r1 = 0.f;
+    float2 loc[16];  // (G_t - P_R) log2 e for channels (c0, c0 + 1), packed pairs
+    if constexpr (kAttn) {  // one decay per token, the same on both channels
+      float run = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        float g0 = 0.f, g1 = 0.f;
-        if (16 * R + i < n) {
-          g0 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(na2, graw[i].x, cb0)));
-          g1 = lb2 * fast_rcp(1.f + fast_exp2(fmaf(na2, graw[i].y, cb1)));
-        }
-        r0 += g0;
-        r1 += g1;
-        loc0[i] = r0;
-        loc1[i] = r1;
+        run += s_gam[16 * R + i];
+        loc[i] = make_float2(run, run);
       }
-      *reinterpret_cast<float2*>(&s_gtot[R][c0]) = make_float2(r0, r1);
+      *reinterpret_cast<float2*>(&s_gtot[R][c0]) = make_float2(run, run);
+    } else {
+      // the gate in log2 units: gamma log2 e = lb2 / (1 + 2^(na2 (g + dt_bias)))
+      const float na2 = -__expf(a.a_log[h]) * kLog2E;
+      const float cb0 = na2 * a.dt_bias[c0 * H + h], cb1 = na2 * a.dt_bias[(c0 + 1) * H + h];
+      const float lb2 = a.lower_bound * kLog2E;
+      // channel pairs ride Blackwell's two-lane fp32 instructions.  Tokens past a partial
+      // chunk's end (their raw gate zeroed above, their k and q zero) run through the same
+      // instructions: their gates lie in [lower_bound, 0] like every other, so their factors
+      // stay in range, and the sub-chunk total stops at the last live token.
+      const float2 na2v = make_float2(na2, na2), cbv = make_float2(cb0, cb1);
+      const float2 one = make_float2(1.f, 1.f), lbv = make_float2(lb2, lb2);
+      float2 run = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 x = __ffma2_rn(na2v, graw[i], cbv);
+        const float2 den = __fadd2_rn(one, make_float2(fast_exp2(x.x), fast_exp2(x.y)));
+        run = __ffma2_rn(lbv, make_float2(fast_rcp(den.x), fast_rcp(den.y)), run);
+        loc[i] = run;
+      }
+      if (n < kC) {
+        const int live = n - 16 * R;  // live tokens of this sub-chunk (may be <= 0)
+        run = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < live) run = loc[i];
+      }
+      *reinterpret_cast<float2*>(&s_gtot[R][c0]) = run;
     }
-    if (tid < kC) s_beta[tid] = (tid < n) ? sigmoidf_(blog) : 0.f;
+    if (tid < kC) s_beta[tid] = (tid < n) ? (kAttn ? blog : sigmoidf_(blog)) : 0.f;
 
     // transposed [128 x 64] tile rows c0, c0 + 1 (tokens contiguous): row c0 takes the low
     // halves, row c0 + 1 the high halves; lanes 4..7 of every 8-lane group write row c0 + 1
@@ -365,7 +389,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
 
     // ---- |q_t|^2: this thread's two channels, then a reduce-scatter over the warp's 32
     //      channel pairs (lanes l and l ^ 1 end with the same token); two warps per token.
-    {
+    if (norm) {
       float v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -429,6 +453,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
       uint8_t* const p128 = sm + P_XL + c_kb * 16384u + uint32_t(R) * 2048u;
       uint8_t* const p160 = sm + P_KB + c_kb * 20480u + uint32_t(R) * 2048u;
       __nv_bfloat16* const qrec = ws.qw + (rec * 64 + 16 * R) * kD + c0;  // Q~ row 16 R
+      // literal order: the key side takes e^{G_{t-1} - P_R}, the previous token's factor
+      // (1 for the sub-chunk's first token)
+      uint32_t e2_prev = 0x3F803F80u;  // bf16 pair (1, 1)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t khw[8], ktw[8];
@@ -437,10 +464,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
           const int i = 8 * hf + ii;
           const uint32_t swi = uint32_t(hf * 1024 + ii * 128) +
                                (((c_chunk ^ uint32_t(ii)) << 4) | c_byte);
-          const float e0 = fast_exp2(loc0[i]), e1 = fast_exp2(loc1[i]);  // e^{G_t - P_R}
+          const float e0 = fast_exp2(loc[i].x), e1 = fast_exp2(loc[i].y);  // e^{G_t - P_R}
           const uint32_t e2 = pack_bf16(e0, e1);
           const uint32_t i2 = pack_bf16(fast_rcp(e0), fast_rcp(e1));  // e^{P_R - G_t}
-          const uint32_t xk = hmul2(kw[i], e2), xq = hmul2(qw[i], e2), kd = hmul2(kw[i], i2);
+          const uint32_t xk = hmul2(kw[i], lit ? e2_prev : e2);
+          const uint32_t xq = hmul2(qw[i], e2), kd = hmul2(kw[i], i2);
+          e2_prev = e2;
           *reinterpret_cast<uint32_t*>(p128 + swi) = xk;             // Xl row t
           *reinterpret_cast<uint32_t*>(p128 + swi + 8 * 1024) = xq;  // Xl row 64 + t
           *reinterpret_cast<uint32_t*>(p160 + swi) = kd;             // Kb diagonal row t
@@ -457,7 +486,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
             *reinterpret_cast<uint32_t*>(qrec + i * kD) = hmul2(xq, eP2);  // q e^{G_t}
           }
           khw[ii] = hmul2(kd, eCP2);  // k e^{G_C - G_t}
-          ktw[ii] = hmul2(xk, eP2);   // k e^{G_t}
+          ktw[ii] = hmul2(xk, eP2);   // k e^{G_t} (literal order: k e^{G_{t-1}})
         }
         store_t8(P_KTT, ktw, 2 * R + hf);
         // K^^T record rows c0, c0 + 1, tokens 16 R + 8 hf .. + 7
@@ -505,17 +534,25 @@ __global__ void __launch_bounds__(kPThreads, 2)
     fence_async_smem();
 
     // ---- norms: |k_r|^2 = A_raw[r][r] (diagonal of D1); |q_r|^2 from the reduction
+    //      (kAttn without L2 norm: rk = 1, rq = scale; literal order: the diagonal holds
+    //      |k_r|^2 e^{-gamma_r})
     if (warp < 2) {
-      float v32[32];
-      tmem_ld32(tl + P_TM_D1 + 32 * warp, v32);
-      float nn = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) nn = (i == lane) ? v32[i] : nn;
       const int r = 32 * warp + lane;
-      s_rk[r] = (r < n) ? rsqrtf(nn + kL2Eps) : 0.f;
+      if (norm) {
+        float v32[32];
+        tmem_ld32(tl + P_TM_D1 + 32 * warp, v32);
+        float nn = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) nn = (i == lane) ? v32[i] : nn;
+        if (lit) nn *= fast_exp2(s_gam[r]);
+        s_rk[r] = (r < n) ? rsqrtf(nn + kL2Eps) : 0.f;
+      } else {
+        s_rk[r] = (r < n) ? 1.f : 0.f;
+      }
     } else if (warp < 4) {
       const int r = tid - 64;
-      s_rq[r] = (r < n) ? a.scale * rsqrtf(s_qq[0][r] + s_qq[1][r] + kL2Eps) : 0.f;
+      s_rq[r] = (r < n) ? a.scale * (norm ? rsqrtf(s_qq[0][r] + s_qq[1][r] + kL2Eps) : 1.f)
+                        : 0.f;
     }
     __syncthreads();
     if (tma_thread) {
@@ -551,17 +588,20 @@ __global__ void __launch_bounds__(kPThreads, 2)
         }
       }
       if (ln < 64) {
+        // L = diag(beta rk) A diag(rk).  The solve reads only L's strictly lower triangle,
+        // so the entries on and above the diagonal are written as they come (finite), with
+        // no mask.
         const float sr = s_beta[r] * s_rk[r];
+        const float2 srv = make_float2(sr, sr);
         float* L = reinterpret_cast<float*>(sm + P_L) + r * LDL + 16 * q;
 #pragma unroll
         for (int m4 = 0; m4 < 4; ++m4) {
           const float4 rk4 = *reinterpret_cast<const float4*>(&s_rk[16 * q + 4 * m4]);
-          float4 o;
-          o.x = (16 * q + 4 * m4 + 0 < r) ? sr * rk4.x * v[4 * m4 + 0] : 0.f;
-          o.y = (16 * q + 4 * m4 + 1 < r) ? sr * rk4.y * v[4 * m4 + 1] : 0.f;
-          o.z = (16 * q + 4 * m4 + 2 < r) ? sr * rk4.z * v[4 * m4 + 2] : 0.f;
-          o.w = (16 * q + 4 * m4 + 3 < r) ? sr * rk4.w * v[4 * m4 + 3] : 0.f;
-          reinterpret_cast<float4*>(L)[m4] = o;
+          const float2 lo = __fmul2_rn(__fmul2_rn(srv, make_float2(rk4.x, rk4.y)),
+                                       make_float2(v[4 * m4 + 0], v[4 * m4 + 1]));
+          const float2 hi = __fmul2_rn(__fmul2_rn(srv, make_float2(rk4.z, rk4.w)),
+                                       make_float2(v[4 * m4 + 2], v[4 * m4 + 3]));
+          reinterpret_cast<float4*>(L)[m4] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
       } else {
         uint32_t pk[8];
@@ -638,20 +678,23 @@ __global__ void __launch_bounds__(kPThreads, 2)
         const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
         const float kv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
         uint32_t pt[4], pw[4];
+        // X is exactly zero above the diagonal inside its diagonal 16 x 16 blocks (forward
+        // substitution) and unwritten in the blocks above them: one test per 8 columns
+        const bool above = (s0 >> 4) > (r >> 4);
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          const float t0v = (s0 + 2 * p <= r) ? xv[2 * p] * bv[2 * p] : 0.f;
-          const float t1v = (s0 + 2 * p + 1 <= r) ? xv[2 * p + 1] * bv[2 * p + 1] : 0.f;
+          const float t0v = above ? 0.f : xv[2 * p] * bv[2 * p];
+          const float t1v = above ? 0.f : xv[2 * p + 1] * bv[2 * p + 1];
           pt[p] = pack_bf16(t0v, t1v);
-          pw[p] = pack_bf16(t0v * kv[2 * p], t1v * kv[2 * p + 1]);
+          // -T diag(rk): MMA2 then yields -W^T, the record's sign, directly
+          pw[p] = pack_bf16(-t0v * kv[2 * p], -t1v * kv[2 * p + 1]);
         }
         const uint32_t off = sw128_offset<2>(64, r, s0);
         if constexpr (kBwd) {  // N = (I + L)^{-1}, lower triangle, row r, columns s0 .. s0 + 7
           uint32_t pn[4];
 #pragma unroll
           for (int p = 0; p < 4; ++p)
-            pn[p] = pack_bf16((s0 + 2 * p <= r) ? xv[2 * p] : 0.f,
-                              (s0 + 2 * p + 1 <= r) ? xv[2 * p + 1] : 0.f);
+            pn[p] = pack_bf16(above ? 0.f : xv[2 * p], above ? 0.f : xv[2 * p + 1]);
           *reinterpret_cast<uint4*>(ws.nrec + (rec * 64 + r) * 64 + s0) =
               make_uint4(pn[0], pn[1], pn[2], pn[3]);
         }
@@ -663,7 +706,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA2: W^T = K~^T (T diag(rk))^T, U~^T = V^T T^T  (M = 128, N = 64, K = 64)
+    // ---- MMA2: -W^T = K~^T (-T diag(rk))^T, U~^T = V^T T^T  (M = 128, N = 64, K = 64)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ts = smem_u32(sm + P_T), tw = smem_u32(sm + P_TW),
@@ -703,10 +746,10 @@ __global__ void __launch_bounds__(kPThreads, 2)
 #pragma unroll
       for (int p = 0; p < 4; ++p)
         *reinterpret_cast<uint4*>(wrow + (((4 * wg + p) ^ (ln & 7)) << 4)) =
-            make_uint4(pack_bf16(-w32[8 * p + 0], -w32[8 * p + 1]),
-                       pack_bf16(-w32[8 * p + 2], -w32[8 * p + 3]),
-                       pack_bf16(-w32[8 * p + 4], -w32[8 * p + 5]),
-                       pack_bf16(-w32[8 * p + 6], -w32[8 * p + 7]));
+            make_uint4(pack_bf16(w32[8 * p + 0], w32[8 * p + 1]),
+                       pack_bf16(w32[8 * p + 2], w32[8 * p + 3]),
+                       pack_bf16(w32[8 * p + 4], w32[8 * p + 5]),
+                       pack_bf16(w32[8 * p + 6], w32[8 * p + 7]));
       float u32[32];
       tmem_ld32(tl + P_TM_DU + 32 * wg, u32);
       // piece P = 4 wg + p of row ln (tokens 8 P .. 8 P + 7) at piece-major position
@@ -726,11 +769,16 @@ __global__ void __launch_bounds__(kPThreads, 2)
       tma_store_2d(&map_ku, sm + P_W, 0, (int)((2 * ws.recs + rec) * 128));
       bulk_commit();
     }
+    rec = rec_next;
     h = h_next;
     tok0 = tok0_next;
     n = n_next;
     have = have_next;
     blog = (have && tid < n) ? a.beta_logits[(tok0 + tid) * H + h] : 0.f;
+    if constexpr (kAttn)
+      if (tid < kC)
+        s_gam[tid] = (have && tid < n && a.decay) ? a.decay[(tok0 + tid) * H + h] * kLog2E
+                                                  : 0.f;
   }
 
   if (!ok) {
@@ -844,19 +892,37 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   // the refill of stage st with chunk ch, its boxes spread over lane 0 of warps 1..7 (the
   // expected bytes were registered by thread 0 with the MMAs that last read the stage)
+  // (the forward reads each record once: evict-first L2 policy)
+  const uint64_t pol_rec = policy_evict_first();
   auto issue_load_spread = [&](int ch, int st) {
     if ((tid & 31) != 0 || warp == 0 || warp > 7) return;
     const long long rec = (slot0 + ch) * H + h;
     uint8_t* b = sm + st * kStage;
     uint64_t* bar = &bar_ld[st];
     switch (warp) {
-      case 1: tma_load_2d(b + S_W, &map_ku, bar, 0, (int)((2 * ws.recs + rec) * 128)); break;
-      case 2: tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128)); break;
-      case 3: bulk_load(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar); break;
-      case 4: bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar); break;
-      case 5: if (want_out) tma_load_2d(b + S_Q, &map_qw, bar, 0, (int)(rec * 64)); break;
-      case 6: if (want_out) tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, (int)(rec * 64)); break;
-      default: if (want_out) tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64)); break;
+      case 1: tma_load_2d_hint(b + S_W, &map_ku, bar, 0, (int)((2 * ws.recs + rec) * 128), pol_rec); break;
+      case 2: tma_load_2d_hint(b + S_KT, &map_ku, bar, 0, (int)(rec * 128), pol_rec); break;
+      case 3: bulk_load_hint(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar, pol_rec); break;
+      case 4: bulk_load_hint(b + S_V, ws.vec + rec * 256, 1024, bar, pol_rec); break;
+      case 5: if (want_out) tma_load_2d_hint(b + S_Q, &map_qw, bar, 0, (int)(rec * 64), pol_rec); break;
+      case 6: if (want_out) tma_load_2d_hint(b + S_Q + 8192, &map_qw, bar, 64, (int)(rec * 64), pol_rec); break;
+      default: if (want_out) tma_load_2d_hint(b + S_M, &map_m, bar, 0, (int)(rec * 64), pol_rec); break;
+    }
+  };
+  // The forward's records are dead once a chunk step has consumed them: their L2 lines
+  // (584 lines of 128 bytes per record) are dropped without a write-back.  Only the
+  // forward (kMode 0) does this; the backward modes keep their records for later launches.
+  auto discard_record = [&](int ch) {
+    const long long rec = (slot0 + ch) * H + h;
+    for (int l = tid; l < 584; l += kSThreads) {
+      const uint8_t* p;
+      if (l < 128) p = reinterpret_cast<const uint8_t*>(ws.qw + rec * 8192) + l * 128;
+      else if (l < 256) p = reinterpret_cast<const uint8_t*>(ws.ku + rec * 8192) + (l - 128) * 128;
+      else if (l < 384) p = reinterpret_cast<const uint8_t*>(ws.ku + (ws.recs + rec) * 8192) + (l - 256) * 128;
+      else if (l < 512) p = reinterpret_cast<const uint8_t*>(ws.ku + (2 * ws.recs + rec) * 8192) + (l - 384) * 128;
+      else if (l < 576) p = reinterpret_cast<const uint8_t*>(ws.m + rec * 4096) + (l - 512) * 128;
+      else p = reinterpret_cast<const uint8_t*>(ws.vec + rec * 256) + (l - 576) * 128;
+      discard_l2_line(p);
     }
   };
   // one chunk record into stage st
@@ -964,6 +1030,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       for (int i = 0; i < 32; ++i) S[i] *= vec[32 * wg + i];
       tmem_st32(tl + S_TM_S + 32 * wg, S);
     }
+    // (and drop the previous chunk's record from L2 while the tensor cores work)
+    if constexpr (kMode == 0)
+      if (ch > 0) discard_record(ch - 1);
     if (!(ok = mma_wait())) break;
     tc_fence_after();
     // ---- U'^T = diag(rk) (U~ + D_U) -> bf16 A operand: thread (j = ln, tokens 16 wg .. + 15)
@@ -1080,6 +1149,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // ---- end of chunk
   }
 
+  if constexpr (kMode == 0)
+    if (ok && nck > 0) discard_record(nck - 1);
   if (!ok) {
     if (tid == 0) {
       atomicOr(&g_split_error, 2u);
@@ -1181,14 +1252,18 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
       !make_map_out(&mo, ws.bwd == 1 ? a.q : a.out, map_rows, a.H) ||
       !make_map_in(&mq, a.q, map_rows, a.H, false) ||
       !make_map_in(&mk, a.k, map_rows, a.H, false) ||
-      !make_map_in(&mv, a.v, map_rows, a.H, false) || !make_map_in(&mg, a.g, map_rows, a.H, true))
+      !make_map_in(&mv, a.v, map_rows, a.H, false) ||
+      // (the attention variant stages no gate tiles: its unused map is laid over q)
+      !make_map_in(&mg, a.g ? (const void*)a.g : a.q, map_rows, a.H, a.g != nullptr))
     return cudaErrorInvalidValue;
   // the per-chunk images of the backward records (laid over q when there are none)
   if (!make_map_2d(&ms0, ws.bwd ? (const void*)ws.s0 : a.q, ws.bwd ? rec_rows * 128 : 1, 128,
                    128) ||
       !make_map_2d(&mut, ws.bwd ? (const void*)ws.ut : a.q, ws.bwd ? rec_rows * 128 : 1, 64, 128))
     return cudaErrorInvalidValue;
-  auto prep = ws.bwd ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+  auto prep = ws.bwd ? chunk_prep_kernel<true, false>
+                     : a.gate_head ? chunk_prep_kernel<false, true>
+                                   : chunk_prep_kernel<false, false>;
   auto scan = ws.bwd == 0 ? chunk_scan_kernel<0> : ws.bwd == 1 ? chunk_scan_kernel<1>
                                                                 : chunk_scan_kernel<2>;
   const size_t scan_smem = ws.bwd ? kSSmemBwd : kSSmem;

@@ -101,6 +101,13 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
                              bool saved, cudaStream_t stream);
 unsigned int chunk_bwd_read_error(bool reset);
 cudaError_t launch_gla(const GlaArgs& a, bool bf16, cudaStream_t stream);
+// Chunked tensor-core form of the same recurrence (key-axis gates only, bf16, D = 128,
+// forward order): per-chunk prep over all chunks, then the state pass, through a workspace.
+bool gla_chunk_supported(const GlaArgs& a, bool bf16);
+size_t gla_chunk_workspace(const GlaArgs& a);
+bool gla_chunk_index_ok(const GlaArgs& a);
+cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t stream);
+unsigned int gla_chunk_read_error(bool reset);
 // One bounded wait on a barrier nothing arrives on (the give-up path of every kernel wait).
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
 unsigned int selftest_read_error(bool reset);

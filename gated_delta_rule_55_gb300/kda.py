@@ -28,7 +28,10 @@ EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_varlen", "kda_chunk_fwd_workspace_siz
            "kda_chunk_fwd_noalloc", "kda_chunk_bwd_workspace_size", "kda_chunk_bwd",
            "kda_chunk_bwd_varlen_workspace_size", "kda_chunk_bwd_varlen",
            "kda_chunk_fwd_train_varlen", "kda_chunk_bwd_saved_varlen",
-           "kda_chunk_fwd_train", "kda_chunk_bwd_saved", "kda_recurrent_attention_fwd", "kda_attention_fwd", "kda_decode_step",
+           "kda_chunk_fwd_train", "kda_chunk_bwd_saved", "kda_recurrent_attention_fwd", "kda_attention_fwd",
+           "kda_attention_fwd_ws", "kda_attention_fwd_workspace_size",
+           "kda_recurrent_attention_fwd_ws", "kda_recurrent_attention_fwd_workspace_size",
+           "kda_decode_step",
            "kda_status_string",
            "kda_version", "kda_device_error", "kda_selftest_bounded_wait")
 KDA_ATTN_NO_QK_L2NORM = 1
@@ -72,6 +75,10 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_fwd_varlen_ws.argtypes = L.kda_chunk_fwd_varlen.argtypes[:-1] + [_P, _Z, _P]
     L.kda_chunk_fwd_noalloc.argtypes = L.kda_chunk_fwd.argtypes
     L.kda_recurrent_attention_fwd.argtypes = ([_P] * 7 + [_F] + [_P] * 4 + [_I] * 8 + [_P])
+    L.kda_recurrent_attention_fwd_ws.argtypes = ([_P] * 7 + [_F] + [_P] * 4 + [_I] * 8 +
+                                                 [_P, _Z, _P])
+    L.kda_recurrent_attention_fwd_workspace_size.argtypes = [_I] * 8
+    L.kda_recurrent_attention_fwd_workspace_size.restype = _Z
     L.kda_chunk_bwd_workspace_size.argtypes = [_I] * 6
     L.kda_chunk_bwd_workspace_size.restype = _Z
     L.kda_chunk_bwd.argtypes = ([_P] * 7 + [_F, _F] + [_P] * 11 + [_I] * 6 + [_P, _Z, _P])
@@ -85,6 +92,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     L.kda_chunk_fwd_train.argtypes = L.kda_chunk_fwd_ws.argtypes
     L.kda_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
                                     _I, _I, _P]
+    L.kda_attention_fwd_ws.argtypes = L.kda_attention_fwd.argtypes[:-1] + [_P, _Z, _P]
+    L.kda_attention_fwd_workspace_size.argtypes = [_I] * 8
+    L.kda_attention_fwd_workspace_size.restype = _Z
     L.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P,
                                   _I, _I, _I, _I, _P]
     L.kda_device_error.argtypes = [_I]
@@ -94,7 +104,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
               "kda_chunk_fwd_varlen_ws", "kda_chunk_fwd_noalloc", "kda_chunk_bwd",
               "kda_chunk_bwd_saved", "kda_chunk_fwd_train", "kda_chunk_bwd_varlen",
               "kda_chunk_fwd_train_varlen", "kda_chunk_bwd_saved_varlen",
-              "kda_attention_fwd", "kda_recurrent_attention_fwd",
+              "kda_attention_fwd", "kda_attention_fwd_ws", "kda_recurrent_attention_fwd",
+              "kda_recurrent_attention_fwd_ws",
               "kda_decode_step", "kda_version", "kda_device_error"):
         getattr(L, f).restype = _I
     L.kda_status_string.argtypes = [_I]
@@ -337,6 +348,33 @@ def kda_recurrent_attention_fwd(query, key, value, out, B, T, Hq, Hkv, D, g=None
         _stream(stream)))
 
 
+KDA_REC_PACKED, KDA_REC_VALUE_GATE, KDA_REC_REVERSE = 1, 2, 4  # include/kda.h
+
+
+def kda_recurrent_attention_fwd_workspace_size(B, T, Hq, Hkv, D, N=0, packed=False,
+                                               value_gate=False, reverse=False,
+                                               dtype=KDA_BF16):
+    """Bytes of workspace kda_recurrent_attention_fwd_ws needs (0: none; see include/kda.h)."""
+    flags = ((KDA_REC_PACKED if packed else 0) | (KDA_REC_VALUE_GATE if value_gate else 0) |
+             (KDA_REC_REVERSE if reverse else 0))
+    return int(lib().kda_recurrent_attention_fwd_workspace_size(N, B, T, Hq, Hkv, D, flags,
+                                                                dtype))
+
+
+def kda_recurrent_attention_fwd_ws(query, key, value, out, B, T, Hq, Hkv, D, g=None,
+                                   g_gamma=None, gk=None, gv=None, softmax_scale=None,
+                                   initial_state=None, final_state=None, cu_seqlens=None, N=0,
+                                   reverse=False, dtype=None, workspace=None, stream=None):
+    """kda_recurrent_attention_fwd through a caller workspace (chunked tensor-core path; see
+    include/kda.h)."""
+    wp, wb = _ws(workspace)
+    _check("kda_recurrent_attention_fwd_ws", lib().kda_recurrent_attention_fwd_ws(
+        _ptr(query), _ptr(key), _ptr(value), _ptr(g), _ptr(g_gamma), _ptr(gk), _ptr(gv),
+        float(softmax_scale or 0.0), _ptr(initial_state), _ptr(out), _ptr(final_state),
+        _ptr(cu_seqlens), N, B, T, Hq, Hkv, D, int(bool(reverse)), _dtype_code(query, dtype),
+        wp, wb, _stream(stream)))
+
+
 def kda_attention_fwd(query, key, value, beta, decay, initial_state, out, final_state, B, T, H,
                       dk, dv, softmax_scale=None, chunk=64, use_qk_l2norm=True,
                       use_chunked=True, order="decay_first", dtype=None, stream=None):
@@ -349,6 +387,32 @@ def kda_attention_fwd(query, key, value, beta, decay, initial_state, out, final_
         _ptr(query), _ptr(key), _ptr(value), _ptr(beta), _ptr(decay), _ptr(initial_state),
         _ptr(out), _ptr(final_state), float(softmax_scale or 0.0), B, T, H, dk, dv, chunk,
         flags, _dtype_code(query, dtype), _stream(stream)))
+
+
+def _attn_flags(use_qk_l2norm, use_chunked, order):
+    return ((0 if use_qk_l2norm else KDA_ATTN_NO_QK_L2NORM) |
+            (0 if use_chunked else KDA_ATTN_RECURRENT) |
+            {"decay_first": 0, "literal": KDA_ATTN_ORDER_LITERAL}[order])
+
+
+def kda_attention_fwd_workspace_size(B, T, H, dk, dv, chunk=64, use_qk_l2norm=True,
+                                     use_chunked=True, order="decay_first", dtype=KDA_BF16):
+    """Bytes of workspace kda_attention_fwd_ws needs (0: none; see include/kda.h)."""
+    return int(lib().kda_attention_fwd_workspace_size(
+        B, T, H, dk, dv, chunk, _attn_flags(use_qk_l2norm, use_chunked, order), dtype))
+
+
+def kda_attention_fwd_ws(query, key, value, beta, decay, initial_state, out, final_state, B, T,
+                         H, dk, dv, softmax_scale=None, chunk=64, use_qk_l2norm=True,
+                         use_chunked=True, order="decay_first", dtype=None, workspace=None,
+                         stream=None):
+    """kda_attention_fwd through a caller workspace (tensor-core path; see include/kda.h)."""
+    wp, wb = _ws(workspace)
+    _check("kda_attention_fwd_ws", lib().kda_attention_fwd_ws(
+        _ptr(query), _ptr(key), _ptr(value), _ptr(beta), _ptr(decay), _ptr(initial_state),
+        _ptr(out), _ptr(final_state), float(softmax_scale or 0.0), B, T, H, dk, dv, chunk,
+        _attn_flags(use_qk_l2norm, use_chunked, order), _dtype_code(query, dtype), wp, wb,
+        _stream(stream)))
 
 
 def kda_decode_step(q, k, v, g, beta_logits, a_log, dt_bias, scale, lower_bound, out, S,

@@ -324,12 +324,37 @@ enum kda_attention_flags {
  *   flags       kda_attention_flags; unknown bits give KDA_ERR_FLAGS
  *   The recurrence is kda_chunk_fwd's with gamma = decay[t, h] on every channel and beta
  *   taken as given.  Runs on the fp32 SIMT kernels (chunked, 16-token chunks, or the
- *   sequential scan).
+ *   sequential scan); kda_attention_fwd_ws below runs the bf16 dk = dv = 128 chunked call on
+ *   the tensor cores.
  */
 int kda_attention_fwd(const void* query, const void* key, const void* value, const float* beta,
                       const float* decay, const float* initial_state, void* out,
                       float* final_state, float softmax_scale, int B, int T, int H, int dk,
                       int dv, int chunk, int flags, int dtype, kda_stream_t stream);
+
+/*
+ * kda_attention_fwd_workspace_size / kda_attention_fwd_ws -- kda_attention_fwd through a
+ *   caller workspace (same arguments, layouts, results and errors, plus the workspace).  For
+ *   bf16 with dk = dv = 128, chunk = 64 and the chunked mode (no KDA_ATTN_RECURRENT) it runs
+ *   on the two-launch tensor-core path of kda_chunk_fwd_ws -- every chunk's
+ *   state-independent part for all chunks at once, then the sequential pass over the state
+ *   (kernel_delta_attention page, "Algorithm modes": chunked, parallel within chunks) --
+ *   with the call's own variants: the per-head log-decay on every channel, beta as given,
+ *   use_qk_l2norm and the literal order.  On that path the decay must lie in [-5, 1] (the
+ *   page asks for decays <= 0): 64-token chunks keep their factorised exponentials inside
+ *   the fp32 range only there; outside it the results are unspecified (no fault).  Every
+ *   other configuration ignores the workspace and runs kda_attention_fwd's kernels.
+ *   workspace: at least kda_attention_fwd_workspace_size(B, T, H, dk, dv, chunk, flags,
+ *   dtype) bytes (0: none needed), 256-byte aligned, caller-owned, contents unspecified on
+ *   return; a smaller or misaligned buffer gives KDA_ERR_WORKSPACE.
+ */
+size_t kda_attention_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
+                                        int flags, int dtype);
+int kda_attention_fwd_ws(const void* query, const void* key, const void* value,
+                         const float* beta, const float* decay, const float* initial_state,
+                         void* out, float* final_state, float softmax_scale, int B, int T, int H,
+                         int dk, int dv, int chunk, int flags, int dtype, void* workspace,
+                         size_t workspace_bytes, kda_stream_t stream);
 
 /*
  * kda_recurrent_attention_fwd -- the recurrent_attention call of the ejkernel "recurrent"
@@ -357,6 +382,39 @@ int kda_recurrent_attention_fwd(const void* query, const void* key, const void* 
                                 void* out, float* final_state, const int32_t* cu_seqlens, int N,
                                 int B, int T, int Hq, int Hkv, int D, int reverse, int dtype,
                                 kda_stream_t stream);
+
+/* Shape options of kda_recurrent_attention_fwd_workspace_size (bitwise OR). */
+enum kda_recurrent_flags {
+  KDA_REC_PACKED = 1,      /* cu_seqlens given: N packed sequences, B = 1, T = packed tokens */
+  KDA_REC_VALUE_GATE = 2,  /* gv given */
+  KDA_REC_REVERSE = 4      /* reverse != 0 */
+};
+
+/*
+ * kda_recurrent_attention_fwd_workspace_size / kda_recurrent_attention_fwd_ws --
+ *   kda_recurrent_attention_fwd through a caller workspace (same arguments, layouts, results
+ *   and errors, plus the workspace).  For bf16 with D = 128, the key-axis gates only (gv
+ *   NULL) and forward order it runs the recurrence in its chunked form on the tensor cores
+ *   (64-token chunks: every chunk's gate-scaled product q k^T and its records at once, then
+ *   the sequential pass over the state; the recurrent page's run parameters g, gk, g_gamma,
+ *   cu_seqlens).  On that path the summed key-axis gate g + gk + g_gamma must lie in
+ *   [-5, 1] at every token and channel, where the chunks' factorised exponentials stay inside
+ *   the fp32 range; outside it the results are unspecified (no fault).  Every other
+ *   configuration ignores the workspace and runs the token-serial kernel.
+ *   workspace: at least kda_recurrent_attention_fwd_workspace_size(N, B, T, Hq, Hkv, D,
+ *   flags, dtype) bytes (flags: kda_recurrent_flags describing the call; 0: none needed),
+ *   256-byte aligned, caller-owned, contents unspecified on return; a smaller or misaligned
+ *   buffer gives KDA_ERR_WORKSPACE.  About 41 KB per (64-token chunk, query head).
+ */
+size_t kda_recurrent_attention_fwd_workspace_size(int N, int B, int T, int Hq, int Hkv, int D,
+                                                  int flags, int dtype);
+int kda_recurrent_attention_fwd_ws(const void* query, const void* key, const void* value,
+                                   const float* g, const float* g_gamma, const float* gk,
+                                   const float* gv, float softmax_scale,
+                                   const float* initial_state, void* out, float* final_state,
+                                   const int32_t* cu_seqlens, int N, int B, int T, int Hq,
+                                   int Hkv, int D, int reverse, int dtype, void* workspace,
+                                   size_t workspace_bytes, kda_stream_t stream);
 
 /*
  * kda_decode_step -- advance the recurrence by exactly one token for B requests, in the
@@ -389,7 +447,9 @@ int kda_version(void);
  *   Bit 0: a bounded wait inside the single-pass tensor-core chunk kernel gave up; bit 1:
  *   one inside the two-launch (workspace) chunk kernels did; bit 2: one inside the
  *   chunked backward's kernels did (the outputs of that launch are incomplete); bit 3: the
- *   wait of kda_selftest_bounded_wait gave up (which is what it is for).  Synchronises the device.  reset != 0 clears the mask.
+ *   wait of kda_selftest_bounded_wait gave up (which is what it is for); bit 4: one inside
+ *   the chunked recurrent-attention kernels did.  Synchronises the device.  reset != 0
+ *   clears the mask.
  *   Returns the mask (>= 0) or KDA_ERR_DEVICE.
  */
 int kda_device_error(int reset);

@@ -162,3 +162,35 @@ def decode_chain(ex, tokens, a_log, dt_bias, scale, lower_bound, S0, workers=Non
         outs[:, :, h0:h1] = o
         state[:, h0:h1] = s
     return outs, state
+
+
+def recurrent(ex, query, key, value, g=None, g_gamma=None, gk=None, gv=None,
+              softmax_scale=None, initial_state=None, workers=None):
+    """``recurrent_attention`` (forward order, fixed-length sequences) over
+    ``[B, T, Hq, D]`` inputs, one task per (batch element, range of query heads); each range
+    covers whole groups of query heads sharing a key / value head.  Same return value as
+    ``recurrent_attention``."""
+    B, T, Hq, D = np.shape(query)
+    Hkv = np.shape(key)[2]
+    grp = Hq // Hkv
+    per = max(1, (Hkv * B) // max(1, workers or default_workers()))
+    per = min(Hkv, per)
+    tasks, where = [], []
+    for b in range(B):
+        for k0 in range(0, Hkv, per):
+            k1 = min(Hkv, k0 + per)
+            h0, h1 = k0 * grp, k1 * grp
+            sl = lambda x: None if x is None else x[b:b + 1, :, h0:h1]  # noqa: E731
+            tasks.append(dict(
+                query=query[b:b + 1, :, h0:h1], key=key[b:b + 1, :, k0:k1],
+                value=value[b:b + 1, :, k0:k1], g=sl(g), gk=sl(gk), gv=sl(gv),
+                g_gamma=None if g_gamma is None else g_gamma[b:b + 1, h0:h1],
+                softmax_scale=softmax_scale,
+                initial_state=None if initial_state is None else initial_state[b:b + 1, h0:h1]))
+            where.append((b, h0, h1))
+    out = np.zeros((B, T, Hq, D))
+    state = np.zeros((B, Hq, D, D))
+    for (b, h0, h1), (o, s) in zip(where, _run(ex, "recurrent_attention", tasks)):
+        out[b, :, h0:h1] = o[0]
+        state[b, h0:h1] = s[0]
+    return out, state

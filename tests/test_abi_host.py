@@ -202,6 +202,42 @@ def test_attention_without_device(L):
         assert _attn(L, flags=flags) == -9
 
 
+def _attn_ws(L, ws, nbytes, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, decay=None, s0=None, out=FAKE, s1=None,
+             scale=0.0, B=1, T=64, H=2, dk=128, dv=128, chunk=64, flags=0, dtype=1)
+    a.update(over)
+    return L.kda_attention_fwd_ws(a["q"], a["k"], a["v"], a["beta"], a["decay"], a["s0"],
+                                  a["out"], a["s1"], a["scale"], a["B"], a["T"], a["H"], a["dk"],
+                                  a["dv"], a["chunk"], a["flags"], a["dtype"], ws, nbytes, None)
+
+
+def test_attention_ws_sizes_and_workspace_checks(L):
+    need = kda.kda_attention_fwd_workspace_size(1, 64, 2, 128, 128, 64)
+    # the same records as kda_chunk_fwd_ws: one per (64-token chunk, head)
+    assert need == kda.kda_chunk_fwd_workspace_size(1, 64, 2, 128, 128, 64, 1) > 0
+    assert kda.kda_attention_fwd_workspace_size(1, 64, 2, 128, 128, 64, use_chunked=False) == 0
+    assert kda.kda_attention_fwd_workspace_size(1, 64, 2, 128, 128, 16) == 0
+    assert kda.kda_attention_fwd_workspace_size(1, 64, 2, 64, 128, 64) == 0
+    assert kda.kda_attention_fwd_workspace_size(1, 64, 2, 128, 128, 64, dtype=0) == 0
+    assert kda.kda_attention_fwd_workspace_size(1, 0, 2, 128, 128, 64) == 0
+    for flags in (0, 1, 4, 5):  # every chunked variant needs its workspace
+        assert _attn_ws(L, None, 0, flags=flags) == -12
+        assert _attn_ws(L, 0x100000, need - 1, flags=flags) == -12
+        assert _attn_ws(L, 0x100080, need, flags=flags) == -12  # not 256-byte aligned
+    assert _attn_ws(L, None, 0, dtype=3) == -7               # argument errors first
+    assert _attn_ws(L, None, 0, flags=8) == -13
+
+
+def test_attention_ws_without_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case is only meaningful without one")
+    need = kda.kda_attention_fwd_workspace_size(1, 64, 2, 128, 128, 64)
+    assert _attn_ws(L, 0x100000, need) == -9
+    assert _attn_ws(L, None, 0, flags=2) == -9               # the recurrent mode: no workspace
+    assert _attn_ws(L, None, 0, dtype=0) == -9               # fp32: no workspace
+
+
 def _al(x):
     return (x + 255) // 256 * 256
 

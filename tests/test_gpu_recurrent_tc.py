@@ -1,0 +1,141 @@
+"""Parity of kda_recurrent_attention_fwd_ws -- the recurrent page's gated linear recurrence
+in its chunked form on the tensor cores (bf16, D = 128, key-axis gates g / gk / g_gamma,
+forward order) -- with the fp64 oracle ``recurrent_attention``: every combination of the
+key-axis gates (none, one, several), grouped key / value heads, packed sequences with empty
+and ragged members, gates from mild to the edge of the supported range [-5, 1], and the
+benchmark's full workload compared element by element.  Bar: max |gpu - oracle| /
+max |oracle| <= 2e-2 per tensor, the oracle fed the same bf16-rounded q, k, v.  Calls that
+the chunked path does not serve (a value-axis gate, reverse order) give the token-serial
+kernel's results bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_55_gb300 as kda
+from gpu_helpers import (bf16_round, bf16_round32, check_full, check_rel, ensure_built, oracle_pool,
+                         to_dev, workspace)
+from oracle import recurrent_attention
+
+pytestmark = pytest.mark.gpu
+D = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    kda.kda_device_error(reset=True)
+    yield
+    assert kda.kda_device_error(reset=True) == 0, "a bounded wait gave up"
+
+
+def _inputs(B, T, Hq, Hkv, seed, gates, state, nseq=None, lo=-0.3, hi=0.0):
+    r = np.random.default_rng(2500 + seed)
+    d = {"q": r.normal(size=(B, T, Hq, D)), "k": r.normal(size=(B, T, Hkv, D)) * D ** -0.5,
+         "v": r.normal(size=(B, T, Hkv, D))}
+    for n in ("g", "gk", "gv"):
+        d[n] = r.uniform(lo, hi, size=(B, T, Hq, D)) if n in gates else None
+    d["g_gamma"] = -r.uniform(0.0, 0.2, size=(B, Hq)) if "g_gamma" in gates else None
+    d["s0"] = r.normal(size=(nseq or B, Hq, D, D)) * 0.1 if state else None
+    return d
+
+
+def _run(d, B, T, Hq, Hkv, scale, cu=None, ws=True, reverse=False):
+    q, k, v = (to_dev(d[n], torch.bfloat16) for n in ("q", "k", "v"))
+    nseq = B if cu is None else len(cu) - 1
+    out = torch.full((B, T, Hq, D), float("nan"), device="cuda", dtype=torch.bfloat16)
+    s1 = torch.full((nseq, Hq, D, D), float("nan"), device="cuda")
+    cu_t = None if cu is None else torch.from_numpy(np.asarray(cu, np.int32)).cuda()
+    kw = dict(g=to_dev(d["g"]), g_gamma=to_dev(d["g_gamma"]), gk=to_dev(d["gk"]),
+              gv=to_dev(d["gv"]), softmax_scale=scale, initial_state=to_dev(d["s0"]),
+              final_state=s1, cu_seqlens=cu_t, N=0 if cu is None else nseq, reverse=reverse)
+    if ws:
+        nb = kda.kda_recurrent_attention_fwd_workspace_size(
+            B, T, Hq, Hkv, D, N=0 if cu is None else nseq, packed=cu is not None,
+            value_gate=d["gv"] is not None, reverse=reverse)
+        kda.kda_recurrent_attention_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, workspace=workspace(nb),
+                                           **kw)
+    else:
+        kda.kda_recurrent_attention_fwd(q, k, v, out, B, T, Hq, Hkv, D, **kw)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), s1.cpu().numpy()
+
+
+def _check(d, out, S, scale, cu=None):
+    o = dict(d)
+    for n in ("q", "k", "v"):
+        o[n] = bf16_round(d[n])
+    ro, rs = recurrent_attention(o["q"], o["k"], o["v"], o["g"], o["g_gamma"], o["gk"], o["gv"],
+                                 scale, o["s0"], False, cu)
+    check_rel(None, "out", out, ro)
+    check_rel(None, "final_state", S, rs)
+
+
+@pytest.mark.parametrize("gates", [(), ("gk",), ("g",), ("g", "gk"), ("gk", "g_gamma"),
+                                   ("g_gamma",), ("g", "gk", "g_gamma")])
+def test_gate_combinations(gates):
+    B, T, Hq, Hkv = 2, 200, 4, 2
+    d = _inputs(B, T, Hq, Hkv, len(gates), gates, True)
+    out, S = _run(d, B, T, Hq, Hkv, None)
+    _check(d, out, S, None)
+
+
+@pytest.mark.parametrize("lo,hi", [(-5.0, 0.0), (-1.0, 0.05), (-0.05, 0.0)])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 300])
+def test_gate_ranges_and_lengths(T, lo, hi):
+    B, Hq, Hkv = 1, 2, 1
+    d = _inputs(B, T, Hq, Hkv, T, ("gk",), T % 2 == 0, lo=lo, hi=hi)
+    out, S = _run(d, B, T, Hq, Hkv, 0.2)
+    _check(d, out, S, 0.2)
+
+
+def test_packed_sequences():
+    lens = [130, 0, 1, 64, 200, 63]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, Hq, Hkv = int(cu[-1]), 4, 4
+    d = _inputs(1, T, Hq, Hkv, 7, ("gk", "g_gamma"), True, nseq=len(lens))
+    out, S = _run(d, 1, T, Hq, Hkv, 0.1, cu=cu)
+    _check(d, out, S, 0.1, cu)
+    # the empty sequence keeps its state (the fp32 copy the device received)
+    np.testing.assert_array_equal(S[1], d["s0"][1].astype(np.float32))
+
+
+def test_many_records_odd_head_count():
+    """More (chunk, head) records than the prep's persistent CTAs, an odd query-head count
+    in groups of 3 per key / value head."""
+    B, T, Hq, Hkv = 2, 1000, 21, 7
+    d = _inputs(B, T, Hq, Hkv, 8, ("gk",), True)
+    out, S = _run(d, B, T, Hq, Hkv, None)
+    _check(d, out, S, None)
+
+
+@pytest.mark.parametrize("which", ["gv", "reverse"])
+def test_unserved_calls_take_the_token_serial_kernel(which):
+    B, T, Hq, Hkv = 1, 90, 2, 2
+    gates = ("gk", "gv") if which == "gv" else ("gk",)
+    d = _inputs(B, T, Hq, Hkv, 11, gates, True)
+    rev = which == "reverse"
+    assert kda.kda_recurrent_attention_fwd_workspace_size(
+        B, T, Hq, Hkv, D, value_gate=which == "gv", reverse=rev) == 0
+    o1, S1 = _run(d, B, T, Hq, Hkv, 0.3, ws=True, reverse=rev)
+    o2, S2 = _run(d, B, T, Hq, Hkv, 0.3, ws=False, reverse=rev)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+
+
+def test_benchmark_workload_full():
+    """The benchmark's workload (B=4, T=4096, Hq=32, Hkv=8, D=128, bf16, gk only ~
+    -0.05 U(0, 1), zero initial state): every element of all 128 (b, h) pairs."""
+    B, T, Hq, Hkv = 4, 4096, 32, 8
+    r = np.random.default_rng(77)
+    d = {"q": r.standard_normal((B, T, Hq, D), dtype=np.float32),
+         "k": r.standard_normal((B, T, Hkv, D), dtype=np.float32) * np.float32(D ** -0.5),
+         "v": r.standard_normal((B, T, Hkv, D), dtype=np.float32),
+         "gk": (-0.05 * r.random((B, T, Hq, D), dtype=np.float32)),
+         "g": None, "gv": None, "g_gamma": None, "s0": None}
+    out, S = _run(d, B, T, Hq, Hkv, None)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(S))
+    from oracle import pool
+    ro, rs = pool.recurrent(oracle_pool(), *(bf16_round32(d[n]) for n in ("q", "k", "v")),
+                            None, None, d["gk"], None, None, None)
+    check_full("recurrent B4 T4096 Hq32 Hkv8, gk, kda_recurrent_attention_fwd_ws",
+                         out, ro, S, rs)

@@ -46,3 +46,19 @@ def test_decode_chain_equals_consecutive_steps(ex):
     o2, s2 = pool.decode_chain(ex, toks, a_log, dt_bias, 0.25, -3.0, S, workers=3)
     np.testing.assert_allclose(o2, np.stack(outs), rtol=0, atol=1e-12)
     np.testing.assert_allclose(s2, S_ref, rtol=0, atol=1e-12)
+
+
+def test_recurrent_groups_equal_one_call(ex):
+    from oracle import recurrent_attention
+    r = np.random.default_rng(9)
+    B, T, Hq, Hkv, D = 2, 13, 6, 3, 8
+    q = r.normal(size=(B, T, Hq, D))
+    k = r.normal(size=(B, T, Hkv, D))
+    v = r.normal(size=(B, T, Hkv, D))
+    gk = -r.uniform(0, 0.5, size=(B, T, Hq, D))
+    gam = -r.uniform(0, 0.2, size=(B, Hq))
+    s0 = r.normal(size=(B, Hq, D, D))
+    o1, s1 = recurrent_attention(q, k, v, None, gam, gk, None, 0.4, s0)
+    o2, s2 = pool.recurrent(ex, q, k, v, None, gam, gk, None, 0.4, s0, workers=3)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(s2, s1, rtol=0, atol=1e-12)
