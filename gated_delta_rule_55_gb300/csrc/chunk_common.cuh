@@ -242,12 +242,6 @@ __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint3
       : "memory");
 }
 
-// Drops the 128-byte L2 line at p (128-byte aligned) without writing it back: for
-// workspace data that has been consumed and will never be read again.
-__device__ __forceinline__ void discard_l2_line(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
-}
-
 // Host: the driver's cuTensorMapEncodeTiled, looked up once through the runtime.
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -892,37 +892,19 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   // the refill of stage st with chunk ch, its boxes spread over lane 0 of warps 1..7 (the
   // expected bytes were registered by thread 0 with the MMAs that last read the stage)
-  // (the forward reads each record once: evict-first L2 policy)
-  const uint64_t pol_rec = policy_evict_first();
   auto issue_load_spread = [&](int ch, int st) {
     if ((tid & 31) != 0 || warp == 0 || warp > 7) return;
     const long long rec = (slot0 + ch) * H + h;
     uint8_t* b = sm + st * kStage;
     uint64_t* bar = &bar_ld[st];
     switch (warp) {
-      case 1: tma_load_2d_hint(b + S_W, &map_ku, bar, 0, (int)((2 * ws.recs + rec) * 128), pol_rec); break;
-      case 2: tma_load_2d_hint(b + S_KT, &map_ku, bar, 0, (int)(rec * 128), pol_rec); break;
-      case 3: bulk_load_hint(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar, pol_rec); break;
-      case 4: bulk_load_hint(b + S_V, ws.vec + rec * 256, 1024, bar, pol_rec); break;
-      case 5: if (want_out) tma_load_2d_hint(b + S_Q, &map_qw, bar, 0, (int)(rec * 64), pol_rec); break;
-      case 6: if (want_out) tma_load_2d_hint(b + S_Q + 8192, &map_qw, bar, 64, (int)(rec * 64), pol_rec); break;
-      default: if (want_out) tma_load_2d_hint(b + S_M, &map_m, bar, 0, (int)(rec * 64), pol_rec); break;
-    }
-  };
-  // The forward's records are dead once a chunk step has consumed them: their L2 lines
-  // (584 lines of 128 bytes per record) are dropped without a write-back.  Only the
-  // forward (kMode 0) does this; the backward modes keep their records for later launches.
-  auto discard_record = [&](int ch) {
-    const long long rec = (slot0 + ch) * H + h;
-    for (int l = tid; l < 584; l += kSThreads) {
-      const uint8_t* p;
-      if (l < 128) p = reinterpret_cast<const uint8_t*>(ws.qw + rec * 8192) + l * 128;
-      else if (l < 256) p = reinterpret_cast<const uint8_t*>(ws.ku + rec * 8192) + (l - 128) * 128;
-      else if (l < 384) p = reinterpret_cast<const uint8_t*>(ws.ku + (ws.recs + rec) * 8192) + (l - 256) * 128;
-      else if (l < 512) p = reinterpret_cast<const uint8_t*>(ws.ku + (2 * ws.recs + rec) * 8192) + (l - 384) * 128;
-      else if (l < 576) p = reinterpret_cast<const uint8_t*>(ws.m + rec * 4096) + (l - 512) * 128;
-      else p = reinterpret_cast<const uint8_t*>(ws.vec + rec * 256) + (l - 576) * 128;
-      discard_l2_line(p);
+      case 1: tma_load_2d(b + S_W, &map_ku, bar, 0, (int)((2 * ws.recs + rec) * 128)); break;
+      case 2: tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128)); break;
+      case 3: bulk_load(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar); break;
+      case 4: bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar); break;
+      case 5: if (want_out) tma_load_2d(b + S_Q, &map_qw, bar, 0, (int)(rec * 64)); break;
+      case 6: if (want_out) tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, (int)(rec * 64)); break;
+      default: if (want_out) tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64)); break;
     }
   };
   // one chunk record into stage st
@@ -1030,9 +1012,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
       for (int i = 0; i < 32; ++i) S[i] *= vec[32 * wg + i];
       tmem_st32(tl + S_TM_S + 32 * wg, S);
     }
-    // (and drop the previous chunk's record from L2 while the tensor cores work)
-    if constexpr (kMode == 0)
-      if (ch > 0) discard_record(ch - 1);
     if (!(ok = mma_wait())) break;
     tc_fence_after();
     // ---- U'^T = diag(rk) (U~ + D_U) -> bf16 A operand: thread (j = ln, tokens 16 wg .. + 15)
@@ -1149,8 +1128,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // ---- end of chunk
   }
 
-  if constexpr (kMode == 0)
-    if (ok && nck > 0) discard_record(nck - 1);
   if (!ok) {
     if (tid == 0) {
       atomicOr(&g_split_error, 2u);
