@@ -111,6 +111,12 @@ __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// The pair (bf16_round(x.x), bf16_round(x.y)) through one bf16x2 conversion.
+__device__ __forceinline__ float2 bf16_round2(float2 x) {
+  const uint32_t p = pack_bf16(x.x, x.y);
+  return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
   asm volatile(
@@ -800,81 +806,104 @@ __global__ void __launch_bounds__(kKThreads, 1)
     float* DKH = reinterpret_cast<float*>(sm + K_DKH);
     const float eP = fast_exp(PR), eCP = fast_exp(GC - PR);
     float dG[16];
-    float dgc = 0.f;
+    // token pairs (t, t + 1) ride Blackwell's two-lane fp32 instructions; every pair operation
+    // rounds exactly as the two scalar ones would
+    const float2 ePv = make_float2(eP, eP), neP = make_float2(-eP, -eP);
+    const float2 eCPv = make_float2(eCP, eCP);
+    float2 dgc2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int cb = 16 * R + 8 * hh;  // first token of this half
-      float e[8], ei[8], kh[8], qh[8], aq[8], pos[8], neg[8], t8[8];
+      float2 E[4], EI[4], KH[4], QH[4], AQ2[4], POS[4], NEG[4], DG[4], T[4];
+      float t8[8];
+      auto load_t = [&](uint32_t col) {
+        tmem_ld8(tl + col, t8);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int t = cb + i;
-        e[i] = fast_exp(loc[8 * hh + i]);
-        ei[i] = fast_exp(-loc[8 * hh + i]);
-        kh[i] = (t < n) ? raw_k(t) * s_rk[t] : 0.f;
-        qh[i] = (t < n) ? raw_q(t) * s_rq[t] : 0.f;
+        for (int p = 0; p < 4; ++p) T[p] = make_float2(t8[2 * p], t8[2 * p + 1]);
+      };
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int t = cb + 2 * p;
+        const float l0 = loc[8 * hh + 2 * p], l1 = loc[8 * hh + 2 * p + 1];
+        E[p] = make_float2(fast_exp(l0), fast_exp(l1));
+        EI[p] = make_float2(fast_exp(-l0), fast_exp(-l1));
+        const float2 rk2 = *reinterpret_cast<const float2*>(&s_rk[t]);
+        const float2 rq2 = *reinterpret_cast<const float2*>(&s_rq[t]);
+        KH[p] = __fmul2_rn(make_float2(raw_k(t), raw_k(t + 1)), rk2);
+        QH[p] = __fmul2_rn(make_float2(raw_q(t), raw_q(t + 1)), rq2);
+        if (t >= n) { KH[p].x = 0.f; QH[p].x = 0.f; }
+        if (t + 1 >= n) { KH[p].y = 0.f; QH[p].y = 0.f; }
       }
       // dq^, dk^ (exact gate factors) and dG; each Xl / Kb term of dG is weighted by the bf16
       // operand value the product used, so that the +G and -G terms of a pair (r, s) of the
       // gate-scaled products cancel as they do in exact arithmetic
-      float dG8[8];
-      tmem_ld8(tl + KT_P1 + cb, t8);
+      load_t(KT_P1 + cb);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        aq[i] = eP * e[i] * t8[i];
-        dG8[i] = qh[i] * aq[i];
+      for (int p = 0; p < 4; ++p) {
+        AQ2[p] = __fmul2_rn(__fmul2_rn(ePv, E[p]), T[p]);
+        DG[p] = __fmul2_rn(QH[p], AQ2[p]);
       }
-      tmem_ld8(tl + KT_P6 + 64 + cb, t8);
+      load_t(KT_P6 + 64 + cb);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        aq[i] += e[i] * t8[i];
-        dG8[i] += bf16_round(qh[i] * e[i]) * t8[i];
+      for (int p = 0; p < 4; ++p) {
+        AQ2[p] = __ffma2_rn(E[p], T[p], AQ2[p]);
+        DG[p] = __ffma2_rn(bf16_round2(__fmul2_rn(QH[p], E[p])), T[p], DG[p]);
       }
-      tmem_ld8(tl + KT_P2 + cb, t8);
+      load_t(KT_P2 + cb);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        pos[i] = -eP * e[i] * t8[i];
-        dG8[i] += kh[i] * pos[i];
+      for (int p = 0; p < 4; ++p) {
+        POS[p] = __fmul2_rn(__fmul2_rn(neP, E[p]), T[p]);
+        DG[p] = __ffma2_rn(KH[p], POS[p], DG[p]);
       }
-      tmem_ld8(tl + KT_P6 + cb, t8);
+      load_t(KT_P6 + cb);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        pos[i] += e[i] * t8[i];
-        dG8[i] += bf16_round(kh[i] * e[i]) * t8[i];
+      for (int p = 0; p < 4; ++p) {
+        POS[p] = __ffma2_rn(E[p], T[p], POS[p]);
+        DG[p] = __ffma2_rn(bf16_round2(__fmul2_rn(KH[p], E[p])), T[p], DG[p]);
       }
-      tmem_ld8(tl + KT_P3 + cb, t8);
+      load_t(KT_P3 + cb);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        neg[i] = eCP * ei[i] * t8[i];
-        dgc += kh[i] * neg[i];
-        dG8[i] -= kh[i] * neg[i];
+      for (int p = 0; p < 4; ++p) {
+        NEG[p] = __fmul2_rn(__fmul2_rn(eCPv, EI[p]), T[p]);
+        dgc2 = __ffma2_rn(KH[p], NEG[p], dgc2);
+        DG[p] = __ffma2_rn(make_float2(-KH[p].x, -KH[p].y), NEG[p], DG[p]);
       }
-      tmem_ld8(tl + KT_P7 + cb, t8);
+      // with -k (the bf16 rounding is symmetric: round(-x) = -round(x))
+      float2 NKD[4];
+      load_t(KT_P7 + cb);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float kd = kh[i] * ei[i];
-        neg[i] += ei[i] * t8[i];
-        dG8[i] -= bf16_round(kd) * t8[i];
+      for (int p = 0; p < 4; ++p) {
+        NKD[p] = __fmul2_rn(make_float2(-KH[p].x, -KH[p].y), EI[p]);
+        NEG[p] = __ffma2_rn(EI[p], T[p], NEG[p]);
+        DG[p] = __ffma2_rn(bf16_round2(NKD[p]), T[p], DG[p]);
       }
 #pragma unroll
       for (int g = 1; g < 4; ++g)
         if (g > R) {
-          tmem_ld8(tl + KT_P7 + kb_base(g) + cb, t8);
+          const float2 fgv = make_float2(fg[g], fg[g]);
+          load_t(KT_P7 + kb_base(g) + cb);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float kd = kh[i] * ei[i];
-            neg[i] += ei[i] * fg[g] * t8[i];
-            dG8[i] -= bf16_round(kd * fg[g]) * t8[i];
+          for (int p = 0; p < 4; ++p) {
+            NEG[p] = __ffma2_rn(__fmul2_rn(EI[p], fgv), T[p], NEG[p]);
+            DG[p] = __ffma2_rn(bf16_round2(__fmul2_rn(NKD[p], fgv)), T[p], DG[p]);
           }
         }
       float qd[8], kd[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float dkh = pos[i] + neg[i];
-        dG[8 * hh + i] = dG8[i];
-        AQ[(cb + i) * kD + c] = aq[i];
-        DKH[(cb + i) * kD + c] = dkh;
-        qd[i] = qh[i] * aq[i];
-        kd[i] = kh[i] * dkh;
+      for (int p = 0; p < 4; ++p) {
+        const float2 dkh = __fadd2_rn(POS[p], NEG[p]);
+        const int i = 2 * p;
+        dG[8 * hh + i] = DG[p].x;
+        dG[8 * hh + i + 1] = DG[p].y;
+        AQ[(cb + i) * kD + c] = AQ2[p].x;
+        AQ[(cb + i + 1) * kD + c] = AQ2[p].y;
+        DKH[(cb + i) * kD + c] = dkh.x;
+        DKH[(cb + i + 1) * kD + c] = dkh.y;
+        const float2 q2 = __fmul2_rn(QH[p], AQ2[p]), k2 = __fmul2_rn(KH[p], dkh);
+        qd[i] = q2.x;
+        qd[i + 1] = q2.y;
+        kd[i] = k2.x;
+        kd[i + 1] = k2.y;
       }
       int tq;
       const float qs = reduce_scatter8(qd, lane, tq);
@@ -884,6 +913,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
         s_kd[sp][cb + tq] = ks;
       }
     }
+    const float dgc = dgc2.x + dgc2.y;
     {
       float sg = 0.f;
 #pragma unroll
