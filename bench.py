@@ -53,7 +53,7 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the decode / varlen / e2e / cpu-baseline measurements")
     p.add_argument("--profile", choices=["chunk", "chunk1", "decode", "varlen", "bwd", "bwd_full",
-                                         "gla"],
+                                         "gla", "gla_chunk"],
                    default=None,
                    help="run two launches of one kernel on a reduced case (for ncu) and exit")
     return p.parse_args()
@@ -471,7 +471,7 @@ def backward_measure(w, d, x, reps=3):
                               "step_ms": ms_train_fwd + ms_saved,
                               "tokens_per_s": B * T / ((ms_train_fwd + ms_saved) * 1e-3)}}
 
-def recurrent_attention_measure(reps=3):
+def recurrent_attention_measure(reps=3, B=4, token_serial=True):
     """kda_recurrent_attention_fwd on B=4, T=4096, Hq=32, Hkv=8, D=128, bf16 q/k/v: with
     per-channel key and value gates (gk, gv fp32; the token-serial kernel), and with the key
     gate only through kda_recurrent_attention_fwd_ws (the chunked tensor-core path).  Median
@@ -479,7 +479,7 @@ def recurrent_attention_measure(reps=3):
     each once)."""
     torch = _torch()
     import gated_delta_rule_55_gb300 as kda
-    B, T, Hq, Hkv, D = 4, 4096, 32, 8, 128
+    T, Hq, Hkv, D = 4096, 32, 8, 128
     g = torch.Generator(device="cuda").manual_seed(7)
     q = torch.randn(B, T, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
     k = (torch.randn(B, T, Hkv, D, device="cuda", generator=g) * D ** -0.5).to(torch.bfloat16)
@@ -514,7 +514,7 @@ def recurrent_attention_measure(reps=3):
 
     io = B * T * (Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * 2) + B * Hq * D * D * 4
     gate = B * T * Hq * D * 4
-    ms = median_ms(both)
+    ms = median_ms(both) if token_serial else float("nan")
     ms_k = median_ms(key_only)
     return {"entry": "kda_recurrent_attention_fwd",
             "workload": "B4 T4096 Hq32 Hkv8 D128 bf16, gk + gv gates", "ms_per_call": ms,
@@ -696,13 +696,19 @@ def profile_case(which):
     build_lib.build()
     import gated_delta_rule_55_gb300 as kda
     kda.lib()
+    desc = None
     if which == "decode":
         w = synth.DECODE_B64
         decode_measure(w, 2, False)
     elif which == "gla":
-        # two kda_recurrent_attention_fwd calls on the benchmark's recurrent workload
-        w = synth.PREFILL_B4
+        # the benchmark's recurrent workload: both calls (token-serial with gk + gv, chunked
+        # with gk), two launches each
         recurrent_attention_measure(reps=1)
+        desc = "recurrent B4 T4096 Hq32 Hkv8 D128"
+    elif which == "gla_chunk":
+        # two chunked calls (gk) on a quarter of the recurrent workload (B = 1)
+        recurrent_attention_measure(reps=1, B=1, token_serial=False)
+        desc = "recurrent B1 T4096 Hq32 Hkv8 D128, chunked"
     elif which in ("bwd", "bwd_full"):
         # two kda_chunk_bwd calls: a quarter of the prefill workload's heads, or all of them
         w = replace(synth.PREFILL_B4, H=8) if which == "bwd" else synth.PREFILL_B4
@@ -715,7 +721,9 @@ def profile_case(which):
         for _ in range(2):
             call_chunk(w, x, single_pass=(which == "chunk1"))
     torch.cuda.synchronize()
-    print(f"profile case {which}: {w.name} (B={w.B}, H={w.H}) done", flush=True)
+    if desc is None:
+        desc = f"{w.name} (B={w.B}, H={w.H})"
+    print(f"profile case {which}: {desc} done", flush=True)
 
 
 # ---------------------------------------------------------------------- reference arm
