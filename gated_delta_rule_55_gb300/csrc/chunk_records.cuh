@@ -20,7 +20,7 @@ constexpr long long kRecVec = 256 * 4;          // e^{G_C}[128], rk[64], rq[64]
 constexpr long long kRecState = 128LL * 128 * 2;  // a bf16 [128 x 128] state image
 
 struct Ws {
-  __nv_bfloat16* qw;   // [recs * 64][128]: Q~ records
+  __nv_bfloat16* qw;   // Q~ records: Q~^T [recs * 128][64] (forward) or Q~ [recs * 64][128]
   // [3 * recs * 128][64]: K^^T records ([128][64] each), then U~^T records (16-byte pieces
   // stored piece-major, [8][128][8]), then -W^T records ([128][64])
   __nv_bfloat16* ku;

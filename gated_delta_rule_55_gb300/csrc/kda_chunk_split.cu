@@ -10,7 +10,8 @@
 //                      reference points), the UT solve T = (I + diag(beta) tril(A,-1))^{-1}
 //                      diag(beta) and the transform W = T diag(rk) K~, U~ = T V (tcgen05).
 //                      It writes one workspace record per (chunk, head):
-//                        Q~   = q e^{G}                     [64 tok][128]  bf16
+//                        Q~^T = (q e^{G})^T                 [128][64 tok]  bf16
+//                               (the backward's records: Q~ [64 tok][128])
 //                        K^^T = (k e^{G_C - G})^T           [128][64 tok]  bf16
 //                        U~^T  16-byte pieces, piece-major  [8][128][8 tok] bf16
 //                        -W^T                               [128][64 tok]  bf16
@@ -21,7 +22,8 @@
 //                        U^T  = U~^T - S^T W^T,  O'^T = S^T Q~^T
 //                        O'^T += U'^T M_raw^T,   S^T <- S^T diag(e^{G_C}) + U'^T K^
 //                      (U' = diag(rk) U, O = diag(rq) O'; S^T lives in Tensor Memory in fp32,
-//                      with a bf16 copy as the A operand of the next chunk's products).
+//                      with a bf16 copy as the A operand of the next chunk's products).  Each
+//                      line is one tcgen05.mma per K step over adjacent B tiles.
 //
 // The algebra is that of the single-pass kernel (kda_chunk_tc.cu); here the key side of
 // every chunk runs on all SMs at once instead of inside the per-sequence scan.
@@ -52,7 +54,8 @@ constexpr int P_T = 40960;              // T [64 x 64] bf16 SW128
 constexpr int P_TW = P_T + 8192;        // -T diag(rk)
 constexpr int P_KS = P_TW + 8192;       // K^^T [128 x 64] staging (after MMA1)
 constexpr int P_MS = P_T;               // M record [64 x 64] staging (readback to T write)
-constexpr int P_W = P_T;                // -W^T [128 x 64] staging (T and T diag(rk), after MMA2)
+constexpr int P_W = P_T;                // -W [64 x 128] or -W^T [128 x 64] staging (T and
+                                        // T diag(rk), after MMA2)
 static_assert(P_Y + 4 * 16 * LDY * 4 <= P_T, "solve scratch overlaps T");
 static_assert(P_KS + 16384 <= P_KTT, "re-used tiles must stay inside Xl/Kb");
 // Staging of the NEXT record's raw inputs (TMA), each tile issued as soon as its space is
@@ -71,8 +74,9 @@ constexpr size_t kPSmem = P_END + 1024;
 
 // Tensor Memory of the prep kernel (256 columns: two CTAs per SM).
 constexpr uint32_t P_TM_D1 = 0;   // [A; M] accumulator, 160 columns
-constexpr uint32_t P_TM_DW = 0;   // -W^T (after D1 is consumed), 64
-constexpr uint32_t P_TM_DU = 64;  // U~^T, 64
+constexpr uint32_t P_TM_DW = 0;    // after D1 is consumed: [T K~; -W] (forward, 128) or
+                                   // -W^T (backward records, 64)
+constexpr uint32_t P_TM_DU = 128;  // U~^T, 64
 constexpr uint32_t kPTmemCols = 256;
 
 __device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split path gave up
@@ -86,6 +90,7 @@ __device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split pa
 template <bool kBwd, bool kAttn>
 __global__ void __launch_bounds__(kPThreads, 2)
     chunk_prep_kernel(const __grid_constant__ CUtensorMap map_ku,
+                      const __grid_constant__ CUtensorMap map_wr,
                       const __grid_constant__ CUtensorMap map_m,
                       const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
@@ -706,18 +711,26 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA2: -W^T = K~^T (-T diag(rk))^T, U~^T = V^T T^T  (M = 128, N = 64, K = 64)
+    // ---- MMA2: U~^T = V^T T^T (M = 128, N = 64, K = 64) and
+    //      forward records: [T; -T diag(rk)] K~ (M = 128: the T and -T diag(rk) tiles are
+    //        adjacent, N = 128 channels): its rows 64..127 are -W, token-major;
+    //      backward records: -W^T = K~^T (-T diag(rk))^T (M = 128 channels, N = 64)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ts = smem_u32(sm + P_T), tw = smem_u32(sm + P_TW),
                      ks = smem_u32(sm + P_KTT), vs = smem_u32(sm + P_V);
-      const uint32_t idesc = make_idesc(1, 128, 64);
+      const uint32_t idesc = make_idesc(1, 128, 64), idesc_n128 = make_idesc(1, 128, 128);
       // V^T as the A operand is v as staged ([64 tok][128] in two 64-channel boxes), read
       // MN-major: 16 tokens (2 KB) per K step, the channel boxes 8 KB apart
       const uint32_t idesc_amn = make_idesc(1, 128, 64, true, false);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        mma_ss(tm + P_TM_DW, sw128_kdesc<2>(ks, 128, s), sw128_kdesc<2>(tw, 64, s), idesc, s > 0);
+        if constexpr (kBwd)
+          mma_ss(tm + P_TM_DW, sw128_kdesc<2>(ks, 128, s), sw128_kdesc<2>(tw, 64, s), idesc,
+                 s > 0);
+        else
+          mma_ss(tm + P_TM_DW, sw128_kdesc<2>(ts, 128, s), sw128_kdesc<2>(ks, 128, s),
+                 idesc_n128, s > 0);
         mma_ss(tm + P_TM_DU, make_sdesc(vs + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
                sw128_kdesc<2>(ts, 64, s), idesc_amn, s > 0);
       }
@@ -735,21 +748,40 @@ __global__ void __launch_bounds__(kPThreads, 2)
       qv_pending = true;
     }
 
-    // ---- records: thread (j = ln, wg) holds row j of W^T and U~^T for tokens 32 wg .. + 31.
-    //      -W^T goes through a swizzled staging tile and one bulk-tensor store; U~^T (read
-    //      only by the scan's threads) is stored piece-major, coalesced as it stands.
+    // ---- records.  U~^T: thread (j = ln, wg) holds row j for tokens 32 wg .. + 31, stored
+    //      piece-major (read only by the scan's threads), coalesced as it stands.
+    //      Forward: -W row t = ln - 64 (TMEM lanes 64..127), channels 64 wg .. + 63, into a
+    //      swizzled [64 x 128] staging tile (two 64-channel boxes) and two bulk-tensor stores.
+    //      Backward records: -W^T row j, tokens 32 wg .. + 31, into a swizzled [128 x 64]
+    //      staging tile and one bulk-tensor store.
     {
       float w32[32];
-      tmem_ld32(tl + P_TM_DW + 32 * wg, w32);
-      // row ln of the swizzled [128 x 64] staging tile: 16-byte pieces 4 wg .. 4 wg + 3
-      uint8_t* const wrow = sm + P_W + (ln >> 3) * 1024 + (ln & 7) * 128;
+      if constexpr (kBwd) {
+        tmem_ld32(tl + P_TM_DW + 32 * wg, w32);
+        // row ln of the swizzled [128 x 64] staging tile: 16-byte pieces 4 wg .. 4 wg + 3
+        uint8_t* const wrow = sm + P_W + (ln >> 3) * 1024 + (ln & 7) * 128;
 #pragma unroll
-      for (int p = 0; p < 4; ++p)
-        *reinterpret_cast<uint4*>(wrow + (((4 * wg + p) ^ (ln & 7)) << 4)) =
-            make_uint4(pack_bf16(w32[8 * p + 0], w32[8 * p + 1]),
-                       pack_bf16(w32[8 * p + 2], w32[8 * p + 3]),
-                       pack_bf16(w32[8 * p + 4], w32[8 * p + 5]),
-                       pack_bf16(w32[8 * p + 6], w32[8 * p + 7]));
+        for (int p = 0; p < 4; ++p)
+          *reinterpret_cast<uint4*>(wrow + (((4 * wg + p) ^ (ln & 7)) << 4)) =
+              make_uint4(pack_bf16(w32[8 * p + 0], w32[8 * p + 1]),
+                         pack_bf16(w32[8 * p + 2], w32[8 * p + 3]),
+                         pack_bf16(w32[8 * p + 4], w32[8 * p + 5]),
+                         pack_bf16(w32[8 * p + 6], w32[8 * p + 7]));
+      } else if (ln >= 64) {  // warp-uniform: warps 2, 3, 6, 7
+        const int t = ln - 64;
+        uint8_t* const wrow = sm + P_W + wg * 8192 + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(tl + P_TM_DW + 64 * wg + 32 * half, w32);
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            *reinterpret_cast<uint4*>(wrow + (((4 * half + p) ^ (t & 7)) << 4)) =
+                make_uint4(pack_bf16(w32[8 * p + 0], w32[8 * p + 1]),
+                           pack_bf16(w32[8 * p + 2], w32[8 * p + 3]),
+                           pack_bf16(w32[8 * p + 4], w32[8 * p + 5]),
+                           pack_bf16(w32[8 * p + 6], w32[8 * p + 7]));
+        }
+      }
       float u32[32];
       tmem_ld32(tl + P_TM_DU + 32 * wg, u32);
       // piece P = 4 wg + p of row ln (tokens 8 P .. 8 P + 7) at piece-major position
@@ -766,7 +798,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tc_fence_before();
     __syncthreads();
     if (tma_thread) {
-      tma_store_2d(&map_ku, sm + P_W, 0, (int)((2 * ws.recs + rec) * 128));
+      if constexpr (kBwd) {
+        tma_store_2d(&map_ku, sm + P_W, 0, (int)((2 * ws.recs + rec) * 128));
+      } else {
+        tma_store_2d(&map_wr, sm + P_W, 0, (int)(rec * 64));
+        tma_store_2d(&map_wr, sm + P_W + 8192, 64, (int)(rec * 64));
+      }
       bulk_commit();
     }
     rec = rec_next;
@@ -800,12 +837,17 @@ __global__ void __launch_bounds__(kPThreads, 2)
 
 constexpr int kSThreads = 512;
 // one stage = one chunk's record
-constexpr int S_Q = 0;          // Q~ [64 x 128] (two 64-channel boxes)
-constexpr int S_W = 16384;      // -W^T [128 x 64]
+// Forward records: [Q~ box 0 | -W box 0 | Q~ box 1 | -W box 1], each [64 tok x 64 ch] bf16
+// with 128-byte swizzle: the K-major B operand [Q~; -W] (channels 0..63 in the first 16 KB,
+// 64..127 in the second) of one N = 128 MMA for the output and U products.  Backward records:
+// Q~ boxes 0 and 1, then -W^T [128 x 64].  K^^T and M_raw are adjacent: the B operand
+// [K^^T; M_raw] of one N = 192 MMA for the state and output updates.
+constexpr int S_Q = 0;          // Q~ [64 x 128] (two 64-channel boxes), with -W (forward)
 constexpr int S_KT = 32768;     // K^^T [128 x 64]
-constexpr int S_UT = 49152;     // U~^T, piece-major [8][128][8 tok]
-constexpr int S_M = 65536;      // M_raw [64 x 64]
+constexpr int S_M = 49152;      // M_raw [64 x 64]
+constexpr int S_UT = 57344;     // U~^T, piece-major [8][128][8 tok]
 constexpr int S_V = 73728;      // e^{G_C}, rk, rq
+static_assert(S_M == S_KT + 16384, "the wide MMA's operand pair");
 constexpr int kStage = 74752;
 constexpr uint32_t kStageTx = 74752;
 constexpr uint32_t kStageTxBwd = kStageTx - 2 * 8192 - 8192;  // no Q~, no M
@@ -819,12 +861,13 @@ static_assert(kStage % 1024 == 0 && S_OS % 1024 == 0 && S_SD % 1024 == 0, "align
 constexpr size_t kSSmem = S_END + 1024;
 constexpr size_t kSSmemBwd = S_END_BWD + 1024;
 
-constexpr uint32_t S_TM_DU = 0;    // S^T (-W)^T, 64
-constexpr uint32_t S_TM_DO = 64;   // O'^T, 64
-constexpr uint32_t S_TM_S = 128;   // fp32 master state S^T, 128
+constexpr uint32_t S_TM_S = 0;     // fp32 master state S^T, 128
+constexpr uint32_t S_TM_DO = 128;  // O'^T, 64 (right after S: one N = 192 accumulator)
+constexpr uint32_t S_TM_DU = 192;  // S^T (-W)^T, 64 (right after O': one N = 128 accumulator)
 constexpr uint32_t S_TM_SA = 256;  // bf16 copy of S^T (A operand), 64
 constexpr uint32_t S_TM_UA = 320;  // U'^T A operand (bf16 pairs), 32
 constexpr uint32_t kSTmemCols = 512;
+static_assert(S_TM_DO == S_TM_S + 128 && S_TM_DU == S_TM_DO + 64, "the wide MMAs' accumulators");
 
 // kMode 0: the forward; 1: the backward's own forward pass (per-chunk images, no output);
 // 2: the training forward (output and per-chunk images)
@@ -832,6 +875,7 @@ template <int kMode>
 __global__ void __launch_bounds__(kSThreads, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qw,
                       const __grid_constant__ CUtensorMap map_ku,
+                      const __grid_constant__ CUtensorMap map_wr,
                       const __grid_constant__ CUtensorMap map_m,
                       const __grid_constant__ CUtensorMap map_o,
                       const __grid_constant__ CUtensorMap map_s0,
@@ -843,10 +887,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __shared__ uint64_t bar_ld[2], bar_mma;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
-  __shared__ __align__(16) float s_vec[256];  // this chunk's e^{G_C}, rk, rq
   __shared__ __align__(16) float s_one[64];   // unit output scale (rq folded into the records)
   constexpr bool bwd = kMode != 0;
   constexpr bool want_out = kMode != 1;
+  constexpr bool fwd = kMode == 0;  // -W records token-major, interleaved with Q~
+  constexpr int q_box1 = fwd ? 16384 : 8192;  // Q~'s second 64-channel box
+  constexpr int w_at = fwd ? 8192 : 16384;    // -W's first box, or -W^T
   if (threadIdx.x < 64) s_one[threadIdx.x] = 1.f;
 
   const int tid = threadIdx.x;
@@ -881,6 +927,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&map_qw);
     tma_prefetch_desc(&map_ku);
+    if (fwd) tma_prefetch_desc(&map_wr);
     tma_prefetch_desc(&map_m);
     tma_prefetch_desc(&map_o);
   }
@@ -898,12 +945,19 @@ __global__ void __launch_bounds__(kSThreads, 1)
     uint8_t* b = sm + st * kStage;
     uint64_t* bar = &bar_ld[st];
     switch (warp) {
-      case 1: tma_load_2d(b + S_W, &map_ku, bar, 0, (int)((2 * ws.recs + rec) * 128)); break;
+      case 1:
+        if (fwd) {
+          tma_load_2d(b + w_at, &map_wr, bar, 0, (int)(rec * 64));
+          tma_load_2d(b + w_at + 16384, &map_wr, bar, 64, (int)(rec * 64));
+        } else {
+          tma_load_2d(b + w_at, &map_ku, bar, 0, (int)((2 * ws.recs + rec) * 128));
+        }
+        break;
       case 2: tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128)); break;
       case 3: bulk_load(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar); break;
       case 4: bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar); break;
       case 5: if (want_out) tma_load_2d(b + S_Q, &map_qw, bar, 0, (int)(rec * 64)); break;
-      case 6: if (want_out) tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, (int)(rec * 64)); break;
+      case 6: if (want_out) tma_load_2d(b + S_Q + q_box1, &map_qw, bar, 64, (int)(rec * 64)); break;
       default: if (want_out) tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64)); break;
     }
   };
@@ -916,10 +970,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int rq = (int)(rec * 64), rw = (int)((2 * ws.recs + rec) * 128);
     if (want_out) {  // the backward's own forward pass computes no output
       tma_load_2d(b + S_Q, &map_qw, bar, 0, rq);
-      tma_load_2d(b + S_Q + 8192, &map_qw, bar, 64, rq);
+      tma_load_2d(b + S_Q + q_box1, &map_qw, bar, 64, rq);
       tma_load_2d(b + S_M, &map_m, bar, 0, (int)(rec * 64));
     }
-    tma_load_2d(b + S_W, &map_ku, bar, 0, rw);
+    if (fwd) {
+      tma_load_2d(b + w_at, &map_wr, bar, 0, rq);
+      tma_load_2d(b + w_at + 16384, &map_wr, bar, 64, rq);
+    } else {
+      tma_load_2d(b + w_at, &map_ku, bar, 0, rw);
+    }
     tma_load_2d(b + S_KT, &map_ku, bar, 0, (int)(rec * 128));
     bulk_load(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar);
     bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar);
@@ -957,6 +1016,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t idesc_n64 = make_idesc(1, 128, 64);
   const uint32_t idesc_n64_bmn = make_idesc(1, 128, 64, false, true);
   const uint32_t idesc_n128 = make_idesc(1, 128, 128);
+  const uint32_t idesc_n192 = make_idesc(1, 128, 192);
   uint32_t mma_phase = 0;
   uint32_t wait_calls = 0;
   auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -975,7 +1035,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   for (int ch = 0; ch < nck; ++ch) {
     const int st = ch & 1;
     uint8_t* const b = sm + st * kStage;
-    const float* const vec = s_vec;
+    // e^{G_C}, rk, rq, read from the stage itself (it is refilled after the output phase)
+    const float* const vec = reinterpret_cast<const float*>(b + S_V);
     const int n = min(kC, len - ch * kC);
     const long long tok0 = bos + (long long)ch * kC;
 
@@ -983,24 +1044,27 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (tid == 0 && bwd) bulk_wait_read_all();
     if (!(ok = block_wait(&bar_ld[st], (ch >> 1) & 1))) break;
     inflight[st] = -1;
-    // the stage's vectors move to static shared memory so that the stage can be refilled
-    // as soon as the tensor cores are done with it (the previous chunk's readers of s_vec
-    // are past the barrier inside block_wait)
-    if (tid < 256) s_vec[tid] = reinterpret_cast<const float*>(b + S_V)[tid];
-    __syncthreads();
 
-    // ---- MMA3: D_U = S^T (-W)^T, O'^T = S^T Q~^T  (M = 128, N = 64, K = 128; the -W^T
-    //      record is the B operand read MN-major, 16 channel rows per K step)
+    // ---- MMA3: O'^T = S^T Q~^T, D_U = S^T (-W)^T  (M = 128, K = 128).  Forward records:
+    //      one N = 128 MMA over the K-major B operand [Q~; -W] into the adjacent O' and D_U
+    //      columns.  Backward records: the -W^T record read MN-major (16 channel rows per K
+    //      step) and Q~ K-major, N = 64 each.
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t ws_ = smem_u32(b + S_W), qs = smem_u32(b + S_Q);
+      const uint32_t ws_ = smem_u32(b + w_at), qs = smem_u32(b + S_Q);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        mma_ts(tm + S_TM_DU, tm + S_TM_SA + 8 * s,
-               make_sdesc(ws_ + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128), idesc_n64_bmn,
-               s > 0);
-        if (want_out)
-          mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
+        if constexpr (fwd) {
+          mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 128, s), idesc_n128,
+                 s > 0);
+        } else {
+          mma_ts(tm + S_TM_DU, tm + S_TM_SA + 8 * s,
+                 make_sdesc(ws_ + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
+                 idesc_n64_bmn, s > 0);
+          if (want_out)
+            mma_ts(tm + S_TM_DO, tm + S_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64,
+                   s > 0);
+        }
       }
       mma_commit(&bar_mma);
     }
@@ -1043,7 +1107,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA4: O'^T += U'^T M_raw^T, S^T += U'^T K^
+    // ---- MMA4: S^T += U'^T K^, O'^T += U'^T M_raw^T: one N = 192 MMA over [K^^T; M_raw]
+    //      (K-major, adjacent) into the adjacent S and O' columns
     if (tid == 0) {
       bulk_wait_read_all();  // the previous chunk's output store has read its staging tile
       if (bwd) {
@@ -1051,12 +1116,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
         bulk_commit();
       }
       tc_fence_after();
-      const uint32_t ms = smem_u32(b + S_M), ks = smem_u32(b + S_KT);
+      const uint32_t ks = smem_u32(b + S_KT);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         if (want_out)
-          mma_ts(tm + S_TM_DO, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ms, 64, s), idesc_n64, 1);
-        mma_ts(tm + S_TM_S, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ks, 128, s), idesc_n128, 1);
+          mma_ts(tm + S_TM_S, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ks, 192, s), idesc_n192, 1);
+        else
+          mma_ts(tm + S_TM_S, tm + S_TM_UA + 8 * s, sw128_kdesc<2>(ks, 128, s), idesc_n128, 1);
       }
       mma_commit(&bar_mma);
       // the refill's bytes land on the stage's next phase (its current phase completed at
@@ -1065,9 +1131,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     if (!(ok = mma_wait())) break;
     tc_fence_after();
-    // the stage is consumed (its last readers were MMA4 and the U' pack): refill it
-    if (ch + 2 < nck) issue_load_spread(ch + 2, st);
-    inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
     // ---- bf16 copy of the new state and the output O = diag(rq) O' (O' itself when the
     //      records carry rq)
     {
@@ -1119,6 +1182,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
         bulk_commit();
       }
     }
+    // the stage is consumed (its last readers were MMA4, the U' pack and the output's rq):
+    // refill it
+    if (ch + 2 < nck) issue_load_spread(ch + 2, st);
+    inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
     if (tid == 0 && bwd && ch + 1 < nck) {
       const int row = (int)(((slot0 + ch + 1) * H + h) * 128);
       tma_store_2d(&map_s0, sm + S_SD, 0, row);
@@ -1221,10 +1288,13 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
   const long long rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
   const long long map_rows = rows > 0 ? rows : 1;
   const long long rec_rows = ws.recs > 0 ? ws.recs : 1;
-  CUtensorMap mqw, mku, mm, mo, mq, mk, mv, mg, ms0, mut;
+  CUtensorMap mqw, mku, mwr, mm, mo, mq, mk, mv, mg, ms0, mut;
   // the backward's scan writes no output: its (unused) output map is laid over q
+  // -W: the forward's records hold it token-major ([64 x 128] per record), in the space the
+  // backward's -W^T records take ([128 x 64], the third part of ku)
   if (!make_map_2d(&mqw, ws.qw, rec_rows * 64, 128, 64) ||
       !make_map_2d(&mku, ws.ku, 3 * rec_rows * 128, 64, 128) ||
+      !make_map_2d(&mwr, ws.ku + 2 * ws.recs * 8192, rec_rows * 64, 128, 64) ||
       !make_map_2d(&mm, ws.m, rec_rows * 64, 64, 64) ||
       !make_map_out(&mo, ws.bwd == 1 ? a.q : a.out, map_rows, a.H) ||
       !make_map_in(&mq, a.q, map_rows, a.H, false) ||
@@ -1256,10 +1326,10 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
     const long long grid = std::min<long long>(ws.recs, 2LL * sms);
-    prep<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mku, mm, mq, mk, mv, mg, a, ws);
+    prep<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mku, mwr, mm, mq, mk, mv, mg, a, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  scan<<<dim3(a.H, a.B), kSThreads, scan_smem, st>>>(mqw, mku, mm, mo, ms0, mut, a, ws);
+  scan<<<dim3(a.H, a.B), kSThreads, scan_smem, st>>>(mqw, mku, mwr, mm, mo, ms0, mut, a, ws);
   return cudaGetLastError();
 }
 
