@@ -477,8 +477,8 @@ constexpr int kHThreads = 512;
 // one stage = one chunk's record and its v tile
 constexpr int H_Q = 0;          // Q~ [64 x 128] (two 64-channel boxes)
 constexpr int H_KT = 16384;     // K^^T [128 x 64]
-constexpr int H_V = 32768;      // v [64 tok x 128] as staged (two SW128 boxes): V^T MN-major
-constexpr int H_M = 49152;      // M [64 x 64]
+constexpr int H_M = 32768;      // M [64 x 64], right after K^^T: the B operand [K^^T; M]
+constexpr int H_V = 40960;      // v [64 tok x 128] as staged (two SW128 boxes): V^T MN-major
 constexpr int H_VEC = 57344;    // e^{G_C} [128], scale per live row [64]
 constexpr int kHStage = 58368;
 constexpr uint32_t kHStageTx = 58368;
@@ -488,8 +488,9 @@ constexpr size_t kHSmem = H_END + 1024;
 static_assert(kHStage % 1024 == 0 && H_OS % 1024 == 0, "alignment");
 
 constexpr uint32_t H_TM_S = 0;     // fp32 master state S^T [128 (value col) x 128 (key ch)]
-constexpr uint32_t H_TM_SA = 128;  // bf16 copy of S^T (A operand), 64 columns
-constexpr uint32_t H_TM_DO = 192;  // O'^T [128 x 64 tok]
+constexpr uint32_t H_TM_DO = 128;  // O'^T [128 x 64 tok], right after S: one N = 192 update
+constexpr uint32_t H_TM_SA = 192;  // bf16 copy of S^T (A operand), 64 columns
+static_assert(H_TM_DO == H_TM_S + 128 && H_M == H_KT + 16384, "the N = 192 update's operands");
 constexpr uint32_t kHTmemCols = 256;
 
 __global__ void __launch_bounds__(kHThreads, 1)
@@ -504,7 +505,6 @@ __global__ void __launch_bounds__(kHThreads, 1)
   __shared__ uint64_t bar_ld[2], bar_mma;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
-  __shared__ __align__(16) float s_vec[256];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -595,8 +595,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   __syncthreads();
 
   const uint32_t idesc_n64 = make_idesc(1, 128, 64);
-  const uint32_t idesc_n64_amn = make_idesc(1, 128, 64, true, false);
-  const uint32_t idesc_n128_amn = make_idesc(1, 128, 128, true, false);
+  const uint32_t idesc_n192_amn = make_idesc(1, 128, 192, true, false);
   uint32_t mma_phase = 0, wait_calls = 0;
   auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     const uint32_t slot_w = wait_calls++ & 1;
@@ -614,7 +613,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
 
     if (!(ok = block_wait(&bar_ld[st], (ch >> 1) & 1))) break;
     inflight[st] = -1;
-    if (tid < 256) s_vec[tid] = reinterpret_cast<const float*>(b + H_VEC)[tid];
+    // e^{G_C} and the output scale, read from the stage itself (refilled after the output)
+    const float* const s_vec = reinterpret_cast<const float*>(b + H_VEC);
     if (n < kC) {  // partial chunk: the v rows past n belong to the next sequence
       for (int u = tid; u < 1024; u += kHThreads) {
         const int row = (u >> 3) & 63;
@@ -626,20 +626,15 @@ __global__ void __launch_bounds__(kHThreads, 1)
     }
     __syncthreads();
 
-    // ---- output product O'^T = S^T Q~^T + V^T M^T (M = 128, N = 64); the V^T operand is
-    //      the staged v tile read MN-major (16 tokens = 2 KB per K step, channel boxes 8 KB
-    //      apart)
+    // ---- output product O'^T = S^T Q~^T (M = 128, N = 64); its V^T M^T part joins the
+    //      state update below
     const uint32_t vs = smem_u32(b + H_V);
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t qs = smem_u32(b + H_Q), ms = smem_u32(b + H_M);
+      const uint32_t qs = smem_u32(b + H_Q);
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         mma_ts(tm + H_TM_DO, tm + H_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tm + H_TM_DO, make_sdesc(vs + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
-               sw128_kdesc<2>(ms, 64, s), idesc_n64_amn, 1);
     }
     // meanwhile: decay the fp32 master state in place (S^T diag(e^{G_C}))
     {
@@ -651,14 +646,17 @@ __global__ void __launch_bounds__(kHThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    // ---- state update S^T += V^T K^ (M = 128, N = 128, K = 64 tokens)
+    // ---- state update and the rest of the output: [S^T | O'^T] += V^T [K^^T; M]^T, one
+    //      N = 192 MMA (M = 128, K = 64 tokens) over the adjacent K^^T and M tiles into the
+    //      adjacent S and O' columns; the V^T operand is the staged v tile read MN-major (16
+    //      tokens = 2 KB per K step, channel boxes 8 KB apart)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ks = smem_u32(b + H_KT);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
         mma_ss(tm + H_TM_S, make_sdesc(vs + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
-               sw128_kdesc<2>(ks, 128, s), idesc_n128_amn, 1);
+               sw128_kdesc<2>(ks, 192, s), idesc_n192_amn, 1);
       mma_commit(&bar_mma);
       // the refill's bytes land on the stage's next phase
       if (ch + 2 < nck) mbar_arrive_expect_tx(&bar_ld[st], kHStageTx);
@@ -666,8 +664,6 @@ __global__ void __launch_bounds__(kHThreads, 1)
     if (!(ok = block_wait(&bar_mma, mma_phase & 1))) break;
     ++mma_phase;
     tc_fence_after();
-    if (ch + 2 < nck) issue_load_spread(ch + 2, st);
-    inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
     // ---- bf16 copy of the new state; the output O = scale O'
     {
       float S[32];
@@ -707,6 +703,9 @@ __global__ void __launch_bounds__(kHThreads, 1)
       tma_store_3d(&map_o, sm + H_OS + 8192, 64, h, (int)tok0);
       bulk_commit();
     }
+    // the stage is consumed (the MMAs, and the output's scale vector): refill it
+    if (ch + 2 < nck) issue_load_spread(ch + 2, st);
+    inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
   }
 
   if (!ok) {
