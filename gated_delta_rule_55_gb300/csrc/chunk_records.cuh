@@ -20,15 +20,29 @@ constexpr long long kRecVec = 256 * 4;          // e^{G_C}[128], rk[64], rq[64]
 constexpr long long kRecState = 128LL * 128 * 2;  // a bf16 [128 x 128] state image
 
 struct Ws {
-  __nv_bfloat16* qw;   // Q~ records: Q~^T [recs * 128][64] (forward) or Q~ [recs * 64][128]
+  __nv_bfloat16* qw;   // [recs * 64][128]: Q~ records
   // [3 * recs * 128][64]: K^^T records ([128][64] each), then U~^T records (16-byte pieces
-  // stored piece-major, [8][128][8]), then -W^T records ([128][64])
+  // stored piece-major, [8][128][8]), then the -W records: token-major [64][128] each for
+  // the forward, -W^T [128][64] for the backward's records (the same bytes)
   __nv_bfloat16* ku;
   __nv_bfloat16* m;    // [recs * 64][64]
   float* vec;          // [recs][256]
   int32_t* coff;       // [N + 1] first chunk slot of each sequence (packed inputs only)
   long long recs;      // chunk slots x heads
   int nck_fixed;       // chunks per sequence (fixed-length inputs)
+  // Chain splitting of the packed forward (null otherwise).  A sequence's scan is a chain
+  // of per-chunk affine maps S' = A_c S + B_c; a long one is cut at chunk `mid` into three
+  // chains that run at once: [0, mid) from the initial state (its end state is S_mid),
+  // [mid, nck) from S = 0 (end state S0, outputs O0) and [mid, nck) from S = I with the
+  // chunk writes dropped (end state P = A_{nck-1} ... A_mid, outputs X).  Then the true
+  // outputs of the second part are O0 + X S_mid and its end state S0 + P S_mid.
+  int4* chains;        // [N + 2 kMaxSplit] scan work, longest first: seq, first chunk,
+                       // end chunk, kind | slot << 2 (kind 0 whole, 1 first part, 2 from
+                       // zero, 3 from identity)
+  int32_t* nchains;    // [2]: chain count, split count
+  int4* splits;        // [kMaxSplit]: seq, mid, nck of each split sequence
+  float* split_st;     // [kMaxSplit][3][H][128][128]: S_mid, S0, P (fp32, [dk][dv])
+  __nv_bfloat16* xbuf; // [total_T][H][128]: X rows of the second parts
   // Records kept for the backward (bwd != 0).  The prep then folds rq into Q~ and into the
   // rows of M (Q~ = q^ e^{G}, M[r][s] = rq_r M_raw[r][s]) and writes N; the scan writes,
   // per chunk, the state entering it and the chunk's U, and computes the output only in
@@ -38,6 +52,9 @@ struct Ws {
   __nv_bfloat16* ut;    // [recs * 128][64]: U^T of the chunk (row j, column = token)
   int bwd;
 };
+
+constexpr int kMaxSplit = 8;      // sequences whose chain may be split, per call
+constexpr int kSplitMinChunks = 16;  // shortest chain worth splitting
 
 inline long long slots_for(const ChunkArgs& a) {
   if (a.cu_seqlens) return (long long)a.total_T / kC + a.B;

@@ -878,6 +878,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                       const __grid_constant__ CUtensorMap map_wr,
                       const __grid_constant__ CUtensorMap map_m,
                       const __grid_constant__ CUtensorMap map_o,
+                      const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_s0,
                       const __grid_constant__ CUtensorMap map_ut, const ChunkArgs a,
                       const Ws ws) {
@@ -900,8 +901,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int wg = tid >> 7;
   const int ln = tid & 127;
   const int lane_base = 32 * (warp & 3);
-  const int h = blockIdx.x, seq = blockIdx.y;
+  const int h = blockIdx.x;
   const int H = a.H;
+  // The chain this CTA scans: a sequence's chunks [c0, nck), from its initial state (kind
+  // 0 or 1), from zero (kind 2) or from the identity with the chunk writes dropped (kind 3).
+  // The planned forward of packed inputs reads it from the chain table (longest first).
+  int seq = blockIdx.y, c0 = 0, kind = 0, slot = 0, c_end = -1;
+  if (fwd && ws.chains) {
+    if ((int)blockIdx.y >= ws.nchains[0]) return;  // uniform: no chain for this CTA
+    const int4 e = ws.chains[blockIdx.y];
+    seq = e.x;
+    c0 = e.y;
+    c_end = e.z;
+    kind = e.w & 3;
+    slot = e.w >> 2;
+  }
   long long bos;
   int len;
   seq_range(a, seq, bos, len);
@@ -914,7 +928,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
     slot0 = (long long)seq * ws.nck_fixed;
     nck = ws.nck_fixed;
   }
+  if (c_end >= 0) nck = c_end;
+  const int nrun = nck - c0;  // chunks this CTA scans
   const long long state_off = ((long long)seq * H + h) * kD * kD;
+  const bool drop_u = kind == 3;
+  const float* const st_in = kind <= 1 ? (a.initial_state ? a.initial_state + state_off : nullptr)
+                                       : nullptr;
+  float* const st_out =
+      kind == 0 ? (a.final_state ? a.final_state + state_off : nullptr)
+                : ws.split_st + ((long long)(3 * slot + kind - 1) * H + h) * kD * kD;
+  const CUtensorMap* const omap = kind == 3 ? &map_x : &map_o;
+  __nv_bfloat16* const obase = static_cast<__nv_bfloat16*>(kind == 3 ? (void*)ws.xbuf : a.out);
 
   if (warp == 0) {
     tmem_alloc(&s_tmem, kSTmemCols);
@@ -929,7 +953,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tma_prefetch_desc(&map_ku);
     if (fwd) tma_prefetch_desc(&map_wr);
     tma_prefetch_desc(&map_m);
-    tma_prefetch_desc(&map_o);
+    tma_prefetch_desc(omap);
   }
   tc_fence_before();
   __syncthreads();
@@ -983,11 +1007,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
     bulk_load(b + S_UT, ws.ku + (ws.recs + rec) * 8192, 16384, bar);
     bulk_load(b + S_V, ws.vec + rec * 256, 1024, bar);
   };
-  // chunk whose record is in flight into each stage (-1: none); same on every thread
-  int inflight[2] = {nck > 0 ? 0 : -1, nck > 1 ? 1 : -1};
+  // step (chunk - c0) whose record is in flight into each stage (-1: none); same on every
+  // thread
+  int inflight[2] = {nrun > 0 ? 0 : -1, nrun > 1 ? 1 : -1};
   if (tid == 0) {
-    if (nck > 0) issue_load(0, 0);
-    if (nck > 1) issue_load(1, 1);
+    if (nrun > 0) issue_load(c0, 0);
+    if (nrun > 1) issue_load(c0 + 1, 1);
   }
 
   // Initial state: thread (j = ln, warpgroup wg) owns S^T[j][32 wg .. 32 wg + 31].
@@ -996,7 +1021,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int c = 32 * wg + i;
-      S[i] = a.initial_state ? a.initial_state[state_off + (long long)c * kD + ln] : 0.f;
+      S[i] = kind == 3 ? (c == ln ? 1.f : 0.f)
+                       : st_in ? st_in[(long long)c * kD + ln] : 0.f;
     }
     tmem_st32(tl + S_TM_S + 32 * wg, S);
     uint32_t w[16];
@@ -1032,8 +1058,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   };
   bool ok = true;
 
-  for (int ch = 0; ch < nck; ++ch) {
-    const int st = ch & 1;
+  for (int ch = c0; ch < nck; ++ch) {
+    const int it = ch - c0;  // step of this CTA's chain
+    const int st = it & 1;
     uint8_t* const b = sm + st * kStage;
     // e^{G_C}, rk, rq, read from the stage itself (it is refilled after the output phase)
     const float* const vec = reinterpret_cast<const float*>(b + S_V);
@@ -1042,7 +1069,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
     // the previous step's image stores have read their staging tiles before they are rewritten
     if (tid == 0 && bwd) bulk_wait_read_all();
-    if (!(ok = block_wait(&bar_ld[st], (ch >> 1) & 1))) break;
+    if (!(ok = block_wait(&bar_ld[st], (it >> 1) & 1))) break;
     inflight[st] = -1;
 
     // ---- MMA3: O'^T = S^T Q~^T, D_U = S^T (-W)^T  (M = 128, K = 128).  Forward records:
@@ -1084,7 +1111,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tmem_ld16(tl + S_TM_DU + 16 * wg, v16);
       const uint4 ua = *reinterpret_cast<const uint4*>(b + S_UT + ((2 * wg) * 128 + ln) * 16);
       const uint4 ub = *reinterpret_cast<const uint4*>(b + S_UT + ((2 * wg + 1) * 128 + ln) * 16);
-      const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+      // (the identity-start chain drops the chunk's write: U~ = 0)
+      const uint32_t uw[8] = {drop_u ? 0u : ua.x, drop_u ? 0u : ua.y, drop_u ? 0u : ua.z,
+                              drop_u ? 0u : ua.w, drop_u ? 0u : ub.x, drop_u ? 0u : ub.y,
+                              drop_u ? 0u : ub.z, drop_u ? 0u : ub.w};
       uint32_t up[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -1163,8 +1193,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 __float2bfloat16_rn(o16[i] * rqv[16 * wg + i]);
           }
         } else {
-          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
-                              ((tok0 + 16 * wg) * H + h) * kD + ln;
+          __nv_bfloat16* op = obase + ((tok0 + 16 * wg) * H + h) * kD + ln;
           const long long stride = (long long)H * kD;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -1177,15 +1206,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
     __syncthreads();
     if (tid == 0 && want_out) {
       if (n == kC) {
-        tma_store_3d(&map_o, sm + S_OS, 0, h, (int)tok0);
-        tma_store_3d(&map_o, sm + S_OS + 8192, 64, h, (int)tok0);
+        tma_store_3d(omap, sm + S_OS, 0, h, (int)tok0);
+        tma_store_3d(omap, sm + S_OS + 8192, 64, h, (int)tok0);
         bulk_commit();
       }
     }
     // the stage is consumed (its last readers were MMA4, the U' pack and the output's rq):
     // refill it
     if (ch + 2 < nck) issue_load_spread(ch + 2, st);
-    inflight[st] = (ch + 2 < nck) ? ch + 2 : -1;
+    inflight[st] = (ch + 2 < nck) ? it + 2 : -1;
     if (tid == 0 && bwd && ch + 1 < nck) {
       const int row = (int)(((slot0 + ch + 1) * H + h) * 128);
       tma_store_2d(&map_s0, sm + S_SD, 0, row);
@@ -1203,14 +1232,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (inflight[st] >= 0) mbar_wait(&bar_ld[st], (inflight[st] >> 1) & 1, 1000000000ull);
     }
     mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
-  } else if (a.final_state) {
+  } else if (st_out) {
     tc_fence_after();
     float S[32];
     tmem_ld32(tl + S_TM_S + 32 * wg, S);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int c = 32 * wg + i;
-      a.final_state[state_off + (long long)c * kD + ln] = S[i];
+      st_out[(long long)c * kD + ln] = S[i];
     }
   }
   if (tid == 0) bulk_wait_all();
@@ -1220,11 +1249,244 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (warp == 0) tmem_dealloc(tm, kSTmemCols);
 }
 
+// ------------------------------------------------------------ split-chain fix-up
+
+// After the scan of a planned packed forward: for each split sequence (slot s, cut at chunk
+// mid) and head h, the end state S0 + P S_mid and, for the tokens of the second part,
+// out += X S_mid (X: the identity-start chain's outputs, tokens x key channels).  Both are
+// tcgen05 products with S_mid as the MN-major B operand; the end state takes P and S_mid
+// each as a bf16 pair (hi, lo = x - hi) and sums Ph Sh + Ph Sl + Pl Sh, about 2^-16 from
+// the fp32 product.  Work units per (s, h): the end state, then the 128-token tiles of the
+// second part; each CTA takes a contiguous range of units, so consecutive units share the
+// staged S_mid, and the next tile's X rows load while the current unit finishes.
+constexpr int kFThreads = 256;
+constexpr int F_X = 0;        // X tile [128 tok x 128] bf16: two 64-channel boxes of 128 rows
+constexpr int F_B = 32768;    // S_mid hi (bf16) as the MN-major B operand [128 k][128 n]
+constexpr int F_BL = 65536;   // S_mid lo
+constexpr int F_PH = 98304;   // P hi (bf16) as the K-major A operand [128 i][128 k]
+constexpr int F_PL = 131072;  // P lo
+constexpr size_t kFSmem = 163840 + 1024;
+
+__global__ void __launch_bounds__(kFThreads, 1)
+    chunk_fixup_kernel(const __grid_constant__ CUtensorMap map_x, const ChunkArgs a,
+                       const Ws ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  __shared__ uint64_t bar_x, bar_mma;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_ok;
+  const int k = ws.nchains[1];
+  if (k == 0) return;  // uniform
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
+  const int H = a.H;
+  // per split: first token of the second part, its end, and its 128-token tile count
+  long long t_first[kMaxSplit], t_end[kMaxSplit], u_first[kMaxSplit + 1];
+  int ntile[kMaxSplit];
+  u_first[0] = 0;
+  for (int s2 = 0; s2 < kMaxSplit; ++s2) {
+    ntile[s2] = 0;
+    t_first[s2] = t_end[s2] = 0;
+    if (s2 < k) {
+      const int4 sp = ws.splits[s2];
+      long long bos;
+      int len;
+      seq_range(a, sp.x, bos, len);
+      t_first[s2] = bos + (long long)sp.y * kC;
+      t_end[s2] = bos + len;
+      ntile[s2] = (int)((t_end[s2] - t_first[s2] + 127) / 128);
+    }
+    u_first[s2 + 1] = u_first[s2] + (long long)H * (1 + ntile[s2]);
+  }
+  const long long total = u_first[k];
+  const long long u_lo = total * blockIdx.x / gridDim.x;
+  const long long u_hi = total * (blockIdx.x + 1) / gridDim.x;
+  if (u_lo >= u_hi) return;  // uniform
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, 128);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_x, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&map_x);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t tl = tm + (uint32_t(32 * (warp & 3)) << 16);
+  const long long sq = (long long)kD * kD;
+  // unit -> (split, head, u): u = 0 the end state, else tile u - 1
+  auto decode = [&](long long unit, int& s2, int& h, int& u) {
+    s2 = 0;
+    while (s2 < k - 1 && unit >= u_first[s2 + 1]) ++s2;
+    const long long r = unit - u_first[s2];
+    const int per = 1 + ntile[s2];
+    h = (int)(r / per);
+    u = (int)(r % per);
+  };
+  auto issue_x = [&](int s2, int h, int tile) {  // thread 0
+    const long long t_lo = t_first[s2] + 128LL * tile;
+    mbar_arrive_expect_tx(&bar_x, 32768);
+    for (int q2 = 0; q2 < 4; ++q2)  // (tokens 0..63 | 64..127) x (channels 0..63 | 64..127)
+      tma_load_3d(sm + F_X + (q2 >> 1) * 16384 + (q2 & 1) * 8192, &map_x, &bar_x,
+                  64 * (q2 >> 1), h, (int)(t_lo + 64 * (q2 & 1)));
+  };
+  // a [128][128] fp32 matrix as bf16 (hi, lo) pairs: element (row, col) of the MN-major B
+  // layout (mn) or of the K-major A layout
+  auto stage_pair = [&](const float* src, uint32_t hi_off, uint32_t lo_off, bool mn) {
+    for (int q2 = tid; q2 < kD * kD / 8; q2 += kFThreads) {
+      const int row = q2 >> 4, c8 = (q2 & 15) * 8;
+      const float4 x0 = *reinterpret_cast<const float4*>(src + row * kD + c8);
+      const float4 x1 = *reinterpret_cast<const float4*>(src + row * kD + c8 + 4);
+      const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hw[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+        lw[e] = pack_bf16(x[2 * e] - bf16_lo(hw[e]), x[2 * e + 1] - bf16_hi(hw[e]));
+      }
+      // both layouts: 64-column block c8 / 64 at 16 KB, rows of 128 bytes in 8-row
+      // swizzled groups (MN-major: row = k, columns = n; K-major: row = i, columns = k)
+      const uint32_t off = uint32_t(c8 >> 6) * 16384u + uint32_t(row >> 3) * 1024u +
+                           uint32_t(row & 7) * 128u +
+                           ((uint32_t((c8 & 63) >> 3) ^ uint32_t(row & 7)) << 4);
+      (void)mn;
+      *reinterpret_cast<uint4*>(sm + hi_off + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      if (lo_off) *reinterpret_cast<uint4*>(sm + lo_off + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  };
+  int staged = -1;  // (s2 * H + h) whose S_mid (hi, lo) is staged
+  uint32_t xphase = 0, mphase = 0;
+  bool x_issued = false;  // the current unit's X rows are already in flight
+  bool ok = true;
+  const uint32_t idesc = make_idesc(1, 128, 128, false, true);
+  for (long long unit = u_lo; unit < u_hi; ++unit) {
+    int s2, h, u;
+    decode(unit, s2, h, u);
+    const int key = s2 * H + h;
+    const float* smid = ws.split_st + ((long long)(3 * s2) * H + h) * sq;
+    const bool state = u == 0;
+    if (state && !a.final_state) continue;  // uniform
+    const int tile = u - 1;
+    const long long t_lo = state ? 0 : t_first[s2] + 128LL * tile;
+    const long long t_hi = state ? 0 : min(t_lo + 128, t_end[s2]);
+    if (!state && tid == 0 && !x_issued) issue_x(s2, h, tile);
+    x_issued = false;
+    // this thread's row of the result: TMEM lane r, columns 64 wg .. + 63; its addend (the
+    // output rows of the tile, or the rows of S0) is loaded while the products run
+    const int r_row = 32 * (warp & 3) + lane;
+    const long long t_row = t_lo + r_row;
+    float* const st_row = a.final_state + ((long long)ws.splits[s2].x * H + h) * sq +
+                          r_row * kD + 64 * wg;
+    uint4* const o4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                               (t_row * H + h) * kD + 64 * wg);
+    uint4 ov[8];
+    if (!state && t_row < t_hi) {
+#pragma unroll
+      for (int q2 = 0; q2 < 8; ++q2) ov[q2] = o4[q2];
+    }
+    if (staged != key) {  // (the previous unit's products, their last reader, are complete)
+      stage_pair(smid, F_B, F_BL, true);
+      staged = key;
+    }
+    if (state)
+      stage_pair(ws.split_st + ((long long)(3 * s2 + 2) * H + h) * sq, F_PH, F_PL, false);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      s_ok = state ? 1 : (mbar_wait(&bar_x, xphase & 1) ? 1 : 0);
+      if (s_ok) {
+        tc_fence_after();
+        const uint32_t bh = smem_u32(sm + F_B), bl = smem_u32(sm + F_BL);
+        auto bdesc = [&](uint32_t base, int s3) {
+          return make_sdesc(base + uint32_t(s3) * 2048u, 16384u, 1024u, kSwizzle128);
+        };
+        if (state) {
+          const uint32_t ph = smem_u32(sm + F_PH), pl = smem_u32(sm + F_PL);
+#pragma unroll
+          for (int s3 = 0; s3 < 8; ++s3)
+            mma_ss(tm, sw128_kdesc<2>(ph, 128, s3), bdesc(bh, s3), idesc, s3 > 0);
+#pragma unroll
+          for (int s3 = 0; s3 < 8; ++s3) mma_ss(tm, sw128_kdesc<2>(ph, 128, s3), bdesc(bl, s3), idesc, 1);
+#pragma unroll
+          for (int s3 = 0; s3 < 8; ++s3) mma_ss(tm, sw128_kdesc<2>(pl, 128, s3), bdesc(bh, s3), idesc, 1);
+        } else {
+          const uint32_t xs = smem_u32(sm + F_X);
+#pragma unroll
+          for (int s3 = 0; s3 < 8; ++s3)
+            mma_ss(tm, sw128_kdesc<2>(xs, 128, s3), bdesc(bh, s3), idesc, s3 > 0);
+        }
+        mma_commit(&bar_mma);
+        s_ok = mbar_wait(&bar_mma, mphase & 1) ? 1 : 0;
+        // the X tile is free: the next unit's rows, when it is a tile
+        if (s_ok && unit + 1 < u_hi) {
+          int ns, nh, nu;
+          decode(unit + 1, ns, nh, nu);
+          if (nu >= 1) {
+            issue_x(ns, nh, nu - 1);
+            s_ok = 3;
+          }
+        }
+      }
+    }
+    if (!state) ++xphase;
+    ++mphase;
+    __syncthreads();
+    if (!s_ok) {
+      ok = false;
+      break;
+    }
+    x_issued = s_ok == 3;
+    tc_fence_after();
+    {
+      float d[64];
+      tmem_ld32(tl + 64 * wg, *reinterpret_cast<float(*)[32]>(d));
+      tmem_ld32(tl + 64 * wg + 32, *reinterpret_cast<float(*)[32]>(d + 32));
+      if (state) {
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          const float4 s0v = *reinterpret_cast<const float4*>(
+              ws.split_st + ((long long)(3 * s2 + 1) * H + h) * sq + r_row * kD + 64 * wg + j);
+          *reinterpret_cast<float4*>(st_row + j) =
+              make_float4(s0v.x + d[j], s0v.y + d[j + 1], s0v.z + d[j + 2], s0v.w + d[j + 3]);
+        }
+      } else if (t_row < t_hi) {
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) {
+          const uint32_t w[4] = {ov[q2].x, ov[q2].y, ov[q2].z, ov[q2].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            o[e] = pack_bf16(bf16_lo(w[e]) + d[8 * q2 + 2 * e],
+                             bf16_hi(w[e]) + d[8 * q2 + 2 * e + 1]);
+          o4[q2] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (!ok && tid == 0) {
+    atomicOr(&g_split_error, 2u);
+    // the unit's loads and products land before the shared memory is released
+    if (xphase > 0) mbar_wait(&bar_x, (xphase - 1) & 1, 1000000000ull);
+    mbar_wait(&bar_mma, (mphase - 1) & 1, 1000000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, 128);
+}
+
 // ------------------------------------------------------------ varlen chunk offsets
 
-// coff[0] = 0, coff[i + 1] = coff[i] + ceil(len_i / 64) (lengths clamped as seq_range does).
-__global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int N,
-                                                             int total_T, int32_t* coff) {
+// coff[0] = 0, coff[i + 1] = coff[i] + ceil(len_i / 64) (lengths clamped as seq_range does);
+// the whole block (1024 threads) takes part.
+__device__ void chunk_offsets_body(const int32_t* cu, int N, int total_T, int32_t* coff) {
   __shared__ int s_warp[32];
   __shared__ int s_carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1269,14 +1531,163 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
   }
 }
 
+__global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, int N,
+                                                             int total_T, int32_t* coff) {
+  chunk_offsets_body(cu, N, total_T, coff);
+}
+
+// The chunk offsets of packed inputs, then the forward scan's plan: which sequences' chains
+// are split (the longest ones, one at a time, while that shortens the longest chain and the
+// chain count stays within `budget` CTAs per head-group), and the chain table in
+// longest-first order, so that a scan with more chains than SMs starts the long ones first.
+constexpr int kPlanSort = 4096;  // chain tables up to this size are sorted
+constexpr int kPlanCache = 2048;  // chunk counts of up to this many sequences kept on chip
+__global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* cu, int N, int total_T,
+                                                          int H, int budget, int32_t* coff,
+                                                          int4* chains, int32_t* counts,
+                                                          int4* splits) {
+  __shared__ unsigned long long s_key[kPlanSort];
+  __shared__ int s_nck[kPlanCache];
+  __shared__ unsigned long long s_red[32];
+  __shared__ int s_top_seq[kMaxSplit + 1], s_top_len[kMaxSplit + 1];
+  __shared__ int s_k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  chunk_offsets_body(cu, N, total_T, coff);
+  __syncthreads();  // coff (global memory) written by this block is visible to it
+  const bool cached = N <= kPlanCache;
+  if (cached)
+    for (int i = tid; i < N; i += 1024) s_nck[i] = coff[i + 1] - coff[i];
+  __syncthreads();
+  auto nck_of = [&](int i) { return cached ? s_nck[i] : coff[i + 1] - coff[i]; };
+  // the r-th longest sequence (ties: the lower index) by a block maximum over the others
+  auto select = [&](int r) {
+    unsigned long long best = 0;
+    for (int i = tid; i < N; i += 1024) {
+      bool taken = false;
+      for (int j = 0; j < r; ++j) taken |= (s_top_seq[j] == i);
+      if (taken) continue;
+      const unsigned long long key =
+          ((unsigned long long)(unsigned)nck_of(i) << 32) | (0xffffffffu - (unsigned)i);
+      best = key > best ? key : best;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+      best = y > best ? y : best;
+    }
+    if (lane == 0) s_red[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long b = 0;
+      for (int w = 0; w < 32; ++w) b = s_red[w] > b ? s_red[w] : b;
+      s_top_seq[r] = (int)(0xffffffffu - (unsigned)(b & 0xffffffffu));
+      s_top_len[r] = (int)(b >> 32);
+    }
+    __syncthreads();
+  };
+  // split the longest sequences one at a time while that shortens the longest chain: after
+  // kk splits it is max(ceil(L_0 / 2), L_kk), L sorted descending (ranks found on demand)
+  if (tid == 0) s_k = 0;
+  for (int r = 0; r < min(2, N); ++r) select(r);
+  int crit = N > 0 ? s_top_len[0] : 0;
+  for (int kk = 1; kk <= min(kMaxSplit, N); ++kk) {
+    if (kk >= 2 && kk < N) select(kk);
+    bool accept = s_top_len[kk - 1] >= kSplitMinChunks &&
+                  (long long)(N + 2 * kk) * H <= (long long)budget;
+    const int nc = max((s_top_len[0] + 1) / 2, kk < N ? s_top_len[kk] : 0);
+    accept = accept && nc < crit;
+    if (!accept) break;  // uniform: every thread reads the same shared values
+    crit = nc;
+    if (tid == 0) s_k = kk;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int k = s_k;
+    for (int s2 = 0; s2 < k; ++s2)
+      splits[s2] = make_int4(s_top_seq[s2], (s_top_len[s2] + 1) / 2, s_top_len[s2], 0);
+    counts[0] = N + 2 * k;
+    counts[1] = k;
+  }
+  __syncthreads();
+  const int k = s_k;
+  const int count = N + 2 * k;
+  // entry e < N: sequence e (whole, or its first part when split); e >= N: the second
+  // part of split slot (e - N) / 2, from zero (even) or from the identity (odd)
+  auto entry = [&](int e) -> int4 {
+    if (e < N) {
+      for (int s2 = 0; s2 < k; ++s2)
+        if (s_top_seq[s2] == e) return make_int4(e, 0, (s_top_len[s2] + 1) / 2, 1 | (s2 << 2));
+      return make_int4(e, 0, nck_of(e), 0);
+    }
+    const int s2 = (e - N) >> 1, part = (e - N) & 1;
+    const int mid = (s_top_len[s2] + 1) / 2;
+    return make_int4(s_top_seq[s2], mid, s_top_len[s2], (2 + part) | (s2 << 2));
+  };
+  if (count <= kPlanSort) {
+    int n2 = 1;
+    while (n2 < count) n2 <<= 1;
+    for (int e = tid; e < n2; e += 1024) {
+      unsigned long long key = ~0ull;  // padding sorts last
+      if (e < count) {
+        const int4 c = entry(e);
+        key = ((unsigned long long)(0x7fffffffu - (unsigned)(c.z - c.y)) << 32) | (unsigned)e;
+      }
+      s_key[e] = key;
+    }
+    __syncthreads();
+    // bitonic sort, ascending: the longest chains first, ties in entry order
+    for (int size = 2; size <= n2; size <<= 1)
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < n2; i += 1024) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const bool up = (i & size) == 0;
+            const unsigned long long a = s_key[i], b = s_key[j];
+            if ((a > b) == up) {
+              s_key[i] = b;
+              s_key[j] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    for (int i = tid; i < count; i += 1024) chains[i] = entry((int)(s_key[i] & 0xffffffffu));
+  } else {
+    // too many to sort here: the split chains' second parts first, then sequence order
+    for (int i = tid; i < count; i += 1024) chains[i] = entry(i < 2 * k ? N + i : i - 2 * k);
+  }
+}
+
 // ------------------------------------------------------------------------- host
 
 }  // namespace
 
+// The split area of a planned packed forward: chain table, counts, split list, the three
+// fp32 states per split and head, and X rows for every token (an upper bound).
+static size_t split_area_bytes(const ChunkArgs& a) {
+  if (!a.cu_seqlens) return 0;
+  return align_up(size_t(a.B + 2 * kMaxSplit) * sizeof(int4), 256) + 256 +
+         align_up(size_t(kMaxSplit) * sizeof(int4), 256) +
+         size_t(kMaxSplit) * 3 * size_t(a.H) * kD * kD * 4 +
+         align_up(size_t(a.total_T) * a.H * kD * 2, 256);
+}
+
+static void carve_split(const ChunkArgs& a, uint8_t* p, Ws& ws) {
+  ws.chains = reinterpret_cast<int4*>(p);
+  p += align_up(size_t(a.B + 2 * kMaxSplit) * sizeof(int4), 256);
+  ws.nchains = reinterpret_cast<int32_t*>(p);
+  p += 256;
+  ws.splits = reinterpret_cast<int4*>(p);
+  p += align_up(size_t(kMaxSplit) * sizeof(int4), 256);
+  ws.split_st = reinterpret_cast<float*>(p);
+  p += size_t(kMaxSplit) * 3 * size_t(a.H) * kD * kD * 4;
+  ws.xbuf = reinterpret_cast<__nv_bfloat16*>(p);
+}
+
 size_t chunk_split_workspace(const ChunkArgs& a) {
   const long long recs = slots_for(a) * a.H;
   const size_t coff = a.cu_seqlens ? align_up(size_t(a.B + 1) * 4, 256) : 0;
-  return record_bytes(recs) + coff;
+  return record_bytes(recs) + coff + split_area_bytes(a);
 }
 
 bool chunk_split_index_ok(const ChunkArgs& a) {
@@ -1288,7 +1699,7 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
   const long long rows = a.cu_seqlens ? a.total_T : (long long)a.B * a.T;
   const long long map_rows = rows > 0 ? rows : 1;
   const long long rec_rows = ws.recs > 0 ? ws.recs : 1;
-  CUtensorMap mqw, mku, mwr, mm, mo, mq, mk, mv, mg, ms0, mut;
+  CUtensorMap mqw, mku, mwr, mm, mo, mx, mq, mk, mv, mg, ms0, mut;
   // the backward's scan writes no output: its (unused) output map is laid over q
   // -W: the forward's records hold it token-major ([64 x 128] per record), in the space the
   // backward's -W^T records take ([128 x 64], the third part of ku)
@@ -1297,6 +1708,8 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
       !make_map_2d(&mwr, ws.ku + 2 * ws.recs * 8192, rec_rows * 64, 128, 64) ||
       !make_map_2d(&mm, ws.m, rec_rows * 64, 64, 64) ||
       !make_map_out(&mo, ws.bwd == 1 ? a.q : a.out, map_rows, a.H) ||
+      // X rows of the split chains (laid over q when the call plans no splits)
+      !make_map_out(&mx, ws.xbuf ? (const void*)ws.xbuf : a.q, map_rows, a.H) ||
       !make_map_in(&mq, a.q, map_rows, a.H, false) ||
       !make_map_in(&mk, a.k, map_rows, a.H, false) ||
       !make_map_in(&mv, a.v, map_rows, a.H, false) ||
@@ -1329,7 +1742,19 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
     prep<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mku, mwr, mm, mq, mk, mv, mg, a, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  scan<<<dim3(a.H, a.B), kSThreads, scan_smem, st>>>(mqw, mku, mwr, mm, mo, ms0, mut, a, ws);
+  // a planned scan has up to 2 kMaxSplit chains more than sequences (the unused CTAs exit)
+  const unsigned ny = (unsigned)a.B + (ws.chains ? 2u * kMaxSplit : 0u);
+  scan<<<dim3(a.H, ny), kSThreads, scan_smem, st>>>(mqw, mku, mwr, mm, mo, mx, ms0, mut, a, ws);
+  if ((e = cudaGetLastError()) != cudaSuccess || !ws.chains) return e;
+  // the split chains' correction (no work, and an immediate return, when nothing was split)
+  if ((e = cudaFuncSetAttribute(chunk_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kFSmem)) != cudaSuccess)
+    return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  chunk_fixup_kernel<<<sms, kFThreads, kFSmem, st>>>(mx, a, ws);
   return cudaGetLastError();
 }
 
@@ -1340,10 +1765,19 @@ cudaError_t split::launch_chunk_offsets(const ChunkArgs& a, const Ws& ws, cudaSt
 
 cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t st) {
   Ws ws{};
-  carve_records(a, workspace, ws);
+  uint8_t* p = carve_records(a, workspace, ws);
   if (a.cu_seqlens) {
-    const cudaError_t e = split::launch_chunk_offsets(a, ws, st);
-    if (e != cudaSuccess) return e;
+    // packed inputs: the chunk offsets and the scan's plan (chains, longest first, with the
+    // longest sequences split while that shortens the longest chain)
+    carve_split(a, p + align_up(size_t(a.B + 1) * 4, 256), ws);
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    chunk_plan_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.B, a.total_T, a.H, 2 * sms, ws.coff,
+                                          ws.chains, ws.nchains, ws.splits);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return split::launch_prep_scan(a, ws, st);
 }

@@ -128,7 +128,12 @@ int kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const floa
  *   kda_chunk_fwd_workspace_size / kda_chunk_fwd_varlen_workspace_size
  *       bytes of device workspace the matching call needs (0: none).  About 74 KB per
  *       (64-token chunk, head): 612 MB for B = 4, T = 4096, H = 32.  The varlen size is an
- *       upper bound from total_T and N (every sequence may end in a partial chunk).
+ *       upper bound from total_T and N (every sequence may end in a partial chunk), plus
+ *       the room to split the scans of up to 8 long sequences: a sequence's chunks form a
+ *       chain of affine state maps (S' = A S + B per chunk), and a long chain is cut in two
+ *       whose second half runs from zero beside a third chain from the identity, then
+ *       corrected by the first half's end state (three fp32 [128 x 128] states per split
+ *       sequence and head, and a bf16 [total_T, H, 128] buffer).
  *   workspace       DEVICE buffer of at least that many bytes, 256-byte aligned, owned by
  *                   the caller; its contents on entry are irrelevant and on return are
  *                   unspecified.  It must not be used by anything else until the stream

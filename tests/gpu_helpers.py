@@ -139,7 +139,7 @@ def run_chunk(d, B, T, H, dk, dv, scale, lb, chunk, bf16, want_state=True, alias
     return (out.float().cpu().numpy(), None if s1 is None else s1.cpu().numpy())
 
 
-def run_varlen(d, H, dk, dv, scale, lb, chunk, bf16, ws=False):
+def run_varlen(d, H, dk, dv, scale, lb, chunk, bf16, ws=False, keep_ws=None):
     io = torch.bfloat16 if bf16 else torch.float32
     total = d["q"].shape[0]
     N = len(d["cu_seqlens"]) - 1
@@ -154,6 +154,8 @@ def run_varlen(d, H, dk, dv, scale, lb, chunk, bf16, ws=False):
         w = workspace(kda.kda_chunk_fwd_varlen_workspace_size(N, total, H, dk, dv, chunk,
                                                               1 if bf16 else 0))
         kda.kda_chunk_fwd_varlen_ws(*args, workspace=w)
+        if keep_ws is not None:
+            keep_ws.append(w)
     else:
         kda.kda_chunk_fwd_varlen(*args)
     torch.cuda.synchronize()

@@ -137,10 +137,23 @@ def test_workspace_size_formula(L):
     assert ws(4, 4096, 32, 64, 128, 64, 1) == 0                  # dk = 64
     assert ws(-1, 4096, 32, 128, 128, 64, 1) == 0                # invalid
     vs = kda.kda_chunk_fwd_varlen_workspace_size
-    # upper bound: total_T / 64 + N chunks, plus the (N + 1) int32 offsets rounded to 256 B
-    assert vs(8, 1000, 16, 128, 128, 64, 1) == (1000 // 64 + 8) * 16 * REC + 256
-    assert vs(300, 64 * 300, 2, 128, 128, 64, 1) == (300 + 300) * 2 * REC + 1280
+    # upper bound: total_T / 64 + N chunks, plus the (N + 1) int32 offsets rounded to 256 B,
+    # plus the area for splitting long chains
+    assert vs(8, 1000, 16, 128, 128, 64, 1) == \
+        (1000 // 64 + 8) * 16 * REC + 256 + _split_area(8, 1000, 16)
+    assert vs(300, 64 * 300, 2, 128, 128, 64, 1) == \
+        (300 + 300) * 2 * REC + 1280 + _split_area(300, 64 * 300, 2)
     assert vs(8, 1000, 16, 128, 128, 64, 0) == 0
+
+
+def _split_area(N, total, H, max_split=8):
+    """The chain-split area of a packed forward: the chain table (N + 2 max_split int4), the
+    counts (256 B), the split list (max_split int4), three fp32 [128 x 128] states per split
+    sequence and head, and one bf16 row of 128 per (token, head); each part 256-byte
+    aligned."""
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    return (al((N + 2 * max_split) * 16) + 256 + al(max_split * 16) +
+            max_split * 3 * H * 128 * 128 * 4 + al(total * H * 128 * 2))
 
 
 def _chunk_ws(L, ws, nbytes, **over):

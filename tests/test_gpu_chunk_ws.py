@@ -177,3 +177,59 @@ def test_varlen_workload_8seq_full():
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(S))
     check_full("varlen 8 seq H16, kda_chunk_fwd_varlen_ws", out, ref_out, S, ref_S,
                d["cu_seqlens"])
+
+
+# One (chunk, head) record of the forward workspace: four bf16 [64 x 128] tiles, one bf16
+# [64 x 64] tile and 256 fp32 values.
+_REC = 4 * 64 * 128 * 2 + 64 * 64 * 2 + 256 * 4
+
+
+def _split_counts(w, N, total, H):
+    """(chains, split sequences) of the scan plan, read from the packed forward's workspace:
+    after the records come the (N + 1) chunk offsets and the chain table (N + 16 int4),
+    each 256-byte aligned, then the two counts."""
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    off = (total // 64 + N) * H * _REC + al((N + 1) * 4) + al((N + 16) * 16)
+    c = w.view(torch.uint8)[off:off + 8].cpu().numpy().view(np.int32)
+    return int(c[0]), int(c[1])
+
+
+def _varlen_split_case(lens, H, seed, lb, splits, initial=True):
+    d = synth.varlen_inputs(lens, H, 128, 128, seed=seed, state_std=0.1)
+    if not initial:
+        d["initial_state"] = None
+    kept = []
+    out, S = run_varlen(d, H, 128, 128, 0.09, lb, 64, True, ws=True, keep_ws=kept)
+    N, total = len(lens), int(sum(lens))
+    assert _split_counts(kept[0], N, total, H) == (N + 2 * splits, splits)
+    o = oracle_inputs(d, True)
+    ref_out, ref_S = kda_forward_varlen(o["q"], o["k"], o["v"], o["g"], o["beta_logits"],
+                                        o["a_log"], o["dt_bias"], d["cu_seqlens"], 0.09, lb,
+                                        o["initial_state"])
+    _check(out, S, ref_out, ref_S)
+    # the same call again gives the same bits (the plan and the correction are deterministic)
+    out2, S2 = run_varlen(d, H, 128, 128, 0.09, lb, 64, True, ws=True)
+    assert np.array_equal(out, out2) and np.array_equal(S, S2)
+    return d, S
+
+
+def test_varlen_split_one_long_sequence():
+    """One sequence much longer than the rest (65 chunks against at most 8): its scan is cut
+    at chunk 33 into three chains (the first part from the initial state, the second from
+    zero and from the identity) and corrected afterwards; an empty and a one-token sequence
+    ride along."""
+    d, S = _varlen_split_case([4133, 300, 500, 65, 1, 0], H=4, seed=41, lb=-2.0, splits=1)
+    np.testing.assert_array_equal(S[5], d["initial_state"][5])
+
+
+@pytest.mark.parametrize("lb,initial", [(-5.0, True), (-0.1, False)])
+def test_varlen_split_two_sequences_ragged_ends(lb, initial):
+    """Two long sequences (41 and 34 chunks, both ending in a partial chunk) split at chunks
+    21 and 17, strong and weak decay, with and without initial states."""
+    _varlen_split_case([64 * 40 + 17, 64 * 33 + 5, 200, 0], H=3, seed=42, lb=lb, splits=2,
+                       initial=initial)
+
+
+def test_varlen_no_split_for_equal_lengths():
+    """Equal lengths: cutting one chain cannot shorten the longest, so nothing is split."""
+    _varlen_split_case([64 * 20] * 3, H=2, seed=43, lb=-1.0, splits=0)
