@@ -1485,17 +1485,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
 // ------------------------------------------------------------ varlen chunk offsets
 
 // coff[0] = 0, coff[i + 1] = coff[i] + ceil(len_i / 64) (lengths clamped as seq_range does);
-// the whole block (1024 threads) takes part.
+// the whole block (a multiple of 32 threads, at most 1024) takes part.
 __device__ void chunk_offsets_body(const int32_t* cu, int N, int total_T, int32_t* coff) {
   __shared__ int s_warp[32];
   __shared__ int s_carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nt = blockDim.x, nw = nt >> 5;
   if (tid == 0) {
     s_carry = 0;
     coff[0] = 0;
   }
   __syncthreads();
-  for (int base = 0; base < N; base += 1024) {
+  for (int base = 0; base < N; base += nt) {
     const int i = base + tid;
     int c = 0;
     if (i < N) {
@@ -1513,20 +1514,20 @@ __device__ void chunk_offsets_body(const int32_t* cu, int N, int total_T, int32_
     if (lane == 31) s_warp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-      int w = s_warp[lane];
+      int w = lane < nw ? s_warp[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, w, o);
         if (lane >= o) w += y;
       }
-      s_warp[lane] = w;
+      if (lane < nw) s_warp[lane] = w;
     }
     __syncthreads();
     const int carry = s_carry;
     const int incl = x + (warp > 0 ? s_warp[warp - 1] : 0);
     if (i < N) coff[i + 1] = carry + incl;
     __syncthreads();
-    if (tid == 1023) s_carry = carry + incl;
+    if (tid == nt - 1) s_carry = carry + incl;
     __syncthreads();
   }
 }
@@ -1542,7 +1543,8 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
 // longest-first order, so that a scan with more chains than SMs starts the long ones first.
 constexpr int kPlanSort = 4096;  // chain tables up to this size are sorted
 constexpr int kPlanCache = 2048;  // chunk counts of up to this many sequences kept on chip
-__global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* cu, int N, int total_T,
+constexpr int kPlanThreads = 256;
+__global__ void __launch_bounds__(kPlanThreads) chunk_plan_kernel(const int32_t* cu, int N, int total_T,
                                                           int H, int budget, int32_t* coff,
                                                           int4* chains, int32_t* counts,
                                                           int4* splits) {
@@ -1552,17 +1554,18 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* cu, int
   __shared__ int s_top_seq[kMaxSplit + 1], s_top_len[kMaxSplit + 1];
   __shared__ int s_k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int nt = kPlanThreads, nw = kPlanThreads / 32;
   chunk_offsets_body(cu, N, total_T, coff);
   __syncthreads();  // coff (global memory) written by this block is visible to it
   const bool cached = N <= kPlanCache;
   if (cached)
-    for (int i = tid; i < N; i += 1024) s_nck[i] = coff[i + 1] - coff[i];
+    for (int i = tid; i < N; i += nt) s_nck[i] = coff[i + 1] - coff[i];
   __syncthreads();
   auto nck_of = [&](int i) { return cached ? s_nck[i] : coff[i + 1] - coff[i]; };
   // the r-th longest sequence (ties: the lower index) by a block maximum over the others
   auto select = [&](int r) {
     unsigned long long best = 0;
-    for (int i = tid; i < N; i += 1024) {
+    for (int i = tid; i < N; i += nt) {
       bool taken = false;
       for (int j = 0; j < r; ++j) taken |= (s_top_seq[j] == i);
       if (taken) continue;
@@ -1579,26 +1582,28 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* cu, int
     __syncthreads();
     if (tid == 0) {
       unsigned long long b = 0;
-      for (int w = 0; w < 32; ++w) b = s_red[w] > b ? s_red[w] : b;
+      for (int w = 0; w < nw; ++w) b = s_red[w] > b ? s_red[w] : b;
       s_top_seq[r] = (int)(0xffffffffu - (unsigned)(b & 0xffffffffu));
       s_top_len[r] = (int)(b >> 32);
     }
     __syncthreads();
   };
-  // split the longest sequences one at a time while that shortens the longest chain: after
-  // kk splits it is max(ceil(L_0 / 2), L_kk), L sorted descending (ranks found on demand)
-  if (tid == 0) s_k = 0;
-  for (int r = 0; r < min(2, N); ++r) select(r);
-  int crit = N > 0 ? s_top_len[0] : 0;
-  for (int kk = 1; kk <= min(kMaxSplit, N); ++kk) {
-    if (kk >= 2 && kk < N) select(kk);
-    bool accept = s_top_len[kk - 1] >= kSplitMinChunks &&
-                  (long long)(N + 2 * kk) * H <= (long long)budget;
-    const int nc = max((s_top_len[0] + 1) / 2, kk < N ? s_top_len[kk] : 0);
-    accept = accept && nc < crit;
-    if (!accept) break;  // uniform: every thread reads the same shared values
-    crit = nc;
-    if (tid == 0) s_k = kk;
+  // split the kk longest sequences, kk chosen to minimise the longest chain, which is then
+  // max(ceil(L_0 / 2), L_kk) (L sorted descending); the fewest splits on a tie
+  const int ranks = min(kMaxSplit + 1, N);
+  for (int r = 0; r < ranks; ++r) select(r);
+  if (tid == 0) {
+    int k = 0, crit = N > 0 ? s_top_len[0] : 0;
+    for (int kk = 1; kk <= min(kMaxSplit, N); ++kk) {
+      if (s_top_len[kk - 1] < kSplitMinChunks) break;
+      if ((long long)(N + 2 * kk) * H > (long long)budget) break;
+      const int nc = max((s_top_len[0] + 1) / 2, kk < N ? s_top_len[kk] : 0);
+      if (nc < crit) {
+        k = kk;
+        crit = nc;
+      }
+    }
+    s_k = k;
   }
   __syncthreads();
   if (tid == 0) {
@@ -1626,7 +1631,7 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* cu, int
   if (count <= kPlanSort) {
     int n2 = 1;
     while (n2 < count) n2 <<= 1;
-    for (int e = tid; e < n2; e += 1024) {
+    for (int e = tid; e < n2; e += nt) {
       unsigned long long key = ~0ull;  // padding sorts last
       if (e < count) {
         const int4 c = entry(e);
@@ -1638,7 +1643,7 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* cu, int
     // bitonic sort, ascending: the longest chains first, ties in entry order
     for (int size = 2; size <= n2; size <<= 1)
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < n2; i += 1024) {
+        for (int i = tid; i < n2; i += nt) {
           const int j = i ^ stride;
           if (j > i) {
             const bool up = (i & size) == 0;
@@ -1651,10 +1656,10 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const int32_t* cu, int
         }
         __syncthreads();
       }
-    for (int i = tid; i < count; i += 1024) chains[i] = entry((int)(s_key[i] & 0xffffffffu));
+    for (int i = tid; i < count; i += nt) chains[i] = entry((int)(s_key[i] & 0xffffffffu));
   } else {
     // too many to sort here: the split chains' second parts first, then sequence order
-    for (int i = tid; i < count; i += 1024) chains[i] = entry(i < 2 * k ? N + i : i - 2 * k);
+    for (int i = tid; i < count; i += nt) chains[i] = entry(i < 2 * k ? N + i : i - 2 * k);
   }
 }
 
@@ -1775,7 +1780,7 @@ cudaError_t launch_chunk_split(const ChunkArgs& a, void* workspace, cudaStream_t
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
-    chunk_plan_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.B, a.total_T, a.H, 2 * sms, ws.coff,
+    chunk_plan_kernel<<<1, kPlanThreads, 0, st>>>(a.cu_seqlens, a.B, a.total_T, a.H, 2 * sms, ws.coff,
                                           ws.chains, ws.nchains, ws.splits);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -230,6 +230,12 @@ def test_varlen_split_two_sequences_ragged_ends(lb, initial):
                        initial=initial)
 
 
-def test_varlen_no_split_for_equal_lengths():
-    """Equal lengths: cutting one chain cannot shorten the longest, so nothing is split."""
-    _varlen_split_case([64 * 20] * 3, H=2, seed=43, lb=-1.0, splits=0)
+def test_varlen_equal_lengths_split_together():
+    """Equal lengths: only cutting every chain shortens the longest, so all three are split
+    (20 chunks into 10 + 10, the cut on a chunk boundary at token 640)."""
+    _varlen_split_case([64 * 20] * 3, H=2, seed=43, lb=-1.0, splits=3)
+
+
+def test_varlen_short_chains_are_not_split():
+    """Chains under 16 chunks stay whole, however uneven the lengths."""
+    _varlen_split_case([64 * 14 + 3, 64, 10], H=2, seed=44, lb=-1.0, splits=0)
