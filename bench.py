@@ -52,8 +52,8 @@ def parse_args():
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the decode / varlen / e2e / cpu-baseline measurements")
-    p.add_argument("--profile", choices=["chunk", "chunk1", "decode", "varlen", "bwd", "bwd_full",
-                                         "gla", "gla_chunk"],
+    p.add_argument("--profile", choices=["chunk", "chunk1", "decode", "varlen", "varlen_full",
+                                         "bwd", "bwd_full", "gla", "gla_chunk"],
                    default=None,
                    help="run two launches of one kernel on a reduced case (for ncu) and exit")
     return p.parse_args()
@@ -714,6 +714,12 @@ def profile_case(which):
         w = replace(synth.PREFILL_B4, H=8) if which == "bwd" else synth.PREFILL_B4
         d, x = device_prefill(w)
         backward_measure(w, d, x, reps=1)
+    elif which == "varlen_full":
+        # two kda_chunk_fwd_varlen_ws calls on the 8-sequence packed workload (H = 16)
+        w = synth.VARLEN_8
+        _, x = device_prefill(w)
+        for _ in range(2):
+            call_chunk(w, x)
     else:
         w = replace(synth.PREFILL_B4, H=8) if which in ("chunk", "chunk1") else \
             replace(synth.VARLEN_8, H=4)
