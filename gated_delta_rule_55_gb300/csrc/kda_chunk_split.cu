@@ -1337,10 +1337,21 @@ __global__ void __launch_bounds__(kFThreads, 1)
   // a [128][128] fp32 matrix as bf16 (hi, lo) pairs: element (row, col) of the MN-major B
   // layout (mn) or of the K-major A layout
   auto stage_pair = [&](const float* src, uint32_t hi_off, uint32_t lo_off, bool mn) {
-    for (int q2 = tid; q2 < kD * kD / 8; q2 += kFThreads) {
+    // all of this thread's loads first (one round trip), then the conversions and stores
+    constexpr int kIt = kD * kD / 8 / kFThreads;
+    float4 ld[2 * kIt];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int q2 = tid + it * kFThreads;
       const int row = q2 >> 4, c8 = (q2 & 15) * 8;
-      const float4 x0 = *reinterpret_cast<const float4*>(src + row * kD + c8);
-      const float4 x1 = *reinterpret_cast<const float4*>(src + row * kD + c8 + 4);
+      ld[2 * it] = *reinterpret_cast<const float4*>(src + row * kD + c8);
+      ld[2 * it + 1] = *reinterpret_cast<const float4*>(src + row * kD + c8 + 4);
+    }
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int q2 = tid + it * kFThreads;
+      const int row = q2 >> 4, c8 = (q2 & 15) * 8;
+      const float4 x0 = ld[2 * it], x1 = ld[2 * it + 1];
       const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       uint32_t hw[4], lw[4];
 #pragma unroll
