@@ -239,3 +239,13 @@ def test_varlen_equal_lengths_split_together():
 def test_varlen_short_chains_are_not_split():
     """Chains under 16 chunks stay whole, however uneven the lengths."""
     _varlen_split_case([64 * 14 + 3, 64, 10], H=2, seed=44, lb=-1.0, splits=0)
+
+
+def test_varlen_many_sequences_past_the_plan_sort():
+    """5,000 packed sequences (mostly under one chunk, two long ones): more chains than the
+    plan sorts on chip (4,096) or keeps the chunk counts of (2,048), and more than two per
+    SM, so nothing is split and the chain table keeps sequence order."""
+    rng = np.random.default_rng(45)
+    lens = [int(x) for x in rng.integers(0, 6, 5000)]
+    lens[10], lens[3000] = 64 * 40, 64 * 18 + 5
+    _varlen_split_case(lens, H=1, seed=46, lb=-2.0, splits=0)
