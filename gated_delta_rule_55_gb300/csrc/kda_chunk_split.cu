@@ -1758,8 +1758,10 @@ cudaError_t split::launch_prep_scan(const ChunkArgs& a, const Ws& ws, cudaStream
     prep<<<(unsigned)grid, kPThreads, kPSmem, st>>>(mku, mwr, mm, mq, mk, mv, mg, a, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // a planned scan has up to 2 kMaxSplit chains more than sequences (the unused CTAs exit)
-  const unsigned ny = (unsigned)a.B + (ws.chains ? 2u * kMaxSplit : 0u);
+  // a planned scan has up to 2 kMaxSplit chains more than sequences (the unused CTAs exit);
+  // the grid's y extent stops at 65535, which only binds when no sequence can be split (the
+  // plan splits only while all chains fit in two per SM)
+  const unsigned ny = std::min(65535u, (unsigned)a.B + (ws.chains ? 2u * kMaxSplit : 0u));
   scan<<<dim3(a.H, ny), kSThreads, scan_smem, st>>>(mqw, mku, mwr, mm, mo, mx, ms0, mut, a, ws);
   if ((e = cudaGetLastError()) != cudaSuccess || !ws.chains) return e;
   // the split chains' correction (no work, and an immediate return, when nothing was split)
