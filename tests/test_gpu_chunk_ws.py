@@ -249,3 +249,32 @@ def test_varlen_many_sequences_past_the_plan_sort():
     lens = [int(x) for x in rng.integers(0, 6, 5000)]
     lens[10], lens[3000] = 64 * 40, 64 * 18 + 5
     _varlen_split_case(lens, H=1, seed=46, lb=-2.0, splits=0)
+
+
+def test_varlen_at_the_sequence_limit():
+    """65,535 packed sequences (the most the entry accepts; all but five empty), no initial or
+    final states: the scan's grid stops at the 65,535 CTAs of its y extent, and the outputs
+    of the five non-empty sequences match the oracle."""
+    N, H = 65535, 1
+    lens = np.zeros(N, dtype=np.int64)
+    picks = [0, 1000, 30000, 65000, N - 1]
+    lens[picks] = [130, 64, 1, 200, 77]
+    d = synth.varlen_inputs([int(x) for x in lens], H, 128, 128, seed=47, state_std=None)
+    total = int(lens.sum())
+    q, k, v = (to_dev(d[n], torch.bfloat16) for n in ("q", "k", "v"))
+    cu = torch.from_numpy(d["cu_seqlens"].astype(np.int32)).cuda()
+    out = torch.full((total, H, 128), float("nan"), device="cuda", dtype=torch.bfloat16)
+    w = workspace(kda.kda_chunk_fwd_varlen_workspace_size(N, total, H, 128, 128, 64, 1))
+    kda.kda_chunk_fwd_varlen_ws(q, k, v, to_dev(d["g"]), to_dev(d["beta_logits"]),
+                                to_dev(d["a_log"]), to_dev(d["dt_bias"]), 0.09, -2.0, cu, N,
+                                total, None, out, None, H, 128, 128, 64, workspace=w)
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy()
+    o = oracle_inputs(d, True)
+    cu_h = d["cu_seqlens"]
+    for n in picks:
+        a, b = int(cu_h[n]), int(cu_h[n + 1])
+        ref, _ = kda_forward(o["q"][None, a:b], o["k"][None, a:b], o["v"][None, a:b],
+                             o["g"][None, a:b], o["beta_logits"][None, a:b], o["a_log"],
+                             o["dt_bias"], 0.09, -2.0, None)
+        check_rel(None, f"out seq {n}", out[a:b], ref[0])
