@@ -1555,6 +1555,79 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* cu, 
 constexpr int kPlanSort = 4096;  // chain tables up to this size are sorted
 constexpr int kPlanCache = 2048;  // chunk counts of up to this many sequences kept on chip
 constexpr int kPlanThreads = 256;
+
+// chunks of packed sequence i (its length clamped as seq_range does)
+__device__ __forceinline__ int chunk_count(const int32_t* cu, int i, int total_T) {
+  int lo = cu[i], hi = cu[i + 1];
+  lo = min(max(lo, 0), total_T);
+  hi = min(max(hi, lo), total_T);
+  return (hi - lo + kC - 1) / kC;
+}
+
+// The plan of chunk_plan_kernel for at most kPlanThreads sequences, one per thread: every
+// sequence's rank by length (longer first, ties by index) and every chain's rank in the
+// table are counted directly (a few block barriers instead of selection rounds and a sort).
+__device__ void plan_small(const int32_t* cu, int N, int total_T, int H, int budget,
+                           int4* chains, int32_t* counts, int4* splits) {
+  __shared__ int s_len[kPlanThreads + 2 * kMaxSplit];
+  __shared__ int s_top_seq[kMaxSplit + 1], s_top_len[kMaxSplit + 1];
+  __shared__ int s_slot[kPlanThreads];  // split slot of each sequence, -1 if whole
+  __shared__ int s_k;
+  const int tid = threadIdx.x;
+  const int nck = tid < N ? chunk_count(cu, tid, total_T) : 0;
+  if (tid < N) s_len[tid] = nck;
+  __syncthreads();
+  if (tid < N) {
+    int r = 0;
+    for (int j = 0; j < N; ++j) r += (s_len[j] > nck) || (s_len[j] == nck && j < tid);
+    if (r <= kMaxSplit) {
+      s_top_seq[r] = tid;
+      s_top_len[r] = nck;
+    }
+    s_slot[tid] = -1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int k = 0, crit = N > 0 ? s_top_len[0] : 0;
+    for (int kk = 1; kk <= min(kMaxSplit, N); ++kk) {
+      if (s_top_len[kk - 1] < kSplitMinChunks) break;
+      if ((long long)(N + 2 * kk) * H > (long long)budget) break;
+      const int nc = max((s_top_len[0] + 1) / 2, kk < N ? s_top_len[kk] : 0);
+      if (nc < crit) {
+        k = kk;
+        crit = nc;
+      }
+    }
+    for (int s2 = 0; s2 < k; ++s2) {
+      splits[s2] = make_int4(s_top_seq[s2], (s_top_len[s2] + 1) / 2, s_top_len[s2], 0);
+      s_slot[s_top_seq[s2]] = s2;
+      // the second parts' lengths: entries N + 2 s2 (from zero) and N + 2 s2 + 1 (identity)
+      s_len[N + 2 * s2] = s_len[N + 2 * s2 + 1] = s_top_len[s2] - (s_top_len[s2] + 1) / 2;
+    }
+    s_k = k;
+    counts[0] = N + 2 * k;
+    counts[1] = k;
+  }
+  __syncthreads();
+  const int k = s_k, count = N + 2 * k;
+  if (tid < N && s_slot[tid] >= 0) s_len[tid] = (nck + 1) / 2;  // a split sequence's first part
+  __syncthreads();
+  for (int e = tid; e < count; e += kPlanThreads) {
+    const int len = s_len[e];
+    int r = 0;
+    for (int j = 0; j < count; ++j) r += (s_len[j] > len) || (s_len[j] == len && j < e);
+    int4 c;
+    if (e < N) {
+      const int s2 = s_slot[e];
+      c = s2 >= 0 ? make_int4(e, 0, len, 1 | (s2 << 2)) : make_int4(e, 0, len, 0);
+    } else {
+      const int s2 = (e - N) >> 1, part = (e - N) & 1;
+      const int mid = (s_top_len[s2] + 1) / 2;
+      c = make_int4(s_top_seq[s2], mid, s_top_len[s2], (2 + part) | (s2 << 2));
+    }
+    chains[r] = c;
+  }
+}
 __global__ void __launch_bounds__(kPlanThreads) chunk_plan_kernel(const int32_t* cu, int N, int total_T,
                                                           int H, int budget, int32_t* coff,
                                                           int4* chains, int32_t* counts,
@@ -1567,6 +1640,10 @@ __global__ void __launch_bounds__(kPlanThreads) chunk_plan_kernel(const int32_t*
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int nt = kPlanThreads, nw = kPlanThreads / 32;
   chunk_offsets_body(cu, N, total_T, coff);
+  if (N <= nt) {  // one sequence per thread: ranks by counting, no sort network
+    plan_small(cu, N, total_T, H, budget, chains, counts, splits);
+    return;
+  }
   __syncthreads();  // coff (global memory) written by this block is visible to it
   const bool cached = N <= kPlanCache;
   if (cached)
