@@ -1334,9 +1334,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
       tma_load_3d(sm + F_X + (q2 >> 1) * 16384 + (q2 & 1) * 8192, &map_x, &bar_x,
                   64 * (q2 >> 1), h, (int)(t_lo + 64 * (q2 & 1)));
   };
-  // a [128][128] fp32 matrix as bf16 (hi, lo) pairs: element (row, col) of the MN-major B
-  // layout (mn) or of the K-major A layout
-  auto stage_pair = [&](const float* src, uint32_t hi_off, uint32_t lo_off, bool mn) {
+  // a [128][128] fp32 matrix as bf16 (hi, lo) pairs, in the layout shared by the MN-major
+  // B operand (rows = k, columns = n) and the K-major A operand (rows = m, columns = k)
+  auto stage_pair = [&](const float* src, uint32_t hi_off, uint32_t lo_off) {
     // all of this thread's loads first (one round trip), then the conversions and stores
     constexpr int kIt = kD * kD / 8 / kFThreads;
     float4 ld[2 * kIt];
@@ -1359,12 +1359,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
         hw[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
         lw[e] = pack_bf16(x[2 * e] - bf16_lo(hw[e]), x[2 * e + 1] - bf16_hi(hw[e]));
       }
-      // both layouts: 64-column block c8 / 64 at 16 KB, rows of 128 bytes in 8-row
-      // swizzled groups (MN-major: row = k, columns = n; K-major: row = i, columns = k)
+      // 64-column block c8 / 64 at 16 KB, rows of 128 bytes in 8-row swizzled groups
       const uint32_t off = uint32_t(c8 >> 6) * 16384u + uint32_t(row >> 3) * 1024u +
                            uint32_t(row & 7) * 128u +
                            ((uint32_t((c8 & 63) >> 3) ^ uint32_t(row & 7)) << 4);
-      (void)mn;
       *reinterpret_cast<uint4*>(sm + hi_off + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       if (lo_off) *reinterpret_cast<uint4*>(sm + lo_off + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
@@ -1400,11 +1398,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
       for (int q2 = 0; q2 < 8; ++q2) ov[q2] = o4[q2];
     }
     if (staged != key) {  // (the previous unit's products, their last reader, are complete)
-      stage_pair(smid, F_B, F_BL, true);
+      stage_pair(smid, F_B, F_BL);
       staged = key;
     }
     if (state)
-      stage_pair(ws.split_st + ((long long)(3 * s2 + 2) * H + h) * sq, F_PH, F_PL, false);
+      stage_pair(ws.split_st + ((long long)(3 * s2 + 2) * H + h) * sq, F_PH, F_PL);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
