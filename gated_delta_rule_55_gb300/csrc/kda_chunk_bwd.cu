@@ -107,11 +107,8 @@ __device__ __forceinline__ float reduce_scatter8(float (&v)[8], int lane, int& t
   return v[0];
 }
 
-__device__ __forceinline__ float bf16_round(float x) {
-  return __bfloat162float(__float2bfloat16_rn(x));
-}
-
-// The pair (bf16_round(x.x), bf16_round(x.y)) through one bf16x2 conversion.
+// Both lanes of x rounded to the nearest bf16 value (kept in fp32), through one bf16x2
+// conversion.
 __device__ __forceinline__ float2 bf16_round2(float2 x) {
   const uint32_t p = pack_bf16(x.x, x.y);
   return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
@@ -504,15 +501,43 @@ __global__ void __launch_bounds__(kKThreads, 1)
   const int c = tid & 127;     // channel (Tensor Memory lane)
   const int sp = warp & 3;     // Tensor Memory sub-partition
   const int H = a.H;
-  const long long rec = blockIdx.x;
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kKTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_raw, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = s_tmem;
+  const uint32_t tl = tm + (uint32_t(32 * sp) << 16);
+  uint32_t mma_phase = 0;
+  uint32_t wait_calls = 0;
+  auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const uint32_t slot_w = wait_calls++ & 3;
+    if (tid == 0) s_wait_ok[slot_w] = mbar_wait(bar, parity) ? 1 : 0;
+    __syncthreads();
+    return s_wait_ok[slot_w] != 0;
+  };
+  bool raw_done = true, ld_done = true;
+  uint32_t ldp = 0;  // phase parity of bar_raw and bar_ld: records this CTA has processed
+  // Persistent: the CTA (one per SM) walks records blockIdx.x, + gridDim.x, ...; the TMEM
+  // allocation and the barriers are set up once, and each record's loads go out as soon as
+  // the previous record's last readers are done.
+  for (long long rec = blockIdx.x; rec < bw.f.recs; rec += gridDim.x) {
   const int h = (int)(rec % H);
   const long long slot = rec / H;
   int seq, jc;
   if (a.cu_seqlens) {
     // record -> sequence; records past the last chunk exist because their count is an
-    // upper bound for packed sequences (uniform over the CTA, before any setup)
+    // upper bound for packed sequences (uniform over the CTA)
     const int N = a.B;
-    if (slot >= bw.f.coff[N]) return;
+    if (slot >= bw.f.coff[N]) continue;
     int lo = 0, hi = N;  // coff[lo] <= slot < coff[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -530,15 +555,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   const long long tok0 = bos + (long long)jc * kC;
   const int n = min(kC, len - jc * kC);
 
-  if (warp == 0) {
-    tmem_alloc(&s_tmem, kKTmemCols);
-    tmem_relinquish();
-  }
   if (tid == 0) {
-    mbar_init(&bar_ld, 1);
-    mbar_init(&bar_raw, 1);
-    mbar_init(&bar_mma, 1);
-    fence_mbar_init();
     // this chunk's raw q, k, g first (the gates need them), then the records and states
     mbar_arrive_expect_tx(&bar_raw, kKRawTx);
     tma_load_3d(sm + K_RQ, &map_q, &bar_raw, 0, h, (int)tok0);
@@ -559,6 +576,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
     tma_load_2d(sm + K_DS, &map_ds, &bar_ld, 0, (int)(rec * 128));
     tma_load_2d(sm + K_DS + 16384, &map_ds, &bar_ld, 64, (int)(rec * 128));
   }
+  raw_done = ld_done = false;
   if (tid < kC) {
     s_beta[tid] = (tid < n) ? sigmoidf_(a.beta_logits[(tok0 + tid) * H + h]) : 0.f;
     s_rk[tid] = bw.f.vec[rec * 256 + 128 + tid];
@@ -566,20 +584,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
   const float ea = __expf(a.a_log[h]);
   const float db = a.dt_bias[c * H + h];
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tm = s_tmem;
-  const uint32_t tl = tm + (uint32_t(32 * sp) << 16);
-  uint32_t mma_phase = 0;
-  uint32_t wait_calls = 0;
-  auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    const uint32_t slot_w = wait_calls++ & 3;
-    if (tid == 0) s_wait_ok[slot_w] = mbar_wait(bar, parity) ? 1 : 0;
-    __syncthreads();
-    return s_wait_ok[slot_w] != 0;
-  };
-  bool raw_done = false, ld_done = false;
   float loc[16], P[4], fg[4], GC, PR;
 
   // element (t, c) of the staged tiles
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   auto row_of = [&](int t) -> long long { return (tok0 + t) * H + h; };
 
   // ---- gates: G_t - P_R for this thread's channel and sub-chunk
-  if (!block_wait(&bar_raw, 0)) goto fail;
+  if (!block_wait(&bar_raw, ldp & 1)) goto fail;
   raw_done = true;
   {
     float run = 0.f;
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
 
   // ---- loaded tiles: clear d_out rows past the chunk, S . dS' per channel (quarter of j)
-  if (!block_wait(&bar_ld, 0)) goto fail;
+  if (!block_wait(&bar_ld, ldp & 1)) goto fail;
   ld_done = true;
   if (n < kC) zero_rows(sm + K_DO, n, tid);
   {
@@ -978,13 +983,16 @@ __global__ void __launch_bounds__(kKThreads, 1)
       atomicAdd(&o.da_log[h], t);
     }
   }
+  ++ldp;
+  __syncthreads();  // this record's last readers are done before the next record's loads
+  }  // records
   goto done;
 
 fail:
   if (tid == 0) {
     atomicOr(&g_bwd_error, 4u);
-    if (!raw_done) mbar_wait(&bar_raw, 0, 1000000000ull);
-    if (!ld_done) mbar_wait(&bar_ld, 0, 1000000000ull);
+    if (!raw_done) mbar_wait(&bar_raw, ldp & 1, 1000000000ull);
+    if (!ld_done) mbar_wait(&bar_ld, ldp & 1, 1000000000ull);
     if (mma_phase > 0) mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
   }
 done:
@@ -1100,7 +1108,13 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const void* d_out, const float*
   bwd_scan_kernel<<<dim3(a.H, a.B), kBSThreads, kBSSmem, st>>>(mqw, mku, mm, mdo, mds, mdut, a,
                                                                  bw, o);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_chunk_kernel<<<(unsigned)recs, kKThreads, kKSmem, st>>>(mdut, mn, mut, mdo, ms0, mds, mq,
+  // persistent: one CTA per SM walks the records
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const long long grid = std::min<long long>(recs, sms);
+  bwd_chunk_kernel<<<(unsigned)grid, kKThreads, kKSmem, st>>>(mdut, mn, mut, mdo, ms0, mds, mq,
                                                                mk, mg, a, bw, o);
   return cudaGetLastError();
 }
