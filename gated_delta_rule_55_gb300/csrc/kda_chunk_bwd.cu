@@ -444,10 +444,11 @@ constexpr int K_END = 188416;
 constexpr int K_XL = K_DS;      // Xl [128 rows][128 c] (two boxes, 16384 apart): after dKd^T
 constexpr int K_KB = 0;         // Kb [160 rows][128 c] (two boxes, 20480 apart): after dA, dM
 constexpr int K_D1 = K_DO;      // dD1 [128 rows][192] (three boxes, 16384 apart): after dA, dM
-constexpr int K_AQ = 0;         // fp32 [64 tok][128 c] dq^ (epilogue)
-constexpr int K_DKH = 32768;    // fp32 [64 tok][128 c] dk^
+// The epilogue reads only the raw tiles and Tensor Memory, so the next record's loaded tiles
+// (everything below K_RQ) go out once the last MMA group is done, and its raw tiles once the
+// epilogue's first half has read them.
 static_assert(K_KB + 2 * 20480 <= K_D1 && K_D1 + 3 * 16384 <= K_XL, "late tiles overlap");
-static_assert(K_XL + 32768 <= K_RQ && K_DKH + 32768 <= K_RQ, "late tiles overlap the raw tiles");
+static_assert(K_XL + 32768 <= K_RQ, "late tiles overlap the raw tiles");
 static_assert(K_DO + 3 * 8192 <= K_END, "rows 64..127 of the d_out A operand read in bounds");
 static_assert(K_DUT + 2 * 16384 <= K_DO, "second M block of the dV^T A operand in bounds");
 constexpr uint32_t kKLoadTx = 16384 + 8192 + 16384 + 16384 + 32768 + 32768;
@@ -464,6 +465,36 @@ constexpr uint32_t KT_DM = 320;  // dO U^T [r][s] (lanes 0..63)
 constexpr uint32_t KT_P6 = 192;  // dXl^T [c][row], 128 (after lam, dA, dM are read)
 constexpr uint32_t KT_P7 = 320;  // dKb^T [c][col], 160
 constexpr uint32_t kKTmemCols = 512;
+// Between the epilogue's halves each thread keeps its 16 tokens' dq^, dk^, q^, k^ and gate
+// argument in Tensor Memory cells that only it reads, once it has read them: the columns
+// 16 R .. 16 R + 15 of P1, P2, P3 and of both halves of P6, in its own lane.
+constexpr uint32_t KT_KEEP_AQ = KT_P1, KT_KEEP_DKH = KT_P2, KT_KEEP_QH = KT_P3,
+                   KT_KEEP_KH = KT_P6, KT_KEEP_X = KT_P6 + 64;
+
+// Store 8 consecutive 32-bit columns of this thread's lane; completion is waited for by
+// tmem_wait_st.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 
 // first Kb row (and dD1 column) of the block that refers the earlier tokens to P_g
 __device__ __forceinline__ int kb_base(int g) { return g == 1 ? 64 : g == 2 ? 80 : 112; }
@@ -524,59 +555,77 @@ __global__ void __launch_bounds__(kKThreads, 1)
     __syncthreads();
     return s_wait_ok[slot_w] != 0;
   };
-  bool raw_done = true, ld_done = true;
-  uint32_t ldp = 0;  // phase parity of bar_raw and bar_ld: records this CTA has processed
-  // Persistent: the CTA (one per SM) walks records blockIdx.x, + gridDim.x, ...; the TMEM
-  // allocation and the barriers are set up once, and each record's loads go out as soon as
-  // the previous record's last readers are done.
-  for (long long rec = blockIdx.x; rec < bw.f.recs; rec += gridDim.x) {
-  const int h = (int)(rec % H);
-  const long long slot = rec / H;
-  int seq, jc;
-  if (a.cu_seqlens) {
-    // record -> sequence; records past the last chunk exist because their count is an
-    // upper bound for packed sequences (uniform over the CTA)
-    const int N = a.B;
-    if (slot >= bw.f.coff[N]) continue;
-    int lo = 0, hi = N;  // coff[lo] <= slot < coff[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (bw.f.coff[mid] <= slot) lo = mid; else hi = mid;
+  // Loads go out from thread 0: raw_armed / ld_armed count the phases it has armed on
+  // bar_raw / bar_ld, raw_seen / ld_seen the phases the block has waited for.  Every record
+  // takes one phase of each, so the record's phase is the count of records processed.
+  uint32_t raw_armed = 0, ld_armed = 0, raw_seen = 0, ld_seen = 0;
+  long long early = -1;  // thread 0: the record whose loads went out during the previous one
+  // record -> first token and token count; false for the slots past the last chunk of packed
+  // sequences (their count is an upper bound), which come after every live slot
+  auto locate = [&](long long r, long long& t0, int& cnt) -> bool {
+    const long long slot = r / H;
+    int seq, jc;
+    if (a.cu_seqlens) {
+      const int N = a.B;
+      if (slot >= bw.f.coff[N]) return false;
+      int lo = 0, hi = N;  // coff[lo] <= slot < coff[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (bw.f.coff[mid] <= slot) lo = mid; else hi = mid;
+      }
+      seq = lo;
+      jc = (int)(slot - bw.f.coff[lo]);
+    } else {
+      seq = (int)(slot / bw.f.nck_fixed);
+      jc = (int)(slot % bw.f.nck_fixed);
     }
-    seq = lo;
-    jc = (int)(slot - bw.f.coff[lo]);
-  } else {
-    seq = (int)(slot / bw.f.nck_fixed);
-    jc = (int)(slot % bw.f.nck_fixed);
-  }
-  long long bos;
-  int len;
-  seq_range(a, seq, bos, len);
-  const long long tok0 = bos + (long long)jc * kC;
-  const int n = min(kC, len - jc * kC);
-
-  if (tid == 0) {
-    // this chunk's raw q, k, g first (the gates need them), then the records and states
+    long long bos;
+    int len;
+    seq_range(a, seq, bos, len);
+    t0 = bos + (long long)jc * kC;
+    cnt = min(kC, len - jc * kC);
+    return true;
+  };
+  // the chunk's raw q, k, g (thread 0)
+  auto issue_raw = [&](long long r, long long t0) {
+    const int hr = (int)(r % H);
     mbar_arrive_expect_tx(&bar_raw, kKRawTx);
-    tma_load_3d(sm + K_RQ, &map_q, &bar_raw, 0, h, (int)tok0);
-    tma_load_3d(sm + K_RQ + 8192, &map_q, &bar_raw, 64, h, (int)tok0);
-    tma_load_3d(sm + K_RK, &map_k, &bar_raw, 0, h, (int)tok0);
-    tma_load_3d(sm + K_RK + 8192, &map_k, &bar_raw, 64, h, (int)tok0);
+    tma_load_3d(sm + K_RQ, &map_q, &bar_raw, 0, hr, (int)t0);
+    tma_load_3d(sm + K_RQ + 8192, &map_q, &bar_raw, 64, hr, (int)t0);
+    tma_load_3d(sm + K_RK, &map_k, &bar_raw, 0, hr, (int)t0);
+    tma_load_3d(sm + K_RK + 8192, &map_k, &bar_raw, 64, hr, (int)t0);
 #pragma unroll
     for (int qt = 0; qt < 4; ++qt)
-      tma_load_3d(sm + K_RG + qt * 8192, &map_g, &bar_raw, 32 * qt, h, (int)tok0);
+      tma_load_3d(sm + K_RG + qt * 8192, &map_g, &bar_raw, 32 * qt, hr, (int)t0);
+    ++raw_armed;
+  };
+  // the record's tiles, states and d_out (thread 0)
+  auto issue_ld = [&](long long r, long long t0) {
+    const int hr = (int)(r % H);
     mbar_arrive_expect_tx(&bar_ld, kKLoadTx);
-    tma_load_2d(sm + K_DUT, &map_dut, &bar_ld, 0, (int)(rec * 128));
-    tma_load_2d(sm + K_NN, &map_n, &bar_ld, 0, (int)(rec * 64));
-    tma_load_2d(sm + K_UT, &map_ut, &bar_ld, 0, (int)(rec * 128));
-    tma_load_3d(sm + K_DO, &map_do, &bar_ld, 0, h, (int)tok0);
-    tma_load_3d(sm + K_DO + 8192, &map_do, &bar_ld, 64, h, (int)tok0);
-    tma_load_2d(sm + K_S0, &map_s0, &bar_ld, 0, (int)(rec * 128));
-    tma_load_2d(sm + K_S0 + 16384, &map_s0, &bar_ld, 64, (int)(rec * 128));
-    tma_load_2d(sm + K_DS, &map_ds, &bar_ld, 0, (int)(rec * 128));
-    tma_load_2d(sm + K_DS + 16384, &map_ds, &bar_ld, 64, (int)(rec * 128));
+    tma_load_2d(sm + K_DUT, &map_dut, &bar_ld, 0, (int)(r * 128));
+    tma_load_2d(sm + K_NN, &map_n, &bar_ld, 0, (int)(r * 64));
+    tma_load_2d(sm + K_UT, &map_ut, &bar_ld, 0, (int)(r * 128));
+    tma_load_3d(sm + K_DO, &map_do, &bar_ld, 0, hr, (int)t0);
+    tma_load_3d(sm + K_DO + 8192, &map_do, &bar_ld, 64, hr, (int)t0);
+    tma_load_2d(sm + K_S0, &map_s0, &bar_ld, 0, (int)(r * 128));
+    tma_load_2d(sm + K_S0 + 16384, &map_s0, &bar_ld, 64, (int)(r * 128));
+    tma_load_2d(sm + K_DS, &map_ds, &bar_ld, 0, (int)(r * 128));
+    tma_load_2d(sm + K_DS + 16384, &map_ds, &bar_ld, 64, (int)(r * 128));
+    ++ld_armed;
+  };
+  // Persistent: the CTA (one per SM) walks records blockIdx.x, + gridDim.x, ...; the TMEM
+  // allocation and the barriers are set up once, and each next record's loads go out while
+  // the current record's epilogue runs.
+  for (long long rec = blockIdx.x; rec < bw.f.recs; rec += gridDim.x) {
+  const int h = (int)(rec % H);
+  long long tok0;
+  int n;
+  if (!locate(rec, tok0, n)) continue;  // uniform over the CTA
+  if (tid == 0 && early != rec) {
+    issue_raw(rec, tok0);
+    issue_ld(rec, tok0);
   }
-  raw_done = ld_done = false;
   if (tid < kC) {
     s_beta[tid] = (tid < n) ? sigmoidf_(a.beta_logits[(tok0 + tid) * H + h]) : 0.f;
     s_rk[tid] = bw.f.vec[rec * 256 + 128 + tid];
@@ -600,8 +649,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
   auto row_of = [&](int t) -> long long { return (tok0 + t) * H + h; };
 
   // ---- gates: G_t - P_R for this thread's channel and sub-chunk
-  if (!block_wait(&bar_raw, ldp & 1)) goto fail;
-  raw_done = true;
+  if (!block_wait(&bar_raw, raw_seen & 1)) goto fail;
+  ++raw_seen;
   {
     float run = 0.f;
 #pragma unroll
@@ -616,8 +665,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
 
   // ---- loaded tiles: clear d_out rows past the chunk, S . dS' per channel (quarter of j)
-  if (!block_wait(&bar_ld, ldp & 1)) goto fail;
-  ld_done = true;
+  if (!block_wait(&bar_ld, ld_seen & 1)) goto fail;
+  ++ld_seen;
   if (n < kC) zero_rows(sm + K_DO, n, tid);
   {
     float acc = 0.f;
@@ -804,11 +853,15 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
   if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
   tc_fence_after();
+  // the next record's tiles, states and d_out: nothing below K_RQ is read from here on
+  if (tid == 0 && rec + gridDim.x < bw.f.recs) {
+    long long nt0;
+    int ncnt;
+    if (locate(rec + gridDim.x, nt0, ncnt)) issue_ld(rec + gridDim.x, nt0);
+  }
 
   // ---- epilogue: per (channel c, token t of sub-chunk R)
   {
-    float* AQ = reinterpret_cast<float*>(sm + K_AQ);
-    float* DKH = reinterpret_cast<float*>(sm + K_DKH);
     const float eP = fast_exp(PR), eCP = fast_exp(GC - PR);
     float dG[16];
     // token pairs (t, t + 1) ride Blackwell's two-lane fp32 instructions; every pair operation
@@ -893,23 +946,44 @@ __global__ void __launch_bounds__(kKThreads, 1)
             DG[p] = __ffma2_rn(bf16_round2(__fmul2_rn(NKD[p], fgv)), T[p], DG[p]);
           }
         }
-      float qd[8], kd[8];
+      float qd[8], kd[8], keep[8];
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         const float2 dkh = __fadd2_rn(POS[p], NEG[p]);
         const int i = 2 * p;
         dG[8 * hh + i] = DG[p].x;
         dG[8 * hh + i + 1] = DG[p].y;
-        AQ[(cb + i) * kD + c] = AQ2[p].x;
-        AQ[(cb + i + 1) * kD + c] = AQ2[p].y;
-        DKH[(cb + i) * kD + c] = dkh.x;
-        DKH[(cb + i + 1) * kD + c] = dkh.y;
         const float2 q2 = __fmul2_rn(QH[p], AQ2[p]), k2 = __fmul2_rn(KH[p], dkh);
         qd[i] = q2.x;
         qd[i + 1] = q2.y;
         kd[i] = k2.x;
         kd[i + 1] = k2.y;
+        keep[i] = dkh.x;
+        keep[i + 1] = dkh.y;
       }
+      // kept for the second half: dq^, dk^, q^, k^ and the gate argument of these tokens
+      tmem_st8(tl + KT_KEEP_DKH + cb, keep);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        keep[2 * p] = AQ2[p].x;
+        keep[2 * p + 1] = AQ2[p].y;
+      }
+      tmem_st8(tl + KT_KEEP_AQ + cb, keep);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        keep[2 * p] = QH[p].x;
+        keep[2 * p + 1] = QH[p].y;
+      }
+      tmem_st8(tl + KT_KEEP_QH + cb, keep);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        keep[2 * p] = KH[p].x;
+        keep[2 * p + 1] = KH[p].y;
+      }
+      tmem_st8(tl + KT_KEEP_KH + cb, keep);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) keep[i] = ea * (rg_t[(cb + i) * 32] + db);
+      tmem_st8(tl + KT_KEEP_X + cb, keep);
       int tq;
       const float qs = reduce_scatter8(qd, lane, tq);
       const float ks = reduce_scatter8(kd, lane, tq);
@@ -926,7 +1000,17 @@ __global__ void __launch_bounds__(kKThreads, 1)
       s_dgs[R][c] = sg;
       s_dgc[R][c] = dgc;
     }
+    tmem_wait_st();
     __syncthreads();
+    // the next record's raw q, k, g: the raw tiles are not read from here on
+    if (tid == 0 && rec + gridDim.x < bw.f.recs) {
+      long long nt0;
+      int ncnt;
+      if (locate(rec + gridDim.x, nt0, ncnt)) {
+        issue_raw(rec + gridDim.x, nt0);
+        early = rec + gridDim.x;
+      }
+    }
     // dgamma_t = sum_{r >= t} dG_r + dG_C
     const float dGC = s_dgc[0][c] + s_dgc[1][c] + s_dgc[2][c] + s_dgc[3][c] +
                       fast_exp(GC) * (s_sdot[0][c] + s_sdot[1][c] + s_sdot[2][c] + s_sdot[3][c]);
@@ -951,24 +1035,32 @@ __global__ void __launch_bounds__(kKThreads, 1)
     __nv_bfloat16* const dq_p = o.dq + base;
     __nv_bfloat16* const dk_p = o.dk + base;
 #pragma unroll
-    for (int i = 15; i >= 0; --i) {
-      carry += dG[i];
-      const int t = 16 * R + i;
-      if (t < n) {
-        // gate: gamma = lb sigmoid(x), x = e^{a_log} (g + dt_bias)
-        const float x = ea * (rg_t[t * 32] + db);
-        const float sg = fast_rcp(1.f + fast_exp(-x));
-        const float dx = carry * lb * sg * (1.f - sg);
-        dg_p[i * tstride] = dx * ea;
-        ddb += dx * ea;
-        dal += dx * x;
-        // L2 norms: q^ = rq q with rq = scale / |q|, k^ = rk k
-        const float qdt = s_qd[0][t], kdt = s_kd[0][t];
-        const float rq = s_rq[t], rk = s_rk[t];
-        const float qh = raw_q(t) * rq;
-        const float kh = raw_k(t) * rk;
-        dq_p[i * tstride] = __float2bfloat16_rn(rq * AQ[t * kD + c] - qh * qdt * rq * inv_s2);
-        dk_p[i * tstride] = __float2bfloat16_rn(rk * DKH[t * kD + c] - kh * kdt * rk);
+    for (int qq = 3; qq >= 0; --qq) {
+      const int cb = 16 * R + 4 * qq;
+      float aq[4], dkh[4], qh[4], kh[4], xg[4];
+      tmem_ld4(tl + KT_KEEP_AQ + cb, aq);
+      tmem_ld4(tl + KT_KEEP_DKH + cb, dkh);
+      tmem_ld4(tl + KT_KEEP_QH + cb, qh);
+      tmem_ld4(tl + KT_KEEP_KH + cb, kh);
+      tmem_ld4(tl + KT_KEEP_X + cb, xg);
+#pragma unroll
+      for (int i = 3; i >= 0; --i) {
+        carry += dG[4 * qq + i];
+        const int t = cb + i;
+        if (t < n) {
+          // gate: gamma = lb sigmoid(x), x = e^{a_log} (g + dt_bias)
+          const float x = xg[i];
+          const float sg = fast_rcp(1.f + fast_exp(-x));
+          const float dx = carry * lb * sg * (1.f - sg);
+          dg_p[(4 * qq + i) * tstride] = dx * ea;
+          ddb += dx * ea;
+          dal += dx * x;
+          // L2 norms: q^ = rq q with rq = scale / |q|, k^ = rk k
+          const float qdt = s_qd[0][t], kdt = s_kd[0][t];
+          const float rq = s_rq[t], rk = s_rk[t];
+          dq_p[(4 * qq + i) * tstride] = __float2bfloat16_rn(rq * aq[i] - qh[i] * qdt * rq * inv_s2);
+          dk_p[(4 * qq + i) * tstride] = __float2bfloat16_rn(rk * dkh[i] - kh[i] * kdt * rk);
+        }
       }
     }
     s_ddb[R][c] = ddb;
@@ -983,16 +1075,18 @@ __global__ void __launch_bounds__(kKThreads, 1)
       atomicAdd(&o.da_log[h], t);
     }
   }
-  ++ldp;
-  __syncthreads();  // this record's last readers are done before the next record's loads
+  __syncthreads();  // this record's last readers of Tensor Memory and of the small arrays are
+                    // done before the next record writes them
   }  // records
   goto done;
 
 fail:
   if (tid == 0) {
     atomicOr(&g_bwd_error, 4u);
-    if (!raw_done) mbar_wait(&bar_raw, ldp & 1, 1000000000ull);
-    if (!ld_done) mbar_wait(&bar_ld, ldp & 1, 1000000000ull);
+    // at most one phase of each is in flight: the next is armed only after the block has
+    // waited for the current one
+    if (raw_armed > raw_seen) mbar_wait(&bar_raw, raw_seen & 1, 1000000000ull);
+    if (ld_armed > ld_seen) mbar_wait(&bar_ld, ld_seen & 1, 1000000000ull);
     if (mma_phase > 0) mbar_wait(&bar_mma, (mma_phase - 1) & 1, 1000000000ull);
   }
 done:
