@@ -196,42 +196,72 @@ __global__ void __launch_bounds__(gla_threads<D>()) gla_kernel(GlaArgs a) {
       s_vb[u][jj] = make_float2(load_as_float(&r.v[u][jj]), a.gv ? __expf(r.gv[u][jj]) : 1.f);
     }
     __syncthreads();
-    for (int u = 0; u < nb; ++u) {
-      const float4 vb01 = *reinterpret_cast<const float4*>(&s_vb[u][4 * c4]);
-      const float4 vb23 = *reinterpret_cast<const float4*>(&s_vb[u][4 * c4 + 2]);
-      const uint64_t vv2[4] = {f2pack(vb01.x, vb01.x), f2pack(vb01.z, vb01.z),
-                               f2pack(vb23.x, vb23.x), f2pack(vb23.z, vb23.z)};
-      const uint64_t bb2[4] = {f2pack(vb01.y, vb01.y), f2pack(vb01.w, vb01.w),
-                               f2pack(vb23.y, vb23.y), f2pack(vb23.w, vb23.w)};
-      uint64_t o2[4] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+    // every token of the block advances the state and leaves this thread's partial output
+    // (its row pairs, four columns); the partials are summed over the warp's row groups once
+    // per block.  Unrolled over the block, so that the next token's operand loads go out
+    // while the current token's products run.
+    float po[kTB * 4];
 #pragma unroll
-      for (int i = 0; i < PPT; ++i) {
-        const int c = 2 * (rg + NRG * i);
-        const uint64_t k2 = *reinterpret_cast<const uint64_t*>(&s_k[u][c]);
-        const uint64_t ea2 = *reinterpret_cast<const uint64_t*>(&s_ea[u][c]);
-        const uint64_t q2 = *reinterpret_cast<const uint64_t*>(&s_q[u][c]);
+    for (int u = 0; u < kTB; ++u) {
+      if (u < nb) {  // uniform
+        const float4 vb01 = *reinterpret_cast<const float4*>(&s_vb[u][4 * c4]);
+        const float4 vb23 = *reinterpret_cast<const float4*>(&s_vb[u][4 * c4 + 2]);
+        const uint64_t vv2[4] = {f2pack(vb01.x, vb01.x), f2pack(vb01.z, vb01.z),
+                                 f2pack(vb23.x, vb23.x), f2pack(vb23.z, vb23.z)};
+        const uint64_t bb2[4] = {f2pack(vb01.y, vb01.y), f2pack(vb01.w, vb01.w),
+                                 f2pack(vb23.y, vb23.y), f2pack(vb23.w, vb23.w)};
+        uint64_t o2[4] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f), f2pack(0.f, 0.f),
+                          f2pack(0.f, 0.f)};
+#pragma unroll
+        for (int i = 0; i < PPT; ++i) {
+          const int c = 2 * (rg + NRG * i);
+          const uint64_t k2 = *reinterpret_cast<const uint64_t*>(&s_k[u][c]);
+          const uint64_t ea2 = *reinterpret_cast<const uint64_t*>(&s_ea[u][c]);
+          const uint64_t q2 = *reinterpret_cast<const uint64_t*>(&s_q[u][c]);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            // S = (e^{a} e^{gv}) S + k v, then the output partial q . S over the two rows
+            S2[i][jj] = f2fma(f2mul(ea2, bb2[jj]), S2[i][jj], f2mul(k2, vv2[jj]));
+            o2[jj] = f2fma(S2[i][jj], q2, o2[jj]);
+          }
+        }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          // S = (e^{a} e^{gv}) S + k v, then the output partial q . S over the two rows
-          S2[i][jj] = f2fma(f2mul(ea2, bb2[jj]), S2[i][jj], f2mul(k2, vv2[jj]));
-          o2[jj] = f2fma(S2[i][jj], q2, o2[jj]);
+          float lo, hi;
+          f2unpack(o2[jj], lo, hi);
+          po[4 * u + jj] = lo + hi;
         }
-      }
-      float o[4];
+      } else {
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        float lo, hi;
-        f2unpack(o2[jj], lo, hi);
-        o[jj] = lo + hi;
+        for (int jj = 0; jj < 4; ++jj) po[4 * u + jj] = 0.f;
       }
-      // the warp's four row groups (lanes c4, c4 + 8, c4 + 16, c4 + 24) share columns
+    }
+    // sums over the warp's four row groups (lanes c4, c4 + 8, c4 + 16, c4 + 24), scattered:
+    // lane bit 3 picks a half of the 32 (token, column) partials, lane bit 4 a quarter, so
+    // that every lane ends with the totals of two tokens (same pairing of the additions as
+    // a per-token butterfly)
+    {
+      const bool up1 = (lane & 8) != 0, up2 = (lane & 16) != 0;
+      float h1[kTB * 2];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        o[jj] += __shfl_xor_sync(0xffffffffu, o[jj], 8);
-        o[jj] += __shfl_xor_sync(0xffffffffu, o[jj], 16);
+      for (int i = 0; i < kTB * 2; ++i) {
+        const float send = up1 ? po[i] : po[i + kTB * 2];
+        const float keep = up1 ? po[i + kTB * 2] : po[i];
+        h1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
       }
-      if (lane < 8)
-        *reinterpret_cast<float4*>(&s_o[u][w][4 * c4]) = make_float4(o[0], o[1], o[2], o[3]);
+      float h2[kTB];
+#pragma unroll
+      for (int i = 0; i < kTB; ++i) {
+        const float send = up2 ? h1[i] : h1[i + kTB];
+        const float keep = up2 ? h1[i + kTB] : h1[i];
+        h2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+      // this lane's totals: partial indices 2 kTB up1 + kTB up2 + (0 .. kTB - 1)
+      const int u0 = (2 * kTB * (up1 ? 1 : 0) + kTB * (up2 ? 1 : 0)) / 4;
+#pragma unroll
+      for (int m = 0; m < kTB / 4; ++m)
+        *reinterpret_cast<float4*>(&s_o[u0 + m][w][4 * c4]) =
+            make_float4(h2[4 * m], h2[4 * m + 1], h2[4 * m + 2], h2[4 * m + 3]);
     }
     __syncthreads();
     for (int e = tid; e < nb * kDVS; e += kThreads) {
