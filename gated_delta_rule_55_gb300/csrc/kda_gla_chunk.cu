@@ -1,7 +1,7 @@
-// Chunked form of the recurrent page's gated linear recurrence on the tensor cores, for
-// key-axis gates only (g, gk, g_gamma; no value-axis gate gv), bf16 q/k/v with head dim 128,
-// 64-token chunks, forward order (ejkernel "recurrent" page, run / recurrent_attention:
-// query, key, value, g, gk, g_gamma, initial_state, cu_seqlens, softmax_scale).
+// Chunked form of the recurrent page's gated linear recurrence on the tensor cores: key-axis
+// gates (g, gk, g_gamma) and the value-axis gate gv, bf16 q/k/v with head dim 128, 64-token
+// chunks, forward order (ejkernel "recurrent" page, run / recurrent_attention: query, key,
+// value, g, gk, gv, g_gamma, initial_state, cu_seqlens, softmax_scale).
 //
 // With a_t = g_t + gk_t + g_gamma per key channel, the recurrence
 //     h_t = diag(e^{a_t}) h_{t-1} + k_t v_t^T,   o_t = h_t^T (scale q_t)
@@ -23,6 +23,20 @@
 //                    and S^T <- S^T diag(e^{G_C}) + V^T K^ (V^T read as staged from the
 //                    input, MN-major), the fp32 state in Tensor Memory with a bf16 copy as
 //                    the A operand of the next chunk's output product.
+//
+// With a value-axis gate, b_t = gv_t per value column and h_t = diag(e^{a_t}) h_{t-1}
+// diag(e^{b_t}) + k_t v_t^T.  With B_r = b_1 + .. + b_r in the chunk, the pair (r, s <= r)
+// carries e^{B_r - B_s} per value column, so per chunk
+//     O = scale (e^{B} o (Q~ S) + sum_s M_rs v_s e^{B_r - B_s}),
+//     S' = diag(e^{G_C}) S diag(e^{B_C}) + K^^T V^,   V^_s = v_s e^{B_C - B_s},
+// (o: elementwise over (r, value column)).  The in-chunk sum is split at the value side's
+// own 16-token reference points Q_R (B just before sub-chunk R): for r in sub-chunk R and s
+// in sub-chunk R' <= R, e^{B_r - B_s} = e^{B_r - Q_R} e^{Q_R - Q_R'} e^{Q_R' - B_s}, so with
+// V~_s = v_s e^{Q_R(s) - B_s} and Y_R' = M[:, R'] V~[R'] (one K = 16 product per R'),
+//     O_r = scale e^{B_r - Q_R} (e^{Q_R} (Q~ S)_r + sum_{R' <= R} e^{Q_R - Q_R'} Y_R',r),
+// every factor within e^{16 |b|} like the key side's.
+//  gla_vprep_kernel  (value gate only) per (chunk, query head): V^, V~, e^{B_r - Q_R} and the
+//                    sub-chunk totals of b, for the scan.
 #include "chunk_records.cuh"
 
 namespace kda {
@@ -41,12 +55,20 @@ constexpr long long kGRecQ = 64LL * 128 * 2;   // Q~ [64 tok][128] bf16
 constexpr long long kGRecK = 128LL * 64 * 2;   // K^^T [128][64 tok] bf16
 constexpr long long kGRecM = 64LL * 64 * 2;    // M [64][64] bf16
 constexpr long long kGRecVec = 256 * 4;        // e^{G_C} [128], scale per live row [64], pad
+constexpr long long kGRecV = 64LL * 128 * 2;   // V^, V~ or e^{B - Q} [64 tok][128] bf16
+constexpr long long kGRecVTot = 4 * 128 * 4;   // sub-chunk totals of b [4][128] fp32
 
 struct GWs {
   __nv_bfloat16* qw;
   __nv_bfloat16* kt;
   __nv_bfloat16* m;
   float* vec;
+  // value gate only: V^ and V~ [64 tok][128] bf16, e^{B_r - Q_R} [64 tok][128] bf16 and the
+  // sub-chunk totals of b [4][128] fp32 per record
+  __nv_bfloat16* vh;
+  __nv_bfloat16* vt;
+  __nv_bfloat16* eb;
+  float* vtot;
   int32_t* coff;  // [nseq + 1] first chunk slot of each sequence (packed inputs only)
   long long recs;
   int nck_fixed;
@@ -70,6 +92,16 @@ void gla_carve(const GlaArgs& a, void* base, GWs& w) {
   p += recs * kGRecM;
   w.vec = reinterpret_cast<float*>(p);
   p += recs * kGRecVec;
+  if (a.gv) {
+    w.vh = reinterpret_cast<__nv_bfloat16*>(p);
+    p += recs * kGRecV;
+    w.vt = reinterpret_cast<__nv_bfloat16*>(p);
+    p += recs * kGRecV;
+    w.eb = reinterpret_cast<__nv_bfloat16*>(p);
+    p += recs * kGRecV;
+    w.vtot = reinterpret_cast<float*>(p);
+    p += recs * kGRecVTot;
+  }
   w.coff = reinterpret_cast<int32_t*>(p);
 }
 
@@ -471,6 +503,68 @@ __global__ void __launch_bounds__(kGThreads, 2)
   if (warp == 0) tmem_dealloc(tm, kGTmemCols);
 }
 
+// ------------------------------------------------------------- value-gate records
+
+// Per (chunk, query head) record, thread j = value column: the in-chunk prefix B of b = gv
+// (fp32; zero past a partial chunk's end, so the totals stop at its last token), then
+//   V^_s = v_s e^{B_C - B_s},  V~_s = v_s e^{Q_R(s) - B_s},  E_r = e^{B_r - Q_R(r)}
+// in bf16 (every row of the record: the rows past the end are zero) and the sub-chunk totals
+// Q_{R+1} - Q_R.  Bound by its memory traffic; one 128-thread CTA walks records with a grid
+// stride.
+constexpr int kVThreads = 128;
+
+__global__ void __launch_bounds__(kVThreads) gla_vprep_kernel(const GlaArgs a, const GWs w) {
+  const int j = threadIdx.x;
+  const int Hq = a.Hq, grp = a.Hq / a.Hkv;
+  const __nv_bfloat16* const v = static_cast<const __nv_bfloat16*>(a.v);
+  for (long long rec = blockIdx.x; rec < w.recs; rec += gridDim.x) {
+    const int h = (int)(rec % Hq);
+    const long long slot = rec / Hq;
+    int seq, jc;
+    if (a.cu_seqlens) {
+      // records past the last chunk exist (their count is an upper bound); every later
+      // record is past it too
+      if (slot >= w.coff[a.nseq]) break;
+      int lo = 0, hi = a.nseq;  // coff[lo] <= slot < coff[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (w.coff[mid] <= slot) lo = mid; else hi = mid;
+      }
+      seq = lo;
+      jc = (int)(slot - w.coff[lo]);
+    } else {
+      seq = (int)(slot / w.nck_fixed);
+      jc = (int)(slot % w.nck_fixed);
+    }
+    long long bos;
+    int len;
+    gla_seq_range(a, seq, bos, len);
+    const long long tok0 = bos + (long long)jc * kC;
+    const int n = min(kC, len - jc * kC);
+    const int hk = h / grp;
+    float B[kC];
+    float run = 0.f;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) {
+      if (t < n) run += a.gv[((tok0 + t) * Hq + h) * kD + j];
+      B[t] = run;
+    }
+    const float Q[5] = {0.f, B[15], B[31], B[47], B[63]};
+    float* const tot = w.vtot + rec * 512 + j;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) tot[r * 128] = Q[r + 1] - Q[r];
+    const long long row0 = rec * kC * kD + j;
+#pragma unroll
+    for (int t = 0; t < kC; ++t) {
+      const float vv = (t < n) ? __bfloat162float(v[((tok0 + t) * a.Hkv + hk) * kD + j]) : 0.f;
+      const float q = Q[t >> 4];
+      w.vh[row0 + t * kD] = __float2bfloat16_rn(vv * __expf(Q[4] - B[t]));
+      w.vt[row0 + t * kD] = __float2bfloat16_rn(vv * __expf(q - B[t]));
+      w.eb[row0 + t * kD] = __float2bfloat16_rn((t < n) ? __expf(B[t] - q) : 0.f);
+    }
+  }
+}
+
 // ------------------------------------------------------------------- scan kernel
 
 constexpr int kHThreads = 512;
@@ -486,19 +580,38 @@ constexpr int H_OS = 2 * kHStage;  // output staging [64 tok x 128] bf16 SW128
 constexpr int H_END = H_OS + 16384;
 constexpr size_t kHSmem = H_END + 1024;
 static_assert(kHStage % 1024 == 0 && H_OS % 1024 == 0, "alignment");
+// With a value gate the stage's v tile is V^ (same layout), followed by:
+constexpr int H_VT = kHStage;        // V~ [64 tok x 128] (two SW128 boxes): V~^T MN-major
+constexpr int H_EB = H_VT + 16384;   // e^{B_r - Q_R} [64 tok][128] bf16, row-major
+constexpr int H_TOT = H_EB + 16384;  // sub-chunk totals of b [4][128] fp32
+constexpr int kHStageVG = H_TOT + 2048;
+constexpr int H_OS_VG = 2 * kHStageVG;
+constexpr size_t kHSmemVG = H_OS_VG + 16384 + 1024;
+static_assert(kHStageVG % 1024 == 0 && H_TOT % 1024 == 0, "alignment");
+static_assert(kHSmemVG + 1024 <= 232448, "two value-gate stages fit one SM's shared memory");
 
 constexpr uint32_t H_TM_S = 0;     // fp32 master state S^T [128 (value col) x 128 (key ch)]
 constexpr uint32_t H_TM_DO = 128;  // O'^T [128 x 64 tok], right after S: one N = 192 update
 constexpr uint32_t H_TM_SA = 192;  // bf16 copy of S^T (A operand), 64 columns
 static_assert(H_TM_DO == H_TM_S + 128 && H_M == H_KT + 16384, "the N = 192 update's operands");
 constexpr uint32_t kHTmemCols = 256;
+// value gate: the in-chunk products Y_R' = M[:, R'] V~[R'] (R' = 0..3), [128 x 64 tok] each
+constexpr uint32_t H_TM_Y = 256;
+constexpr uint32_t kHTmemColsVG = 512;
 
+// kVG: the value-axis gate (map_v then addresses the V^ records, map_vt the V~ records).
+template <bool kVG>
 __global__ void __launch_bounds__(kHThreads, 1)
     gla_scan_kernel(const __grid_constant__ CUtensorMap map_qw,
                     const __grid_constant__ CUtensorMap map_kt,
                     const __grid_constant__ CUtensorMap map_m,
                     const __grid_constant__ CUtensorMap map_v,
+                    const __grid_constant__ CUtensorMap map_vt,
                     const __grid_constant__ CUtensorMap map_o, const GlaArgs a, const GWs w) {
+  constexpr int kStg = kVG ? kHStageVG : kHStage;
+  constexpr uint32_t kStgTx = kVG ? kHStageVG : kHStageTx;
+  constexpr int kOS = kVG ? H_OS_VG : H_OS;
+  constexpr uint32_t kTmCols = kVG ? kHTmemColsVG : kHTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -529,7 +642,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   const long long state_off = ((long long)seq * Hq + h) * kD * kD;
 
   if (warp == 0) {
-    tmem_alloc(&s_tmem, kHTmemCols);
+    tmem_alloc(&s_tmem, kTmCols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -541,6 +654,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
     tma_prefetch_desc(&map_kt);
     tma_prefetch_desc(&map_m);
     tma_prefetch_desc(&map_v);
+    if (kVG) tma_prefetch_desc(&map_vt);
     tma_prefetch_desc(&map_o);
   }
   tc_fence_before();
@@ -552,11 +666,13 @@ __global__ void __launch_bounds__(kHThreads, 1)
   const uint64_t pol_rec = policy_evict_first();
   // chunk ch's record and v tile into stage st: its seven boxes from lane 0 of warps 1..7
   // (the expected bytes were registered by thread 0)
+  // (value gate: the V^ record in place of the v tile, then V~, e^{B - Q} and the totals, from
+  // lane 0 of warps 8..11)
   auto issue_load_spread = [&](int ch, int st) {
-    if ((tid & 31) != 0 || warp == 0 || warp > 7) return;
+    if ((tid & 31) != 0 || warp == 0 || warp > (kVG ? 11 : 7)) return;
     const long long rec = (slot0 + ch) * Hq + h;
     const int tok = (int)(bos + (long long)ch * kC);
-    uint8_t* b = sm + st * kHStage;
+    uint8_t* b = sm + st * kStg;
     uint64_t* bar = &bar_ld[st];
     switch (warp) {
       case 1: tma_load_2d_hint(b + H_Q, &map_qw, bar, 0, (int)(rec * 64), pol_rec); break;
@@ -564,14 +680,24 @@ __global__ void __launch_bounds__(kHThreads, 1)
       case 3: tma_load_2d_hint(b + H_KT, &map_kt, bar, 0, (int)(rec * 128), pol_rec); break;
       case 4: tma_load_2d_hint(b + H_M, &map_m, bar, 0, (int)(rec * 64), pol_rec); break;
       case 5: bulk_load_hint(b + H_VEC, w.vec + rec * 256, 1024, bar, pol_rec); break;
-      case 6: tma_load_3d_hint(b + H_V, &map_v, bar, 0, hk, tok, pol_rec); break;
-      default: tma_load_3d_hint(b + H_V + 8192, &map_v, bar, 64, hk, tok, pol_rec); break;
+      case 6:
+        if (kVG) tma_load_2d_hint(b + H_V, &map_v, bar, 0, (int)(rec * 64), pol_rec);
+        else tma_load_3d_hint(b + H_V, &map_v, bar, 0, hk, tok, pol_rec);
+        break;
+      case 7:
+        if (kVG) tma_load_2d_hint(b + H_V + 8192, &map_v, bar, 64, (int)(rec * 64), pol_rec);
+        else tma_load_3d_hint(b + H_V + 8192, &map_v, bar, 64, hk, tok, pol_rec);
+        break;
+      case 8: tma_load_2d_hint(b + H_VT, &map_vt, bar, 0, (int)(rec * 64), pol_rec); break;
+      case 9: tma_load_2d_hint(b + H_VT + 8192, &map_vt, bar, 64, (int)(rec * 64), pol_rec); break;
+      case 10: bulk_load_hint(b + H_EB, w.eb + rec * (kC * kD), 16384, bar, pol_rec); break;
+      default: bulk_load_hint(b + H_TOT, w.vtot + rec * 512, 2048, bar, pol_rec); break;
     }
   };
   int inflight[2] = {nck > 0 ? 0 : -1, nck > 1 ? 1 : -1};
   if (tid == 0) {
-    if (nck > 0) mbar_arrive_expect_tx(&bar_ld[0], kHStageTx);
-    if (nck > 1) mbar_arrive_expect_tx(&bar_ld[1], kHStageTx);
+    if (nck > 0) mbar_arrive_expect_tx(&bar_ld[0], kStgTx);
+    if (nck > 1) mbar_arrive_expect_tx(&bar_ld[1], kStgTx);
   }
   __syncthreads();
   if (nck > 0) issue_load_spread(0, 0);
@@ -596,6 +722,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
 
   const uint32_t idesc_n64 = make_idesc(1, 128, 64);
   const uint32_t idesc_n192_amn = make_idesc(1, 128, 192, true, false);
+  const uint32_t idesc_n128_amn = make_idesc(1, 128, 128, true, false);
+  const uint32_t idesc_n64_amn = make_idesc(1, 128, 64, true, false);
   uint32_t mma_phase = 0, wait_calls = 0;
   auto block_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     const uint32_t slot_w = wait_calls++ & 1;
@@ -607,7 +735,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
 
   for (int ch = 0; ch < nck; ++ch) {
     const int st = ch & 1;
-    uint8_t* const b = sm + st * kHStage;
+    uint8_t* const b = sm + st * kStg;
     const int n = min(kC, len - ch * kC);
     const long long tok0 = bos + (long long)ch * kC;
 
@@ -635,13 +763,29 @@ __global__ void __launch_bounds__(kHThreads, 1)
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         mma_ts(tm + H_TM_DO, tm + H_TM_SA + 8 * s, sw128_kdesc<2>(qs, 64, s), idesc_n64, s > 0);
+      if constexpr (kVG) {
+        // Y_R'^T = V~^T[:, R'] M[:, R']^T: K = the 16 tokens of sub-chunk R' (one K step),
+        // V~^T read MN-major from the staged V~ tile, M K-major
+        const uint32_t vts = smem_u32(b + H_VT), ms = smem_u32(b + H_M);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          mma_ss(tm + H_TM_Y + 64 * r,
+                 make_sdesc(vts + uint32_t(r) * 2048u, 8192u, 1024u, kSwizzle128),
+                 sw128_kdesc<2>(ms, 64, r), idesc_n64_amn, 0);
+      }
     }
-    // meanwhile: decay the fp32 master state in place (S^T diag(e^{G_C}))
+    // meanwhile: decay the fp32 master state in place (S^T diag(e^{G_C}), and with a value
+    // gate diag(e^{B_C}) S^T: row j of S^T is value column j)
     {
       float S[32];
       tmem_ld32(tl + H_TM_S + 32 * wg, S);
+      float eb_c = 1.f;
+      if constexpr (kVG) {
+        const float* tot = reinterpret_cast<const float*>(b + H_TOT) + ln;
+        eb_c = __expf(tot[0] + tot[128] + tot[256] + tot[384]);
+      }
 #pragma unroll
-      for (int i = 0; i < 32; ++i) S[i] *= s_vec[32 * wg + i];
+      for (int i = 0; i < 32; ++i) S[i] *= s_vec[32 * wg + i] * eb_c;
       tmem_st32(tl + H_TM_S + 32 * wg, S);
     }
     tc_fence_before();
@@ -654,12 +798,17 @@ __global__ void __launch_bounds__(kHThreads, 1)
       tc_fence_after();
       const uint32_t ks = smem_u32(b + H_KT);
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tm + H_TM_S, make_sdesc(vs + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
-               sw128_kdesc<2>(ks, 192, s), idesc_n192_amn, 1);
+      for (int s = 0; s < 4; ++s) {
+        if constexpr (kVG)  // S^T += V^^T K^ only (the output's in-chunk part is the Y's)
+          mma_ss(tm + H_TM_S, make_sdesc(vs + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
+                 sw128_kdesc<2>(ks, 128, s), idesc_n128_amn, 1);
+        else
+          mma_ss(tm + H_TM_S, make_sdesc(vs + uint32_t(s) * 2048u, 8192u, 1024u, kSwizzle128),
+                 sw128_kdesc<2>(ks, 192, s), idesc_n192_amn, 1);
+      }
       mma_commit(&bar_mma);
       // the refill's bytes land on the stage's next phase
-      if (ch + 2 < nck) mbar_arrive_expect_tx(&bar_ld[st], kHStageTx);
+      if (ch + 2 < nck) mbar_arrive_expect_tx(&bar_ld[st], kStgTx);
     }
     if (!(ok = block_wait(&bar_mma, mma_phase & 1))) break;
     ++mma_phase;
@@ -674,6 +823,34 @@ __global__ void __launch_bounds__(kHThreads, 1)
       tmem_st16(tl + H_TM_SA + 16 * wg, sp);
       float o16[16];
       tmem_ld16(tl + H_TM_DO + 16 * wg, o16);
+      if constexpr (kVG) {
+        // O'_r = e^{B_r - Q_R} (e^{Q_R} (Q~ S)_r + sum_{R' <= R} e^{Q_R - Q_R'} Y_R',r) for
+        // this thread's value column j = ln and the tokens of sub-chunk R = wg
+        const float* tot = reinterpret_cast<const float*>(b + H_TOT) + ln;
+        float qcum = 0.f;  // Q_R
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+          if (r < wg) qcum += tot[128 * r];
+        const float eq = __expf(qcum);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o16[i] *= eq;
+        float qr = 0.f;  // Q_R'
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (r <= wg) {  // warp-uniform
+            float y16[16];
+            tmem_ld16(tl + H_TM_Y + 64 * r + 16 * wg, y16);
+            const float f = __expf(qcum - qr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o16[i] += f * y16[i];
+          }
+          qr += tot[128 * r];
+        }
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(b + H_EB) +
+                                 (16 * wg) * kD + ln;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o16[i] *= __bfloat162float(e[i * kD]);
+      }
       if (tid == 0) bulk_wait_read_all();  // the previous output store has read its tile
       __syncthreads();
       if (n == kC) {
@@ -683,7 +860,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
         for (int i = 0; i < 16; ++i) {
           const uint32_t off = ob + uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
                                (((och ^ uint32_t(i & 7)) << 4) | oby);
-          *reinterpret_cast<__nv_bfloat16*>(sm + H_OS + off) =
+          *reinterpret_cast<__nv_bfloat16*>(sm + kOS + off) =
               __float2bfloat16_rn(o16[i] * s_vec[128 + 16 * wg + i]);
         }
       } else {
@@ -699,8 +876,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && n == kC) {
-      tma_store_3d(&map_o, sm + H_OS, 0, h, (int)tok0);
-      tma_store_3d(&map_o, sm + H_OS + 8192, 64, h, (int)tok0);
+      tma_store_3d(&map_o, sm + kOS, 0, h, (int)tok0);
+      tma_store_3d(&map_o, sm + kOS + 8192, 64, h, (int)tok0);
       bulk_commit();
     }
     // the stage is consumed (the MMAs, and the output's scale vector): refill it
@@ -729,7 +906,7 @@ __global__ void __launch_bounds__(kHThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tm, kHTmemCols);
+  if (warp == 0) tmem_dealloc(tm, kTmCols);
 }
 
 // ------------------------------------------------------------------------- host
@@ -742,13 +919,14 @@ bool map_in(CUtensorMap* m, const void* base, long long rows, int H, bool fp32) 
 }  // namespace
 
 bool gla_chunk_supported(const GlaArgs& a, bool bf16) {
-  return bf16 && a.D == kD && a.gv == nullptr && !a.reverse;
+  return bf16 && a.D == kD && !a.reverse;
 }
 
 size_t gla_chunk_workspace(const GlaArgs& a) {
   const long long recs = gla_slots(a) * a.Hq;
   const size_t coff = a.cu_seqlens ? split::align_up(size_t(a.nseq + 1) * 4, 256) : 0;
-  return size_t(recs) * size_t(kGRecQ + kGRecK + kGRecM + kGRecVec) + coff;
+  const long long vg = a.gv ? 3 * kGRecV + kGRecVTot : 0;
+  return size_t(recs) * size_t(kGRecQ + kGRecK + kGRecM + kGRecVec + vg) + coff;
 }
 
 bool gla_chunk_index_ok(const GlaArgs& a) {
@@ -773,12 +951,17 @@ cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t st)
   const long long rec_rows = w.recs > 0 ? w.recs : 1;
   const float* gstage = a.gk ? a.gk : a.g;                 // staged by TMA
   const float* gate2 = (a.gk && a.g) ? a.g : nullptr;      // read from global memory
-  CUtensorMap mqw, mkt, mm, mv, mo, mq, mk, mg;
+  const bool vg = a.gv != nullptr;
+  CUtensorMap mqw, mkt, mm, mv, mvt, mo, mq, mk, mg;
   if (!split::make_map_2d(&mqw, w.qw, rec_rows * 64, 128, 64) ||
       !split::make_map_2d(&mkt, w.kt, rec_rows * 128, 64, 128) ||
       !split::make_map_2d(&mm, w.m, rec_rows * 64, 64, 64) ||
       !map_in(&mq, a.q, map_rows, a.Hq, false) || !map_in(&mk, a.k, map_rows, a.Hkv, false) ||
-      !map_in(&mv, a.v, map_rows, a.Hkv, false) ||
+      // value gate: the scan's v tile is the V^ record, its V~ tile the V~ record
+      !(vg ? split::make_map_2d(&mv, w.vh, rec_rows * 64, 128, 64)
+           : map_in(&mv, a.v, map_rows, a.Hkv, false)) ||
+      !split::make_map_2d(&mvt, vg ? (const void*)w.vt : (const void*)w.qw, rec_rows * 64, 128,
+                          64) ||
       // (without a gate tensor the unused gate map is laid over q)
       !map_in(&mg, gstage ? (const void*)gstage : a.q, map_rows, a.Hq, gstage != nullptr) ||
       !split::make_map_out(&mo, a.out, map_rows, a.Hq))
@@ -786,8 +969,9 @@ cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t st)
   cudaError_t e = cudaFuncSetAttribute(gla_prep_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gla_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kHSmem);
+  auto scan = vg ? gla_scan_kernel<true> : gla_scan_kernel<false>;
+  const size_t scan_smem = vg ? kHSmemVG : kHSmem;
+  e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem);
   if (e != cudaSuccess) return e;
   if (w.recs > 0) {
     int dev = 0, sms = 0;
@@ -797,8 +981,13 @@ cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t st)
     const long long grid = std::min<long long>(w.recs, 2LL * sms);
     gla_prep_kernel<<<(unsigned)grid, kGThreads, kGSmem, st>>>(mkt, mm, mq, mk, mg, a, gate2, w);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (vg) {
+      const long long vgrid = std::min<long long>(w.recs, 16LL * sms);
+      gla_vprep_kernel<<<(unsigned)vgrid, kVThreads, 0, st>>>(a, w);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
-  gla_scan_kernel<<<dim3(a.Hq, a.nseq), kHThreads, kHSmem, st>>>(mqw, mkt, mm, mv, mo, a, w);
+  scan<<<dim3(a.Hq, a.nseq), kHThreads, scan_smem, st>>>(mqw, mkt, mm, mv, mvt, mo, a, w);
   return cudaGetLastError();
 }
 

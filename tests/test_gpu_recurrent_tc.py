@@ -1,12 +1,12 @@
 """Parity of kda_recurrent_attention_fwd_ws -- the recurrent page's gated linear recurrence
-in its chunked form on the tensor cores (bf16, D = 128, key-axis gates g / gk / g_gamma,
-forward order) -- with the fp64 oracle ``recurrent_attention``: every combination of the
-key-axis gates (none, one, several), grouped key / value heads, packed sequences with empty
-and ragged members, gates from mild to the edge of the supported range [-5, 1], and the
-benchmark's full workload compared element by element.  Bar: max |gpu - oracle| /
-max |oracle| <= 2e-2 per tensor, the oracle fed the same bf16-rounded q, k, v.  Calls that
-the chunked path does not serve (a value-axis gate, reverse order) give the token-serial
-kernel's results bit for bit."""
+in its chunked form on the tensor cores (bf16, D = 128, key-axis gates g / gk / g_gamma and
+the value-axis gate gv, forward order) -- with the fp64 oracle ``recurrent_attention``: every
+combination of the key-axis gates (none, one, several) with and without gv, grouped key /
+value heads, packed sequences with empty and ragged members, gates from mild to the edge of
+the supported range [-5, 1], and the benchmark's full workloads (gk; gk + gv) compared
+element by element.  Bar: max |gpu - oracle| / max |oracle| <= 2e-2 per tensor, the oracle
+fed the same bf16-rounded q, k, v.  Calls that the chunked path does not serve (reverse
+order) give the token-serial kernel's results bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -71,7 +71,8 @@ def _check(d, out, S, scale, cu=None):
 
 
 @pytest.mark.parametrize("gates", [(), ("gk",), ("g",), ("g", "gk"), ("gk", "g_gamma"),
-                                   ("g_gamma",), ("g", "gk", "g_gamma")])
+                                   ("g_gamma",), ("g", "gk", "g_gamma"), ("gv",), ("gk", "gv"),
+                                   ("g", "gv", "g_gamma"), ("g", "gk", "gv", "g_gamma")])
 def test_gate_combinations(gates):
     B, T, Hq, Hkv = 2, 200, 4, 2
     d = _inputs(B, T, Hq, Hkv, len(gates), gates, True)
@@ -79,52 +80,56 @@ def test_gate_combinations(gates):
     _check(d, out, S, None)
 
 
+@pytest.mark.parametrize("gates", [("gk",), ("gk", "gv"), ("gv",)])
 @pytest.mark.parametrize("lo,hi", [(-5.0, 0.0), (-1.0, 0.05), (-0.05, 0.0)])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 300])
-def test_gate_ranges_and_lengths(T, lo, hi):
+def test_gate_ranges_and_lengths(T, lo, hi, gates):
     B, Hq, Hkv = 1, 2, 1
-    d = _inputs(B, T, Hq, Hkv, T, ("gk",), T % 2 == 0, lo=lo, hi=hi)
+    d = _inputs(B, T, Hq, Hkv, T, gates, T % 2 == 0, lo=lo, hi=hi)
     out, S = _run(d, B, T, Hq, Hkv, 0.2)
     _check(d, out, S, 0.2)
 
 
-def test_packed_sequences():
+@pytest.mark.parametrize("gates", [("gk", "g_gamma"), ("gk", "gv", "g_gamma")])
+def test_packed_sequences(gates):
     lens = [130, 0, 1, 64, 200, 63]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     T, Hq, Hkv = int(cu[-1]), 4, 4
-    d = _inputs(1, T, Hq, Hkv, 7, ("gk", "g_gamma"), True, nseq=len(lens))
+    d = _inputs(1, T, Hq, Hkv, 7, gates, True, nseq=len(lens))
     out, S = _run(d, 1, T, Hq, Hkv, 0.1, cu=cu)
     _check(d, out, S, 0.1, cu)
     # the empty sequence keeps its state (the fp32 copy the device received)
     np.testing.assert_array_equal(S[1], d["s0"][1].astype(np.float32))
 
 
-def test_many_records_odd_head_count():
+@pytest.mark.parametrize("gates", [("gk",), ("gk", "gv")])
+def test_many_records_odd_head_count(gates):
     """More (chunk, head) records than the prep's persistent CTAs, an odd query-head count
     in groups of 3 per key / value head."""
     B, T, Hq, Hkv = 2, 1000, 21, 7
-    d = _inputs(B, T, Hq, Hkv, 8, ("gk",), True)
+    d = _inputs(B, T, Hq, Hkv, 8, gates, True)
     out, S = _run(d, B, T, Hq, Hkv, None)
     _check(d, out, S, None)
 
 
-@pytest.mark.parametrize("which", ["gv", "reverse"])
-def test_unserved_calls_take_the_token_serial_kernel(which):
+@pytest.mark.parametrize("gates", [("gk",), ("gk", "gv")])
+def test_reverse_takes_the_token_serial_kernel(gates):
     B, T, Hq, Hkv = 1, 90, 2, 2
-    gates = ("gk", "gv") if which == "gv" else ("gk",)
     d = _inputs(B, T, Hq, Hkv, 11, gates, True)
-    rev = which == "reverse"
+    rev = True
     assert kda.kda_recurrent_attention_fwd_workspace_size(
-        B, T, Hq, Hkv, D, value_gate=which == "gv", reverse=rev) == 0
+        B, T, Hq, Hkv, D, value_gate="gv" in gates, reverse=rev) == 0
     o1, S1 = _run(d, B, T, Hq, Hkv, 0.3, ws=True, reverse=rev)
     o2, S2 = _run(d, B, T, Hq, Hkv, 0.3, ws=False, reverse=rev)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(S1, S2)
 
 
-def test_benchmark_workload_full():
-    """The benchmark's workload (B=4, T=4096, Hq=32, Hkv=8, D=128, bf16, gk only ~
-    -0.05 U(0, 1), zero initial state): every element of all 128 (b, h) pairs."""
+@pytest.mark.parametrize("value_gate", [False, True])
+def test_benchmark_workload_full(value_gate):
+    """The benchmark's workloads (B=4, T=4096, Hq=32, Hkv=8, D=128, bf16, gk ~ -0.05 U(0, 1),
+    and gv ~ -0.05 U(0, 1) for the second, zero initial state): every element of all 128
+    (b, h) pairs."""
     B, T, Hq, Hkv = 4, 4096, 32, 8
     r = np.random.default_rng(77)
     d = {"q": r.standard_normal((B, T, Hq, D), dtype=np.float32),
@@ -132,10 +137,12 @@ def test_benchmark_workload_full():
          "v": r.standard_normal((B, T, Hkv, D), dtype=np.float32),
          "gk": (-0.05 * r.random((B, T, Hq, D), dtype=np.float32)),
          "g": None, "gv": None, "g_gamma": None, "s0": None}
+    if value_gate:
+        d["gv"] = -0.05 * r.random((B, T, Hq, D), dtype=np.float32)
     out, S = _run(d, B, T, Hq, Hkv, None)
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(S))
     from oracle import pool
     ro, rs = pool.recurrent(oracle_pool(), *(bf16_round32(d[n]) for n in ("q", "k", "v")),
-                            None, None, d["gk"], None, None, None)
-    check_full("recurrent B4 T4096 Hq32 Hkv8, gk, kda_recurrent_attention_fwd_ws",
-                         out, ro, S, rs)
+                            None, None, d["gk"], d["gv"], None, None)
+    check_full("recurrent B4 T4096 Hq32 Hkv8, gk" + (" + gv" if value_gate else "") +
+               ", kda_recurrent_attention_fwd_ws", out, ro, S, rs)
