@@ -472,11 +472,12 @@ def backward_measure(w, d, x, reps=3):
                               "tokens_per_s": B * T / ((ms_train_fwd + ms_saved) * 1e-3)}}
 
 def recurrent_attention_measure(reps=3, B=4, token_serial=True):
-    """kda_recurrent_attention_fwd on B=4, T=4096, Hq=32, Hkv=8, D=128, bf16 q/k/v: with
-    per-channel key and value gates (gk, gv fp32; the token-serial kernel), and with the key
-    gate only through kda_recurrent_attention_fwd_ws (the chunked tensor-core path).  Median
-    time per call and its algorithmic bytes (q, k, v, the gates, out and the final state,
-    each once)."""
+    """The recurrent page's call on B=4, T=4096, Hq=32, Hkv=8, D=128, bf16 q/k/v: with
+    per-channel key and value gates (gk, gv fp32) through kda_recurrent_attention_fwd_ws (the
+    chunked tensor-core path) and, beside it, through kda_recurrent_attention_fwd (the
+    token-serial kernel); and with the key gate only through kda_recurrent_attention_fwd_ws.
+    Median time per call and its algorithmic bytes (q, k, v, the gates, out and the final
+    state, each once)."""
     torch = _torch()
     import gated_delta_rule_55_gb300 as kda
     T, Hq, Hkv, D = 4096, 32, 8, 128
@@ -488,10 +489,15 @@ def recurrent_attention_measure(reps=3, B=4, token_serial=True):
     gv = -0.05 * torch.rand(B, T, Hq, D, device="cuda", generator=g)
     out = torch.empty(B, T, Hq, D, device="cuda", dtype=torch.bfloat16)
     fs = torch.empty(B, Hq, D, D, device="cuda")
-    ws = torch.empty(kda.kda_recurrent_attention_fwd_workspace_size(B, T, Hq, Hkv, D),
-                     dtype=torch.uint8, device="cuda")
+    nb_k = kda.kda_recurrent_attention_fwd_workspace_size(B, T, Hq, Hkv, D)
+    nb_kv = kda.kda_recurrent_attention_fwd_workspace_size(B, T, Hq, Hkv, D, value_gate=True)
+    ws = torch.empty(max(nb_k, nb_kv), dtype=torch.uint8, device="cuda")
 
     def both():
+        kda.kda_recurrent_attention_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, gk=gk, gv=gv,
+                                           final_state=fs, workspace=ws)
+
+    def both_serial():
         kda.kda_recurrent_attention_fwd(q, k, v, out, B, T, Hq, Hkv, D, gk=gk, gv=gv,
                                         final_state=fs)
 
@@ -514,18 +520,21 @@ def recurrent_attention_measure(reps=3, B=4, token_serial=True):
 
     io = B * T * (Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * 2) + B * Hq * D * D * 4
     gate = B * T * Hq * D * 4
-    ms = median_ms(both) if token_serial else float("nan")
+    ms = median_ms(both)
+    ms_s = median_ms(both_serial) if token_serial else float("nan")
     ms_k = median_ms(key_only)
-    return {"entry": "kda_recurrent_attention_fwd",
+    return {"entry": "kda_recurrent_attention_fwd_ws (chunked, tensor cores)",
             "workload": "B4 T4096 Hq32 Hkv8 D128 bf16, gk + gv gates", "ms_per_call": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "algorithmic_bytes": io + 2 * gate,
-            "hbm_gbs": (io + 2 * gate) / (ms * 1e-3) / 1e9,
+            "hbm_gbs": (io + 2 * gate) / (ms * 1e-3) / 1e9, "workspace_bytes": nb_kv,
+            "token_serial": {"entry": "kda_recurrent_attention_fwd (token by token)",
+                             "ms_per_call": ms_s, "tokens_per_s": B * T / (ms_s * 1e-3)},
             "key_gate_only": {"entry": "kda_recurrent_attention_fwd_ws (chunked, tensor cores)",
                               "workload": "B4 T4096 Hq32 Hkv8 D128 bf16, gk gate",
                               "ms_per_call": ms_k, "tokens_per_s": B * T / (ms_k * 1e-3),
                               "algorithmic_bytes": io + gate,
                               "hbm_gbs": (io + gate) / (ms_k * 1e-3) / 1e9,
-                              "workspace_bytes": int(ws.numel())}}
+                              "workspace_bytes": nb_k}}
 
 
 def attention_measure(w, x, reps=5):
@@ -701,12 +710,12 @@ def profile_case(which):
         w = synth.DECODE_B64
         decode_measure(w, 2, False)
     elif which == "gla":
-        # the benchmark's recurrent workload: both calls (token-serial with gk + gv, chunked
-        # with gk), two launches each
+        # the benchmark's recurrent workload: its calls (chunked with gk + gv, token-serial
+        # with gk + gv, chunked with gk), twice each
         recurrent_attention_measure(reps=1)
         desc = "recurrent B4 T4096 Hq32 Hkv8 D128"
     elif which == "gla_chunk":
-        # two chunked calls (gk) on a quarter of the recurrent workload (B = 1)
+        # the chunked calls (gk + gv, then gk) on a quarter of the recurrent workload (B = 1)
         recurrent_attention_measure(reps=1, B=1, token_serial=False)
         desc = "recurrent B1 T4096 Hq32 Hkv8 D128, chunked"
     elif which in ("bwd", "bwd_full"):

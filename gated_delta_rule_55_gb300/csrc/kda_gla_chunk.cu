@@ -505,16 +505,19 @@ __global__ void __launch_bounds__(kGThreads, 2)
 
 // ------------------------------------------------------------- value-gate records
 
-// Per (chunk, query head) record, thread j = value column: the in-chunk prefix B of b = gv
-// (fp32; zero past a partial chunk's end, so the totals stop at its last token), then
-//   V^_s = v_s e^{B_C - B_s},  V~_s = v_s e^{Q_R(s) - B_s},  E_r = e^{B_r - Q_R(r)}
-// in bf16 (every row of the record: the rows past the end are zero) and the sub-chunk totals
-// Q_{R+1} - Q_R.  Bound by its memory traffic; one 128-thread CTA walks records with a grid
-// stride.
-constexpr int kVThreads = 128;
+// Per (chunk, query head) record, thread (R, j): value column j, the 16 tokens of sub-chunk
+// R.  The gate's prefix inside the sub-chunk, L_t = B_t - Q_R (b = gv, fp32; zero past a
+// partial chunk's end, so the totals stop at its last token), and the sub-chunk totals
+// T_R = Q_{R+1} - Q_R give
+//   V^_s = v_s e^{B_C - B_s} = v_s e^{(T_R + .. + T_3) - L_s},  V~_s = v_s e^{-L_s},
+//   E_r = e^{L_r}
+// in bf16 (every row of the record: the rows past the end are zero) and the totals.  Bound
+// by its memory traffic; CTAs walk the records with a grid stride.
+constexpr int kVThreads = 512;
 
-__global__ void __launch_bounds__(kVThreads) gla_vprep_kernel(const GlaArgs a, const GWs w) {
-  const int j = threadIdx.x;
+__global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a, const GWs w) {
+  __shared__ float s_tot[4][kD];
+  const int j = threadIdx.x & (kD - 1), R = threadIdx.x >> 7;
   const int Hq = a.Hq, grp = a.Hq / a.Hkv;
   const __nv_bfloat16* const v = static_cast<const __nv_bfloat16*>(a.v);
   for (long long rec = blockIdx.x; rec < w.recs; rec += gridDim.x) {
@@ -523,7 +526,7 @@ __global__ void __launch_bounds__(kVThreads) gla_vprep_kernel(const GlaArgs a, c
     int seq, jc;
     if (a.cu_seqlens) {
       // records past the last chunk exist (their count is an upper bound); every later
-      // record is past it too
+      // record is past it too (uniform over the CTA)
       if (slot >= w.coff[a.nseq]) break;
       int lo = 0, hi = a.nseq;  // coff[lo] <= slot < coff[hi]
       while (hi - lo > 1) {
@@ -539,29 +542,39 @@ __global__ void __launch_bounds__(kVThreads) gla_vprep_kernel(const GlaArgs a, c
     long long bos;
     int len;
     gla_seq_range(a, seq, bos, len);
-    const long long tok0 = bos + (long long)jc * kC;
-    const int n = min(kC, len - jc * kC);
+    const long long ctok = bos + (long long)jc * kC;  // the chunk's first token (live)
+    const long long tok0 = ctok + 16 * R;              // this thread's first token
+    const int nr = min(16, len - jc * kC - 16 * R);    // its live tokens (may be <= 0)
     const int hk = h / grp;
-    float B[kC];
+    // the loads are unconditional (rows past the end read the chunk's first token instead
+    // and are masked), so that all sixteen are in flight at once
+    float L[16];
     float run = 0.f;
 #pragma unroll
-    for (int t = 0; t < kC; ++t) {
-      if (t < n) run += a.gv[((tok0 + t) * Hq + h) * kD + j];
-      B[t] = run;
+    for (int i = 0; i < 16; ++i) {
+      const long long row = (i < nr) ? tok0 + i : ctok;
+      const float x = a.gv[(row * Hq + h) * kD + j];
+      run += (i < nr) ? x : 0.f;
+      L[i] = run;
     }
-    const float Q[5] = {0.f, B[15], B[31], B[47], B[63]};
-    float* const tot = w.vtot + rec * 512 + j;
+    s_tot[R][j] = run;
+    w.vtot[rec * 512 + R * 128 + j] = run;
+    __syncthreads();
+    float tail = 0.f;  // B_C - Q_R
 #pragma unroll
-    for (int r = 0; r < 4; ++r) tot[r * 128] = Q[r + 1] - Q[r];
-    const long long row0 = rec * kC * kD + j;
+    for (int r = 0; r < 4; ++r)
+      if (r >= R) tail += s_tot[r][j];
+    const long long row0 = (rec * kC + 16 * R) * kD + j;
 #pragma unroll
-    for (int t = 0; t < kC; ++t) {
-      const float vv = (t < n) ? __bfloat162float(v[((tok0 + t) * a.Hkv + hk) * kD + j]) : 0.f;
-      const float q = Q[t >> 4];
-      w.vh[row0 + t * kD] = __float2bfloat16_rn(vv * __expf(Q[4] - B[t]));
-      w.vt[row0 + t * kD] = __float2bfloat16_rn(vv * __expf(q - B[t]));
-      w.eb[row0 + t * kD] = __float2bfloat16_rn((t < n) ? __expf(B[t] - q) : 0.f);
+    for (int i = 0; i < 16; ++i) {
+      const long long row = (i < nr) ? tok0 + i : ctok;
+      const float vr = __bfloat162float(v[(row * a.Hkv + hk) * kD + j]);
+      const float vv = (i < nr) ? vr : 0.f;
+      w.vh[row0 + i * kD] = __float2bfloat16_rn(vv * __expf(tail - L[i]));
+      w.vt[row0 + i * kD] = __float2bfloat16_rn(vv * __expf(-L[i]));
+      w.eb[row0 + i * kD] = __float2bfloat16_rn((i < nr) ? __expf(L[i]) : 0.f);
     }
+    __syncthreads();  // s_tot is rewritten for the next record
   }
 }
 
@@ -982,7 +995,7 @@ cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t st)
     gla_prep_kernel<<<(unsigned)grid, kGThreads, kGSmem, st>>>(mkt, mm, mq, mk, mg, a, gate2, w);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (vg) {
-      const long long vgrid = std::min<long long>(w.recs, 16LL * sms);
+      const long long vgrid = std::min<long long>(w.recs, 2LL * sms);
       gla_vprep_kernel<<<(unsigned)vgrid, kVThreads, 0, st>>>(a, w);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
