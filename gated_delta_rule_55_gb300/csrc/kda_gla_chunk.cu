@@ -505,21 +505,23 @@ __global__ void __launch_bounds__(kGThreads, 2)
 
 // ------------------------------------------------------------- value-gate records
 
-// Per (chunk, query head) record, thread (R, j): value column j, the 16 tokens of sub-chunk
-// R.  The gate's prefix inside the sub-chunk, L_t = B_t - Q_R (b = gv, fp32; zero past a
-// partial chunk's end, so the totals stop at its last token), and the sub-chunk totals
-// T_R = Q_{R+1} - Q_R give
+// Per (chunk, query head) record, thread (P, cp): value columns 2 cp and 2 cp + 1 (fp32 and
+// bf16 pairs), the 8 tokens 8 P .. 8 P + 7 (half of sub-chunk R = P / 2).  The gate's prefix
+// inside the sub-chunk, L_t = B_t - Q_R (b = gv, fp32; zero past a partial chunk's end, so
+// the totals stop at its last token), and the sub-chunk totals T_R = Q_{R+1} - Q_R give
 //   V^_s = v_s e^{B_C - B_s} = v_s e^{(T_R + .. + T_3) - L_s},  V~_s = v_s e^{-L_s},
 //   E_r = e^{L_r}
-// in bf16 (every row of the record: the rows past the end are zero) and the totals.  Bound
-// by its memory traffic; CTAs walk the records with a grid stride.
+// in bf16 (every row of the record: the rows past the end are zero) and the totals.  A
+// thread's gate and v loads all go out before the one block barrier (the exchange of the
+// 8-token totals).  Bound by its memory traffic; CTAs walk the records with a grid stride.
 constexpr int kVThreads = 512;
 
 __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a, const GWs w) {
-  __shared__ float s_tot[4][kD];
-  const int j = threadIdx.x & (kD - 1), R = threadIdx.x >> 7;
+  __shared__ float2 s_tot[8][kD / 2];
+  const int cp = threadIdx.x & 63, P = threadIdx.x >> 6, R = P >> 1;
+  const int c0 = 2 * cp;
   const int Hq = a.Hq, grp = a.Hq / a.Hkv;
-  const __nv_bfloat16* const v = static_cast<const __nv_bfloat16*>(a.v);
+  const long long gstride = (long long)Hq * kD, vstride = (long long)a.Hkv * kD;
   for (long long rec = blockIdx.x; rec < w.recs; rec += gridDim.x) {
     const int h = (int)(rec % Hq);
     const long long slot = rec / Hq;
@@ -543,36 +545,54 @@ __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a
     int len;
     gla_seq_range(a, seq, bos, len);
     const long long ctok = bos + (long long)jc * kC;  // the chunk's first token (live)
-    const long long tok0 = ctok + 16 * R;              // this thread's first token
-    const int nr = min(16, len - jc * kC - 16 * R);    // its live tokens (may be <= 0)
+    const int n = min(kC, len - jc * kC);             // its live tokens (>= 1)
     const int hk = h / grp;
-    // the loads are unconditional (rows past the end read the chunk's first token instead
-    // and are masked), so that all sixteen are in flight at once
-    float L[16];
-    float run = 0.f;
+    // rows past the end read the chunk's first token instead and are masked, so that the
+    // loads are unconditional and all in flight at once
+    const float* const gbase = a.gv + (ctok * Hq + h) * kD + c0;
+    const __nv_bfloat16* const vbase =
+        static_cast<const __nv_bfloat16*>(a.v) + (ctok * a.Hkv + hk) * kD + c0;
+    float2 L[8];
+    uint32_t vw[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const long long row = (i < nr) ? tok0 + i : ctok;
-      const float x = a.gv[(row * Hq + h) * kD + j];
-      run += (i < nr) ? x : 0.f;
+    for (int i = 0; i < 8; ++i) {
+      const int t = 8 * P + i, tt = t < n ? t : 0;
+      L[i] = *reinterpret_cast<const float2*>(gbase + tt * gstride);
+      vw[i] = *reinterpret_cast<const uint32_t*>(vbase + tt * vstride);
+    }
+    float2 run = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (8 * P + i >= n) L[i] = make_float2(0.f, 0.f);
+      run = __fadd2_rn(run, L[i]);
       L[i] = run;
     }
-    s_tot[R][j] = run;
-    w.vtot[rec * 512 + R * 128 + j] = run;
+    s_tot[P][cp] = run;
     __syncthreads();
-    float tail = 0.f;  // B_C - Q_R
+    // the sub-chunk's first half before this thread's tokens; the totals T_r; B_C - Q_R
+    const float2 first = s_tot[2 * R][cp];
+    if (P & 1) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
-      if (r >= R) tail += s_tot[r][j];
-    const long long row0 = (rec * kC + 16 * R) * kD + j;
+      for (int i = 0; i < 8; ++i) L[i] = __fadd2_rn(first, L[i]);
+    }
+    float2 tail = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const long long row = (i < nr) ? tok0 + i : ctok;
-      const float vr = __bfloat162float(v[(row * a.Hkv + hk) * kD + j]);
-      const float vv = (i < nr) ? vr : 0.f;
-      w.vh[row0 + i * kD] = __float2bfloat16_rn(vv * __expf(tail - L[i]));
-      w.vt[row0 + i * kD] = __float2bfloat16_rn(vv * __expf(-L[i]));
-      w.eb[row0 + i * kD] = __float2bfloat16_rn((i < nr) ? __expf(L[i]) : 0.f);
+    for (int r = 0; r < 4; ++r) {
+      const float2 tr = __fadd2_rn(s_tot[2 * r][cp], s_tot[2 * r + 1][cp]);
+      if (r >= R) tail = __fadd2_rn(tail, tr);
+      if (P == 0) *reinterpret_cast<float2*>(w.vtot + rec * 512 + r * 128 + c0) = tr;
+    }
+    const long long row0 = (rec * kC + 8 * P) * kD + c0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool live = 8 * P + i < n;
+      const float v0 = live ? bf16_lo(vw[i]) : 0.f, v1 = live ? bf16_hi(vw[i]) : 0.f;
+      *reinterpret_cast<uint32_t*>(w.vh + row0 + i * kD) =
+          pack_bf16(v0 * __expf(tail.x - L[i].x), v1 * __expf(tail.y - L[i].y));
+      *reinterpret_cast<uint32_t*>(w.vt + row0 + i * kD) =
+          pack_bf16(v0 * __expf(-L[i].x), v1 * __expf(-L[i].y));
+      *reinterpret_cast<uint32_t*>(w.eb + row0 + i * kD) =
+          live ? pack_bf16(__expf(L[i].x), __expf(L[i].y)) : 0u;
     }
     __syncthreads();  // s_tot is rewritten for the next record
   }
