@@ -221,14 +221,15 @@ def test_recurrent_attention_chunked_replay():
     v = torch.from_numpy(r.standard_normal((B, T, Hkv, D), dtype=np.float32)).to(
         "cuda", torch.bfloat16)
     gk = torch.from_numpy(-0.05 * r.random((B, T, Hq, D), dtype=np.float32)).cuda()  # [B,T,Hq,D]
+    gv = torch.from_numpy(-0.05 * r.random((B, T, Hq, D), dtype=np.float32)).cuda()
     out = torch.empty(B, T, Hq, D, device="cuda", dtype=torch.bfloat16)
     fs = torch.empty(B, Hq, D, D, device="cuda")
-    nbytes = kda.kda_recurrent_attention_fwd_workspace_size(B, T, Hq, Hkv, D)
+    nbytes = kda.kda_recurrent_attention_fwd_workspace_size(B, T, Hq, Hkv, D, value_gate=True)
     assert nbytes > 0
     w = workspace(nbytes)
 
     def call():
-        kda.kda_recurrent_attention_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, gk=gk,
+        kda.kda_recurrent_attention_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, gk=gk, gv=gv,
                                            final_state=fs, workspace=w)
 
     call()
