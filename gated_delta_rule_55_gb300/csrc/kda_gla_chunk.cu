@@ -92,7 +92,7 @@ void gla_carve(const GlaArgs& a, void* base, GWs& w) {
   p += recs * kGRecM;
   w.vec = reinterpret_cast<float*>(p);
   p += recs * kGRecVec;
-  if (a.gv) {
+  if (a.gv || a.reverse) {  // (reverse order runs on the value records, gate or not)
     w.vh = reinterpret_cast<__nv_bfloat16*>(p);
     p += recs * kGRecV;
     w.vt = reinterpret_cast<__nv_bfloat16*>(p);
@@ -137,6 +137,12 @@ constexpr uint32_t kGTmemCols = 256;  // D1 = Xl Kb^T: 160 columns
 static_assert(G_MS + 8192 <= G_K, "record staging must stay inside Kb");
 
 // Rows 64..127 of Xl are not written: the MMA's lanes 64..127 are never read.
+// kRev: reverse order.  Every position p of a record is token p of the chunk walked
+// backwards: chunk jc covers the tokens end - 64 (jc + 1) .. end - 64 jc - 1 of its sequence,
+// staged as they lie (row 63 - p holds position p; rows before the sequence's first token
+// are dead positions p >= n), so the records are those of the forward recurrence on the
+// reversed sequence.
+template <bool kRev>
 __global__ void __launch_bounds__(kGThreads, 2)
     gla_prep_kernel(const __grid_constant__ CUtensorMap map_kt,
                     const __grid_constant__ CUtensorMap map_m,
@@ -198,7 +204,8 @@ __global__ void __launch_bounds__(kGThreads, 2)
     gla_seq_range(a, seq, bos, len);
     seq_ = seq;
     n_ = min(kC, len - jc * kC);
-    tok0_ = bos + (long long)jc * kC;
+    // the first token of the staged tile (reverse: it may lie before the sequence's start)
+    tok0_ = kRev ? bos + len - (long long)(jc + 1) * kC : bos + (long long)jc * kC;
     return true;
   };
 
@@ -264,10 +271,12 @@ __global__ void __launch_bounds__(kGThreads, 2)
   const uint32_t c_kb = uint32_t(c0 >> 6);
   const uint32_t c_chunk = uint32_t(((c0 & 63) * 2) >> 4);
   const uint32_t c_byte = uint32_t(((c0 & 63) * 2) & 15);
-  const uint32_t tile_base = c_kb * 8192u + uint32_t(R) * 2048u;
+  // staged row of this thread's position 16 R + i (reverse: row 63 - 16 R - i)
+  auto srow = [&](int i) -> int { return kRev ? 63 - 16 * R - i : 16 * R + i; };
   auto swz = [&](int i) -> uint32_t {
-    return uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
-           (((c_chunk ^ uint32_t(i & 7)) << 4) | c_byte);
+    const int rr = srow(i);
+    return c_kb * 8192u + uint32_t((rr >> 3) * 1024 + (rr & 7) * 128) +
+           (((c_chunk ^ uint32_t(rr & 7)) << 4) | c_byte);
   };
   while (have) {
     cur_p += gridDim.x;
@@ -279,20 +288,21 @@ __global__ void __launch_bounds__(kGThreads, 2)
     ld_pending = false;
     float2 graw[16];
     uint32_t kw[16], qw[16];
-    const uint8_t* gsrc = sm + G_G + (c0 >> 5) * 8192 + (16 * R) * 128 + (c0 & 31) * 4;
+    const uint8_t* gsrc = sm + G_G + (c0 >> 5) * 8192 + (c0 & 31) * 4;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      graw[i] = staged_gate ? *reinterpret_cast<const float2*>(gsrc + i * 128)
+      graw[i] = staged_gate ? *reinterpret_cast<const float2*>(gsrc + srow(i) * 128)
                             : make_float2(0.f, 0.f);
-      kw[i] = *reinterpret_cast<const uint32_t*>(sm + G_K + tile_base + swz(i));
-      qw[i] = *reinterpret_cast<const uint32_t*>(sm + G_Q + tile_base + swz(i));
+      kw[i] = *reinterpret_cast<const uint32_t*>(sm + G_K + swz(i));
+      qw[i] = *reinterpret_cast<const uint32_t*>(sm + G_Q + swz(i));
     }
     if (gate2) {  // both g and gk given: the second one straight from global memory
-      const float* g2 = gate2 + ((tok0 + 16 * R) * Hq + h) * kD + c0;
+      const float* g2 = gate2 + (tok0 * Hq + h) * kD + c0;
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (16 * R + i < n) {
-          const float2 x = *reinterpret_cast<const float2*>(g2 + (long long)i * Hq * kD);
+          const float2 x =
+              *reinterpret_cast<const float2*>(g2 + (long long)srow(i) * Hq * kD);
           graw[i] = __fadd2_rn(graw[i], x);
         }
     }
@@ -516,6 +526,9 @@ __global__ void __launch_bounds__(kGThreads, 2)
 // 8-token totals).  Bound by its memory traffic; CTAs walk the records with a grid stride.
 constexpr int kVThreads = 512;
 
+// Without a value gate (reverse order routes every call through these records) b = 0:
+// V^ = V~ = v, E = 1.  kRev: position p is token 63 - p of the staged tile, as in the prep.
+template <bool kRev>
 __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a, const GWs w) {
   __shared__ float2 s_tot[8][kD / 2];
   const int cp = threadIdx.x & 63, P = threadIdx.x >> 6, R = P >> 1;
@@ -544,20 +557,23 @@ __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a
     long long bos;
     int len;
     gla_seq_range(a, seq, bos, len);
-    const long long ctok = bos + (long long)jc * kC;  // the chunk's first token (live)
-    const int n = min(kC, len - jc * kC);             // its live tokens (>= 1)
+    const int n = min(kC, len - jc * kC);  // live positions (>= 1)
+    // token of position 0 (live) and the step between positions
+    const long long ctok = kRev ? bos + len - 1 - (long long)jc * kC : bos + (long long)jc * kC;
+    const int dir = kRev ? -1 : 1;
     const int hk = h / grp;
-    // rows past the end read the chunk's first token instead and are masked, so that the
-    // loads are unconditional and all in flight at once
-    const float* const gbase = a.gv + (ctok * Hq + h) * kD + c0;
+    // positions past the end read position 0 instead and are masked, so that the loads are
+    // unconditional and all in flight at once
+    const float* const gbase = a.gv ? a.gv + (ctok * Hq + h) * kD + c0 : nullptr;
     const __nv_bfloat16* const vbase =
         static_cast<const __nv_bfloat16*>(a.v) + (ctok * a.Hkv + hk) * kD + c0;
     float2 L[8];
     uint32_t vw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int t = 8 * P + i, tt = t < n ? t : 0;
-      L[i] = *reinterpret_cast<const float2*>(gbase + tt * gstride);
+      const int t = 8 * P + i, tt = (t < n ? t : 0) * dir;
+      L[i] = gbase ? *reinterpret_cast<const float2*>(gbase + tt * gstride)
+                   : make_float2(0.f, 0.f);
       vw[i] = *reinterpret_cast<const uint32_t*>(vbase + tt * vstride);
     }
     float2 run = make_float2(0.f, 0.f);
@@ -633,7 +649,10 @@ constexpr uint32_t H_TM_Y = 256;
 constexpr uint32_t kHTmemColsVG = 512;
 
 // kVG: the value-axis gate (map_v then addresses the V^ records, map_vt the V~ records).
-template <bool kVG>
+// kRev: reverse order (always with the V^ / V~ records, which hold the positions in the
+// records' order): position p of chunk ch is token end - 64 ch - 1 - p, so the output tile's
+// row 63 - p.
+template <bool kVG, bool kRev>
 __global__ void __launch_bounds__(kHThreads, 1)
     gla_scan_kernel(const __grid_constant__ CUtensorMap map_qw,
                     const __grid_constant__ CUtensorMap map_kt,
@@ -770,7 +789,8 @@ __global__ void __launch_bounds__(kHThreads, 1)
     const int st = ch & 1;
     uint8_t* const b = sm + st * kStg;
     const int n = min(kC, len - ch * kC);
-    const long long tok0 = bos + (long long)ch * kC;
+    // first token of the chunk's token tile (reverse: the tile ends at position 0)
+    const long long tok0 = kRev ? bos + len - (long long)(ch + 1) * kC : bos + (long long)ch * kC;
 
     if (!(ok = block_wait(&bar_ld[st], (ch >> 1) & 1))) break;
     inflight[st] = -1;
@@ -887,19 +907,21 @@ __global__ void __launch_bounds__(kHThreads, 1)
       if (tid == 0) bulk_wait_read_all();  // the previous output store has read its tile
       __syncthreads();
       if (n == kC) {
-        const uint32_t ob = uint32_t(ln >> 6) * 8192u + uint32_t(wg) * 2048u;
+        const uint32_t ob = uint32_t(ln >> 6) * 8192u;
         const uint32_t och = uint32_t(((ln & 63) * 2) >> 4), oby = uint32_t(((ln & 63) * 2) & 15);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint32_t off = ob + uint32_t((i >> 3) * 1024 + (i & 7) * 128) +
-                               (((och ^ uint32_t(i & 7)) << 4) | oby);
+          const int rr = kRev ? 63 - 16 * wg - i : 16 * wg + i;  // the tile row of position
+          const uint32_t off = ob + uint32_t((rr >> 3) * 1024 + (rr & 7) * 128) +
+                               (((och ^ uint32_t(rr & 7)) << 4) | oby);
           *reinterpret_cast<__nv_bfloat16*>(sm + kOS + off) =
               __float2bfloat16_rn(o16[i] * s_vec[128 + 16 * wg + i]);
         }
       } else {
-        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
-                            ((tok0 + 16 * wg) * Hq + h) * kD + ln;
-        const long long stride = (long long)Hq * kD;
+        // the token of position 16 wg; positions step by one token (backwards in reverse)
+        const long long p0 = kRev ? tok0 + 63 - 16 * wg : tok0 + 16 * wg;
+        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) + (p0 * Hq + h) * kD + ln;
+        const long long stride = (kRev ? -1LL : 1LL) * Hq * kD;
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           if (16 * wg + i < n) op[i * stride] = __float2bfloat16_rn(o16[i] * s_vec[128 + 16 * wg + i]);
@@ -952,13 +974,13 @@ bool map_in(CUtensorMap* m, const void* base, long long rows, int H, bool fp32) 
 }  // namespace
 
 bool gla_chunk_supported(const GlaArgs& a, bool bf16) {
-  return bf16 && a.D == kD && !a.reverse;
+  return bf16 && a.D == kD;
 }
 
 size_t gla_chunk_workspace(const GlaArgs& a) {
   const long long recs = gla_slots(a) * a.Hq;
   const size_t coff = a.cu_seqlens ? split::align_up(size_t(a.nseq + 1) * 4, 256) : 0;
-  const long long vg = a.gv ? 3 * kGRecV + kGRecVTot : 0;
+  const long long vg = (a.gv || a.reverse) ? 3 * kGRecV + kGRecVTot : 0;
   return size_t(recs) * size_t(kGRecQ + kGRecK + kGRecM + kGRecVec + vg) + coff;
 }
 
@@ -984,7 +1006,8 @@ cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t st)
   const long long rec_rows = w.recs > 0 ? w.recs : 1;
   const float* gstage = a.gk ? a.gk : a.g;                 // staged by TMA
   const float* gate2 = (a.gk && a.g) ? a.g : nullptr;      // read from global memory
-  const bool vg = a.gv != nullptr;
+  const bool rev = a.reverse != 0;
+  const bool vg = a.gv != nullptr || rev;  // reverse order runs on the value records
   CUtensorMap mqw, mkt, mm, mv, mvt, mo, mq, mk, mg;
   if (!split::make_map_2d(&mqw, w.qw, rec_rows * 64, 128, 64) ||
       !split::make_map_2d(&mkt, w.kt, rec_rows * 128, 64, 128) ||
@@ -999,10 +1022,12 @@ cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t st)
       !map_in(&mg, gstage ? (const void*)gstage : a.q, map_rows, a.Hq, gstage != nullptr) ||
       !split::make_map_out(&mo, a.out, map_rows, a.Hq))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(gla_prep_kernel,
+  auto prep = rev ? gla_prep_kernel<true> : gla_prep_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(prep,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
   if (e != cudaSuccess) return e;
-  auto scan = vg ? gla_scan_kernel<true> : gla_scan_kernel<false>;
+  auto scan = rev ? gla_scan_kernel<true, true>
+                 : vg ? gla_scan_kernel<true, false> : gla_scan_kernel<false, false>;
   const size_t scan_smem = vg ? kHSmemVG : kHSmem;
   e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem);
   if (e != cudaSuccess) return e;
@@ -1012,11 +1037,12 @@ cudaError_t launch_gla_chunk(const GlaArgs& a, void* workspace, cudaStream_t st)
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
     const long long grid = std::min<long long>(w.recs, 2LL * sms);
-    gla_prep_kernel<<<(unsigned)grid, kGThreads, kGSmem, st>>>(mkt, mm, mq, mk, mg, a, gate2, w);
+    prep<<<(unsigned)grid, kGThreads, kGSmem, st>>>(mkt, mm, mq, mk, mg, a, gate2, w);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (vg) {
       const long long vgrid = std::min<long long>(w.recs, 2LL * sms);
-      gla_vprep_kernel<<<(unsigned)vgrid, kVThreads, 0, st>>>(a, w);
+      (rev ? gla_vprep_kernel<true> : gla_vprep_kernel<false>)<<<(unsigned)vgrid, kVThreads, 0,
+                                                                 st>>>(a, w);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }

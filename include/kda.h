@@ -398,20 +398,19 @@ enum kda_recurrent_flags {
 /*
  * kda_recurrent_attention_fwd_workspace_size / kda_recurrent_attention_fwd_ws --
  *   kda_recurrent_attention_fwd through a caller workspace (same arguments, layouts, results
- *   and errors, plus the workspace).  For bf16 with D = 128 and forward order it runs the
- *   recurrence in its chunked form on the tensor cores (64-token chunks: every chunk's
- *   gate-scaled product q k^T and its records at once, then the sequential pass over the
- *   state; the recurrent page's run parameters g, gk, g_gamma, gv, cu_seqlens).  On that path
- *   the summed key-axis gate g + gk + g_gamma and the value-axis gate gv must each lie in
- *   [-5, 1] at every token and channel, where the chunks' factorised exponentials stay inside
- *   the fp32 range; outside it the results are unspecified (no fault).  Every other
- *   configuration (fp32, other head dims, reverse order) ignores the workspace and runs the
- *   token-serial kernel.
+ *   and errors, plus the workspace).  For bf16 with D = 128 it runs the recurrence in its
+ *   chunked form on the tensor cores (64-token chunks: every chunk's gate-scaled product
+ *   q k^T and its records at once, then the sequential pass over the state; the recurrent
+ *   page's run parameters g, gk, g_gamma, gv, cu_seqlens, reverse).  On that path the summed
+ *   key-axis gate g + gk + g_gamma and the value-axis gate gv must each lie in [-5, 1] at
+ *   every token and channel, where the chunks' factorised exponentials stay inside the fp32
+ *   range; outside it the results are unspecified (no fault).  Every other configuration
+ *   (fp32, other head dims) ignores the workspace and runs the token-serial kernel.
  *   workspace: at least kda_recurrent_attention_fwd_workspace_size(N, B, T, Hq, Hkv, D,
  *   flags, dtype) bytes (flags: kda_recurrent_flags describing the call; 0: none needed),
  *   256-byte aligned, caller-owned, contents unspecified on return; a smaller or misaligned
  *   buffer gives KDA_ERR_WORKSPACE.  About 41 KB per (64-token chunk, query head), 91 KB
- *   with a value-axis gate.
+ *   with a value-axis gate or in reverse order.
  */
 size_t kda_recurrent_attention_fwd_workspace_size(int N, int B, int T, int Hq, int Hkv, int D,
                                                   int flags, int dtype);

@@ -436,8 +436,9 @@ def test_selftest_rejects_unbounded_limits(L, limit):
 def test_recurrent_workspace_sizes(L):
     """kda_recurrent_attention_fwd_workspace_size: the chunked path's records per (64-token
     chunk slot, query head) -- Q~, K^^T, M and the vector; with a value gate also V^, V~,
-    e^{B - Q} and the sub-chunk totals -- plus, for packed sequences, the chunk offsets; 0
-    where the token-serial kernel runs (reverse order, fp32, other head dims)."""
+    e^{B - Q} and the sub-chunk totals (reverse order uses them too) -- plus, for packed
+    sequences, the chunk offsets; 0 where the token-serial kernel runs (fp32, other head
+    dims)."""
     f = L.kda_recurrent_attention_fwd_workspace_size
     per = 16384 + 16384 + 8192 + 1024
     vg = 3 * 16384 + 2048
@@ -445,8 +446,8 @@ def test_recurrent_workspace_sizes(L):
     recs = B * ((T + 63) // 64) * Hq
     assert f(0, B, T, Hq, Hkv, 128, 0, 1) == recs * per
     assert f(0, B, T, Hq, Hkv, 128, 2, 1) == recs * (per + vg)
-    assert f(0, B, T, Hq, Hkv, 128, 4, 1) == 0  # reverse
-    assert f(0, B, T, Hq, Hkv, 128, 2 | 4, 1) == 0
+    assert f(0, B, T, Hq, Hkv, 128, 4, 1) == recs * (per + vg)  # reverse
+    assert f(0, B, T, Hq, Hkv, 128, 2 | 4, 1) == recs * (per + vg)
     assert f(0, B, T, Hq, Hkv, 128, 2, 0) == 0  # fp32
     assert f(0, B, T, Hq, Hkv, 64, 2, 1) == 0  # D = 64
     N = 3

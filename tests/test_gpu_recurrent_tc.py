@@ -1,12 +1,12 @@
 """Parity of kda_recurrent_attention_fwd_ws -- the recurrent page's gated linear recurrence
 in its chunked form on the tensor cores (bf16, D = 128, key-axis gates g / gk / g_gamma and
-the value-axis gate gv, forward order) -- with the fp64 oracle ``recurrent_attention``: every
+the value-axis gate gv, forward and reverse order) -- with the fp64 oracle ``recurrent_attention``: every
 combination of the key-axis gates (none, one, several) with and without gv, grouped key /
 value heads, packed sequences with empty and ragged members, gates from mild to the edge of
 the supported range [-5, 1], and the benchmark's full workloads (gk; gk + gv) compared
 element by element.  Bar: max |gpu - oracle| / max |oracle| <= 2e-2 per tensor, the oracle
-fed the same bf16-rounded q, k, v.  Calls that the chunked path does not serve (reverse
-order) give the token-serial kernel's results bit for bit."""
+fed the same bf16-rounded q, k, v.  Reverse order (the chunks walked from each sequence's
+end) is checked the same way."""
 import numpy as np
 import pytest
 import torch
@@ -112,17 +112,42 @@ def test_many_records_odd_head_count(gates):
     _check(d, out, S, None)
 
 
-@pytest.mark.parametrize("gates", [("gk",), ("gk", "gv")])
-def test_reverse_takes_the_token_serial_kernel(gates):
-    B, T, Hq, Hkv = 1, 90, 2, 2
-    d = _inputs(B, T, Hq, Hkv, 11, gates, True)
-    rev = True
-    assert kda.kda_recurrent_attention_fwd_workspace_size(
-        B, T, Hq, Hkv, D, value_gate="gv" in gates, reverse=rev) == 0
-    o1, S1 = _run(d, B, T, Hq, Hkv, 0.3, ws=True, reverse=rev)
-    o2, S2 = _run(d, B, T, Hq, Hkv, 0.3, ws=False, reverse=rev)
-    np.testing.assert_array_equal(o1, o2)
-    np.testing.assert_array_equal(S1, S2)
+def _check_rev(d, out, S, scale, cu=None):
+    o = dict(d)
+    for n in ("q", "k", "v"):
+        o[n] = bf16_round(d[n])
+    ro, rs = recurrent_attention(o["q"], o["k"], o["v"], o["g"], o["g_gamma"], o["gk"], o["gv"],
+                                 scale, o["s0"], True, cu)
+    check_rel(None, "out", out, ro)
+    check_rel(None, "final_state", S, rs)
+
+
+@pytest.mark.parametrize("gates", [(), ("gk",), ("gv",), ("gk", "gv"), ("g", "gk", "g_gamma"),
+                                   ("g", "gk", "gv", "g_gamma")])
+@pytest.mark.parametrize("T", [1, 63, 64, 90, 200])
+def test_reverse_order(gates, T):
+    B, Hq, Hkv = 2, 4, 2
+    d = _inputs(B, T, Hq, Hkv, 11 + T, gates, True)
+    out, S = _run(d, B, T, Hq, Hkv, 0.3, reverse=True)
+    _check_rev(d, out, S, 0.3)
+
+
+@pytest.mark.parametrize("gates", [("gk", "g_gamma"), ("gk", "gv")])
+def test_reverse_packed_sequences(gates):
+    lens = [130, 0, 1, 64, 200, 63]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, Hq, Hkv = int(cu[-1]), 4, 2
+    d = _inputs(1, T, Hq, Hkv, 17, gates, True, nseq=len(lens))
+    out, S = _run(d, 1, T, Hq, Hkv, 0.1, cu=cu, reverse=True)
+    _check_rev(d, out, S, 0.1, cu)
+
+
+def test_reverse_gate_edge_many_records():
+    """Gates at the edge of the range, more records than the prep's persistent CTAs."""
+    B, T, Hq, Hkv = 2, 1000, 6, 3
+    d = _inputs(B, T, Hq, Hkv, 19, ("gk", "gv"), True, lo=-5.0, hi=0.0)
+    out, S = _run(d, B, T, Hq, Hkv, None, reverse=True)
+    _check_rev(d, out, S, None)
 
 
 @pytest.mark.parametrize("value_gate", [False, True])
