@@ -579,26 +579,48 @@ def cpu_baseline(w, d, budget_s=12.0):
     """The fp64 oracle on a bounded sample of the workload, on every host core: all (b, h)
     pairs, the first T_s tokens, cut into (batch element, head range) groups that run in a
     pool of spawned worker processes (one per core, single-threaded numpy each); T_s grows
-    until one run takes a few seconds."""
+    until one run takes a few seconds.  The oracle is fed the bf16 values the device path
+    reads (q, k, v rounded outside the timed calls).  Returns the baseline and, when the
+    sample is the whole workload, the oracle's output and final state."""
     from oracle import pool
+    torch = _torch()
+    qkv = [torch.from_numpy(np.ascontiguousarray(d[n])).to(torch.bfloat16).to(torch.float64)
+           .numpy() for n in ("q", "k", "v")]
     p = pool.Pool()
     try:
         Ts = 32
         while True:
             t0 = time.perf_counter()
-            pool.forward(p.ex, d["q"][:, :Ts], d["k"][:, :Ts], d["v"][:, :Ts], d["g"][:, :Ts],
-                         d["beta_logits"][:, :Ts], d["a_log"], d["dt_bias"], w.q_scale,
-                         w.lower_bound, d["initial_state"], workers=p.workers)
+            res = pool.forward(p.ex, qkv[0][:, :Ts], qkv[1][:, :Ts], qkv[2][:, :Ts],
+                               d["g"][:, :Ts], d["beta_logits"][:, :Ts], d["a_log"],
+                               d["dt_bias"], w.q_scale, w.lower_bound, d["initial_state"],
+                               workers=p.workers)
             dt = time.perf_counter() - t0
             if dt > budget_s / 3 or Ts >= w.T:
                 break
             Ts = min(w.T, Ts * 2)
     finally:
         p.close()
-    return {"value": w.B * Ts / dt, "unit": "tokens/s", "cores": p.workers, "kind": "oracle",
-            "sample": f"B={w.B}, all {w.H} heads, first {Ts} of {w.T} tokens ({dt:.1f} s; "
-                      f"numpy fp64 token scan over {p.workers} worker processes, one per "
-                      f"host core, single-threaded each)"}
+    return ({"value": w.B * Ts / dt, "unit": "tokens/s", "cores": p.workers, "kind": "oracle",
+             "sample": f"B={w.B}, all {w.H} heads, first {Ts} of {w.T} tokens ({dt:.1f} s; "
+                       f"numpy fp64 token scan over {p.workers} worker processes, one per "
+                       f"host core, single-threaded each)"},
+            res if Ts >= w.T else None)
+
+
+def parity_report(out, state, ref_out, ref_state, floor=1e-3):
+    """The benchmarked call's errors against the fp64 oracle over the whole workload:
+    max |gpu - oracle| / max |oracle| per tensor (the parity bar is 2e-2), and the
+    elementwise relative error with a floor of 1e-3 max |oracle| (maximum, 99th percentile)."""
+    rep_ = {"vs": "fp64 oracle on the same bf16-rounded inputs, every element", "bar": 2e-2}
+    for name, g, r in (("out", out, ref_out), ("final_state", state, ref_state)):
+        r = np.asarray(r, np.float64)
+        err = np.abs(np.asarray(g, np.float64) - r)
+        top = max(float(np.max(np.abs(r))), 1e-30)
+        el = err / np.maximum(np.abs(r), floor * top)
+        rep_[name] = {"max_rel": float(np.max(err)) / top, "elem_max": float(np.max(el)),
+                      "elem_p99": float(np.quantile(el, 0.99))}
+    return rep_
 
 
 def native(args):
@@ -618,6 +640,10 @@ def native(args):
     clocks.start()
     ms = timed(lambda: call_chunk(w, x), K, W, dist, clocks)
     clk = clocks.stop()
+    # the benchmarked call's results (every step computes the same ones), for the comparison
+    # with the oracle that the CPU baseline's run yields
+    step_out = x["out"].float().cpu().numpy()
+    step_state = x["final_state"].cpu().numpy()
     tokens = w.B * w.T * K * dist.world
     value = tokens / (ms * 1e-3)
     pk = peaks()
@@ -690,7 +716,9 @@ def native(args):
         line["attention"]["vs_chunk_fwd_ws_step"] = line["attention"]["ms_per_call"] / (ms / K)
         line["backward"] = backward_measure(w, d, x)
         line["backward"]["frac_of_hbm_peak"] = line["backward"]["hbm_gbs"] / pk["hbm_gbs"]
-        line["cpu_baseline"] = cpu_baseline(w, d)
+        line["cpu_baseline"], ref = cpu_baseline(w, d)
+        if ref is not None:
+            line["parity"] = parity_report(step_out, step_state, *ref)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
