@@ -603,12 +603,13 @@ __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a
     for (int i = 0; i < 8; ++i) {
       const bool live = 8 * P + i < n;
       const float v0 = live ? bf16_lo(vw[i]) : 0.f, v1 = live ? bf16_hi(vw[i]) : 0.f;
+      // e^{L} lies within e^{+-80} (16 gates in [-5, 1]): its reciprocal is e^{-L}
+      const float e0 = __expf(L[i].x), e1 = __expf(L[i].y);
       *reinterpret_cast<uint32_t*>(w.vh + row0 + i * kD) =
           pack_bf16(v0 * __expf(tail.x - L[i].x), v1 * __expf(tail.y - L[i].y));
       *reinterpret_cast<uint32_t*>(w.vt + row0 + i * kD) =
-          pack_bf16(v0 * __expf(-L[i].x), v1 * __expf(-L[i].y));
-      *reinterpret_cast<uint32_t*>(w.eb + row0 + i * kD) =
-          live ? pack_bf16(__expf(L[i].x), __expf(L[i].y)) : 0u;
+          pack_bf16(v0 * fast_rcp(e0), v1 * fast_rcp(e1));
+      *reinterpret_cast<uint32_t*>(w.eb + row0 + i * kD) = live ? pack_bf16(e0, e1) : 0u;
     }
     __syncthreads();  // s_tot is rewritten for the next record
   }
