@@ -17,15 +17,15 @@ int check_device() {
     cudaGetLastError();
     return KDA_ERR_DEVICE;
   }
-  static int verdict[64] = {0};  // 0 unknown, 1 ok, -1 bad
-  if (dev < 64 && verdict[dev] != 0) return verdict[dev] > 0 ? KDA_OK : KDA_ERR_DEVICE;
+  static int dev_state[64] = {0};  // per device: 0 unchecked, 1 usable, -1 not
+  if (dev < 64 && dev_state[dev] != 0) return dev_state[dev] > 0 ? KDA_OK : KDA_ERR_DEVICE;
   int major = 0, minor = 0;
   const bool ok =
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
       major == 10 && minor == 3;
   cudaGetLastError();
-  if (dev < 64) verdict[dev] = ok ? 1 : -1;
+  if (dev < 64) dev_state[dev] = ok ? 1 : -1;
   return ok ? KDA_OK : KDA_ERR_DEVICE;
 }
 
