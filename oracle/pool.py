@@ -165,8 +165,8 @@ def decode_chain(ex, tokens, a_log, dt_bias, scale, lower_bound, S0, workers=Non
 
 
 def recurrent(ex, query, key, value, g=None, g_gamma=None, gk=None, gv=None,
-              softmax_scale=None, initial_state=None, workers=None):
-    """``recurrent_attention`` (forward order, fixed-length sequences) over
+              softmax_scale=None, initial_state=None, workers=None, reverse=False):
+    """``recurrent_attention`` (either order, fixed-length sequences) over
     ``[B, T, Hq, D]`` inputs, one task per (batch element, range of query heads); each range
     covers whole groups of query heads sharing a key / value head.  Same return value as
     ``recurrent_attention``."""
@@ -185,7 +185,7 @@ def recurrent(ex, query, key, value, g=None, g_gamma=None, gk=None, gv=None,
                 query=query[b:b + 1, :, h0:h1], key=key[b:b + 1, :, k0:k1],
                 value=value[b:b + 1, :, k0:k1], g=sl(g), gk=sl(gk), gv=sl(gv),
                 g_gamma=None if g_gamma is None else g_gamma[b:b + 1, h0:h1],
-                softmax_scale=softmax_scale,
+                softmax_scale=softmax_scale, reverse=reverse,
                 initial_state=None if initial_state is None else initial_state[b:b + 1, h0:h1]))
             where.append((b, h0, h1))
     out = np.zeros((B, T, Hq, D))

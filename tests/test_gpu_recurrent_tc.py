@@ -171,3 +171,16 @@ def test_benchmark_workload_full(value_gate):
                             None, None, d["gk"], d["gv"], None, None)
     check_full("recurrent B4 T4096 Hq32 Hkv8, gk" + (" + gv" if value_gate else "") +
                ", kda_recurrent_attention_fwd_ws", out, ro, S, rs)
+
+
+def test_reverse_value_gate_long_sequences():
+    """Reverse order with both gates over 128-chunk sequences (B=2, T=8192, Hq=8, Hkv=2,
+    initial states), every element against the oracle."""
+    B, T, Hq, Hkv = 2, 8192, 8, 2
+    d = _inputs(B, T, Hq, Hkv, 23, ("gk", "gv"), True, lo=-0.1, hi=0.0)
+    out, S = _run(d, B, T, Hq, Hkv, None, reverse=True)
+    from oracle import pool
+    ro, rs = pool.recurrent(oracle_pool(), *(bf16_round(d[n]) for n in ("q", "k", "v")),
+                            None, None, d["gk"], d["gv"], None, d["s0"], reverse=True)
+    check_rel(None, "out", out, ro)
+    check_rel(None, "final_state", S, rs)
