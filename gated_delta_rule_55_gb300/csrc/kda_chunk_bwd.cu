@@ -516,11 +516,11 @@ __global__ void __launch_bounds__(kKThreads, 1)
   __shared__ uint64_t bar_ld, bar_raw, bar_mma;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[4];
-  __shared__ __align__(16) float s_gtot[4][kD];
+  __shared__ __align__(16) float s_half[8][kD];  // gate total of each half sub-chunk
   __shared__ __align__(16) float s_beta[kC], s_rk[kC], s_rq[kC];
   __shared__ __align__(16) float s_lu[4][kC];
   __shared__ __align__(16) float s_sdot[4][kD];
-  __shared__ __align__(16) float s_dgs[4][kD];
+  __shared__ __align__(16) float s_dgs[8][kD];  // sum of dG over each half sub-chunk
   __shared__ __align__(16) float s_dgc[4][kD];
   __shared__ __align__(16) float s_qd[4][kC], s_kd[4][kC];
   __shared__ __align__(16) float s_ddb[4][kD];
@@ -528,8 +528,15 @@ __global__ void __launch_bounds__(kKThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int R = tid >> 7;      // sub-chunk (tokens 16 R .. 16 R + 15)
+  const int R = tid >> 7;      // warpgroup: a quarter of the work in the split phases
   const int c = tid & 127;     // channel (Tensor Memory lane)
+  // The token-wise phases give each warpgroup two half sub-chunks ("units": 8 tokens of
+  // sub-chunk uR[u], half uh), paired so that every warpgroup carries the same off-diagonal
+  // work (sub-chunk r has 3 - r off-diagonal blocks): warpgroups 0, 1 take sub-chunks 0 and
+  // 3, warpgroups 2, 3 sub-chunks 1 and 2, each one half of both.
+  const int uh = R & 1;
+  const int uR[2] = {R < 2 ? 0 : 1, R < 2 ? 3 : 2};
+  const int ut0[2] = {16 * uR[0] + 8 * uh, 16 * uR[1] + 8 * uh};  // first token of each unit
   const int sp = warp & 3;     // Tensor Memory sub-partition
   const int H = a.H;
   if (warp == 0) {
@@ -634,7 +641,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   const float ea = __expf(a.a_log[h]);
   const float db = a.dt_bias[c * H + h];
   __syncthreads();
-  float loc[16], P[4], fg[4], GC, PR;
+  float loc[16], P[4], fg[2][4], GC, PR[2];
 
   // element (t, c) of the staged tiles
   const uint8_t* const rq_t = sm + K_RQ;
@@ -648,25 +655,35 @@ __global__ void __launch_bounds__(kKThreads, 1)
   };
   auto row_of = [&](int t) -> long long { return (tok0 + t) * H + h; };
 
-  // ---- gates: G_t - P_R for this thread's channel and sub-chunk
+  // ---- gates: the prefix inside each of this thread's units (completed to G_t - P_R once
+  //      the first halves' totals are known)
   if (!block_wait(&bar_raw, raw_seen & 1)) goto fail;
   ++raw_seen;
-  {
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
     float run = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = 16 * R + i;
+    for (int i = 0; i < 8; ++i) {
+      const int t = ut0[u] + i;
       float gm = 0.f;
       if (t < n) gm = a.lower_bound * fast_rcp(1.f + fast_exp(-ea * (rg_t[t * 32] + db)));
       run += gm;
-      loc[i] = run;
+      loc[8 * u + i] = run;
     }
-    s_gtot[R][c] = run;
+    s_half[2 * uR[u] + uh][c] = run;
   }
 
   // ---- loaded tiles: clear d_out rows past the chunk, S . dS' per channel (quarter of j)
   if (!block_wait(&bar_ld, ld_seen & 1)) goto fail;
   ++ld_seen;
+  if (uh) {  // second halves: add the first half's total
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float first = s_half[2 * uR[u]][c];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) loc[8 * u + i] += first;
+    }
+  }
   if (n < kC) zero_rows(sm + K_DO, n, tid);
   {
     float acc = 0.f;
@@ -701,16 +718,19 @@ __global__ void __launch_bounds__(kKThreads, 1)
     }
     mma_commit(&bar_mma);
   }
-  // meanwhile: the sub-chunk reference points
+  // meanwhile: the sub-chunk reference points, and each unit's P_R and e^{P_g - P_R}
   P[0] = 0.f;
 #pragma unroll
-  for (int r = 1; r < 4; ++r) P[r] = P[r - 1] + s_gtot[r - 1][c];
-  GC = P[3] + s_gtot[3][c];
-  PR = P[0];
+  for (int r = 1; r < 4; ++r) P[r] = P[r - 1] + (s_half[2 * r - 2][c] + s_half[2 * r - 1][c]);
+  GC = P[3] + (s_half[6][c] + s_half[7][c]);
 #pragma unroll
-  for (int r = 1; r < 4; ++r) PR = (R == r) ? P[r] : PR;
+  for (int u = 0; u < 2; ++u) {
+    PR[u] = P[0];
 #pragma unroll
-  for (int g = 0; g < 4; ++g) fg[g] = (g > R) ? fast_exp(P[g] - PR) : 0.f;
+    for (int r = 1; r < 4; ++r) PR[u] = (uR[u] == r) ? P[r] : PR[u];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) fg[u][g] = (g > uR[u]) ? fast_exp(P[g] - PR[u]) : 0.f;
+  }
   if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
   tc_fence_after();
 
@@ -773,7 +793,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   // whose readers (dKd^T and the S . dS' sums) are done
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const int t = 16 * R + i;
+    const int t = ut0[i >> 3] + (i & 7);
     const bool live = t < n;
     const float kh = live ? raw_k(t) * s_rk[t] : 0.f;
     const float qh = live ? raw_q(t) * s_rq[t] : 0.f;
@@ -824,14 +844,14 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const int t = 16 * R + i;
+    const int u = i >> 3, t = ut0[u] + (i & 7);
     const float kd = (t < n) ? raw_k(t) * s_rk[t] * fast_exp(-loc[i]) : 0.f;
     *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(t, c, 20480)) = __float2bfloat16_rn(kd);
 #pragma unroll
     for (int g = 1; g < 4; ++g)
-      if (g > R)
+      if (g > uR[u])
         *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(kb_base(g) + t, c, 20480)) =
-            __float2bfloat16_rn(kd * fg[g]);
+            __float2bfloat16_rn(kd * fg[u][g]);
   }
   fence_async_smem();
   tc_fence_before();
@@ -860,18 +880,18 @@ __global__ void __launch_bounds__(kKThreads, 1)
     if (locate(rec + gridDim.x, nt0, ncnt)) issue_ld(rec + gridDim.x, nt0);
   }
 
-  // ---- epilogue: per (channel c, token t of sub-chunk R)
+  // ---- epilogue: per (channel c, token t of each of this thread's units)
   {
-    const float eP = fast_exp(PR), eCP = fast_exp(GC - PR);
     float dG[16];
-    // token pairs (t, t + 1) ride Blackwell's two-lane fp32 instructions; every pair operation
-    // rounds exactly as the two scalar ones would
-    const float2 ePv = make_float2(eP, eP), neP = make_float2(-eP, -eP);
-    const float2 eCPv = make_float2(eCP, eCP);
     float2 dgc2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int cb = 16 * R + 8 * hh;  // first token of this half
+    for (int hh = 0; hh < 2; ++hh) {  // (unit hh: sub-chunk uR[hh])
+      const int cb = ut0[hh];  // first token of this unit
+      const float eP = fast_exp(PR[hh]), eCP = fast_exp(GC - PR[hh]);
+      // token pairs (t, t + 1) ride Blackwell's two-lane fp32 instructions; every pair
+      // operation rounds exactly as the two scalar ones would
+      const float2 ePv = make_float2(eP, eP), neP = make_float2(-eP, -eP);
+      const float2 eCPv = make_float2(eCP, eCP);
       float2 E[4], EI[4], KH[4], QH[4], AQ2[4], POS[4], NEG[4], DG[4], T[4];
       float t8[8];
       auto load_t = [&](uint32_t col) {
@@ -937,8 +957,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
       }
 #pragma unroll
       for (int g = 1; g < 4; ++g)
-        if (g > R) {
-          const float2 fgv = make_float2(fg[g], fg[g]);
+        if (g > uR[hh]) {
+          const float2 fgv = make_float2(fg[hh][g], fg[hh][g]);
           load_t(KT_P7 + kb_base(g) + cb);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
@@ -993,13 +1013,14 @@ __global__ void __launch_bounds__(kKThreads, 1)
       }
     }
     const float dgc = dgc2.x + dgc2.y;
-    {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
       float sg = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) sg += dG[i];
-      s_dgs[R][c] = sg;
-      s_dgc[R][c] = dgc;
+      for (int i = 0; i < 8; ++i) sg += dG[8 * u + i];
+      s_dgs[2 * uR[u] + uh][c] = sg;
     }
+    s_dgc[R][c] = dgc;
     tmem_wait_st();
     __syncthreads();
     // the next record's raw q, k, g: the raw tiles are not read from here on
@@ -1014,10 +1035,6 @@ __global__ void __launch_bounds__(kKThreads, 1)
     // dgamma_t = sum_{r >= t} dG_r + dG_C
     const float dGC = s_dgc[0][c] + s_dgc[1][c] + s_dgc[2][c] + s_dgc[3][c] +
                       fast_exp(GC) * (s_sdot[0][c] + s_sdot[1][c] + s_sdot[2][c] + s_sdot[3][c]);
-    float carry = dGC;
-#pragma unroll
-    for (int r = 1; r < 4; ++r)
-      if (r > R) carry += s_dgs[r][c];
     // per-token sums of q^ . dq^ and k^ . dk^ over the four warps of each sub-chunk
     if (tid < kC) {
       s_qd[0][tid] += s_qd[1][tid] + s_qd[2][tid] + s_qd[3][tid];
@@ -1029,14 +1046,23 @@ __global__ void __launch_bounds__(kKThreads, 1)
     float ddb = 0.f, dal = 0.f;
     const float inv_s2 = 1.f / (a.scale * a.scale);
     const float lb = a.lower_bound;
-    // this thread's element of token 16 R in each [B, T, H, 128] output; tokens H * 128 apart
-    const long long base = row_of(16 * R) * kD + c, tstride = (long long)H * kD;
+    const long long tstride = (long long)H * kD;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+    // the sum of dG over every later half sub-chunk, then this unit's tokens backwards
+    float carry = dGC;
+#pragma unroll
+    for (int x = 1; x < 8; ++x)
+      if (x > 2 * uR[u] + uh) carry += s_dgs[x][c];
+    // this thread's element of the unit's first token in each [B, T, H, 128] output; tokens
+    // H * 128 apart
+    const long long base = row_of(ut0[u]) * kD + c;
     float* const dg_p = o.dg + base;
     __nv_bfloat16* const dq_p = o.dq + base;
     __nv_bfloat16* const dk_p = o.dk + base;
 #pragma unroll
-    for (int qq = 3; qq >= 0; --qq) {
-      const int cb = 16 * R + 4 * qq;
+    for (int qq = 1; qq >= 0; --qq) {
+      const int cb = ut0[u] + 4 * qq;
       float aq[4], dkh[4], qh[4], kh[4], xg[4];
       tmem_ld4(tl + KT_KEEP_AQ + cb, aq);
       tmem_ld4(tl + KT_KEEP_DKH + cb, dkh);
@@ -1045,7 +1071,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
       tmem_ld4(tl + KT_KEEP_X + cb, xg);
 #pragma unroll
       for (int i = 3; i >= 0; --i) {
-        carry += dG[4 * qq + i];
+        carry += dG[8 * u + 4 * qq + i];
         const int t = cb + i;
         if (t < n) {
           // gate: gamma = lb sigmoid(x), x = e^{a_log} (g + dt_bias)
@@ -1063,6 +1089,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
         }
       }
     }
+    }  // units
     s_ddb[R][c] = ddb;
     dal = warp_sum(dal);
     if (lane == 0) s_dal[warp] = dal;
