@@ -809,33 +809,35 @@ __global__ void __launch_bounds__(kKThreads, 1)
   //      (k^ e^{P_R - G_t}) and base_g + t (k^ e^{P_g - G_t}) over dU^T, N and U^T;
   //      dbeta_logits
   if (sp < 2) {
-    float da[16], dm[16];
-    tmem_ld16(tl + KT_DA + 16 * R, da);
-    tmem_ld16(tl + KT_DM + 16 * R, dm);
+    // row r of dA and dM; the columns of this thread's two units (8 tokens s of sub-chunk
+    // uR[u]), placed in the diagonal block and the off-diagonal blocks that refer them
     const int r = 32 * sp + lane, Rr = r >> 4;
     const bool live = r < n;
-    uint32_t wa[8], wm[8];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const int s0 = 16 * R + 2 * p;
-      wa[p] = pack_bf16((live && s0 < r) ? -da[2 * p] : 0.f, (live && s0 + 1 < r) ? -da[2 * p + 1] : 0.f);
-      wm[p] = pack_bf16((live && s0 <= r) ? dm[2 * p] : 0.f, (live && s0 + 1 <= r) ? dm[2 * p + 1] : 0.f);
-    }
-    auto put = [&](int row, int col0, bool on, const uint32_t (&w)[8]) {
-      uint8_t* t = sm + K_D1;
-      const uint4 lo = on ? make_uint4(w[0], w[1], w[2], w[3]) : make_uint4(0, 0, 0, 0);
-      const uint4 hi = on ? make_uint4(w[4], w[5], w[6], w[7]) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(t + sw_off(row, col0, 16384)) = lo;
-      *reinterpret_cast<uint4*>(t + sw_off(row, col0 + 8, 16384)) = hi;
+    auto put = [&](int row, int col0, bool on, const uint32_t (&w)[4]) {
+      *reinterpret_cast<uint4*>(sm + K_D1 + sw_off(row, col0, 16384)) =
+          on ? make_uint4(w[0], w[1], w[2], w[3]) : make_uint4(0, 0, 0, 0);
     };
-    put(r, 16 * R, R == Rr, wa);
-    put(64 + r, 16 * R, R == Rr, wm);
 #pragma unroll
-    for (int g = 1; g < 4; ++g)
-      if (g > R) {
-        put(r, kb_base(g) + 16 * R, Rr == g, wa);
-        put(64 + r, kb_base(g) + 16 * R, Rr == g, wm);
+    for (int u = 0; u < 2; ++u) {
+      float da[8], dm[8];
+      tmem_ld8(tl + KT_DA + ut0[u], da);
+      tmem_ld8(tl + KT_DM + ut0[u], dm);
+      uint32_t wa[4], wm[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int s0 = ut0[u] + 2 * p;
+        wa[p] = pack_bf16((live && s0 < r) ? -da[2 * p] : 0.f, (live && s0 + 1 < r) ? -da[2 * p + 1] : 0.f);
+        wm[p] = pack_bf16((live && s0 <= r) ? dm[2 * p] : 0.f, (live && s0 + 1 <= r) ? dm[2 * p + 1] : 0.f);
       }
+      put(r, ut0[u], uR[u] == Rr, wa);
+      put(64 + r, ut0[u], uR[u] == Rr, wm);
+#pragma unroll
+      for (int g = 1; g < 4; ++g)
+        if (g > uR[u]) {
+          put(r, kb_base(g) + ut0[u], Rr == g, wa);
+          put(64 + r, kb_base(g) + ut0[u], Rr == g, wm);
+        }
+    }
   } else if (tid >= 64 && tid < 64 + kC) {  // warps 2 and 3 (sub-partitions 2, 3)
     const int t = tid - 64;
     if (t < n)
