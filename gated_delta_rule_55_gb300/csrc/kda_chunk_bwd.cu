@@ -523,6 +523,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   __shared__ __align__(16) float s_dgs[8][kD];  // sum of dG over each half sub-chunk
   __shared__ __align__(16) float s_dgc[4][kD];
   __shared__ __align__(16) float s_qd[4][kC], s_kd[4][kC];
+  __shared__ __align__(16) float4 s_tf[kC];  // per token: rq, q^.dq^ / scale^2, rk, k^.dk^
   __shared__ __align__(16) float s_ddb[4][kD];
   __shared__ float s_dal[16];
 
@@ -813,22 +814,24 @@ __global__ void __launch_bounds__(kKThreads, 1)
     // uR[u]), placed in the diagonal block and the off-diagonal blocks that refer them
     const int r = 32 * sp + lane, Rr = r >> 4;
     const bool live = r < n;
-    auto put = [&](int row, int col0, bool on, const uint32_t (&w)[4]) {
+    auto put = [&](int row, int col0, bool on, uint4 w) {
       *reinterpret_cast<uint4*>(sm + K_D1 + sw_off(row, col0, 16384)) =
-          on ? make_uint4(w[0], w[1], w[2], w[3]) : make_uint4(0, 0, 0, 0);
+          on ? w : make_uint4(0, 0, 0, 0);
     };
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       float da[8], dm[8];
       tmem_ld8(tl + KT_DA + ut0[u], da);
       tmem_ld8(tl + KT_DM + ut0[u], dm);
-      uint32_t wa[4], wm[4];
+      uint32_t pa[4], pm[4];
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         const int s0 = ut0[u] + 2 * p;
-        wa[p] = pack_bf16((live && s0 < r) ? -da[2 * p] : 0.f, (live && s0 + 1 < r) ? -da[2 * p + 1] : 0.f);
-        wm[p] = pack_bf16((live && s0 <= r) ? dm[2 * p] : 0.f, (live && s0 + 1 <= r) ? dm[2 * p + 1] : 0.f);
+        pa[p] = pack_bf16((live && s0 < r) ? -da[2 * p] : 0.f, (live && s0 + 1 < r) ? -da[2 * p + 1] : 0.f);
+        pm[p] = pack_bf16((live && s0 <= r) ? dm[2 * p] : 0.f, (live && s0 + 1 <= r) ? dm[2 * p + 1] : 0.f);
       }
+      const uint4 wa = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+      const uint4 wm = make_uint4(pm[0], pm[1], pm[2], pm[3]);
       put(r, ut0[u], uR[u] == Rr, wa);
       put(64 + r, ut0[u], uR[u] == Rr, wm);
 #pragma unroll
@@ -1037,17 +1040,19 @@ __global__ void __launch_bounds__(kKThreads, 1)
     // dgamma_t = sum_{r >= t} dG_r + dG_C
     const float dGC = s_dgc[0][c] + s_dgc[1][c] + s_dgc[2][c] + s_dgc[3][c] +
                       fast_exp(GC) * (s_sdot[0][c] + s_sdot[1][c] + s_sdot[2][c] + s_sdot[3][c]);
-    // per-token sums of q^ . dq^ and k^ . dk^ over the four warps of each sub-chunk
+    // per token: the sums of q^ . dq^ and k^ . dk^ over the four warps that hold its
+    // channels, beside the norms' factors, for one 16-byte read per token below
+    const float inv_s2 = 1.f / (a.scale * a.scale);
     if (tid < kC) {
-      s_qd[0][tid] += s_qd[1][tid] + s_qd[2][tid] + s_qd[3][tid];
-    } else if (tid < 2 * kC) {
-      const int t = tid - kC;
-      s_kd[0][t] += s_kd[1][t] + s_kd[2][t] + s_kd[3][t];
+      const float qs = s_qd[0][tid] + s_qd[1][tid] + s_qd[2][tid] + s_qd[3][tid];
+      const float ks = s_kd[0][tid] + s_kd[1][tid] + s_kd[2][tid] + s_kd[3][tid];
+      s_tf[tid] = make_float4(s_rq[tid], qs * inv_s2, s_rk[tid], ks);
     }
     __syncthreads();
-    float ddb = 0.f, dal = 0.f;
-    const float inv_s2 = 1.f / (a.scale * a.scale);
-    const float lb = a.lower_bound;
+    // dx_t = carry_t lb sg (1 - sg) with sg = sigmoid(x_t): sw sums carry sg (1 - sg) and swx
+    // the same times x_t, so that ddt_bias = lb ea sw and da_log = lb swx
+    float sw = 0.f, swx = 0.f;
+    const float lb = a.lower_bound, lbea = a.lower_bound * ea;
     const long long tstride = (long long)H * kD;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -1079,21 +1084,21 @@ __global__ void __launch_bounds__(kKThreads, 1)
           // gate: gamma = lb sigmoid(x), x = e^{a_log} (g + dt_bias)
           const float x = xg[i];
           const float sg = fast_rcp(1.f + fast_exp(-x));
-          const float dx = carry * lb * sg * (1.f - sg);
-          dg_p[(4 * qq + i) * tstride] = dx * ea;
-          ddb += dx * ea;
-          dal += dx * x;
-          // L2 norms: q^ = rq q with rq = scale / |q|, k^ = rk k
-          const float qdt = s_qd[0][t], kdt = s_kd[0][t];
-          const float rq = s_rq[t], rk = s_rk[t];
-          dq_p[(4 * qq + i) * tstride] = __float2bfloat16_rn(rq * aq[i] - qh[i] * qdt * rq * inv_s2);
-          dk_p[(4 * qq + i) * tstride] = __float2bfloat16_rn(rk * dkh[i] - kh[i] * kdt * rk);
+          const float cw = carry * fmaf(-sg, sg, sg);  // carry sg (1 - sg)
+          dg_p[(4 * qq + i) * tstride] = cw * lbea;
+          sw += cw;
+          swx = fmaf(cw, x, swx);
+          // L2 norms: q^ = rq q with rq = scale / |q|, k^ = rk k:
+          //   dq = rq (dq^ - q^ (q^ . dq^) / scale^2),  dk = rk (dk^ - k^ (k^ . dk^))
+          const float4 f = s_tf[t];
+          dq_p[(4 * qq + i) * tstride] = __float2bfloat16_rn(f.x * fmaf(-qh[i], f.y, aq[i]));
+          dk_p[(4 * qq + i) * tstride] = __float2bfloat16_rn(f.z * fmaf(-kh[i], f.w, dkh[i]));
         }
       }
     }
     }  // units
-    s_ddb[R][c] = ddb;
-    dal = warp_sum(dal);
+    s_ddb[R][c] = lbea * sw;
+    const float dal = warp_sum(lb * swx);
     if (lane == 0) s_dal[warp] = dal;
     __syncthreads();
     if (R == 0) atomicAdd(&o.ddt_bias[c * H + h], s_ddb[0][c] + s_ddb[1][c] + s_ddb[2][c] + s_ddb[3][c]);
