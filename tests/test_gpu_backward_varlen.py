@@ -93,6 +93,41 @@ def test_varlen_backward_matches_per_sequence_oracle(lengths, lb):
     assert kda.kda_device_error(1) == 0
 
 
+def test_varlen_backward_tails_at_every_half_sub_chunk_boundary():
+    """Sequences whose last chunk ends just before, at and just after each 8-token boundary
+    (the per-chunk kernel's token work runs on half sub-chunks of 8 tokens, each 64-thread
+    group taking one half of an early and one of a late sub-chunk), each sequence's dq, dk,
+    dv, dg and initial-state gradient compared with the oracle run on it alone.
+
+    dbeta_logits is judged over the packed tensor, as in the other tests: per token it is
+    (1 - beta) lam . u, a 128-term dot product whose terms cancel, so the bf16 rounding of its
+    operands (the last chunk's dS' is the final-state cotangent rounded to bf16) shows as a
+    few per cent of the largest value in a 70-token sequence (2.8% at length 73 with this
+    seed, the same before and after the pairing of half sub-chunks), against 0.4% of the
+    packed tensor's largest value."""
+    tails = [1, 7, 8, 9, 15, 16, 17, 23, 24, 25, 31, 32, 33, 40, 47, 48, 49, 56, 57, 63]
+    lengths = [64 + t for t in tails]
+    H, scale, lb = 2, 128 ** -0.5, -3.0
+    d, total = _packed(lengths, H, 21)
+    gpu = _run(d, total, len(lengths), H, scale, lb)
+    ref = _oracle(d, lengths, H, scale, lb)
+    cu = d["cu_seqlens"]
+    for i, L in enumerate(lengths):
+        a, b = int(cu[i]), int(cu[i + 1])
+        for n in ("dq", "dk", "dv", "dg"):
+            e = rel_err(gpu[n][a:b], ref[n][a:b])
+            assert e <= BF16_REL, (L, n, e)
+        e = rel_err(gpu["dinitial_state"][i], ref["dinitial_state"][i])
+        assert e <= BF16_REL, (L, "dinitial_state", e)
+    e = rel_err(gpu["dbeta_logits"], ref["dbeta_logits"])
+    assert e <= BF16_REL, ("dbeta_logits", e)
+    scales = param_grad_scales(ref["dg"], d["g"], d["dt_bias"])
+    for n in ("da_log", "ddt_bias"):
+        e = bwd_err(n, gpu[n], ref[n], scales)
+        assert e <= BF16_REL, (n, e)
+    assert kda.kda_device_error(1) == 0
+
+
 def test_varlen_backward_equals_fixed_length_backward():
     """Equal lengths: the packed layout is the fixed-length layout, so the gradients agree
     with kda_chunk_bwd exactly (da_log and ddt_bias up to the order of their atomic sums)."""
