@@ -73,7 +73,8 @@ def test_variants(norm, order, decay):
     _check(d, out, S, 0.3, norm, order)
 
 
-@pytest.mark.parametrize("T", [1, 63, 64, 65, 130])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130,
+                               79, 80, 81, 95, 96, 97, 111, 112, 113])  # 16-token boundaries
 @pytest.mark.parametrize("order", ["decay_first", "literal"])
 def test_ragged_lengths(T, order):
     B, H = 2, 2

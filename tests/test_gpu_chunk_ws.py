@@ -119,6 +119,28 @@ def test_varlen_small_with_empty_and_ragged_sequences():
         np.testing.assert_array_equal(S[6], d["initial_state"][6])
 
 
+def test_varlen_tails_at_every_sub_chunk_boundary():
+    """Packed sequences whose last chunk ends just before, at and just after each 16-token
+    sub-chunk boundary and each 8-token half (the prep's gate totals stop at the last live
+    token of a sub-chunk; the rows past it are zeroed), each sequence's output and final
+    state compared with the oracle on its own."""
+    tails = [1, 7, 8, 9, 15, 16, 17, 24, 31, 32, 33, 40, 47, 48, 49, 56, 63]
+    lens = [64 + t for t in tails] + [t for t in tails]
+    H = 2
+    d = synth.varlen_inputs(lens, H, 128, 128, seed=23, state_std=0.1)
+    for lb in (-5.0, -0.5):
+        out, S = run_varlen(d, H, 128, 128, 0.09, lb, 64, True, ws=True)
+        o = oracle_inputs(d, True)
+        ref_out, ref_S = kda_forward_varlen(o["q"], o["k"], o["v"], o["g"], o["beta_logits"],
+                                            o["a_log"], o["dt_bias"], d["cu_seqlens"], 0.09,
+                                            lb, o["initial_state"])
+        cu = d["cu_seqlens"]
+        for i, L in enumerate(lens):
+            a, b = int(cu[i]), int(cu[i + 1])
+            check_rel(f"varlen_tail[len={L} lb={lb}]", "out", out[a:b], ref_out[a:b])
+            check_rel(f"varlen_tail[len={L} lb={lb}]", "final_state", S[i], ref_S[i])
+
+
 def test_varlen_many_short_sequences():
     """More sequences than one pass of the chunk-offset scan (1024), mostly shorter than a
     chunk, a few spanning several chunks."""
