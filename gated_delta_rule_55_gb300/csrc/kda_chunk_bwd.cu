@@ -641,6 +641,10 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
   const float ea = __expf(a.a_log[h]);
   const float db = a.dt_bias[c * H + h];
+  // the gate in log2 units: gamma log2 e = lb2 / (1 + 2^(nea2 (g + dt_bias))); every
+  // cumulative gate below (loc, P, PR, GC, the half totals) is in log2 units, so each
+  // factor e^{G} is one 2^x
+  const float lb2 = a.lower_bound * kLog2E, nea2 = -ea * kLog2E;
   __syncthreads();
   float loc[16], P[4], fg[2][4], GC, PR[2];
 
@@ -667,7 +671,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
     for (int i = 0; i < 8; ++i) {
       const int t = ut0[u] + i;
       float gm = 0.f;
-      if (t < n) gm = a.lower_bound * fast_rcp(1.f + fast_exp(-ea * (rg_t[t * 32] + db)));
+      if (t < n) gm = lb2 * fast_rcp(1.f + fast_exp2(nea2 * (rg_t[t * 32] + db)));
       run += gm;
       loc[8 * u + i] = run;
     }
@@ -730,7 +734,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
 #pragma unroll
     for (int r = 1; r < 4; ++r) PR[u] = (uR[u] == r) ? P[r] : PR[u];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) fg[u][g] = (g > uR[u]) ? fast_exp(P[g] - PR[u]) : 0.f;
+    for (int g = 0; g < 4; ++g) fg[u][g] = (g > uR[u]) ? fast_exp2(P[g] - PR[u]) : 0.f;
   }
   if (!block_wait(&bar_mma, mma_phase++ & 1)) goto fail;
   tc_fence_after();
@@ -798,7 +802,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
     const bool live = t < n;
     const float kh = live ? raw_k(t) * s_rk[t] : 0.f;
     const float qh = live ? raw_q(t) * s_rq[t] : 0.f;
-    const float e = fast_exp(loc[i]);
+    const float e = fast_exp2(loc[i]);
     *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(t, c, 16384)) = __float2bfloat16_rn(kh * e);
     *reinterpret_cast<__nv_bfloat16*>(sm + K_XL + sw_off(64 + t, c, 16384)) =
         __float2bfloat16_rn(qh * e);
@@ -850,7 +854,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int u = i >> 3, t = ut0[u] + (i & 7);
-    const float kd = (t < n) ? raw_k(t) * s_rk[t] * fast_exp(-loc[i]) : 0.f;
+    const float kd = (t < n) ? raw_k(t) * s_rk[t] * fast_exp2(-loc[i]) : 0.f;
     *reinterpret_cast<__nv_bfloat16*>(sm + K_KB + sw_off(t, c, 20480)) = __float2bfloat16_rn(kd);
 #pragma unroll
     for (int g = 1; g < 4; ++g)
@@ -892,7 +896,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {  // (unit hh: sub-chunk uR[hh])
       const int cb = ut0[hh];  // first token of this unit
-      const float eP = fast_exp(PR[hh]), eCP = fast_exp(GC - PR[hh]);
+      const float eP = fast_exp2(PR[hh]), eCP = fast_exp2(GC - PR[hh]);
       // token pairs (t, t + 1) ride Blackwell's two-lane fp32 instructions; every pair
       // operation rounds exactly as the two scalar ones would
       const float2 ePv = make_float2(eP, eP), neP = make_float2(-eP, -eP);
@@ -908,8 +912,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
       for (int p = 0; p < 4; ++p) {
         const int t = cb + 2 * p;
         const float l0 = loc[8 * hh + 2 * p], l1 = loc[8 * hh + 2 * p + 1];
-        E[p] = make_float2(fast_exp(l0), fast_exp(l1));
-        EI[p] = make_float2(fast_exp(-l0), fast_exp(-l1));
+        E[p] = make_float2(fast_exp2(l0), fast_exp2(l1));
+        EI[p] = make_float2(fast_exp2(-l0), fast_exp2(-l1));
         const float2 rk2 = *reinterpret_cast<const float2*>(&s_rk[t]);
         const float2 rq2 = *reinterpret_cast<const float2*>(&s_rq[t]);
         KH[p] = __fmul2_rn(make_float2(raw_k(t), raw_k(t + 1)), rk2);
@@ -1039,7 +1043,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
     }
     // dgamma_t = sum_{r >= t} dG_r + dG_C
     const float dGC = s_dgc[0][c] + s_dgc[1][c] + s_dgc[2][c] + s_dgc[3][c] +
-                      fast_exp(GC) * (s_sdot[0][c] + s_sdot[1][c] + s_sdot[2][c] + s_sdot[3][c]);
+                      fast_exp2(GC) * (s_sdot[0][c] + s_sdot[1][c] + s_sdot[2][c] + s_sdot[3][c]);
     // per token: the sums of q^ . dq^ and k^ . dk^ over the four warps that hold its
     // channels, beside the norms' factors, for one 16-byte read per token below
     const float inv_s2 = 1.f / (a.scale * a.scale);
