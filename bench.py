@@ -53,7 +53,7 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the decode / varlen / e2e / cpu-baseline measurements")
     p.add_argument("--profile", choices=["chunk", "chunk1", "decode", "varlen", "varlen_full",
-                                         "bwd", "bwd_full", "gla", "gla_chunk"],
+                                         "bwd", "bwd_full", "gla", "gla_chunk", "attention"],
                    default=None,
                    help="run two launches of one kernel on a reduced case (for ncu) and exit")
     return p.parse_args()
@@ -751,6 +751,11 @@ def profile_case(which):
         w = replace(synth.PREFILL_B4, H=8) if which == "bwd" else synth.PREFILL_B4
         d, x = device_prefill(w)
         backward_measure(w, d, x, reps=1)
+    elif which == "attention":
+        # the benchmark's kda_attention_fwd_ws calls on the prefill workload (B4 T4096 H32)
+        w = synth.PREFILL_B4
+        _, x = device_prefill(w)
+        attention_measure(w, x, reps=1)
     elif which == "varlen_full":
         # two kda_chunk_fwd_varlen_ws calls on the 8-sequence packed workload (H = 16)
         w = synth.VARLEN_8
