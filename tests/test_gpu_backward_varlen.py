@@ -3,6 +3,8 @@ alone (its own initial state and final-state cotangent; da_log and ddt_bias summ
 sequences), and against kda_chunk_bwd when every sequence has the same length.  bf16:
 max-norm relative error <= 2e-2 per gradient tensor, the oracle fed the same bf16-rounded
 q, k, v and d_out."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -125,6 +127,39 @@ def test_varlen_backward_tails_at_every_half_sub_chunk_boundary():
     for n in ("da_log", "ddt_bias"):
         e = bwd_err(n, gpu[n], ref[n], scales)
         assert e <= BF16_REL, (n, e)
+    assert kda.kda_device_error(1) == 0
+
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    for case in range(n):
+        N = int(rng.integers(1, 7))
+        H = int(rng.integers(1, 4))
+        lens = rng.integers(0, 400, N)
+        if rng.random() < 0.5:
+            lens[rng.integers(0, N)] = int(rng.integers(600, 1500))
+        if case % 3 == 0:
+            lens[rng.integers(0, N)] = int(rng.integers(0, 2))  # empty or one token
+        if lens.sum() == 0:
+            lens[0] = 41
+        yield case, [int(x) for x in lens], H, float(rng.choice([-5.0, -2.0, -0.1]))
+
+
+def test_random_packed_configurations():
+    """Seeded random packed configurations (sequence counts, lengths with empty and
+    one-token sequences and a long one, head counts, gate lower bounds) through
+    kda_chunk_bwd_varlen against the per-sequence oracle backward.  The case count is
+    KDA_RANDOM_CASES (default 4), so that a longer sweep runs the same code."""
+    n = int(os.environ.get("KDA_RANDOM_CASES", "4"))
+    scale = 128 ** -0.5
+    for case, lens, H, lb in _random_cases(n, 77):
+        d, total = _packed(lens, H, 3000 + case)
+        gpu = _run(d, total, len(lens), H, scale, lb)
+        ref = _oracle(d, lens, H, scale, lb)
+        scales = param_grad_scales(ref["dg"], d["g"], d["dt_bias"])
+        for name in ref:
+            e = bwd_err(name, gpu[name], ref[name], scales)
+            assert e <= BF16_REL, (case, lens, H, lb, name, e)
     assert kda.kda_device_error(1) == 0
 
 

@@ -3,8 +3,11 @@ oracle: sequence counts, lengths (empty, one token, ragged, and up to two sequen
 enough for the plan to split their chains), head counts, gate lower bounds and initial
 states drawn at random.  Each case holds the bf16 bar (max-norm relative error <= 2e-2 for
 the packed output and the final states); across the cases the plan must have split chains
-at least once, so the split path is part of what is drawn.
+at least once, so the split path is part of what is drawn.  The case count is
+KDA_RANDOM_CASES (default 12), so that a longer sweep runs the same code.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -53,7 +56,7 @@ def _cases(n, seed):
 def test_random_packed_configurations():
     ex = oracle_pool()
     splits = 0
-    for case, lens, H, lb, init in _cases(12, 2024):
+    for case, lens, H, lb, init in _cases(int(os.environ.get("KDA_RANDOM_CASES", "12")), 2024):
         d = synth.varlen_inputs(lens, H, 128, 128, seed=5000 + case,
                                 state_std=0.1 if init else None)
         kept = []
