@@ -7,6 +7,8 @@ the supported range [-5, 1], and the benchmark's full workloads (gk; gk + gv) co
 element by element.  Bar: max |gpu - oracle| / max |oracle| <= 2e-2 per tensor, the oracle
 fed the same bf16-rounded q, k, v.  Reverse order (the chunks walked from each sequence's
 end) is checked the same way."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -184,3 +186,46 @@ def test_reverse_value_gate_long_sequences():
                             None, None, d["gk"], d["gv"], None, d["s0"], reverse=True)
     check_rel(None, "out", out, ro)
     check_rel(None, "final_state", S, rs)
+
+
+def test_random_configurations():
+    """Seeded random calls: every subset of the gates (g, gk, gv, g_gamma), either order,
+    grouped heads (1 to 3 query heads per key / value head), fixed-length or packed inputs
+    (empty, one-token and ragged sequences among them), with and without an initial state,
+    gate ranges from mild to the edge of the call's contract (the summed key-axis gate and
+    the value-axis gate each in [-5, 1]).  The case count is KDA_RANDOM_CASES
+    (default 6), so that a longer sweep runs the same code."""
+    rng = np.random.default_rng(4242)
+    names = ("g", "gk", "gv", "g_gamma")
+    for case in range(int(os.environ.get("KDA_RANDOM_CASES", "6"))):
+        gates = tuple(n for n in names if rng.random() < 0.5)
+        Hkv = int(rng.integers(1, 4))
+        Hq = Hkv * int(rng.integers(1, 4))
+        rev = bool(rng.integers(0, 2))
+        state = bool(rng.integers(0, 2))
+        lo, hi = [(-0.3, 0.0), (-5.0, 0.0), (-1.0, 0.05)][int(rng.integers(0, 3))]
+        if "g" in gates and "gk" in gates:
+            # the summed key-axis gate g + gk + g_gamma stays in [-5, 1] (g_gamma >= -0.2)
+            lo = max(lo, -2.4)
+        scale = [None, 0.1, 0.3][int(rng.integers(0, 3))]
+        if rng.random() < 0.5:
+            lens = [int(x) for x in rng.integers(0, 300, int(rng.integers(1, 6)))]
+            if case % 2 == 0:
+                lens[int(rng.integers(0, len(lens)))] = int(rng.integers(0, 2))
+            if sum(lens) == 0:
+                lens[0] = 29
+            cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+            B, T, nseq = 1, int(cu[-1]), len(lens)
+        else:
+            cu, B, T, nseq = None, int(rng.integers(1, 3)), int(rng.integers(1, 400)), None
+        d = _inputs(B, T, Hq, Hkv, 900 + case, gates, state, nseq=nseq, lo=lo, hi=hi)
+        out, S = _run(d, B, T, Hq, Hkv, scale, cu=cu, reverse=rev)
+        o = dict(d)
+        for n in ("q", "k", "v"):
+            o[n] = bf16_round(d[n])
+        ro, rs = recurrent_attention(o["q"], o["k"], o["v"], o["g"], o["g_gamma"], o["gk"],
+                                     o["gv"], scale, o["s0"], rev, cu)
+        label = (f"random_rec[{case}: gates={'+'.join(gates) or 'none'} Hq={Hq} Hkv={Hkv} "
+                 f"rev={int(rev)} packed={int(cu is not None)} T={T}]")
+        check_rel(label, "out", out, ro)
+        check_rel(label, "final_state", S, rs)
