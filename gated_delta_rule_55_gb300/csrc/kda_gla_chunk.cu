@@ -48,7 +48,14 @@ using namespace chunk;
 constexpr int kC = 64;
 constexpr int kD = 128;
 
-__device__ unsigned int g_gla_error;  // bit 4: a bounded wait of this path gave up
+__device__ unsigned int g_gla_error;  // bit 4: a bounded wait of this path gave up;
+                                      // bit 5: a sub-chunk's summed gate left this path's range
+// Gates in [-5, 1] per token keep every factor e^{+-x} of a 16-token sub-chunk inside fp32:
+// the sum of a sub-chunk's (or half sub-chunk's) gates then lies in [-80, 16] (resp.
+// [-40, 8]).  The kernels check those sums (a little slack for rounding), one comparison per
+// thread and record, and record bit 5 where one falls outside.
+constexpr float kSubLo2 = -80.01f * kLog2E, kSubHi2 = 16.01f * kLog2E;  // log2 units
+constexpr float kHalfLo = -40.01f, kHalfHi = 8.01f;
 
 // Workspace records per (chunk slot, query head).
 constexpr long long kGRecQ = 64LL * 128 * 2;   // Q~ [64 tok][128] bf16
@@ -158,6 +165,7 @@ __global__ void __launch_bounds__(kGThreads, 2)
   __shared__ uint64_t bar_mma, bar_ld;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
+  __shared__ int s_gate_out;  // a sub-chunk's summed key-axis gate left [-80, 16]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -236,6 +244,7 @@ __global__ void __launch_bounds__(kGThreads, 2)
     tmem_relinquish();
   }
   if (tid == 0) {
+    s_gate_out = 0;
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_ld, 1);
     fence_mbar_init();
@@ -328,6 +337,8 @@ __global__ void __launch_bounds__(kGThreads, 2)
         run = __ffma2_rn(l2e, __fadd2_rn(graw[i], gv2), run);
         loc[i] = run;
       }
+      if (!(run.x >= kSubLo2 && run.x <= kSubHi2 && run.y >= kSubLo2 && run.y <= kSubHi2))
+        s_gate_out = 1;
       if (n < kC) {
         const int live = n - 16 * R;
         run = make_float2(0.f, 0.f);
@@ -510,6 +521,7 @@ __global__ void __launch_bounds__(kGThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0 && s_gate_out) atomicOr(&g_gla_error, 32u);
   if (warp == 0) tmem_dealloc(tm, kGTmemCols);
 }
 
@@ -535,6 +547,7 @@ __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a
   const int c0 = 2 * cp;
   const int Hq = a.Hq, grp = a.Hq / a.Hkv;
   const long long gstride = (long long)Hq * kD, vstride = (long long)a.Hkv * kD;
+  bool gate_out = false;  // a half sub-chunk's summed value-axis gate left [-40, 8]
   for (long long rec = blockIdx.x; rec < w.recs; rec += gridDim.x) {
     const int h = (int)(rec % Hq);
     const long long slot = rec / Hq;
@@ -584,6 +597,7 @@ __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a
       L[i] = run;
     }
     s_tot[P][cp] = run;
+    gate_out |= !(run.x >= kHalfLo && run.x <= kHalfHi && run.y >= kHalfLo && run.y <= kHalfHi);
     __syncthreads();
     // the sub-chunk's first half before this thread's tokens; the totals T_r; B_C - Q_R
     const float2 first = s_tot[2 * R][cp];
@@ -613,6 +627,7 @@ __global__ void __launch_bounds__(kVThreads, 2) gla_vprep_kernel(const GlaArgs a
     }
     __syncthreads();  // s_tot is rewritten for the next record
   }
+  if (__any_sync(0xffffffffu, gate_out) && (threadIdx.x & 31) == 0) atomicOr(&g_gla_error, 32u);
 }
 
 // ------------------------------------------------------------------- scan kernel

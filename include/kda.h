@@ -404,7 +404,8 @@ enum kda_recurrent_flags {
  *   page's run parameters g, gk, g_gamma, gv, cu_seqlens, reverse).  On that path the summed
  *   key-axis gate g + gk + g_gamma and the value-axis gate gv must each lie in [-5, 1] at
  *   every token and channel, where the chunks' factorised exponentials stay inside the fp32
- *   range; outside it the results are unspecified (no fault).  Every other configuration
+ *   range; outside it the results are unspecified (no fault), and gates far enough outside
+ *   to overflow a sub-chunk's factors set bit 5 of kda_device_error.  Every other configuration
  *   (fp32, other head dims) ignores the workspace and runs the token-serial kernel.
  *   workspace: at least kda_recurrent_attention_fwd_workspace_size(N, B, T, Hq, Hkv, D,
  *   flags, dtype) bytes (flags: kda_recurrent_flags describing the call; 0: none needed),
@@ -454,7 +455,11 @@ int kda_version(void);
  *   one inside the two-launch (workspace) chunk kernels did; bit 2: one inside the
  *   chunked backward's kernels did (the outputs of that launch are incomplete); bit 3: the
  *   wait of kda_selftest_bounded_wait gave up (which is what it is for); bit 4: one inside
- *   the chunked recurrent-attention kernels did.  Synchronises the device.  reset != 0
+ *   the chunked recurrent-attention kernels did; bit 5: those kernels met gates outside
+ *   their range, detected per 16-token sub-chunk (a summed key-axis gate totalling outside
+ *   [-80, 16] over a sub-chunk, or a value-axis gate outside [-40, 8] over half of one,
+ *   which gates in [-5, 1] rule out; that call's results are unspecified).  Synchronises
+ *   the device.  reset != 0
  *   clears the mask.
  *   Returns the mask (>= 0) or KDA_ERR_DEVICE.
  */

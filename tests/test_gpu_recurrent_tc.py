@@ -229,3 +229,20 @@ def test_random_configurations():
                  f"rev={int(rev)} packed={int(cu is not None)} T={T}]")
         check_rel(label, "out", out, ro)
         check_rel(label, "final_state", S, rs)
+
+
+def test_gate_outside_the_range_is_reported():
+    """Gates outside the chunked path's range (the summed key-axis gate and the value-axis
+    gate each in [-5, 1]): the call completes and records bit 5 of kda_device_error; inside
+    the range nothing is recorded."""
+    B, T, Hq, Hkv = 1, 100, 2, 1
+    kda.kda_device_error(reset=True)
+    d = _inputs(B, T, Hq, Hkv, 31, ("gk",), False, lo=-4.0, hi=-4.0)  # inside
+    _run(d, B, T, Hq, Hkv, None)
+    assert kda.kda_device_error(reset=True) == 0
+    d = _inputs(B, T, Hq, Hkv, 31, ("g", "gk"), False, lo=-4.0, hi=-4.0)  # sum -8
+    _run(d, B, T, Hq, Hkv, None)
+    assert kda.kda_device_error(reset=True) == 32
+    d = _inputs(B, T, Hq, Hkv, 32, ("gv",), False, lo=1.5, hi=1.5)  # value gate above 1
+    _run(d, B, T, Hq, Hkv, None, reverse=True)
+    assert kda.kda_device_error(reset=True) == 32
