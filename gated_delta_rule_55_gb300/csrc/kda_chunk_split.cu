@@ -79,7 +79,9 @@ constexpr uint32_t P_TM_DW = 0;    // after D1 is consumed: [T K~; -W] (forward,
 constexpr uint32_t P_TM_DU = 128;  // U~^T, 64
 constexpr uint32_t kPTmemCols = 256;
 
-__device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split path gave up
+__device__ unsigned int g_split_error;  // bit 1: a bounded wait of the split path gave up;
+                                        // bit 5: the attention mode met a decay whose
+                                        // 16-token sum left [-80, 16]
 
 // kBwd: also the backward's records (rq folded into Q~ and M, and N).
 // kAttn: the kernel_delta_attention call's own variants (ChunkArgs gate_head): a per-head
@@ -110,6 +112,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
   __shared__ uint64_t bar_mma, bar_ld, bar_qv;
   __shared__ uint32_t s_tmem;
   __shared__ int s_wait_ok[2];
+  __shared__ int s_decay_out;  // kAttn: a sub-chunk's summed decay left [-80, 16]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -231,6 +234,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tmem_relinquish();
   }
   if (tid == 0) {
+    s_decay_out = 0;
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_qv, 1);
@@ -323,6 +327,9 @@ __global__ void __launch_bounds__(kPThreads, 2)
         loc[i] = make_float2(run, run);
       }
       *reinterpret_cast<float2*>(&s_gtot[R][c0]) = make_float2(run, run);
+      // decays in [-5, 1] keep a sub-chunk's sum in [-80, 16], where its factors stay
+      // inside fp32; a sum outside it is reported (bit 5 of the device error mask)
+      if (!(run >= -80.01f * kLog2E && run <= 16.01f * kLog2E)) s_decay_out = 1;
     } else {
       // the gate in log2 units: gamma log2 e = lb2 / (1 + 2^(na2 (g + dt_bias)))
       const float na2 = -__expf(a.a_log[h]) * kLog2E;
@@ -830,6 +837,8 @@ __global__ void __launch_bounds__(kPThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (kAttn)
+    if (tid == 0 && s_decay_out) atomicOr(&g_split_error, 32u);
   if (warp == 0) tmem_dealloc(tm, kPTmemCols);
 }
 

@@ -347,7 +347,9 @@ int kda_attention_fwd(const void* query, const void* key, const void* value, con
  *   with the call's own variants: the per-head log-decay on every channel, beta as given,
  *   use_qk_l2norm and the literal order.  On that path the decay must lie in [-5, 1] (the
  *   page asks for decays <= 0): 64-token chunks keep their factorised exponentials inside
- *   the fp32 range only there; outside it the results are unspecified (no fault).  Every
+ *   the fp32 range only there; outside it the results are unspecified (no fault), and
+ *   decays far enough outside to overflow a sub-chunk's factors set bit 5 of
+ *   kda_device_error.  Every
  *   other configuration ignores the workspace and runs kda_attention_fwd's kernels.
  *   workspace: at least kda_attention_fwd_workspace_size(B, T, H, dk, dv, chunk, flags,
  *   dtype) bytes (0: none needed), 256-byte aligned, caller-owned, contents unspecified on
@@ -455,8 +457,9 @@ int kda_version(void);
  *   one inside the two-launch (workspace) chunk kernels did; bit 2: one inside the
  *   chunked backward's kernels did (the outputs of that launch are incomplete); bit 3: the
  *   wait of kda_selftest_bounded_wait gave up (which is what it is for); bit 4: one inside
- *   the chunked recurrent-attention kernels did; bit 5: those kernels met gates outside
- *   their range, detected per 16-token sub-chunk (a summed key-axis gate totalling outside
+ *   the chunked recurrent-attention kernels did; bit 5: a tensor-core kernel of
+ *   kda_recurrent_attention_fwd_ws or kda_attention_fwd_ws met gates outside its range,
+ *   detected per 16-token sub-chunk (a summed key-axis gate or decay totalling outside
  *   [-80, 16] over a sub-chunk, or a value-axis gate outside [-40, 8] over half of one,
  *   which gates in [-5, 1] rule out; that call's results are unspecified).  Synchronises
  *   the device.  reset != 0

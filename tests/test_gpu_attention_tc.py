@@ -111,3 +111,18 @@ def test_other_configurations_ignore_the_workspace():
         outs.append((out.cpu().numpy(), s1.cpu().numpy()))
     np.testing.assert_array_equal(outs[0][0], outs[1][0])
     np.testing.assert_array_equal(outs[0][1], outs[1][1])
+
+
+def test_decay_outside_the_range_is_reported():
+    """A per-head decay outside the tensor-core path's range [-5, 1]: the call completes and
+    records bit 5 of kda_device_error (a 16-token sub-chunk's summed decay leaves [-80, 16]);
+    at the range's edge nothing is recorded."""
+    B, T, H = 1, 100, 2
+    kda.kda_device_error(reset=True)
+    d = _inputs(B, T, H, 41, True, "neg", False)
+    d["decay"] = np.full((B, T, H), -5.0)  # the edge: inside
+    _run(d, B, T, H, None, True, "decay_first")
+    assert kda.kda_device_error(reset=True) == 0
+    d["decay"] = np.full((B, T, H), -6.0)
+    _run(d, B, T, H, None, True, "decay_first")
+    assert kda.kda_device_error(reset=True) == 32
