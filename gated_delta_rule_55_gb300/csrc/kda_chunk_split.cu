@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
     tmem_relinquish();
   }
   if (tid == 0) {
-    s_decay_out = 0;
+    if constexpr (kAttn) s_decay_out = 0;
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_qv, 1);
